@@ -1,0 +1,44 @@
+"""Float64 CPU oracle for the lightning indexer over a paged NVFP4 key pool.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports this package:
+only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg (and its ``--impl reference`` arm) may call it. It shares no code with the
+CUDA path under ``sparse_attention_top_paged_gb300/``; the two meet only in
+the seeded input arrays that ``sparse_attention_top_paged_gb300.workloads``
+produces.
+
+Every function states the passage of the source pages it follows:
+
+* "indexer_score_topk.cu" (nvfp4-megamoe-kernel, dsv4/kernels/indexer):
+  the header comment (CSA lightning indexer, eq. 16), the "FP4
+  dequantization (NVFP4 scheme)" section, the "Min-heap for top-k" section,
+  the "Main kernel" section and the "PyTorch binding" section.
+* "Commit graph, dsv4/kernels/indexer": commits e74c844 (E2M1 lookup table),
+  79ef87f (E2M1 decode fix) and c2f705a (score+top-k, gather KV,
+  compute_valid_lens).
+* "metrale_model_layers/layers/ops/qsa.rs": the doc comments of
+  ``qsa_block_pool``, ``qsa_score``, ``qsa_gather`` and ``qsa_score_rows``.
+
+Parity status. Every function is pinned by ``tests/test_oracle_pins.py``
+except the RoPE pairing convention inside ``block_pool`` (the pages do not say
+which dimensions are paired): parity unpinned for that convention; its
+special cases (identity at position 0, norm preservation, rot=0) are pinned.
+"""
+
+from .indexer import (  # noqa: F401
+    E2M1_MAGNITUDES,
+    e2m1_decode,
+    e4m3_decode,
+    unpack_nibbles,
+    resolve_slots,
+    dequant_rows,
+    index_scores,
+    topk_sorted,
+    score_topk,
+    score_topk_rows,
+    valid_lens_from_blocks,
+    STATUS_BAD_BLOCK,
+    STATUS_BAD_LEN,
+    STATUS_BAD_SEL,
+)
+from .qsa import block_pool, qsa_score, gather_kv, expand_blocks  # noqa: F401

@@ -1,0 +1,119 @@
+"""QSA key pooling, QSA block score, and the selected-row K/V gather, in float64.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Source: "metrale_model_layers/layers/ops/qsa.rs" (doc comments of
+``qsa_block_pool``, ``qsa_score`` and ``qsa_gather``) and the gather described
+in commit c2f705a of "Commit graph, dsv4/kernels/indexer" (dense tile from the
+paged pool through the block table).
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from .indexer import STATUS_BAD_BLOCK, STATUS_BAD_SEL
+
+
+def block_pool(raw_keys, k_norm_w, first_block: int, n_new: int, ratio: int,
+               rot: int, theta: float, eps: float, *, interleaved: bool = False) -> np.ndarray:
+    """Pool ``n_new`` newly complete blocks starting at ``first_block``.
+
+    qsa.rs, ``qsa_block_pool``: the mean of ``ratio`` raw keys, then RMSNorm
+    scaled by ``1 + w``, then rope at the block's first token position.
+    Returns ``[n_new, hd]``; row ``i`` is block ``first_block + i``, pooled
+    from raw rows ``[(first_block+i)*ratio, (first_block+i+1)*ratio)`` at
+    position ``(first_block+i)*ratio``.
+
+    Readings where the page is silent: RMSNorm is
+    ``m / sqrt(mean(m^2) + eps) * (1 + w)``; rope rotates the first ``rot``
+    dimensions, pairing ``i`` with ``i + rot/2`` (half split; ``interleaved``
+    pairs ``2i`` with ``2i+1`` instead) at angle ``pos * theta^(-2i/rot)``.
+    Parity unpinned for the pairing convention.
+    """
+    raw = np.asarray(raw_keys, dtype=np.float64)
+    w = np.asarray(k_norm_w, dtype=np.float64)
+    hd = raw.shape[1]
+    out = np.zeros((n_new, hd), dtype=np.float64)
+    half = rot // 2
+    for i in range(n_new):
+        b = first_block + i
+        m = raw[b * ratio:(b + 1) * ratio].mean(axis=0)
+        y = m / math.sqrt(float(np.mean(m * m)) + eps) * (1.0 + w)
+        pos = b * ratio
+        z = y.copy()
+        for j in range(half):
+            ang = pos * theta ** (-2.0 * j / rot)
+            c, s = math.cos(ang), math.sin(ang)
+            a_i, b_i = (2 * j, 2 * j + 1) if interleaved else (j, j + half)
+            x1, x2 = y[a_i], y[b_i]
+            z[a_i] = x1 * c - x2 * s
+            z[b_i] = x2 * c + x1 * s
+        out[i] = z
+    return out
+
+
+def qsa_score(q, block_keys) -> np.ndarray:
+    """qsa.rs, ``qsa_score``: ``scores[b] = sum_h relu(q_h . k_b) / sqrt(hd)``."""
+    q = np.asarray(q, dtype=np.float64)            # [n_heads, hd]
+    kb = np.asarray(block_keys, dtype=np.float64)  # [n_blocks, hd]
+    return np.maximum(kb @ q.T, 0.0).sum(axis=1) / math.sqrt(q.shape[1])
+
+
+def expand_blocks(blocks, ratio: int) -> np.ndarray:
+    """Token positions of selected blocks, for the gather.
+
+    qsa.rs, ``qsa_gather``: slot ``i`` of the scratch holds position
+    ``sel[i]``. The page does not fix the order of the selected blocks; the
+    reading taken is ascending block order, each block expanded to its
+    ``ratio`` positions in ascending order, ``-1`` after the last selected
+    block. ``blocks``: ``[T, nb]`` block indices, ``-1`` for none.
+    """
+    blocks = np.asarray(blocks, dtype=np.int64)
+    T, nb = blocks.shape
+    out = np.full((T, nb * ratio), -1, dtype=np.int64)
+    for t in range(T):
+        sel = sorted(int(b) for b in blocks[t] if b >= 0)
+        pos = [b * ratio + r for b in sel for r in range(ratio)]
+        out[t, :len(pos)] = pos
+    return out
+
+
+def gather_kv(sel, block_table, bt_stride: int, max_lb: int, block_size: int,
+              k_cache, v_cache):
+    """Copy the selected rows of a paged K/V cache into a dense tile.
+
+    qsa.rs, ``qsa_gather`` (slot ``i`` holds position ``sel[i]``) and commit
+    c2f705a's gather (rows resolved through the block table). For position
+    ``p``: ``phys = table[t][p // block_size]``, row ``p % block_size``.
+    ``p < 0`` gives a zero row; a logical block outside the table or a
+    physical block outside ``[0, P)`` also gives a zero row and sets a status
+    bit. ``k_cache``/``v_cache``: ``[P, block_size, ...]`` of any dtype; the
+    copy is of the stored elements, unchanged.
+    """
+    sel = np.asarray(sel, dtype=np.int64)
+    kc, vc = np.asarray(k_cache), np.asarray(v_cache)
+    T, n = sel.shape
+    n_phys = kc.shape[0]
+    flat = np.asarray(block_table, dtype=np.int64).reshape(-1)
+    k_out = np.zeros((T, n) + kc.shape[2:], dtype=kc.dtype)
+    v_out = np.zeros((T, n) + vc.shape[2:], dtype=vc.dtype)
+    status = 0
+    for t in range(T):
+        for i in range(n):
+            p = int(sel[t, i])
+            if p < 0:
+                continue
+            lb = p // block_size
+            if lb >= max_lb:
+                status |= STATUS_BAD_SEL
+                continue
+            phys = int(flat[t * bt_stride + lb])
+            if phys < 0 or phys >= n_phys:
+                status |= STATUS_BAD_BLOCK
+                continue
+            k_out[t, i] = kc[phys, p % block_size]
+            v_out[t, i] = vc[phys, p % block_size]
+    return k_out, v_out, status

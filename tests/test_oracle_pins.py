@@ -1,0 +1,427 @@
+"""Pins of the float64 oracle against what the pages and the mathematics fix.
+
+Each ``pin_*`` helper returns True when the oracle agrees with an independent
+source: a value the pages print (fixtures under ``tests/golden/``), a library
+routine computing the same quantity another way, a closed form, a layout
+probe whose answer is known by construction, or an exact invariance. The
+mutation tests at the end plant plausible mistakes in the oracle (on the CPU)
+and check that some pin then fails.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.indexer as oi
+from sparse_attention_top_paged_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load_table(name):
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        a, b = line.split()
+        rows.append((int(a, 0), float(b)))
+    return rows
+
+
+def _load_case(name):
+    c = json.load(open(os.path.join(GOLDEN, name)))
+    c["expected_score"] = [[-math.inf if v == "-inf" else v for v in r] for r in c["expected_score"]]
+    return c
+
+
+def _run_case(c):
+    arr = lambda x, dt: np.asarray(x, dtype=dt)
+    idx, sc, status, rows = oracle.score_topk(
+        arr(c["q"], np.float32), arr(c["w"], np.float32), arr(c["block_table"], np.int32),
+        c["bt_stride"], len(c["block_table"][0]), arr(c["valid_lens"], np.int32), c["epb"], c["k"],
+        keys_fp4=arr(c["keys_fp4"], np.uint8), key_scale=arr(c["key_scale"], np.uint8),
+        key_gscale=arr(c["key_gscale"], np.float32))
+    return idx, sc, status, rows
+
+
+# ----------------------------------------------------------------- pins ----
+
+def pin_e2m1_printed_table():
+    """Oracle E2M1 decode == the table printed in commits 79ef87f / e74c844."""
+    tab = _load_table("e2m1_table.txt")
+    codes = np.array([c for c, _ in tab])
+    want = np.array([v for _, v in tab])
+    got = oracle.e2m1_decode(codes)
+    return np.array_equal(got, want) and np.array_equal(np.signbit(got), np.signbit(want))
+
+
+def bitlevel_e2m1(code):
+    """Bit-level E2M1 decode as commit 79ef87f describes it (bias 1;
+    exponent field 0 is subnormal with 0b001 = 0.5), written without the
+    lookup table."""
+    sign = -1.0 if code & 8 else 1.0
+    e, m = (code >> 1) & 3, code & 1
+    mag = m * 0.5 if e == 0 else (1.0 + 0.5 * m) * 2.0 ** (e - 1)
+    return sign * mag
+
+
+def pin_e2m1_bitlevel():
+    got = oracle.e2m1_decode(np.arange(16))
+    want = np.array([bitlevel_e2m1(c) for c in range(16)])
+    return np.array_equal(got, want)
+
+
+def pin_e4m3_library():
+    """All 256 E4M3 codes vs torch's float8_e4m3fn -> float32 (a library routine)."""
+    import torch
+    lib = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_decode(np.arange(256))
+    nan_ok = np.array_equal(np.isnan(got), np.isnan(lib))
+    fin = ~np.isnan(lib)
+    return nan_ok and np.array_equal(got[fin], lib[fin]) and np.array_equal(np.signbit(got[fin]), np.signbit(lib[fin]))
+
+
+def pin_e4m3_anchors():
+    ok = True
+    for code, v in _load_table("e4m3_anchors.txt"):
+        g = float(oracle.e4m3_decode(code))
+        ok &= (math.isnan(g) and math.isnan(v)) or (g == v and math.copysign(1, g) == math.copysign(1, v))
+    return ok
+
+
+def pin_golden(name):
+    c = _load_case(name)
+    idx, sc, status, rows = _run_case(c)
+    ok = status == 0
+    for t, want in enumerate(c["scores"]):
+        ok &= np.array_equal(rows[t], np.asarray(want, dtype=np.float64))
+    ok &= np.array_equal(idx, np.asarray(c["expected_idx"]))
+    ok &= np.array_equal(sc, np.asarray(c["expected_score"], dtype=np.float64))
+    return bool(ok)
+
+
+def _onehot_pool(d, code, P=3, epb=16, D=128):
+    """Pool whose only non-zero element is ``code`` at element ``d`` of
+    (phys 2, slot 5); every group scale is 448 (0x7E) except group d//16 of
+    that row, which is 1.0 (0x38); gscale 1/4."""
+    fp4 = np.zeros((P, epb, D // 2), dtype=np.uint8)
+    fp4[2, 5, d // 2] = (code << 4) if d % 2 else code
+    sc = np.full((P, epb, D // 16), 0x7E, dtype=np.uint8)
+    sc[2, 5, d // 16] = 0x38
+    g = np.full(P, 0.25, dtype=np.float32)
+    return fp4, sc, g
+
+
+def pin_onehot_layout():
+    """q = +-e_d probes every element position through the table: with the
+    single non-zero code placed at logical key 21 (logical block 1 -> phys 2,
+    slot 5), I[s] must be ReLU(+-value * 1.0 * 0.25) at s=21 and 0 elsewhere,
+    the value taken from the printed E2M1 table."""
+    tab = dict(_load_table("e2m1_table.txt"))
+    bt = np.array([[0, 2, 1]], dtype=np.int32)
+    ok = True
+    for d in range(0, 128, 7):
+        for code in (3, 7, 13):
+            fp4, sc, g = _onehot_pool(d, code)
+            for sign in (1.0, -1.0):
+                q = np.zeros((1, 1, 128), dtype=np.float32)
+                q[0, 0, d] = sign
+                rows, status = oracle.score_topk_rows(q, np.ones((1, 1), np.float32), bt, 3, 3,
+                                                      np.array([48], np.int32), 16,
+                                                      keys_fp4=fp4, key_scale=sc, key_gscale=g)
+                want = np.zeros(48)
+                want[21] = max(sign * tab[code] * 1.0 * 0.25, 0.0)
+                ok &= np.array_equal(rows[0], want)
+                # the same code probed at every other element gives zero
+                q2 = np.zeros_like(q)
+                q2[0, 0, (d + 1) % 128] = 1.0
+                rows2, _ = oracle.score_topk_rows(q2, np.ones((1, 1), np.float32), bt, 3, 3,
+                                                  np.array([48], np.int32), 16,
+                                                  keys_fp4=fp4, key_scale=sc, key_gscale=g)
+                ok &= not rows2[0].any()
+    return bool(ok)
+
+
+def pin_closed_form():
+    """All nibbles code c, all scales byte e, global scale g, q = 1: every key
+    decodes to 128 copies of LUT[c]*E4M3[e]*g, so I = sum_h w_h ReLU(128 *
+    LUT[c] * E4M3[e] * g) for every s (values from the printed tables)."""
+    tab = dict(_load_table("e2m1_table.txt"))
+    anchors = dict(_load_table("e4m3_anchors.txt"))
+    ok = True
+    rng = np.random.default_rng(5)
+    w = rng.standard_normal((1, 4)).astype(np.float32)
+    for c in (1, 5, 7, 9, 15):
+        for e in (0x01, 0x30, 0x3C, 0x7E):
+            fp4 = np.full((2, 64, 64), c | (c << 4), dtype=np.uint8)
+            sc = np.full((2, 64, 8), e, dtype=np.uint8)
+            g = np.array([0.125, 0.125], np.float32)
+            q = np.ones((1, 4, 128), np.float32)
+            rows, _ = oracle.score_topk_rows(q, w, np.array([[1, 0]], np.int32), 2, 2,
+                                             np.array([100], np.int32), 64,
+                                             keys_fp4=fp4, key_scale=sc, key_gscale=g)
+            dot = 128 * tab[c] * anchors[e] * 0.125
+            want = sum(float(w[0, h]) * max(dot, 0.0) for h in range(4))
+            ok &= np.allclose(rows[0], want, rtol=1e-15, atol=0)
+    return bool(ok)
+
+
+def pin_block_permutation():
+    """Moving the physical blocks and rewriting the table to match leaves
+    every score bit-identical."""
+    W = wl.tiny_decode(11, gscale_pow2_jitter=2)
+    rows0, _ = oracle.score_topk_rows(W.q, W.w, W.block_table, W.bt_stride, W.max_lb, W.valid_lens,
+                                      W.epb, **W.oracle_kwargs())
+    pi = np.random.default_rng(3).permutation(W.P)
+    fp4 = np.empty_like(W.keys_fp4); fp4[pi] = W.keys_fp4
+    sc = np.empty_like(W.key_scale); sc[pi] = W.key_scale
+    g = np.empty_like(W.key_gscale); g[pi] = W.key_gscale
+    bt = pi[W.block_table].astype(np.int32)
+    rows1, _ = oracle.score_topk_rows(W.q, W.w, bt, W.bt_stride, W.max_lb, W.valid_lens, W.epb,
+                                      keys_fp4=fp4, key_scale=sc, key_gscale=g)
+    return all(np.array_equal(rows0[t], rows1[t]) for t in rows0)
+
+
+def pin_pow2_scaling():
+    """w -> 2^j w and gscale -> 2^j gscale scale every score by exactly 2^j."""
+    W = wl.tiny_decode(12)
+    base, _ = oracle.score_topk_rows(W.q, W.w, W.block_table, W.bt_stride, W.max_lb, W.valid_lens,
+                                     W.epb, **W.oracle_kwargs())
+    ok = True
+    for j in (-3, 5):
+        r, _ = oracle.score_topk_rows(W.q, W.w * 2.0 ** j, W.block_table, W.bt_stride, W.max_lb,
+                                      W.valid_lens, W.epb, **W.oracle_kwargs())
+        ok &= all(np.array_equal(r[t], base[t] * 2.0 ** j) for t in base)
+        kw = W.oracle_kwargs()
+        kw["key_gscale"] = (W.key_gscale * 2.0 ** j).astype(np.float32)
+        r, _ = oracle.score_topk_rows(W.q, W.w, W.block_table, W.bt_stride, W.max_lb,
+                                      W.valid_lens, W.epb, **kw)
+        ok &= all(np.array_equal(r[t], base[t] * 2.0 ** j) for t in base)
+    return bool(ok)
+
+
+def pin_positive_scaling_topk():
+    """w -> c w (c > 0) scales scores by c and leaves the top-k indices alone."""
+    W = wl.tiny_decode(13)
+    i0, s0, _, _ = oracle.score_topk(W.q, W.w, W.block_table, W.bt_stride, W.max_lb, W.valid_lens,
+                                     W.epb, W.top_k, **W.oracle_kwargs())
+    i1, s1, _, _ = oracle.score_topk(W.q, (W.w.astype(np.float64) * 3.7), W.block_table, W.bt_stride,
+                                     W.max_lb, W.valid_lens, W.epb, W.top_k, **W.oracle_kwargs())
+    return np.array_equal(i0, i1) and np.allclose(s1, 3.7 * s0, rtol=1e-12)
+
+
+def pin_topk_vs_lexsort():
+    """Top-k == first k of numpy.lexsort on (index, -score), including ties."""
+    rng = np.random.default_rng(9)
+    ok = True
+    for n, k in ((50, 8), (300, 300), (40, 64), (1000, 17)):
+        s = rng.integers(-5, 5, size=n).astype(np.float64)   # many ties
+        idx, sc = oracle.topk_sorted(s, k)
+        order = np.lexsort((np.arange(n), -s))[:k]
+        m = min(n, k)
+        ok &= np.array_equal(idx[:m], order) and np.array_equal(sc[:m], s[order])
+        ok &= bool(np.all(idx[m:] == -1) and np.all(np.isneginf(sc[m:])))
+    return bool(ok)
+
+
+def pin_topk_bruteforce():
+    """Top-k == repeated selection of the best remaining entry (tiny inputs)."""
+    rng = np.random.default_rng(10)
+    ok = True
+    for _ in range(20):
+        n = int(rng.integers(0, 12)); k = int(rng.integers(1, 10))
+        s = rng.integers(-3, 3, size=n).astype(np.float64)
+        left = list(range(n)); want = []
+        for _ in range(min(n, k)):
+            best = left[0]
+            for j in left:
+                if s[j] > s[best] or (s[j] == s[best] and j < best):
+                    best = j
+            want.append(best); left.remove(best)
+        idx, _ = oracle.topk_sorted(s, k)
+        ok &= list(idx[:len(want)]) == want
+    return bool(ok)
+
+
+def pin_mask():
+    """Keys at or past valid_len, made huge, never appear."""
+    W = wl.tiny_decode(14)
+    fp4 = W.keys_fp4.copy(); sc = W.key_scale.copy()
+    L = 1000                                   # mid-block: 15 blocks + 40 slots
+    for t in range(W.T):
+        for lb in range(W.max_lb):
+            phys = W.block_table[t, lb]
+            lo = max(0, L - lb * W.epb)
+            if lo < W.epb:
+                fp4[phys, lo:] = 0x77; sc[phys, lo:] = 0x7E
+    vl = np.full(W.T, L, np.int32)
+    idx, _, _, rows = oracle.score_topk(W.q, W.w, W.block_table, W.bt_stride, W.max_lb, vl, W.epb,
+                                        W.top_k, keys_fp4=fp4, key_scale=sc, key_gscale=W.key_gscale)
+    return bool(np.all(idx < L)) and all(len(rows[t]) == L for t in rows)
+
+
+def pin_bad_inputs():
+    """Out-of-range table entries drop their keys and set bit 1; an
+    out-of-range valid length pads the whole query and sets bit 2."""
+    c = _load_case("tiny_score_a.json")
+    c2 = dict(c); c2["block_table"] = [[1, 7]]           # logical block 1 -> phys 7 (P=2)
+    idx, sc, status, _ = _run_case(c2)
+    ok = status == oracle.STATUS_BAD_BLOCK and list(idx[0]) == [0, 1, -1, -1]
+    c3 = dict(c); c3["valid_lens"] = [5]                 # > max_lb * epb = 4
+    idx, sc, status, _ = _run_case(c3)
+    ok &= status == oracle.STATUS_BAD_LEN and bool(np.all(idx == -1))
+    return bool(ok)
+
+
+def pin_valid_lens_from_blocks():
+    """compute_valid_lens of commit c2f705a: block count * entries per block."""
+    return list(oracle.valid_lens_from_blocks([0, 1, 3], 64)) == [0, 64, 192]
+
+
+def pin_gather_library():
+    """Gather == numpy fancy indexing over the flattened paged view."""
+    rng = np.random.default_rng(4)
+    P, bs, nkv, hd, T, n = 9, 4, 2, 8, 2, 13
+    kc = rng.integers(0, 65535, size=(P, bs, nkv, hd), dtype=np.uint16)
+    vc = rng.integers(0, 65535, size=(P, bs, nkv, hd), dtype=np.uint16)
+    table = np.stack([rng.permutation(P)[:6] for _ in range(T)]).astype(np.int32)
+    sel = rng.integers(0, 6 * bs, size=(T, n)); sel[0, 3] = -1
+    k_out, v_out, st = oracle.gather_kv(sel, table, 6, 6, bs, kc, vc)
+    flat_k = kc.reshape(P * bs, nkv, hd); flat_v = vc.reshape(P * bs, nkv, hd)
+    rows = table[np.arange(T)[:, None], np.clip(sel, 0, None) // bs] * bs + np.clip(sel, 0, None) % bs
+    want_k = np.where((sel >= 0)[..., None, None], flat_k[rows], 0)
+    want_v = np.where((sel >= 0)[..., None, None], flat_v[rows], 0)
+    return st == 0 and np.array_equal(k_out, want_k) and np.array_equal(v_out, want_v)
+
+
+def pin_pool_special_cases():
+    rng = np.random.default_rng(6)
+    raw = rng.standard_normal((64, 16))
+    w = rng.standard_normal(16) * 0.1
+    ok = True
+    # block 0 sits at position 0: rope is the identity there
+    a = oracle.block_pool(raw, w, 0, 1, 4, 8, 1e6, 1e-6)
+    b = oracle.block_pool(raw, w, 0, 1, 4, 0, 1e6, 1e-6)
+    ok &= np.allclose(a, b, rtol=0, atol=0)
+    # rope preserves the norm of every rotated pair
+    a = oracle.block_pool(raw, w, 3, 5, 4, 8, 1e4, 1e-6)
+    b = oracle.block_pool(raw, w, 3, 5, 4, 0, 1e4, 1e-6)
+    for j in range(4):
+        ok &= np.allclose(a[:, j] ** 2 + a[:, j + 4] ** 2, b[:, j] ** 2 + b[:, j + 4] ** 2, rtol=1e-12)
+    ok &= np.array_equal(a[:, 8:], b[:, 8:])
+    # ratio 1, w = 0, rot = 0: plain RMS normalisation of each row -> RMS 1, same direction
+    c = oracle.block_pool(raw, np.zeros(16), 0, 64, 1, 0, 1e6, 0.0)
+    ok &= np.allclose(np.sqrt(np.mean(c * c, axis=1)), 1.0, rtol=1e-12)
+    ok &= np.allclose(c * np.linalg.norm(raw, axis=1, keepdims=True) / np.linalg.norm(c, axis=1, keepdims=True), raw)
+    # closed form: hd 4, rot 2, ratio 2, rows [1,1,1,1],[3,3,3,3] -> mean 2, RMS-normalised 1;
+    # block 1 sits at position 2 -> the pair (0,1) turns by 2 rad (frequency theta^0)
+    r2 = np.array([[1, 1, 1, 1], [3, 3, 3, 3], [1, 1, 1, 1], [3, 3, 3, 3.0]])
+    out = oracle.block_pool(r2, np.zeros(4), 1, 1, 2, 2, 1e6, 0.0)
+    want = [math.cos(2) - math.sin(2), math.cos(2) + math.sin(2), 1, 1]
+    ok &= np.allclose(out[0], want, rtol=1e-14, atol=1e-15)
+    # second pair frequency: hd 4, rot 4, position 8 -> pair (1,3) turns by 8 * theta^(-1/2)
+    out = oracle.block_pool(np.ones((16, 4)), np.zeros(4), 1, 1, 8, 4, 100.0, 0.0)
+    ang = 8 * 100.0 ** -0.5
+    ok &= np.allclose(out[0, [1, 3]], [math.cos(ang) - math.sin(ang), math.cos(ang) + math.sin(ang)], atol=1e-14)
+    return bool(ok)
+
+
+def pin_qsa_score_handcase():
+    """qsa.rs qsa_score on a hand-summed case: heads [1,0,..] and [0,-1,..],
+    keys [2,3,..] and [-1,1,..], hd=4 -> score0 = (2 + 0)/2 = 1,
+    score1 = (0 + 0)/2 = 0 (both dots of key 1 are <= 0: -1 and -1)."""
+    q = np.array([[1, 0, 0, 0], [0, -1, 0, 0]], float)
+    k = np.array([[2, 3, 0, 0], [-1, 1, 0, 0]], float)
+    return np.array_equal(oracle.qsa_score(q, k), [1.0, 0.0])
+
+
+def pin_expand_blocks():
+    got = oracle.expand_blocks(np.array([[5, -1, 2]]), 3)
+    return list(got[0]) == [6, 7, 8, 15, 16, 17, -1, -1, -1]
+
+
+PINS = [pin_e2m1_printed_table, pin_e2m1_bitlevel, pin_e4m3_library, pin_e4m3_anchors,
+        lambda: pin_golden("tiny_score_a.json"), lambda: pin_golden("tiny_score_ties.json"),
+        lambda: pin_golden("tiny_score_shared.json"), pin_onehot_layout, pin_closed_form,
+        pin_block_permutation, pin_pow2_scaling, pin_positive_scaling_topk, pin_topk_vs_lexsort,
+        pin_topk_bruteforce, pin_mask, pin_bad_inputs, pin_valid_lens_from_blocks,
+        pin_gather_library, pin_pool_special_cases, pin_qsa_score_handcase, pin_expand_blocks]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda f: getattr(f, "__name__", "golden"))
+def test_pin(pin):
+    assert pin()
+
+
+def test_integer_decode_is_a_negative_control():
+    """The integer decode shipped before commit 79ef87f differs from E2M1 on
+    every non-zero magnitude code: the bug report that commit describes."""
+    integer = np.arange(8, dtype=np.float64)
+    e2m1 = oracle.e2m1_decode(np.arange(8))
+    assert list(np.nonzero(integer != e2m1)[0]) == [1, 2, 3, 4, 5, 6, 7]
+
+
+# ------------------------------------------------------- planted mistakes ----
+
+def _all_pins_pass():
+    return all(p() for p in PINS)
+
+
+MUTATIONS = {
+    "integer_fp4_decode": ("e2m1_decode", lambda c: np.where(np.asarray(c) & 8, -1.0, 1.0) * (np.asarray(c) & 7)),
+    "nibble_order_swapped": ("unpack_nibbles", lambda p: (lambda a: np.stack([(a >> 4) & 0xF, a & 0xF], -1).reshape(a.shape[:-1] + (-1,)))(np.asarray(p, np.int64))),
+    "e4m3_bias_8": ("e4m3_decode", lambda b: (lambda x: np.where((x >> 3) & 15 == 0, (x & 7) / 8 * 2.0 ** -7, (1 + (x & 7) / 8) * np.exp2(((x >> 3) & 15) - 8.0)) * np.where(x & 128, -1, 1))(np.asarray(b, np.int64) & 255)),
+}
+
+
+def _mut_index_scores_no_relu(q_t, w_t, K):
+    return (np.asarray(K, np.float64) @ np.asarray(q_t, np.float64).T) @ np.asarray(w_t, np.float64)
+
+
+def _mut_group_by_8(keys_fp4, key_scale, key_gscale, phys, slot):
+    codes = oi.unpack_nibbles(np.asarray(keys_fp4)[phys, slot])
+    vals = oi.e2m1_decode(codes)
+    scales = oi.e4m3_decode(np.asarray(key_scale)[phys, slot])
+    grp = np.minimum(np.arange(vals.shape[-1]) // 8, scales.shape[-1] - 1)
+    return vals * scales[:, grp] * np.asarray(key_gscale, np.float64)[phys][:, None]
+
+
+def _mut_slot_swapped(table_row, valid_len, epb, n_phys):
+    s = np.arange(int(valid_len))
+    logical = np.minimum(s % epb, len(table_row) - 1)
+    slot = np.minimum(s // epb, epb - 1)
+    phys = np.asarray(table_row, np.int64)[logical]
+    return phys, slot, (phys >= 0) & (phys < n_phys)
+
+
+def _mut_ties_high_index_first(scores, k, index=None):
+    sc = np.asarray(scores, np.float64)
+    ix = np.arange(len(sc)) if index is None else np.asarray(index)
+    order = np.lexsort((-ix, -sc))
+    out_i = np.full(k, -1); out_s = np.full(k, -np.inf)
+    n = min(k, len(sc)); out_i[:n] = ix[order][:n]; out_s[:n] = sc[order][:n]
+    return out_i, out_s
+
+
+def _mut_weight_inside_relu(q_t, w_t, K):
+    dots = np.asarray(K, np.float64) @ np.asarray(q_t, np.float64).T
+    return np.maximum(dots * np.asarray(w_t, np.float64), 0.0).sum(axis=1)
+
+
+@pytest.mark.parametrize("name,target,fn", [
+    *[(k, v[0], v[1]) for k, v in MUTATIONS.items()],
+    ("relu_dropped", "index_scores", _mut_index_scores_no_relu),
+    ("weight_inside_relu", "index_scores", _mut_weight_inside_relu),
+    ("group_of_8", "dequant_rows", _mut_group_by_8),
+    ("block_and_slot_swapped", "resolve_slots", _mut_slot_swapped),
+    ("ties_high_index_first", "topk_sorted", _mut_ties_high_index_first),
+])
+def test_planted_mistake_is_caught(monkeypatch, name, target, fn):
+    monkeypatch.setattr(oi, target, fn)
+    monkeypatch.setattr(oracle, target, fn, raising=False)
+    assert not _all_pins_pass(), f"planted mistake {name!r} in {target} went unnoticed"
