@@ -1,0 +1,364 @@
+"""Benchmark of the lightning-indexer hot path on GB300.
+
+One step = one idx_score_topk call (tcgen05 scoring kernel + top-k merge
+kernel) over the batched-decode workload: T=64 queries, H=64 heads, D=128,
+valid lengths uniform in [8192, 32768], 64-entry blocks, per-query block tables
+over a 40000-block NVFP4 pool, top_k=512. Inputs are seeded and synthetic and
+resident in HBM when timing starts; L2 is flushed (a 256 MB write) before
+every timed step, outside the timed events.
+
+Prints one JSON line: scored (query, key) pairs per second (whole job), the
+device-timed value, an end-to-end value through the public API with host
+buffers (pinned H2D of the step's q, w, block table and valid lengths; D2H of
+the top-k indices and scores), the roofline of the scoring kernel against the
+measured HBM copy bandwidth, and the float64 CPU oracle timed on a bounded
+sample of the same workload.
+
+--impl reference times that oracle alone (the CPU reference arm).
+--gpus N (under torchrun): every rank runs its own batch (weak scaling); the
+timed region is bracketed by a barrier and synchronisation and the slowest
+rank's time is used.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "indexer (query,key) scores+top-k per sec; % of HBM / tensor-core roofline"
+UNIT = "pairs/s"
+BYTES_PER_PAIR = 64 + 8 + 4.0 / 64 + 4.0 / 64     # nibbles + E4M3 scales + gscale + table entry
+WORKLOAD = "batched_decode"
+
+
+def workload_config(W):
+    return {
+        "workload": f"{WORKLOAD}: T={W.T} H={W.H} D={W.D} valid_lens~U[8192,32768] epb={W.epb} "
+                    f"P={W.P} top_k={W.top_k} NVFP4 keys, per-query block tables",
+        "T": W.T, "H": W.H, "D": W.D, "entries_per_block": W.epb, "pool_blocks": W.P,
+        "top_k": W.top_k, "pairs_per_step": W.pairs,
+        "l2": "flushed before every timed step (256 MB write, outside the timed events)",
+        "seed": W.meta.get("seed"),
+    }
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank scores its own batch (weak scaling): seed 1001 + rank."""
+    return 1001 + rank
+
+
+def whole_job(pairs_per_rank, steps: int, seconds_per_rank, dist=None, device=None):
+    """Whole-job throughput: all ranks' pairs over the slowest rank's time.
+
+    With ``dist`` the per-rank pair counts are summed and the times maxed
+    across the process group; returns ``(pairs_per_second, max_seconds)``."""
+    if dist is None:
+        return pairs_per_rank * steps / seconds_per_rank, seconds_per_rank
+    import torch
+    t = torch.tensor([float(seconds_per_rank)], dtype=torch.float64, device=device)
+    n = torch.tensor([float(pairs_per_rank)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(n.item()) * steps / float(t.item()), float(t.item())
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0])); mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _oracle_sample(args):
+    """Runs in a spawned process: the float64 oracle on the first n queries."""
+    seed, n_queries, threads = args
+    os.environ["OPENBLAS_NUM_THREADS"] = str(threads)
+    os.environ["OMP_NUM_THREADS"] = str(threads)
+    import numpy as np  # noqa: F401
+    import oracle
+    from sparse_attention_top_paged_gb300 import workloads as wl
+    W = wl.batched_decode(seed)
+    rows = list(range(n_queries))
+    t0 = time.perf_counter()
+    oracle.score_topk(W.q, W.w, W.block_table, W.bt_stride, W.max_lb, W.valid_lens, W.epb, W.top_k,
+                      rows=rows, **W.oracle_kwargs())
+    dt = time.perf_counter() - t0
+    pairs = int(sum(int(W.valid_lens[t]) for t in rows))
+    return pairs, dt
+
+
+def cpu_baseline(seed: int, n_queries: int):
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0))
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(1) as pool:
+        pairs, dt = pool.apply(_oracle_sample, ((seed, n_queries, cores),))
+    return {"value": pairs / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {n_queries} of the {WORKLOAD} queries ({pairs} pairs), numpy float64, "
+                      f"{dt:.2f} s", "seconds": dt}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is a bounded sample."""
+    if rank != 0:
+        return
+    from sparse_attention_top_paged_gb300 import workloads as wl
+    W = wl.batched_decode(1001)
+    n_q = args.ref_queries
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state; warm-up steps are skipped
+    times, pairs = [], 0
+    for _ in range(args.steps):
+        p, dt = _oracle_sample((1001, n_q, len(os.sched_getaffinity(0))))
+        times.append(dt)
+        pairs += p
+    total = sum(times)
+    value = pairs / total
+    cores = len(os.sched_getaffinity(0))
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(W), "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"first {n_q} queries per step, numpy float64"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="auto", choices=["auto", "tensor", "simt"])
+    ap.add_argument("--ref-queries", type=int, default=4)
+    ap.add_argument("--cpu-queries", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import numpy as np
+    import torch
+    import sparse_attention_top_paged_gb300 as idx
+    from sparse_attention_top_paged_gb300 import _lib
+    from sparse_attention_top_paged_gb300 import workloads as wl
+
+    # the CPU baseline runs in a spawned process before any GPU work
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(1001, args.cpu_queries)
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    W = wl.batched_decode(rank_seed(rank))
+    dev = torch.device("cuda", local)
+    q = torch.from_numpy(W.q).to(dev)
+    w = torch.from_numpy(W.w).to(dev)
+    bt = torch.from_numpy(W.block_table).to(dev)
+    vl = torch.from_numpy(W.valid_lens).to(dev)
+    fp4 = torch.from_numpy(W.keys_fp4).to(dev)
+    sc = torch.from_numpy(W.key_scale).to(dev)
+    gs = torch.from_numpy(W.key_gscale).to(dev)
+    k = W.top_k
+    out_i = torch.empty((W.T, k), dtype=torch.int32, device=dev)
+    out_s = torch.empty((W.T, k), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    lib = idx.load_library()
+    stream = torch.cuda.current_stream(dev)
+
+    a = idx.make_score_args(q, w, bt, vl, k, entries_per_block=W.epb, keys_fp4=fp4, key_scale=sc,
+                            key_gscale=gs, topk_idx=out_i, topk_score=out_s, dev_status=status,
+                            path=args.path)
+    ws_bytes = idx.score_topk_workspace_bytes(a)
+    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    import ctypes
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    def step(events=None):
+        if events is not None:
+            a.timing_events[0] = events[0].cuda_event
+            a.timing_events[1] = events[1].cuda_event
+        else:
+            a.timing_events[0] = None
+            a.timing_events[1] = None
+        rc = lib.idx_score_topk(ctypes.byref(a), sptr)
+        if rc != 0:
+            raise idx.IndexerError("idx_score_topk", rc)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for pair in kev:          # torch creates the CUDA event on first record; the library records it later
+        pair[0].record(stream)
+        pair[1].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step(kev[i])
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if dist:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in ev]
+    kern_ms = [s.elapsed_time(e) for s, e in kev]
+    pairs_step = W.pairs
+    value, t_total = whole_job(pairs_step, K, sum(step_ms) / 1e3, dist, dev)
+
+    # ---- end to end through the public Python API with host buffers ----
+    pin = lambda x: torch.from_numpy(x).pin_memory()
+    hq, hw, hbt, hvl = pin(W.q), pin(W.w), pin(W.block_table), pin(W.valid_lens)
+    ho_i = torch.empty((W.T, k), dtype=torch.int32).pin_memory()
+    ho_s = torch.empty((W.T, k), dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hw, hbt, hvl))
+    d2h = ho_i.numel() * 4 + ho_s.numel() * 4
+    E = max(10, K // 10)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True); w.copy_(hw, non_blocking=True)
+        bt.copy_(hbt, non_blocking=True); vl.copy_(hvl, non_blocking=True)
+        idx.score_topk(q, w, bt, vl, k, entries_per_block=W.epb, keys_fp4=fp4, key_scale=sc, key_gscale=gs,
+                       out=(out_i, out_s), workspace=ws)
+        ho_i.copy_(out_i, non_blocking=True); ho_s.copy_(out_s, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(E):
+        flush.zero_()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        e2e_step()
+        s1.record(stream)
+        e2e_ms.append((s0, s1))
+    torch.cuda.synchronize()
+    e2e_value, _ = whole_job(pairs_step, E, sum(s.elapsed_time(e) for s, e in e2e_ms) / 1e3, dist, dev)
+
+    # ---- roofline of the scoring kernel (HBM bound) ----
+    peak, peak_kind = peaks()
+    kern_s = statistics.mean(kern_ms) / 1e3
+    algo_bytes = pairs_step * BYTES_PER_PAIR + W.T * (4 * W.H * W.D + 4 * W.H + 4)
+    achieved = algo_bytes / kern_s / 1e9
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "score_tc_kernel.traffic.json")
+    if os.path.exists(tfile):
+        traffic = json.load(open(tfile)).get("bytes_per_launch")
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_total / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": dict(workload_config(W), parallelism=f"replicas x{world} (independent batches)",
+                           mma="tcgen05 kind::f16, f16 x f16 -> f32 (exact for NVFP4 x bf16-valued q)"),
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * K,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "score_tc_kernel", "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_launch": algo_bytes,
+                         "kernel_ms": 1e3 * kern_s},
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "wall_s": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

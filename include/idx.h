@@ -1,0 +1,230 @@
+/*
+ * idx.h — C ABI of libidx: the sparse-attention lightning indexer over a paged
+ * NVFP4 key pool, QSA-style key pooling, and the selected-row K/V gather, for
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers marked "device" are CUDA device (or managed) memory owned by the
+ *   caller; the library never frees or retains them and allocates nothing.
+ * - Every call is asynchronous on `stream` (NULL = the legacy default stream).
+ *   Nothing synchronises the host.
+ * - The return value reports what the host can check before launching:
+ *   IDX_ERR_INVALID_ARG (a null pointer, a negative size, a misaligned
+ *   pointer), IDX_ERR_UNSUPPORTED (a legal shape this build has no kernel
+ *   for), IDX_ERR_WORKSPACE_TOO_SMALL, IDX_ERR_CUDA (a launch error). On any
+ *   error nothing has been launched.
+ * - Bad data that only the device can see never faults and never traps: it
+ *   ORs a bit into the optional device word `dev_status` (IDX_STATUS_*) and
+ *   the affected outputs take their "empty" value (index -1, score -inf, a
+ *   zero row). `dev_status` is never cleared by the library.
+ * - `idx_stream_t` is the same handle as `cudaStream_t`.
+ */
+#ifndef IDX_H_
+#define IDX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *idx_stream_t;
+
+typedef enum {
+  IDX_OK = 0,
+  IDX_ERR_INVALID_ARG = 1,
+  IDX_ERR_UNSUPPORTED = 2,
+  IDX_ERR_WORKSPACE_TOO_SMALL = 3,
+  IDX_ERR_CUDA = 4
+} idx_status_t;
+
+/* Bits ORed into the caller's device status word. */
+#define IDX_STATUS_BAD_BLOCK 1 /* a block-table entry outside [0, P)                       */
+#define IDX_STATUS_BAD_LEN 2   /* a valid length outside [0, max_logical_blocks * epb]      */
+#define IDX_STATUS_BAD_SEL 4   /* a gather position whose logical block is past the table   */
+#define IDX_STATUS_TIMEOUT 8   /* an internal pipeline wait gave up (2 s); outputs invalid   */
+
+typedef enum { IDX_KEYS_NVFP4 = 0, IDX_KEYS_F32 = 1 } idx_key_format_t;
+
+/* Which kernels idx_score_topk runs. AUTO picks the tensor-core path for
+ * NVFP4 keys and the CUDA-core path for F32 keys. */
+typedef enum { IDX_PATH_AUTO = 0, IDX_PATH_TENSOR = 1, IDX_PATH_SIMT = 2 } idx_path_t;
+
+/*
+ * idx_score_topk — lightning-indexer scores and their top-k.
+ *
+ * Computes, for every query t and every valid key s < valid_lens[t],
+ *     I[t,s] = sum_h w[t,h] * max(q[t,h,:] . K[s,:], 0)
+ * (eq. 16 in the header comment of "indexer_score_topk.cu",
+ * nvfp4-megamoe-kernel dsv4/kernels/indexer; one key row per s shared by all
+ * heads, as that page's main loop reads it), and returns TopK(I[t,:], top_k)
+ * sorted by score descending, lower index first on equal scores, padded with
+ * index -1 / score -inf when fewer than top_k keys are valid (the top-k
+ * write-out section of the same page). -0.0 scores are reported as +0.0.
+ *
+ * Keys (the "Main kernel" argument list of that page):
+ *   NVFP4: K[s,d] = e2m1(code) * e4m3(key_scale[row, d/16]) * key_gscale[phys]
+ *     keys_fp4   device [P, epb, D/2] uint8, low nibble = even element d;
+ *                E2M1 magnitudes {0,.5,1,1.5,2,3,4,6}, bit 3 the sign
+ *                (commits 79ef87f and e74c844 of the indexer commit graph)
+ *     key_scale  device [P, epb, D/16] uint8, FP8 E4M3 (OCP e4m3fn)
+ *     key_gscale device [P] float32
+ *   F32: keys_f32 device [P, epb, D] float32 (the QSA pooled keys of
+ *     "metrale_model_layers/layers/ops/qsa.rs", qsa_score).
+ * Slot resolution: lb = s / epb, slot = s % epb,
+ *   phys = block_table[t * bt_stride + lb], row = phys * epb + slot.
+ *   bt_stride = 0 makes every query read table row 0 (one sequence, many rows).
+ *
+ * Arguments (all sizes in elements):
+ *   T >= 0, H in [1, 256], D: 128 (NVFP4) or 64/128 (F32)
+ *   q          device [T, H, D] float32 (callers upcast bf16, as the
+ *              score_topk launcher of commit c2f705a does)
+ *   w          device [T, H] float32
+ *   P >= 1, entries_per_block (epb) >= 1; NVFP4 needs epb % 16 == 0
+ *   block_table device int32, row t at block_table + t * bt_stride, with
+ *              max_logical_blocks entries
+ *   valid_lens device [T] int32
+ *   top_k in [1, 4096]
+ *   topk_idx   device [T, top_k] int32   (output)
+ *   topk_score device [T, top_k] float32 (output)
+ *   scores_out optional device [T, ld_scores] float32: when non-NULL, every
+ *              I[t,s] (s < valid_lens[t]) is also written, -inf for keys of
+ *              an out-of-range block; ld_scores >= max_logical_blocks * epb
+ *   dev_status optional device int32 (IDX_STATUS_* bits ORed in)
+ *   workspace  device scratch of at least idx_score_topk_workspace_size()
+ *              bytes, 256-byte aligned. It must be zero-filled before its
+ *              first use; every call leaves it ready for the next one.
+ *              Calls that share a workspace must not overlap in time.
+ *   path       idx_path_t
+ *   num_ctas   CTAs of the persistent score kernel; 0 = one per SM
+ *   timing_events optional pair of cudaEvent_t (as void*): when both are
+ *              non-NULL, [0] is recorded on `stream` just before the scoring
+ *              kernel and [1] just after it (the top-k kernel follows), so a
+ *              caller can time the scoring kernel alone.
+ * Device-side errors: a table entry outside [0,P) drops that block's keys
+ * (IDX_STATUS_BAD_BLOCK); a valid length outside [0, max_logical_blocks*epb]
+ * pads that query's whole output (IDX_STATUS_BAD_LEN).
+ */
+typedef struct {
+  int32_t T, H, D;
+  const float *q;
+  const float *w;
+  int32_t key_format; /* idx_key_format_t */
+  const uint8_t *keys_fp4;
+  const uint8_t *key_scale;
+  const float *key_gscale;
+  const float *keys_f32;
+  int32_t P, entries_per_block;
+  const int32_t *block_table;
+  int32_t max_logical_blocks;
+  int64_t bt_stride;
+  const int32_t *valid_lens;
+  int32_t top_k;
+  int32_t *topk_idx;
+  float *topk_score;
+  float *scores_out;
+  int64_t ld_scores;
+  int32_t *dev_status;
+  void *workspace;
+  size_t workspace_bytes;
+  int32_t path;     /* idx_path_t */
+  int32_t num_ctas; /* 0 = one per SM of the current device */
+  void *timing_events[2];
+} idx_score_topk_args;
+
+/* Bytes of workspace idx_score_topk needs for these arguments (host only; no
+ * device work; with num_ctas == 0 it queries the current device's SM count).
+ * Writes *bytes; returns IDX_ERR_INVALID_ARG / IDX_ERR_UNSUPPORTED like
+ * idx_score_topk would. */
+idx_status_t idx_score_topk_workspace_size(const idx_score_topk_args *args, size_t *bytes);
+
+idx_status_t idx_score_topk(const idx_score_topk_args *args, idx_stream_t stream);
+
+/*
+ * idx_gather_kv — copy selected rows of a paged K/V cache into a dense tile.
+ *
+ * "metrale_model_layers/layers/ops/qsa.rs", qsa_gather: slot i of the output
+ * holds position sel[t,i]; and the gather of commit c2f705a (indexer commit
+ * graph): rows resolved through the block table. For p = sel[t,i] >= 0:
+ *   phys = block_table[t * bt_stride + p / block_size], row p % block_size,
+ *   k_out[t,i,:] = k_cache[phys, row, :] (bytes, unchanged), same for v.
+ * p < 0 gives a zero row. p / block_size >= max_logical_blocks gives a zero
+ * row and IDX_STATUS_BAD_SEL; phys outside [0,P) a zero row and
+ * IDX_STATUS_BAD_BLOCK.
+ *   sel          device [T, n_sel] int32
+ *   k_cache, v_cache device [P, block_size, row_bytes] (any element type);
+ *                v_cache / v_out may both be NULL (K only)
+ *   row_bytes    > 0, multiple of 16; all four data pointers 16-byte aligned
+ *   k_out, v_out device [T, n_sel, row_bytes]
+ */
+typedef struct {
+  int32_t T, n_sel;
+  const int32_t *sel;
+  const int32_t *block_table;
+  int32_t max_logical_blocks;
+  int64_t bt_stride;
+  int32_t P, block_size;
+  const void *k_cache;
+  const void *v_cache;
+  int64_t row_bytes;
+  void *k_out;
+  void *v_out;
+  int32_t *dev_status;
+} idx_gather_kv_args;
+
+idx_status_t idx_gather_kv(const idx_gather_kv_args *args, idx_stream_t stream);
+
+/*
+ * idx_block_pool — pool newly complete blocks of raw keys into block keys.
+ *
+ * "metrale_model_layers/layers/ops/qsa.rs", qsa_block_pool: for block
+ * b = first_block + i, i < n_new: the mean m of raw rows
+ * [b*ratio, (b+1)*ratio), then y = m / sqrt(mean(m^2) + eps) * (1 + w), then
+ * rope on the first `rot` dimensions at position b*ratio, pairing d with
+ * d + rot/2 at angle pos * theta^(-2d/rot) (d < rot/2).
+ *   raw_keys    device [(first_block+n_new)*ratio, hd] bf16 (raw bit patterns)
+ *   k_norm_w    device [hd] float32
+ *   block_keys  device [first_block + n_new, hd] float32; rows
+ *               first_block .. first_block+n_new-1 are written
+ *   hd a multiple of 32 in [32, 1024]; rot even, rot <= hd; ratio >= 1
+ * n_new == 0 returns IDX_OK without launching (as qsa_block_pool does).
+ */
+idx_status_t idx_block_pool(const uint16_t *raw_keys, const float *k_norm_w, float *block_keys,
+                            uint32_t first_block, uint32_t n_new, uint32_t ratio, uint32_t hd,
+                            uint32_t rot, float theta, float eps, idx_stream_t stream);
+
+/*
+ * idx_expand_blocks — token positions of selected blocks, for idx_gather_kv.
+ *
+ * qsa.rs, qsa_gather fills slot i with position sel[i]; the page does not
+ * say in which order blocks are laid out. This call takes the selected block
+ * indices of each query (blocks [T, n_blocks], -1 = none, any order, e.g. a
+ * top-k output), sorts them ascending and writes each block's `ratio`
+ * positions b*ratio .. b*ratio+ratio-1 in order, then -1 in the unused tail:
+ *   positions device [T, n_blocks * ratio] int32.
+ * n_blocks in [0, 4096], ratio >= 1.
+ */
+idx_status_t idx_expand_blocks(const int32_t *blocks, int32_t T, int32_t n_blocks, int32_t ratio,
+                               int32_t *positions, idx_stream_t stream);
+
+/*
+ * idx_valid_lens_from_blocks — valid_lens[t] = block_lens[t] * epb.
+ * compute_valid_lens of commit c2f705a (every entry of an allocated block is
+ * valid).  block_lens, valid_lens: device [T] int32.
+ */
+idx_status_t idx_valid_lens_from_blocks(const int32_t *block_lens, int32_t T, int32_t epb,
+                                        int32_t *valid_lens, idx_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *idx_status_string(idx_status_t status);
+
+/* Library ABI version, (major << 16) | minor. */
+uint32_t idx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IDX_H_ */

@@ -1,0 +1,230 @@
+"""GB300-native lightning indexer over a paged NVFP4 key pool.
+
+Python face of libidx (``include/idx.h``). Each function checks and marshals
+its torch arguments and calls the library; outputs are allocated with torch on
+the inputs' device, and work is queued on the current CUDA stream.
+
+* :func:`score_topk`   -> ``idx_score_topk``   (scores, top-k indices and scores)
+* :func:`gather_kv`    -> ``idx_gather_kv``    (selected K/V rows -> dense tile)
+* :func:`block_pool`   -> ``idx_block_pool``   (QSA mean -> RMSNorm(1+w) -> RoPE)
+* :func:`expand_blocks` -> ``idx_expand_blocks`` (selected blocks -> positions)
+* :func:`valid_lens_from_blocks` -> ``idx_valid_lens_from_blocks``
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+from ._lib import (IndexerError, KEYS_F32, KEYS_NVFP4, PATHS, STATUS_BAD_BLOCK,  # noqa: F401
+                   STATUS_BAD_LEN, STATUS_BAD_SEL, load_library)
+
+_workspaces: dict = {}
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, dtype=None, dims=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dims, got {t.dim()}")
+
+
+def _stream(device):
+    torch = _torch()
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _raise(where, code):
+    if code != _lib.IDX_OK:
+        raise IndexerError(where, code)
+
+
+def _workspace(device, nbytes):
+    """A zero-filled workspace of at least ``nbytes`` on ``device``, reused
+    across calls (the library leaves it ready for the next call)."""
+    torch = _torch()
+    key = (str(device),)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def make_score_args(q, w, block_table, valid_lens, top_k, *, entries_per_block, keys_fp4=None,
+                    key_scale=None, key_gscale=None, keys_f32=None, bt_stride=None,
+                    topk_idx=None, topk_score=None, scores_out=None, dev_status=None,
+                    path="auto", num_ctas=0):
+    """Build an ``idx_score_topk_args`` from torch tensors (no device work)."""
+    torch = _torch()
+    _check(q, "q", torch.float32, 3)
+    _check(w, "w", torch.float32, 2)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(valid_lens, "valid_lens", torch.int32, 1)
+    T, H, D = q.shape
+    a = _lib.ScoreTopkArgs()
+    a.T, a.H, a.D = T, H, D
+    a.q, a.w = q.data_ptr(), w.data_ptr()
+    if keys_f32 is not None:
+        _check(keys_f32, "keys_f32", torch.float32, 3)
+        a.key_format = KEYS_F32
+        a.keys_f32 = keys_f32.data_ptr()
+        a.P = keys_f32.shape[0]
+    else:
+        _check(keys_fp4, "keys_fp4", torch.uint8, 3)
+        _check(key_scale, "key_scale", torch.uint8, 3)
+        _check(key_gscale, "key_gscale", torch.float32, 1)
+        a.key_format = KEYS_NVFP4
+        a.keys_fp4, a.key_scale, a.key_gscale = keys_fp4.data_ptr(), key_scale.data_ptr(), key_gscale.data_ptr()
+        a.P = keys_fp4.shape[0]
+    a.entries_per_block = entries_per_block
+    a.block_table = block_table.data_ptr()
+    a.max_logical_blocks = block_table.shape[1]
+    a.bt_stride = block_table.shape[1] if bt_stride is None else bt_stride
+    a.valid_lens = valid_lens.data_ptr()
+    a.top_k = top_k
+    if topk_idx is not None:
+        a.topk_idx = topk_idx.data_ptr()
+    if topk_score is not None:
+        a.topk_score = topk_score.data_ptr()
+    if scores_out is not None:
+        _check(scores_out, "scores_out", torch.float32, 2)
+        a.scores_out = scores_out.data_ptr()
+        a.ld_scores = scores_out.shape[1]
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32)
+        a.dev_status = dev_status.data_ptr()
+    a.path = PATHS[path]
+    a.num_ctas = num_ctas
+    return a
+
+
+def score_topk(q, w, block_table, valid_lens, top_k, *, entries_per_block, keys_fp4=None,
+               key_scale=None, key_gscale=None, keys_f32=None, bt_stride=None, scores_out=None,
+               dev_status=None, path="auto", num_ctas=0, out=None, workspace=None):
+    """Top-k lightning-indexer keys per query: ``(topk_idx [T,k] int32,
+    topk_score [T,k] float32)``. ``bt_stride=0`` shares table row 0 across
+    queries. ``scores_out`` (``[T, ld]`` float32) also receives every score."""
+    torch = _torch()
+    T = q.shape[0]
+    if out is None:
+        topk_idx = torch.empty((T, top_k), dtype=torch.int32, device=q.device)
+        topk_score = torch.empty((T, top_k), dtype=torch.float32, device=q.device)
+    else:
+        topk_idx, topk_score = out
+    a = make_score_args(q, w, block_table, valid_lens, top_k, entries_per_block=entries_per_block,
+                        keys_fp4=keys_fp4, key_scale=key_scale, key_gscale=key_gscale,
+                        keys_f32=keys_f32, bt_stride=bt_stride, topk_idx=topk_idx,
+                        topk_score=topk_score, scores_out=scores_out, dev_status=dev_status,
+                        path=path, num_ctas=num_ctas)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        need = ctypes.c_size_t(0)
+        _raise("idx_score_topk_workspace_size", lib.idx_score_topk_workspace_size(ctypes.byref(a), ctypes.byref(need)))
+        ws = workspace if workspace is not None else _workspace(q.device, need.value)
+        a.workspace = ws.data_ptr()
+        a.workspace_bytes = ws.numel() * ws.element_size()
+        _raise("idx_score_topk", lib.idx_score_topk(ctypes.byref(a), _stream(q.device)))
+    return topk_idx, topk_score
+
+
+def score_topk_workspace_bytes(args) -> int:
+    need = ctypes.c_size_t(0)
+    _raise("idx_score_topk_workspace_size",
+           load_library().idx_score_topk_workspace_size(ctypes.byref(args), ctypes.byref(need)))
+    return need.value
+
+
+def gather_kv(sel, block_table, block_size, k_cache, v_cache=None, *, bt_stride=None,
+              dev_status=None, out=None):
+    """Dense ``[T, n_sel, ...]`` copies of the K (and V) cache rows at the
+    positions ``sel [T, n_sel]`` (-1: zero row). Caches: ``[P, block_size, ...]``."""
+    torch = _torch()
+    _check(sel, "sel", torch.int32, 2)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(k_cache, "k_cache")
+    if v_cache is not None:
+        _check(v_cache, "v_cache")
+    T, n = sel.shape
+    row_shape = tuple(k_cache.shape[2:])
+    if out is None:
+        k_out = torch.empty((T, n) + row_shape, dtype=k_cache.dtype, device=k_cache.device)
+        v_out = None if v_cache is None else torch.empty((T, n) + row_shape, dtype=v_cache.dtype, device=v_cache.device)
+    else:
+        k_out, v_out = out
+    a = _lib.GatherKvArgs()
+    a.T, a.n_sel = T, n
+    a.sel, a.block_table = sel.data_ptr(), block_table.data_ptr()
+    a.max_logical_blocks = block_table.shape[1]
+    a.bt_stride = block_table.shape[1] if bt_stride is None else bt_stride
+    a.P, a.block_size = k_cache.shape[0], block_size
+    a.k_cache = k_cache.data_ptr()
+    a.v_cache = v_cache.data_ptr() if v_cache is not None else None
+    a.row_bytes = k_cache[0, 0].numel() * k_cache.element_size()
+    a.k_out = k_out.data_ptr()
+    a.v_out = v_out.data_ptr() if v_out is not None else None
+    a.dev_status = dev_status.data_ptr() if dev_status is not None else None
+    lib = load_library()
+    with torch.cuda.device(k_cache.device):
+        _raise("idx_gather_kv", lib.idx_gather_kv(ctypes.byref(a), _stream(k_cache.device)))
+    return k_out, v_out
+
+
+def block_pool(raw_keys, k_norm_w, block_keys, first_block, n_new, ratio, rot, theta, eps):
+    """Pool blocks ``first_block .. first_block+n_new-1`` of ``raw_keys``
+    (bf16 ``[n_tok, hd]``) into rows of ``block_keys`` (float32 ``[nb, hd]``)."""
+    torch = _torch()
+    _check(raw_keys, "raw_keys", dims=2)
+    if raw_keys.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError("raw_keys must hold bf16 bit patterns (bfloat16 or 16-bit int)")
+    _check(k_norm_w, "k_norm_w", torch.float32, 1)
+    _check(block_keys, "block_keys", torch.float32, 2)
+    hd = raw_keys.shape[1]
+    if (first_block + n_new) * ratio > raw_keys.shape[0] or first_block + n_new > block_keys.shape[0]:
+        raise ValueError("block range exceeds raw_keys or block_keys")
+    lib = load_library()
+    with torch.cuda.device(raw_keys.device):
+        _raise("idx_block_pool", lib.idx_block_pool(
+            _ptr(raw_keys), _ptr(k_norm_w), _ptr(block_keys), first_block, n_new, ratio, hd, rot,
+            ctypes.c_float(theta), ctypes.c_float(eps), _stream(raw_keys.device)))
+    return block_keys
+
+
+def expand_blocks(blocks, ratio):
+    """``[T, nb]`` selected block ids (-1 none) -> ``[T, nb*ratio]`` ascending positions."""
+    torch = _torch()
+    _check(blocks, "blocks", torch.int32, 2)
+    T, nb = blocks.shape
+    pos = torch.empty((T, nb * ratio), dtype=torch.int32, device=blocks.device)
+    lib = load_library()
+    with torch.cuda.device(blocks.device):
+        _raise("idx_expand_blocks", lib.idx_expand_blocks(_ptr(blocks), T, nb, ratio, _ptr(pos),
+                                                          _stream(blocks.device)))
+    return pos
+
+
+def valid_lens_from_blocks(block_lens, entries_per_block):
+    torch = _torch()
+    _check(block_lens, "block_lens", torch.int32, 1)
+    out = torch.empty_like(block_lens)
+    lib = load_library()
+    with torch.cuda.device(block_lens.device):
+        _raise("idx_valid_lens_from_blocks", lib.idx_valid_lens_from_blocks(
+            _ptr(block_lens), block_lens.shape[0], entries_per_block, _ptr(out), _stream(block_lens.device)))
+    return out

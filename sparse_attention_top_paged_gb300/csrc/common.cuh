@@ -1,0 +1,238 @@
+// common.cuh — device helpers shared by the libidx kernels (sm_103a).
+//
+// Top-k machinery. Every candidate is a 64-bit composite key
+//     key = (order(score) << 32) | (0xFFFFFFFF - index)
+// where order() maps float bits to an unsigned integer with the same order
+// (-0.0 is folded into +0.0 first). A larger key is a better candidate: higher
+// score, then lower index — the output order of the top-k write-out in
+// "indexer_score_topk.cu" (score descending, lower index first on ties). Keys
+// are unique, so "the k largest keys" is one well-defined set and no tie
+// needs a rule beyond the key itself. Key 0 never encodes a real candidate
+// and serves as padding.
+//
+// A TopkGroup is a streaming top-k accumulator run by a group of NT threads
+// (whole warps) of one CTA: threads offer keys, the group appends those at or
+// above a running threshold to a shared-memory buffer, and when the buffer
+// fills it radix-selects the k largest keys in place and raises the threshold
+// to a value no greater than the k-th largest key seen so far. Nothing is
+// ever discarded that could still belong to the final top-k.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace idx {
+
+__device__ __forceinline__ uint32_t float_order(float f) {
+  uint32_t b = __float_as_uint(__fadd_rn(f, 0.0f));  // -0 + 0 = +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float order_float(uint32_t u) {
+  uint32_t b = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(b);
+}
+
+__device__ __forceinline__ uint64_t pack_key(float score, int32_t index) {
+  return (static_cast<uint64_t>(float_order(score)) << 32) |
+         static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(index));
+}
+
+__device__ __forceinline__ float key_score(uint64_t key) {
+  return order_float(static_cast<uint32_t>(key >> 32));
+}
+
+__device__ __forceinline__ int32_t key_index(uint64_t key) {
+  return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+}
+
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Named barrier over the NT threads of a group (ids 1..15; 0 is __syncthreads).
+template <int NT>
+__device__ __forceinline__ void group_sync(int bar_id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(NT) : "memory");
+}
+
+struct TopkShared {
+  uint32_t hist[256];
+  int count;   // entries in the buffer
+  int wcount;  // write cursor during compaction
+  int sel_bin, sel_above, sel_cnt;
+  int pad_;
+  unsigned long long thr;  // keys below thr can no longer enter the top-k
+};
+
+template <int NT>
+struct TopkGroup {
+  TopkShared *s;
+  uint64_t *buf;
+  int cap;     // buffer capacity in keys (>= k + NT)
+  int gtid;    // thread index within the group
+  int bar_id;  // named barrier of the group
+
+  __device__ __forceinline__ void sync() const { group_sync<NT>(bar_id); }
+
+  __device__ void reset() {
+    if (gtid == 0) {
+      s->count = 0;
+      s->thr = 0ull;
+    }
+    sync();
+  }
+
+  // Every thread of the group calls offer() once per round (valid=false to
+  // offer nothing). The caller guarantees count + NT <= cap before a round
+  // and calls after_round() after it.
+  __device__ __forceinline__ void offer(uint64_t key, bool valid) {
+    const bool acc = valid && key >= s->thr;
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, acc);
+    int base = 0;
+    if (lane_id() == 0 && m) base = atomicAdd(&s->count, __popc(m));
+    base = __shfl_sync(0xFFFFFFFFu, base, 0);
+    if (acc) buf[base + __popc(m & lanemask_lt())] = key;
+  }
+
+  // Ends a round of offers; compacts to the top k when the buffer could not
+  // take another round.
+  __device__ void after_round(int k) {
+    sync();
+    if (s->count > cap - NT) compact(k);
+  }
+
+  // Keep exactly the k largest keys (if more than k are held).
+  __device__ void compact(int k) {
+    const int n = s->count;
+    if (n <= k) return;
+    uint64_t prefix = 0, mask = 0;
+    int need = k;
+    for (int pass = 0; pass < 8; ++pass) {
+      const int shift = 56 - 8 * pass;
+      for (int i = gtid; i < 256; i += NT) s->hist[i] = 0u;
+      sync();
+      for (int i0 = gtid - static_cast<int>(lane_id()); i0 < n; i0 += NT) {
+        const int i = i0 + static_cast<int>(lane_id());
+        uint64_t key = 0;
+        bool part = false;
+        if (i < n) {
+          key = buf[i];
+          part = (key & mask) == prefix;
+        }
+        const uint32_t act = __ballot_sync(0xFFFFFFFFu, part);
+        if (part) {
+          const uint32_t dig = static_cast<uint32_t>(key >> shift) & 255u;
+          const uint32_t peers = __match_any_sync(act, dig);
+          if (static_cast<int>(lane_id()) == __ffs(peers) - 1) atomicAdd(&s->hist[dig], __popc(peers));
+        }
+      }
+      sync();
+      if (gtid < 32) {
+        // lane l owns bins 255-8l .. 248-8l, scanned from the top down
+        uint32_t c[8], tot = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = s->hist[255 - 8 * gtid - j];
+          tot += c[j];
+        }
+        uint32_t incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (gtid >= o) incl += v;
+        }
+        uint32_t run = incl - tot;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run < static_cast<uint32_t>(need) && run + c[j] >= static_cast<uint32_t>(need)) {
+            s->sel_bin = 255 - 8 * gtid - j;
+            s->sel_above = static_cast<int>(run);
+            s->sel_cnt = static_cast<int>(c[j]);
+          }
+          run += c[j];
+        }
+      }
+      sync();
+      const int bin = s->sel_bin;
+      need -= s->sel_above;
+      const int cnt = s->sel_cnt;
+      prefix |= static_cast<uint64_t>(bin) << shift;
+      mask |= 255ull << shift;
+      if (cnt == need) break;
+    }
+    // Keys whose masked prefix is >= prefix are exactly the k largest.
+    if (gtid == 0) s->wcount = 0;
+    sync();
+    constexpr int R = 8;
+    for (int base = 0; base < n; base += NT * R) {
+      uint64_t v[R];
+      bool keep[R];
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const int i = base + j * NT + gtid;
+        v[j] = (i < n) ? buf[i] : 0ull;
+        keep[j] = (i < n) && ((v[j] & mask) >= prefix);
+      }
+      sync();  // every key of this round is in registers before any write
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, keep[j]);
+        int b = 0;
+        if (lane_id() == 0 && m) b = atomicAdd(&s->wcount, __popc(m));
+        b = __shfl_sync(0xFFFFFFFFu, b, 0);
+        if (keep[j]) buf[b + __popc(m & lanemask_lt())] = v[j];
+      }
+      // Writes of this round land below base + NT*R (at most as many keys are
+      // kept as were read), so the next round's keys are untouched.
+    }
+    sync();
+    if (gtid == 0) {
+      s->count = s->wcount;
+      if (prefix > s->thr) s->thr = prefix;
+    }
+    sync();
+  }
+
+  // Sort the (at most k) held keys descending into buf[0 .. m), m the next
+  // power of two >= count, padding with key 0. Call after compact(k).
+  __device__ void sort_desc() {
+    const int n = s->count;
+    int m = 1;
+    while (m < n) m <<= 1;
+    for (int i = n + gtid; i < m; i += NT) buf[i] = 0ull;
+    sync();
+    for (int size = 2; size <= m; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = gtid; i < (m >> 1); i += NT) {
+          const int lo = 2 * stride * (i / stride) + (i % stride);
+          const int hi = lo + stride;
+          const bool desc = (lo & size) == 0;
+          const uint64_t a = buf[lo], b = buf[hi];
+          if ((a < b) == desc) {
+            buf[lo] = b;
+            buf[hi] = a;
+          }
+        }
+        sync();
+      }
+    }
+  }
+};
+
+// Shared-memory capacity (keys) of the top-k buffer of the row / merge kernels.
+__host__ __device__ inline int topk_rows_cap(int k, int nt) {
+  int kp = 1;
+  while (kp < k) kp <<= 1;
+  int cap = 4 * kp;
+  if (cap < 4096) cap = 4096;
+  if (cap > 16384) cap = 16384;
+  if (cap < kp + 2 * nt) cap = kp + 2 * nt;
+  return cap;
+}
+
+}  // namespace idx

@@ -1,0 +1,185 @@
+// gather_pool.cu — the selected-row K/V gather, QSA block-key pooling, the
+// block -> position expansion for the gather, and valid lengths from block
+// counts.
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace idx {
+namespace {
+
+// ---------------------------------------------------------------- gather ----
+// qsa.rs, qsa_gather: slot i of the dense output holds position sel[i]; the
+// row is found through the block table (commit c2f705a's gather_kv resolves
+// rows the same way). One warp copies one row in 16-byte vectors.
+constexpr int kGatherWarps = 8;
+
+__global__ void __launch_bounds__(kGatherWarps * 32) gather_kv_kernel(idx_gather_kv_args a) {
+  const long long r = static_cast<long long>(blockIdx.x) * kGatherWarps + (threadIdx.x >> 5);
+  const long long n_rows = static_cast<long long>(a.T) * a.n_sel;
+  if (r >= n_rows) return;
+  const int t = static_cast<int>(r / a.n_sel);
+  const int pos = a.sel[r];
+  long long src_row = -1;
+  int err = 0;
+  if (pos >= 0) {
+    const int lb = pos / a.block_size;
+    if (lb >= a.max_logical_blocks) {
+      err = IDX_STATUS_BAD_SEL;
+    } else {
+      const int phys = a.block_table[static_cast<long long>(t) * a.bt_stride + lb];
+      if (phys < 0 || phys >= a.P)
+        err = IDX_STATUS_BAD_BLOCK;
+      else
+        src_row = static_cast<long long>(phys) * a.block_size + pos % a.block_size;
+    }
+  }
+  if (err && lane_id() == 0 && a.dev_status) atomicOr(a.dev_status, err);
+  const long long nvec = a.row_bytes / 16;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  {
+    const uint4 *src = static_cast<const uint4 *>(a.k_cache) + (src_row >= 0 ? src_row : 0) * nvec;
+    uint4 *dst = static_cast<uint4 *>(a.k_out) + r * nvec;
+    for (long long c = lane_id(); c < nvec; c += 32) __stcs(dst + c, src_row >= 0 ? __ldg(src + c) : zero);
+  }
+  if (a.v_cache) {
+    const uint4 *src = static_cast<const uint4 *>(a.v_cache) + (src_row >= 0 ? src_row : 0) * nvec;
+    uint4 *dst = static_cast<uint4 *>(a.v_out) + r * nvec;
+    for (long long c = lane_id(); c < nvec; c += 32) __stcs(dst + c, src_row >= 0 ? __ldg(src + c) : zero);
+  }
+}
+
+// ------------------------------------------------------------ block pool ----
+// qsa.rs, qsa_block_pool: per block, the mean of `ratio` raw keys, RMSNorm
+// scaled by (1 + w), then rope on the first `rot` dimensions at the block's
+// first token position. One CTA per block, one thread per dimension (the
+// page's launch shape: grid n_new, block hd). Rope pairs d with d + rot/2;
+// the angle is formed in double precision.
+__global__ void block_pool_kernel(const uint16_t *__restrict__ raw, const float *__restrict__ w,
+                                  float *__restrict__ out, uint32_t first_block, uint32_t ratio,
+                                  uint32_t hd, uint32_t rot, float theta, float eps) {
+  extern __shared__ float sm[];  // [hd] pooled-normalised values, then [32] partial sums
+  float *y_s = sm;
+  float *red = sm + hd;
+  const uint32_t d = threadIdx.x;
+  const uint32_t b = first_block + blockIdx.x;
+  float m = 0.0f;
+  for (uint32_t r = 0; r < ratio; ++r) {
+    const uint32_t bits = raw[(static_cast<long long>(b) * ratio + r) * hd + d];
+    m += __uint_as_float(bits << 16);
+  }
+  m = m / static_cast<float>(ratio);
+  float sq = m * m;
+  for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+  if (lane_id() == 0) red[d >> 5] = sq;
+  __syncthreads();
+  if (d < 32) {
+    float v = (d < (hd + 31) / 32) ? red[d] : 0.0f;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if (d == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float inv_rms = rsqrtf(red[0] / static_cast<float>(hd) + eps);
+  const float y = m * inv_rms * (1.0f + w[d]);
+  y_s[d] = y;
+  __syncthreads();
+  float o = y;
+  const uint32_t half = rot / 2;
+  if (d < rot) {
+    const uint32_t i = d < half ? d : d - half;
+    const double pos = static_cast<double>(b) * ratio;
+    const double ang = pos * pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(rot));
+    double sn, cs;
+    sincos(ang, &sn, &cs);
+    const float c = static_cast<float>(cs), s = static_cast<float>(sn);
+    if (d < half)
+      o = y * c - y_s[d + half] * s;
+    else
+      o = y * c + y_s[d - half] * s;
+  }
+  out[static_cast<long long>(b) * hd + d] = o;
+}
+
+// --------------------------------------------------------- expand blocks ----
+// Selected block ids -> ascending token positions for the gather.
+constexpr int kExpandThreads = 256;
+
+__global__ void __launch_bounds__(kExpandThreads) expand_blocks_kernel(const int32_t *blocks, int n_blocks,
+                                                                       int ratio, int32_t *positions) {
+  extern __shared__ int32_t ids[];
+  const int t = blockIdx.x;
+  int m = 1;
+  while (m < n_blocks) m <<= 1;
+  for (int i = threadIdx.x; i < m; i += kExpandThreads) {
+    int32_t v = INT_MAX;
+    if (i < n_blocks) {
+      const int32_t b = blocks[static_cast<long long>(t) * n_blocks + i];
+      if (b >= 0) v = b;
+    }
+    ids[i] = v;
+  }
+  __syncthreads();
+  for (int size = 2; size <= m; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < (m >> 1); i += kExpandThreads) {
+        const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+        const bool asc = (lo & size) == 0;
+        const int32_t a = ids[lo], c = ids[hi];
+        if ((a > c) == asc) {
+          ids[lo] = c;
+          ids[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  const long long n_out = static_cast<long long>(n_blocks) * ratio;
+  for (long long i = threadIdx.x; i < n_out; i += kExpandThreads) {
+    const int32_t b = ids[i / ratio];
+    positions[static_cast<long long>(t) * n_out + i] =
+        (b == INT_MAX) ? -1 : static_cast<int32_t>(static_cast<long long>(b) * ratio + i % ratio);
+  }
+}
+
+__global__ void valid_lens_kernel(const int32_t *block_lens, int T, int epb, int32_t *valid_lens) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < T) valid_lens[t] = block_lens[t] * epb;
+}
+
+}  // namespace
+
+cudaError_t launch_gather_kv(const idx_gather_kv_args &a, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(a.T) * a.n_sel;
+  if (rows == 0) return cudaSuccess;
+  const long long grid = (rows + kGatherWarps - 1) / kGatherWarps;
+  gather_kv_kernel<<<static_cast<unsigned>(grid), kGatherWarps * 32, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_block_pool(const uint16_t *raw, const float *w, float *out, uint32_t first_block,
+                              uint32_t n_new, uint32_t ratio, uint32_t hd, uint32_t rot, float theta,
+                              float eps, cudaStream_t stream) {
+  const size_t smem = (static_cast<size_t>(hd) + 32) * sizeof(float);
+  block_pool_kernel<<<n_new, hd, smem, stream>>>(raw, w, out, first_block, ratio, hd, rot, theta, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expand_blocks(const int32_t *blocks, int T, int n_blocks, int ratio,
+                                 int32_t *positions, cudaStream_t stream) {
+  if (T == 0 || n_blocks == 0) return cudaSuccess;
+  int m = 1;
+  while (m < n_blocks) m <<= 1;
+  expand_blocks_kernel<<<T, kExpandThreads, static_cast<size_t>(m) * 4, stream>>>(blocks, n_blocks, ratio,
+                                                                                  positions);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_valid_lens(const int32_t *block_lens, int T, int epb, int32_t *valid_lens,
+                              cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  valid_lens_kernel<<<(T + 255) / 256, 256, 0, stream>>>(block_lens, T, epb, valid_lens);
+  return cudaGetLastError();
+}
+
+}  // namespace idx

@@ -1,0 +1,613 @@
+// score_tc.cu — tensor-core (tcgen05) lightning-indexer scorer with fused
+// per-segment top-k.
+//
+// What it computes: eq. 16 of "indexer_score_topk.cu" (nvfp4-megamoe-kernel,
+// dsv4/kernels/indexer), I[t,s] = sum_h w[t,h] * ReLU(q[t,h] . K[s]), over NVFP4
+// keys resolved through the block table, then the k best keys of every
+// segment (see below); the merge kernel in topk.cu finishes TopK(I[t,:], k).
+// That page's kernel runs one CTA per query with scalar FP32 dot products and
+// a locked shared heap; this one is a persistent, warp-specialised tcgen05
+// pipeline:
+//
+//   work     The tiles of 128 consecutive keys of every query, laid end to end,
+//            are split evenly over the CTAs (one per SM). A "segment" is a
+//            CTA's run of tiles of one query; each segment hands its top-k
+//            candidates to the merge.
+//   warp 0   producer: resolves each tile's blocks through the table and
+//            streams their packed E2M1 nibbles (2-D TMA, 64-byte swizzle) and
+//            E4M3 scales (1-D bulk copy) into a ring of shared-memory stages.
+//   warps 2-5 decoders: one thread per key row decodes 128 elements
+//            e2m1 * e4m3 exactly into f16 (hardware converts) and stores them
+//            to tensor memory as the MMA's A operand. At each segment start
+//            they also turn q[t] into the B operand: per head a power-of-two
+//            scale 2^sigma, then f16 hi and lo parts (the lo part only feeds
+//            the MMA when some q value is not exact in f16, e.g. bf16-valued q
+//            never needs it).
+//   warp 1   MMA issuer: D[128 keys x Npad heads] = A * B^T in f32, K = 128, as
+//            8 (or 16 with the lo part) tcgen05.mma kind::f16 steps.
+//   warps 6-9 epilogue: one thread per key reads its accumulator row from
+//            tensor memory and forms I = g * sum_h (w_h 2^-sigma_h) relu(acc_h)
+//            (the per-block global scale g is factored out, so relu(g a) = g
+//            relu(a) for g > 0 and g min(a,0) for g < 0), then feeds a
+//            streaming top-k (common.cuh).
+//
+// Products e2m1 * e4m3 are exact in f16, and bf16-valued q is exact in the
+// scaled f16 hi part, so a single MMA pass computes the dot products with f32
+// accumulation only; full-precision f32 q takes the second (lo) pass.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace idx {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kTileKeys = 128;
+constexpr int kNS = 6;                   // raw stages
+constexpr int kR = 16;                   // metadata ring
+constexpr uint32_t kStageBytes = 9216;   // 128 x 64 B nibbles + 128 x 8 B scales
+constexpr uint32_t kScaleOff = 8192;
+constexpr int kMaxBlocksPerTile = 8;     // epb >= 16
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kEpiBar = 1, kEpiVoteBar = 2;
+
+struct MetaEntry {
+  float g[kMaxBlocksPerTile];
+  uint32_t mask;  // bit b: block b of the tile resolved to a valid physical block
+  int lb0;        // first logical block of the tile
+  int pad_[6];
+};
+static_assert(sizeof(MetaEntry) == 64, "meta entry");
+
+struct TcLayout {
+  int Npad, nseg, nd, cap, box_rows;
+  uint32_t off_b, b_bytes, off_raw, off_w, off_flags, off_meta, off_bar, off_misc, off_tsh, off_tbuf;
+  uint32_t smem_bytes;
+};
+
+// barrier indices (uint64 slots from off_bar)
+constexpr int B_FULL_RAW = 0, B_EMPTY_RAW = kNS, B_FULL_A = 2 * kNS, B_EMPTY_A = 2 * kNS + 2,
+              B_FULL_D = 2 * kNS + 4, B_EMPTY_D = 2 * kNS + 6, B_META_FULL = 2 * kNS + 8,
+              B_META_EMPTY = 2 * kNS + 8 + kR, B_SEG_FULL = 2 * kNS + 8 + 2 * kR,
+              B_SEG_BFREE = B_SEG_FULL + 2, B_SEG_WFREE = B_SEG_FULL + 4, B_COUNT = B_SEG_FULL + 6;
+
+// misc ints
+constexpr int M_TMEM = 0, M_ABORT = 1, M_T0 = 2, M_J0 = 3, M_SCAN = 8;  // scan: 10 longs
+
+__host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+__device__ __forceinline__ int ntiles_of(const ScoreParams &p, int t) {
+  const int L = p.valid_lens[t];
+  if (L <= 0 || static_cast<long long>(L) > static_cast<long long>(p.max_lb) * p.epb) return 0;
+  return (L + kTileKeys - 1) / kTileKeys;
+}
+
+// Deterministic walk over a CTA's tiles; every role runs its own copy.
+struct Walker {
+  int t, j, nt;
+  __device__ void init(const ScoreParams &p, int t0, int j0) {
+    t = t0;
+    j = j0;
+    nt = (t0 < p.T) ? ntiles_of(p, t0) : 0;
+  }
+  __device__ void next(const ScoreParams &p) {
+    if (++j == nt) {
+      j = 0;
+      do {
+        ++t;
+      } while (t < p.T && (nt = ntiles_of(p, t)) == 0);
+    }
+  }
+};
+
+// Block-wide inclusive scan of one long long per thread (all kThreads threads).
+__device__ long long block_incl_scan(long long v, long long *scratch, long long *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  long long before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const long long s = scratch[w];
+    if (w < warp) before += s;
+    all += s;
+  }
+  __syncthreads();
+  *total = all;
+  return before + x;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    score_tc_kernel(const __grid_constant__ CUtensorMap tmap_nib, ScoreParams p, TcLayout lay,
+                    int32_t *__restrict__ seg_first, int32_t *__restrict__ seg_last,
+                    int32_t *__restrict__ cand_count, uint64_t *__restrict__ cand) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + lay.off_bar);
+  int *misc = reinterpret_cast<int *>(sm + lay.off_misc);
+  volatile int *abort_flag = misc + M_ABORT;
+  auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      ptx::mbar_init(bar(B_FULL_RAW + s), 1);
+      ptx::mbar_init(bar(B_EMPTY_RAW + s), 4);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(bar(B_FULL_A + a), 4);
+      ptx::mbar_init(bar(B_EMPTY_A + a), 1);
+      ptx::mbar_init(bar(B_FULL_D + a), 1);
+      ptx::mbar_init(bar(B_EMPTY_D + a), 4);
+      ptx::mbar_init(bar(B_SEG_FULL + a), 4);
+      ptx::mbar_init(bar(B_SEG_BFREE + a), 1);
+      ptx::mbar_init(bar(B_SEG_WFREE + a), 1);
+    }
+    for (int r = 0; r < kR; ++r) {
+      ptx::mbar_init(bar(B_META_FULL + r), 1);
+      ptx::mbar_init(bar(B_META_EMPTY + r), 4);
+    }
+    misc[M_ABORT] = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) ptx::tmem_alloc(ptx::smem_addr(misc + M_TMEM), 512);
+
+  // ---- work partition: tiles [g0, g1) of the concatenated tile list ----
+  long long *scan = reinterpret_cast<long long *>(misc + M_SCAN);
+  long long total = 0;
+  {
+    long long local = 0;
+    for (int t = threadIdx.x; t < p.T; t += kThreads) local += ntiles_of(p, t);
+    long long tot;
+    block_incl_scan(local, scan, &tot);
+    total = tot;
+  }
+  const long long G = gridDim.x, c = blockIdx.x;
+  const long long qg = total / G, rg = total % G;
+  const long long g0 = c * qg + (c * rg) / G;
+  const long long g1 = (c + 1) * qg + ((c + 1) * rg) / G;
+  if (threadIdx.x == 0) {
+    misc[M_T0] = p.T;
+    misc[M_J0] = 0;
+  }
+  __syncthreads();
+  {
+    long long base = 0;
+    for (int chunk = 0; chunk < p.T; chunk += kThreads) {
+      const int t = chunk + threadIdx.x;
+      const long long v = (t < p.T) ? ntiles_of(p, t) : 0;
+      long long tot;
+      const long long incl = block_incl_scan(v, scan, &tot);
+      const long long excl = incl - v;
+      if (v > 0 && base + excl <= g0 && g0 < base + incl) {
+        misc[M_T0] = t;
+        misc[M_J0] = static_cast<int>(g0 - (base + excl));
+      }
+      base += tot;
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = static_cast<uint32_t>(misc[M_TMEM]);
+  const int t0 = misc[M_T0], j0 = misc[M_J0];
+  const long long n_tiles = (g0 < g1) ? (g1 - g0) : 0;
+  const int Npad = lay.Npad, nseg = lay.nseg, nd = lay.nd;
+  const uint32_t b_bytes = lay.b_bytes;
+  uint8_t *sB = sm + lay.off_b;
+  uint8_t *sRaw = sm + lay.off_raw;
+  float *sW = reinterpret_cast<float *>(sm + lay.off_w);
+  int *sFlags = reinterpret_cast<int *>(sm + lay.off_flags);
+  MetaEntry *sMeta = reinterpret_cast<MetaEntry *>(sm + lay.off_meta);
+  const uint32_t tmem_a = tmem;              // A slots: columns 0, 64
+  const uint32_t tmem_d = tmem + 128;        // D slots: columns 128, 128 + Npad
+
+  if (warp == 0) {
+    // ================================================================ producer
+    if (lane == 0) {
+      Walker w;
+      w.init(p, t0, j0);
+      long long issued = 0;
+      for (long long i = 0; i < n_tiles; ++i, w.next(p)) {
+        const int s = static_cast<int>(i % kNS);
+        const uint32_t u = static_cast<uint32_t>(i / kNS);
+        if (!ptx::mbar_wait(bar(B_EMPTY_RAW + s), (u & 1u) ^ 1u, abort_flag, kTimeoutNs)) break;
+        const int r = static_cast<int>(i % kR);
+        if (!ptx::mbar_wait(bar(B_META_EMPTY + r), (static_cast<uint32_t>(i / kR) & 1u) ^ 1u, abort_flag,
+                            kTimeoutNs))
+          break;
+        const int L = p.valid_lens[w.t];
+        const int s0 = w.j * kTileKeys;
+        const int s_end = min(s0 + kTileKeys, L);
+        const int lb0 = s0 / p.epb, lb1 = (s_end - 1) / p.epb;
+        MetaEntry &m = sMeta[r];
+        int phys_of[kMaxBlocksPerTile];
+        uint32_t mask = 0, bytes = 0;
+        for (int lb = lb0; lb <= lb1; ++lb) {
+          const int b = lb - lb0;
+          const int phys = p.block_table[static_cast<long long>(w.t) * p.bt_stride + lb];
+          phys_of[b] = phys;
+          if (phys < 0 || phys >= p.P) {
+            m.g[b] = 0.0f;
+            if (p.dev_status) atomicOr(p.dev_status, IDX_STATUS_BAD_BLOCK);
+            continue;
+          }
+          mask |= 1u << b;
+          m.g[b] = p.key_gscale[phys];
+          const int blk0 = lb * p.epb;
+          const int lo = max(s0, blk0), hi = min(s0 + kTileKeys, blk0 + p.epb);
+          bytes += static_cast<uint32_t>(hi - lo) * 72u;
+        }
+        m.mask = mask;
+        m.lb0 = lb0;
+        ptx::mbar_arrive(bar(B_META_FULL + r));
+        const uint32_t full = bar(B_FULL_RAW + s);
+        uint8_t *stage = sRaw + static_cast<size_t>(s) * kStageBytes;
+        if (bytes == 0) {
+          ptx::mbar_arrive(full);
+        } else {
+          ptx::mbar_arrive_expect_tx(full, bytes);
+          for (int lb = lb0; lb <= lb1; ++lb) {
+            const int b = lb - lb0;
+            if (!((mask >> b) & 1u)) continue;
+            const int blk0 = lb * p.epb;
+            const int lo = max(s0, blk0), hi = min(s0 + kTileKeys, blk0 + p.epb);
+            const long long row0 = static_cast<long long>(phys_of[b]) * p.epb + (lo - blk0);
+            const int dst_row = lo - s0;
+            for (int rr = 0; rr < hi - lo; rr += lay.box_rows) {
+              const uint32_t dst = ptx::smem_addr(stage + (dst_row + rr) * 64);
+              asm volatile(
+                  "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                  " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+                  "l"(reinterpret_cast<uint64_t>(&tmap_nib)), "r"(0), "r"(static_cast<int>(row0 + rr)),
+                  "r"(full)
+                  : "memory");
+            }
+            ptx::bulk_g2s(ptx::smem_addr(stage + kScaleOff + dst_row * 8), p.key_scale + row0 * 8,
+                          static_cast<uint32_t>(hi - lo) * 8u, full);
+          }
+        }
+        ++issued;
+      }
+      // never leave with copies in flight
+      for (long long i = (issued > kNS ? issued - kNS : 0); i < issued; ++i) {
+        volatile int no_abort = 0;
+        ptx::mbar_wait(bar(B_FULL_RAW + static_cast<int>(i % kNS)), static_cast<uint32_t>(i / kNS) & 1u,
+                       &no_abort, kTimeoutNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      Walker w;
+      w.init(p, t0, j0);
+      const uint32_t idesc = ptx::idesc_f16_f32(128, Npad);
+      int seg = -1, ss = 0;
+      bool need_lo = false;
+      for (long long i = 0; i < n_tiles; ++i, w.next(p)) {
+        const bool seg_start = (i == 0) || (w.j == 0);
+        const bool seg_end = (i == n_tiles - 1) || (w.j == w.nt - 1);
+        if (seg_start) {
+          ++seg;
+          ss = seg % nseg;
+          if (!ptx::mbar_wait(bar(B_SEG_FULL + ss), static_cast<uint32_t>(seg / nseg) & 1u, abort_flag,
+                              kTimeoutNs))
+            break;
+          need_lo = (sFlags[ss * 4 + 0] | sFlags[ss * 4 + 1] | sFlags[ss * 4 + 2] | sFlags[ss * 4 + 3]) != 0;
+        }
+        const int a = static_cast<int>(i & 1);
+        if (!ptx::mbar_wait(bar(B_FULL_A + a), static_cast<uint32_t>(i >> 1) & 1u, abort_flag, kTimeoutNs))
+          break;
+        const int d = static_cast<int>(i % nd);
+        if (!ptx::mbar_wait(bar(B_EMPTY_D + d), (static_cast<uint32_t>(i / nd) & 1u) ^ 1u, abort_flag,
+                            kTimeoutNs))
+          break;
+        ptx::tc_fence_after();
+        const uint32_t dt = tmem_d + d * Npad, at = tmem_a + a * 64;
+        const uint32_t bh = ptx::smem_addr(sB + (ss * 2 + 0) * b_bytes);
+        const uint32_t bl = ptx::smem_addr(sB + (ss * 2 + 1) * b_bytes);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t boff = (k >> 2) * (Npad * 128) + (k & 3) * 32;
+          ptx::mma_ts_f16(dt, at + 8 * k, ptx::sdesc_sw128(bh + boff), idesc, k > 0 ? 1u : 0u);
+        }
+        if (need_lo) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t boff = (k >> 2) * (Npad * 128) + (k & 3) * 32;
+            ptx::mma_ts_f16(dt, at + 8 * k, ptx::sdesc_sw128(bl + boff), idesc, 1u);
+          }
+        }
+        ptx::mma_commit(bar(B_EMPTY_A + a));
+        ptx::mma_commit(bar(B_FULL_D + d));
+        if (seg_end) ptx::mma_commit(bar(B_SEG_BFREE + ss));
+      }
+    }
+  } else if (warp < 6) {
+    // ============================================================== decoders
+    const int dw = warp - 2;                   // 0..3: which heads this warp converts
+    const int row = 32 * (warp & 3) + lane;    // the TMEM lane this thread may write
+    const int rsw = (row >> 1) & 3;            // 64-byte swizzle of this row's chunks
+    Walker w;
+    w.init(p, t0, j0);
+    int seg = -1;
+    for (long long i = 0; i < n_tiles; ++i, w.next(p)) {
+      const bool seg_start = (i == 0) || (w.j == 0);
+      if (seg_start) {
+        ++seg;
+        const int ss = seg % nseg;
+        if (seg >= nseg) {
+          const uint32_t ph = static_cast<uint32_t>(seg / nseg - 1) & 1u;
+          bool ok = ptx::mbar_wait(bar(B_SEG_BFREE + ss), ph, abort_flag, kTimeoutNs);
+          ok = ok && ptx::mbar_wait(bar(B_SEG_WFREE + ss), ph, abort_flag, kTimeoutNs);
+          if (!__all_sync(0xFFFFFFFFu, ok)) break;  // warp-uniform exit before any .aligned op
+        }
+        // q[t] -> B operand (f16 hi / lo, 128-byte swizzled, K-major) and w' = w 2^-sigma
+        uint8_t *bh = sB + (ss * 2 + 0) * b_bytes;
+        uint8_t *bl = sB + (ss * 2 + 1) * b_bytes;
+        bool any_lo = false;
+        for (int h = dw; h < Npad; h += 4) {
+          float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (h < p.H)
+            x = reinterpret_cast<const float4 *>(p.q + (static_cast<long long>(w.t) * p.H + h) * 128)[lane];
+          float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+          const int sigma = (amax > 0.0f) ? 14 - ilogbf(amax) : 0;
+          const float xs[4] = {ldexpf(x.x, sigma), ldexpf(x.y, sigma), ldexpf(x.z, sigma), ldexpf(x.w, sigma)};
+          __half hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi[e] = __float2half_rn(xs[e]);
+            lo[e] = __float2half_rn(xs[e] - __half2float(hi[e]));
+            any_lo |= (__half2float(lo[e]) != 0.0f);
+          }
+          const int ch = lane >> 1, kb = ch >> 3, jj = ch & 7;
+          const uint32_t off = kb * (Npad * 128) + h * 128 + ((jj ^ (h & 7)) * 16) + (lane & 1) * 8;
+          uint2 vh, vl;
+          vh.x = static_cast<uint32_t>(__half_as_ushort(hi[0])) | (static_cast<uint32_t>(__half_as_ushort(hi[1])) << 16);
+          vh.y = static_cast<uint32_t>(__half_as_ushort(hi[2])) | (static_cast<uint32_t>(__half_as_ushort(hi[3])) << 16);
+          vl.x = static_cast<uint32_t>(__half_as_ushort(lo[0])) | (static_cast<uint32_t>(__half_as_ushort(lo[1])) << 16);
+          vl.y = static_cast<uint32_t>(__half_as_ushort(lo[2])) | (static_cast<uint32_t>(__half_as_ushort(lo[3])) << 16);
+          *reinterpret_cast<uint2 *>(bh + off) = vh;
+          *reinterpret_cast<uint2 *>(bl + off) = vl;
+          if (lane == 0) sW[ss * 256 + h] = (h < p.H) ? ldexpf(p.w[static_cast<long long>(w.t) * p.H + h], -sigma) : 0.0f;
+        }
+        const bool warp_lo = __any_sync(0xFFFFFFFFu, any_lo);
+        if (lane == 0) sFlags[ss * 4 + dw] = warp_lo ? 1 : 0;
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(B_SEG_FULL + ss));
+      }
+      const int s = static_cast<int>(i % kNS);
+      const int a = static_cast<int>(i & 1);
+      bool ok = ptx::mbar_wait(bar(B_FULL_RAW + s), static_cast<uint32_t>(i / kNS) & 1u, abort_flag, kTimeoutNs);
+      ok = ok && ptx::mbar_wait(bar(B_EMPTY_A + a), (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u, abort_flag,
+                                kTimeoutNs);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      ptx::tc_fence_after();
+      const uint8_t *stage = sRaw + static_cast<size_t>(s) * kStageBytes;
+      const uint2 scw = *reinterpret_cast<const uint2 *>(stage + kScaleOff + row * 8);
+      const uint32_t taddr = tmem_a + a * 64 + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = half * 2 + cc;  // 16-byte chunk: elements 32c .. 32c+31, groups 2c, 2c+1
+          const uint4 raw = *reinterpret_cast<const uint4 *>(stage + row * 64 + ((c ^ rsw) * 16));
+          const uint32_t sc2 = ptx::e4m3x2_to_f16x2(((c < 2 ? scw.x : scw.y) >> (16 * (c & 1))) & 0xFFFFu);
+          const uint32_t s_lo = __byte_perm(sc2, 0, 0x1010), s_hi = __byte_perm(sc2, 0, 0x3232);
+          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t e[4];
+            ptx::e2m1x8_to_f16x2x4(wv[q4], e);
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb) v[cc * 16 + q4 * 4 + bb] = ptx::hmul2(e[bb], q4 < 2 ? s_lo : s_hi);
+          }
+        }
+        ptx::tmem_st32(taddr + half * 32, v);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(bar(B_FULL_A + a));
+        ptx::mbar_arrive(bar(B_EMPTY_RAW + s));
+      }
+    }
+  } else {
+    // ============================================================== epilogue
+    const int et = threadIdx.x - 192;          // 0..127: index in the top-k group
+    const int row = 32 * (warp & 3) + lane;    // the TMEM lane (key row) this thread reads
+    TopkGroup<128> tk{reinterpret_cast<TopkShared *>(sm + lay.off_tsh),
+                      reinterpret_cast<uint64_t *>(sm + lay.off_tbuf), lay.cap, et, kEpiBar};
+    tk.reset();
+    Walker w;
+    w.init(p, t0, j0);
+    int seg = -1, ss = 0, L = 0;
+    const int k = p.top_k;
+    for (long long i = 0; i < n_tiles; ++i, w.next(p)) {
+      const bool seg_start = (i == 0) || (w.j == 0);
+      const bool seg_end = (i == n_tiles - 1) || (w.j == w.nt - 1);
+      bool ok = true;
+      if (seg_start) {
+        ++seg;
+        ss = seg % nseg;
+        L = p.valid_lens[w.t];
+        ok = ptx::mbar_wait(bar(B_SEG_FULL + ss), static_cast<uint32_t>(seg / nseg) & 1u, abort_flag, kTimeoutNs);
+      }
+      const int d = static_cast<int>(i % nd);
+      const int r = static_cast<int>(i % kR);
+      ok = ok && ptx::mbar_wait(bar(B_FULL_D + d), static_cast<uint32_t>(i / nd) & 1u, abort_flag, kTimeoutNs);
+      ok = ok && ptx::mbar_wait(bar(B_META_FULL + r), static_cast<uint32_t>(i / kR) & 1u, abort_flag, kTimeoutNs);
+      if (!ptx::bar_and(kEpiVoteBar, 128, ok)) break;
+      ptx::tc_fence_after();
+      if (seg_start && w.j == 0 && et == 0) seg_first[w.t] = w.t + static_cast<int>(blockIdx.x);
+      const int s_key = w.j * kTileKeys + row;
+      const int b = s_key / p.epb - sMeta[r].lb0;
+      const bool in_len = s_key < L;
+      const bool valid = in_len && b < kMaxBlocksPerTile && ((sMeta[r].mask >> b) & 1u);
+      const float g = (b < kMaxBlocksPerTile) ? sMeta[r].g[b] : 0.0f;
+      const float *wv = sW + ss * 256;
+      float sum = 0.0f;
+      const uint32_t taddr = tmem_d + d * Npad + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+      for (int c0 = 0; c0 < Npad; c0 += 32) {
+        uint32_t v[32];
+        __syncwarp();  // the per-row sign branch below must not leave the warp split at this load
+        ptx::tmem_ld32(taddr + c0, v);
+        ptx::tmem_wait_ld();
+        if (g >= 0.0f) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sum = fmaf(wv[c0 + e], fmaxf(__uint_as_float(v[e]), 0.0f), sum);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sum = fmaf(wv[c0 + e], fminf(__uint_as_float(v[e]), 0.0f), sum);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(bar(B_EMPTY_D + d));
+        ptx::mbar_arrive(bar(B_META_EMPTY + r));
+      }
+      const float I = g * sum;
+      if (p.scores_out && in_len)
+        p.scores_out[static_cast<long long>(w.t) * p.ld_scores + s_key] = valid ? __fadd_rn(I, 0.0f) : -INFINITY;
+      tk.offer(pack_key(I, s_key), valid);
+      tk.after_round(k);
+      if (seg_end) {
+        tk.compact(k);
+        const int slot = w.t + static_cast<int>(blockIdx.x);
+        const int n = tk.s->count;
+        for (int x = et; x < n; x += 128) cand[static_cast<long long>(slot) * k + x] = tk.buf[x];
+        if (et == 0) {
+          cand_count[slot] = n;
+          if (w.j == w.nt - 1) seg_last[w.t] = slot;
+        }
+        tk.sync();
+        tk.reset();
+        if (et == 0) ptx::mbar_arrive(bar(B_SEG_WFREE + ss));
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && misc[M_ABORT] && p.dev_status) atomicOr(p.dev_status, IDX_STATUS_TIMEOUT);
+}
+
+// ------------------------------------------------------------------- host --
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+bool make_layout(const ScoreParams &p, TcLayout *out) {
+  TcLayout l{};
+  l.Npad = round_up(p.H, 32);
+  if (l.Npad > 256) return false;
+  l.nseg = (l.Npad <= 128) ? 2 : 1;
+  l.nd = (l.Npad <= 192) ? 2 : 1;
+  int box = 128;
+  while (p.epb % box != 0) box >>= 1;
+  if (box < 16) return false;
+  l.box_rows = box;
+  uint32_t off = 0;
+  l.b_bytes = static_cast<uint32_t>(l.Npad) * 256u;
+  l.off_b = off;
+  off += static_cast<uint32_t>(l.nseg) * 2u * l.b_bytes;
+  l.off_raw = off;
+  off += kNS * kStageBytes;
+  l.off_w = off;
+  off += static_cast<uint32_t>(l.nseg) * 256u * 4u;
+  l.off_flags = off;
+  off += 64;
+  l.off_meta = off;
+  off += kR * sizeof(MetaEntry);
+  l.off_bar = off;
+  off += B_COUNT * 8;
+  off = (off + 15) & ~15u;
+  l.off_misc = off;
+  off += 8 * 4 + 16 * 8;
+  off = (off + 15) & ~15u;
+  l.off_tsh = off;
+  off += (sizeof(TopkShared) + 15) & ~size_t(15);
+  l.off_tbuf = off;
+  int kp = 1;
+  while (kp < p.top_k) kp <<= 1;
+  const int min_cap = (kp > p.top_k + 256 ? kp : p.top_k + 256);
+  const long long room = static_cast<long long>(kSmemLimit) - 1024 - off;
+  long long cap = room / 8;
+  if (cap > 16384) cap = 16384;
+  if (cap < min_cap) return false;
+  l.cap = static_cast<int>(cap);
+  off += static_cast<uint32_t>(cap) * 8u;
+  l.smem_bytes = off + 1024;
+  *out = l;
+  return true;
+}
+
+}  // namespace
+
+bool score_tc_supported(const ScoreParams &p) {
+  TcLayout l;
+  if (static_cast<long long>(p.P) * p.epb >= (1LL << 31)) return false;  // TMA row coordinate is int32
+  return p.D == 128 && p.keys_fp4 != nullptr && make_layout(p, &l) && get_encode() != nullptr;
+}
+
+cudaError_t launch_score_tc(const ScoreParams &p, const TcWorkspace &ws, void *workspace, cudaStream_t stream) {
+  TcLayout lay;
+  if (!make_layout(p, &lay)) return cudaErrorNotSupported;
+  auto encode = get_encode();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(p.P) * static_cast<cuuint64_t>(p.epb)};
+  const cuuint64_t strides[1] = {64};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(lay.box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(p.keys_fp4), dims, strides,
+                       box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(lay.smem_bytes));
+  if (e != cudaSuccess) return e;
+  uint8_t *base = static_cast<uint8_t *>(workspace);
+  score_tc_kernel<<<ws.num_ctas, kThreads, lay.smem_bytes, stream>>>(
+      tmap, p, lay, reinterpret_cast<int32_t *>(base + ws.seg_first), reinterpret_cast<int32_t *>(base + ws.seg_last),
+      reinterpret_cast<int32_t *>(base + ws.cand_count), reinterpret_cast<uint64_t *>(base + ws.cand));
+  return cudaGetLastError();
+}
+
+}  // namespace idx

@@ -1,0 +1,60 @@
+"""Shared helpers of the GPU parity tests (imported only by ``-m gpu`` tests)."""
+
+import numpy as np
+
+import oracle
+from tests.parity import check_query, check_scores_row
+
+
+def ensure_built():
+    from sparse_attention_top_paged_gb300 import _lib, build
+    build.build()
+    return _lib.load_library()
+
+
+def to_device(W):
+    import torch
+    dev = "cuda"
+    d = {
+        "q": torch.from_numpy(np.ascontiguousarray(W.q)).to(dev),
+        "w": torch.from_numpy(np.ascontiguousarray(W.w)).to(dev),
+        "bt": torch.from_numpy(np.ascontiguousarray(W.block_table, dtype=np.int32)).to(dev),
+        "vl": torch.from_numpy(np.ascontiguousarray(W.valid_lens, dtype=np.int32)).to(dev),
+    }
+    if W.keys_f32 is not None:
+        d["keys_f32"] = torch.from_numpy(np.ascontiguousarray(W.keys_f32)).to(dev)
+    else:
+        d["keys_fp4"] = torch.from_numpy(np.ascontiguousarray(W.keys_fp4)).to(dev)
+        d["key_scale"] = torch.from_numpy(np.ascontiguousarray(W.key_scale)).to(dev)
+        d["key_gscale"] = torch.from_numpy(np.ascontiguousarray(W.key_gscale)).to(dev)
+    return d
+
+
+def run_gpu(W, path="auto", *, scores=False, num_ctas=0, dev=None):
+    """One idx_score_topk call through the C ABI; returns numpy results."""
+    import torch
+    import sparse_attention_top_paged_gb300 as idx
+    d = dev if dev is not None else to_device(W)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    so = None
+    if scores:
+        so = torch.full((W.T, W.max_lb * W.epb), float("nan"), dtype=torch.float32, device="cuda")
+    keys = {k: d[k] for k in ("keys_fp4", "key_scale", "key_gscale", "keys_f32") if k in d}
+    gi, gs = idx.score_topk(d["q"], d["w"], d["bt"], d["vl"], W.top_k, entries_per_block=W.epb,
+                            bt_stride=W.bt_stride, scores_out=so, dev_status=st, path=path,
+                            num_ctas=num_ctas, **keys)
+    torch.cuda.synchronize()
+    return (gi.cpu().numpy(), gs.cpu().numpy(), int(st.item()),
+            None if so is None else so.cpu().numpy())
+
+
+def oracle_rows(W, rows=None):
+    return oracle.score_topk_rows(W.q, W.w, W.block_table, W.bt_stride, W.max_lb, W.valid_lens,
+                                  W.epb, rows=rows, **W.oracle_kwargs())
+
+
+def check_against_oracle(W, gi, gs, ref_rows, so=None, label=""):
+    for t, I in ref_rows.items():
+        check_query(I, gi[t], gs[t], W.top_k, where=f"{label} query {t}")
+        if so is not None and I is not None:
+            check_scores_row(I, so[t], where=f"{label} scores row {t}")

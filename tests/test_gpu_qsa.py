@@ -1,0 +1,151 @@
+"""GPU parity of the QSA pieces and the K/V gather against the float64 oracle:
+idx_block_pool, idx_gather_kv (bit-exact), idx_expand_blocks (exact),
+idx_valid_lens_from_blocks (exact), and the QSA workload end to end
+(pool -> score -> top-k -> expand -> gather)."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_attention_top_paged_gb300 import workloads as wl
+from tests.gpu_common import ensure_built
+from tests.parity import check_query
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+POOL_REL_TOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+
+
+def _idx():
+    import sparse_attention_top_paged_gb300 as idx
+    return idx
+
+
+def _pool_gpu(Q, first_block, n_new, out=None):
+    raw = torch.from_numpy(Q.raw_keys_bits.view(np.int16)).cuda()
+    w = torch.from_numpy(Q.k_norm_w).cuda()
+    if out is None:
+        out = torch.full((Q.n_blocks, raw.shape[1]), float("nan"), device="cuda")
+    _idx().block_pool(raw, w, out, first_block, n_new, Q.ratio, Q.rot, Q.theta, Q.eps)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def test_block_pool_all_blocks():
+    Q = wl.qsa()
+    got = _pool_gpu(Q, 0, Q.n_blocks)
+    ref = oracle.block_pool(Q.raw_keys, Q.k_norm_w, 0, Q.n_blocks, Q.ratio, Q.rot, Q.theta, Q.eps)
+    tol = POOL_REL_TOL * np.max(np.abs(ref))
+    assert np.max(np.abs(got - ref)) <= tol
+
+
+def test_block_pool_incremental_rows_only():
+    Q = wl.qsa(seed=7)
+    got = _pool_gpu(Q, 100, 7)
+    ref = oracle.block_pool(Q.raw_keys, Q.k_norm_w, 100, 7, Q.ratio, Q.rot, Q.theta, Q.eps)
+    assert np.max(np.abs(got[100:107] - ref)) <= POOL_REL_TOL * np.max(np.abs(ref))
+    assert np.all(np.isnan(got[:100])) and np.all(np.isnan(got[107:]))
+    got0 = _pool_gpu(Q, 3, 0)                     # n_new == 0 launches nothing
+    assert np.all(np.isnan(got0))
+
+
+def _gather_case(seed=3, T=3, n=200, P=40, bs=16, nkv=4, hd=128):
+    rng = np.random.default_rng(seed)
+    kc = rng.integers(0, 65536, size=(P, bs, nkv, hd), dtype=np.uint16)
+    vc = rng.integers(0, 65536, size=(P, bs, nkv, hd), dtype=np.uint16)
+    max_lb = 12
+    table = np.stack([rng.permutation(P)[:max_lb] for _ in range(T)]).astype(np.int32)
+    sel = rng.integers(0, max_lb * bs, size=(T, n)).astype(np.int32)
+    sel[0, :5] = -1
+    return kc, vc, table, sel, bs, max_lb
+
+
+def _gather_gpu(kc, vc, table, sel, bs, with_v=True):
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k_out, v_out = _idx().gather_kv(torch.from_numpy(sel).cuda(), torch.from_numpy(table).cuda(), bs,
+                                    torch.from_numpy(kc.view(np.int16)).cuda(),
+                                    torch.from_numpy(vc.view(np.int16)).cuda() if with_v else None,
+                                    dev_status=st)
+    torch.cuda.synchronize()
+    return (k_out.cpu().numpy().view(np.uint16),
+            None if v_out is None else v_out.cpu().numpy().view(np.uint16), int(st.item()))
+
+
+def test_gather_bit_exact():
+    kc, vc, table, sel, bs, max_lb = _gather_case()
+    k, v, st = _gather_gpu(kc, vc, table, sel, bs)
+    rk, rv, rst = oracle.gather_kv(sel, table, max_lb, max_lb, bs, kc, vc)
+    assert st == rst == 0
+    assert np.array_equal(k, rk) and np.array_equal(v, rv)
+
+
+def test_gather_bad_rows_and_k_only():
+    kc, vc, table, sel, bs, max_lb = _gather_case(seed=4)
+    sel[1, 7] = max_lb * bs + 3        # logical block past the table
+    table[2, 0] = kc.shape[0] + 1      # physical block out of range
+    sel[2, :4] = [0, 1, 2, 15]         # ... and positions that use it
+    k, v, st = _gather_gpu(kc, vc, table, sel, bs)
+    rk, rv, rst = oracle.gather_kv(sel, table, max_lb, max_lb, bs, kc, vc)
+    assert st == rst == (oracle.STATUS_BAD_SEL | oracle.STATUS_BAD_BLOCK)
+    assert np.array_equal(k, rk) and np.array_equal(v, rv)
+    k2, v2, _ = _gather_gpu(kc, vc, table, sel, bs, with_v=False)
+    assert v2 is None and np.array_equal(k2, rk)
+
+
+def test_expand_blocks_exact():
+    rng = np.random.default_rng(5)
+    blocks = np.stack([rng.permutation(512)[:64] for _ in range(3)]).astype(np.int32)
+    blocks[1, 10:] = -1
+    got = _idx().expand_blocks(torch.from_numpy(blocks).cuda(), 16).cpu().numpy()
+    assert np.array_equal(got, oracle.expand_blocks(blocks, 16))
+
+
+def test_valid_lens_exact():
+    bl = np.array([0, 1, 7, 4096], np.int32)
+    got = _idx().valid_lens_from_blocks(torch.from_numpy(bl).cuda(), 64).cpu().numpy()
+    assert np.array_equal(got, oracle.valid_lens_from_blocks(bl, 64))
+
+
+def test_qsa_end_to_end():
+    """The QSA workload: pool 8192 raw keys in blocks of 16, score the 512
+    block keys with 32 heads (w = 1/sqrt(128)), keep the top 64 blocks,
+    expand to 1024 positions and gather K/V (4 kv heads, 16-token pages)."""
+    Q = wl.qsa()
+    idx = _idx()
+    hd = Q.raw_keys.shape[1]
+    raw = torch.from_numpy(Q.raw_keys_bits.view(np.int16)).cuda()
+    bk = torch.empty((Q.n_blocks, hd), device="cuda")
+    idx.block_pool(raw, torch.from_numpy(Q.k_norm_w).cuda(), bk, 0, Q.n_blocks, Q.ratio, Q.rot, Q.theta, Q.eps)
+    nb = Q.n_blocks
+    q = torch.from_numpy(Q.q[None]).cuda()
+    w = torch.full((1, Q.q.shape[0]), 1.0 / math.sqrt(hd), device="cuda")
+    table = torch.arange(nb // 64, dtype=torch.int32, device="cuda").reshape(1, -1)
+    gi, gs = idx.score_topk(q, w, table, torch.tensor([nb], dtype=torch.int32, device="cuda"), Q.top_k,
+                            entries_per_block=64, keys_f32=bk.reshape(nb // 64, 64, hd))
+    pos = idx.expand_blocks(gi, Q.ratio)
+    kc = torch.from_numpy(Q.k_cache_bits.view(np.int16)).cuda()
+    vc = torch.from_numpy(Q.v_cache_bits.view(np.int16)).cuda()
+    k_out, v_out = idx.gather_kv(pos, torch.from_numpy(Q.page_table).cuda(), Q.block_size, kc, vc)
+    torch.cuda.synchronize()
+
+    ref_keys = oracle.block_pool(Q.raw_keys, Q.k_norm_w, 0, nb, Q.ratio, Q.rot, Q.theta, Q.eps)
+    ref_scores = oracle.qsa_score(Q.q, ref_keys)
+    gi_np, gs_np = gi.cpu().numpy(), gs.cpu().numpy()
+    check_query(ref_scores, gi_np[0], gs_np[0], Q.top_k, where="qsa e2e")
+    pos_np = pos.cpu().numpy()
+    assert np.array_equal(pos_np, oracle.expand_blocks(gi_np, Q.ratio))
+    rk, rv, st = oracle.gather_kv(pos_np, Q.page_table, Q.page_table.shape[1], Q.page_table.shape[1],
+                                  Q.block_size, Q.k_cache_bits, Q.v_cache_bits)
+    assert st == 0
+    assert np.array_equal(k_out.cpu().numpy().view(np.uint16), rk)
+    assert np.array_equal(v_out.cpu().numpy().view(np.uint16), rv)

@@ -1,0 +1,204 @@
+"""GPU parity of idx_score_topk against the float64 oracle (through the C ABI).
+
+Both score paths run: "simt" (CUDA cores, full score rows + row top-k) and
+"tensor" (tcgen05 tensor cores, fused segment top-k + merge). Small cases
+compare every output with the oracle; the full-size workloads compare every
+returned entry of sampled queries, in the launch configuration the benchmark
+times.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_attention_top_paged_gb300 import workloads as wl
+from tests.gpu_common import check_against_oracle, ensure_built, oracle_rows, run_gpu, to_device
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+PATHS = ["simt", "tensor"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("jitter", [0, 2])
+def test_tiny_decode(path, jitter):
+    W = wl.tiny_decode(1000 + jitter, gscale_pow2_jitter=jitter)
+    gi, gs, st, so = run_gpu(W, path, scores=True)
+    rows, ost = oracle_rows(W)
+    assert st == ost == 0
+    check_against_oracle(W, gi, gs, rows, so, f"tiny/{path}")
+
+
+def _small(seed, T=8, lo=1, hi=6000, H=64, k=128, P=1024, max_lb=100, q_bf16=True):
+    rng = np.random.default_rng(seed)
+    vl = rng.integers(lo, hi + 1, size=T)
+    return wl.decode_workload("small", seed, T=T, H=H, valid_lens=vl, max_lb=max_lb, P=P,
+                              top_k=k, q_bf16=q_bf16)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_small_batched(path, seed):
+    W = _small(seed, q_bf16=(seed != 3))
+    gi, gs, st, so = run_gpu(W, path, scores=True)
+    rows, _ = oracle_rows(W)
+    assert st == 0
+    check_against_oracle(W, gi, gs, rows, so, f"small{seed}/{path}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_ragged_lengths(path):
+    k = 200
+    lens = [0, 1, 15, 16, 63, 64, 65, 127, 128, 129, 199, 200, 201, 1000, 2047, 4095]
+    W = wl.decode_workload("ragged", 77, T=len(lens), H=64, valid_lens=lens, max_lb=64, P=1100, top_k=k)
+    gi, gs, st, so = run_gpu(W, path, scores=True)
+    rows, _ = oracle_rows(W)
+    assert st == 0
+    check_against_oracle(W, gi, gs, rows, so, f"ragged/{path}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("k", [1, 4096])
+def test_k_extremes(path, k):
+    W = _small(40 + k, T=4, lo=3000, hi=9000, k=k, max_lb=150, P=700)
+    gi, gs, st, _ = run_gpu(W, path)
+    rows, _ = oracle_rows(W)
+    check_against_oracle(W, gi, gs, rows, None, f"k{k}/{path}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("H", [1, 12, 200, 256])
+def test_head_counts(path, H):
+    W = _small(90 + H, T=3, lo=500, hi=3000, H=H, k=64, max_lb=50, P=200)
+    gi, gs, st, so = run_gpu(W, path, scores=True)
+    rows, _ = oracle_rows(W)
+    check_against_oracle(W, gi, gs, rows, so, f"H{H}/{path}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_shared_table_rows(path):
+    W = wl.prefill(5, rows=96, base=4000, ratio=4, n_blocks=24, top_k=256)
+    gi, gs, st, so = run_gpu(W, path, scores=True)
+    rows, _ = oracle_rows(W)
+    check_against_oracle(W, gi, gs, rows, so, f"shared/{path}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_all_equal_scores_take_lowest_indices(path):
+    W = _small(7, T=3, lo=700, hi=900, k=300, max_lb=20, P=64)
+    W.keys_fp4[:] = 0                      # every key decodes to zero -> every score is exactly 0
+    gi, gs, st, _ = run_gpu(W, path)
+    assert np.array_equal(gi, np.tile(np.arange(300), (3, 1)))
+    assert np.all(gs == 0.0) and not np.any(np.signbit(gs))
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bad_inputs_report_status(path):
+    W = _small(8, T=4, lo=2000, hi=3000, k=64, max_lb=50, P=300)
+    W.block_table[0, 3] = W.P + 5          # query 0 loses keys 192..255
+    W.block_table[1, 0] = -3               # query 1 loses keys 0..63
+    W.valid_lens[2] = W.max_lb * W.epb + 1  # query 2: bad length -> padding
+    W.valid_lens[3] = -1                   # query 3: bad length -> padding
+    gi, gs, st, so = run_gpu(W, path, scores=True)
+    rows, ost = oracle_rows(W)
+    assert st == ost == (oracle.STATUS_BAD_BLOCK | oracle.STATUS_BAD_LEN)
+    for t in (0, 1):
+        check_against_oracle(W, gi, gs, {t: rows[t]}, so, f"bad/{path}")
+    for t in (2, 3):
+        assert np.all(gi[t] == -1) and np.all(np.isneginf(gs[t]))
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_block_permutation_is_bit_exact(path):
+    W = _small(9, T=4, lo=3000, hi=5000, k=100, max_lb=80, P=400)
+    gi0, gs0, _, _ = run_gpu(W, path)
+    pi = np.random.default_rng(1).permutation(W.P)
+    W2 = wl.ScoreWorkload("perm", W.q, W.w, pi[W.block_table].astype(np.int32), W.bt_stride,
+                          W.valid_lens, W.epb, W.top_k)
+    W2.keys_fp4 = np.empty_like(W.keys_fp4); W2.keys_fp4[pi] = W.keys_fp4
+    W2.key_scale = np.empty_like(W.key_scale); W2.key_scale[pi] = W.key_scale
+    W2.key_gscale = np.empty_like(W.key_gscale); W2.key_gscale[pi] = W.key_gscale
+    gi1, gs1, _, _ = run_gpu(W2, path)
+    assert np.array_equal(gi0, gi1) and np.array_equal(gs0.view(np.uint32), gs1.view(np.uint32))
+
+
+def test_paths_agree_on_scores():
+    W = _small(10, T=4, lo=2000, hi=4000, k=128)
+    _, _, _, so_s = run_gpu(W, "simt", scores=True)
+    _, _, _, so_t = run_gpu(W, "tensor", scores=True)
+    rows, _ = oracle_rows(W)
+    for t, I in rows.items():
+        tol = 1e-3 * np.max(np.abs(I))
+        assert np.all(np.abs(so_s[t, :len(I)] - so_t[t, :len(I)]) <= tol)
+
+
+@pytest.mark.parametrize("num_ctas", [1, 7, 300])
+def test_tensor_partition_independent(num_ctas):
+    W = _small(11, T=6, lo=1000, hi=20000, k=256, max_lb=320, P=2000)
+    gi0, gs0, _, _ = run_gpu(W, "tensor")
+    gi1, gs1, _, _ = run_gpu(W, "tensor", num_ctas=num_ctas)
+    assert np.array_equal(gi0, gi1) and np.array_equal(gs0, gs1)
+
+
+def test_repeated_calls_are_identical():
+    W = _small(12, T=5, lo=3000, hi=8000, k=256, max_lb=130, P=700)
+    d = to_device(W)
+    a = run_gpu(W, "auto", dev=d)
+    b = run_gpu(W, "auto", dev=d)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_f32_keys_qsa_scores():
+    """F32 key format (QSA pooled keys) with w = 1/sqrt(hd): qsa_score."""
+    rng = np.random.default_rng(13)
+    nb, hd, nh = 512, 128, 32
+    keys = rng.standard_normal((nb, hd)).astype(np.float32)
+    q = rng.standard_normal((1, nh, hd)).astype(np.float32)
+    w = np.full((1, nh), 1.0 / np.sqrt(hd), np.float32)
+    W = wl.ScoreWorkload("qsa_score", q, w, np.arange(8, dtype=np.int32).reshape(1, 8), 8,
+                         np.array([nb], np.int32), 64, 64, keys_f32=keys.reshape(8, 64, hd))
+    gi, gs, st, so = run_gpu(W, "auto", scores=True)
+    ref = oracle.qsa_score(q[0], keys)
+    from tests.parity import check_query, check_scores_row
+    check_query(ref, gi[0], gs[0], 64, where="qsa")
+    check_scores_row(ref, so[0], where="qsa")
+    import sparse_attention_top_paged_gb300 as idx
+    with pytest.raises(idx.IndexerError):
+        run_gpu(W, "tensor")
+
+
+# ----------------------------------------------- full-size workloads ----
+
+@pytest.mark.parametrize("path", ["tensor", "simt"])
+def test_batched_decode_full(path):
+    W = wl.batched_decode()
+    gi, gs, st, _ = run_gpu(W, path)
+    assert st == 0
+    sample = list(range(0, 64, 4))
+    rows, _ = oracle_rows(W, rows=sample)
+    check_against_oracle(W, gi, gs, rows, None, f"batched/{path}")
+
+
+def test_long_decode_full():
+    W = wl.long_decode()
+    gi, gs, st, _ = run_gpu(W, "auto")
+    assert st == 0
+    rows, _ = oracle_rows(W, rows=[0, 15])
+    check_against_oracle(W, gi, gs, rows, None, "long")
+
+
+def test_prefill_full():
+    W = wl.prefill()
+    gi, gs, st, _ = run_gpu(W, "auto")
+    assert st == 0
+    sample = [0, 1, 2, 1000, 2047, 3000, 4094, 4095]
+    rows, _ = oracle_rows(W, rows=sample)
+    check_against_oracle(W, gi, gs, rows, None, "prefill")
