@@ -205,6 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = static_cast<uint32_t>(misc[M_TMEM]);
   const int t0 = misc[M_T0], j0 = misc[M_J0];
   const long long n_tiles = (g0 < g1) ? (g1 - g0) : 0;
+  // A CTA with no tiles (fewer tiles than CTAs) may sit inside the CTA range of a
+  // query t0 = the query holding tile g0; the merge then reads slot t0 + c, so
+  // record it as empty. No real segment (t, c') can share that slot: t0 - 1 has
+  // no tile at or after g0, and t0 + 1 none before it.
+  if (n_tiles == 0 && threadIdx.x == 0) cand_count[t0 + static_cast<int>(blockIdx.x)] = 0;
   const int Npad = lay.Npad, nseg = lay.nseg, nd = lay.nd;
   const uint32_t b_bytes = lay.b_bytes;
   uint8_t *sB = sm + lay.off_b;

@@ -202,3 +202,21 @@ def test_prefill_full():
     sample = [0, 1, 2, 1000, 2047, 3000, 4094, 4095]
     rows, _ = oracle_rows(W, rows=sample)
     check_against_oracle(W, gi, gs, rows, None, "prefill")
+
+
+def test_tensor_more_ctas_than_tiles():
+    """Fewer 128-key tiles than CTAs: empty CTAs sit inside query ranges."""
+    W = _small(14, T=3, lo=100, hi=300, k=64, max_lb=8, P=40)
+    for g in (152, 400):
+        gi, gs, st, so = run_gpu(W, "tensor", scores=True, num_ctas=g)
+        rows, _ = oracle_rows(W)
+        check_against_oracle(W, gi, gs, rows, so, f"sparse-tiles/{g}")
+
+
+@pytest.mark.parametrize("num_ctas", [0, 5])
+def test_tensor_many_short_queries(num_ctas):
+    """Hundreds of short queries: many segments per CTA cycle both segment slots."""
+    W = _small(15, T=300, lo=0, hi=700, k=32, max_lb=11, P=3400)
+    gi, gs, st, so = run_gpu(W, "tensor", scores=True, num_ctas=num_ctas)
+    rows, _ = oracle_rows(W)
+    check_against_oracle(W, gi, gs, rows, so, f"short/{num_ctas}")
