@@ -143,6 +143,29 @@ idx_status_t idx_score_topk_workspace_size(const idx_score_topk_args *args, size
 idx_status_t idx_score_topk(const idx_score_topk_args *args, idx_stream_t stream);
 
 /*
+ * idx_score_topk_static — idx_score_topk for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this call; it exists for callers that may
+ * not call cudaMalloc (for example an operator plugged into a host runtime
+ * that owns all device memory and offers no allocator, or a serving loop that
+ * must not allocate after start-up). It computes exactly what idx_score_topk
+ * computes, with the same arguments, but ignores `workspace` and
+ * `workspace_bytes`: its scratch is an array of IDX_STATIC_SCRATCH_BYTES
+ * bytes inside the library's own device image, which every GPU that loads
+ * libidx holds until the process exits. It calls no allocator.
+ *   - Returns IDX_ERR_WORKSPACE_TOO_SMALL, without launching, when the
+ *     arguments need more scratch than IDX_STATIC_SCRATCH_BYTES
+ *     (idx_score_topk_workspace_size tells how much they need).
+ *   - The first call on each device (with that device current) looks up the
+ *     array's device address once; make that first call before any stream
+ *     capture.
+ *   - All calls share the one array: calls whose execution overlaps on the
+ *     GPU race. Nothing in the array needs to start at zero.
+ */
+#define IDX_STATIC_SCRATCH_BYTES (8u << 20)
+idx_status_t idx_score_topk_static(const idx_score_topk_args *args, idx_stream_t stream);
+
+/*
  * idx_gather_kv — copy selected rows of a paged K/V cache into a dense tile.
  *
  * "metrale_model_layers/layers/ops/qsa.rs", qsa_gather: slot i of the output

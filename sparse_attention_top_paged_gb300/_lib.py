@@ -19,7 +19,8 @@ STATUS_NAMES = {0: "IDX_OK", 1: "IDX_ERR_INVALID_ARG", 2: "IDX_ERR_UNSUPPORTED",
                 3: "IDX_ERR_WORKSPACE_TOO_SMALL", 4: "IDX_ERR_CUDA"}
 KEYS_NVFP4, KEYS_F32 = 0, 1
 PATHS = {"auto": 0, "tensor": 1, "simt": 2}
-STATUS_BAD_BLOCK, STATUS_BAD_LEN, STATUS_BAD_SEL = 1, 2, 4
+STATUS_BAD_BLOCK, STATUS_BAD_LEN, STATUS_BAD_SEL, STATUS_TIMEOUT = 1, 2, 4, 8
+STATIC_SCRATCH_BYTES = 8 << 20
 
 c_i32, c_i64, c_u32, c_size, c_f32, c_vp = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32,
                                              ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p)
@@ -84,6 +85,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.idx_score_topk_workspace_size.restype = c_i32
         lib.idx_score_topk.argtypes = [P(ScoreTopkArgs), c_vp]
         lib.idx_score_topk.restype = c_i32
+        lib.idx_score_topk_static.argtypes = [P(ScoreTopkArgs), c_vp]
+        lib.idx_score_topk_static.restype = c_i32
         lib.idx_gather_kv.argtypes = [P(GatherKvArgs), c_vp]
         lib.idx_gather_kv.restype = c_i32
         lib.idx_block_pool.argtypes = [c_vp, c_vp, c_vp, c_u32, c_u32, c_u32, c_u32, c_u32, c_f32, c_f32, c_vp]
