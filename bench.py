@@ -72,6 +72,31 @@ def whole_job(pairs_per_rank, steps: int, seconds_per_rank, dist=None, device=No
     return float(n.item()) * steps / float(t.item()), float(t.item())
 
 
+KERNEL_SOURCES = ("score_tc.cu", "tc_ptx.cuh", "common.cuh", "internal.h")
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the sources the scoring kernel is built from."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "sparse_attention_top_paged_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the scoring kernel from the committed ncu
+    summary, or None when those counters were taken on other kernel sources."""
+    tfile = os.path.join(ROOT, "profiles", "score_tc_kernel.traffic.json")
+    if not os.path.exists(tfile):
+        return None
+    rec = json.load(open(tfile))
+    if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    return rec.get("bytes_per_launch")
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -331,10 +356,7 @@ def main():
     kern_s = statistics.mean(kern_ms) / 1e3
     algo_bytes = pairs_step * BYTES_PER_PAIR + W.T * (4 * W.H * W.D + 4 * W.H + 4)
     achieved = algo_bytes / kern_s / 1e9
-    traffic = None
-    tfile = os.path.join(ROOT, "profiles", "score_tc_kernel.traffic.json")
-    if os.path.exists(tfile):
-        traffic = json.load(open(tfile)).get("bytes_per_launch")
+    traffic = recorded_traffic()
 
     if rank == 0:
         clocks = clk.summary()

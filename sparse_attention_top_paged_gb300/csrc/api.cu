@@ -31,10 +31,20 @@ int device_sm_count() {
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-TcWorkspace tc_workspace_layout(int T, int top_k, int num_ctas) {
+bool tc_rows_mode(long long max_len, int top_k) { return max_len < 8LL * top_k; }
+
+TcWorkspace tc_workspace_layout(int T, int top_k, int num_ctas, long long max_len, bool have_scores_out,
+                                long long ld_scores_out) {
   TcWorkspace ws{};
   ws.num_ctas = num_ctas;
   ws.n_slots = T + num_ctas;
+  ws.rows_mode = tc_rows_mode(max_len, top_k);
+  if (ws.rows_mode) {
+    ws.ld = have_scores_out ? ld_scores_out : max_len;
+    ws.scores = 0;
+    ws.total = have_scores_out ? 0 : align256(static_cast<size_t>(T) * static_cast<size_t>(max_len) * 4);
+    return ws;
+  }
   size_t off = 0;
   ws.seg_first = off;
   off = align256(off + static_cast<size_t>(T) * 4);
@@ -138,7 +148,7 @@ idx_status_t resolve(const idx_score_topk_args *a, Resolved *r) {
     int g = a->num_ctas;
     if (g == 0) g = device_sm_count();
     if (g <= 0) return IDX_ERR_CUDA;
-    r->tc = tc_workspace_layout(a->T, a->top_k, g);
+    r->tc = tc_workspace_layout(a->T, a->top_k, g, max_len, a->scores_out != nullptr, a->ld_scores);
     r->ws_bytes = r->tc.total;
   }
   return IDX_OK;
@@ -177,6 +187,15 @@ idx_status_t idx_score_topk(const idx_score_topk_args *args, idx_stream_t stream
     e = launch_score_simt(r.p, args->key_format == IDX_KEYS_F32, scores, r.ld, s);
     if (e == cudaSuccess && timed) e = cudaEventRecord(ev1, s);
     if (e == cudaSuccess) e = launch_topk_rows(r.p, scores, r.ld, s);
+  } else if (r.tc.rows_mode) {
+    ScoreParams q = r.p;
+    if (q.scores_out == nullptr) {
+      q.scores_out = static_cast<float *>(args->workspace);
+      q.ld_scores = r.tc.ld;
+    }
+    e = launch_score_tc(q, r.tc, args->workspace, s);
+    if (e == cudaSuccess && timed) e = cudaEventRecord(ev1, s);
+    if (e == cudaSuccess) e = launch_topk_rows(q, q.scores_out, q.ld_scores, s);
   } else {
     e = launch_score_tc(r.p, r.tc, args->workspace, s);
     if (e == cudaSuccess && timed) e = cudaEventRecord(ev1, s);

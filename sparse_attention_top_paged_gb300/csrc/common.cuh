@@ -116,19 +116,26 @@ struct TopkGroup {
       const int shift = 56 - 8 * pass;
       for (int i = gtid; i < 256; i += NT) s->hist[i] = 0u;
       sync();
-      for (int i0 = gtid - static_cast<int>(lane_id()); i0 < n; i0 += NT) {
-        const int i = i0 + static_cast<int>(lane_id());
-        uint64_t key = 0;
-        bool part = false;
-        if (i < n) {
-          key = buf[i];
-          part = (key & mask) == prefix;
+      // Four keys per thread per step, loaded before any is used, so a group
+      // of a few warps still keeps several shared-memory loads in flight.
+      constexpr int U = 4;
+      for (int i0 = gtid - static_cast<int>(lane_id()); i0 < n; i0 += U * NT) {
+        uint64_t key[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = i0 + u * NT + static_cast<int>(lane_id());
+          key[u] = (i < n) ? buf[i] : 0ull;
         }
-        const uint32_t act = __ballot_sync(0xFFFFFFFFu, part);
-        if (part) {
-          const uint32_t dig = static_cast<uint32_t>(key >> shift) & 255u;
-          const uint32_t peers = __match_any_sync(act, dig);
-          if (static_cast<int>(lane_id()) == __ffs(peers) - 1) atomicAdd(&s->hist[dig], __popc(peers));
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = i0 + u * NT + static_cast<int>(lane_id());
+          const bool part = (i < n) && ((key[u] & mask) == prefix);
+          const uint32_t act = __ballot_sync(0xFFFFFFFFu, part);
+          if (part) {
+            const uint32_t dig = static_cast<uint32_t>(key[u] >> shift) & 255u;
+            const uint32_t peers = __match_any_sync(act, dig);
+            if (static_cast<int>(lane_id()) == __ffs(peers) - 1) atomicAdd(&s->hist[dig], __popc(peers));
+          }
         }
       }
       sync();

@@ -31,12 +31,21 @@ struct ScoreParams {
 };
 
 // Workspace sections of the tensor-core path (byte offsets; 256-aligned).
+// In rows mode the scoring kernel writes every score to a [T, ld] matrix
+// (`scores`, or the caller's scores_out) and the per-row top-k kernel selects;
+// otherwise it keeps per-segment candidates for the merge kernel.
 struct TcWorkspace {
-  size_t seg_first, seg_last, cand_count, cand, total;
+  size_t seg_first, seg_last, cand_count, cand, scores, total;
   int num_ctas, n_slots;
+  bool rows_mode;
+  long long ld;  // row stride of the score matrix in rows mode
 };
 
-TcWorkspace tc_workspace_layout(int T, int top_k, int num_ctas);
+// Rows mode pays when a query keeps a large share of its keys (the streaming
+// select inside the scoring kernel then compacts often): max_len < 8 * top_k.
+bool tc_rows_mode(long long max_len, int top_k);
+TcWorkspace tc_workspace_layout(int T, int top_k, int num_ctas, long long max_len, bool have_scores_out,
+                                long long ld_scores_out);
 
 // score_simt.cu
 cudaError_t launch_score_simt(const ScoreParams &p, bool f32_keys, float *scores, long long ld,
@@ -49,7 +58,7 @@ cudaError_t launch_topk_merge(const ScoreParams &p, const TcWorkspace &ws, void 
 // score_tc.cu
 bool score_tc_supported(const ScoreParams &p);
 cudaError_t launch_score_tc(const ScoreParams &p, const TcWorkspace &ws, void *workspace,
-                            cudaStream_t stream);
+                            cudaStream_t stream);  // rows mode: scores land in p.scores_out
 // gather_pool.cu
 cudaError_t launch_gather_kv(const idx_gather_kv_args &a, cudaStream_t stream);
 cudaError_t launch_block_pool(const uint16_t *raw, const float *w, float *out, uint32_t first_block,

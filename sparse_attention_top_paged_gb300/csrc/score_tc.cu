@@ -13,9 +13,12 @@
 //            are split evenly over the CTAs (one per SM). A "segment" is a
 //            CTA's run of tiles of one query; each segment hands its top-k
 //            candidates to the merge.
-//   warp 0   producer: resolves each tile's blocks through the table and
-//            streams their packed E2M1 nibbles (2-D TMA, 64-byte swizzle) and
-//            E4M3 scales (1-D bulk copy) into a ring of shared-memory stages.
+//   warp 10  resolver: looks up block-table entries and per-block global
+//            scales 32 blocks at a time (one per lane) into a ring of per-tile
+//            records, so no dependent global load sits on the copy path.
+//   warp 0   producer: streams each tile's packed E2M1 nibbles (2-D TMA,
+//            64-byte swizzle) and E4M3 scales (1-D bulk copy) into a ring of
+//            shared-memory stages.
 //   warps 2-5 decoders: one thread per key row decodes 128 elements
 //            e2m1 * e4m3 exactly into f16 (hardware converts) and stores them
 //            to tensor memory as the MMA's A operand. At each segment start
@@ -47,27 +50,33 @@
 namespace idx {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kTileKeys = 128;
 constexpr int kNS = 6;                   // raw stages
-constexpr int kR = 16;                   // metadata ring
+constexpr int kR = 64;                   // metadata ring (tiles)
 constexpr uint32_t kStageBytes = 9216;   // 128 x 64 B nibbles + 128 x 8 B scales
 constexpr uint32_t kScaleOff = 8192;
 constexpr int kMaxBlocksPerTile = 8;     // epb >= 16
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr int kSmemLimit = 227 * 1024;
-constexpr int kEpiBar = 1, kEpiVoteBar = 2;
+constexpr int kEpiBar = 1, kEpiVoteBar = 2;  // top-k group syncs / per-tile vote
 
+// One tile's resolved blocks, written by the resolver warp, read by the
+// producer (physical blocks) and the epilogue (global scales, validity).
 struct MetaEntry {
+  int phys[kMaxBlocksPerTile];
   float g[kMaxBlocksPerTile];
   uint32_t mask;  // bit b: block b of the tile resolved to a valid physical block
   int lb0;        // first logical block of the tile
-  int pad_[6];
+  int s0;         // first key of the tile
+  int nblk;       // blocks the tile touches (up to its last valid key)
+  int pad_[12];
 };
-static_assert(sizeof(MetaEntry) == 64, "meta entry");
+static_assert(sizeof(MetaEntry) == 128, "meta entry");
 
 struct TcLayout {
-  int Npad, nseg, nd, cap, box_rows;
+  int Npad, nseg, nd, cap, box_rows, bpt, trig, epb_shift;
+  int rows_mode;  // write every score to p.scores_out; no in-kernel top-k
   uint32_t off_b, b_bytes, off_raw, off_w, off_flags, off_meta, off_bar, off_misc, off_tsh, off_tbuf;
   uint32_t smem_bytes;
 };
@@ -103,6 +112,21 @@ struct Walker {
       do {
         ++t;
       } while (t < p.T && (nt = ntiles_of(p, t)) == 0);
+    }
+  }
+};
+
+// Slot and phase parity of a ring of mbarrier-guarded buffers, advanced one use
+// at a time (no division in the per-tile loops). Consumers wait on "full" with
+// `phase`; producers wait on "empty" with `phase ^ 1` (a fresh barrier counts
+// as having completed that phase).
+struct Ring {
+  int idx = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++idx == n) {
+      idx = 0;
+      phase ^= 1u;
     }
   }
 };
@@ -157,8 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(B_SEG_WFREE + a), 1);
     }
     for (int r = 0; r < kR; ++r) {
-      ptx::mbar_init(bar(B_META_FULL + r), 1);
-      ptx::mbar_init(bar(B_META_EMPTY + r), 4);
+      ptx::mbar_init(bar(B_META_FULL + r), 1);   // resolver
+      ptx::mbar_init(bar(B_META_EMPTY + r), 4);  // epilogue warps
     }
     misc[M_ABORT] = 0;
     ptx::fence_mbar_init();
@@ -204,12 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[M_TMEM]);
   const int t0 = misc[M_T0], j0 = misc[M_J0];
-  const long long n_tiles = (g0 < g1) ? (g1 - g0) : 0;
+  const int n_tiles = (g0 < g1) ? static_cast<int>(g1 - g0) : 0;
   // A CTA with no tiles (fewer tiles than CTAs) may sit inside the CTA range of a
   // query t0 = the query holding tile g0; the merge then reads slot t0 + c, so
   // record it as empty. No real segment (t, c') can share that slot: t0 - 1 has
   // no tile at or after g0, and t0 + 1 none before it.
-  if (n_tiles == 0 && threadIdx.x == 0) cand_count[t0 + static_cast<int>(blockIdx.x)] = 0;
+  if (n_tiles == 0 && threadIdx.x == 0 && !lay.rows_mode) cand_count[t0 + static_cast<int>(blockIdx.x)] = 0;
   const int Npad = lay.Npad, nseg = lay.nseg, nd = lay.nd;
   const uint32_t b_bytes = lay.b_bytes;
   uint8_t *sB = sm + lay.off_b;
@@ -223,54 +247,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ================================================================ producer
     if (lane == 0) {
-      Walker w;
-      w.init(p, t0, j0);
-      long long issued = 0;
-      for (long long i = 0; i < n_tiles; ++i, w.next(p)) {
-        const int s = static_cast<int>(i % kNS);
-        const uint32_t u = static_cast<uint32_t>(i / kNS);
-        if (!ptx::mbar_wait(bar(B_EMPTY_RAW + s), (u & 1u) ^ 1u, abort_flag, kTimeoutNs)) break;
-        const int r = static_cast<int>(i % kR);
-        if (!ptx::mbar_wait(bar(B_META_EMPTY + r), (static_cast<uint32_t>(i / kR) & 1u) ^ 1u, abort_flag,
-                            kTimeoutNs))
-          break;
-        const int L = p.valid_lens[w.t];
-        const int s0 = w.j * kTileKeys;
-        const int s_end = min(s0 + kTileKeys, L);
-        const int lb0 = s0 / p.epb, lb1 = (s_end - 1) / p.epb;
-        MetaEntry &m = sMeta[r];
-        int phys_of[kMaxBlocksPerTile];
-        uint32_t mask = 0, bytes = 0;
-        for (int lb = lb0; lb <= lb1; ++lb) {
-          const int b = lb - lb0;
-          const int phys = p.block_table[static_cast<long long>(w.t) * p.bt_stride + lb];
-          phys_of[b] = phys;
-          if (phys < 0 || phys >= p.P) {
-            m.g[b] = 0.0f;
-            if (p.dev_status) atomicOr(p.dev_status, IDX_STATUS_BAD_BLOCK);
-            continue;
-          }
-          mask |= 1u << b;
-          m.g[b] = p.key_gscale[phys];
-          const int blk0 = lb * p.epb;
-          const int lo = max(s0, blk0), hi = min(s0 + kTileKeys, blk0 + p.epb);
-          bytes += static_cast<uint32_t>(hi - lo) * 72u;
+      int issued = 0;
+      Ring raw, meta;
+      for (int i = 0; i < n_tiles; ++i, raw.next(kNS), meta.next(kR)) {
+        const int s = raw.idx, r = meta.idx;
+        if (!ptx::mbar_wait(bar(B_EMPTY_RAW + s), raw.phase ^ 1u, abort_flag, kTimeoutNs)) break;
+        if (!ptx::mbar_wait(bar(B_META_FULL + r), meta.phase, abort_flag, kTimeoutNs)) break;
+        const MetaEntry &m = sMeta[r];
+        const uint32_t mask = m.mask;
+        const int s0 = m.s0, lb0 = m.lb0, nblk = m.nblk;
+        uint32_t bytes = 0;
+        for (int b = 0; b < nblk; ++b) {
+          if (!((mask >> b) & 1u)) continue;
+          const int blk0 = (lb0 + b) << lay.epb_shift;
+          bytes += static_cast<uint32_t>(min(s0 + kTileKeys, blk0 + p.epb) - max(s0, blk0)) * 72u;
         }
-        m.mask = mask;
-        m.lb0 = lb0;
-        ptx::mbar_arrive(bar(B_META_FULL + r));
         const uint32_t full = bar(B_FULL_RAW + s);
         uint8_t *stage = sRaw + static_cast<size_t>(s) * kStageBytes;
         if (bytes == 0) {
           ptx::mbar_arrive(full);
         } else {
           ptx::mbar_arrive_expect_tx(full, bytes);
-          for (int lb = lb0; lb <= lb1; ++lb) {
-            const int b = lb - lb0;
+          for (int b = 0; b < nblk; ++b) {
             if (!((mask >> b) & 1u)) continue;
-            const int blk0 = lb * p.epb;
+            const int blk0 = (lb0 + b) << lay.epb_shift;
             const int lo = max(s0, blk0), hi = min(s0 + kTileKeys, blk0 + p.epb);
-            const long long row0 = static_cast<long long>(phys_of[b]) * p.epb + (lo - blk0);
+            const long long row0 = (static_cast<long long>(m.phys[b]) << lay.epb_shift) + (lo - blk0);
             const int dst_row = lo - s0;
             for (int rr = 0; rr < hi - lo; rr += lay.box_rows) {
               const uint32_t dst = ptx::smem_addr(stage + (dst_row + rr) * 64);
@@ -288,58 +290,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++issued;
       }
       // never leave with copies in flight
-      for (long long i = (issued > kNS ? issued - kNS : 0); i < issued; ++i) {
+      for (int i = (issued > kNS ? issued - kNS : 0); i < issued; ++i) {
         volatile int no_abort = 0;
-        ptx::mbar_wait(bar(B_FULL_RAW + static_cast<int>(i % kNS)), static_cast<uint32_t>(i / kNS) & 1u,
-                       &no_abort, kTimeoutNs);
+        ptx::mbar_wait(bar(B_FULL_RAW + i % kNS), static_cast<uint32_t>(i / kNS) & 1u, &no_abort, kTimeoutNs);
       }
     }
   } else if (warp == 1) {
     // ============================================================ MMA issuer
-    if (lane == 0) {
-      Walker w;
-      w.init(p, t0, j0);
-      const uint32_t idesc = ptx::idesc_f16_f32(128, Npad);
-      int seg = -1, ss = 0;
-      bool need_lo = false;
-      for (long long i = 0; i < n_tiles; ++i, w.next(p)) {
-        const bool seg_start = (i == 0) || (w.j == 0);
-        const bool seg_end = (i == n_tiles - 1) || (w.j == w.nt - 1);
-        if (seg_start) {
-          ++seg;
-          ss = seg % nseg;
-          if (!ptx::mbar_wait(bar(B_SEG_FULL + ss), static_cast<uint32_t>(seg / nseg) & 1u, abort_flag,
-                              kTimeoutNs))
-            break;
-          need_lo = (sFlags[ss * 4 + 0] | sFlags[ss * 4 + 1] | sFlags[ss * 4 + 2] | sFlags[ss * 4 + 3]) != 0;
-        }
-        const int a = static_cast<int>(i & 1);
-        if (!ptx::mbar_wait(bar(B_FULL_A + a), static_cast<uint32_t>(i >> 1) & 1u, abort_flag, kTimeoutNs))
-          break;
-        const int d = static_cast<int>(i % nd);
-        if (!ptx::mbar_wait(bar(B_EMPTY_D + d), (static_cast<uint32_t>(i / nd) & 1u) ^ 1u, abort_flag,
-                            kTimeoutNs))
-          break;
-        ptx::tc_fence_after();
-        const uint32_t dt = tmem_d + d * Npad, at = tmem_a + a * 64;
+    // The whole warp walks the tiles in lockstep; one elected lane issues.
+    // Descriptors are built once per segment so the issue loop is nothing
+    // but tcgen05.mma instructions.
+    Walker w;
+    w.init(p, t0, j0);
+    const uint32_t idesc = ptx::idesc_f16_f32(128, Npad);
+    bool need_lo = false;
+    uint64_t bdh[8], bdl[8];
+    Ring ra, rd, rs;
+    rs.idx = -1;  // advanced at each segment start
+    int ss = 0;
+    for (int i = 0; i < n_tiles; ++i, w.next(p), ra.next(2), rd.next(nd)) {
+      const bool seg_start = (i == 0) || (w.j == 0);
+      const bool seg_end = (i == n_tiles - 1) || (w.j == w.nt - 1);
+      bool ok = true;
+      if (seg_start) {
+        if (i > 0) rs.next(nseg); else rs.idx = 0;
+        ss = rs.idx;
+        ok = ptx::mbar_wait(bar(B_SEG_FULL + ss), rs.phase, abort_flag, kTimeoutNs);
+        need_lo = (sFlags[ss * 4 + 0] | sFlags[ss * 4 + 1] | sFlags[ss * 4 + 2] | sFlags[ss * 4 + 3]) != 0;
         const uint32_t bh = ptx::smem_addr(sB + (ss * 2 + 0) * b_bytes);
         const uint32_t bl = ptx::smem_addr(sB + (ss * 2 + 1) * b_bytes);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t boff = (k >> 2) * (Npad * 128) + (k & 3) * 32;
-          ptx::mma_ts_f16(dt, at + 8 * k, ptx::sdesc_sw128(bh + boff), idesc, k > 0 ? 1u : 0u);
+          bdh[k] = ptx::sdesc_sw128(bh + boff);
+          bdl[k] = ptx::sdesc_sw128(bl + boff);
         }
+      }
+      const int a = ra.idx, d = rd.idx;
+      ok = ok && ptx::mbar_wait(bar(B_FULL_A + a), ra.phase, abort_flag, kTimeoutNs);
+      ok = ok && ptx::mbar_wait(bar(B_EMPTY_D + d), rd.phase ^ 1u, abort_flag, kTimeoutNs);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      ptx::tc_fence_after();
+      const uint32_t dt = tmem_d + d * Npad, at = tmem_a + a * 64;
+      if (ptx::elect_one()) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ptx::mma_ts_f16(dt, at + 8 * k, bdh[k], idesc, k > 0 ? 1u : 0u);
         if (need_lo) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t boff = (k >> 2) * (Npad * 128) + (k & 3) * 32;
-            ptx::mma_ts_f16(dt, at + 8 * k, ptx::sdesc_sw128(bl + boff), idesc, 1u);
-          }
+          for (int k = 0; k < 8; ++k) ptx::mma_ts_f16(dt, at + 8 * k, bdl[k], idesc, 1u);
         }
         ptx::mma_commit(bar(B_EMPTY_A + a));
         ptx::mma_commit(bar(B_FULL_D + d));
         if (seg_end) ptx::mma_commit(bar(B_SEG_BFREE + ss));
       }
+      __syncwarp();
     }
   } else if (warp < 6) {
     // ============================================================== decoders
@@ -348,48 +352,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rsw = (row >> 1) & 3;            // 64-byte swizzle of this row's chunks
     Walker w;
     w.init(p, t0, j0);
-    int seg = -1;
-    for (long long i = 0; i < n_tiles; ++i, w.next(p)) {
+    Ring rraw, ra, rs;
+    for (int i = 0; i < n_tiles; ++i, w.next(p), rraw.next(kNS), ra.next(2)) {
       const bool seg_start = (i == 0) || (w.j == 0);
       if (seg_start) {
-        ++seg;
-        const int ss = seg % nseg;
-        if (seg >= nseg) {
-          const uint32_t ph = static_cast<uint32_t>(seg / nseg - 1) & 1u;
-          bool ok = ptx::mbar_wait(bar(B_SEG_BFREE + ss), ph, abort_flag, kTimeoutNs);
-          ok = ok && ptx::mbar_wait(bar(B_SEG_WFREE + ss), ph, abort_flag, kTimeoutNs);
+        if (i > 0) rs.next(nseg);
+        const int ss = rs.idx;
+        {  // the slot's previous segment must be done with its B operand (MMA) and w' (epilogue)
+          bool ok = ptx::mbar_wait(bar(B_SEG_BFREE + ss), rs.phase ^ 1u, abort_flag, kTimeoutNs);
+          ok = ok && ptx::mbar_wait(bar(B_SEG_WFREE + ss), rs.phase ^ 1u, abort_flag, kTimeoutNs);
           if (!__all_sync(0xFFFFFFFFu, ok)) break;  // warp-uniform exit before any .aligned op
         }
         // q[t] -> B operand (f16 hi / lo, 128-byte swizzled, K-major) and w' = w 2^-sigma
         uint8_t *bh = sB + (ss * 2 + 0) * b_bytes;
         uint8_t *bl = sB + (ss * 2 + 1) * b_bytes;
         bool any_lo = false;
-        for (int h = dw; h < Npad; h += 4) {
-          float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (h < p.H)
-            x = reinterpret_cast<const float4 *>(p.q + (static_cast<long long>(w.t) * p.H + h) * 128)[lane];
-          float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+        constexpr int kQChunk = 8;  // heads per chunk: their loads are all in flight at once
+        for (int h0 = dw; h0 < Npad; h0 += 4 * kQChunk) {
+          float4 xq[kQChunk];
+          float wq[kQChunk], down[kQChunk];
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-          const int sigma = (amax > 0.0f) ? 14 - ilogbf(amax) : 0;
-          const float xs[4] = {ldexpf(x.x, sigma), ldexpf(x.y, sigma), ldexpf(x.z, sigma), ldexpf(x.w, sigma)};
-          __half hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            hi[e] = __float2half_rn(xs[e]);
-            lo[e] = __float2half_rn(xs[e] - __half2float(hi[e]));
-            any_lo |= (__half2float(lo[e]) != 0.0f);
+          for (int c = 0; c < kQChunk; ++c) {
+            const int h = h0 + 4 * c;
+            xq[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            wq[c] = 0.0f;
+            if (h < p.H) {
+              xq[c] = reinterpret_cast<const float4 *>(p.q + (static_cast<long long>(w.t) * p.H + h) * 128)[lane];
+              if (lane == 0) wq[c] = p.w[static_cast<long long>(w.t) * p.H + h];
+            }
           }
-          const int ch = lane >> 1, kb = ch >> 3, jj = ch & 7;
-          const uint32_t off = kb * (Npad * 128) + h * 128 + ((jj ^ (h & 7)) * 16) + (lane & 1) * 8;
-          uint2 vh, vl;
-          vh.x = static_cast<uint32_t>(__half_as_ushort(hi[0])) | (static_cast<uint32_t>(__half_as_ushort(hi[1])) << 16);
-          vh.y = static_cast<uint32_t>(__half_as_ushort(hi[2])) | (static_cast<uint32_t>(__half_as_ushort(hi[3])) << 16);
-          vl.x = static_cast<uint32_t>(__half_as_ushort(lo[0])) | (static_cast<uint32_t>(__half_as_ushort(lo[1])) << 16);
-          vl.y = static_cast<uint32_t>(__half_as_ushort(lo[2])) | (static_cast<uint32_t>(__half_as_ushort(lo[3])) << 16);
-          *reinterpret_cast<uint2 *>(bh + off) = vh;
-          *reinterpret_cast<uint2 *>(bl + off) = vl;
-          if (lane == 0) sW[ss * 256 + h] = (h < p.H) ? ldexpf(p.w[static_cast<long long>(w.t) * p.H + h], -sigma) : 0.0f;
+#pragma unroll
+          for (int c = 0; c < kQChunk; ++c) {
+            const int h = h0 + 4 * c;
+            if (h >= Npad) break;
+            const float4 x = xq[c];
+            float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+            // sigma puts the head's largest |q| in [2^14, 2^15): 2^sigma from the
+            // exponent field (amax normal; subnormal or zero heads keep sigma 0),
+            // clamped so 2^sigma and 2^-sigma are both normal floats.
+            const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+            const int sigma = (ex == 0) ? 0 : max(-126, min(126, 141 - ex));
+            const float up = __uint_as_float(static_cast<uint32_t>(127 + sigma) << 23);
+            down[c] = __uint_as_float(static_cast<uint32_t>(127 - sigma) << 23);
+            const float xs[4] = {x.x * up, x.y * up, x.z * up, x.w * up};
+            __half hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              hi[e] = __float2half_rn(xs[e]);
+              lo[e] = __float2half_rn(xs[e] - __half2float(hi[e]));
+              any_lo |= (__half2float(lo[e]) != 0.0f);
+            }
+            const int ch = lane >> 1, kb = ch >> 3, jj = ch & 7;
+            const uint32_t off = kb * (Npad * 128) + h * 128 + ((jj ^ (h & 7)) * 16) + (lane & 1) * 8;
+            uint2 vh, vl;
+            vh.x = static_cast<uint32_t>(__half_as_ushort(hi[0])) | (static_cast<uint32_t>(__half_as_ushort(hi[1])) << 16);
+            vh.y = static_cast<uint32_t>(__half_as_ushort(hi[2])) | (static_cast<uint32_t>(__half_as_ushort(hi[3])) << 16);
+            vl.x = static_cast<uint32_t>(__half_as_ushort(lo[0])) | (static_cast<uint32_t>(__half_as_ushort(lo[1])) << 16);
+            vl.y = static_cast<uint32_t>(__half_as_ushort(lo[2])) | (static_cast<uint32_t>(__half_as_ushort(lo[3])) << 16);
+            *reinterpret_cast<uint2 *>(bh + off) = vh;
+            *reinterpret_cast<uint2 *>(bl + off) = vl;
+            if (lane == 0) sW[ss * 256 + h] = (h < p.H) ? wq[c] * down[c] : 0.0f;
+          }
         }
         const bool warp_lo = __any_sync(0xFFFFFFFFu, any_lo);
         if (lane == 0) sFlags[ss * 4 + dw] = warp_lo ? 1 : 0;
@@ -397,11 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(B_SEG_FULL + ss));
       }
-      const int s = static_cast<int>(i % kNS);
-      const int a = static_cast<int>(i & 1);
-      bool ok = ptx::mbar_wait(bar(B_FULL_RAW + s), static_cast<uint32_t>(i / kNS) & 1u, abort_flag, kTimeoutNs);
-      ok = ok && ptx::mbar_wait(bar(B_EMPTY_A + a), (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u, abort_flag,
-                                kTimeoutNs);
+      const int s = rraw.idx, a = ra.idx;
+      bool ok = ptx::mbar_wait(bar(B_FULL_RAW + s), rraw.phase, abort_flag, kTimeoutNs);
+      ok = ok && ptx::mbar_wait(bar(B_EMPTY_A + a), ra.phase ^ 1u, abort_flag, kTimeoutNs);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       ptx::tc_fence_after();
       const uint8_t *stage = sRaw + static_cast<size_t>(s) * kStageBytes;
@@ -435,6 +458,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar(B_EMPTY_RAW + s));
       }
     }
+  } else if (warp == 10) {
+    // ============================================================== resolver
+    // Resolves block-table entries and global scales for batches of 32 blocks
+    // at once (one per lane), so the two dependent global loads per block
+    // overlap across the batch instead of serialising the TMA producer.
+    const int bpt = lay.bpt;                 // blocks per full tile (epb a power of two)
+    const int tpb = 32 / bpt;                // tiles per batch
+    const int d = lane / bpt, b = lane % bpt;
+    Walker w;
+    w.init(p, t0, j0);
+    int prefetched_t = -1;
+    for (int base = 0; base < n_tiles; base += tpb) {
+      // The decoders turn q[t] into the MMA's B operand at each segment start;
+      // pull the rows of every query this batch reaches into L2 ahead of them.
+      if (lane == 0) {
+        Walker wp = w;
+        for (int x = 0; x < tpb && base + x < n_tiles; ++x, wp.next(p)) {
+          if (wp.t != prefetched_t) {
+            prefetched_t = wp.t;
+            ptx::bulk_prefetch_l2(p.q + static_cast<long long>(wp.t) * p.H * 128, static_cast<uint32_t>(p.H) * 512u);
+          }
+        }
+      }
+      const int i = base + d;
+      const bool tile_ok = i < n_tiles;
+      Walker wl = w;
+      for (int x = 0; x < d && tile_ok; ++x) wl.next(p);
+      int L = 0, s0 = 0, lb0 = 0, nblk = 0, phys = -1;
+      float g = 0.0f;
+      bool blk_ok = false, pv = false;
+      if (tile_ok) {
+        L = p.valid_lens[wl.t];
+        s0 = wl.j * kTileKeys;
+        const int s_end = min(s0 + kTileKeys, L);
+        lb0 = s0 >> lay.epb_shift;
+        nblk = ((s_end - 1) >> lay.epb_shift) - lb0 + 1;
+        blk_ok = b < nblk;
+        if (blk_ok) {
+          phys = p.block_table[static_cast<long long>(wl.t) * p.bt_stride + lb0 + b];
+          pv = phys >= 0 && phys < p.P;
+          if (pv) g = p.key_gscale[phys];
+        }
+      }
+      if (blk_ok && !pv && p.dev_status) atomicOr(p.dev_status, IDX_STATUS_BAD_BLOCK);
+      const uint32_t valid_bits = __ballot_sync(0xFFFFFFFFu, pv);
+      const int r = i & (kR - 1);   // kR is a power of two
+      bool ok = true;
+      if (tile_ok && b == 0)
+        ok = ptx::mbar_wait(bar(B_META_EMPTY + r), (static_cast<uint32_t>(i / kR) & 1u) ^ 1u, abort_flag,
+                            kTimeoutNs);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      MetaEntry &m = sMeta[r];
+      if (blk_ok) {
+        m.phys[b] = phys;
+        m.g[b] = g;
+      }
+      if (tile_ok && b == 0) {
+        m.mask = (valid_bits >> (d * bpt)) & ((bpt == 32) ? 0xFFFFFFFFu : ((1u << bpt) - 1u));
+        m.lb0 = lb0;
+        m.s0 = s0;
+        m.nblk = nblk;
+      }
+      __syncwarp();
+      if (tile_ok && b == 0) ptx::mbar_arrive(bar(B_META_FULL + r));
+      for (int x = 0; x < tpb; ++x) w.next(p);
+    }
   } else {
     // ============================================================== epilogue
     const int et = threadIdx.x - 192;          // 0..127: index in the top-k group
@@ -444,57 +533,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     tk.reset();
     Walker w;
     w.init(p, t0, j0);
-    int seg = -1, ss = 0, L = 0;
+    int ss = 0, L = 0;
     const int k = p.top_k;
-    for (long long i = 0; i < n_tiles; ++i, w.next(p)) {
+    Ring rd, rm, rs;
+    for (int i = 0; i < n_tiles; ++i, w.next(p), rd.next(nd), rm.next(kR)) {
       const bool seg_start = (i == 0) || (w.j == 0);
       const bool seg_end = (i == n_tiles - 1) || (w.j == w.nt - 1);
       bool ok = true;
       if (seg_start) {
-        ++seg;
-        ss = seg % nseg;
+        if (i > 0) rs.next(nseg);
+        ss = rs.idx;
         L = p.valid_lens[w.t];
-        ok = ptx::mbar_wait(bar(B_SEG_FULL + ss), static_cast<uint32_t>(seg / nseg) & 1u, abort_flag, kTimeoutNs);
+        ok = ptx::mbar_wait(bar(B_SEG_FULL + ss), rs.phase, abort_flag, kTimeoutNs);
       }
-      const int d = static_cast<int>(i % nd);
-      const int r = static_cast<int>(i % kR);
-      ok = ok && ptx::mbar_wait(bar(B_FULL_D + d), static_cast<uint32_t>(i / nd) & 1u, abort_flag, kTimeoutNs);
-      ok = ok && ptx::mbar_wait(bar(B_META_FULL + r), static_cast<uint32_t>(i / kR) & 1u, abort_flag, kTimeoutNs);
-      if (!ptx::bar_and(kEpiVoteBar, 128, ok)) break;
-      ptx::tc_fence_after();
-      if (seg_start && w.j == 0 && et == 0) seg_first[w.t] = w.t + static_cast<int>(blockIdx.x);
+      const int d = rd.idx, r = rm.idx;
+      ok = ok && ptx::mbar_wait(bar(B_FULL_D + d), rd.phase, abort_flag, kTimeoutNs);
+      ok = ok && ptx::mbar_wait(bar(B_META_FULL + r), rm.phase, abort_flag, kTimeoutNs);
+      ok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform before the .aligned TMEM loads
+      if (seg_start && w.j == 0 && et == 0 && !lay.rows_mode) seg_first[w.t] = w.t + static_cast<int>(blockIdx.x);
       const int s_key = w.j * kTileKeys + row;
-      const int b = s_key / p.epb - sMeta[r].lb0;
-      const bool in_len = s_key < L;
-      const bool valid = in_len && b < kMaxBlocksPerTile && ((sMeta[r].mask >> b) & 1u);
-      const float g = (b < kMaxBlocksPerTile) ? sMeta[r].g[b] : 0.0f;
-      const float *wv = sW + ss * 256;
-      float sum = 0.0f;
-      const uint32_t taddr = tmem_d + d * Npad + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-      for (int c0 = 0; c0 < Npad; c0 += 32) {
-        uint32_t v[32];
-        __syncwarp();  // the per-row sign branch below must not leave the warp split at this load
-        ptx::tmem_ld32(taddr + c0, v);
-        ptx::tmem_wait_ld();
-        if (g >= 0.0f) {
+      bool valid = false, in_len = false;
+      float I = 0.0f;
+      if (ok) {
+        ptx::tc_fence_after();
+        const int b = (s_key >> lay.epb_shift) - sMeta[r].lb0;
+        in_len = s_key < L;
+        valid = in_len && b < kMaxBlocksPerTile && ((sMeta[r].mask >> b) & 1u);
+        const float g = (b < kMaxBlocksPerTile) ? sMeta[r].g[b] : 0.0f;
+        const uint64_t *wv2 = reinterpret_cast<const uint64_t *>(sW + ss * 256);  // (w'_h, w'_h+1) pairs
+        uint64_t acc2[2] = {0ull, 0ull};                                          // two independent chains
+        const uint32_t taddr = tmem_d + d * Npad + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+        for (int c0 = 0; c0 < Npad; c0 += 64) {
+          uint32_t v[64];
+          __syncwarp();  // the per-row sign branch below must not leave the warp split at these loads
+          ptx::tmem_ld32(taddr + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          if (c0 + 32 < Npad) ptx::tmem_ld32(taddr + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          ptx::tmem_wait_ld();
+          if (c0 + 64 >= Npad) {   // every accumulator column is in registers: hand back the slots
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::mbar_arrive(bar(B_EMPTY_D + d));
+              ptx::mbar_arrive(bar(B_META_EMPTY + r));
+            }
+          }
+          const int ncol = (Npad - c0 < 64) ? (Npad - c0) : 64;
+          if (g >= 0.0f) {          // relu(g a) = g max(a, 0)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) sum = fmaf(wv[c0 + e], fmaxf(__uint_as_float(v[e]), 0.0f), sum);
-        } else {
+            for (int e = 0; e < 64; e += 4) {
+              if (e < ncol) {
+                ptx::ffma2(acc2[0], wv2[(c0 + e) >> 1],
+                           ptx::pack2(fmaxf(__uint_as_float(v[e]), 0.0f), fmaxf(__uint_as_float(v[e + 1]), 0.0f)));
+                ptx::ffma2(acc2[1], wv2[((c0 + e) >> 1) + 1],
+                           ptx::pack2(fmaxf(__uint_as_float(v[e + 2]), 0.0f), fmaxf(__uint_as_float(v[e + 3]), 0.0f)));
+              }
+            }
+          } else {                  // relu(g a) = g min(a, 0)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) sum = fmaf(wv[c0 + e], fminf(__uint_as_float(v[e]), 0.0f), sum);
+            for (int e = 0; e < 64; e += 4) {
+              if (e < ncol) {
+                ptx::ffma2(acc2[0], wv2[(c0 + e) >> 1],
+                           ptx::pack2(fminf(__uint_as_float(v[e]), 0.0f), fminf(__uint_as_float(v[e + 1]), 0.0f)));
+                ptx::ffma2(acc2[1], wv2[((c0 + e) >> 1) + 1],
+                           ptx::pack2(fminf(__uint_as_float(v[e + 2]), 0.0f), fminf(__uint_as_float(v[e + 3]), 0.0f)));
+              }
+            }
+          }
         }
+        const float sum = (__uint_as_float(static_cast<uint32_t>(acc2[0])) + __uint_as_float(static_cast<uint32_t>(acc2[0] >> 32))) +
+                          (__uint_as_float(static_cast<uint32_t>(acc2[1])) + __uint_as_float(static_cast<uint32_t>(acc2[1] >> 32)));
+        I = g * sum;
+        if (p.scores_out && in_len)
+          p.scores_out[static_cast<long long>(w.t) * p.ld_scores + s_key] = valid ? __fadd_rn(I, 0.0f) : -INFINITY;
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(bar(B_EMPTY_D + d));
-        ptx::mbar_arrive(bar(B_META_EMPTY + r));
+      if (lay.rows_mode) {   // scores already written above; the row top-k kernel selects
+        if (!ptx::bar_and(kEpiVoteBar, 128, ok)) break;
+        if (seg_end && et == 0) ptx::mbar_arrive(bar(B_SEG_WFREE + ss));  // w' of this segment is free
+        continue;
       }
-      const float I = g * sum;
-      if (p.scores_out && in_len)
-        p.scores_out[static_cast<long long>(w.t) * p.ld_scores + s_key] = valid ? __fadd_rn(I, 0.0f) : -INFINITY;
       tk.offer(pack_key(I, s_key), valid);
-      tk.after_round(k);
+      if (!ptx::bar_and(kEpiVoteBar, 128, ok)) break;  // ends the offer round for the whole group
+      if (tk.s->count > lay.trig) tk.compact(k);
       if (seg_end) {
         tk.compact(k);
         const int slot = w.t + static_cast<int>(blockIdx.x);
@@ -544,10 +663,11 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   if (l.Npad > 256) return false;
   l.nseg = (l.Npad <= 128) ? 2 : 1;
   l.nd = (l.Npad <= 192) ? 2 : 1;
-  int box = 128;
-  while (p.epb % box != 0) box >>= 1;
-  if (box < 16) return false;
-  l.box_rows = box;
+  if (p.epb < 16 || (p.epb & (p.epb - 1)) != 0) return false;  // power-of-two blocks of >= 16 keys
+  l.box_rows = p.epb < 128 ? p.epb : 128;
+  l.bpt = p.epb < 128 ? 128 / p.epb : 1;
+  l.epb_shift = 0;
+  while ((1 << l.epb_shift) < p.epb) ++l.epb_shift;
   uint32_t off = 0;
   l.b_bytes = static_cast<uint32_t>(l.Npad) * 256u;
   l.off_b = off;
@@ -577,6 +697,12 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   if (cap > 16384) cap = 16384;
   if (cap < min_cap) return false;
   l.cap = static_cast<int>(cap);
+  // Compact early: once k keys are kept the threshold rejects most later keys
+  // at the offer, so the buffer (and each radix select over it) stays small.
+  long long trig = 2LL * kp;
+  if (trig < 1024) trig = 1024;
+  if (trig > cap - 128) trig = cap - 128;
+  l.trig = static_cast<int>(trig);
   off += static_cast<uint32_t>(cap) * 8u;
   l.smem_bytes = off + 1024;
   *out = l;
@@ -594,6 +720,8 @@ bool score_tc_supported(const ScoreParams &p) {
 cudaError_t launch_score_tc(const ScoreParams &p, const TcWorkspace &ws, void *workspace, cudaStream_t stream) {
   TcLayout lay;
   if (!make_layout(p, &lay)) return cudaErrorNotSupported;
+  lay.rows_mode = ws.rows_mode ? 1 : 0;
+  if (lay.rows_mode && p.scores_out == nullptr) return cudaErrorInvalidValue;
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap tmap;

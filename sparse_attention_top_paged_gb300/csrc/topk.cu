@@ -16,6 +16,7 @@ namespace idx {
 namespace {
 
 constexpr int kTopkThreads = 512;
+constexpr int kFlatSegs = kTopkThreads;  // segments per query read in one flat pass
 
 template <bool kMerge>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(ScoreParams p, const float *scores,
@@ -52,9 +53,42 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(ScoreParams p, const
       g.offer(pack_key(v, s), s < L && v != -INFINITY);
       g.after_round(k);
     }
-  } else {
-    if (L > 0) {
-      const int j0 = seg_first[t], j1 = seg_last[t];
+  } else if (L > 0) {
+    // The query's segments are slots j0..j1. With at most kFlatSegs of them,
+    // read every count at once, prefix them in shared memory and stream all
+    // candidates as one flat list (no per-segment round trip to memory).
+    __shared__ int seg_off[kFlatSegs + 1];
+    __shared__ int warp_tot[kTopkThreads / 32];
+    const int j0 = seg_first[t], j1 = seg_last[t];
+    const int nseg = j1 - j0 + 1;
+    if (nseg <= kFlatSegs) {
+      const int j = static_cast<int>(threadIdx.x);
+      int c = (j < nseg) ? cand_count[j0 + j] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, c, o);
+        if (lane_id() >= static_cast<uint32_t>(o)) c += v;
+      }
+      if (lane_id() == 31) warp_tot[threadIdx.x >> 5] = c;
+      __syncthreads();
+      int before = 0;
+      for (int wi = 0; wi < static_cast<int>(threadIdx.x >> 5); ++wi) before += warp_tot[wi];
+      if (j < nseg) seg_off[j + 1] = before + c;
+      if (j == 0) seg_off[0] = 0;
+      __syncthreads();
+      const int total = seg_off[nseg];
+      int js = 0;
+      for (int base = 0; base < total; base += kTopkThreads) {
+        const int i = base + static_cast<int>(threadIdx.x);
+        const bool have = i < total;
+        uint64_t key = 0ull;
+        if (have) {
+          while (seg_off[js + 1] <= i) ++js;   // segment holding flat index i (monotone in i)
+          key = cand[static_cast<long long>(j0 + js) * k + (i - seg_off[js])];
+        }
+        g.offer(key, have);
+        g.after_round(k);
+      }
+    } else {
       for (int j = j0; j <= j1; ++j) {
         const int n = cand_count[j];
         const uint64_t *c = cand + static_cast<long long>(j) * k;

@@ -90,7 +90,7 @@ def test_static_scratch_rejects_oversized_arguments(lib):
     T, k = 1200, 4096                                   # needs > 8 MiB of candidates
     q = torch.zeros((T, 1, 128), dtype=torch.float32, device="cuda")
     w = torch.zeros((T, 1), dtype=torch.float32, device="cuda")
-    bt = torch.zeros((T, 1), dtype=torch.int32, device="cuda")
+    bt = torch.zeros((T, 1024), dtype=torch.int32, device="cuda")   # 65536 keys per row
     vl = torch.zeros(T, dtype=torch.int32, device="cuda")
     fp4 = torch.zeros((1, 64, 64), dtype=torch.uint8, device="cuda")
     sc = torch.zeros((1, 64, 8), dtype=torch.uint8, device="cuda")
