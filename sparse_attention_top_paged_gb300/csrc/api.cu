@@ -31,33 +31,6 @@ int device_sm_count() {
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-bool tc_rows_mode(long long max_len, int top_k) { return max_len < 8LL * top_k; }
-
-TcWorkspace tc_workspace_layout(int T, int top_k, int num_ctas, long long max_len, bool have_scores_out,
-                                long long ld_scores_out) {
-  TcWorkspace ws{};
-  ws.num_ctas = num_ctas;
-  ws.n_slots = T + num_ctas;
-  ws.rows_mode = tc_rows_mode(max_len, top_k);
-  if (ws.rows_mode) {
-    ws.ld = have_scores_out ? ld_scores_out : max_len;
-    ws.scores = 0;
-    ws.total = have_scores_out ? 0 : align256(static_cast<size_t>(T) * static_cast<size_t>(max_len) * 4);
-    return ws;
-  }
-  size_t off = 0;
-  ws.seg_first = off;
-  off = align256(off + static_cast<size_t>(T) * 4);
-  ws.seg_last = off;
-  off = align256(off + static_cast<size_t>(T) * 4);
-  ws.cand_count = off;
-  off = align256(off + static_cast<size_t>(ws.n_slots) * 4);
-  ws.cand = off;
-  off = align256(off + static_cast<size_t>(ws.n_slots) * top_k * 8);
-  ws.total = off;
-  return ws;
-}
-
 }  // namespace idx
 
 using namespace idx;
@@ -72,9 +45,8 @@ struct Resolved {
   Plan plan = Plan::kNone;
   ScoreParams p{};
   size_t ws_bytes = 0;
-  TcWorkspace tc{};
-  bool use_scores_out = false;
-  long long ld = 0;
+  SelectPlan sel{};
+  int num_ctas = 0;
 };
 
 idx_status_t resolve(const idx_score_topk_args *a, Resolved *r) {
@@ -140,17 +112,17 @@ idx_status_t resolve(const idx_score_topk_args *a, Resolved *r) {
     plan = Plan::kSimt;
   }
   r->plan = plan;
-  if (plan == Plan::kSimt) {
-    r->use_scores_out = a->scores_out != nullptr;
-    r->ld = r->use_scores_out ? a->ld_scores : max_len;
-    r->ws_bytes = r->use_scores_out ? 0 : align256(static_cast<size_t>(a->T) * max_len * 4);
-  } else {
+  if (plan == Plan::kTensor) {
     int g = a->num_ctas;
     if (g == 0) g = device_sm_count();
     if (g <= 0) return IDX_ERR_CUDA;
-    r->tc = tc_workspace_layout(a->T, a->top_k, g, max_len, a->scores_out != nullptr, a->ld_scores);
-    r->ws_bytes = r->tc.total;
+    r->num_ctas = g;
   }
+  // Both paths write I[t, s] to a [T, ld] matrix (the caller's scores_out, or
+  // the workspace), then select from it.
+  if (!select_supported(a->top_k, max_len)) return IDX_ERR_UNSUPPORTED;
+  r->sel = select_plan(a->T, a->top_k, max_len, a->scores_out != nullptr, a->ld_scores);
+  r->ws_bytes = r->sel.total;
   return IDX_OK;
 }
 
@@ -182,25 +154,15 @@ idx_status_t idx_score_topk(const idx_score_topk_args *args, idx_stream_t stream
   const bool timed = ev0 != nullptr && ev1 != nullptr;
   cudaError_t e = timed ? cudaEventRecord(ev0, s) : cudaSuccess;
   if (e != cudaSuccess) return IDX_ERR_CUDA;
-  if (r.plan == Plan::kSimt) {
-    float *scores = r.use_scores_out ? args->scores_out : static_cast<float *>(args->workspace);
-    e = launch_score_simt(r.p, args->key_format == IDX_KEYS_F32, scores, r.ld, s);
-    if (e == cudaSuccess && timed) e = cudaEventRecord(ev1, s);
-    if (e == cudaSuccess) e = launch_topk_rows(r.p, scores, r.ld, s);
-  } else if (r.tc.rows_mode) {
-    ScoreParams q = r.p;
-    if (q.scores_out == nullptr) {
-      q.scores_out = static_cast<float *>(args->workspace);
-      q.ld_scores = r.tc.ld;
-    }
-    e = launch_score_tc(q, r.tc, args->workspace, s);
-    if (e == cudaSuccess && timed) e = cudaEventRecord(ev1, s);
-    if (e == cudaSuccess) e = launch_topk_rows(q, q.scores_out, q.ld_scores, s);
-  } else {
-    e = launch_score_tc(r.p, r.tc, args->workspace, s);
-    if (e == cudaSuccess && timed) e = cudaEventRecord(ev1, s);
-    if (e == cudaSuccess) e = launch_topk_merge(r.p, r.tc, args->workspace, s);
-  }
+  float *scores = r.sel.own_scores ? reinterpret_cast<float *>(static_cast<unsigned char *>(args->workspace) +
+                                                               r.sel.scores_off)
+                                   : args->scores_out;
+  if (r.plan == Plan::kSimt)
+    e = launch_score_simt(r.p, args->key_format == IDX_KEYS_F32, scores, r.sel.ld, s);
+  else
+    e = launch_score_tc(r.p, r.num_ctas, scores, r.sel.ld, s);
+  if (e == cudaSuccess && timed) e = cudaEventRecord(ev1, s);
+  if (e == cudaSuccess) e = launch_select(r.p, scores, r.sel.ld, r.sel, args->workspace, s);
   return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 

@@ -231,15 +231,4 @@ struct TopkGroup {
   }
 };
 
-// Shared-memory capacity (keys) of the top-k buffer of the row / merge kernels.
-__host__ __device__ inline int topk_rows_cap(int k, int nt) {
-  int kp = 1;
-  while (kp < k) kp <<= 1;
-  int cap = 4 * kp;
-  if (cap < 4096) cap = 4096;
-  if (cap > 16384) cap = 16384;
-  if (cap < kp + 2 * nt) cap = kp + 2 * nt;
-  return cap;
-}
-
 }  // namespace idx

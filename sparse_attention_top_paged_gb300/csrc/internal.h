@@ -30,35 +30,28 @@ struct ScoreParams {
   int32_t *dev_status;
 };
 
-// Workspace sections of the tensor-core path (byte offsets; 256-aligned).
-// In rows mode the scoring kernel writes every score to a [T, ld] matrix
-// (`scores`, or the caller's scores_out) and the per-row top-k kernel selects;
-// otherwise it keeps per-segment candidates for the merge kernel.
-struct TcWorkspace {
-  size_t seg_first, seg_last, cand_count, cand, scores, total;
-  int num_ctas, n_slots;
-  bool rows_mode;
-  long long ld;  // row stride of the score matrix in rows mode
+// How TopK(I[t,:], k) is taken from the [T, ld] score matrix, and the
+// workspace sections the score path needs (byte offsets; 256-aligned).
+struct SelectPlan {
+  bool two_stage;    // chunk select over (chunk, query) CTAs, then a per-query merge
+  int chunk, n_ch;   // keys per chunk, chunks per row (two-stage only)
+  bool own_scores;   // the score matrix lives in the workspace (no caller scores_out)
+  long long ld;      // row stride of the score matrix
+  size_t scores_off, count_off, cand_off, total;
 };
 
-// Rows mode pays when a query keeps a large share of its keys (the streaming
-// select inside the scoring kernel then compacts often): max_len < 8 * top_k.
-bool tc_rows_mode(long long max_len, int top_k);
-TcWorkspace tc_workspace_layout(int T, int top_k, int num_ctas, long long max_len, bool have_scores_out,
-                                long long ld_scores_out);
+SelectPlan select_plan(int T, int top_k, long long max_len, bool have_scores_out, long long ld_out);
+bool select_supported(int top_k, long long max_len);  // the merge's chunk table fits shared memory
 
 // score_simt.cu
 cudaError_t launch_score_simt(const ScoreParams &p, bool f32_keys, float *scores, long long ld,
                               cudaStream_t stream);
 // topk.cu
-cudaError_t launch_topk_rows(const ScoreParams &p, const float *scores, long long ld,
-                             cudaStream_t stream);
-cudaError_t launch_topk_merge(const ScoreParams &p, const TcWorkspace &ws, void *workspace,
-                              cudaStream_t stream);
+cudaError_t launch_select(const ScoreParams &p, const float *scores, long long ld, const SelectPlan &plan,
+                          void *workspace, cudaStream_t stream);
 // score_tc.cu
 bool score_tc_supported(const ScoreParams &p);
-cudaError_t launch_score_tc(const ScoreParams &p, const TcWorkspace &ws, void *workspace,
-                            cudaStream_t stream);  // rows mode: scores land in p.scores_out
+cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, float *scores, long long ld, cudaStream_t stream);
 // gather_pool.cu
 cudaError_t launch_gather_kv(const idx_gather_kv_args &a, cudaStream_t stream);
 cudaError_t launch_block_pool(const uint16_t *raw, const float *w, float *out, uint32_t first_block,

@@ -3,16 +3,15 @@
 //
 // What it computes: eq. 16 of "indexer_score_topk.cu" (nvfp4-megamoe-kernel,
 // dsv4/kernels/indexer), I[t,s] = sum_h w[t,h] * ReLU(q[t,h] . K[s]), over NVFP4
-// keys resolved through the block table, then the k best keys of every
-// segment (see below); the merge kernel in topk.cu finishes TopK(I[t,:], k).
+// keys resolved through the block table, written to a [T, ld] score matrix;
+// the selection kernels in topk.cu then take TopK(I[t,:], k).
 // That page's kernel runs one CTA per query with scalar FP32 dot products and
 // a locked shared heap; this one is a persistent, warp-specialised tcgen05
 // pipeline:
 //
 //   work     The tiles of 128 consecutive keys of every query, laid end to end,
 //            are split evenly over the CTAs (one per SM). A "segment" is a
-//            CTA's run of tiles of one query; each segment hands its top-k
-//            candidates to the merge.
+//            CTA's run of tiles of one query (it shares one B operand).
 //   warp 10  resolver: looks up block-table entries and per-block global
 //            scales 32 blocks at a time (one per lane) into a ring of per-tile
 //            records, so no dependent global load sits on the copy path.
@@ -31,8 +30,9 @@
 //   warps 6-9 epilogue: one thread per key reads its accumulator row from
 //            tensor memory and forms I = g * sum_h (w_h 2^-sigma_h) relu(acc_h)
 //            (the per-block global scale g is factored out, so relu(g a) = g
-//            relu(a) for g > 0 and g min(a,0) for g < 0), then feeds a
-//            streaming top-k (common.cuh).
+//            relu(a) for g > 0 and g min(a,0) for g < 0), then stores I to the
+//            score matrix (coalesced: a warp writes 32 consecutive keys). The
+//            four epilogue warps never wait for one another.
 //
 // Products e2m1 * e4m3 are exact in f16, and bf16-valued q is exact in the
 // scaled f16 hi part, so a single MMA pass computes the dot products with f32
@@ -43,7 +43,6 @@
 
 #include <mutex>
 
-#include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -52,14 +51,13 @@ namespace {
 
 constexpr int kThreads = 352;
 constexpr int kTileKeys = 128;
-constexpr int kNS = 6;                   // raw stages
+constexpr int kMaxNS = 16;               // raw stages (as many as shared memory holds)
 constexpr int kR = 64;                   // metadata ring (tiles)
 constexpr uint32_t kStageBytes = 9216;   // 128 x 64 B nibbles + 128 x 8 B scales
 constexpr uint32_t kScaleOff = 8192;
 constexpr int kMaxBlocksPerTile = 8;     // epb >= 16
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr int kSmemLimit = 227 * 1024;
-constexpr int kEpiBar = 1, kEpiVoteBar = 2;  // top-k group syncs / per-tile vote
 
 // One tile's resolved blocks, written by the resolver warp, read by the
 // producer (physical blocks) and the epilogue (global scales, validity).
@@ -75,16 +73,15 @@ struct MetaEntry {
 static_assert(sizeof(MetaEntry) == 128, "meta entry");
 
 struct TcLayout {
-  int Npad, nseg, nd, cap, box_rows, bpt, trig, epb_shift;
-  int rows_mode;  // write every score to p.scores_out; no in-kernel top-k
+  int Npad, nseg, nd, ns, box_rows, bpt, epb_shift;
   uint32_t off_b, b_bytes, off_raw, off_w, off_flags, off_meta, off_bar, off_misc, off_tsh, off_tbuf;
   uint32_t smem_bytes;
 };
 
 // barrier indices (uint64 slots from off_bar)
-constexpr int B_FULL_RAW = 0, B_EMPTY_RAW = kNS, B_FULL_A = 2 * kNS, B_EMPTY_A = 2 * kNS + 2,
-              B_FULL_D = 2 * kNS + 4, B_EMPTY_D = 2 * kNS + 6, B_META_FULL = 2 * kNS + 8,
-              B_META_EMPTY = 2 * kNS + 8 + kR, B_SEG_FULL = 2 * kNS + 8 + 2 * kR,
+constexpr int B_FULL_RAW = 0, B_EMPTY_RAW = kMaxNS, B_FULL_A = 2 * kMaxNS, B_EMPTY_A = 2 * kMaxNS + 2,
+              B_FULL_D = 2 * kMaxNS + 4, B_EMPTY_D = 2 * kMaxNS + 6, B_META_FULL = 2 * kMaxNS + 8,
+              B_META_EMPTY = 2 * kMaxNS + 8 + kR, B_SEG_FULL = 2 * kMaxNS + 8 + 2 * kR,
               B_SEG_BFREE = B_SEG_FULL + 2, B_SEG_WFREE = B_SEG_FULL + 4, B_COUNT = B_SEG_FULL + 6;
 
 // misc ints
@@ -156,8 +153,7 @@ __device__ long long block_incl_scan(long long v, long long *scratch, long long 
 
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmap_nib, ScoreParams p, TcLayout lay,
-                    int32_t *__restrict__ seg_first, int32_t *__restrict__ seg_last,
-                    int32_t *__restrict__ cand_count, uint64_t *__restrict__ cand) {
+                    float *__restrict__ scores, long long ld) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -167,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNS; ++s) {
+    for (int s = 0; s < lay.ns; ++s) {
       ptx::mbar_init(bar(B_FULL_RAW + s), 1);
       ptx::mbar_init(bar(B_EMPTY_RAW + s), 4);
     }
@@ -178,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(B_EMPTY_D + a), 4);
       ptx::mbar_init(bar(B_SEG_FULL + a), 4);
       ptx::mbar_init(bar(B_SEG_BFREE + a), 1);
-      ptx::mbar_init(bar(B_SEG_WFREE + a), 1);
+      ptx::mbar_init(bar(B_SEG_WFREE + a), 4);  // one arrive per epilogue warp
     }
     for (int r = 0; r < kR; ++r) {
       ptx::mbar_init(bar(B_META_FULL + r), 1);   // resolver
@@ -229,11 +225,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = static_cast<uint32_t>(misc[M_TMEM]);
   const int t0 = misc[M_T0], j0 = misc[M_J0];
   const int n_tiles = (g0 < g1) ? static_cast<int>(g1 - g0) : 0;
-  // A CTA with no tiles (fewer tiles than CTAs) may sit inside the CTA range of a
-  // query t0 = the query holding tile g0; the merge then reads slot t0 + c, so
-  // record it as empty. No real segment (t, c') can share that slot: t0 - 1 has
-  // no tile at or after g0, and t0 + 1 none before it.
-  if (n_tiles == 0 && threadIdx.x == 0 && !lay.rows_mode) cand_count[t0 + static_cast<int>(blockIdx.x)] = 0;
   const int Npad = lay.Npad, nseg = lay.nseg, nd = lay.nd;
   const uint32_t b_bytes = lay.b_bytes;
   uint8_t *sB = sm + lay.off_b;
@@ -249,7 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int issued = 0;
       Ring raw, meta;
-      for (int i = 0; i < n_tiles; ++i, raw.next(kNS), meta.next(kR)) {
+      const int ns = lay.ns;
+      for (int i = 0; i < n_tiles; ++i, raw.next(ns), meta.next(kR)) {
         const int s = raw.idx, r = meta.idx;
         if (!ptx::mbar_wait(bar(B_EMPTY_RAW + s), raw.phase ^ 1u, abort_flag, kTimeoutNs)) break;
         if (!ptx::mbar_wait(bar(B_META_FULL + r), meta.phase, abort_flag, kTimeoutNs)) break;
@@ -290,9 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++issued;
       }
       // never leave with copies in flight
-      for (int i = (issued > kNS ? issued - kNS : 0); i < issued; ++i) {
+      for (int i = (issued > ns ? issued - ns : 0); i < issued; ++i) {
         volatile int no_abort = 0;
-        ptx::mbar_wait(bar(B_FULL_RAW + i % kNS), static_cast<uint32_t>(i / kNS) & 1u, &no_abort, kTimeoutNs);
+        ptx::mbar_wait(bar(B_FULL_RAW + i % ns), static_cast<uint32_t>(i / ns) & 1u, &no_abort, kTimeoutNs);
       }
     }
   } else if (warp == 1) {
@@ -353,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Walker w;
     w.init(p, t0, j0);
     Ring rraw, ra, rs;
-    for (int i = 0; i < n_tiles; ++i, w.next(p), rraw.next(kNS), ra.next(2)) {
+    for (int i = 0; i < n_tiles; ++i, w.next(p), rraw.next(lay.ns), ra.next(2)) {
       const bool seg_start = (i == 0) || (w.j == 0);
       if (seg_start) {
         if (i > 0) rs.next(nseg);
@@ -526,15 +518,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ============================================================== epilogue
-    const int et = threadIdx.x - 192;          // 0..127: index in the top-k group
     const int row = 32 * (warp & 3) + lane;    // the TMEM lane (key row) this thread reads
-    TopkGroup<128> tk{reinterpret_cast<TopkShared *>(sm + lay.off_tsh),
-                      reinterpret_cast<uint64_t *>(sm + lay.off_tbuf), lay.cap, et, kEpiBar};
-    tk.reset();
     Walker w;
     w.init(p, t0, j0);
     int ss = 0, L = 0;
-    const int k = p.top_k;
     Ring rd, rm, rs;
     for (int i = 0; i < n_tiles; ++i, w.next(p), rd.next(nd), rm.next(kR)) {
       const bool seg_start = (i == 0) || (w.j == 0);
@@ -549,83 +536,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int d = rd.idx, r = rm.idx;
       ok = ok && ptx::mbar_wait(bar(B_FULL_D + d), rd.phase, abort_flag, kTimeoutNs);
       ok = ok && ptx::mbar_wait(bar(B_META_FULL + r), rm.phase, abort_flag, kTimeoutNs);
-      ok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform before the .aligned TMEM loads
-      if (seg_start && w.j == 0 && et == 0 && !lay.rows_mode) seg_first[w.t] = w.t + static_cast<int>(blockIdx.x);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;  // warp-uniform exit before the .aligned TMEM loads
+      ptx::tc_fence_after();
       const int s_key = w.j * kTileKeys + row;
-      bool valid = false, in_len = false;
-      float I = 0.0f;
-      if (ok) {
-        ptx::tc_fence_after();
-        const int b = (s_key >> lay.epb_shift) - sMeta[r].lb0;
-        in_len = s_key < L;
-        valid = in_len && b < kMaxBlocksPerTile && ((sMeta[r].mask >> b) & 1u);
-        const float g = (b < kMaxBlocksPerTile) ? sMeta[r].g[b] : 0.0f;
-        const uint64_t *wv2 = reinterpret_cast<const uint64_t *>(sW + ss * 256);  // (w'_h, w'_h+1) pairs
-        uint64_t acc2[2] = {0ull, 0ull};                                          // two independent chains
-        const uint32_t taddr = tmem_d + d * Npad + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-        for (int c0 = 0; c0 < Npad; c0 += 64) {
-          uint32_t v[64];
-          __syncwarp();  // the per-row sign branch below must not leave the warp split at these loads
-          ptx::tmem_ld32(taddr + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-          if (c0 + 32 < Npad) ptx::tmem_ld32(taddr + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-          ptx::tmem_wait_ld();
-          if (c0 + 64 >= Npad) {   // every accumulator column is in registers: hand back the slots
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              ptx::mbar_arrive(bar(B_EMPTY_D + d));
-              ptx::mbar_arrive(bar(B_META_EMPTY + r));
+      const int b = (s_key >> lay.epb_shift) - sMeta[r].lb0;
+      const bool in_len = s_key < L;
+      const bool valid = in_len && b < kMaxBlocksPerTile && ((sMeta[r].mask >> b) & 1u);
+      const float g = (b < kMaxBlocksPerTile) ? sMeta[r].g[b] : 0.0f;
+      const uint64_t *wv2 = reinterpret_cast<const uint64_t *>(sW + ss * 256);  // (w'_h, w'_h+1) pairs
+      uint64_t acc2[2] = {0ull, 0ull};                                          // two independent chains
+      const uint32_t taddr = tmem_d + d * Npad + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+      for (int c0 = 0; c0 < Npad; c0 += 64) {
+        uint32_t v[64];
+        __syncwarp();  // the per-row sign branch below must not leave the warp split at these loads
+        ptx::tmem_ld32(taddr + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        if (c0 + 32 < Npad) ptx::tmem_ld32(taddr + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        ptx::tmem_wait_ld();
+        if (c0 + 64 >= Npad) {   // every accumulator column is in registers: hand back the slots
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::mbar_arrive(bar(B_EMPTY_D + d));
+            ptx::mbar_arrive(bar(B_META_EMPTY + r));
+          }
+        }
+        const int ncol = (Npad - c0 < 64) ? (Npad - c0) : 64;
+        if (g >= 0.0f) {          // relu(g a) = g max(a, 0)
+#pragma unroll
+          for (int e = 0; e < 64; e += 4) {
+            if (e < ncol) {
+              ptx::ffma2(acc2[0], wv2[(c0 + e) >> 1],
+                         ptx::pack2(fmaxf(__uint_as_float(v[e]), 0.0f), fmaxf(__uint_as_float(v[e + 1]), 0.0f)));
+              ptx::ffma2(acc2[1], wv2[((c0 + e) >> 1) + 1],
+                         ptx::pack2(fmaxf(__uint_as_float(v[e + 2]), 0.0f), fmaxf(__uint_as_float(v[e + 3]), 0.0f)));
             }
           }
-          const int ncol = (Npad - c0 < 64) ? (Npad - c0) : 64;
-          if (g >= 0.0f) {          // relu(g a) = g max(a, 0)
+        } else {                  // relu(g a) = g min(a, 0)
 #pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-              if (e < ncol) {
-                ptx::ffma2(acc2[0], wv2[(c0 + e) >> 1],
-                           ptx::pack2(fmaxf(__uint_as_float(v[e]), 0.0f), fmaxf(__uint_as_float(v[e + 1]), 0.0f)));
-                ptx::ffma2(acc2[1], wv2[((c0 + e) >> 1) + 1],
-                           ptx::pack2(fmaxf(__uint_as_float(v[e + 2]), 0.0f), fmaxf(__uint_as_float(v[e + 3]), 0.0f)));
-              }
-            }
-          } else {                  // relu(g a) = g min(a, 0)
-#pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-              if (e < ncol) {
-                ptx::ffma2(acc2[0], wv2[(c0 + e) >> 1],
-                           ptx::pack2(fminf(__uint_as_float(v[e]), 0.0f), fminf(__uint_as_float(v[e + 1]), 0.0f)));
-                ptx::ffma2(acc2[1], wv2[((c0 + e) >> 1) + 1],
-                           ptx::pack2(fminf(__uint_as_float(v[e + 2]), 0.0f), fminf(__uint_as_float(v[e + 3]), 0.0f)));
-              }
+          for (int e = 0; e < 64; e += 4) {
+            if (e < ncol) {
+              ptx::ffma2(acc2[0], wv2[(c0 + e) >> 1],
+                         ptx::pack2(fminf(__uint_as_float(v[e]), 0.0f), fminf(__uint_as_float(v[e + 1]), 0.0f)));
+              ptx::ffma2(acc2[1], wv2[((c0 + e) >> 1) + 1],
+                         ptx::pack2(fminf(__uint_as_float(v[e + 2]), 0.0f), fminf(__uint_as_float(v[e + 3]), 0.0f)));
             }
           }
         }
-        const float sum = (__uint_as_float(static_cast<uint32_t>(acc2[0])) + __uint_as_float(static_cast<uint32_t>(acc2[0] >> 32))) +
-                          (__uint_as_float(static_cast<uint32_t>(acc2[1])) + __uint_as_float(static_cast<uint32_t>(acc2[1] >> 32)));
-        I = g * sum;
-        if (p.scores_out && in_len)
-          p.scores_out[static_cast<long long>(w.t) * p.ld_scores + s_key] = valid ? __fadd_rn(I, 0.0f) : -INFINITY;
       }
-      if (lay.rows_mode) {   // scores already written above; the row top-k kernel selects
-        if (!ptx::bar_and(kEpiVoteBar, 128, ok)) break;
-        if (seg_end && et == 0) ptx::mbar_arrive(bar(B_SEG_WFREE + ss));  // w' of this segment is free
-        continue;
-      }
-      tk.offer(pack_key(I, s_key), valid);
-      if (!ptx::bar_and(kEpiVoteBar, 128, ok)) break;  // ends the offer round for the whole group
-      if (tk.s->count > lay.trig) tk.compact(k);
-      if (seg_end) {
-        tk.compact(k);
-        const int slot = w.t + static_cast<int>(blockIdx.x);
-        const int n = tk.s->count;
-        for (int x = et; x < n; x += 128) cand[static_cast<long long>(slot) * k + x] = tk.buf[x];
-        if (et == 0) {
-          cand_count[slot] = n;
-          if (w.j == w.nt - 1) seg_last[w.t] = slot;
-        }
-        tk.sync();
-        tk.reset();
-        if (et == 0) ptx::mbar_arrive(bar(B_SEG_WFREE + ss));
+      const float sum = (__uint_as_float(static_cast<uint32_t>(acc2[0])) + __uint_as_float(static_cast<uint32_t>(acc2[0] >> 32))) +
+                        (__uint_as_float(static_cast<uint32_t>(acc2[1])) + __uint_as_float(static_cast<uint32_t>(acc2[1] >> 32)));
+      if (in_len) scores[static_cast<long long>(w.t) * ld + s_key] = valid ? __fadd_rn(g * sum, 0.0f) : -INFINITY;
+      if (seg_end) {             // this warp is done with the segment's w'
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(B_SEG_WFREE + ss));
       }
     }
   }
@@ -668,12 +631,21 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   l.bpt = p.epb < 128 ? 128 / p.epb : 1;
   l.epb_shift = 0;
   while ((1 << l.epb_shift) < p.epb) ++l.epb_shift;
-  uint32_t off = 0;
+  // B operands first (multiples of 8 KB), then the raw stages (1 KB-aligned,
+  // as many as fit), then the small tables.
   l.b_bytes = static_cast<uint32_t>(l.Npad) * 256u;
-  l.off_b = off;
-  off += static_cast<uint32_t>(l.nseg) * 2u * l.b_bytes;
+  l.off_b = 0;
+  const uint32_t b_total = static_cast<uint32_t>(l.nseg) * 2u * l.b_bytes;
+  const uint32_t tail = static_cast<uint32_t>(l.nseg) * 256u * 4u + 64 + kR * sizeof(MetaEntry) +
+                        ((B_COUNT * 8 + 15) & ~15u) + ((8 * 4 + 16 * 8 + 15) & ~15u);
+  const long long room = static_cast<long long>(kSmemLimit) - 1024 - b_total - tail;
+  long long ns = room / kStageBytes;
+  if (ns > kMaxNS) ns = kMaxNS;
+  if (ns < 3) return false;
+  l.ns = static_cast<int>(ns);
+  uint32_t off = b_total;
   l.off_raw = off;
-  off += kNS * kStageBytes;
+  off += static_cast<uint32_t>(l.ns) * kStageBytes;
   l.off_w = off;
   off += static_cast<uint32_t>(l.nseg) * 256u * 4u;
   l.off_flags = off;
@@ -686,24 +658,6 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   l.off_misc = off;
   off += 8 * 4 + 16 * 8;
   off = (off + 15) & ~15u;
-  l.off_tsh = off;
-  off += (sizeof(TopkShared) + 15) & ~size_t(15);
-  l.off_tbuf = off;
-  int kp = 1;
-  while (kp < p.top_k) kp <<= 1;
-  const int min_cap = (kp > p.top_k + 256 ? kp : p.top_k + 256);
-  const long long room = static_cast<long long>(kSmemLimit) - 1024 - off;
-  long long cap = room / 8;
-  if (cap > 16384) cap = 16384;
-  if (cap < min_cap) return false;
-  l.cap = static_cast<int>(cap);
-  // Compact early: once k keys are kept the threshold rejects most later keys
-  // at the offer, so the buffer (and each radix select over it) stays small.
-  long long trig = 2LL * kp;
-  if (trig < 1024) trig = 1024;
-  if (trig > cap - 128) trig = cap - 128;
-  l.trig = static_cast<int>(trig);
-  off += static_cast<uint32_t>(cap) * 8u;
   l.smem_bytes = off + 1024;
   *out = l;
   return true;
@@ -717,11 +671,9 @@ bool score_tc_supported(const ScoreParams &p) {
   return p.D == 128 && p.keys_fp4 != nullptr && make_layout(p, &l) && get_encode() != nullptr;
 }
 
-cudaError_t launch_score_tc(const ScoreParams &p, const TcWorkspace &ws, void *workspace, cudaStream_t stream) {
+cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, float *scores, long long ld, cudaStream_t stream) {
   TcLayout lay;
   if (!make_layout(p, &lay)) return cudaErrorNotSupported;
-  lay.rows_mode = ws.rows_mode ? 1 : 0;
-  if (lay.rows_mode && p.scores_out == nullptr) return cudaErrorInvalidValue;
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap tmap;
@@ -736,10 +688,7 @@ cudaError_t launch_score_tc(const ScoreParams &p, const TcWorkspace &ws, void *w
   cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(lay.smem_bytes));
   if (e != cudaSuccess) return e;
-  uint8_t *base = static_cast<uint8_t *>(workspace);
-  score_tc_kernel<<<ws.num_ctas, kThreads, lay.smem_bytes, stream>>>(
-      tmap, p, lay, reinterpret_cast<int32_t *>(base + ws.seg_first), reinterpret_cast<int32_t *>(base + ws.seg_last),
-      reinterpret_cast<int32_t *>(base + ws.cand_count), reinterpret_cast<uint64_t *>(base + ws.cand));
+  score_tc_kernel<<<num_ctas, kThreads, lay.smem_bytes, stream>>>(tmap, p, lay, scores, ld);
   return cudaGetLastError();
 }
 
