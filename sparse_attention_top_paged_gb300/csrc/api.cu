@@ -29,8 +29,6 @@ int device_sm_count() {
   return cache[dev];
 }
 
-static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
 }  // namespace idx
 
 using namespace idx;

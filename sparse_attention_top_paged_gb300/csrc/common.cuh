@@ -10,12 +10,9 @@
 // needs a rule beyond the key itself. Key 0 never encodes a real candidate
 // and serves as padding.
 //
-// A TopkGroup is a streaming top-k accumulator run by a group of NT threads
-// (whole warps) of one CTA: threads offer keys, the group appends those at or
-// above a running threshold to a shared-memory buffer, and when the buffer
-// fills it radix-selects the k largest keys in place and raises the threshold
-// to a value no greater than the k-th largest key seen so far. Nothing is
-// ever discarded that could still belong to the final top-k.
+// A TopkGroup is an exact radix select run by a group of NT threads (whole
+// warps) of one CTA over keys held in a shared-memory buffer: compact(k)
+// keeps exactly the k largest keys, in place, by 8-bit digit histograms.
 #pragma once
 
 #include <cstdint>
@@ -65,46 +62,16 @@ struct TopkShared {
   int count;   // entries in the buffer
   int wcount;  // write cursor during compaction
   int sel_bin, sel_above, sel_cnt;
-  int pad_;
-  unsigned long long thr;  // keys below thr can no longer enter the top-k
 };
 
 template <int NT>
 struct TopkGroup {
   TopkShared *s;
   uint64_t *buf;
-  int cap;     // buffer capacity in keys (>= k + NT)
   int gtid;    // thread index within the group
   int bar_id;  // named barrier of the group
 
   __device__ __forceinline__ void sync() const { group_sync<NT>(bar_id); }
-
-  __device__ void reset() {
-    if (gtid == 0) {
-      s->count = 0;
-      s->thr = 0ull;
-    }
-    sync();
-  }
-
-  // Every thread of the group calls offer() once per round (valid=false to
-  // offer nothing). The caller guarantees count + NT <= cap before a round
-  // and calls after_round() after it.
-  __device__ __forceinline__ void offer(uint64_t key, bool valid) {
-    const bool acc = valid && key >= s->thr;
-    const uint32_t m = __ballot_sync(0xFFFFFFFFu, acc);
-    int base = 0;
-    if (lane_id() == 0 && m) base = atomicAdd(&s->count, __popc(m));
-    base = __shfl_sync(0xFFFFFFFFu, base, 0);
-    if (acc) buf[base + __popc(m & lanemask_lt())] = key;
-  }
-
-  // Ends a round of offers; compacts to the top k when the buffer could not
-  // take another round.
-  __device__ void after_round(int k) {
-    sync();
-    if (s->count > cap - NT) compact(k);
-  }
 
   // Keep exactly the k largest keys (if more than k are held).
   __device__ void compact(int k) {
@@ -198,36 +165,8 @@ struct TopkGroup {
       // kept as were read), so the next round's keys are untouched.
     }
     sync();
-    if (gtid == 0) {
-      s->count = s->wcount;
-      if (prefix > s->thr) s->thr = prefix;
-    }
+    if (gtid == 0) s->count = s->wcount;
     sync();
-  }
-
-  // Sort the (at most k) held keys descending into buf[0 .. m), m the next
-  // power of two >= count, padding with key 0. Call after compact(k).
-  __device__ void sort_desc() {
-    const int n = s->count;
-    int m = 1;
-    while (m < n) m <<= 1;
-    for (int i = n + gtid; i < m; i += NT) buf[i] = 0ull;
-    sync();
-    for (int size = 2; size <= m; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = gtid; i < (m >> 1); i += NT) {
-          const int lo = 2 * stride * (i / stride) + (i % stride);
-          const int hi = lo + stride;
-          const bool desc = (lo & size) == 0;
-          const uint64_t a = buf[lo], b = buf[hi];
-          if ((a < b) == desc) {
-            buf[lo] = b;
-            buf[hi] = a;
-          }
-        }
-        sync();
-      }
-    }
   }
 };
 

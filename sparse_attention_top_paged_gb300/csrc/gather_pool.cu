@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kExpandThreads) expand_blocks_kernel(const int
   for (int size = 2; size <= m; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       for (int i = threadIdx.x; i < (m >> 1); i += kExpandThreads) {
-        const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+        const int lo = ((i & ~(stride - 1)) << 1) | (i & (stride - 1)), hi = lo + stride;
         const bool asc = (lo & size) == 0;
         const int32_t a = ids[lo], c = ids[hi];
         if ((a > c) == asc) {

@@ -32,16 +32,22 @@ struct ScoreParams {
 
 // How TopK(I[t,:], k) is taken from the [T, ld] score matrix, and the
 // workspace sections the score path needs (byte offsets; 256-aligned).
+// Selection runs in stages: stage 0 reads the score rows; while a query's
+// keys exceed one cluster's reach, a stage writes the k best keys of each
+// piece to a candidate list and the next stage selects from those lists.
+constexpr int kMaxSelectStages = 8;
 struct SelectPlan {
-  bool two_stage;    // chunk select over (chunk, query) CTAs, then a per-query merge
-  int chunk, n_ch;   // keys per chunk, chunks per row (two-stage only)
-  bool own_scores;   // the score matrix lives in the workspace (no caller scores_out)
-  long long ld;      // row stride of the score matrix
-  size_t scores_off, count_off, cand_off, total;
+  int n_stages;
+  int C[kMaxSelectStages];          // cluster size (CTAs) of each stage
+  int pieces[kMaxSelectStages];     // clusters per query of each stage
+  long long n_in[kMaxSelectStages]; // keys per query a stage reads (stage 0: max row length)
+  bool own_scores;                  // the score matrix lives in the workspace (no caller scores_out)
+  long long ld;                     // row stride of the score matrix
+  size_t scores_off, cand_off[2], total;
 };
 
 SelectPlan select_plan(int T, int top_k, long long max_len, bool have_scores_out, long long ld_out);
-bool select_supported(int top_k, long long max_len);  // the merge's chunk table fits shared memory
+bool select_supported(int top_k, long long max_len);  // the stages end in one cluster per query
 
 // score_simt.cu
 cudaError_t launch_score_simt(const ScoreParams &p, bool f32_keys, float *scores, long long ld,

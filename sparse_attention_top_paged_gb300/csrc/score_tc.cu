@@ -73,15 +73,16 @@ struct MetaEntry {
 static_assert(sizeof(MetaEntry) == 128, "meta entry");
 
 struct TcLayout {
-  int Npad, nseg, nd, ns, box_rows, bpt, epb_shift;
-  uint32_t off_b, b_bytes, off_raw, off_w, off_flags, off_meta, off_bar, off_misc, off_tsh, off_tbuf;
+  int Npad, nseg, na, nd, ns, box_rows, bpt, epb_shift;
+  uint32_t off_b, b_bytes, off_raw, off_w, off_flags, off_meta, off_bar, off_misc;
   uint32_t smem_bytes;
 };
 
 // barrier indices (uint64 slots from off_bar)
-constexpr int B_FULL_RAW = 0, B_EMPTY_RAW = kMaxNS, B_FULL_A = 2 * kMaxNS, B_EMPTY_A = 2 * kMaxNS + 2,
-              B_FULL_D = 2 * kMaxNS + 4, B_EMPTY_D = 2 * kMaxNS + 6, B_META_FULL = 2 * kMaxNS + 8,
-              B_META_EMPTY = 2 * kMaxNS + 8 + kR, B_SEG_FULL = 2 * kMaxNS + 8 + 2 * kR,
+constexpr int kMaxSlots = 4;  // tensor-memory A and D slots (each)
+constexpr int B_FULL_RAW = 0, B_EMPTY_RAW = kMaxNS, B_FULL_A = 2 * kMaxNS, B_EMPTY_A = B_FULL_A + kMaxSlots,
+              B_FULL_D = B_EMPTY_A + kMaxSlots, B_EMPTY_D = B_FULL_D + kMaxSlots,
+              B_META_FULL = B_EMPTY_D + kMaxSlots, B_META_EMPTY = B_META_FULL + kR, B_SEG_FULL = B_META_EMPTY + kR,
               B_SEG_BFREE = B_SEG_FULL + 2, B_SEG_WFREE = B_SEG_FULL + 4, B_COUNT = B_SEG_FULL + 6;
 
 // misc ints
@@ -167,11 +168,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(B_FULL_RAW + s), 1);
       ptx::mbar_init(bar(B_EMPTY_RAW + s), 4);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kMaxSlots; ++a) {
       ptx::mbar_init(bar(B_FULL_A + a), 4);
       ptx::mbar_init(bar(B_EMPTY_A + a), 1);
       ptx::mbar_init(bar(B_FULL_D + a), 1);
       ptx::mbar_init(bar(B_EMPTY_D + a), 4);
+    }
+    for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar(B_SEG_FULL + a), 4);
       ptx::mbar_init(bar(B_SEG_BFREE + a), 1);
       ptx::mbar_init(bar(B_SEG_WFREE + a), 4);  // one arrive per epilogue warp
@@ -225,15 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = static_cast<uint32_t>(misc[M_TMEM]);
   const int t0 = misc[M_T0], j0 = misc[M_J0];
   const int n_tiles = (g0 < g1) ? static_cast<int>(g1 - g0) : 0;
-  const int Npad = lay.Npad, nseg = lay.nseg, nd = lay.nd;
+  const int Npad = lay.Npad, nseg = lay.nseg, na = lay.na, nd = lay.nd;
   const uint32_t b_bytes = lay.b_bytes;
   uint8_t *sB = sm + lay.off_b;
   uint8_t *sRaw = sm + lay.off_raw;
   float *sW = reinterpret_cast<float *>(sm + lay.off_w);
   int *sFlags = reinterpret_cast<int *>(sm + lay.off_flags);
   MetaEntry *sMeta = reinterpret_cast<MetaEntry *>(sm + lay.off_meta);
-  const uint32_t tmem_a = tmem;              // A slots: columns 0, 64
-  const uint32_t tmem_d = tmem + 128;        // D slots: columns 128, 128 + Npad
+  const uint32_t tmem_a = tmem;                                  // A slots: 64 columns each
+  const uint32_t tmem_d = tmem + 64u * static_cast<uint32_t>(na);  // D slots: Npad columns each
 
   if (warp == 0) {
     // ================================================================ producer
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ring ra, rd, rs;
     rs.idx = -1;  // advanced at each segment start
     int ss = 0;
-    for (int i = 0; i < n_tiles; ++i, w.next(p), ra.next(2), rd.next(nd)) {
+    for (int i = 0; i < n_tiles; ++i, w.next(p), ra.next(na), rd.next(nd)) {
       const bool seg_start = (i == 0) || (w.j == 0);
       const bool seg_end = (i == n_tiles - 1) || (w.j == w.nt - 1);
       bool ok = true;
@@ -345,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Walker w;
     w.init(p, t0, j0);
     Ring rraw, ra, rs;
-    for (int i = 0; i < n_tiles; ++i, w.next(p), rraw.next(lay.ns), ra.next(2)) {
+    for (int i = 0; i < n_tiles; ++i, w.next(p), rraw.next(lay.ns), ra.next(na)) {
       const bool seg_start = (i == 0) || (w.j == 0);
       if (seg_start) {
         if (i > 0) rs.next(nseg);
@@ -625,7 +628,13 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   l.Npad = round_up(p.H, 32);
   if (l.Npad > 256) return false;
   l.nseg = (l.Npad <= 128) ? 2 : 1;
-  l.nd = (l.Npad <= 192) ? 2 : 1;
+  // Tensor memory (512 columns): na A slots of 64 columns (128 keys x 128 f16)
+  // and nd D slots of Npad columns (128 keys x Npad f32 accumulators); more
+  // slots let the decoders, the MMA and the epilogue run further apart.
+  l.na = (l.Npad <= 128) ? 4 : 2;
+  l.nd = (512 - 64 * l.na) / l.Npad;
+  if (l.nd > kMaxSlots) l.nd = kMaxSlots;
+  if (l.nd < 1) return false;
   if (p.epb < 16 || (p.epb & (p.epb - 1)) != 0) return false;  // power-of-two blocks of >= 16 keys
   l.box_rows = p.epb < 128 ? p.epb : 128;
   l.bpt = p.epb < 128 ? 128 / p.epb : 1;

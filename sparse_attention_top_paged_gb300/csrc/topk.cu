@@ -1,24 +1,85 @@
-// topk.cu — TopK(I[t,:], k) from a score matrix, on all SMs.
+// topk.cu — TopK(I[t,:], k) from a score matrix, one thread-block cluster per
+// query (or per piece of a very long query).
 //
 // Output order is the top-k write-out of "indexer_score_topk.cu": score
 // descending, lower index first on equal scores, -1 / -inf padding. Both score
 // paths write I[t, 0..valid_len) (with -inf for keys of out-of-range blocks)
-// into a [T, ld] matrix; selection (BlockSelect, select.cuh) then runs in one
-// of two plans:
-//   * one pass: one CTA per query selects from its whole row and sorts the k
-//     survivors (bitonic) — when a row fits one chunk;
-//   * two stages: a grid of (chunk, query) CTAs each keeps the k best keys of
-//     its chunk, then one CTA per query selects from that query's chunk
-//     candidates and sorts — so long rows use every SM, not one per query.
+// into a [T, ld] matrix; this file selects from it.
+//
+// A cluster of C CTAs (C <= 8) holds up to C * 4096 keys of one query in
+// registers (16 per thread) and finds the k largest composite keys (see
+// common.cuh) without re-reading them:
+//   1. every CTA builds a 4096-bin shared-memory histogram of the next 12 key
+//      bits of its keys;
+//   2. CTA r sums bins [r*4096/C, (r+1)*4096/C) over the cluster through
+//      distributed shared memory and publishes its slice total to all CTAs;
+//   3. the CTA whose slice holds the k-th key locates that bin and publishes
+//      it; if the bin holds more keys than the boundary buffer, the keys in it
+//      are histogrammed again on the next 12 bits (still from registers);
+//   4. every CTA appends its keys above the boundary bin, and those inside it,
+//      to buffers in CTA 0 (distributed shared-memory atomics); CTA 0 then
+//      radix-selects the missing keys from the boundary bin and sorts.
+// A query longer than one cluster's reach is split into pieces whose k best
+// keys go to a candidate list; the next launch selects from those lists the
+// same way (each stage shrinks a query's keys at least 8-fold).
 #include "common.cuh"
 #include "internal.h"
-#include "select.cuh"
 
 namespace idx {
 namespace {
 
-constexpr int kTopkThreads = 512;
-constexpr int kBndCap = 2048;
+constexpr int kSelThreads = 256;
+constexpr int kSelR = 16;                           // keys per thread, in registers
+constexpr int kCtaKeys = kSelThreads * kSelR;       // 4096
+constexpr int kBins = 4096;                         // 12-bit digits
+constexpr int kBndCap = 2048;                       // boundary-bin buffer (keys)
+constexpr int kMaxCluster = 8;
+
+// ------------------------------------------- cluster / DSMEM primitives ----
+namespace cl {
+__device__ __forceinline__ uint32_t rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t nranks() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// All threads of every CTA of the cluster; orders shared-memory writes before
+// the barrier (any CTA's) with reads after it.
+__device__ __forceinline__ void sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+// Address of the same shared-memory variable in CTA `r` of the cluster.
+__device__ __forceinline__ uint32_t map(const void *p, uint32_t r) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(a)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(r));
+  return a;
+}
+__device__ __forceinline__ uint32_t ld_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_u32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_u64(uint32_t a, uint64_t v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_add(uint32_t a, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(a), "r"(v) : "memory");
+  return old;
+}
+}  // namespace cl
 
 __host__ __device__ inline int pow2_at_least(int k) {
   int kp = 1;
@@ -26,219 +87,406 @@ __host__ __device__ inline int pow2_at_least(int k) {
   return kp;
 }
 
-// Shared memory of a selecting CTA: SelectShared, TopkShared, out (a power of
-// two >= k keys), boundary buffer.
-struct SelectSmem {
-  size_t sel, tsh, out, bnd, total;
+struct SelShared {
+  uint32_t hist[kBins];               // this CTA's histogram of the current digit
+  uint32_t slice_tot[kMaxCluster];    // per rank: keys in its slice of bins
+  uint32_t warp_sum[kSelThreads / 32];
+  int b_bin, b_above, b_cnt;          // boundary bin, published by its owner
+  int n_out, n_bnd;                   // CTA 0: append cursors
+  TopkShared tsh;                     // CTA 0: exact select of the boundary bin
 };
 
-__host__ __device__ inline SelectSmem select_smem(int k) {
-  SelectSmem m{};
-  size_t off = 0;
-  m.sel = off;
-  off += (sizeof(SelectShared) + 15) & ~size_t(15);
-  m.tsh = off;
-  off += (sizeof(TopkShared) + 15) & ~size_t(15);
-  m.out = off;
-  off += static_cast<size_t>(pow2_at_least(k)) * 8;
-  m.bnd = off;
-  off += static_cast<size_t>(kBndCap) * 8;
-  m.total = off;
+// Dynamic shared memory: SelShared, then out (a power of two >= max(k, 64)
+// keys: the sort works on whole warps' 64-key segments), then the boundary
+// buffer.
+struct SelSmem {
+  size_t out, bnd, total;
+};
+__host__ __device__ inline SelSmem sel_smem(int k) {
+  SelSmem m{};
+  m.out = (sizeof(SelShared) + 15) & ~size_t(15);
+  m.bnd = m.out + static_cast<size_t>(pow2_at_least(k < 64 ? 64 : k)) * 8;
+  m.total = m.bnd + static_cast<size_t>(kBndCap) * 8;
   return m;
 }
 
-__device__ __forceinline__ BlockSelect<kTopkThreads> make_select(unsigned char *smem, int k) {
-  const SelectSmem m = select_smem(k);
-  return BlockSelect<kTopkThreads>{reinterpret_cast<SelectShared *>(smem + m.sel),
-                                   reinterpret_cast<TopkShared *>(smem + m.tsh),
-                                   reinterpret_cast<uint64_t *>(smem + m.out),
-                                   reinterpret_cast<uint64_t *>(smem + m.bnd), kBndCap, 1};
-}
+struct SelArgs {
+  const float *scores;      // stage 0: [T, ld]
+  long long ld;
+  const uint64_t *cand_in;  // later stages: [T, n_in] keys (0 = none)
+  long long n_in;
+  uint64_t *cand_out;       // non-final stages: [T, gridDim.x / C, k] keys
+};
 
 __device__ __forceinline__ bool bad_len(const ScoreParams &p, int L) {
   return L < 0 || static_cast<long long>(L) > static_cast<long long>(p.max_lb) * p.epb;
 }
 
-__device__ void write_padding(const ScoreParams &p, int t) {
-  if (threadIdx.x == 0 && p.dev_status) atomicOr(p.dev_status, IDX_STATUS_BAD_LEN);
-  for (int i = threadIdx.x; i < p.top_k; i += kTopkThreads) {
-    p.topk_idx[static_cast<long long>(t) * p.top_k + i] = -1;
-    p.topk_score[static_cast<long long>(t) * p.top_k + i] = -INFINITY;
-  }
-}
-
-__device__ void write_sorted(const ScoreParams &p, int t, BlockSelect<kTopkThreads> &sel, int count) {
-  const int k = p.top_k;
-  sel.sort_desc(count);
-  int32_t *out_i = p.topk_idx + static_cast<long long>(t) * k;
-  float *out_s = p.topk_score + static_cast<long long>(t) * k;
-  for (int i = threadIdx.x; i < k; i += kTopkThreads) {
-    if (i < count) {
-      const uint64_t key = sel.out[i];
-      out_i[i] = key_index(key);
-      out_s[i] = key_score(key);
-    } else {
-      out_i[i] = -1;
-      out_s[i] = -INFINITY;
+// Sorts out[0 .. m) descending (m a power of two, 64 <= m): bitonic network,
+// strides >= 64 through shared memory, strides <= 32 in registers (a warp
+// holds 64 consecutive keys) so they need no block barrier.
+__device__ void sort_desc(uint64_t *out, int m) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kSelThreads / 32;
+  // in-register stages of one bitonic merge of `size`, strides 32 .. 1
+  auto warp_phase = [&](int size, int smax) {
+    for (int seg = warp; seg < (m >> 6); seg += kWarps) {
+      const int e0 = seg * 64 + lane;          // elements e0 and e0 + 32
+      uint64_t a = out[e0], b = out[e0 + 32];
+      for (int sz = (size < 64 ? 2 : size); sz <= (size < 64 ? 64 : size); sz <<= 1) {
+        for (int s = min(sz >> 1, smax); s > 0; s >>= 1) {
+          if (s == 32) {
+            const bool desc = ((e0 & sz) == 0);
+            if ((a < b) == desc) {
+              const uint64_t x = a;
+              a = b;
+              b = x;
+            }
+          } else {
+            // partner lane ^ s; the lower element of the pair keeps the larger
+            // key in a descending run
+            const uint64_t pa = __shfl_xor_sync(0xFFFFFFFFu, a, s);
+            const uint64_t pb = __shfl_xor_sync(0xFFFFFFFFu, b, s);
+            const bool lower = (lane & s) == 0;
+            const bool da = ((e0 & sz) == 0), db = (((e0 + 32) & sz) == 0);
+            a = (lower == da) ? (a > pa ? a : pa) : (a < pa ? a : pa);
+            b = (lower == db) ? (b > pb ? b : pb) : (b < pb ? b : pb);
+          }
+        }
+      }
+      out[e0] = a;
+      out[e0 + 32] = b;
     }
-  }
-}
-
-// Scores row[lo .. lo+n) as keys (index = position in the row; -inf = none).
-struct RowSrc {
-  const float *row;
-  int lo;
-  __device__ void begin() {}
-  __device__ __forceinline__ uint64_t get(int i) const {
-    const float v = row[lo + i];
-    return v == -INFINITY ? 0ull : pack_key(v, lo + i);
-  }
-};
-
-// The candidates of chunks j0 .. j0+nseg-1 laid end to end (offsets in seg_off).
-struct CandSrc {
-  const uint64_t *cand;
-  const int *seg_off;
-  long long j0;
-  int k, js;
-  __device__ void begin() { js = 0; }
-  __device__ __forceinline__ uint64_t get(int i) {
-    while (seg_off[js + 1] <= i) ++js;   // i increases per thread within a pass
-    return cand[(j0 + js) * k + (i - seg_off[js])];
-  }
-};
-
-// ---------------------------------------------------------------- one pass --
-__global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(ScoreParams p, const float *scores, long long ld) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  const int t = blockIdx.x;
-  const int L = p.valid_lens[t];
-  if (bad_len(p, L)) return write_padding(p, t);
-  BlockSelect<kTopkThreads> sel = make_select(smem_raw, p.top_k);
-  RowSrc src{scores + static_cast<long long>(t) * ld, 0};
-  const int count = sel.run(src, L, p.top_k);
-  write_sorted(p, t, sel, count);
-}
-
-// ------------------------------------------------------ stage 1: chunks ----
-__global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(ScoreParams p, const float *scores, long long ld,
-                                                                  int chunk, int n_ch, uint64_t *cand,
-                                                                  int32_t *cand_count) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  const int c = blockIdx.x, t = blockIdx.y;
-  const long long slot = static_cast<long long>(t) * n_ch + c;
-  const int L = p.valid_lens[t];
-  const int lo = c * chunk;
-  const int hi = bad_len(p, L) ? lo : min(L, lo + chunk);
-  if (hi <= lo) {
-    if (threadIdx.x == 0) cand_count[slot] = 0;
-    return;
-  }
-  BlockSelect<kTopkThreads> sel = make_select(smem_raw, p.top_k);
-  RowSrc src{scores + static_cast<long long>(t) * ld, lo};
-  const int count = sel.run(src, hi - lo, p.top_k);
-  uint64_t *dst = cand + slot * p.top_k;
-  for (int i = threadIdx.x; i < count; i += kTopkThreads) dst[i] = sel.out[i];
-  if (threadIdx.x == 0) cand_count[slot] = count;
-}
-
-// ------------------------------------------------------- stage 2: merge ----
-__global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(ScoreParams p, int n_ch, const uint64_t *cand,
-                                                                  const int32_t *cand_count) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ int warp_tot[kTopkThreads / 32];
-  const int t = blockIdx.x;
-  const int L = p.valid_lens[t];
-  if (bad_len(p, L)) return write_padding(p, t);
-  // chunk offsets (prefix of the counts) live behind the selection's own memory
-  int *seg_off = reinterpret_cast<int *>(smem_raw + select_smem(p.top_k).total);
-  const long long j0 = static_cast<long long>(t) * n_ch;
-  int carry = 0;
-  for (int cb = 0; cb < n_ch; cb += kTopkThreads) {
-    const int j = cb + static_cast<int>(threadIdx.x);
-    int cnt = (j < n_ch) ? cand_count[j0 + j] : 0;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, cnt, o);
-      if (lane_id() >= static_cast<uint32_t>(o)) cnt += v;
-    }
-    if (lane_id() == 31) warp_tot[threadIdx.x >> 5] = cnt;
-    __syncthreads();
-    int before = carry;
-    int all = 0;
-    for (int wi = 0; wi < kTopkThreads / 32; ++wi) {
-      if (wi < static_cast<int>(threadIdx.x >> 5)) before += warp_tot[wi];
-      all += warp_tot[wi];
-    }
-    if (j < n_ch) seg_off[j + 1] = before + cnt;
-    __syncthreads();
-    carry += all;
-  }
-  if (threadIdx.x == 0) seg_off[0] = 0;
+  };
+  warp_phase(0, 32);   // sizes 2 .. 64 entirely in registers
   __syncthreads();
-  BlockSelect<kTopkThreads> sel = make_select(smem_raw, p.top_k);
-  CandSrc src{cand, seg_off, j0, p.top_k, 0};
-  const int count = sel.run(src, seg_off[n_ch], p.top_k);
-  write_sorted(p, t, sel, count);
+  for (int size = 128; size <= m; size <<= 1) {
+    for (int stride = size >> 1; stride >= 64; stride >>= 1) {
+      for (int i = tid; i < (m >> 1); i += kSelThreads) {
+        const int lo = ((i & ~(stride - 1)) << 1) | (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const uint64_t a = out[lo], b = out[hi];
+        if ((a < b) == desc) {
+          out[lo] = b;
+          out[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+    warp_phase(size, 32);
+    __syncthreads();
+  }
+}
+
+template <int C, bool kFromCand, bool kFinal>
+__global__ void __launch_bounds__(kSelThreads, C == 1 ? 3 : 4) topk_cluster_kernel(ScoreParams p, SelArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SelShared *sh = reinterpret_cast<SelShared *>(smem_raw);
+  const SelSmem lay = sel_smem(p.top_k);
+  uint64_t *out = reinterpret_cast<uint64_t *>(smem_raw + lay.out);
+  uint64_t *bnd = reinterpret_cast<uint64_t *>(smem_raw + lay.bnd);
+  const uint32_t r = cl::rank();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = blockIdx.y;
+  const int piece = blockIdx.x / C;
+  const int k = p.top_k;
+
+  // ---- this CTA's keys ----
+  long long n;  // keys of query t at this stage
+  if (kFromCand) {
+    n = a.n_in;
+  } else {
+    const int L = p.valid_lens[t];
+    if (bad_len(p, L)) {  // uniform over the cluster: nobody reaches a cluster barrier
+      if (r == 0) {
+        if (kFinal) {
+          if (tid == 0 && p.dev_status) atomicOr(p.dev_status, IDX_STATUS_BAD_LEN);
+          for (int i = tid; i < k; i += kSelThreads) {
+            p.topk_idx[static_cast<long long>(t) * k + i] = -1;
+            p.topk_score[static_cast<long long>(t) * k + i] = -INFINITY;
+          }
+        } else {
+          if (piece == 0 && tid == 0 && p.dev_status) atomicOr(p.dev_status, IDX_STATUS_BAD_LEN);
+          uint64_t *dst = a.cand_out + (static_cast<long long>(t) * (gridDim.x / C) + piece) * k;
+          for (int i = tid; i < k; i += kSelThreads) dst[i] = 0ull;
+        }
+      }
+      return;
+    }
+    n = L;
+  }
+  const long long lo = static_cast<long long>(piece) * C * kCtaKeys + static_cast<long long>(r) * kCtaKeys;
+  const long long hi = min(n, lo + kCtaKeys);
+  uint64_t key[kSelR];
+#pragma unroll
+  for (int j = 0; j < kSelR; ++j) {
+    const long long i = lo + j * kSelThreads + tid;
+    uint64_t kv = 0ull;
+    if (i < hi) {
+      if (kFromCand) {
+        kv = a.cand_in[static_cast<long long>(t) * a.n_in + i];
+      } else {
+        const float v = a.scores[static_cast<long long>(t) * a.ld + i];
+        kv = (v == -INFINITY) ? 0ull : pack_key(v, static_cast<int32_t>(i));
+      }
+    }
+    key[j] = kv;
+  }
+  if (r == 0 && tid == 0) {
+    sh->n_out = 0;
+    sh->n_bnd = 0;
+  }
+
+  // ---- locate the boundary bin, digit by digit ----
+  constexpr int sl = kBins / C;             // bins per rank
+  constexpr int per = sl / kSelThreads;     // bins per thread (>= 2)
+  const int bin_top = (static_cast<int>(r) + 1) * sl - 1;
+  uint64_t prefix = 0, mask = 0;
+  int need = k, shift = 52, width = 12;
+  bool take_all = false;
+  while (true) {
+    for (int b = tid; b < kBins; b += kSelThreads) sh->hist[b] = 0u;
+    __syncthreads();
+    const uint32_t dmask = (1u << width) - 1u;
+#pragma unroll
+    for (int j = 0; j < kSelR; ++j)
+      if (key[j] != 0ull && (key[j] & mask) == prefix)
+        atomicAdd(&sh->hist[static_cast<uint32_t>(key[j] >> shift) & dmask], 1u);
+    cl::sync();
+    // sum my slice over the cluster; thread tid owns bins bin_top - per*tid - j
+    uint32_t c[per];
+    uint32_t tot = 0;
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      const int b = bin_top - per * tid - j;
+      c[j] = 0u;
+#pragma unroll
+      for (int q = 0; q < C; ++q) c[j] += cl::ld_u32(cl::map(&sh->hist[b], q));
+      tot += c[j];
+    }
+    uint32_t incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) sh->warp_sum[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0, slice = 0;
+#pragma unroll
+    for (int w = 0; w < kSelThreads / 32; ++w) {
+      const uint32_t s = sh->warp_sum[w];
+      if (w < warp) before += s;
+      slice += s;
+    }
+    if (tid < C) cl::st_u32(cl::map(&sh->slice_tot[r], tid), slice);
+    cl::sync();
+    uint32_t above = 0, all = 0;
+#pragma unroll
+    for (int q = 0; q < C; ++q) {
+      const uint32_t s = sh->slice_tot[q];
+      if (q > static_cast<int>(r)) above += s;
+      all += s;
+    }
+    if (all <= static_cast<uint32_t>(need)) {
+      take_all = true;  // every key matching the prefix is selected (same decision in every CTA)
+      break;
+    }
+    uint32_t run = above + before + incl - tot;
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      if (run < static_cast<uint32_t>(need) && run + c[j] >= static_cast<uint32_t>(need)) {
+        const int b = bin_top - per * tid - j;
+        for (int q = 0; q < C; ++q) {
+          cl::st_u32(cl::map(&sh->b_bin, q), static_cast<uint32_t>(b));
+          cl::st_u32(cl::map(&sh->b_above, q), run);
+          cl::st_u32(cl::map(&sh->b_cnt, q), c[j]);
+        }
+      }
+      run += c[j];
+    }
+    cl::sync();
+    const int bin = sh->b_bin, cnt = sh->b_cnt;
+    prefix |= static_cast<uint64_t>(bin) << shift;
+    mask |= static_cast<uint64_t>(dmask) << shift;
+    if (cnt <= kBndCap || shift == 0) break;
+    need -= sh->b_above;
+    // digits: bits 63..52, 51..40, 39..28, 27..16, 15..4, then 3..0
+    if (shift >= 12) {
+      shift -= 12;
+      width = 12;
+    } else {
+      width = shift;
+      shift = 0;
+    }
+    // the histogram is cleared next round: every CTA has finished reading it
+    // (the reads precede the barrier just passed)
+  }
+
+  // ---- collect into CTA 0: keys above the boundary to out, inside it to bnd ----
+  const uint32_t out_base = cl::map(out, 0), bnd_base = cl::map(bnd, 0);
+  const uint32_t nout_a = cl::map(&sh->n_out, 0), nbnd_a = cl::map(&sh->n_bnd, 0);
+#pragma unroll
+  for (int j = 0; j < kSelR; ++j) {
+    const uint64_t mk = key[j] & mask;
+    const bool up = key[j] != 0ull && (take_all ? mk >= prefix : mk > prefix);
+    const bool eq = key[j] != 0ull && !take_all && mk == prefix;
+    const uint32_t mu = __ballot_sync(0xFFFFFFFFu, up), me = __ballot_sync(0xFFFFFFFFu, eq);
+    uint32_t bu = 0, be = 0;
+    if (lane == 0) {
+      if (mu) bu = cl::atom_add(nout_a, __popc(mu));
+      if (me) be = cl::atom_add(nbnd_a, __popc(me));
+    }
+    bu = __shfl_sync(0xFFFFFFFFu, bu, 0);
+    be = __shfl_sync(0xFFFFFFFFu, be, 0);
+    const uint32_t below = lanemask_lt();
+    if (up) cl::st_u64(out_base + 8u * (bu + __popc(mu & below)), key[j]);
+    if (eq) cl::st_u64(bnd_base + 8u * (be + __popc(me & below)), key[j]);
+  }
+  cl::sync();
+  if (r != 0) return;  // nothing touches this CTA's shared memory any more
+
+  // ---- CTA 0: finish the boundary bin, then sort / write ----
+  int count = sh->n_out;
+  if (!take_all) {
+    const int nb = sh->n_bnd;
+    const int want = k - count;  // 1 .. nb
+    TopkGroup<kSelThreads> g{&sh->tsh, bnd, tid, 1};
+    if (tid == 0) sh->tsh.count = nb;
+    __syncthreads();
+    g.compact(want);  // keeps the `want` largest boundary keys in bnd[0 .. want)
+    for (int i = tid; i < want; i += kSelThreads) out[count + i] = bnd[i];
+    count += want;
+  }
+  if (kFinal) {
+    const int m = max(64, pow2_at_least(count));
+    for (int i = count + tid; i < m; i += kSelThreads) out[i] = 0ull;
+    __syncthreads();
+    sort_desc(out, m);
+    int32_t *oi = p.topk_idx + static_cast<long long>(t) * k;
+    float *os = p.topk_score + static_cast<long long>(t) * k;
+    for (int i = tid; i < k; i += kSelThreads) {
+      if (i < count) {
+        const uint64_t kv = out[i];
+        oi[i] = key_index(kv);
+        os[i] = key_score(kv);
+      } else {
+        oi[i] = -1;
+        os[i] = -INFINITY;
+      }
+    }
+  } else {
+    __syncthreads();
+    uint64_t *dst = a.cand_out + (static_cast<long long>(t) * (gridDim.x / C) + piece) * k;
+    for (int i = tid; i < k; i += kSelThreads) dst[i] = (i < count) ? out[i] : 0ull;
+  }
+}
+
+template <int C, bool kFromCand, bool kFinal>
+cudaError_t launch_stage_c(const ScoreParams &p, const SelArgs &a, int pieces, size_t smem, cudaStream_t stream) {
+  auto fn = topk_cluster_kernel<C, kFromCand, kFinal>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(C * pieces), static_cast<unsigned>(p.T), 1);
+  cfg.blockDim = dim3(kSelThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, p, a);
+}
+
+template <bool kFromCand, bool kFinal>
+cudaError_t launch_stage(const ScoreParams &p, const SelArgs &a, int C, int pieces, size_t smem,
+                         cudaStream_t stream) {
+  switch (C) {
+    case 1: return launch_stage_c<1, kFromCand, kFinal>(p, a, pieces, smem, stream);
+    case 2: return launch_stage_c<2, kFromCand, kFinal>(p, a, pieces, smem, stream);
+    case 4: return launch_stage_c<4, kFromCand, kFinal>(p, a, pieces, smem, stream);
+    case 8: return launch_stage_c<8, kFromCand, kFinal>(p, a, pieces, smem, stream);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
+
+// Stage shape for n keys per query: cluster size and number of pieces.
+// The cluster size is a power of two so that it divides the 4096 bins.
+void stage_shape(long long n, int *C, long long *pieces) {
+  long long c = 1;
+  while (c < kMaxCluster && c * kCtaKeys < n) c <<= 1;
+  *C = static_cast<int>(c);
+  long long pc = (n + c * kCtaKeys - 1) / (c * kCtaKeys);
+  *pieces = pc < 1 ? 1 : pc;
 }
 
 }  // namespace
 
 SelectPlan select_plan(int T, int top_k, long long max_len, bool have_scores_out, long long ld_out) {
   SelectPlan pl{};
-  const int kp = pow2_at_least(top_k);
-  long long chunk = 16LL * kp;
-  if (chunk < 4096) chunk = 4096;
-  pl.chunk = static_cast<int>(chunk);
-  pl.two_stage = max_len > chunk;
-  pl.n_ch = pl.two_stage ? static_cast<int>((max_len + chunk - 1) / chunk) : 0;
   pl.own_scores = !have_scores_out;
   pl.ld = have_scores_out ? ld_out : max_len;
+  long long n = max_len;
+  long long biggest[2] = {0, 0};  // largest candidate list sizes (keys per query) of even / odd stages
+  pl.n_stages = 0;
+  while (pl.n_stages < kMaxSelectStages) {
+    int C;
+    long long pieces;
+    stage_shape(n, &C, &pieces);
+    pl.C[pl.n_stages] = C;
+    pl.pieces[pl.n_stages] = static_cast<int>(pieces);
+    pl.n_in[pl.n_stages] = n;
+    ++pl.n_stages;
+    if (pieces == 1) break;
+    n = pieces * top_k;
+    long long &b = biggest[(pl.n_stages - 1) & 1];
+    if (n > b) b = n;
+  }
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = 0;
   pl.scores_off = off;
   if (pl.own_scores) off = al(off + static_cast<size_t>(T) * static_cast<size_t>(max_len) * 4);
-  pl.count_off = off;
-  if (pl.two_stage) off = al(off + static_cast<size_t>(T) * pl.n_ch * 4);
-  pl.cand_off = off;
-  if (pl.two_stage) off = al(off + static_cast<size_t>(T) * pl.n_ch * top_k * 8);
+  for (int i = 0; i < 2; ++i) {
+    pl.cand_off[i] = off;
+    off = al(off + static_cast<size_t>(T) * static_cast<size_t>(biggest[i]) * 8);
+  }
   pl.total = off;
   return pl;
 }
 
 bool select_supported(int top_k, long long max_len) {
-  const long long chunk = 16LL * pow2_at_least(top_k) < 4096 ? 4096 : 16LL * pow2_at_least(top_k);
-  const long long n_ch = max_len > chunk ? (max_len + chunk - 1) / chunk : 0;
-  const size_t merge_smem = select_smem(top_k).total + static_cast<size_t>(n_ch + 1) * 4;
-  return merge_smem <= 227 * 1024;
+  SelectPlan pl = select_plan(1, top_k, max_len, true, max_len);
+  int C;
+  long long pieces;
+  stage_shape(pl.n_in[pl.n_stages - 1], &C, &pieces);
+  return pieces == 1 && sel_smem(top_k).total <= 227 * 1024;
 }
 
 cudaError_t launch_select(const ScoreParams &p, const float *scores, long long ld, const SelectPlan &pl,
                           void *workspace, cudaStream_t stream) {
   if (p.T == 0) return cudaSuccess;
-  cudaError_t e;
-  const size_t smem = select_smem(p.top_k).total;
-  if (!pl.two_stage) {
-    if ((e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(smem))) != cudaSuccess)
-      return e;
-    topk_rows_kernel<<<p.T, kTopkThreads, smem, stream>>>(p, scores, ld);
-    return cudaGetLastError();
-  }
+  const size_t smem = sel_smem(p.top_k).total;
   unsigned char *base = static_cast<unsigned char *>(workspace);
-  uint64_t *cand = reinterpret_cast<uint64_t *>(base + pl.cand_off);
-  int32_t *count = reinterpret_cast<int32_t *>(base + pl.count_off);
-  if ((e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem))) != cudaSuccess)
-    return e;
-  topk_chunk_kernel<<<dim3(pl.n_ch, p.T), kTopkThreads, smem, stream>>>(p, scores, ld, pl.chunk, pl.n_ch, cand,
-                                                                      count);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t smem2 = smem + static_cast<size_t>(pl.n_ch + 1) * 4;
-  if ((e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem2))) != cudaSuccess)
-    return e;
-  topk_merge_kernel<<<p.T, kTopkThreads, smem2, stream>>>(p, pl.n_ch, cand, count);
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  for (int s = 0; s < pl.n_stages && e == cudaSuccess; ++s) {
+    SelArgs a{};
+    a.scores = scores;
+    a.ld = ld;
+    a.n_in = pl.n_in[s];
+    if (s > 0) a.cand_in = reinterpret_cast<const uint64_t *>(base + pl.cand_off[(s - 1) & 1]);
+    const bool final = (s == pl.n_stages - 1);
+    if (!final) a.cand_out = reinterpret_cast<uint64_t *>(base + pl.cand_off[s & 1]);
+    if (s == 0 && final) e = launch_stage<false, true>(p, a, pl.C[s], pl.pieces[s], smem, stream);
+    else if (s == 0) e = launch_stage<false, false>(p, a, pl.C[s], pl.pieces[s], smem, stream);
+    else if (final) e = launch_stage<true, true>(p, a, pl.C[s], pl.pieces[s], smem, stream);
+    else e = launch_stage<true, false>(p, a, pl.C[s], pl.pieces[s], smem, stream);
+  }
+  return e;
 }
 
 }  // namespace idx
