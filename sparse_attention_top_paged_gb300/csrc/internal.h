@@ -57,7 +57,9 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
                           void *workspace, cudaStream_t stream);
 // score_tc.cu
 bool score_tc_supported(const ScoreParams &p);
-cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, float *scores, long long ld, cudaStream_t stream);
+size_t score_tc_workspace(const ScoreParams &p);  // per-query q records (bytes)
+cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, float *scores, long long ld,
+                            cudaStream_t stream);
 // gather_pool.cu
 cudaError_t launch_gather_kv(const idx_gather_kv_args &a, cudaStream_t stream);
 cudaError_t launch_block_pool(const uint16_t *raw, const float *w, float *out, uint32_t first_block,

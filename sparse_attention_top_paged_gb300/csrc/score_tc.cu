@@ -1,14 +1,19 @@
-// score_tc.cu — tensor-core (tcgen05) lightning-indexer scorer with fused
-// per-segment top-k.
+// score_tc.cu — tensor-core (tcgen05) lightning-indexer scorer.
 //
 // What it computes: eq. 16 of "indexer_score_topk.cu" (nvfp4-megamoe-kernel,
 // dsv4/kernels/indexer), I[t,s] = sum_h w[t,h] * ReLU(q[t,h] . K[s]), over NVFP4
 // keys resolved through the block table, written to a [T, ld] score matrix;
 // the selection kernels in topk.cu then take TopK(I[t,:], k).
 // That page's kernel runs one CTA per query with scalar FP32 dot products and
-// a locked shared heap; this one is a persistent, warp-specialised tcgen05
-// pipeline:
+// a locked shared heap; here two kernels run back to back (the second may
+// start before the first ends):
 //
+// qprep_kernel turns each q[t] into the MMA's B operand once, as a record in
+// global memory: per head a power-of-two scale 2^sigma, f16 hi and lo parts
+// (the lo part only feeds the MMA when some q value is not exact in f16, e.g.
+// bf16-valued q never needs it), w' = w 2^-sigma and the lo flags.
+//
+// score_tc_kernel is a persistent, warp-specialised pipeline:
 //   work     The tiles of 128 consecutive keys of every query, laid end to end,
 //            are split evenly over the CTAs (one per SM). A "segment" is a
 //            CTA's run of tiles of one query (it shares one B operand).
@@ -17,14 +22,11 @@
 //            records, so no dependent global load sits on the copy path.
 //   warp 0   producer: streams each tile's packed E2M1 nibbles (2-D TMA,
 //            64-byte swizzle) and E4M3 scales (1-D bulk copy) into a ring of
-//            shared-memory stages.
+//            shared-memory stages, and at each segment start copies the
+//            query's q record into one of two segment slots.
 //   warps 2-5 decoders: one thread per key row decodes 128 elements
 //            e2m1 * e4m3 exactly into f16 (hardware converts) and stores them
-//            to tensor memory as the MMA's A operand. At each segment start
-//            they also turn q[t] into the B operand: per head a power-of-two
-//            scale 2^sigma, then f16 hi and lo parts (the lo part only feeds
-//            the MMA when some q value is not exact in f16, e.g. bf16-valued q
-//            never needs it).
+//            to tensor memory as the MMA's A operand.
 //   warp 1   MMA issuer: D[128 keys x Npad heads] = A * B^T in f32, K = 128, as
 //            8 (or 16 with the lo part) tcgen05.mma kind::f16 steps.
 //   warps 6-9 epilogue: one thread per key reads its accumulator row from
@@ -68,13 +70,20 @@ struct MetaEntry {
   int lb0;        // first logical block of the tile
   int s0;         // first key of the tile
   int nblk;       // blocks the tile touches (up to its last valid key)
-  int pad_[12];
+  int t;          // the tile's query
+  int seg;        // 1: first tile of a segment (the producer brings in q[t]'s B operand)
+  int pad_[10];
 };
 static_assert(sizeof(MetaEntry) == 128, "meta entry");
 
+// Per-query B-operand record, written by qprep_kernel to global memory and
+// copied verbatim into a shared-memory segment slot: f16 hi rows, f16 lo rows
+// (each Npad heads x 128 dims, K-major, 128-byte swizzled), w' (Npad floats),
+// lo flags (Npad ints).
 struct TcLayout {
   int Npad, nseg, na, nd, ns, box_rows, bpt, epb_shift;
-  uint32_t off_b, b_bytes, off_raw, off_w, off_flags, off_meta, off_bar, off_misc;
+  uint32_t b_bytes, rec_w, rec_flags, rec_bytes, rec_smem;
+  uint32_t off_b, off_raw, off_meta, off_bar, off_misc;
   uint32_t smem_bytes;
 };
 
@@ -152,9 +161,62 @@ __device__ long long block_incl_scan(long long v, long long *scratch, long long 
   return before + x;
 }
 
+// q[t] -> the B-operand record of query t: one warp per head, 4 dims per lane.
+// Per head a power-of-two scale 2^sigma puts the largest |q| in [2^14, 2^15)
+// (sigma from the exponent field; subnormal or zero heads keep sigma 0;
+// clamped so 2^sigma and 2^-sigma are normal floats); the scaled values are
+// split into f16 hi + lo (lo = 0 whenever q is exact in f16 after scaling,
+// e.g. for bf16-valued q) and w' = w 2^-sigma undoes the scale after the ReLU.
+__global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay, uint8_t *__restrict__ rec) {
+  ptx::launch_dependents();  // the scorer may start its prologue meanwhile
+  const int t = blockIdx.x;
+  const int h = blockIdx.y * 8 + static_cast<int>(threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (h >= lay.Npad) return;
+  uint8_t *r = rec + static_cast<size_t>(t) * lay.rec_bytes;
+  float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wv = 0.0f;
+  if (h < p.H) {
+    x = reinterpret_cast<const float4 *>(p.q + (static_cast<long long>(t) * p.H + h) * 128)[lane];
+    wv = p.w[static_cast<long long>(t) * p.H + h];
+  }
+  float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  const int sigma = (ex == 0) ? 0 : max(-126, min(126, 141 - ex));
+  const float up = __uint_as_float(static_cast<uint32_t>(127 + sigma) << 23);
+  const float down = __uint_as_float(static_cast<uint32_t>(127 - sigma) << 23);
+  const float xs[4] = {x.x * up, x.y * up, x.z * up, x.w * up};
+  __half hi[4], lo[4];
+  bool any_lo = false;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    hi[e] = __float2half_rn(xs[e]);
+    lo[e] = __float2half_rn(xs[e] - __half2float(hi[e]));
+    any_lo |= (__half2float(lo[e]) != 0.0f);
+  }
+  // dims 4*lane .. 4*lane+3: K block kb = lane / 16 (64 dims each), 16-byte
+  // chunk jj = (lane / 2) % 8 of the head's 128-byte row, swizzled by h % 8
+  const int ch = lane >> 1, kb = ch >> 3, jj = ch & 7;
+  const uint32_t off = kb * (lay.Npad * 128) + h * 128 + ((jj ^ (h & 7)) * 16) + (lane & 1) * 8;
+  uint2 vh, vl;
+  vh.x = static_cast<uint32_t>(__half_as_ushort(hi[0])) | (static_cast<uint32_t>(__half_as_ushort(hi[1])) << 16);
+  vh.y = static_cast<uint32_t>(__half_as_ushort(hi[2])) | (static_cast<uint32_t>(__half_as_ushort(hi[3])) << 16);
+  vl.x = static_cast<uint32_t>(__half_as_ushort(lo[0])) | (static_cast<uint32_t>(__half_as_ushort(lo[1])) << 16);
+  vl.y = static_cast<uint32_t>(__half_as_ushort(lo[2])) | (static_cast<uint32_t>(__half_as_ushort(lo[3])) << 16);
+  *reinterpret_cast<uint2 *>(r + off) = vh;
+  *reinterpret_cast<uint2 *>(r + lay.b_bytes + off) = vl;
+  const bool warp_lo = __any_sync(0xFFFFFFFFu, any_lo);
+  if (lane == 0) {
+    reinterpret_cast<float *>(r + lay.rec_w)[h] = wv * down;
+    reinterpret_cast<int *>(r + lay.rec_flags)[h] = warp_lo ? 1 : 0;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmap_nib, ScoreParams p, TcLayout lay,
-                    float *__restrict__ scores, long long ld) {
+                    const uint8_t *__restrict__ qrec, float *__restrict__ scores, long long ld) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -164,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
 
   if (threadIdx.x == 0) {
+    ptx::launch_dependents();  // the selection kernel may be scheduled as CTAs of this one finish
     for (int s = 0; s < lay.ns; ++s) {
       ptx::mbar_init(bar(B_FULL_RAW + s), 1);
       ptx::mbar_init(bar(B_EMPTY_RAW + s), 4);
@@ -175,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(B_EMPTY_D + a), 4);
     }
     for (int a = 0; a < 2; ++a) {
-      ptx::mbar_init(bar(B_SEG_FULL + a), 4);
+      ptx::mbar_init(bar(B_SEG_FULL + a), 1);   // producer (record copy)
       ptx::mbar_init(bar(B_SEG_BFREE + a), 1);
       ptx::mbar_init(bar(B_SEG_WFREE + a), 4);  // one arrive per epilogue warp
     }
@@ -232,8 +295,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_bytes = lay.b_bytes;
   uint8_t *sB = sm + lay.off_b;
   uint8_t *sRaw = sm + lay.off_raw;
-  float *sW = reinterpret_cast<float *>(sm + lay.off_w);
-  int *sFlags = reinterpret_cast<int *>(sm + lay.off_flags);
   MetaEntry *sMeta = reinterpret_cast<MetaEntry *>(sm + lay.off_meta);
   const uint32_t tmem_a = tmem;                                  // A slots: 64 columns each
   const uint32_t tmem_d = tmem + 64u * static_cast<uint32_t>(na);  // D slots: Npad columns each
@@ -241,14 +302,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ================================================================ producer
     if (lane == 0) {
-      int issued = 0;
-      Ring raw, meta;
+      int issued = 0, segs = 0;
+      Ring raw, meta, rs;
       const int ns = lay.ns;
+      bool qrec_ready = false;
       for (int i = 0; i < n_tiles; ++i, raw.next(ns), meta.next(kR)) {
         const int s = raw.idx, r = meta.idx;
         if (!ptx::mbar_wait(bar(B_EMPTY_RAW + s), raw.phase ^ 1u, abort_flag, kTimeoutNs)) break;
         if (!ptx::mbar_wait(bar(B_META_FULL + r), meta.phase, abort_flag, kTimeoutNs)) break;
         const MetaEntry &m = sMeta[r];
+        if (m.seg) {
+          // First tile of a segment: copy q[t]'s B-operand record into the next
+          // segment slot once its previous segment is done with it.
+          if (segs > 0) rs.next(nseg);
+          const int ss = rs.idx;
+          if (!ptx::mbar_wait(bar(B_SEG_BFREE + ss), rs.phase ^ 1u, abort_flag, kTimeoutNs)) break;
+          if (!ptx::mbar_wait(bar(B_SEG_WFREE + ss), rs.phase ^ 1u, abort_flag, kTimeoutNs)) break;
+          if (!qrec_ready) {
+            ptx::wait_prior_grid();  // the records are written by the kernel launched just before
+            qrec_ready = true;
+          }
+          const uint32_t sfull = bar(B_SEG_FULL + ss);
+          ptx::mbar_arrive_expect_tx(sfull, lay.rec_bytes);
+          ptx::bulk_g2s(ptx::smem_addr(sB + ss * lay.rec_smem), qrec + static_cast<size_t>(m.t) * lay.rec_bytes,
+                        lay.rec_bytes, sfull);
+          ++segs;
+        }
         const uint32_t mask = m.mask;
         const int s0 = m.s0, lb0 = m.lb0, nblk = m.nblk;
         uint32_t bytes = 0;
@@ -284,11 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++issued;
       }
-      // never leave with copies in flight
-      for (int i = (issued > ns ? issued - ns : 0); i < issued; ++i) {
-        volatile int no_abort = 0;
+      // never leave with copies in flight: the last ns tile stages and the
+      // last segment record (an earlier one was waited for before its slot's reuse)
+      volatile int no_abort = 0;
+      for (int i = (issued > ns ? issued - ns : 0); i < issued; ++i)
         ptx::mbar_wait(bar(B_FULL_RAW + i % ns), static_cast<uint32_t>(i / ns) & 1u, &no_abort, kTimeoutNs);
-      }
+      if (segs > 0) ptx::mbar_wait(bar(B_SEG_FULL + rs.idx), rs.phase, &no_abort, kTimeoutNs);
     }
   } else if (warp == 1) {
     // ============================================================ MMA issuer
@@ -311,9 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i > 0) rs.next(nseg); else rs.idx = 0;
         ss = rs.idx;
         ok = ptx::mbar_wait(bar(B_SEG_FULL + ss), rs.phase, abort_flag, kTimeoutNs);
-        need_lo = (sFlags[ss * 4 + 0] | sFlags[ss * 4 + 1] | sFlags[ss * 4 + 2] | sFlags[ss * 4 + 3]) != 0;
-        const uint32_t bh = ptx::smem_addr(sB + (ss * 2 + 0) * b_bytes);
-        const uint32_t bl = ptx::smem_addr(sB + (ss * 2 + 1) * b_bytes);
+        const uint8_t *slot = sB + ss * lay.rec_smem;
+        const int *flags = reinterpret_cast<const int *>(slot + lay.rec_flags);
+        int f = 0;
+        for (int h = lane; h < Npad; h += 32) f |= flags[h];
+        need_lo = __any_sync(0xFFFFFFFFu, f != 0);
+        const uint32_t bh = ptx::smem_addr(slot);
+        const uint32_t bl = ptx::smem_addr(slot + b_bytes);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t boff = (k >> 2) * (Npad * 128) + (k & 3) * 32;
@@ -342,81 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 6) {
     // ============================================================== decoders
-    const int dw = warp - 2;                   // 0..3: which heads this warp converts
-    const int row = 32 * (warp & 3) + lane;    // the TMEM lane this thread may write
+    const int row = 32 * (warp & 3) + lane;    // the TMEM lane this thread writes
     const int rsw = (row >> 1) & 3;            // 64-byte swizzle of this row's chunks
-    Walker w;
-    w.init(p, t0, j0);
-    Ring rraw, ra, rs;
-    for (int i = 0; i < n_tiles; ++i, w.next(p), rraw.next(lay.ns), ra.next(na)) {
-      const bool seg_start = (i == 0) || (w.j == 0);
-      if (seg_start) {
-        if (i > 0) rs.next(nseg);
-        const int ss = rs.idx;
-        {  // the slot's previous segment must be done with its B operand (MMA) and w' (epilogue)
-          bool ok = ptx::mbar_wait(bar(B_SEG_BFREE + ss), rs.phase ^ 1u, abort_flag, kTimeoutNs);
-          ok = ok && ptx::mbar_wait(bar(B_SEG_WFREE + ss), rs.phase ^ 1u, abort_flag, kTimeoutNs);
-          if (!__all_sync(0xFFFFFFFFu, ok)) break;  // warp-uniform exit before any .aligned op
-        }
-        // q[t] -> B operand (f16 hi / lo, 128-byte swizzled, K-major) and w' = w 2^-sigma
-        uint8_t *bh = sB + (ss * 2 + 0) * b_bytes;
-        uint8_t *bl = sB + (ss * 2 + 1) * b_bytes;
-        bool any_lo = false;
-        constexpr int kQChunk = 8;  // heads per chunk: their loads are all in flight at once
-        for (int h0 = dw; h0 < Npad; h0 += 4 * kQChunk) {
-          float4 xq[kQChunk];
-          float wq[kQChunk], down[kQChunk];
-#pragma unroll
-          for (int c = 0; c < kQChunk; ++c) {
-            const int h = h0 + 4 * c;
-            xq[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-            wq[c] = 0.0f;
-            if (h < p.H) {
-              xq[c] = reinterpret_cast<const float4 *>(p.q + (static_cast<long long>(w.t) * p.H + h) * 128)[lane];
-              if (lane == 0) wq[c] = p.w[static_cast<long long>(w.t) * p.H + h];
-            }
-          }
-#pragma unroll
-          for (int c = 0; c < kQChunk; ++c) {
-            const int h = h0 + 4 * c;
-            if (h >= Npad) break;
-            const float4 x = xq[c];
-            float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-            // sigma puts the head's largest |q| in [2^14, 2^15): 2^sigma from the
-            // exponent field (amax normal; subnormal or zero heads keep sigma 0),
-            // clamped so 2^sigma and 2^-sigma are both normal floats.
-            const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-            const int sigma = (ex == 0) ? 0 : max(-126, min(126, 141 - ex));
-            const float up = __uint_as_float(static_cast<uint32_t>(127 + sigma) << 23);
-            down[c] = __uint_as_float(static_cast<uint32_t>(127 - sigma) << 23);
-            const float xs[4] = {x.x * up, x.y * up, x.z * up, x.w * up};
-            __half hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              hi[e] = __float2half_rn(xs[e]);
-              lo[e] = __float2half_rn(xs[e] - __half2float(hi[e]));
-              any_lo |= (__half2float(lo[e]) != 0.0f);
-            }
-            const int ch = lane >> 1, kb = ch >> 3, jj = ch & 7;
-            const uint32_t off = kb * (Npad * 128) + h * 128 + ((jj ^ (h & 7)) * 16) + (lane & 1) * 8;
-            uint2 vh, vl;
-            vh.x = static_cast<uint32_t>(__half_as_ushort(hi[0])) | (static_cast<uint32_t>(__half_as_ushort(hi[1])) << 16);
-            vh.y = static_cast<uint32_t>(__half_as_ushort(hi[2])) | (static_cast<uint32_t>(__half_as_ushort(hi[3])) << 16);
-            vl.x = static_cast<uint32_t>(__half_as_ushort(lo[0])) | (static_cast<uint32_t>(__half_as_ushort(lo[1])) << 16);
-            vl.y = static_cast<uint32_t>(__half_as_ushort(lo[2])) | (static_cast<uint32_t>(__half_as_ushort(lo[3])) << 16);
-            *reinterpret_cast<uint2 *>(bh + off) = vh;
-            *reinterpret_cast<uint2 *>(bl + off) = vl;
-            if (lane == 0) sW[ss * 256 + h] = (h < p.H) ? wq[c] * down[c] : 0.0f;
-          }
-        }
-        const bool warp_lo = __any_sync(0xFFFFFFFFu, any_lo);
-        if (lane == 0) sFlags[ss * 4 + dw] = warp_lo ? 1 : 0;
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(B_SEG_FULL + ss));
-      }
+    Ring rraw, ra;
+    for (int i = 0; i < n_tiles; ++i, rraw.next(lay.ns), ra.next(na)) {
       const int s = rraw.idx, a = ra.idx;
       bool ok = ptx::mbar_wait(bar(B_FULL_RAW + s), rraw.phase, abort_flag, kTimeoutNs);
       ok = ok && ptx::mbar_wait(bar(B_EMPTY_A + a), ra.phase ^ 1u, abort_flag, kTimeoutNs);
@@ -463,19 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int d = lane / bpt, b = lane % bpt;
     Walker w;
     w.init(p, t0, j0);
-    int prefetched_t = -1;
     for (int base = 0; base < n_tiles; base += tpb) {
-      // The decoders turn q[t] into the MMA's B operand at each segment start;
-      // pull the rows of every query this batch reaches into L2 ahead of them.
-      if (lane == 0) {
-        Walker wp = w;
-        for (int x = 0; x < tpb && base + x < n_tiles; ++x, wp.next(p)) {
-          if (wp.t != prefetched_t) {
-            prefetched_t = wp.t;
-            ptx::bulk_prefetch_l2(p.q + static_cast<long long>(wp.t) * p.H * 128, static_cast<uint32_t>(p.H) * 512u);
-          }
-        }
-      }
       const int i = base + d;
       const bool tile_ok = i < n_tiles;
       Walker wl = w;
@@ -514,6 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         m.lb0 = lb0;
         m.s0 = s0;
         m.nblk = nblk;
+        m.t = wl.t;
+        m.seg = (i == 0 || wl.j == 0) ? 1 : 0;
       }
       __syncwarp();
       if (tile_ok && b == 0) ptx::mbar_arrive(bar(B_META_FULL + r));
@@ -546,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool in_len = s_key < L;
       const bool valid = in_len && b < kMaxBlocksPerTile && ((sMeta[r].mask >> b) & 1u);
       const float g = (b < kMaxBlocksPerTile) ? sMeta[r].g[b] : 0.0f;
-      const uint64_t *wv2 = reinterpret_cast<const uint64_t *>(sW + ss * 256);  // (w'_h, w'_h+1) pairs
+      const uint64_t *wv2 = reinterpret_cast<const uint64_t *>(sB + ss * lay.rec_smem + lay.rec_w);  // (w'_h, w'_h+1)
       uint64_t acc2[2] = {0ull, 0ull};                                          // two independent chains
       const uint32_t taddr = tmem_d + d * Npad + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
       for (int c0 = 0; c0 < Npad; c0 += 64) {
@@ -640,13 +643,16 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   l.bpt = p.epb < 128 ? 128 / p.epb : 1;
   l.epb_shift = 0;
   while ((1 << l.epb_shift) < p.epb) ++l.epb_shift;
-  // B operands first (multiples of 8 KB), then the raw stages (1 KB-aligned,
-  // as many as fit), then the small tables.
+  // B-operand records first (1 KB-aligned slots), then the raw stages (1 KB
+  // multiples, as many as fit), then the small tables.
   l.b_bytes = static_cast<uint32_t>(l.Npad) * 256u;
+  l.rec_w = 2u * l.b_bytes;
+  l.rec_flags = l.rec_w + static_cast<uint32_t>(l.Npad) * 4u;
+  l.rec_bytes = (l.rec_flags + static_cast<uint32_t>(l.Npad) * 4u + 127u) & ~127u;
+  l.rec_smem = (l.rec_bytes + 1023u) & ~1023u;
   l.off_b = 0;
-  const uint32_t b_total = static_cast<uint32_t>(l.nseg) * 2u * l.b_bytes;
-  const uint32_t tail = static_cast<uint32_t>(l.nseg) * 256u * 4u + 64 + kR * sizeof(MetaEntry) +
-                        ((B_COUNT * 8 + 15) & ~15u) + ((8 * 4 + 16 * 8 + 15) & ~15u);
+  const uint32_t b_total = static_cast<uint32_t>(l.nseg) * l.rec_smem;
+  const uint32_t tail = kR * sizeof(MetaEntry) + ((B_COUNT * 8 + 15) & ~15u) + ((8 * 4 + 16 * 8 + 15) & ~15u);
   const long long room = static_cast<long long>(kSmemLimit) - 1024 - b_total - tail;
   long long ns = room / kStageBytes;
   if (ns > kMaxNS) ns = kMaxNS;
@@ -655,10 +661,6 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   uint32_t off = b_total;
   l.off_raw = off;
   off += static_cast<uint32_t>(l.ns) * kStageBytes;
-  l.off_w = off;
-  off += static_cast<uint32_t>(l.nseg) * 256u * 4u;
-  l.off_flags = off;
-  off += 64;
   l.off_meta = off;
   off += kR * sizeof(MetaEntry);
   l.off_bar = off;
@@ -680,7 +682,14 @@ bool score_tc_supported(const ScoreParams &p) {
   return p.D == 128 && p.keys_fp4 != nullptr && make_layout(p, &l) && get_encode() != nullptr;
 }
 
-cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, float *scores, long long ld, cudaStream_t stream) {
+size_t score_tc_workspace(const ScoreParams &p) {
+  TcLayout lay;
+  if (!make_layout(p, &lay)) return 0;
+  return static_cast<size_t>(p.T) * lay.rec_bytes;
+}
+
+cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, float *scores, long long ld,
+                            cudaStream_t stream) {
   TcLayout lay;
   if (!make_layout(p, &lay)) return cudaErrorNotSupported;
   auto encode = get_encode();
@@ -697,8 +706,22 @@ cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, float *scores, l
   cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(lay.smem_bytes));
   if (e != cudaSuccess) return e;
-  score_tc_kernel<<<num_ctas, kThreads, lay.smem_bytes, stream>>>(tmap, p, lay, scores, ld);
-  return cudaGetLastError();
+  uint8_t *rec = static_cast<uint8_t *>(qrec);
+  qprep_kernel<<<dim3(static_cast<unsigned>(p.T), static_cast<unsigned>(lay.Npad / 8)), 256, 0, stream>>>(p, lay, rec);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // The scorer may launch while qprep_kernel runs: its producer waits for the
+  // records (griddepcontrol.wait) only before the first record copy.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_ctas), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = lay.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, score_tc_kernel, tmap, p, lay, static_cast<const uint8_t *>(rec), scores, ld);
 }
 
 }  // namespace idx

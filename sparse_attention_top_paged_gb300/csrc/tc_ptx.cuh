@@ -67,6 +67,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// Lets the next kernel on the stream (launched with programmatic stream
+// serialization) begin before this one ends.
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the preceding kernel on the stream has completed and its memory
+// operations are visible (returns at once without a programmatic dependency).
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ TMA ----
 // 1-D bulk copy global -> shared, completing `bytes` transactions on `bar`.
 // dst and src 16-byte aligned, bytes a multiple of 16.

@@ -16,9 +16,9 @@
 //   3. the CTA whose slice holds the k-th key locates that bin and publishes
 //      it; if the bin holds more keys than the boundary buffer, the keys in it
 //      are histogrammed again on the next 12 bits (still from registers);
-//   4. every CTA appends its keys above the boundary bin, and those inside it,
-//      to buffers in CTA 0 (distributed shared-memory atomics); CTA 0 then
-//      radix-selects the missing keys from the boundary bin and sorts.
+//   4. every CTA appends its keys at or above the boundary bin to a buffer in
+//      CTA 0 (one distributed shared-memory atomic per warp); CTA 0 sorts the
+//      buffer (bitonic, short strides in registers) and keeps the first k.
 // A query longer than one cluster's reach is split into pieces whose k best
 // keys go to a candidate list; the next launch selects from those lists the
 // same way (each stage shrinks a query's keys at least 8-fold).
@@ -92,21 +92,20 @@ struct SelShared {
   uint32_t slice_tot[kMaxCluster];    // per rank: keys in its slice of bins
   uint32_t warp_sum[kSelThreads / 32];
   int b_bin, b_above, b_cnt;          // boundary bin, published by its owner
-  int n_out, n_bnd;                   // CTA 0: append cursors
-  TopkShared tsh;                     // CTA 0: exact select of the boundary bin
+  int n_buf;                          // CTA 0: append cursor
 };
 
-// Dynamic shared memory: SelShared, then out (a power of two >= max(k, 64)
-// keys: the sort works on whole warps' 64-key segments), then the boundary
-// buffer.
+// Dynamic shared memory: SelShared, then the collect buffer: up to k - 1
+// keys above the boundary bin plus at most kBndCap keys in it, rounded up to a
+// power of two (>= 64: the sort works on whole warps' 64-key segments).
 struct SelSmem {
-  size_t out, bnd, total;
+  size_t buf, total;
 };
 __host__ __device__ inline SelSmem sel_smem(int k) {
   SelSmem m{};
-  m.out = (sizeof(SelShared) + 15) & ~size_t(15);
-  m.bnd = m.out + static_cast<size_t>(pow2_at_least(k < 64 ? 64 : k)) * 8;
-  m.total = m.bnd + static_cast<size_t>(kBndCap) * 8;
+  m.buf = (sizeof(SelShared) + 15) & ~size_t(15);
+  const int cap = k + kBndCap;
+  m.total = m.buf + static_cast<size_t>(pow2_at_least(cap < 64 ? 64 : cap)) * 8;
   return m;
 }
 
@@ -184,13 +183,15 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 3 : 4) topk_cluster_kern
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SelShared *sh = reinterpret_cast<SelShared *>(smem_raw);
   const SelSmem lay = sel_smem(p.top_k);
-  uint64_t *out = reinterpret_cast<uint64_t *>(smem_raw + lay.out);
-  uint64_t *bnd = reinterpret_cast<uint64_t *>(smem_raw + lay.bnd);
+  uint64_t *buf = reinterpret_cast<uint64_t *>(smem_raw + lay.buf);
   const uint32_t r = cl::rank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t = blockIdx.y;
   const int piece = blockIdx.x / C;
   const int k = p.top_k;
+  // This kernel may be launched before the one writing its input has ended:
+  // wait for that kernel's completion and memory first.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- this CTA's keys ----
   long long n;  // keys of query t at this stage
@@ -233,10 +234,7 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 3 : 4) topk_cluster_kern
     }
     key[j] = kv;
   }
-  if (r == 0 && tid == 0) {
-    sh->n_out = 0;
-    sh->n_bnd = 0;
-  }
+  if (r == 0 && tid == 0) sh->n_buf = 0;
 
   // ---- locate the boundary bin, digit by digit ----
   constexpr int sl = kBins / C;             // bins per rank
@@ -257,13 +255,19 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 3 : 4) topk_cluster_kern
     // sum my slice over the cluster; thread tid owns bins bin_top - per*tid - j
     uint32_t c[per];
     uint32_t tot = 0;
+    {
+      uint32_t part[per][C];   // every remote load in flight before the sums
 #pragma unroll
-    for (int j = 0; j < per; ++j) {
-      const int b = bin_top - per * tid - j;
-      c[j] = 0u;
+      for (int j = 0; j < per; ++j)
 #pragma unroll
-      for (int q = 0; q < C; ++q) c[j] += cl::ld_u32(cl::map(&sh->hist[b], q));
-      tot += c[j];
+        for (int q = 0; q < C; ++q) part[j][q] = cl::ld_u32(cl::map(&sh->hist[bin_top - per * tid - j], q));
+#pragma unroll
+      for (int j = 0; j < per; ++j) {
+        c[j] = 0u;
+#pragma unroll
+        for (int q = 0; q < C; ++q) c[j] += part[j][q];
+        tot += c[j];
+      }
     }
     uint32_t incl = tot;
 #pragma unroll
@@ -324,51 +328,41 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 3 : 4) topk_cluster_kern
     // (the reads precede the barrier just passed)
   }
 
-  // ---- collect into CTA 0: keys above the boundary to out, inside it to bnd ----
-  const uint32_t out_base = cl::map(out, 0), bnd_base = cl::map(bnd, 0);
-  const uint32_t nout_a = cl::map(&sh->n_out, 0), nbnd_a = cl::map(&sh->n_bnd, 0);
+  // ---- collect into CTA 0 every key at or above the boundary bin ----
+  // (one cluster atomic per warp: count first, then place)
+  const uint32_t buf_base = cl::map(buf, 0), nbuf_a = cl::map(&sh->n_buf, 0);
+  uint32_t total = 0;
+#pragma unroll
+  for (int j = 0; j < kSelR; ++j)
+    total += __popc(__ballot_sync(0xFFFFFFFFu, key[j] != 0ull && (key[j] & mask) >= prefix));
+  uint32_t base = 0;
+  if (lane == 0 && total) base = cl::atom_add(nbuf_a, total);
+  base = __shfl_sync(0xFFFFFFFFu, base, 0);
+  const uint32_t below = lanemask_lt();
 #pragma unroll
   for (int j = 0; j < kSelR; ++j) {
-    const uint64_t mk = key[j] & mask;
-    const bool up = key[j] != 0ull && (take_all ? mk >= prefix : mk > prefix);
-    const bool eq = key[j] != 0ull && !take_all && mk == prefix;
-    const uint32_t mu = __ballot_sync(0xFFFFFFFFu, up), me = __ballot_sync(0xFFFFFFFFu, eq);
-    uint32_t bu = 0, be = 0;
-    if (lane == 0) {
-      if (mu) bu = cl::atom_add(nout_a, __popc(mu));
-      if (me) be = cl::atom_add(nbnd_a, __popc(me));
-    }
-    bu = __shfl_sync(0xFFFFFFFFu, bu, 0);
-    be = __shfl_sync(0xFFFFFFFFu, be, 0);
-    const uint32_t below = lanemask_lt();
-    if (up) cl::st_u64(out_base + 8u * (bu + __popc(mu & below)), key[j]);
-    if (eq) cl::st_u64(bnd_base + 8u * (be + __popc(me & below)), key[j]);
+    const bool take = key[j] != 0ull && (key[j] & mask) >= prefix;
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
+    if (take) cl::st_u64(buf_base + 8u * (base + __popc(m & below)), key[j]);
+    base += __popc(m);
   }
   cl::sync();
   if (r != 0) return;  // nothing touches this CTA's shared memory any more
 
-  // ---- CTA 0: finish the boundary bin, then sort / write ----
-  int count = sh->n_out;
-  if (!take_all) {
-    const int nb = sh->n_bnd;
-    const int want = k - count;  // 1 .. nb
-    TopkGroup<kSelThreads> g{&sh->tsh, bnd, tid, 1};
-    if (tid == 0) sh->tsh.count = nb;
-    __syncthreads();
-    g.compact(want);  // keeps the `want` largest boundary keys in bnd[0 .. want)
-    for (int i = tid; i < want; i += kSelThreads) out[count + i] = bnd[i];
-    count += want;
-  }
+  // ---- CTA 0: sort what was collected (all keys above the boundary bin and
+  // every key in it) and keep the first k ----
+  const int count = sh->n_buf;
+  const int m = max(64, pow2_at_least(count));
+  for (int i = count + tid; i < m; i += kSelThreads) buf[i] = 0ull;
+  __syncthreads();
+  sort_desc(buf, m);
+  const int kept = min(count, k);
   if (kFinal) {
-    const int m = max(64, pow2_at_least(count));
-    for (int i = count + tid; i < m; i += kSelThreads) out[i] = 0ull;
-    __syncthreads();
-    sort_desc(out, m);
     int32_t *oi = p.topk_idx + static_cast<long long>(t) * k;
     float *os = p.topk_score + static_cast<long long>(t) * k;
     for (int i = tid; i < k; i += kSelThreads) {
-      if (i < count) {
-        const uint64_t kv = out[i];
+      if (i < kept) {
+        const uint64_t kv = buf[i];
         oi[i] = key_index(kv);
         os[i] = key_score(kv);
       } else {
@@ -377,9 +371,8 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 3 : 4) topk_cluster_kern
       }
     }
   } else {
-    __syncthreads();
     uint64_t *dst = a.cand_out + (static_cast<long long>(t) * (gridDim.x / C) + piece) * k;
-    for (int i = tid; i < k; i += kSelThreads) dst[i] = (i < count) ? out[i] : 0ull;
+    for (int i = tid; i < k; i += kSelThreads) dst[i] = (i < kept) ? buf[i] : 0ull;
   }
 }
 
@@ -393,13 +386,15 @@ cudaError_t launch_stage_c(const ScoreParams &p, const SelArgs &a, int pieces, s
   cfg.blockDim = dim3(kSelThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(C);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap the previous kernel's tail
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, fn, p, a);
 }
 
