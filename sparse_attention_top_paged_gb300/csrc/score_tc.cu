@@ -17,24 +17,26 @@
 //   work     The tiles of 128 consecutive keys of every query, laid end to end,
 //            are split evenly over the CTAs (one per SM). A "segment" is a
 //            CTA's run of tiles of one query (it shares one B operand).
-//   warp 10  resolver: looks up block-table entries and per-block global
+//   warp 14  resolver: looks up block-table entries and per-block global
 //            scales 32 blocks at a time (one per lane) into a ring of per-tile
 //            records, so no dependent global load sits on the copy path.
 //   warp 0   producer: streams each tile's packed E2M1 nibbles (2-D TMA,
 //            64-byte swizzle) and E4M3 scales (1-D bulk copy) into a ring of
-//            shared-memory stages, and at each segment start copies the
-//            query's q record into one of two segment slots.
+//            shared-memory stages, several tiles at once (one per lane), and
+//            at each segment start copies the query's q record into one of
+//            two segment slots.
 //   warps 2-5 decoders: one thread per key row decodes 128 elements
 //            e2m1 * e4m3 exactly into f16 (hardware converts) and stores them
 //            to tensor memory as the MMA's A operand.
 //   warp 1   MMA issuer: D[128 keys x Npad heads] = A * B^T in f32, K = 128, as
 //            8 (or 16 with the lo part) tcgen05.mma kind::f16 steps.
-//   warps 6-9 epilogue: one thread per key reads its accumulator row from
+//   warps 6-13 epilogue, two groups of four taking alternate tiles: one
+//            thread per key reads its accumulator row from
 //            tensor memory and forms I = g * sum_h (w_h 2^-sigma_h) relu(acc_h)
 //            (the per-block global scale g is factored out, so relu(g a) = g
 //            relu(a) for g > 0 and g min(a,0) for g < 0), then stores I to the
 //            score matrix (coalesced: a warp writes 32 consecutive keys). The
-//            four epilogue warps never wait for one another.
+//            epilogue warps never wait for one another.
 //
 // Products e2m1 * e4m3 are exact in f16, and bf16-valued q is exact in the
 // scaled f16 hi part, so a single MMA pass computes the dot products with f32
@@ -45,13 +47,14 @@
 
 #include <mutex>
 
+#include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
 
 namespace idx {
 namespace {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 480;
 constexpr int kTileKeys = 128;
 constexpr int kMaxNS = 16;               // raw stages (as many as shared memory holds)
 constexpr int kR = 64;                   // metadata ring (tiles)
@@ -71,7 +74,7 @@ struct MetaEntry {
   int s0;         // first key of the tile
   int nblk;       // blocks the tile touches (up to its last valid key)
   int t;          // the tile's query
-  int seg;        // 1: first tile of a segment (the producer brings in q[t]'s B operand)
+  int seg;        // first tile of the CTA's segment number seg - 1; 0: not a segment start
   int pad_[10];
 };
 static_assert(sizeof(MetaEntry) == 128, "meta entry");
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar(B_SEG_FULL + a), 1);   // producer (record copy)
       ptx::mbar_init(bar(B_SEG_BFREE + a), 1);
-      ptx::mbar_init(bar(B_SEG_WFREE + a), 4);  // one arrive per epilogue warp
+      ptx::mbar_init(bar(B_SEG_WFREE + a), 8);  // one arrive per epilogue warp
     }
     for (int r = 0; r < kR; ++r) {
       ptx::mbar_init(bar(B_META_FULL + r), 1);   // resolver
@@ -301,33 +304,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ================================================================ producer
-    if (lane == 0) {
-      int issued = 0, segs = 0;
-      Ring raw, meta, rs;
-      const int ns = lay.ns;
-      bool qrec_ready = false;
-      for (int i = 0; i < n_tiles; ++i, raw.next(ns), meta.next(kR)) {
-        const int s = raw.idx, r = meta.idx;
-        if (!ptx::mbar_wait(bar(B_EMPTY_RAW + s), raw.phase ^ 1u, abort_flag, kTimeoutNs)) break;
-        if (!ptx::mbar_wait(bar(B_META_FULL + r), meta.phase, abort_flag, kTimeoutNs)) break;
+    // The warp issues tiles in batches of nb, one tile per lane, so the
+    // per-tile waits and copy issues run side by side; the q-record copies
+    // of segments starting in a batch follow, in segment order, from lane 0.
+    const int ns = lay.ns;
+    // at most half the stages per batch, so the other half stays in flight
+    // and no two tiles of a batch share a stage
+    const int nb = min(8, ns / 2);
+    int issued = 0, last_seg = -1;
+    bool qrec_ready = false;
+    for (int base = 0; base < n_tiles; base += nb) {
+      const int i = base + lane;
+      const bool act = lane < nb && i < n_tiles;
+      const int s = i % ns, r = i & (kR - 1);
+      bool ok = true;
+      int seg = 0, tq = 0;
+      if (act) {
+        ok = ptx::mbar_wait(bar(B_EMPTY_RAW + s), (static_cast<uint32_t>(i / ns) & 1u) ^ 1u, abort_flag, kTimeoutNs);
+        ok = ok && ptx::mbar_wait(bar(B_META_FULL + r), static_cast<uint32_t>(i / kR) & 1u, abort_flag, kTimeoutNs);
+      }
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      if (act) {
         const MetaEntry &m = sMeta[r];
-        if (m.seg) {
-          // First tile of a segment: copy q[t]'s B-operand record into the next
-          // segment slot once its previous segment is done with it.
-          if (segs > 0) rs.next(nseg);
-          const int ss = rs.idx;
-          if (!ptx::mbar_wait(bar(B_SEG_BFREE + ss), rs.phase ^ 1u, abort_flag, kTimeoutNs)) break;
-          if (!ptx::mbar_wait(bar(B_SEG_WFREE + ss), rs.phase ^ 1u, abort_flag, kTimeoutNs)) break;
-          if (!qrec_ready) {
-            ptx::wait_prior_grid();  // the records are written by the kernel launched just before
-            qrec_ready = true;
-          }
-          const uint32_t sfull = bar(B_SEG_FULL + ss);
-          ptx::mbar_arrive_expect_tx(sfull, lay.rec_bytes);
-          ptx::bulk_g2s(ptx::smem_addr(sB + ss * lay.rec_smem), qrec + static_cast<size_t>(m.t) * lay.rec_bytes,
-                        lay.rec_bytes, sfull);
-          ++segs;
-        }
+        seg = m.seg;
+        tq = m.t;
         const uint32_t mask = m.mask;
         const int s0 = m.s0, lb0 = m.lb0, nblk = m.nblk;
         uint32_t bytes = 0;
@@ -361,15 +361,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                           static_cast<uint32_t>(hi - lo) * 8u, full);
           }
         }
-        ++issued;
       }
-      // never leave with copies in flight: the last ns tile stages and the
-      // last segment record (an earlier one was waited for before its slot's reuse)
-      volatile int no_abort = 0;
-      for (int i = (issued > ns ? issued - ns : 0); i < issued; ++i)
-        ptx::mbar_wait(bar(B_FULL_RAW + i % ns), static_cast<uint32_t>(i / ns) & 1u, &no_abort, kTimeoutNs);
-      if (segs > 0) ptx::mbar_wait(bar(B_SEG_FULL + rs.idx), rs.phase, &no_abort, kTimeoutNs);
+      issued = min(base + nb, n_tiles);
+      // Segments starting in this batch: copy q[t]'s B-operand record into
+      // slot (ordinal mod nseg) once that slot's previous segment is done
+      // with it. The batch's tiles are already on their way, so the waits
+      // cannot hold up the segment they wait for.
+      uint32_t segs = __ballot_sync(0xFFFFFFFFu, act && seg != 0);
+      bool seg_ok = true;
+      while (segs) {
+        const int L = __ffs(segs) - 1;
+        segs &= segs - 1;
+        const int ord = __shfl_sync(0xFFFFFFFFu, seg, L) - 1, t_seg = __shfl_sync(0xFFFFFFFFu, tq, L);
+        if (lane == 0) {
+          const int ss = ord % nseg;
+          const uint32_t ph = static_cast<uint32_t>(ord / nseg) & 1u;
+          seg_ok = ptx::mbar_wait(bar(B_SEG_BFREE + ss), ph ^ 1u, abort_flag, kTimeoutNs) &&
+                   ptx::mbar_wait(bar(B_SEG_WFREE + ss), ph ^ 1u, abort_flag, kTimeoutNs);
+          if (seg_ok) {
+            if (!qrec_ready) {
+              ptx::wait_prior_grid();  // the records are written by the kernel launched just before
+              qrec_ready = true;
+            }
+            const uint32_t sfull = bar(B_SEG_FULL + ss);
+            ptx::mbar_arrive_expect_tx(sfull, lay.rec_bytes);
+            ptx::bulk_g2s(ptx::smem_addr(sB + ss * lay.rec_smem), qrec + static_cast<size_t>(t_seg) * lay.rec_bytes,
+                          lay.rec_bytes, sfull);
+            last_seg = ord;
+          }
+        }
+        if (!__all_sync(0xFFFFFFFFu, __shfl_sync(0xFFFFFFFFu, seg_ok, 0))) break;
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, seg_ok, 0)) break;
     }
+    // Never leave with copies in flight: the last ns tile stages (one per
+    // lane) and the last segment record (an earlier one was waited for before
+    // its slot's reuse).
+    volatile int no_abort = 0;
+    if (lane < ns) {
+      const int i = issued - ns + lane;
+      if (i >= 0)
+        ptx::mbar_wait(bar(B_FULL_RAW + i % ns), static_cast<uint32_t>(i / ns) & 1u, &no_abort, kTimeoutNs);
+    }
+    last_seg = __shfl_sync(0xFFFFFFFFu, last_seg, 0);
+    if (lane == 0 && last_seg >= 0)
+      ptx::mbar_wait(bar(B_SEG_FULL + last_seg % nseg), static_cast<uint32_t>(last_seg / nseg) & 1u, &no_abort,
+                     kTimeoutNs);
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     // The whole warp walks the tiles in lockstep; one elected lane issues.
@@ -466,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar(B_EMPTY_RAW + s));
       }
     }
-  } else if (warp == 10) {
+  } else if (warp == 14) {
     // ============================================================== resolver
     // Resolves block-table entries and global scales for batches of 32 blocks
     // at once (one per lane), so the two dependent global loads per block
@@ -476,6 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int d = lane / bpt, b = lane % bpt;
     Walker w;
     w.init(p, t0, j0);
+    int seg_base = 0;  // segments started before this batch
     for (int base = 0; base < n_tiles; base += tpb) {
       const int i = base + d;
       const bool tile_ok = i < n_tiles;
@@ -499,6 +537,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (blk_ok && !pv && p.dev_status) atomicOr(p.dev_status, IDX_STATUS_BAD_BLOCK);
       const uint32_t valid_bits = __ballot_sync(0xFFFFFFFFu, pv);
+      const bool starts = tile_ok && b == 0 && (i == 0 || wl.j == 0);
+      const uint32_t start_bits = __ballot_sync(0xFFFFFFFFu, starts);
+      const int ord = seg_base + __popc(start_bits & lanemask_lt());
+      seg_base += __popc(start_bits);
       const int r = i & (kR - 1);   // kR is a power of two
       bool ok = true;
       if (tile_ok && b == 0)
@@ -516,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m.s0 = s0;
         m.nblk = nblk;
         m.t = wl.t;
-        m.seg = (i == 0 || wl.j == 0) ? 1 : 0;
+        m.seg = starts ? ord + 1 : 0;
       }
       __syncwarp();
       if (tile_ok && b == 0) ptx::mbar_arrive(bar(B_META_FULL + r));
@@ -524,7 +566,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ============================================================== epilogue
+    // Two groups of four warps take alternate tiles. Every warp still walks
+    // every tile: it waits for each segment's q record and signals when it
+    // is done with each segment's w', so a slot is reused only after both
+    // groups are done with it.
     const int row = 32 * (warp & 3) + lane;    // the TMEM lane (key row) this thread reads
+    const int grp = (warp - 6) >> 2;
     Walker w;
     w.init(p, t0, j0);
     int ss = 0, L = 0;
@@ -538,6 +585,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ss = rs.idx;
         L = p.valid_lens[w.t];
         ok = ptx::mbar_wait(bar(B_SEG_FULL + ss), rs.phase, abort_flag, kTimeoutNs);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      }
+      if ((i & 1) != grp) {       // the other group's tile
+        if (seg_end) {
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(B_SEG_WFREE + ss));
+        }
+        continue;
       }
       const int d = rd.idx, r = rm.idx;
       ok = ok && ptx::mbar_wait(bar(B_FULL_D + d), rd.phase, abort_flag, kTimeoutNs);

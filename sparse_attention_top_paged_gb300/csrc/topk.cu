@@ -33,6 +33,7 @@ constexpr int kSelR = 16;                           // keys per thread, in regis
 constexpr int kCtaKeys = kSelThreads * kSelR;       // 4096
 constexpr int kBins = 4096;                         // 12-bit digits
 constexpr int kBndCap = 2048;                       // boundary-bin buffer (keys)
+constexpr int kRankMax = 512;                       // largest boundary bin ranked without a sort
 constexpr int kMaxCluster = 8;
 
 // ------------------------------------------- cluster / DSMEM primitives ----
@@ -179,7 +180,7 @@ __device__ void sort_desc(uint64_t *out, int m) {
 }
 
 template <int C, bool kFromCand, bool kFinal>
-__global__ void __launch_bounds__(kSelThreads, C == 1 ? 3 : 4) topk_cluster_kernel(ScoreParams p, SelArgs a) {
+__global__ void __launch_bounds__(kSelThreads, C == 1 ? 2 : (C == 2 ? 3 : 4)) topk_cluster_kernel(ScoreParams p, SelArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SelShared *sh = reinterpret_cast<SelShared *>(smem_raw);
   const SelSmem lay = sel_smem(p.top_k);
@@ -241,7 +242,8 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 3 : 4) topk_cluster_kern
   constexpr int per = sl / kSelThreads;     // bins per thread (>= 2)
   const int bin_top = (static_cast<int>(r) + 1) * sl - 1;
   uint64_t prefix = 0, mask = 0;
-  int need = k, shift = 52, width = 12;
+  int need = k, shift = 52, width = 12, rounds = 0;
+  uint32_t all_keys = 0;
   bool take_all = false;
   while (true) {
     for (int b = tid; b < kBins; b += kSelThreads) sh->hist[b] = 0u;
@@ -293,11 +295,26 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 3 : 4) topk_cluster_kern
       if (q > static_cast<int>(r)) above += s;
       all += s;
     }
+    uint32_t run = above + before + incl - tot;
+    if (shift == 52) {
+      // First digit: publish, for every bin that holds some of the k best
+      // keys, its place in the output (keys in higher bins) and its count,
+      // packed as start | count << 16, into CTA 0's histogram array (no CTA
+      // reads histograms any more this round).
+      uint32_t rb = run;
+#pragma unroll
+      for (int j = 0; j < per; ++j) {
+        if (c[j] != 0u && rb < static_cast<uint32_t>(k))
+          cl::st_u32(cl::map(&sh->hist[bin_top - per * tid - j], 0), rb | (c[j] << 16));
+        rb += c[j];
+      }
+    }
+    all_keys = all;
     if (all <= static_cast<uint32_t>(need)) {
       take_all = true;  // every key matching the prefix is selected (same decision in every CTA)
+      cl::sync();
       break;
     }
-    uint32_t run = above + before + incl - tot;
 #pragma unroll
     for (int j = 0; j < per; ++j) {
       if (run < static_cast<uint32_t>(need) && run + c[j] >= static_cast<uint32_t>(need)) {
@@ -314,6 +331,7 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 3 : 4) topk_cluster_kern
     const int bin = sh->b_bin, cnt = sh->b_cnt;
     prefix |= static_cast<uint64_t>(bin) << shift;
     mask |= static_cast<uint64_t>(dmask) << shift;
+    ++rounds;
     if (cnt <= kBndCap || shift == 0) break;
     need -= sh->b_above;
     // digits: bits 63..52, 51..40, 39..28, 27..16, 15..4, then 3..0
@@ -328,7 +346,50 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 3 : 4) topk_cluster_kern
     // (the reads precede the barrier just passed)
   }
 
-  // ---- collect into CTA 0 every key at or above the boundary bin ----
+  // ---- decided on the first digit, with a small boundary bin: rank path ----
+  // Every key at or above the boundary bin goes straight into its bin's
+  // segment of CTA 0's buffer (bins in descending order); CTA 0 then ranks
+  // each key inside its bin and writes it to its final place. No sort.
+  if ((take_all && rounds == 0) || (!take_all && rounds == 1 && sh->b_cnt <= kRankMax)) {
+    const uint32_t table = cl::map(sh->hist, 0), buf_r = cl::map(buf, 0);
+#pragma unroll
+    for (int j = 0; j < kSelR; ++j) {
+      if (key[j] != 0ull && (key[j] & mask) >= prefix) {
+        const uint32_t old = cl::atom_add(table + 4u * static_cast<uint32_t>(key[j] >> 52), 1u);
+        cl::st_u64(buf_r + 8u * (old & 0xFFFFu), key[j]);
+      }
+    }
+    cl::sync();
+    if (r != 0) return;
+    const int total = take_all ? static_cast<int>(all_keys) : sh->b_above + sh->b_cnt;
+    uint64_t *dst = kFinal ? nullptr : a.cand_out + (static_cast<long long>(t) * (gridDim.x / C) + piece) * k;
+    for (int p0 = tid; p0 < total; p0 += kSelThreads) {
+      const uint64_t kv = buf[p0];
+      const uint32_t pk = sh->hist[kv >> 52];
+      const int end = static_cast<int>(pk & 0xFFFFu), start = end - static_cast<int>(pk >> 16);
+      int pos = start;
+      for (int q = start; q < end; ++q) pos += (buf[q] > kv) ? 1 : 0;
+      if (pos < k) {
+        if (kFinal) {
+          p.topk_idx[static_cast<long long>(t) * k + pos] = key_index(kv);
+          p.topk_score[static_cast<long long>(t) * k + pos] = key_score(kv);
+        } else {
+          dst[pos] = kv;
+        }
+      }
+    }
+    for (int i = total + tid; i < k; i += kSelThreads) {
+      if (kFinal) {
+        p.topk_idx[static_cast<long long>(t) * k + i] = -1;
+        p.topk_score[static_cast<long long>(t) * k + i] = -INFINITY;
+      } else {
+        dst[i] = 0ull;
+      }
+    }
+    return;
+  }
+
+  // ---- otherwise collect into CTA 0 every key at or above the boundary bin ----
   // (one cluster atomic per warp: count first, then place)
   const uint32_t buf_base = cl::map(buf, 0), nbuf_a = cl::map(&sh->n_buf, 0);
   uint32_t total = 0;
