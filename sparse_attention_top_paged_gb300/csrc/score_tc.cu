@@ -604,8 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool in_len = s_key < L;
       const bool valid = in_len && b < kMaxBlocksPerTile && ((sMeta[r].mask >> b) & 1u);
       const float g = (b < kMaxBlocksPerTile) ? sMeta[r].g[b] : 0.0f;
-      const uint64_t *wv2 = reinterpret_cast<const uint64_t *>(sB + ss * lay.rec_smem + lay.rec_w);  // (w'_h, w'_h+1)
-      uint64_t acc2[2] = {0ull, 0ull};                                          // two independent chains
+      const float *wq = reinterpret_cast<const float *>(sB + ss * lay.rec_smem + lay.rec_w);  // w'_h
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // eight independent chains
       const uint32_t taddr = tmem_d + d * Npad + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
       for (int c0 = 0; c0 < Npad; c0 += 64) {
         uint32_t v[64];
@@ -622,30 +622,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const int ncol = (Npad - c0 < 64) ? (Npad - c0) : 64;
+        const float4 *w4 = reinterpret_cast<const float4 *>(wq + c0);
         if (g >= 0.0f) {          // relu(g a) = g max(a, 0)
 #pragma unroll
           for (int e = 0; e < 64; e += 4) {
             if (e < ncol) {
-              ptx::ffma2(acc2[0], wv2[(c0 + e) >> 1],
-                         ptx::pack2(fmaxf(__uint_as_float(v[e]), 0.0f), fmaxf(__uint_as_float(v[e + 1]), 0.0f)));
-              ptx::ffma2(acc2[1], wv2[((c0 + e) >> 1) + 1],
-                         ptx::pack2(fmaxf(__uint_as_float(v[e + 2]), 0.0f), fmaxf(__uint_as_float(v[e + 3]), 0.0f)));
+              const float4 ww = w4[e >> 2];
+              float *ac = acc + ((e >> 2) & 1) * 4;
+              ac[0] = fmaf(ww.x, fmaxf(__uint_as_float(v[e + 0]), 0.0f), ac[0]);
+              ac[1] = fmaf(ww.y, fmaxf(__uint_as_float(v[e + 1]), 0.0f), ac[1]);
+              ac[2] = fmaf(ww.z, fmaxf(__uint_as_float(v[e + 2]), 0.0f), ac[2]);
+              ac[3] = fmaf(ww.w, fmaxf(__uint_as_float(v[e + 3]), 0.0f), ac[3]);
             }
           }
         } else {                  // relu(g a) = g min(a, 0)
 #pragma unroll
           for (int e = 0; e < 64; e += 4) {
             if (e < ncol) {
-              ptx::ffma2(acc2[0], wv2[(c0 + e) >> 1],
-                         ptx::pack2(fminf(__uint_as_float(v[e]), 0.0f), fminf(__uint_as_float(v[e + 1]), 0.0f)));
-              ptx::ffma2(acc2[1], wv2[((c0 + e) >> 1) + 1],
-                         ptx::pack2(fminf(__uint_as_float(v[e + 2]), 0.0f), fminf(__uint_as_float(v[e + 3]), 0.0f)));
+              const float4 ww = w4[e >> 2];
+              float *ac = acc + ((e >> 2) & 1) * 4;
+              ac[0] = fmaf(ww.x, fminf(__uint_as_float(v[e + 0]), 0.0f), ac[0]);
+              ac[1] = fmaf(ww.y, fminf(__uint_as_float(v[e + 1]), 0.0f), ac[1]);
+              ac[2] = fmaf(ww.z, fminf(__uint_as_float(v[e + 2]), 0.0f), ac[2]);
+              ac[3] = fmaf(ww.w, fminf(__uint_as_float(v[e + 3]), 0.0f), ac[3]);
             }
           }
         }
       }
-      const float sum = (__uint_as_float(static_cast<uint32_t>(acc2[0])) + __uint_as_float(static_cast<uint32_t>(acc2[0] >> 32))) +
-                        (__uint_as_float(static_cast<uint32_t>(acc2[1])) + __uint_as_float(static_cast<uint32_t>(acc2[1] >> 32)));
+      const float sum = ((acc[0] + acc[4]) + (acc[1] + acc[5])) + ((acc[2] + acc[6]) + (acc[3] + acc[7]));
       if (in_len) scores[static_cast<long long>(w.t) * ld + s_key] = valid ? __fadd_rn(g * sum, 0.0f) : -INFINITY;
       if (seg_end) {             // this warp is done with the segment's w'
         __syncwarp();

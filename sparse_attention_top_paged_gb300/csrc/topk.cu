@@ -11,14 +11,18 @@
 // common.cuh) without re-reading them:
 //   1. every CTA builds a 4096-bin shared-memory histogram of the next 12 key
 //      bits of its keys;
-//   2. CTA r sums bins [r*4096/C, (r+1)*4096/C) over the cluster through
-//      distributed shared memory and publishes its slice total to all CTAs;
+//   2. every CTA adds its nonzero bins into the owners' sums (CTA r owns bins
+//      [r*4096/C, (r+1)*4096/C)) with distributed shared-memory reductions,
+//      and each owner publishes its slice total to all CTAs;
 //   3. the CTA whose slice holds the k-th key locates that bin and publishes
 //      it; if the bin holds more keys than the boundary buffer, the keys in it
 //      are histogrammed again on the next 12 bits (still from registers);
-//   4. every CTA appends its keys at or above the boundary bin to a buffer in
-//      CTA 0 (one distributed shared-memory atomic per warp); CTA 0 sorts the
-//      buffer (bitonic, short strides in registers) and keeps the first k.
+//   4. when the first digit decides, every key at or above the boundary bin
+//      goes straight into its bin's segment of a buffer in CTA 0, which ranks
+//      each key inside its bin and writes it to its output slot; after a
+//      refinement the keys are collected (one distributed shared-memory
+//      atomic per warp) and CTA 0 sorts them (bitonic, short strides in
+//      registers) and keeps the first k.
 // A query longer than one cluster's reach is split into pieces whose k best
 // keys go to a candidate list; the next launch selects from those lists the
 // same way (each stage shrinks a query's keys at least 8-fold).
@@ -32,8 +36,7 @@ constexpr int kSelThreads = 256;
 constexpr int kSelR = 16;                           // keys per thread, in registers
 constexpr int kCtaKeys = kSelThreads * kSelR;       // 4096
 constexpr int kBins = 4096;                         // 12-bit digits
-constexpr int kBndCap = 2048;                       // boundary-bin buffer (keys)
-constexpr int kRankMax = 512;                       // largest boundary bin ranked without a sort
+constexpr int kBndCap = 512;                        // largest boundary bin collected (else refine)
 constexpr int kMaxCluster = 8;
 
 // ------------------------------------------- cluster / DSMEM primitives ----
@@ -41,11 +44,6 @@ namespace cl {
 __device__ __forceinline__ uint32_t rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t nranks() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
 // All threads of every CTA of the cluster; orders shared-memory writes before
@@ -56,6 +54,8 @@ __device__ __forceinline__ void sync() {
       "barrier.cluster.wait.acquire.aligned;" ::
           : "memory");
 }
+__device__ __forceinline__ void arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 // Address of the same shared-memory variable in CTA `r` of the cluster.
 __device__ __forceinline__ uint32_t map(const void *p, uint32_t r) {
   uint32_t a;
@@ -64,16 +64,14 @@ __device__ __forceinline__ uint32_t map(const void *p, uint32_t r) {
                : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(r));
   return a;
 }
-__device__ __forceinline__ uint32_t ld_u32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-  return v;
-}
 __device__ __forceinline__ void st_u32(uint32_t a, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 __device__ __forceinline__ void st_u64(uint32_t a, uint64_t v) {
   asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ void red_add(uint32_t a, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 __device__ __forceinline__ uint32_t atom_add(uint32_t a, uint32_t v) {
   uint32_t old;
@@ -90,6 +88,7 @@ __host__ __device__ inline int pow2_at_least(int k) {
 
 struct SelShared {
   uint32_t hist[kBins];               // this CTA's histogram of the current digit
+  uint32_t red[kBins / 2];            // cluster sums of this rank's slice of bins (C >= 2)
   uint32_t slice_tot[kMaxCluster];    // per rank: keys in its slice of bins
   uint32_t warp_sum[kSelThreads / 32];
   int b_bin, b_above, b_cnt;          // boundary bin, published by its owner
@@ -195,10 +194,23 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 2 : (C == 2 ? 3 : 4)) to
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- this CTA's keys ----
-  long long n;  // keys of query t at this stage
-  if (kFromCand) {
-    n = a.n_in;
-  } else {
+  // Row positions are loaded up to the row capacity (max_lb * epb <= ld) and
+  // masked by the valid length afterwards, so the loads need not wait for it.
+  const long long lo = static_cast<long long>(piece) * C * kCtaKeys + static_cast<long long>(r) * kCtaKeys;
+  const long long cap = kFromCand ? a.n_in : static_cast<long long>(p.max_lb) * p.epb;
+  const long long hi_cap = min(cap, lo + kCtaKeys);
+  float sv[kFromCand ? 1 : kSelR];
+  uint64_t key[kSelR];
+#pragma unroll
+  for (int j = 0; j < kSelR; ++j) {
+    const long long i = lo + j * kSelThreads + tid;
+    if (kFromCand) {
+      key[j] = (i < hi_cap) ? a.cand_in[static_cast<long long>(t) * a.n_in + i] : 0ull;
+    } else {
+      sv[kFromCand ? 0 : j] = (i < hi_cap) ? a.scores[static_cast<long long>(t) * a.ld + i] : -INFINITY;
+    }
+  }
+  if (!kFromCand) {
     const int L = p.valid_lens[t];
     if (bad_len(p, L)) {  // uniform over the cluster: nobody reaches a cluster barrier
       if (r == 0) {
@@ -216,24 +228,12 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 2 : (C == 2 ? 3 : 4)) to
       }
       return;
     }
-    n = L;
-  }
-  const long long lo = static_cast<long long>(piece) * C * kCtaKeys + static_cast<long long>(r) * kCtaKeys;
-  const long long hi = min(n, lo + kCtaKeys);
-  uint64_t key[kSelR];
 #pragma unroll
-  for (int j = 0; j < kSelR; ++j) {
-    const long long i = lo + j * kSelThreads + tid;
-    uint64_t kv = 0ull;
-    if (i < hi) {
-      if (kFromCand) {
-        kv = a.cand_in[static_cast<long long>(t) * a.n_in + i];
-      } else {
-        const float v = a.scores[static_cast<long long>(t) * a.ld + i];
-        kv = (v == -INFINITY) ? 0ull : pack_key(v, static_cast<int32_t>(i));
-      }
+    for (int j = 0; j < kSelR; ++j) {
+      const long long i = lo + j * kSelThreads + tid;
+      const float v = sv[kFromCand ? 0 : j];
+      key[j] = (i < L && v != -INFINITY) ? pack_key(v, static_cast<int32_t>(i)) : 0ull;
     }
-    key[j] = kv;
   }
   if (r == 0 && tid == 0) sh->n_buf = 0;
 
@@ -245,6 +245,10 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 2 : (C == 2 ? 3 : 4)) to
   int need = k, shift = 52, width = 12, rounds = 0;
   uint32_t all_keys = 0;
   bool take_all = false;
+  if (C > 1)
+    for (int b = tid; b < sl; b += kSelThreads) sh->red[b] = 0u;
+  cl::arrive();  // every CTA's sums are zero (and it has started) before anyone adds into them
+  bool first = true;
   while (true) {
     for (int b = tid; b < kBins; b += kSelThreads) sh->hist[b] = 0u;
     __syncthreads();
@@ -253,23 +257,33 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 2 : (C == 2 ? 3 : 4)) to
     for (int j = 0; j < kSelR; ++j)
       if (key[j] != 0ull && (key[j] & mask) == prefix)
         atomicAdd(&sh->hist[static_cast<uint32_t>(key[j] >> shift) & dmask], 1u);
+    __syncthreads();
+    if (first) {
+      cl::wait();
+      first = false;
+    }
+    if (C > 1) {  // add every nonzero bin into its owner's sums (no round trip)
+#pragma unroll
+      for (int j = 0; j < kBins / kSelThreads; ++j) {
+        const int b = tid + j * kSelThreads;
+        const uint32_t v = sh->hist[b];
+        if (v != 0u) cl::red_add(cl::map(&sh->red[b % sl], static_cast<uint32_t>(b / sl)), v);
+      }
+    }
     cl::sync();
-    // sum my slice over the cluster; thread tid owns bins bin_top - per*tid - j
+    // my slice's cluster sums; thread tid owns bins bin_top - per*tid - j
     uint32_t c[per];
     uint32_t tot = 0;
-    {
-      uint32_t part[per][C];   // every remote load in flight before the sums
 #pragma unroll
-      for (int j = 0; j < per; ++j)
-#pragma unroll
-        for (int q = 0; q < C; ++q) part[j][q] = cl::ld_u32(cl::map(&sh->hist[bin_top - per * tid - j], q));
-#pragma unroll
-      for (int j = 0; j < per; ++j) {
-        c[j] = 0u;
-#pragma unroll
-        for (int q = 0; q < C; ++q) c[j] += part[j][q];
-        tot += c[j];
+    for (int j = 0; j < per; ++j) {
+      const int lb = sl - 1 - per * tid - j;   // index within the slice
+      if (C > 1) {
+        c[j] = sh->red[lb];
+        sh->red[lb] = 0u;                       // ready for the next digit's sums
+      } else {
+        c[j] = sh->hist[lb];
       }
+      tot += c[j];
     }
     uint32_t incl = tot;
 #pragma unroll
@@ -350,7 +364,7 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 2 : (C == 2 ? 3 : 4)) to
   // Every key at or above the boundary bin goes straight into its bin's
   // segment of CTA 0's buffer (bins in descending order); CTA 0 then ranks
   // each key inside its bin and writes it to its final place. No sort.
-  if ((take_all && rounds == 0) || (!take_all && rounds == 1 && sh->b_cnt <= kRankMax)) {
+  if ((take_all && rounds == 0) || (!take_all && rounds == 1)) {
     const uint32_t table = cl::map(sh->hist, 0), buf_r = cl::map(buf, 0);
 #pragma unroll
     for (int j = 0; j < kSelR; ++j) {
@@ -367,8 +381,15 @@ __global__ void __launch_bounds__(kSelThreads, C == 1 ? 2 : (C == 2 ? 3 : 4)) to
       const uint64_t kv = buf[p0];
       const uint32_t pk = sh->hist[kv >> 52];
       const int end = static_cast<int>(pk & 0xFFFFu), start = end - static_cast<int>(pk >> 16);
-      int pos = start;
-      for (int q = start; q < end; ++q) pos += (buf[q] > kv) ? 1 : 0;
+      int pos = start, q = start;
+      for (; q + 8 <= end; q += 8) {   // eight loads in flight per step
+        uint64_t x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = buf[q + u];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) pos += (x[u] > kv) ? 1 : 0;
+      }
+      for (; q < end; ++q) pos += (buf[q] > kv) ? 1 : 0;
       if (pos < k) {
         if (kFinal) {
           p.topk_idx[static_cast<long long>(t) * k + pos] = key_index(kv);
