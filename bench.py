@@ -98,21 +98,9 @@ def recorded_traffic():
 
 
 def launches_per_step(W) -> int:
-    """Our kernels per idx_score_topk call: the scorer, then one selection
-    stage per launch. A stage gives each query (or piece of one) a cluster of
-    up to 8 CTAs x 4096 keys; while a query needs more than one cluster, the
-    stage keeps top_k candidates per piece and another stage follows (the
-    library's selection plan)."""
-    n, stages = W.max_lb * W.epb, 0
-    while True:
-        stages += 1
-        c = 1
-        while c < 8 and c * 4096 < n:
-            c <<= 1
-        pieces = max(1, -(-n // (c * 4096)))
-        if pieces == 1:
-            return 1 + stages
-        n = pieces * W.top_k
+    """Our kernels per idx_score_topk call on the tensor path: q preparation,
+    the scorer, and the selection kernel."""
+    return 3
 
 
 def peaks():

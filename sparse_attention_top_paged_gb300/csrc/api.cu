@@ -44,7 +44,7 @@ struct Resolved {
   ScoreParams p{};
   size_t ws_bytes = 0;
   SelectPlan sel{};
-  size_t qrec_off = 0;
+  size_t qrec_off = 0, hist_off = 0;
   int num_ctas = 0;
 };
 
@@ -122,9 +122,11 @@ idx_status_t resolve(const idx_score_topk_args *a, Resolved *r) {
   if (!select_supported(a->top_k, max_len)) return IDX_ERR_UNSUPPORTED;
   r->sel = select_plan(a->T, a->top_k, max_len, a->scores_out != nullptr, a->ld_scores);
   r->ws_bytes = r->sel.total;
-  if (plan == Plan::kTensor) {  // then the scorer's per-query q records
+  if (plan == Plan::kTensor) {  // then the scorer's per-query q records and key histograms
     r->qrec_off = r->ws_bytes;
     r->ws_bytes += (score_tc_workspace(p) + 255) & ~size_t(255);
+    r->hist_off = r->ws_bytes;
+    r->ws_bytes += static_cast<size_t>(a->T) * kScoreBins * 4;
   }
   return IDX_OK;
 }
@@ -163,10 +165,15 @@ idx_status_t idx_score_topk(const idx_score_topk_args *args, idx_stream_t stream
   if (r.plan == Plan::kSimt)
     e = launch_score_simt(r.p, args->key_format == IDX_KEYS_F32, scores, r.sel.ld, s);
   else
-    e = launch_score_tc(r.p, r.num_ctas, static_cast<unsigned char *>(args->workspace) + r.qrec_off, scores,
-                        r.sel.ld, s);
+    e = launch_score_tc(r.p, r.num_ctas, static_cast<unsigned char *>(args->workspace) + r.qrec_off,
+                        reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(args->workspace) + r.hist_off),
+                        scores, r.sel.ld, s);
   if (e == cudaSuccess && timed) e = cudaEventRecord(ev1, s);
-  if (e == cudaSuccess) e = launch_select(r.p, scores, r.sel.ld, r.sel, args->workspace, s);
+  const uint32_t *hist = r.plan == Plan::kTensor
+                             ? reinterpret_cast<const uint32_t *>(static_cast<unsigned char *>(args->workspace) +
+                                                                  r.hist_off)
+                             : nullptr;
+  if (e == cudaSuccess) e = launch_select(r.p, scores, r.sel.ld, hist, r.sel, args->workspace, s);
   return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 

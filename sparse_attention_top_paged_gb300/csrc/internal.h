@@ -30,36 +30,34 @@ struct ScoreParams {
   int32_t *dev_status;
 };
 
-// How TopK(I[t,:], k) is taken from the [T, ld] score matrix, and the
-// workspace sections the score path needs (byte offsets; 256-aligned).
-// Selection runs in stages: stage 0 reads the score rows; while a query's
-// keys exceed one cluster's reach, a stage writes the k best keys of each
-// piece to a candidate list and the next stage selects from those lists.
-constexpr int kMaxSelectStages = 8;
+// How TopK(I[t,:], k) is taken from the [T, ld] score matrix: one streaming
+// selection kernel per call; the workspace holds the matrix when the caller
+// passes no scores_out (byte offsets; 256-aligned).
 struct SelectPlan {
-  int n_stages;
-  int C[kMaxSelectStages];          // cluster size (CTAs) of each stage
-  int pieces[kMaxSelectStages];     // clusters per query of each stage
-  long long n_in[kMaxSelectStages]; // keys per query a stage reads (stage 0: max row length)
-  bool own_scores;                  // the score matrix lives in the workspace (no caller scores_out)
-  long long ld;                     // row stride of the score matrix
-  size_t scores_off, cand_off[2], total;
+  bool own_scores;   // the score matrix lives in the workspace (no caller scores_out)
+  long long ld;      // row stride of the score matrix
+  size_t scores_off, total;
 };
 
 SelectPlan select_plan(int T, int top_k, long long max_len, bool have_scores_out, long long ld_out);
-bool select_supported(int top_k, long long max_len);  // the stages end in one cluster per query
+bool select_supported(int top_k, long long max_len);  // the selection's buffers fit shared memory
 
 // score_simt.cu
 cudaError_t launch_score_simt(const ScoreParams &p, bool f32_keys, float *scores, long long ld,
                               cudaStream_t stream);
 // topk.cu
-cudaError_t launch_select(const ScoreParams &p, const float *scores, long long ld, const SelectPlan &plan,
-                          void *workspace, cudaStream_t stream);
+// hist: per-query histograms of the top 12 key bits of the scores (from the
+// tensor scorer), or nullptr.
+cudaError_t launch_select(const ScoreParams &p, const float *scores, long long ld, const uint32_t *hist,
+                          const SelectPlan &plan, void *workspace, cudaStream_t stream);
 // score_tc.cu
 bool score_tc_supported(const ScoreParams &p);
 size_t score_tc_workspace(const ScoreParams &p);  // per-query q records (bytes)
-cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, float *scores, long long ld,
-                            cudaStream_t stream);
+// Also fills hist[t][d] (kScoreBins per query) with the number of valid keys
+// of query t whose selection key has top 12 bits d.
+constexpr int kScoreBins = 4096;
+cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint32_t *hist, float *scores,
+                            long long ld, cudaStream_t stream);
 // gather_pool.cu
 cudaError_t launch_gather_kv(const idx_gather_kv_args &a, cudaStream_t stream);
 cudaError_t launch_block_pool(const uint16_t *raw, const float *w, float *out, uint32_t first_block,

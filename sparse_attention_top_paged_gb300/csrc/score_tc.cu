@@ -170,9 +170,14 @@ __device__ long long block_incl_scan(long long v, long long *scratch, long long 
 // clamped so 2^sigma and 2^-sigma are normal floats); the scaled values are
 // split into f16 hi + lo (lo = 0 whenever q is exact in f16 after scaling,
 // e.g. for bf16-valued q) and w' = w 2^-sigma undoes the scale after the ReLU.
-__global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay, uint8_t *__restrict__ rec) {
+__global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay, uint8_t *__restrict__ rec,
+                                                    uint32_t *__restrict__ hist) {
   ptx::launch_dependents();  // the scorer may start its prologue meanwhile
   const int t = blockIdx.x;
+  {  // the blocks of query t zero its key histogram between them
+    uint32_t *hz = hist + static_cast<size_t>(t) * kScoreBins;
+    for (int i = blockIdx.y * blockDim.x + threadIdx.x; i < kScoreBins; i += gridDim.y * blockDim.x) hz[i] = 0u;
+  }
   const int h = blockIdx.y * 8 + static_cast<int>(threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (h >= lay.Npad) return;
@@ -219,7 +224,8 @@ __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay,
 
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmap_nib, ScoreParams p, TcLayout lay,
-                    const uint8_t *__restrict__ qrec, float *__restrict__ scores, long long ld) {
+                    const uint8_t *__restrict__ qrec, uint32_t *__restrict__ hist, float *__restrict__ scores,
+                    long long ld) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -650,7 +656,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float sum = ((acc[0] + acc[4]) + (acc[1] + acc[5])) + ((acc[2] + acc[6]) + (acc[3] + acc[7]));
-      if (in_len) scores[static_cast<long long>(w.t) * ld + s_key] = valid ? __fadd_rn(g * sum, 0.0f) : -INFINITY;
+      if (in_len) {
+        const float sc = __fadd_rn(g * sum, 0.0f);
+        scores[static_cast<long long>(w.t) * ld + s_key] = valid ? sc : -INFINITY;
+        // the selection's first digit: top 12 bits of the order-preserving key
+        if (valid && sc != -INFINITY)   // exactly the keys the selection will see
+          atomicAdd(hist + static_cast<size_t>(w.t) * kScoreBins + (float_order(sc) >> 20), 1u);
+      }
       if (seg_end) {             // this warp is done with the segment's w'
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(B_SEG_WFREE + ss));
@@ -747,8 +759,8 @@ size_t score_tc_workspace(const ScoreParams &p) {
   return static_cast<size_t>(p.T) * lay.rec_bytes;
 }
 
-cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, float *scores, long long ld,
-                            cudaStream_t stream) {
+cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint32_t *hist, float *scores,
+                            long long ld, cudaStream_t stream) {
   TcLayout lay;
   if (!make_layout(p, &lay)) return cudaErrorNotSupported;
   auto encode = get_encode();
@@ -766,7 +778,7 @@ cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, floa
                                        static_cast<int>(lay.smem_bytes));
   if (e != cudaSuccess) return e;
   uint8_t *rec = static_cast<uint8_t *>(qrec);
-  qprep_kernel<<<dim3(static_cast<unsigned>(p.T), static_cast<unsigned>(lay.Npad / 8)), 256, 0, stream>>>(p, lay, rec);
+  qprep_kernel<<<dim3(static_cast<unsigned>(p.T), static_cast<unsigned>(lay.Npad / 8)), 256, 0, stream>>>(p, lay, rec, hist);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // The scorer may launch while qprep_kernel runs: its producer waits for the
   // records (griddepcontrol.wait) only before the first record copy.
@@ -780,7 +792,7 @@ cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, floa
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, score_tc_kernel, tmap, p, lay, static_cast<const uint8_t *>(rec), scores, ld);
+  return cudaLaunchKernelEx(&cfg, score_tc_kernel, tmap, p, lay, static_cast<const uint8_t *>(rec), hist, scores, ld);
 }
 
 }  // namespace idx
