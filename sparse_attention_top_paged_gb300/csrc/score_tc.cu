@@ -317,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // at most half the stages per batch, so the other half stays in flight
     // and no two tiles of a batch share a stage
     const int nb = min(8, ns / 2);
+    const uint64_t pol_stream = ptx::policy_evict_first();   // keys are read once
     int issued = 0, last_seg = -1;
     bool qrec_ready = false;
     for (int base = 0; base < n_tiles; base += nb) {
@@ -357,14 +358,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int rr = 0; rr < hi - lo; rr += lay.box_rows) {
               const uint32_t dst = ptx::smem_addr(stage + (dst_row + rr) * 64);
               asm volatile(
-                  "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-                  " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+                  "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                  " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
                   "l"(reinterpret_cast<uint64_t>(&tmap_nib)), "r"(0), "r"(static_cast<int>(row0 + rr)),
-                  "r"(full)
+                  "r"(full), "l"(pol_stream)
                   : "memory");
             }
-            ptx::bulk_g2s(ptx::smem_addr(stage + kScaleOff + dst_row * 8), p.key_scale + row0 * 8,
-                          static_cast<uint32_t>(hi - lo) * 8u, full);
+            ptx::bulk_g2s_hint(ptx::smem_addr(stage + kScaleOff + dst_row * 8), p.key_scale + row0 * 8,
+                               static_cast<uint32_t>(hi - lo) * 8u, full, pol_stream);
           }
         }
       }

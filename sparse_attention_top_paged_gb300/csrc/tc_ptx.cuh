@@ -92,6 +92,23 @@ __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol
 // ------------------------------------------------------------------ TMA ----
 // 1-D bulk copy global -> shared, completing `bytes` transactions on `bar`.
 // dst and src 16-byte aligned, bytes a multiple of 16.
+// L2 policy for data read once (streamed keys): evicted first, so what the
+// kernel writes (the score matrix, read next by the selection) stays in L2.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// As bulk_g2s, with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),

@@ -14,15 +14,19 @@
 //      key (the boundary bin) and the place in the output of every bin above;
 //   2. if the boundary bin holds more than kBndCap keys, its keys are
 //      histogrammed on the next digit (another pass) until it does not;
-//   3. decided on the first digit (the usual case): one pass drops every key
-//      at or above the boundary bin straight into its bin's segment of a
-//      shared-memory buffer (bins in descending order); each key is then
-//      ranked inside its bin — the boundary bin first split by the next 8
-//      bits — and written to its output slot. No sort.
-//      Decided on a later digit: one pass collects the keys at or above the
-//      boundary and a bitonic sort orders them.
+//   3. decided on the first digit with no bin above the boundary holding more
+//      than kRankBinMax keys (the decode case): one pass drops every key at
+//      or above the boundary bin straight into its bin's segment of a
+//      shared-memory buffer (bins in descending order); then each warp sorts
+//      whole bins in registers, one at a time, and writes every key to its
+//      output slot (its bin's start + its rank in the bin).
+//      Otherwise: one pass collects the keys at or above the boundary and a
+//      bitonic sort orders them.
+// The row streams through 16-byte loads, four per thread in flight, and its
+// first block is requested before the first digit is decided.
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace idx {
 namespace {
@@ -30,9 +34,13 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kBins = kScoreBins;                 // 12-bit digits
 constexpr int kPer = kBins / kThreads;            // bins each thread owns in a scan
-constexpr int kBndCap = 512;                      // largest boundary bin collected (else refine)
-constexpr int kUnroll = 8;                        // score loads in flight per thread
-static_assert(kBndCap <= kThreads, "the boundary-bin split holds one key per thread");
+constexpr int kBndCap = 2048;                     // largest boundary bin collected (else refine)
+constexpr int kRankBinMax = kBndCap;              // largest bin above the boundary ordered in place
+constexpr int kWarpBin = 64;                      // bins up to this size are sorted by one warp
+constexpr int kMaxLarge = 8;                      // more larger bins than this: sort the whole buffer
+constexpr int kLargeKeys = kBndCap / kThreads;    // a large bin's keys per thread
+constexpr int kUnroll = 4;                        // 16-byte score loads in flight per thread
+static_assert(kBndCap % kThreads == 0, "a large bin's keys spread evenly over the threads");
 
 __host__ __device__ inline int pow2_at_least(int k) {
   int kp = 1;
@@ -44,23 +52,34 @@ struct SelShared {
   uint32_t table[kBins];      // counts of the current digit; once the first digit decides,
                               // per bin: end of its buffer segment | count << 16
   uint32_t warp_sum[kThreads / 32];
-  uint32_t sub_cnt[256], sub_cur[256];  // the boundary bin's split by the next 8 bits
+  uint32_t warp_max[kThreads / 32];   // largest bin above the boundary (first digit)
   int b_bin, b_above, b_cnt;  // boundary bin, its keys above, its keys
   int n_buf;                  // append cursor (later-digit decisions)
+  int abort_flag;             // a staging copy never completed
+  uint32_t sub_cnt[256], sub_cur[256];  // a large bin's split by the next 8 key bits
+  int n_large;
+  uint32_t large[8];          // packed entries of the large bins (kMaxLarge)
 };
 
 // Dynamic shared memory: SelShared, then the key buffer: up to k - 1 keys
 // above the boundary bin plus at most kBndCap keys in it, rounded up to a
 // power of two (>= 64: the sort works on whole warps' 64-key segments).
+// Then the row staging area (a whole row of up to kStageMax scores, else
+// chunks of that size, copied in by one bulk copy each) and its mbarrier.
+constexpr int kStageMax = 32768;
 struct SelSmem {
-  size_t buf, cap, total;  // cap: keys the buffer holds
+  size_t buf, cap, stage, stage_floats, bar, total;  // cap: keys the buffer holds
 };
-__host__ __device__ inline SelSmem sel_smem(int k) {
+__host__ __device__ inline SelSmem sel_smem(int k, long long max_len) {
   SelSmem m{};
   m.buf = (sizeof(SelShared) + 15) & ~size_t(15);
   const int want = k + kBndCap;
   m.cap = static_cast<size_t>(pow2_at_least(want < 64 ? 64 : want));
-  m.total = m.buf + m.cap * 8;
+  m.stage = m.buf + m.cap * 8;
+  const long long sf = (max_len + 3) & ~3LL;
+  m.stage_floats = static_cast<size_t>(sf < kStageMax ? sf : kStageMax);
+  m.bar = m.stage + m.stage_floats * 4;
+  m.total = m.bar + 8;
   return m;
 }
 
@@ -126,31 +145,153 @@ __device__ __forceinline__ bool bad_len(const ScoreParams &p, int L) {
   return L < 0 || static_cast<long long>(L) > static_cast<long long>(p.max_lb) * p.epb;
 }
 
-// Calls f(key) for every key of row[0 .. L) that is not -inf, kUnroll loads
-// in flight per thread.
-template <class F>
-__device__ __forceinline__ void for_each_key(const float *row, int L, F &&f) {
-  for (long long base = 0; base < L; base += kThreads * kUnroll) {
-    float v[kUnroll];
+// The scores of one row, read pass by pass. A 16-byte-aligned row comes in
+// through bulk copies into shared memory, kStageMax scores at a time (a row
+// that fits stays resident across passes; the first copy is issued before the
+// first digit is decided); another row is read with 16-byte global loads,
+// four per thread in flight. pass(thr, f) calls f(key) for every key whose
+// score is not -inf and whose order (the key's top 32 bits) is >= thr.
+constexpr int kBlock = kThreads * 4 * kUnroll;
+struct RowSource {
+  const float *row;
+  int L;
+  bool staged;
+  float *stage;
+  int chunk;            // scores per staged chunk
+  uint32_t bar, phase;  // staging mbarrier and the parity of its next phase
+  int resident, pending;
+  volatile int *abort;
+
+  template <class F>
+  __device__ __forceinline__ static void key4(float4 v, long long i0, uint32_t thr, F &f) {
+    const float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const long long i = base + u * kThreads + threadIdx.x;
-      v[u] = (i < L) ? row[i] : -INFINITY;
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const long long i = base + u * kThreads + threadIdx.x;
-      if (v[u] != -INFINITY) f(pack_key(v[u], static_cast<int32_t>(i)));
+    for (int q = 0; q < 4; ++q) {
+      if (e[q] == -INFINITY) continue;
+      const uint32_t o = float_order(e[q]);
+      if (o >= thr)
+        f((static_cast<uint64_t>(o) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(i0 + q)));
     }
   }
+  // Thread 0 starts copying chunk c (its 16-byte part; the tail of at most
+  // three scores is read from global memory when processed).
+  __device__ void issue(int c) {
+    if (threadIdx.x == 0) {
+      const long long c0 = static_cast<long long>(c) * chunk;
+      const int n4 = static_cast<int>(min(static_cast<long long>(chunk), L - c0)) & ~3;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (n4 > 0) {
+        ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n4) * 4u);
+        ptx::bulk_g2s(ptx::smem_addr(stage), row + c0, static_cast<uint32_t>(n4) * 4u, bar);
+      } else {
+        ptx::mbar_arrive(bar);
+      }
+    }
+    pending = c;
+  }
+  __device__ void prefetch() {
+    if (staged && L > 0) issue(0);
+  }
+  __device__ void wait() {
+    if (!ptx::mbar_wait(bar, phase, abort, 2000000000ull)) {
+      volatile int no_abort = 0;   // give up on this row, but never leave with the copy in flight
+      ptx::mbar_wait(bar, phase, &no_abort, 2000000000ull);
+    }
+    phase ^= 1u;
+  }
+  template <class F>
+  __device__ void pass(uint32_t thr, F &&f) {
+    if (!staged) {
+      for (long long base = 0; base < L; base += kBlock) {
+        float4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const long long i0 = base + 4LL * (u * kThreads + threadIdx.x);
+          v[u].x = (i0 + 0 < L) ? row[i0 + 0] : -INFINITY;
+          v[u].y = (i0 + 1 < L) ? row[i0 + 1] : -INFINITY;
+          v[u].z = (i0 + 2 < L) ? row[i0 + 2] : -INFINITY;
+          v[u].w = (i0 + 3 < L) ? row[i0 + 3] : -INFINITY;
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) key4(v[u], base + 4LL * (u * kThreads + threadIdx.x), thr, f);
+      }
+      return;
+    }
+    const int nch = static_cast<int>((static_cast<long long>(L) + chunk - 1) / chunk);
+    for (int c = 0; c < nch; ++c) {
+      if (resident != c) {
+        if (pending != c) {
+          __syncthreads();   // everyone is done with the previous chunk
+          issue(c);
+        }
+        wait();
+        resident = c;
+        pending = -1;
+      }
+      // (after a copy that never completed the chunk holds stale scores: the
+      // pass goes on, every index stays bounded, and the call reports it)
+      const long long c0 = static_cast<long long>(c) * chunk;
+      const int n = static_cast<int>(min(static_cast<long long>(chunk), L - c0)), n4 = n & ~3;
+      const float4 *s4 = reinterpret_cast<const float4 *>(stage);
+      for (int i = threadIdx.x; i < (n4 >> 2); i += kThreads) key4(s4[i], c0 + 4LL * i, thr, f);
+      for (int i = n4 + threadIdx.x; i < n; i += kThreads) {
+        const float e = row[c0 + i];
+        if (e == -INFINITY) continue;
+        const uint32_t o = float_order(e);
+        if (o >= thr) f((static_cast<uint64_t>(o) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(c0 + i)));
+      }
+    }
+  }
+};
+
+// One warp sorts buf[start .. start+n) (n <= 32*E) descending in registers
+// (E keys per lane, lane l holding positions l*E .. l*E+E-1; padding keys 0
+// sort last) and hands each key with its final position to emit.
+template <int E, class Emit>
+__device__ __forceinline__ void warp_sort_segment(const uint64_t *buf, int start, int n, Emit &emit) {
+  const int lane = threadIdx.x & 31;
+  uint64_t v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = (lane * E + e < n) ? buf[start + lane * E + e] : 0ull;
+  constexpr int m = 32 * E;
+#pragma unroll
+  for (int sz = 2; sz <= m; sz <<= 1) {
+#pragma unroll
+    for (int s = sz >> 1; s > 0; s >>= 1) {
+      if (s < E) {  // both keys of a pair in this lane
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if ((e & s) == 0) {
+            const bool desc = (((lane * E + e) & sz) == 0);
+            if ((v[e] < v[e | s]) == desc) {
+              const uint64_t x = v[e];
+              v[e] = v[e | s];
+              v[e | s] = x;
+            }
+          }
+        }
+      } else {      // partner in lane ^ (s / E)
+        const int ls = s / E;
+        const bool lower = (lane & ls) == 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const uint64_t pv = __shfl_xor_sync(0xFFFFFFFFu, v[e], ls);
+          const bool desc = (((lane * E + e) & sz) == 0);
+          v[e] = (lower == desc) ? (v[e] > pv ? v[e] : pv) : (v[e] < pv ? v[e] : pv);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (lane * E + e < n) emit(v[e], start + lane * E + e);
 }
 
-
-__global__ void __launch_bounds__(kThreads) topk_stream_kernel(ScoreParams p, const float *__restrict__ scores,
+__global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p, const float *__restrict__ scores,
                                                               long long ld, const uint32_t *__restrict__ hist) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SelShared *sh = reinterpret_cast<SelShared *>(smem_raw);
-  const SelSmem lay = sel_smem(p.top_k);
+  const SelSmem lay = sel_smem(p.top_k, static_cast<long long>(p.max_lb) * p.epb);
   uint64_t *buf = reinterpret_cast<uint64_t *>(smem_raw + lay.buf);
   const int cap = static_cast<int>(lay.cap);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -172,6 +313,16 @@ __global__ void __launch_bounds__(kThreads) topk_stream_kernel(ScoreParams p, co
     return;
   }
   const float *row = scores + static_cast<long long>(t) * ld;
+  const uint32_t sbar = ptx::smem_addr(smem_raw + lay.bar);
+  RowSource rs{row, L, lay.stage_floats > 0 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0,
+               reinterpret_cast<float *>(smem_raw + lay.stage), static_cast<int>(lay.stage_floats), sbar, 0u, -1, -1,
+               &sh->abort_flag};
+  if (tid == 0) {
+    sh->abort_flag = 0;
+    ptx::mbar_init(sbar, 1);
+    ptx::fence_mbar_init();
+  }
+  rs.prefetch();   // the row is on its way while the first digit is decided
   if (tid == 0) {
     sh->b_bin = 0;
     sh->b_above = 0;
@@ -195,7 +346,7 @@ __global__ void __launch_bounds__(kThreads) topk_stream_kernel(ScoreParams p, co
     } else {
       for (int b = tid; b < kBins; b += kThreads) sh->table[b] = 0u;
       __syncthreads();
-      for_each_key(row, L, [&](uint64_t key) {
+      rs.pass(0u, [&](uint64_t key) {
         if ((key & mask) == prefix) atomicAdd(&sh->table[static_cast<uint32_t>(key >> shift) & dmask], 1u);
       });
       __syncthreads();
@@ -225,12 +376,17 @@ __global__ void __launch_bounds__(kThreads) topk_stream_kernel(ScoreParams p, co
       // First digit: for every bin holding some of the k best keys, the end
       // of its segment (before any key is placed: its start) | its count.
       // Each thread rewrites only the bins it owns and has already read.
-      uint32_t rb = run0;
+      // Also the largest such bin other than the boundary bin.
+      uint32_t rb = run0, mx = 0;
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
-        if (c[j] != 0u && rb < static_cast<uint32_t>(k)) sh->table[kBins - 1 - kPer * tid - j] = rb | (c[j] << 16);
+        const bool rel = c[j] != 0u && rb < static_cast<uint32_t>(k);
+        sh->table[kBins - 1 - kPer * tid - j] = rel ? (rb | (c[j] << 16)) : 0u;   // 0: holds none of the k best
+        if (rel && (all <= static_cast<uint32_t>(k) || rb + c[j] < static_cast<uint32_t>(k))) mx = max(mx, c[j]);
         rb += c[j];
       }
+      mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+      if (lane == 0) sh->warp_max[warp] = mx;
     }
     all_keys = all;
     if (all <= static_cast<uint32_t>(need)) {
@@ -274,9 +430,13 @@ __global__ void __launch_bounds__(kThreads) topk_stream_kernel(ScoreParams p, co
   };
   int produced;  // output slots filled; the rest is padding
 
-  if ((take_all && rounds == 0) || (!take_all && rounds == 1)) {
+  uint32_t max_above = 0;   // largest first-digit bin above the boundary
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) max_above = max(max_above, sh->warp_max[w]);
+  if (((take_all && rounds == 0) || (!take_all && rounds == 1)) && max_above <= kRankBinMax) {
     // ---- decided on the first digit: place, rank, write ----
-    for_each_key(row, L, [&](uint64_t key) {
+    // (keys below the boundary bin are dropped on their top 32 bits alone)
+    rs.pass(static_cast<uint32_t>(prefix >> 32), [&](uint64_t key) {
       if ((key & mask) >= prefix) {
         const uint32_t old = atomicAdd(&sh->table[key >> 52], 1u);
         if (static_cast<int>(old & 0xFFFFu) < cap) buf[old & 0xFFFFu] = key;
@@ -284,73 +444,113 @@ __global__ void __launch_bounds__(kThreads) topk_stream_kernel(ScoreParams p, co
     });
     __syncthreads();
     const int total = min(take_all ? static_cast<int>(all_keys) : sh->b_above + sh->b_cnt, cap);
-    // rank of kv among buf[q0 .. q1): keys above it
-    auto rank_in = [&](uint64_t kv, int q0, int q1) {
-      int n = 0, q = q0;
-      for (; q + 8 <= q1; q += 8) {  // eight loads in flight per step
-        uint64_t x[8];
+    // Every bin holding some of the k best keys is now a contiguous segment
+    // of buf. Bins of more than kWarpBin keys ("large") are first ordered by
+    // the next 8 key bits, one bin at a time by the whole CTA, so each of
+    // their keys is then ranked only among keys sharing those bits too; the
+    // other bins are sorted by one warp each, in registers. Many large bins
+    // (broad selections) make one bitonic sort of the whole buffer cheaper.
+    if (tid == 0) sh->n_large = 0;
+    __syncthreads();
 #pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = buf[q + u];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) n += (x[u] > kv) ? 1 : 0;
-      }
-      for (; q < q1; ++q) n += (buf[q] > kv) ? 1 : 0;
-      return n;
-    };
-    // The boundary bin (often a few hundred keys) is first ordered by the
-    // next 8 key bits, so each of its keys is ranked only among keys sharing
-    // those too.
-    const int bs = take_all ? total : min(sh->b_above, total), be = total;
-    const bool split = be - bs > 64;
-    if (split) {
-      if (tid < 256) sh->sub_cnt[tid] = 0u;
-      __syncthreads();
-      const bool mine = bs + tid < be;       // one boundary key per thread
-      const uint64_t bk = mine ? buf[bs + tid] : 0ull;
-      const uint32_t sd = static_cast<uint32_t>(bk >> 44) & 255u;
-      if (mine) atomicAdd(&sh->sub_cnt[sd], 1u);
-      __syncthreads();
-      if (warp == 0) {  // descending exclusive scan: sub-bin d starts after all keys of sub-bins > d
-        uint32_t c8[8], tot = 0;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          c8[u] = sh->sub_cnt[255 - 8 * lane - u];
-          tot += c8[u];
-        }
-        uint32_t incl = tot;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        uint32_t r = incl - tot;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          sh->sub_cur[255 - 8 * lane - u] = r;
-          r += c8[u];
-        }
-      }
-      __syncthreads();
-      const uint32_t spos = mine ? atomicAdd(&sh->sub_cur[sd], 1u) : 0u;
-      __syncthreads();  // every boundary key is in a register: its segment may be rewritten
-      if (mine) buf[bs + static_cast<int>(spos)] = bk;
-      __syncthreads();
-      if (mine) {  // sub_cur[sd] now ends sub-bin sd's run; it starts sub_cnt[sd] earlier
-        const int q1 = bs + static_cast<int>(sh->sub_cur[sd]), q0 = q1 - static_cast<int>(sh->sub_cnt[sd]);
-        emit(bk, q0 + rank_in(bk, q0, q1));
+    for (int j = 0; j < kPer; ++j) {
+      const uint32_t e = sh->table[kBins - 1 - kPer * tid - j];
+      if (static_cast<int>(e >> 16) > kWarpBin) {
+        const int slot = atomicAdd(&sh->n_large, 1);
+        if (slot < kMaxLarge) sh->large[slot] = e;
       }
     }
-    for (int p0 = tid; p0 < (split ? bs : total); p0 += kThreads) {
-      const uint64_t kv = buf[p0];
-      const uint32_t pk = sh->table[kv >> 52];
-      const int end = min(static_cast<int>(pk & 0xFFFFu), total);
-      const int start = max(0, static_cast<int>(pk & 0xFFFFu) - static_cast<int>(pk >> 16));
-      emit(kv, start + rank_in(kv, start, end));
+    __syncthreads();
+    const int n_large = sh->n_large;
+    if (n_large > kMaxLarge) {
+      const int m = max(64, pow2_at_least(total));   // total <= k - 1 + kBndCap, m <= cap
+      for (int i = total + tid; i < m; i += kThreads) buf[i] = 0ull;
+      __syncthreads();
+      sort_desc(buf, m);
+      for (int i = tid; i < min(total, k); i += kThreads) emit(buf[i], i);
+    } else {
+      for (int x = 0; x < n_large; ++x) {
+        const uint32_t e = sh->large[x];
+        const int n = static_cast<int>(e >> 16);
+        const int start = max(0, min(static_cast<int>(e & 0xFFFFu) - n, total));
+        const int cnt = min(n, total - start);
+        if (tid < 256) sh->sub_cnt[tid] = 0u;
+        __syncthreads();
+        uint64_t kk[kLargeKeys];   // this thread's keys of the bin
+        uint32_t sd[kLargeKeys], sp[kLargeKeys];
+#pragma unroll
+        for (int u = 0; u < kLargeKeys; ++u) {
+          const int q = tid + u * kThreads;
+          kk[u] = (q < cnt) ? buf[start + q] : 0ull;
+          sd[u] = static_cast<uint32_t>(kk[u] >> 44) & 255u;
+          if (q < cnt) atomicAdd(&sh->sub_cnt[sd[u]], 1u);
+        }
+        __syncthreads();
+        if (warp == 0) {  // descending exclusive scan: sub-bin d starts after all keys of sub-bins > d
+          uint32_t c8[8], tot = 0;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            c8[u] = sh->sub_cnt[255 - 8 * lane - u];
+            tot += c8[u];
+          }
+          uint32_t incl = tot;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
+          }
+          uint32_t r = incl - tot;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            sh->sub_cur[255 - 8 * lane - u] = r;
+            r += c8[u];
+          }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kLargeKeys; ++u)
+          if (tid + u * kThreads < cnt) sp[u] = atomicAdd(&sh->sub_cur[sd[u]], 1u);
+        __syncthreads();   // the bin's keys are all in registers: its segment may be rewritten
+#pragma unroll
+        for (int u = 0; u < kLargeKeys; ++u)
+          if (tid + u * kThreads < cnt) buf[start + static_cast<int>(sp[u])] = kk[u];
+        __syncthreads();
+        // sub_cur[d] now ends sub-bin d's run; it starts sub_cnt[d] earlier
+#pragma unroll
+        for (int u = 0; u < kLargeKeys; ++u) {
+          if (tid + u * kThreads < cnt) {
+            const int q1 = start + static_cast<int>(sh->sub_cur[sd[u]]), q0 = q1 - static_cast<int>(sh->sub_cnt[sd[u]]);
+            int pos = q0;
+            for (int q = q0; q < q1; ++q) pos += (buf[q] > kk[u]) ? 1 : 0;
+            emit(kk[u], pos);
+          }
+        }
+        __syncthreads();   // sub_cnt / sub_cur are reused by the next large bin
+      }
+      // Warp w sorts the small bins w, w + 16, ... one at a time, in
+      // registers, and writes each key to its output slot.
+      auto emit_if = [&](uint64_t kv, int pos) { emit(kv, pos); };
+      for (int b0 = warp; b0 < kBins; b0 += 32 * (kThreads / 32)) {
+        const int b = b0 + (kThreads / 32) * lane;       // this lane's bin of the group
+        const uint32_t pk = (b < kBins) ? sh->table[b] : 0u;
+        uint32_t todo = __ballot_sync(0xFFFFFFFFu, pk != 0u && static_cast<int>(pk >> 16) <= kWarpBin);
+        while (todo) {
+          const int l = __ffs(todo) - 1;
+          todo &= todo - 1;
+          const uint32_t e = __shfl_sync(0xFFFFFFFFu, pk, l);
+          const int n = static_cast<int>(e >> 16);
+          const int start = max(0, min(static_cast<int>(e & 0xFFFFu) - n, total));   // the cursor ended at start + n
+          const int cnt = min(n, total - start);
+          if (cnt <= 32) warp_sort_segment<1>(buf, start, cnt, emit_if);
+          else warp_sort_segment<2>(buf, start, cnt, emit_if);
+        }
+      }
     }
     produced = min(total, k);
   } else {
-    // ---- decided on a later digit: collect, sort, write ----
-    for_each_key(row, L, [&](uint64_t key) {
+    // ---- decided on a later digit, or a bin above the boundary too large to
+    // rank by comparison: collect, sort, write ----
+    rs.pass(static_cast<uint32_t>(prefix >> 32), [&](uint64_t key) {
       if ((key & mask) >= prefix) {
         const int slot = atomicAdd(&sh->n_buf, 1);
         if (slot < cap) buf[slot] = key;
@@ -369,6 +569,7 @@ __global__ void __launch_bounds__(kThreads) topk_stream_kernel(ScoreParams p, co
     oi[i] = -1;
     os[i] = -INFINITY;
   }
+  if (tid == 0 && sh->abort_flag && p.dev_status) atomicOr(p.dev_status, IDX_STATUS_TIMEOUT);
 }
 
 }  // namespace
@@ -384,8 +585,7 @@ SelectPlan select_plan(int T, int top_k, long long max_len, bool have_scores_out
 }
 
 bool select_supported(int top_k, long long max_len) {
-  (void)max_len;
-  return sel_smem(top_k).total <= 227 * 1024;
+  return sel_smem(top_k, max_len).total <= 227 * 1024;
 }
 
 cudaError_t launch_select(const ScoreParams &p, const float *scores, long long ld, const uint32_t *hist,
@@ -393,7 +593,7 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
   (void)pl;
   (void)workspace;
   if (p.T == 0) return cudaSuccess;
-  const size_t smem = sel_smem(p.top_k).total;
+  const size_t smem = sel_smem(p.top_k, static_cast<long long>(p.max_lb) * p.epb).total;
   cudaError_t e =
       cudaFuncSetAttribute(topk_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
