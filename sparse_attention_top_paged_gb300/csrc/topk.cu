@@ -39,8 +39,6 @@ constexpr int kRankBinMax = kBndCap;              // largest bin above the bound
 constexpr int kWarpBin = 64;                      // bins up to this size are sorted by one warp
 constexpr int kMaxLarge = 8;                      // more larger bins than this: sort the whole buffer
 constexpr int kLargeKeys = kBndCap / kThreads;    // a large bin's keys per thread
-constexpr int kScatter = 12;                      // collected keys per thread
-static_assert(kScatter * kThreads >= kMaxTopK + kBndCap, "every key at or above the boundary bin fits in registers");
 constexpr int kUnroll = 4;                        // 16-byte score loads in flight per thread
 static_assert(kBndCap % kThreads == 0, "a large bin's keys spread evenly over the threads");
 
@@ -66,8 +64,8 @@ struct SelShared {
 // Dynamic shared memory: SelShared, then the key buffer: up to k - 1 keys
 // above the boundary bin plus at most kBndCap keys in it, rounded up to a
 // power of two (>= 64: the sort works on whole warps' 64-key segments).
-// Then the row staging area (a whole row of up to kStageMax scores, else two
-// buffers of kStageMax / 2) and its two mbarriers.
+// Then the row staging area (a whole row of up to kStageMax scores, else
+// chunks of that size, copied in by one bulk copy each) and its mbarrier.
 constexpr int kStageMax = 32768;
 struct SelSmem {
   size_t buf, cap, stage, stage_floats, bar, total;  // cap: keys the buffer holds
@@ -81,7 +79,7 @@ __host__ __device__ inline SelSmem sel_smem(int k, long long max_len) {
   const long long sf = (max_len + 3) & ~3LL;
   m.stage_floats = static_cast<size_t>(sf < kStageMax ? sf : kStageMax);
   m.bar = m.stage + m.stage_floats * 4;
-  m.total = m.bar + 16;   // two mbarriers
+  m.total = m.bar + 8;
   return m;
 }
 
@@ -148,76 +146,58 @@ __device__ __forceinline__ bool bad_len(const ScoreParams &p, int L) {
 }
 
 // The scores of one row, read pass by pass. A 16-byte-aligned row comes in
-// through bulk copies into shared memory: a row of up to kStageMax scores in
-// one buffer that stays resident across passes, a longer one in chunks of
-// kStageMax / 2 through two buffers, the next chunk copied while the current
-// one is processed. Each copy is split into pieces of up to kPiece scores
-// issued by the lanes of warp 0 side by side; the first copy is issued before
-// the first digit is decided. Another row is read with 16-byte global loads,
+// through bulk copies into shared memory, kStageMax scores at a time (a row
+// that fits stays resident across passes; the first copy is issued before the
+// first digit is decided); another row is read with 16-byte global loads,
 // four per thread in flight. pass(thr, f) calls f(key) for every key whose
 // score is not -inf and whose order (the key's top 32 bits) is >= thr.
 constexpr int kBlock = kThreads * 4 * kUnroll;
-constexpr int kPiece = 4096;
 struct RowSource {
   const float *row;
   int L;
   bool staged;
   float *stage;
-  int chunk;            // scores per chunk
-  int nch;              // chunks per pass
-  uint32_t bar0;        // mbarriers of buffers 0 and 1 (8 bytes apart)
+  int chunk;            // scores per staged chunk
+  uint32_t bar, phase;  // staging mbarrier and the parity of its next phase
+  int resident, pending;
   volatile int *abort;
-  // per buffer b: parity of the mbarrier's next phase, chunk held or being
-  // copied, copy in flight (two named fields each, kept in registers)
-  uint32_t phase0 = 0u, phase1 = 0u;
-  int held0 = -1, held1 = -1;
-  bool inflight0 = false, inflight1 = false;
 
-  __device__ int buf_of(int c) const { return nch > 1 ? (c & 1) : 0; }
-  __device__ int &held(int b) { return b ? held1 : held0; }
-  __device__ bool &inflight(int b) { return b ? inflight1 : inflight0; }
-  __device__ uint32_t &phase(int b) { return b ? phase1 : phase0; }
   template <class F>
-  __device__ __forceinline__ static void key1(float e, long long i, uint32_t thr, F &f) {
-    if (e == -INFINITY) return;
-    const uint32_t o = float_order(e);
-    if (o >= thr) f((static_cast<uint64_t>(o) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(i)));
+  __device__ __forceinline__ static void key4(float4 v, long long i0, uint32_t thr, F &f) {
+    const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (e[q] == -INFINITY) continue;
+      const uint32_t o = float_order(e[q]);
+      if (o >= thr)
+        f((static_cast<uint64_t>(o) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(i0 + q)));
+    }
   }
-  // Warp 0 starts copying chunk c (its 16-byte part; the tail of at most
+  // Thread 0 starts copying chunk c (its 16-byte part; the tail of at most
   // three scores is read from global memory when processed).
   __device__ void issue(int c) {
-    const int b = buf_of(c);
-    if ((threadIdx.x >> 5) == 0) {
-      const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
       const long long c0 = static_cast<long long>(c) * chunk;
       const int n4 = static_cast<int>(min(static_cast<long long>(chunk), L - c0)) & ~3;
-      const uint32_t bar = bar0 + 8u * b;
-      if (lane == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (n4 > 0) ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n4) * 4u);
-        else ptx::mbar_arrive(bar);
-      }
-      __syncwarp();
-      for (int q = lane * kPiece; q < n4; q += 32 * kPiece) {
-        const int len = min(kPiece, n4 - q);
-        ptx::bulk_g2s(ptx::smem_addr(stage + static_cast<size_t>(b) * chunk + q), row + c0 + q,
-                      static_cast<uint32_t>(len) * 4u, bar);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (n4 > 0) {
+        ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n4) * 4u);
+        ptx::bulk_g2s(ptx::smem_addr(stage), row + c0, static_cast<uint32_t>(n4) * 4u, bar);
+      } else {
+        ptx::mbar_arrive(bar);
       }
     }
-    held(b) = c;
-    inflight(b) = true;
+    pending = c;
   }
   __device__ void prefetch() {
     if (staged && L > 0) issue(0);
   }
-  __device__ void wait(int b) {
-    const uint32_t bar = bar0 + 8u * b;
-    if (!ptx::mbar_wait(bar, phase(b), abort, 2000000000ull)) {
+  __device__ void wait() {
+    if (!ptx::mbar_wait(bar, phase, abort, 2000000000ull)) {
       volatile int no_abort = 0;   // give up on this row, but never leave with the copy in flight
-      ptx::mbar_wait(bar, phase(b), &no_abort, 2000000000ull);
+      ptx::mbar_wait(bar, phase, &no_abort, 2000000000ull);
     }
-    phase(b) ^= 1u;
-    inflight(b) = false;
+    phase ^= 1u;
   }
   template <class F>
   __device__ void pass(uint32_t thr, F &&f) {
@@ -233,103 +213,32 @@ struct RowSource {
           v[u].w = (i0 + 3 < L) ? row[i0 + 3] : -INFINITY;
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const long long i0 = base + 4LL * (u * kThreads + threadIdx.x);
-          key1(v[u].x, i0, thr, f);
-          key1(v[u].y, i0 + 1, thr, f);
-          key1(v[u].z, i0 + 2, thr, f);
-          key1(v[u].w, i0 + 3, thr, f);
-        }
+        for (int u = 0; u < kUnroll; ++u) key4(v[u], base + 4LL * (u * kThreads + threadIdx.x), thr, f);
       }
       return;
     }
+    const int nch = static_cast<int>((static_cast<long long>(L) + chunk - 1) / chunk);
     for (int c = 0; c < nch; ++c) {
-      if (held(buf_of(c)) != c) {   // (only at a pass's first chunk)
-        __syncthreads();
-        issue(c);
+      if (resident != c) {
+        if (pending != c) {
+          __syncthreads();   // everyone is done with the previous chunk
+          issue(c);
+        }
+        wait();
+        resident = c;
+        pending = -1;
       }
-      if (nch > 1 && c + 1 < nch && held(buf_of(c + 1)) != c + 1) {
-        __syncthreads();   // everyone is done with the chunk this buffer held
-        issue(c + 1);      // copied while chunk c is processed
-      }
-      if (inflight(buf_of(c))) wait(buf_of(c));
       // (after a copy that never completed the chunk holds stale scores: the
       // pass goes on, every index stays bounded, and the call reports it)
       const long long c0 = static_cast<long long>(c) * chunk;
       const int n = static_cast<int>(min(static_cast<long long>(chunk), L - c0)), n4 = n & ~3;
-      const float4 *s4 = reinterpret_cast<const float4 *>(stage + static_cast<size_t>(buf_of(c)) * chunk);
-      for (int i = threadIdx.x; i < (n4 >> 2); i += kThreads) {
-        const float4 v = s4[i];
-        const long long i0 = c0 + 4LL * i;
-        key1(v.x, i0, thr, f);
-        key1(v.y, i0 + 1, thr, f);
-        key1(v.z, i0 + 2, thr, f);
-        key1(v.w, i0 + 3, thr, f);
-      }
-      for (int i = n4 + threadIdx.x; i < n; i += kThreads) key1(row[c0 + i], c0 + i, thr, f);
-    }
-  }
-  // Appends every key of the row whose order is >= thr and whose masked bits
-  // are >= pfx to out[*count ...] (unordered, at most cap kept). Lanes test
-  // their keys side by side and each warp takes its slots with one atomic per
-  // step, so a burst of keys of one bin costs no same-address contention.
-  __device__ void collect(uint32_t thr, uint64_t pfx, uint64_t msk, uint64_t *out, int *count, int cap) {
-    const int lane = threadIdx.x & 31;
-    auto put = [&](bool take, uint64_t key) {
-      const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
-      if (m == 0u) return;
-      int base = 0;
-      if (lane == 0) base = atomicAdd(count, __popc(m));
-      base = __shfl_sync(0xFFFFFFFFu, base, 0);
-      const int slot = base + __popc(m & lanemask_lt());
-      if (take && slot < cap) out[slot] = key;
-    };
-    auto test = [&](float e, long long i, bool valid) {
-      bool take = false;
-      uint64_t key = 0ull;
-      if (valid && e != -INFINITY) {
+      const float4 *s4 = reinterpret_cast<const float4 *>(stage);
+      for (int i = threadIdx.x; i < (n4 >> 2); i += kThreads) key4(s4[i], c0 + 4LL * i, thr, f);
+      for (int i = n4 + threadIdx.x; i < n; i += kThreads) {
+        const float e = row[c0 + i];
+        if (e == -INFINITY) continue;
         const uint32_t o = float_order(e);
-        if (o >= thr) {
-          key = (static_cast<uint64_t>(o) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(i));
-          take = (key & msk) >= pfx;
-        }
-      }
-      put(take, key);
-    };
-    const int wbase = threadIdx.x - lane;   // loops below are uniform over each warp
-    if (!staged) {
-      for (long long base = 0; base < L; base += kThreads) {
-        const long long i = base + wbase + lane;
-        test(i < L ? row[i] : -INFINITY, i, i < L);
-      }
-      return;
-    }
-    for (int c = 0; c < nch; ++c) {
-      if (held(buf_of(c)) != c) {
-        __syncthreads();
-        issue(c);
-      }
-      if (nch > 1 && c + 1 < nch && held(buf_of(c + 1)) != c + 1) {
-        __syncthreads();
-        issue(c + 1);
-      }
-      if (inflight(buf_of(c))) wait(buf_of(c));
-      const long long c0 = static_cast<long long>(c) * chunk;
-      const int n = static_cast<int>(min(static_cast<long long>(chunk), L - c0)), n4 = n & ~3;
-      const float4 *s4 = reinterpret_cast<const float4 *>(stage + static_cast<size_t>(buf_of(c)) * chunk);
-      for (int i0 = wbase; i0 < (n4 >> 2); i0 += kThreads) {
-        const int i = i0 + lane;
-        const bool valid = i < (n4 >> 2);
-        const float4 v = valid ? s4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-        const long long k0 = c0 + 4LL * i;
-        test(v.x, k0, valid);
-        test(v.y, k0 + 1, valid);
-        test(v.z, k0 + 2, valid);
-        test(v.w, k0 + 3, valid);
-      }
-      for (int i0 = n4 + wbase; i0 < n; i0 += kThreads) {
-        const int i = i0 + lane;
-        test(i < n ? row[c0 + i] : -INFINITY, c0 + i, i < n);
+        if (o >= thr) f((static_cast<uint64_t>(o) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(c0 + i)));
       }
     }
   }
@@ -405,18 +314,14 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p,
   }
   const float *row = scores + static_cast<long long>(t) * ld;
   const uint32_t sbar = ptx::smem_addr(smem_raw + lay.bar);
-  const int sf = static_cast<int>(lay.stage_floats);
-  const int chunk = (L <= sf) ? sf : sf / 2;   // whole row, or two buffers
-  RowSource rs{row, L, sf >= 8 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0,
-               reinterpret_cast<float *>(smem_raw + lay.stage), max(chunk, 4), 0, sbar, &sh->abort_flag};
-  rs.nch = (L + rs.chunk - 1) / rs.chunk;
+  RowSource rs{row, L, lay.stage_floats > 0 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0,
+               reinterpret_cast<float *>(smem_raw + lay.stage), static_cast<int>(lay.stage_floats), sbar, 0u, -1, -1,
+               &sh->abort_flag};
   if (tid == 0) {
     sh->abort_flag = 0;
     ptx::mbar_init(sbar, 1);
-    ptx::mbar_init(sbar + 8u, 1);
     ptx::fence_mbar_init();
   }
-  __syncthreads();   // the barriers are initialised before warp 0 uses them
   rs.prefetch();   // the row is on its way while the first digit is decided
   if (tid == 0) {
     sh->b_bin = 0;
@@ -441,11 +346,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p,
     } else {
       for (int b = tid; b < kBins; b += kThreads) sh->table[b] = 0u;
       __syncthreads();
-      const uint64_t pfx = prefix, msk = mask;
-      const int sft = shift;
-      const uint32_t dm = dmask;
-      rs.pass(0u, [=](uint64_t key) {
-        if ((key & msk) == pfx) atomicAdd(&sh->table[static_cast<uint32_t>(key >> sft) & dm], 1u);
+      rs.pass(0u, [&](uint64_t key) {
+        if ((key & mask) == prefix) atomicAdd(&sh->table[static_cast<uint32_t>(key >> shift) & dmask], 1u);
       });
       __syncthreads();
 #pragma unroll
@@ -534,25 +436,12 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p,
   if (((take_all && rounds == 0) || (!take_all && rounds == 1)) && max_above <= kRankBinMax) {
     // ---- decided on the first digit: place, rank, write ----
     // (keys below the boundary bin are dropped on their top 32 bits alone)
-    rs.collect(static_cast<uint32_t>(prefix >> 32), prefix, mask, buf, &sh->n_buf, cap);
-    __syncthreads();
-    {  // then into their bins' segments (bins in descending order)
-      const int nc = min(min(sh->n_buf, cap), kScatter * kThreads);
-      uint64_t kk[kScatter];
-#pragma unroll
-      for (int u = 0; u < kScatter; ++u) {
-        const int q = tid + u * kThreads;
-        kk[u] = (q < nc) ? buf[q] : 0ull;
+    rs.pass(static_cast<uint32_t>(prefix >> 32), [&](uint64_t key) {
+      if ((key & mask) >= prefix) {
+        const uint32_t old = atomicAdd(&sh->table[key >> 52], 1u);
+        if (static_cast<int>(old & 0xFFFFu) < cap) buf[old & 0xFFFFu] = key;
       }
-      __syncthreads();   // every collected key is in a register
-#pragma unroll
-      for (int u = 0; u < kScatter; ++u) {
-        if (tid + u * kThreads < nc) {
-          const uint32_t old = atomicAdd(&sh->table[kk[u] >> 52], 1u);
-          if (static_cast<int>(old & 0xFFFFu) < cap) buf[old & 0xFFFFu] = kk[u];
-        }
-      }
-    }
+    });
     __syncthreads();
     const int total = min(take_all ? static_cast<int>(all_keys) : sh->b_above + sh->b_cnt, cap);
     // Every bin holding some of the k best keys is now a contiguous segment
@@ -661,7 +550,12 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p,
   } else {
     // ---- decided on a later digit, or a bin above the boundary too large to
     // rank by comparison: collect, sort, write ----
-    rs.collect(static_cast<uint32_t>(prefix >> 32), prefix, mask, buf, &sh->n_buf, cap);
+    rs.pass(static_cast<uint32_t>(prefix >> 32), [&](uint64_t key) {
+      if ((key & mask) >= prefix) {
+        const int slot = atomicAdd(&sh->n_buf, 1);
+        if (slot < cap) buf[slot] = key;
+      }
+    });
     __syncthreads();
     const int count = min(sh->n_buf, cap);
     const int m = max(64, pow2_at_least(count));
