@@ -1,7 +1,7 @@
 """Benchmark of the lightning-indexer hot path on GB300.
 
-One step = one idx_score_topk call (tcgen05 scoring kernel, then the chunk
-top-k and merge kernels) over the batched-decode workload: T=64 queries, H=64 heads, D=128,
+One step = one idx_score_topk call (q preparation, the tcgen05 scoring kernel,
+then the selection kernel) over the batched-decode workload: T=64 queries, H=64 heads, D=128,
 valid lengths uniform in [8192, 32768], 64-entry blocks, per-query block tables
 over a 40000-block NVFP4 pool, top_k=512. Inputs are seeded and synthetic and
 resident in HBM when timing starts; L2 is flushed (a 256 MB write) before
@@ -38,13 +38,25 @@ if ROOT not in sys.path:
 METRIC = "indexer (query,key) scores+top-k per sec; % of HBM / tensor-core roofline"
 UNIT = "pairs/s"
 BYTES_PER_PAIR = 64 + 8 + 4.0 / 64 + 4.0 / 64     # nibbles + E4M3 scales + gscale + table entry
-WORKLOAD = "batched_decode"
+
+# name -> (generator name in workloads, base seed, valid-length description, table description)
+WORKLOADS = {
+    "batched_decode": ("batched_decode", 1001, "valid_lens~U[8192,32768]", "per-query block tables"),
+    "long_decode": ("long_decode", 1002, "valid_lens=262144", "per-query block tables"),
+    "prefill": ("prefill", 1003, "valid_lens=(r+28672)//4", "one shared block table"),
+}
+
+
+def make_workload(name: str, seed: int):
+    from sparse_attention_top_paged_gb300 import workloads
+    return getattr(workloads, WORKLOADS[name][0])(seed)
 
 
 def workload_config(W):
+    _, _, lens, table = WORKLOADS[W.name]
     return {
-        "workload": f"{WORKLOAD}: T={W.T} H={W.H} D={W.D} valid_lens~U[8192,32768] epb={W.epb} "
-                    f"P={W.P} top_k={W.top_k} NVFP4 keys, per-query block tables",
+        "workload": f"{W.name}: T={W.T} H={W.H} D={W.D} {lens} epb={W.epb} "
+                    f"P={W.P} top_k={W.top_k} NVFP4 keys, {table}",
         "T": W.T, "H": W.H, "D": W.D, "entries_per_block": W.epb, "pool_blocks": W.P,
         "top_k": W.top_k, "pairs_per_step": W.pairs,
         "l2": "flushed before every timed step (256 MB write, outside the timed events)",
@@ -52,9 +64,9 @@ def workload_config(W):
     }
 
 
-def rank_seed(rank: int) -> int:
-    """Each rank scores its own batch (weak scaling): seed 1001 + rank."""
-    return 1001 + rank
+def rank_seed(name: str, rank: int) -> int:
+    """Each rank scores its own batch (weak scaling): the workload's seed + rank."""
+    return WORKLOADS[name][1] + rank
 
 
 def whole_job(pairs_per_rank, steps: int, seconds_per_rank, dist=None, device=None):
@@ -85,14 +97,15 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
-def recorded_traffic():
+def recorded_traffic(name: str):
     """DRAM bytes per launch of the scoring kernel from the committed ncu
-    summary, or None when those counters were taken on other kernel sources."""
+    summary, or None when those counters were taken on another workload or
+    on other kernel sources."""
     tfile = os.path.join(ROOT, "profiles", "score_tc_kernel.traffic.json")
     if not os.path.exists(tfile):
         return None
     rec = json.load(open(tfile))
-    if rec.get("source_sha256") != kernel_source_hash():
+    if rec.get("source_sha256") != kernel_source_hash() or rec.get("workload_name") != name:
         return None
     return rec.get("bytes_per_launch")
 
@@ -104,11 +117,32 @@ def launches_per_step(W) -> int:
 
 
 def peaks():
+    """(HBM GB/s, dense bf16/f16 tensor TFLOP/s burst, "measured"|"fallback")."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def roofline(W, kern_s):
+    """Roofline of the scoring kernel (q preparation + scorer). Decode
+    workloads stream every key once: HBM bound, 72.125 B per pair plus q, w
+    and the length per query. Prefill shares 128 blocks of keys between 4096
+    rows: the 2*H*D flops per pair on the tensor cores bound it (f16 runs at
+    the bf16 rate)."""
+    hbm, tensor, kind = peaks()
+    if W.name == "prefill":
+        flops = 2.0 * W.H * W.D * W.pairs
+        achieved = flops / kern_s / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": tensor, "unit": "TFLOP/s",
+                "frac": achieved / tensor, "traffic": None, "kernel": "score_tc_kernel",
+                "peak_kind": kind, "algorithmic_flops_per_launch": flops}
+    algo_bytes = W.pairs * BYTES_PER_PAIR + W.T * (4 * W.H * W.D + 4 * W.H + 4)
+    achieved = algo_bytes / kern_s / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": recorded_traffic(W.name), "kernel": "score_tc_kernel", "peak_kind": kind,
+            "algorithmic_bytes_per_launch": algo_bytes}
 
 
 class ClockSampler:
@@ -132,6 +166,12 @@ class ClockSampler:
             self.thread.start()
         except OSError:
             self.proc = None
+            return self
+        # nvidia-smi takes a moment to start: wait for its first sample so the
+        # samples cover the timed region
+        t0 = time.perf_counter()
+        while not self.lines and time.perf_counter() - t0 < 5.0 and self.proc.poll() is None:
+            time.sleep(0.01)
         return self
 
     def _read(self):
@@ -164,58 +204,77 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _oracle_sample(args):
-    """Runs in a spawned process: the float64 oracle on the first n queries."""
-    seed, n_queries, threads = args
+def _oracle_run(W, rows, cap=None):
+    """The float64 oracle on query rows ``rows`` of W, each truncated to its
+    first ``cap`` keys when cap is given. Returns (pairs, seconds)."""
+    import numpy as np
+    import oracle
+    lens = W.valid_lens if cap is None else np.minimum(W.valid_lens, cap).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.score_topk(W.q, W.w, W.block_table, W.bt_stride, W.max_lb, lens, W.epb, W.top_k,
+                      rows=list(rows), **W.oracle_kwargs())
+    dt = time.perf_counter() - t0
+    return int(sum(int(lens[t]) for t in rows)), dt
+
+
+def _set_threads(threads: int):
     os.environ["OPENBLAS_NUM_THREADS"] = str(threads)
     os.environ["OMP_NUM_THREADS"] = str(threads)
-    import numpy as np  # noqa: F401
-    import oracle
-    from sparse_attention_top_paged_gb300 import workloads as wl
-    W = wl.batched_decode(seed)
-    rows = list(range(n_queries))
-    t0 = time.perf_counter()
-    oracle.score_topk(W.q, W.w, W.block_table, W.bt_stride, W.max_lb, W.valid_lens, W.epb, W.top_k,
-                      rows=rows, **W.oracle_kwargs())
-    dt = time.perf_counter() - t0
-    pairs = int(sum(int(W.valid_lens[t]) for t in rows))
-    return pairs, dt
 
 
-def cpu_baseline(seed: int, n_queries: int):
+def _oracle_sample(args):
+    """Runs in a spawned process: the float64 oracle on the first n queries."""
+    name, seed, n_queries, threads = args
+    _set_threads(threads)
+    W = make_workload(name, seed)
+    n = min(n_queries, W.T)
+    return _oracle_run(W, range(n)) + (n,)
+
+
+def cpu_baseline(name: str, seed: int, n_queries: int):
     import multiprocessing as mp
     cores = len(os.sched_getaffinity(0))
     ctx = mp.get_context("spawn")
     with ctx.Pool(1) as pool:
-        pairs, dt = pool.apply(_oracle_sample, ((seed, n_queries, cores),))
+        pairs, dt, n = pool.apply(_oracle_sample, ((name, seed, n_queries, cores),))
     return {"value": pairs / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"first {n_queries} of the {WORKLOAD} queries ({pairs} pairs), numpy float64, "
+            "sample": f"first {n} of the {name} queries ({pairs} pairs), numpy float64, "
                       f"{dt:.2f} s", "seconds": dt}
 
 
+REFERENCE_BUDGET_S = 120.0
+
+
 def run_reference(args, rank, world):
-    """The CPU oracle as the reference arm: each step is a bounded sample."""
+    """The CPU oracle as the reference arm. Every step scores one query row
+    (rows taken in turn), truncated to its first n keys, where n is sized from
+    a calibration run so that all timed steps together take about two
+    minutes of oracle time."""
     if rank != 0:
         return
-    from sparse_attention_top_paged_gb300 import workloads as wl
-    W = wl.batched_decode(1001)
-    n_q = args.ref_queries
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm-up state; warm-up steps are skipped
+    cores = len(os.sched_getaffinity(0))
+    _set_threads(cores)
+    name = args.workload
+    W = make_workload(name, WORKLOADS[name][1])
+    p, dt = _oracle_run(W, [0])                  # calibration, untimed
+    per_step = max(256, min(int(W.valid_lens.max()), int(p / dt * REFERENCE_BUDGET_S / max(args.steps, 1))))
+    for i in range(args.warmup):
+        _oracle_run(W, [i % W.T], per_step)
     times, pairs = [], 0
-    for _ in range(args.steps):
-        p, dt = _oracle_sample((1001, n_q, len(os.sched_getaffinity(0))))
+    for i in range(args.steps):
+        p, dt = _oracle_run(W, [i % W.T], per_step)
         times.append(dt)
         pairs += p
     total = sum(times)
     value = pairs / total
-    cores = len(os.sched_getaffinity(0))
+    sample = (f"one query row per step (rows in turn), at most its first {per_step} keys "
+              f"(rows hold {int(W.valid_lens.min())}..{int(W.valid_lens.max())}), numpy float64")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(W), "impl": "reference",
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"first {n_q} queries per step, numpy float64"},
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -223,11 +282,11 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "tensor", "simt"])
-    ap.add_argument("--ref-queries", type=int, default=4)
+    ap.add_argument("--workload", default="batched_decode", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-queries", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -240,16 +299,13 @@ def main():
     if args.impl == "reference":
         return run_reference(args, rank, world)
 
-    import numpy as np
     import torch
     import sparse_attention_top_paged_gb300 as idx
-    from sparse_attention_top_paged_gb300 import _lib
-    from sparse_attention_top_paged_gb300 import workloads as wl
 
     # the CPU baseline runs in a spawned process before any GPU work
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(1001, args.cpu_queries)
+        cpu = cpu_baseline(args.workload, rank_seed(args.workload, 0), args.cpu_queries)
 
     torch.cuda.set_device(local)
     dist = None
@@ -257,7 +313,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    W = wl.batched_decode(rank_seed(rank))
+    W = make_workload(args.workload, rank_seed(args.workload, rank))
     dev = torch.device("cuda", local)
     q = torch.from_numpy(W.q).to(dev)
     w = torch.from_numpy(W.w).to(dev)
@@ -274,7 +330,8 @@ def main():
     lib = idx.load_library()
     stream = torch.cuda.current_stream(dev)
 
-    a = idx.make_score_args(q, w, bt, vl, k, entries_per_block=W.epb, keys_fp4=fp4, key_scale=sc,
+    a = idx.make_score_args(q, w, bt, vl, k, entries_per_block=W.epb, bt_stride=W.bt_stride,
+                            keys_fp4=fp4, key_scale=sc,
                             key_gscale=gs, topk_idx=out_i, topk_score=out_s, dev_status=status,
                             path=args.path)
     ws_bytes = idx.score_topk_workspace_bytes(a)
@@ -303,7 +360,13 @@ def main():
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    # The scoring kernel is bracketed by events on every KSAMPLE-th timed step:
+    # an event recorded between the scorer and the selection kernel stops the
+    # selection's programmatic early launch (about 5 us per step), so
+    # bracketing every step would inflate the step time it is part of.
+    KSAMPLE = 8
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range((K + KSAMPLE - 1) // KSAMPLE)]
     for pair in kev:          # torch creates the CUDA event on first record; the library records it later
         pair[0].record(stream)
         pair[1].record(stream)
@@ -316,7 +379,7 @@ def main():
         for i in range(K):
             flush.zero_()
             ev[i][0].record(stream)
-            step(kev[i])
+            step(kev[i // KSAMPLE] if i % KSAMPLE == 0 else None)
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
@@ -339,7 +402,8 @@ def main():
     def e2e_step():
         q.copy_(hq, non_blocking=True); w.copy_(hw, non_blocking=True)
         bt.copy_(hbt, non_blocking=True); vl.copy_(hvl, non_blocking=True)
-        idx.score_topk(q, w, bt, vl, k, entries_per_block=W.epb, keys_fp4=fp4, key_scale=sc, key_gscale=gs,
+        idx.score_topk(q, w, bt, vl, k, entries_per_block=W.epb, bt_stride=W.bt_stride, keys_fp4=fp4,
+                       key_scale=sc, key_gscale=gs,
                        out=(out_i, out_s), workspace=ws)
         ho_i.copy_(out_i, non_blocking=True); ho_s.copy_(out_s, non_blocking=True)
 
@@ -357,12 +421,8 @@ def main():
     torch.cuda.synchronize()
     e2e_value, _ = whole_job(pairs_step, E, sum(s.elapsed_time(e) for s, e in e2e_ms) / 1e3, dist, dev)
 
-    # ---- roofline of the scoring kernel (HBM bound) ----
-    peak, peak_kind = peaks()
     kern_s = statistics.mean(kern_ms) / 1e3
-    algo_bytes = pairs_step * BYTES_PER_PAIR + W.T * (4 * W.H * W.D + 4 * W.H + 4)
-    achieved = algo_bytes / kern_s / 1e9
-    traffic = recorded_traffic()
+    roof = roofline(W, kern_s)
 
     if rank == 0:
         clocks = clk.summary()
@@ -374,11 +434,7 @@ def main():
                            mma="tcgen05 kind::f16, f16 x f16 -> f32 (exact for NVFP4 x bf16-valued q)"),
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step(W) * K,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "score_tc_kernel", "peak_kind": peak_kind,
-                         "algorithmic_bytes_per_launch": algo_bytes,
-                         "kernel_ms": 1e3 * kern_s},
+            "roofline": dict(roof, kernel_ms=1e3 * kern_s, kernel_timed_steps=len(kern_ms)),
             "cpu_baseline": cpu,
             "clocks": clocks,
             "wall_s": wall,

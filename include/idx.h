@@ -100,9 +100,12 @@ typedef enum { IDX_PATH_AUTO = 0, IDX_PATH_TENSOR = 1, IDX_PATH_SIMT = 2 } idx_p
  *   path       idx_path_t
  *   num_ctas   CTAs of the persistent score kernel; 0 = one per SM
  *   timing_events optional pair of cudaEvent_t (as void*): when both are
- *              non-NULL, [0] is recorded on `stream` just before the scoring
- *              kernel and [1] just after it (the top-k kernel follows), so a
- *              caller can time the scoring kernel alone.
+ *              non-NULL, [0] is recorded on `stream` just before the q
+ *              preparation and scoring kernels and [1] just after them (the
+ *              selection kernel follows), so a caller can time the scoring
+ *              alone. The second record keeps the selection kernel from
+ *              launching early under the scorer's tail, which lengthens
+ *              that call by a few microseconds.
  * Device-side errors: a table entry outside [0,P) drops that block's keys
  * (IDX_STATUS_BAD_BLOCK); a valid length outside [0, max_logical_blocks*epb]
  * pads that query's whole output (IDX_STATUS_BAD_LEN).

@@ -1,7 +1,8 @@
 """GPU parity of idx_score_topk against the float64 oracle (through the C ABI).
 
-Both score paths run: "simt" (CUDA cores, full score rows + row top-k) and
-"tensor" (tcgen05 tensor cores, fused segment top-k + merge). Small cases
+Both score paths run: "simt" (CUDA cores, full score rows + row selection) and
+"tensor" (tcgen05 tensor cores writing score rows and a per-row score
+histogram, then the histogram-guided row selection). Small cases
 compare every output with the oracle; the full-size workloads compare every
 returned entry of sampled queries, in the launch configuration the benchmark
 times.

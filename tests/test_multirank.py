@@ -25,7 +25,7 @@ def _worker(rank, world, port, out):
     seconds = 1.0 + rank            # rank 1 is the slower one
     pairs = 1000 * (rank + 1)
     value, tmax = bench.whole_job(pairs, 10, seconds, dist, "cpu")
-    out[rank] = (value, tmax, bench.rank_seed(rank))
+    out[rank] = (value, tmax, bench.rank_seed("batched_decode", rank))
     dist.barrier()
     dist.destroy_process_group()
 
