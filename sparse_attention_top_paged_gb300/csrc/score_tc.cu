@@ -17,7 +17,7 @@
 //   work     The tiles of 128 consecutive keys of every query, laid end to end,
 //            are split evenly over the CTAs (one per SM). A "segment" is a
 //            CTA's run of tiles of one query (it shares one B operand).
-//   warp 14  resolver: looks up block-table entries and per-block global
+//   warp 18  resolver: looks up block-table entries and per-block global
 //            scales 32 blocks at a time (one per lane) into a ring of per-tile
 //            records, so no dependent global load sits on the copy path.
 //   warp 0   producer: streams each tile's packed E2M1 nibbles (2-D TMA,
@@ -30,9 +30,9 @@
 //            to tensor memory as the MMA's A operand.
 //   warp 1   MMA issuer: D[128 keys x Npad heads] = A * B^T in f32, K = 128, as
 //            8 (or 16 with the lo part) tcgen05.mma kind::f16 steps.
-//   warps 6-13 epilogue, two groups of four taking alternate tiles: one
-//            thread per key reads its accumulator row from
-//            tensor memory and forms I = g * sum_h (w_h 2^-sigma_h) relu(acc_h)
+//   warps 6-17 epilogue, three groups of four taking tiles in turn: one
+//            thread per key reads its accumulator row (32 columns at a
+//            time) from tensor memory and forms I = g * sum_h (w_h 2^-sigma_h) relu(acc_h)
 //            (the per-block global scale g is factored out, so relu(g a) = g
 //            relu(a) for g > 0 and g min(a,0) for g < 0), then stores I to the
 //            score matrix (coalesced: a warp writes 32 consecutive keys). The
@@ -54,7 +54,9 @@
 namespace idx {
 namespace {
 
-constexpr int kThreads = 480;
+constexpr int kEpiGroups = 3;                      // epilogue groups of four warps
+constexpr int kResolverWarp = 6 + 4 * kEpiGroups;   // after the epilogue warps
+constexpr int kThreads = 32 * (kResolverWarp + 1);
 constexpr int kTileKeys = 128;
 constexpr int kMaxNS = 16;               // raw stages (as many as shared memory holds)
 constexpr int kR = 64;                   // metadata ring (tiles)
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar(B_SEG_FULL + a), 1);   // producer (record copy)
       ptx::mbar_init(bar(B_SEG_BFREE + a), 1);
-      ptx::mbar_init(bar(B_SEG_WFREE + a), 8);  // one arrive per epilogue warp
+      ptx::mbar_init(bar(B_SEG_WFREE + a), 4 * kEpiGroups);  // one arrive per epilogue warp
     }
     for (int r = 0; r < kR; ++r) {
       ptx::mbar_init(bar(B_META_FULL + r), 1);   // resolver
@@ -510,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar(B_EMPTY_RAW + s));
       }
     }
-  } else if (warp == 14) {
+  } else if (warp == kResolverWarp) {
     // ============================================================== resolver
     // Resolves block-table entries and global scales for batches of 32 blocks
     // at once (one per lane), so the two dependent global loads per block
@@ -573,17 +575,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ============================================================== epilogue
-    // Two groups of four warps take alternate tiles. Every warp still walks
-    // every tile: it waits for each segment's q record and signals when it
-    // is done with each segment's w', so a slot is reused only after both
-    // groups are done with it.
+    // kEpiGroups groups of four warps take tiles in turn (one group's tile
+    // takes longer than the MMA of one tile). Every warp still walks every
+    // tile: it waits for each segment's q record and signals when it is done
+    // with each segment's w', so a slot is reused only after every group is
+    // done with it.
     const int row = 32 * (warp & 3) + lane;    // the TMEM lane (key row) this thread reads
     const int grp = (warp - 6) >> 2;
     Walker w;
     w.init(p, t0, j0);
     int ss = 0, L = 0;
-    Ring rd, rm, rs;
-    for (int i = 0; i < n_tiles; ++i, w.next(p), rd.next(nd), rm.next(kR)) {
+    Ring rd, rm, rs, rg;   // rg.idx: the group whose tile this is
+    for (int i = 0; i < n_tiles; ++i, w.next(p), rd.next(nd), rm.next(kR), rg.next(kEpiGroups)) {
       const bool seg_start = (i == 0) || (w.j == 0);
       const bool seg_end = (i == n_tiles - 1) || (w.j == w.nt - 1);
       bool ok = true;
@@ -594,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = ptx::mbar_wait(bar(B_SEG_FULL + ss), rs.phase, abort_flag, kTimeoutNs);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
       }
-      if ((i & 1) != grp) {       // the other group's tile
+      if (rg.idx != grp) {       // another group's tile
         if (seg_end) {
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(bar(B_SEG_WFREE + ss));
@@ -614,13 +617,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *wq = reinterpret_cast<const float *>(sB + ss * lay.rec_smem + lay.rec_w);  // w'_h
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // eight independent chains
       const uint32_t taddr = tmem_d + d * Npad + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-      for (int c0 = 0; c0 < Npad; c0 += 64) {
-        uint32_t v[64];
+      for (int c0 = 0; c0 < Npad; c0 += 32) {   // Npad is a multiple of 32
+        uint32_t v[32];
         __syncwarp();  // the per-row sign branch below must not leave the warp split at these loads
-        ptx::tmem_ld32(taddr + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        if (c0 + 32 < Npad) ptx::tmem_ld32(taddr + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        ptx::tmem_ld32(taddr + c0, v);
         ptx::tmem_wait_ld();
-        if (c0 + 64 >= Npad) {   // every accumulator column is in registers: hand back the slots
+        if (c0 + 32 >= Npad) {   // every accumulator column is in registers: hand back the slots
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) {
@@ -628,31 +630,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive(bar(B_META_EMPTY + r));
           }
         }
-        const int ncol = (Npad - c0 < 64) ? (Npad - c0) : 64;
         const float4 *w4 = reinterpret_cast<const float4 *>(wq + c0);
         if (g >= 0.0f) {          // relu(g a) = g max(a, 0)
 #pragma unroll
-          for (int e = 0; e < 64; e += 4) {
-            if (e < ncol) {
-              const float4 ww = w4[e >> 2];
-              float *ac = acc + ((e >> 2) & 1) * 4;
-              ac[0] = fmaf(ww.x, fmaxf(__uint_as_float(v[e + 0]), 0.0f), ac[0]);
-              ac[1] = fmaf(ww.y, fmaxf(__uint_as_float(v[e + 1]), 0.0f), ac[1]);
-              ac[2] = fmaf(ww.z, fmaxf(__uint_as_float(v[e + 2]), 0.0f), ac[2]);
-              ac[3] = fmaf(ww.w, fmaxf(__uint_as_float(v[e + 3]), 0.0f), ac[3]);
-            }
+          for (int e = 0; e < 32; e += 4) {
+            const float4 ww = w4[e >> 2];
+            float *ac = acc + ((e >> 2) & 1) * 4;
+            ac[0] = fmaf(ww.x, fmaxf(__uint_as_float(v[e + 0]), 0.0f), ac[0]);
+            ac[1] = fmaf(ww.y, fmaxf(__uint_as_float(v[e + 1]), 0.0f), ac[1]);
+            ac[2] = fmaf(ww.z, fmaxf(__uint_as_float(v[e + 2]), 0.0f), ac[2]);
+            ac[3] = fmaf(ww.w, fmaxf(__uint_as_float(v[e + 3]), 0.0f), ac[3]);
           }
         } else {                  // relu(g a) = g min(a, 0)
 #pragma unroll
-          for (int e = 0; e < 64; e += 4) {
-            if (e < ncol) {
-              const float4 ww = w4[e >> 2];
-              float *ac = acc + ((e >> 2) & 1) * 4;
-              ac[0] = fmaf(ww.x, fminf(__uint_as_float(v[e + 0]), 0.0f), ac[0]);
-              ac[1] = fmaf(ww.y, fminf(__uint_as_float(v[e + 1]), 0.0f), ac[1]);
-              ac[2] = fmaf(ww.z, fminf(__uint_as_float(v[e + 2]), 0.0f), ac[2]);
-              ac[3] = fmaf(ww.w, fminf(__uint_as_float(v[e + 3]), 0.0f), ac[3]);
-            }
+          for (int e = 0; e < 32; e += 4) {
+            const float4 ww = w4[e >> 2];
+            float *ac = acc + ((e >> 2) & 1) * 4;
+            ac[0] = fmaf(ww.x, fminf(__uint_as_float(v[e + 0]), 0.0f), ac[0]);
+            ac[1] = fmaf(ww.y, fminf(__uint_as_float(v[e + 1]), 0.0f), ac[1]);
+            ac[2] = fmaf(ww.z, fminf(__uint_as_float(v[e + 2]), 0.0f), ac[2]);
+            ac[3] = fmaf(ww.w, fminf(__uint_as_float(v[e + 3]), 0.0f), ac[3]);
           }
         }
       }

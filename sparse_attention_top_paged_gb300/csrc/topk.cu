@@ -22,8 +22,10 @@
 //      output slot (its bin's start + its rank in the bin).
 //      Otherwise: one pass collects the keys at or above the boundary and a
 //      bitonic sort orders them.
-// The row streams through 16-byte loads, four per thread in flight, and its
-// first block is requested before the first digit is decided.
+// Each pass reads the row from shared memory: one bulk copy stages the whole
+// row when it holds at most kStageMax scores (else the row goes through in
+// chunks of that size, one copy each), and the first copy is issued before
+// the first digit is decided.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
