@@ -54,8 +54,10 @@
 namespace idx {
 namespace {
 
+constexpr int kDecWarps = 4;                       // 4: a warp decodes whole rows; 8: half rows
 constexpr int kEpiGroups = 3;                      // epilogue groups of four warps
-constexpr int kResolverWarp = 6 + 4 * kEpiGroups;   // after the epilogue warps
+constexpr int kEpiWarp0 = 2 + kDecWarps;           // first epilogue warp
+constexpr int kResolverWarp = kEpiWarp0 + 4 * kEpiGroups;   // after the epilogue warps
 constexpr int kThreads = 32 * (kResolverWarp + 1);
 constexpr int kTileKeys = 128;
 constexpr int kMaxNS = 16;               // raw stages (as many as shared memory holds)
@@ -100,7 +102,8 @@ constexpr int B_FULL_RAW = 0, B_EMPTY_RAW = kMaxNS, B_FULL_A = 2 * kMaxNS, B_EMP
               B_SEG_BFREE = B_SEG_FULL + 2, B_SEG_WFREE = B_SEG_FULL + 4, B_COUNT = B_SEG_FULL + 6;
 
 // misc ints
-constexpr int M_TMEM = 0, M_ABORT = 1, M_T0 = 2, M_J0 = 3, M_SCAN = 8;  // scan: 10 longs
+constexpr int M_TMEM = 0, M_ABORT = 1, M_T0 = 2, M_J0 = 3, M_SCAN = 8;  // then one long per warp (scan)
+constexpr uint32_t kMiscBytes = 8 * 4 + (kThreads / 32) * 8;
 
 __host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
@@ -240,10 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::launch_dependents();  // the selection kernel may be scheduled as CTAs of this one finish
     for (int s = 0; s < lay.ns; ++s) {
       ptx::mbar_init(bar(B_FULL_RAW + s), 1);
-      ptx::mbar_init(bar(B_EMPTY_RAW + s), 4);
+      ptx::mbar_init(bar(B_EMPTY_RAW + s), kDecWarps);
     }
     for (int a = 0; a < kMaxSlots; ++a) {
-      ptx::mbar_init(bar(B_FULL_A + a), 4);
+      ptx::mbar_init(bar(B_FULL_A + a), kDecWarps);
       ptx::mbar_init(bar(B_EMPTY_A + a), 1);
       ptx::mbar_init(bar(B_FULL_D + a), 1);
       ptx::mbar_init(bar(B_EMPTY_D + a), 4);
@@ -264,24 +267,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- work partition: tiles [g0, g1) of the concatenated tile list ----
   long long *scan = reinterpret_cast<long long *>(misc + M_SCAN);
-  long long total = 0;
-  {
-    long long local = 0;
-    for (int t = threadIdx.x; t < p.T; t += kThreads) local += ntiles_of(p, t);
-    long long tot;
-    block_incl_scan(local, scan, &tot);
-    total = tot;
-  }
   const long long G = gridDim.x, c = blockIdx.x;
-  const long long qg = total / G, rg = total % G;
-  const long long g0 = c * qg + (c * rg) / G;
-  const long long g1 = (c + 1) * qg + ((c + 1) * rg) / G;
-  if (threadIdx.x == 0) {
-    misc[M_T0] = p.T;
-    misc[M_J0] = 0;
-  }
-  __syncthreads();
-  {
+  long long g0 = 0, g1 = 0;
+  if (p.T <= kThreads) {
+    // one query per thread: a single scan gives the total and each query's range
+    const long long v = (static_cast<int>(threadIdx.x) < p.T) ? ntiles_of(p, threadIdx.x) : 0;
+    long long total;
+    const long long incl = block_incl_scan(v, scan, &total);
+    const long long qg = total / G, rg = total % G;
+    g0 = c * qg + (c * rg) / G;
+    g1 = (c + 1) * qg + ((c + 1) * rg) / G;
+    const long long excl = incl - v;
+    if (v > 0 && excl <= g0 && g0 < incl) {   // exactly one thread when g0 < total
+      misc[M_T0] = static_cast<int>(threadIdx.x);
+      misc[M_J0] = static_cast<int>(g0 - excl);
+    }
+    if (threadIdx.x == 0 && g0 >= total) {
+      misc[M_T0] = p.T;
+      misc[M_J0] = 0;
+    }
+  } else {
+    long long total = 0;
+    {
+      long long local = 0;
+      for (int t = threadIdx.x; t < p.T; t += kThreads) local += ntiles_of(p, t);
+      long long tot;
+      block_incl_scan(local, scan, &tot);
+      total = tot;
+    }
+    const long long qg = total / G, rg = total % G;
+    g0 = c * qg + (c * rg) / G;
+    g1 = (c + 1) * qg + ((c + 1) * rg) / G;
+    if (threadIdx.x == 0) {
+      misc[M_T0] = p.T;
+      misc[M_J0] = 0;
+    }
+    __syncthreads();
     long long base = 0;
     for (int chunk = 0; chunk < p.T; chunk += kThreads) {
       const int t = chunk + threadIdx.x;
@@ -470,10 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
-  } else if (warp < 6) {
+  } else if (warp < kEpiWarp0) {
     // ============================================================== decoders
     const int row = 32 * (warp & 3) + lane;    // the TMEM lane this thread writes
     const int rsw = (row >> 1) & 3;            // 64-byte swizzle of this row's chunks
+    constexpr int kHalves = 8 / kDecWarps;     // 64-element halves of the row per warp
+    const int half0 = (kDecWarps == 8) ? ((warp - 2) >> 2) : 0;
     Ring rraw, ra;
     for (int i = 0; i < n_tiles; ++i, rraw.next(lay.ns), ra.next(na)) {
       const int s = rraw.idx, a = ra.idx;
@@ -485,7 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint2 scw = *reinterpret_cast<const uint2 *>(stage + kScaleOff + row * 8);
       const uint32_t taddr = tmem_a + a * 64 + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int hh = 0; hh < kHalves; ++hh) {
+        const int half = half0 + hh;
         uint32_t v[32];
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -581,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // with each segment's w', so a slot is reused only after every group is
     // done with it.
     const int row = 32 * (warp & 3) + lane;    // the TMEM lane (key row) this thread reads
-    const int grp = (warp - 6) >> 2;
+    const int grp = (warp - kEpiWarp0) >> 2;
     Walker w;
     w.init(p, t0, j0);
     int ss = 0, L = 0;
@@ -721,7 +745,7 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   l.rec_smem = (l.rec_bytes + 1023u) & ~1023u;
   l.off_b = 0;
   const uint32_t b_total = static_cast<uint32_t>(l.nseg) * l.rec_smem;
-  const uint32_t tail = kR * sizeof(MetaEntry) + ((B_COUNT * 8 + 15) & ~15u) + ((8 * 4 + 16 * 8 + 15) & ~15u);
+  const uint32_t tail = kR * sizeof(MetaEntry) + ((B_COUNT * 8 + 15) & ~15u) + ((kMiscBytes + 15) & ~15u);
   const long long room = static_cast<long long>(kSmemLimit) - 1024 - b_total - tail;
   long long ns = room / kStageBytes;
   if (ns > kMaxNS) ns = kMaxNS;
@@ -736,7 +760,7 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   off += B_COUNT * 8;
   off = (off + 15) & ~15u;
   l.off_misc = off;
-  off += 8 * 4 + 16 * 8;
+  off += kMiscBytes;
   off = (off + 15) & ~15u;
   l.smem_bytes = off + 1024;
   *out = l;
