@@ -38,7 +38,7 @@ constexpr int kBins = kScoreBins;                 // 12-bit digits
 constexpr int kPer = kBins / kThreads;            // bins each thread owns in a scan
 constexpr int kBndCap = 2048;                     // largest boundary bin collected (else refine)
 constexpr int kRankBinMax = kBndCap;              // largest bin above the boundary ordered in place
-constexpr int kWarpBin = 64;                      // bins up to this size are sorted by one warp
+constexpr int kWarpBin = 128;                     // bins up to this size are sorted by one warp
 constexpr int kMaxLarge = 8;                      // more larger bins than this: sort the whole buffer
 constexpr int kLargeKeys = kBndCap / kThreads;    // a large bin's keys per thread
 constexpr int kUnroll = 4;                        // 16-byte score loads in flight per thread
@@ -544,7 +544,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p,
           const int start = max(0, min(static_cast<int>(e & 0xFFFFu) - n, total));   // the cursor ended at start + n
           const int cnt = min(n, total - start);
           if (cnt <= 32) warp_sort_segment<1>(buf, start, cnt, emit_if);
-          else warp_sort_segment<2>(buf, start, cnt, emit_if);
+          else if (cnt <= 64) warp_sort_segment<2>(buf, start, cnt, emit_if);
+          else warp_sort_segment<4>(buf, start, cnt, emit_if);
         }
       }
     }
