@@ -279,6 +279,127 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+QSA_STEP = "block_pool (8192 raw bf16 keys -> 512 pooled blocks) + score_topk (32 heads, F32 keys, k=64) + expand_blocks + gather_kv (1024 tokens, 4 kv heads x 128, K and V)"
+
+
+def _qsa_oracle(Q):
+    """The float64 oracle over the whole QSA chain; returns seconds."""
+    import numpy as np
+    import oracle
+    t0 = time.perf_counter()
+    keys = oracle.block_pool(Q.raw_keys, Q.k_norm_w, 0, Q.n_blocks, Q.ratio, Q.rot, Q.theta, Q.eps)
+    sc = oracle.qsa_score(Q.q, keys)
+    order = np.lexsort((np.arange(sc.size), -sc))[:Q.top_k]
+    pos = oracle.expand_blocks(order[None].astype(np.int32), Q.ratio)
+    oracle.gather_kv(pos, Q.page_table, Q.page_table.shape[1], Q.page_table.shape[1], Q.block_size,
+                     Q.k_cache_bits, Q.v_cache_bits)
+    return time.perf_counter() - t0
+
+
+def run_qsa(args, rank, world):
+    """The QSA chain (pooling, block scoring, top-k, expansion, K/V gather) as
+    one step, replayed from a CUDA graph of the public API calls:
+    latency-bound, reported in pairs/s (512 scored blocks per step) and
+    microseconds."""
+    import math
+    import numpy as np
+    import torch
+    import sparse_attention_top_paged_gb300 as idx
+    from sparse_attention_top_paged_gb300 import workloads
+    Q = workloads.qsa(1004 + rank)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt = _qsa_oracle(Q)
+        cpu = {"value": Q.n_blocks / dt, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"the whole QSA chain once, numpy float64, {dt:.3f} s", "seconds": dt}
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = torch.device("cuda")
+    hd, nb = Q.raw_keys.shape[1], Q.n_blocks
+    raw = torch.from_numpy(Q.raw_keys_bits.view(np.int16)).to(dev)
+    nw = torch.from_numpy(Q.k_norm_w).to(dev)
+    q = torch.from_numpy(Q.q[None]).to(dev)
+    w = torch.full((1, Q.q.shape[0]), 1.0 / math.sqrt(hd), device=dev)
+    table = torch.arange(nb // 64, dtype=torch.int32, device=dev).reshape(1, -1)
+    lens = torch.tensor([nb], dtype=torch.int32, device=dev)
+    kc = torch.from_numpy(Q.k_cache_bits.view(np.int16)).to(dev)
+    vc = torch.from_numpy(Q.v_cache_bits.view(np.int16)).to(dev)
+    ptab = torch.from_numpy(Q.page_table).to(dev)
+    bk = torch.empty((nb, hd), device=dev)
+    gi = torch.empty((1, Q.top_k), dtype=torch.int32, device=dev)
+    gs = torch.empty((1, Q.top_k), device=dev)
+    n_tok = Q.top_k * Q.ratio
+    k_out = torch.empty((1, n_tok) + tuple(kc.shape[2:]), dtype=kc.dtype, device=dev)
+    v_out = torch.empty_like(k_out)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        idx.block_pool(raw, nw, bk, 0, nb, Q.ratio, Q.rot, Q.theta, Q.eps)
+        idx.score_topk(q, w, table, lens, Q.top_k, entries_per_block=64, keys_f32=bk.reshape(nb // 64, 64, hd),
+                       out=(gi, gs))
+        pos = idx.expand_blocks(gi, Q.ratio)
+        idx.gather_kv(pos, ptab, Q.block_size, kc, vc, out=(k_out, v_out))
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    # The five launches of a step are captured once in a CUDA graph: issued
+    # from Python one by one they take longer on the host than on the device.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    value, t_total = whole_job(nb, K, sum(ms) / 1e3)
+    # end to end: q in from pinned host memory, the selected blocks and their scores out
+    hq = torch.from_numpy(Q.q[None].copy()).pin_memory()
+    ho_i = torch.empty((1, Q.top_k), dtype=torch.int32).pin_memory()
+    ho_s = torch.empty((1, Q.top_k), dtype=torch.float32).pin_memory()
+    E = max(10, K // 10)
+    e2e = []
+    for _ in range(E):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        q.copy_(hq, non_blocking=True)
+        graph.replay()
+        ho_i.copy_(gi, non_blocking=True)
+        ho_s.copy_(gs, non_blocking=True)
+        b.record(stream)
+        e2e.append((a, b))
+    torch.cuda.synchronize()
+    e2e_value, _ = whole_job(nb, E, sum(a.elapsed_time(b) for a, b in e2e) / 1e3)
+    # algorithmic bytes: raw keys in, pooled keys out and back in, the gathered rows in and out
+    row = int(np.prod(kc.shape[2:])) * kc.element_size()
+    algo = raw.numel() * 2 + 2 * bk.numel() * 4 + 2 * 2 * n_tok * row
+    hbm, _, kind = peaks()
+    achieved = algo / (t_total / K) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t_total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "qsa: " + QSA_STEP, "pairs_per_step": nb, "seed": 1004, "cuda_graph": True,
+                       "l2": "flushed before every timed step (256 MB write, outside the timed events)"},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": hq.numel() * 4,
+                    "d2h_bytes_per_step": ho_i.numel() * 4 + ho_s.numel() * 4},
+            "gpu_launches": 5 * K,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": None, "kernel": "whole QSA chain (latency-bound)", "peak_kind": kind,
+                         "algorithmic_bytes_per_launch": algo},
+            "cpu_baseline": cpu, "clocks": clk.summary()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -286,7 +407,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "tensor", "simt"])
-    ap.add_argument("--workload", default="batched_decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="batched_decode", choices=sorted(WORKLOADS) + ["qsa"])
     ap.add_argument("--cpu-queries", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -298,6 +419,8 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.workload == "qsa":
+        return run_qsa(args, rank, world)
 
     import torch
     import sparse_attention_top_paged_gb300 as idx

@@ -209,7 +209,9 @@ idx_status_t idx_gather_kv(const idx_gather_kv_args *args, idx_stream_t stream);
  * b = first_block + i, i < n_new: the mean m of raw rows
  * [b*ratio, (b+1)*ratio), then y = m / sqrt(mean(m^2) + eps) * (1 + w), then
  * rope on the first `rot` dimensions at position b*ratio, pairing d with
- * d + rot/2 at angle pos * theta^(-2d/rot) (d < rot/2).
+ * d + rot/2 at angle pos * theta^(-2d/rot) (d < rot/2). The angle is formed
+ * and reduced to [-pi, pi] in double precision; its sine and cosine are
+ * taken in single precision.
  *   raw_keys    device [(first_block+n_new)*ratio, hd] bf16 (raw bit patterns)
  *   k_norm_w    device [hd] float32
  *   block_keys  device [first_block + n_new, hd] float32; rows

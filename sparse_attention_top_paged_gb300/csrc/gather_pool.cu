@@ -3,6 +3,8 @@
 // counts.
 #include <climits>
 
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -54,11 +56,20 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_kv_kernel(idx_gather
 // qsa.rs, qsa_block_pool: per block, the mean of `ratio` raw keys, RMSNorm
 // scaled by (1 + w), then rope on the first `rot` dimensions at the block's
 // first token position. One CTA per block, one thread per dimension (the
-// page's launch shape: grid n_new, block hd). Rope pairs d with d + rot/2;
-// the angle is formed in double precision.
+// page's launch shape: grid n_new, block hd). Rope pairs d with d + rot/2.
+// The frequencies theta^(-2i/rot) come from the host in double precision, the
+// angle pos * freq is formed in double and reduced to [-pi, pi] in double,
+// and only the sine and cosine of the reduced angle are taken in single
+// precision (double-precision trigonometry per thread cost more than the rest
+// of the kernel).
+constexpr int kMaxRopeFreqs = 512;  // rot <= hd <= 1024
+struct RopeFreqs {
+  double f[kMaxRopeFreqs];
+};
+
 __global__ void block_pool_kernel(const uint16_t *__restrict__ raw, const float *__restrict__ w,
                                   float *__restrict__ out, uint32_t first_block, uint32_t ratio,
-                                  uint32_t hd, uint32_t rot, float theta, float eps) {
+                                  uint32_t hd, uint32_t rot, float eps, const __grid_constant__ RopeFreqs rf) {
   extern __shared__ float sm[];  // [hd] pooled-normalised values, then [32] partial sums
   float *y_s = sm;
   float *red = sm + hd;
@@ -89,10 +100,12 @@ __global__ void block_pool_kernel(const uint16_t *__restrict__ raw, const float 
   if (d < rot) {
     const uint32_t i = d < half ? d : d - half;
     const double pos = static_cast<double>(b) * ratio;
-    const double ang = pos * pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(rot));
-    double sn, cs;
-    sincos(ang, &sn, &cs);
-    const float c = static_cast<float>(cs), s = static_cast<float>(sn);
+    const double ang = pos * rf.f[i];
+    constexpr double kTwoPi = 6.283185307179586476925286766559;
+    const double turns = rint(ang * (1.0 / kTwoPi));
+    const float red = static_cast<float>(fma(-turns, kTwoPi, ang));
+    float s, c;
+    sincosf(red, &s, &c);
     if (d < half)
       o = y * c - y_s[d + half] * s;
     else
@@ -161,7 +174,11 @@ cudaError_t launch_block_pool(const uint16_t *raw, const float *w, float *out, u
                               uint32_t n_new, uint32_t ratio, uint32_t hd, uint32_t rot, float theta,
                               float eps, cudaStream_t stream) {
   const size_t smem = (static_cast<size_t>(hd) + 32) * sizeof(float);
-  block_pool_kernel<<<n_new, hd, smem, stream>>>(raw, w, out, first_block, ratio, hd, rot, theta, eps);
+  if (rot / 2 > static_cast<uint32_t>(kMaxRopeFreqs)) return cudaErrorInvalidValue;
+  RopeFreqs rf;
+  for (uint32_t i = 0; i < rot / 2; ++i)
+    rf.f[i] = std::pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(rot));
+  block_pool_kernel<<<n_new, hd, smem, stream>>>(raw, w, out, first_block, ratio, hd, rot, eps, rf);
   return cudaGetLastError();
 }
 

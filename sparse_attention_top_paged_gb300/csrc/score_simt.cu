@@ -15,7 +15,7 @@
 namespace idx {
 namespace {
 
-constexpr int kSimtThreads = 128;
+constexpr int kSimtThreads = 64;
 
 __constant__ float kE2m1Lut[16] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f,
                                    -0.0f, -0.5f, -1.0f, -1.5f, -2.0f, -3.0f, -4.0f, -6.0f};
@@ -82,9 +82,15 @@ __global__ void __launch_bounds__(kSimtThreads) score_simt_kernel(ScoreParams p,
       I = 0.0f;
       for (int h = 0; h < p.H; ++h) {
         const float *qh = q_s + h * D;
-        float dot = 0.0f;
+        float dot0 = 0.0f, dot1 = 0.0f, dot2 = 0.0f, dot3 = 0.0f;   // four independent chains
 #pragma unroll
-        for (int d = 0; d < D; ++d) dot = fmaf(qh[d], k[d], dot);
+        for (int d = 0; d < D; d += 4) {
+          dot0 = fmaf(qh[d], k[d], dot0);
+          dot1 = fmaf(qh[d + 1], k[d + 1], dot1);
+          dot2 = fmaf(qh[d + 2], k[d + 2], dot2);
+          dot3 = fmaf(qh[d + 3], k[d + 3], dot3);
+        }
+        const float dot = (dot0 + dot1) + (dot2 + dot3);
         I = fmaf(w_s[h], fmaxf(dot, 0.0f), I);
       }
     }

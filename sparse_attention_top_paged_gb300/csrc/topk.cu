@@ -22,6 +22,8 @@
 //      output slot (its bin's start + its rank in the bin).
 //      Otherwise: one pass collects the keys at or above the boundary and a
 //      bitonic sort orders them.
+// Rows of at most kSmallRow keys skip the digits: every candidate key goes
+// into the buffer and one bitonic sort orders them.
 // Each pass reads the row from shared memory: one bulk copy stages the whole
 // row when it holds at most kStageMax scores (else the row goes through in
 // chunks of that size, one copy each), and the first copy is issued before
@@ -42,6 +44,7 @@ constexpr int kWarpBin = 128;                     // bins up to this size are so
 constexpr int kMaxLarge = 8;                      // more larger bins than this: sort the whole buffer
 constexpr int kLargeKeys = kBndCap / kThreads;    // a large bin's keys per thread
 constexpr int kUnroll = 4;                        // 16-byte score loads in flight per thread
+constexpr int kSmallRow = 2048;                   // rows up to this long are sorted whole
 static_assert(kBndCap % kThreads == 0, "a large bin's keys spread evenly over the threads");
 
 __host__ __device__ inline int pow2_at_least(int k) {
@@ -315,6 +318,29 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p,
     return;
   }
   const float *row = scores + static_cast<long long>(t) * ld;
+
+  // ---- a short row: every candidate key into the buffer, one sort ----
+  if (L <= kSmallRow && pow2_at_least(max(L, 64)) <= cap) {
+    if (tid == 0) sh->n_buf = 0;
+    __syncthreads();
+    for (int i = tid; i < L; i += kThreads) {
+      const float v = row[i];
+      if (v != -INFINITY) buf[atomicAdd(&sh->n_buf, 1)] = pack_key(v, i);   // at most L <= cap keys
+    }
+    __syncthreads();
+    const int count = sh->n_buf;
+    const int m = max(64, pow2_at_least(count));
+    for (int i = count + tid; i < m; i += kThreads) buf[i] = 0ull;
+    __syncthreads();
+    sort_desc(buf, m);
+    const int got = min(count, k);
+    for (int i = tid; i < k; i += kThreads) {
+      oi[i] = i < got ? key_index(buf[i]) : -1;
+      os[i] = i < got ? key_score(buf[i]) : -INFINITY;
+    }
+    return;
+  }
+
   const uint32_t sbar = ptx::smem_addr(smem_raw + lay.bar);
   RowSource rs{row, L, lay.stage_floats > 0 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0,
                reinterpret_cast<float *>(smem_raw + lay.stage), static_cast<int>(lay.stage_floats), sbar, 0u, -1, -1,
