@@ -120,7 +120,8 @@ idx_status_t resolve(const idx_score_topk_args *a, Resolved *r) {
   // Both paths write I[t, s] to a [T, ld] matrix (the caller's scores_out, or
   // the workspace), then select from it.
   if (!select_supported(a->top_k, max_len)) return IDX_ERR_UNSUPPORTED;
-  r->sel = select_plan(a->T, a->top_k, max_len, a->scores_out != nullptr, a->ld_scores);
+  r->sel = select_plan(a->T, a->top_k, max_len, a->scores_out != nullptr, a->ld_scores,
+                       plan == Plan::kTensor ? device_sm_count() : 0);
   r->ws_bytes = r->sel.total;
   if (plan == Plan::kTensor) {  // then the scorer's per-query q records and key histograms
     r->qrec_off = r->ws_bytes;

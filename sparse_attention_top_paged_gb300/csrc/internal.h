@@ -37,9 +37,18 @@ struct SelectPlan {
   bool own_scores;   // the score matrix lives in the workspace (no caller scores_out)
   long long ld;      // row stride of the score matrix
   size_t scores_off, total;
+  // Split collection (few long rows next to a scorer histogram): `chunks` CTAs
+  // per row gather the row's candidate keys into the workspace before the
+  // one-CTA-per-row selection orders them. chunks == 0: no split.
+  int chunks;
+  int cand_cap;             // candidate keys per row
+  size_t cand_off, cnt_off; // [T][cand_cap] composite keys, [T] counters (left zero)
 };
 
-SelectPlan select_plan(int T, int top_k, long long max_len, bool have_scores_out, long long ld_out);
+// split_sms: SM count when the rows come with a scorer histogram (tensor
+// path), 0 otherwise.
+SelectPlan select_plan(int T, int top_k, long long max_len, bool have_scores_out, long long ld_out,
+                       int split_sms);
 bool select_supported(int top_k, long long max_len);  // the selection's buffers fit shared memory
 
 // score_simt.cu

@@ -28,6 +28,8 @@
 // row when it holds at most kStageMax scores (else the row goes through in
 // chunks of that size, one copy each), and the first copy is issued before
 // the first digit is decided.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -45,6 +47,11 @@ constexpr int kMaxLarge = 8;                      // more larger bins than this:
 constexpr int kLargeKeys = kBndCap / kThreads;    // a large bin's keys per thread
 constexpr int kUnroll = 4;                        // 16-byte score loads in flight per thread
 constexpr int kSmallRow = 2048;                   // rows up to this long are sorted whole
+constexpr int kCollectThreads = 256;              // split collection: threads per CTA,
+constexpr int kCollectMin = 2048;                 // at least this many keys per CTA,
+constexpr int kMaxChunks = 32;                    // at most this many CTAs per row
+constexpr int kCollectBuf = 2048;                 // keys a collecting CTA holds before flushing
+constexpr long long kSplitMinLen = 65536;         // split only rows at least this long
 static_assert(kBndCap % kThreads == 0, "a large bin's keys spread evenly over the threads");
 
 __host__ __device__ inline int pow2_at_least(int k) {
@@ -292,8 +299,133 @@ __device__ __forceinline__ void warp_sort_segment(const uint64_t *buf, int start
     if (lane * E + e < n) emit(v[e], start + lane * E + e);
 }
 
+// Split collection, ahead of topk_stream_kernel on rows that come with the
+// scorer's first-digit histogram: CTA c of row t takes the c-th slice of the
+// row and appends every key the selection would place (at or above the
+// boundary bin, or every key when the row holds at most k) to the row's
+// candidate list. It decides from the histogram exactly as the selection
+// does; rows the selection will refine are left alone. The selection checks
+// the list's length against the histogram before it uses the list, and
+// otherwise reads the row itself.
+__global__ void __launch_bounds__(kCollectThreads) select_collect_kernel(ScoreParams p,
+                                                                        const float *__restrict__ scores,
+                                                                        long long ld,
+                                                                        const uint32_t *__restrict__ hist,
+                                                                        uint64_t *__restrict__ cand,
+                                                                        uint32_t *__restrict__ cand_cnt, int cap) {
+  constexpr int kW = kCollectThreads / 32, kPerC = kBins / kCollectThreads;
+  constexpr int kRound = 4 * kCollectThreads;   // keys per round (one 16-byte load per thread)
+  static_assert(kCollectBuf >= 2 * kRound, "a round never overfills the buffer");
+  __shared__ uint32_t warp_sum[kW], warp_max[kW];
+  __shared__ int s_bin, s_cnt;
+  __shared__ uint32_t s_n, s_base;
+  __shared__ uint64_t s_buf[kCollectBuf];
+  const int t = blockIdx.y, c = blockIdx.x, C = gridDim.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int L = p.valid_lens[t];
+  if (bad_len(p, L) || L <= kSmallRow) return;
+  const uint32_t k = static_cast<uint32_t>(p.top_k);
+  // descending scan of the first-digit histogram (thread tid: bins kBins-1-kPerC*tid-j)
+  const uint32_t *h = hist + static_cast<size_t>(t) * kBins;
+  uint32_t cnt[kPerC], tot = 0;
+#pragma unroll
+  for (int j = 0; j < kPerC; ++j) {
+    cnt[j] = h[kBins - 1 - kPerC * tid - j];
+    tot += cnt[j];
+  }
+  uint32_t incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  if (tid == 0) {
+    s_bin = 0;
+    s_cnt = 0;
+  }
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) {
+    if (w < warp) before += warp_sum[w];
+    all += warp_sum[w];
+  }
+  const bool take_all = all <= k;
+  uint32_t run = before + incl - tot, mx = 0;
+#pragma unroll
+  for (int j = 0; j < kPerC; ++j) {
+    if (!take_all && run < k && run + cnt[j] >= k) {
+      s_bin = kBins - 1 - kPerC * tid - j;
+      s_cnt = static_cast<int>(cnt[j]);
+    }
+    if (cnt[j] != 0u && (take_all || run + cnt[j] < k)) mx = max(mx, cnt[j]);   // bins above the boundary
+    run += cnt[j];
+  }
+  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+  if (lane == 0) warp_max[warp] = mx;
+  __syncthreads();
+  uint32_t max_above = 0;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) max_above = max(max_above, warp_max[w]);
+  if (max_above > static_cast<uint32_t>(kRankBinMax) || (!take_all && s_cnt > kBndCap)) return;
+  const uint32_t thr = take_all ? 0u : static_cast<uint32_t>(s_bin);   // first digit of the weakest key taken
+
+  const long long per = ((static_cast<long long>(L) + C - 1) / C + 3) & ~3LL;
+  const long long s0 = static_cast<long long>(c) * per, s1 = min(static_cast<long long>(L), s0 + per);
+  const float *row = scores + static_cast<long long>(t) * ld;
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  uint64_t *out = cand + static_cast<size_t>(t) * cap;
+  // Keys go to a shared-memory buffer first (one shared atomic per warp and
+  // element position); the buffer goes out with one global reservation when
+  // it holds a round's worth, and at the end.
+  if (tid == 0) s_n = 0u;
+  __syncthreads();
+  auto flush = [&]() {   // all threads, after a barrier
+    const uint32_t n = s_n;
+    if (tid == 0) s_base = atomicAdd(cand_cnt + t, n);
+    __syncthreads();
+    const uint32_t b0 = s_base;
+    for (uint32_t i = tid; i < n; i += kCollectThreads)
+      if (b0 + i < static_cast<uint32_t>(cap)) out[b0 + i] = s_buf[i];
+    __syncthreads();
+    if (tid == 0) s_n = 0u;
+    __syncthreads();
+  };
+  for (long long base = s0; base < s1; base += kRound) {
+    const long long i0 = base + 4LL * tid;
+    float e[4];
+    if (vec && i0 + 3 < s1) {
+      const float4 v = __ldcs(reinterpret_cast<const float4 *>(row + i0));
+      e[0] = v.x; e[1] = v.y; e[2] = v.z; e[3] = v.w;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) e[q] = (i0 + q < s1) ? row[i0 + q] : -INFINITY;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const bool ok = e[q] != -INFINITY && (float_order(e[q]) >> 20) >= thr;
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, ok);
+      if (m == 0u) continue;
+      uint32_t slot0 = 0;
+      if (lane == 0) slot0 = atomicAdd(&s_n, static_cast<uint32_t>(__popc(m)));
+      slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
+      const uint32_t slot = slot0 + __popc(m & lanemask_lt());
+      if (ok && slot < static_cast<uint32_t>(kCollectBuf)) s_buf[slot] = pack_key(e[q], static_cast<int32_t>(i0 + q));
+    }
+    __syncthreads();
+    if (s_n > static_cast<uint32_t>(kCollectBuf - kRound)) flush();   // room for one more round
+  }
+  __syncthreads();
+  if (s_n > 0u) flush();
+}
+
 __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p, const float *__restrict__ scores,
-                                                              long long ld, const uint32_t *__restrict__ hist) {
+                                                              long long ld, const uint32_t *__restrict__ hist,
+                                                              const uint64_t *__restrict__ cand,
+                                                              uint32_t *__restrict__ cand_cnt, int cand_cap) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SelShared *sh = reinterpret_cast<SelShared *>(smem_raw);
   const SelSmem lay = sel_smem(p.top_k, static_cast<long long>(p.max_lb) * p.epb);
@@ -350,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p,
     ptx::mbar_init(sbar, 1);
     ptx::fence_mbar_init();
   }
-  rs.prefetch();   // the row is on its way while the first digit is decided
+  if (cand == nullptr) rs.prefetch();   // the row is on its way while the first digit is decided
   if (tid == 0) {
     sh->b_bin = 0;
     sh->b_above = 0;
@@ -464,12 +596,21 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p,
   if (((take_all && rounds == 0) || (!take_all && rounds == 1)) && max_above <= kRankBinMax) {
     // ---- decided on the first digit: place, rank, write ----
     // (keys below the boundary bin are dropped on their top 32 bits alone)
-    rs.pass(static_cast<uint32_t>(prefix >> 32), [&](uint64_t key) {
+    auto place = [&](uint64_t key) {
       if ((key & mask) >= prefix) {
         const uint32_t old = atomicAdd(&sh->table[key >> 52], 1u);
         if (static_cast<int>(old & 0xFFFFu) < cap) buf[old & 0xFFFFu] = key;
       }
-    });
+    };
+    // the split collection's list, when it holds exactly the keys to place
+    const uint32_t want = take_all ? all_keys : static_cast<uint32_t>(sh->b_above + sh->b_cnt);
+    const uint32_t n_cand = (cand != nullptr) ? cand_cnt[t] : 0u;
+    if (cand != nullptr && n_cand == want && n_cand <= static_cast<uint32_t>(cand_cap)) {
+      const uint64_t *cl = cand + static_cast<size_t>(t) * cand_cap;
+      for (int i = tid; i < static_cast<int>(n_cand); i += kThreads) place(cl[i]);
+    } else {
+      rs.pass(static_cast<uint32_t>(prefix >> 32), place);
+    }
     __syncthreads();
     const int total = min(take_all ? static_cast<int>(all_keys) : sh->b_above + sh->b_cnt, cap);
     // Every bin holding some of the k best keys is now a contiguous segment
@@ -599,17 +740,38 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p,
     os[i] = -INFINITY;
   }
   if (tid == 0 && sh->abort_flag && p.dev_status) atomicOr(p.dev_status, IDX_STATUS_TIMEOUT);
+  if (cand_cnt != nullptr) {
+    __syncthreads();   // every thread has read the row's count
+    if (tid == 0) cand_cnt[t] = 0u;   // left zero for the next call
+  }
 }
 
 }  // namespace
 
-SelectPlan select_plan(int T, int top_k, long long max_len, bool have_scores_out, long long ld_out) {
-  (void)top_k;
+SelectPlan select_plan(int T, int top_k, long long max_len, bool have_scores_out, long long ld_out,
+                       int split_sms) {
   SelectPlan pl{};
   pl.own_scores = !have_scores_out;
   pl.ld = have_scores_out ? ld_out : max_len;
   pl.scores_off = 0;
   pl.total = pl.own_scores ? ((static_cast<size_t>(T) * static_cast<size_t>(max_len) * 4 + 255) & ~size_t(255)) : 0;
+  // Fewer rows than SMs, each long: split the collection so about two CTAs
+  // per SM stream the rows, at least kCollectMin keys each. (On rows of up
+  // to 32K keys the extra launch costs more than it saves: +10 us per call
+  // on 64 rows of 8K-32K keys, against -25 us on 16 rows of 256K keys.)
+  if (split_sms > 0 && T > 0 && T < split_sms && max_len >= kSplitMinLen) {
+    const long long by_sms = (2LL * split_sms + T - 1) / T;
+    const long long by_len = (max_len + kCollectMin - 1) / kCollectMin;
+    const int chunks = static_cast<int>(std::min<long long>(std::min(by_sms, by_len), kMaxChunks));
+    if (chunks >= 2) {
+      pl.chunks = chunks;
+      pl.cand_cap = static_cast<int>(sel_smem(top_k, max_len).cap);
+      pl.cand_off = pl.total;
+      pl.total += (static_cast<size_t>(T) * pl.cand_cap * 8 + 255) & ~size_t(255);
+      pl.cnt_off = pl.total;
+      pl.total += (static_cast<size_t>(T) * 4 + 255) & ~size_t(255);
+    }
+  }
   return pl;
 }
 
@@ -619,13 +781,28 @@ bool select_supported(int top_k, long long max_len) {
 
 cudaError_t launch_select(const ScoreParams &p, const float *scores, long long ld, const uint32_t *hist,
                           const SelectPlan &pl, void *workspace, cudaStream_t stream) {
-  (void)pl;
-  (void)workspace;
   if (p.T == 0) return cudaSuccess;
   const size_t smem = sel_smem(p.top_k, static_cast<long long>(p.max_lb) * p.epb).total;
   cudaError_t e =
       cudaFuncSetAttribute(topk_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  uint64_t *cand = nullptr;
+  uint32_t *cand_cnt = nullptr;
+  if (pl.chunks > 0 && hist != nullptr) {
+    cand = reinterpret_cast<uint64_t *>(static_cast<unsigned char *>(workspace) + pl.cand_off);
+    cand_cnt = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(workspace) + pl.cnt_off);
+    cudaLaunchConfig_t ca{};
+    ca.gridDim = dim3(static_cast<unsigned>(pl.chunks), static_cast<unsigned>(p.T), 1);
+    ca.blockDim = dim3(kCollectThreads, 1, 1);
+    ca.stream = stream;
+    cudaLaunchAttribute aa[1];
+    aa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    aa[0].val.programmaticStreamSerializationAllowed = 1;
+    ca.attrs = aa;
+    ca.numAttrs = 1;
+    e = cudaLaunchKernelEx(&ca, select_collect_kernel, p, scores, ld, hist, cand, cand_cnt, pl.cand_cap);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(p.T), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -636,7 +813,8 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, topk_stream_kernel, p, scores, ld, hist);
+  return cudaLaunchKernelEx(&cfg, topk_stream_kernel, p, scores, ld, hist, static_cast<const uint64_t *>(cand),
+                            cand_cnt, pl.cand_cap);
 }
 
 }  // namespace idx

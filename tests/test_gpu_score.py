@@ -102,6 +102,47 @@ def test_all_equal_scores_take_lowest_indices(path):
 
 
 @pytest.mark.parametrize("path", PATHS)
+def test_all_equal_scores_long_rows(path):
+    """Rows past the short-row sort where every score ties: the boundary bin
+    holds every key, so the selection refines digit by digit on the row."""
+    W = _small(17, T=2, lo=5000, hi=6000, k=300, max_lb=100, P=200)
+    W.keys_fp4[:] = 0
+    gi, gs, st, _ = run_gpu(W, path)
+    assert np.array_equal(gi, np.tile(np.arange(300), (2, 1)))
+    assert np.all(gs == 0.0) and not np.any(np.signbit(gs))
+
+
+def _long_rows(seed, T, lo, hi, k, P):
+    return _small(seed, T=T, lo=lo, hi=hi, k=k, max_lb=(hi + 63) // 64, P=P)
+
+
+def test_split_collection_long_rows():
+    """Few rows of 64K+ keys: several CTAs per row collect the candidates
+    before the selection orders them."""
+    W = _long_rows(18, T=3, lo=65536, hi=90000, k=512, P=4400)
+    gi, gs, st, _ = run_gpu(W, "tensor")
+    assert st == 0
+    rows, _ = oracle_rows(W)
+    check_against_oracle(W, gi, gs, rows, None, "split")
+
+
+def test_split_collection_falls_back_and_takes_all():
+    """Row 0: every score ties, so no candidate list is made and the selection
+    refines on the row itself. Row 1: most blocks are bad, fewer valid keys
+    than k remain, all of them taken from the list."""
+    W = _long_rows(19, T=2, lo=70000, hi=70000, k=700, P=2300)
+    nblk = (70000 + 63) // 64
+    W.keys_fp4[W.block_table[0, :nblk]] = 0
+    W.block_table[1, 10:nblk] = -1
+    gi, gs, st, _ = run_gpu(W, "tensor")
+    rows, ost = oracle_rows(W)
+    assert st == ost == oracle.STATUS_BAD_BLOCK
+    assert np.array_equal(gi[0], np.arange(700)) and np.all(gs[0] == 0.0)
+    check_against_oracle(W, gi, gs, {1: rows[1]}, None, "split-take-all")
+    assert np.all(gi[1, 640:] == -1) and np.all(np.isneginf(gs[1, 640:]))
+
+
+@pytest.mark.parametrize("path", PATHS)
 def test_bad_inputs_report_status(path):
     W = _small(8, T=4, lo=2000, hi=3000, k=64, max_lb=50, P=300)
     W.block_table[0, 3] = W.P + 5          # query 0 loses keys 192..255
