@@ -17,9 +17,11 @@
 //   3. decided on the first digit with no bin above the boundary holding more
 //      than kRankBinMax keys (the decode case): one pass drops every key at
 //      or above the boundary bin straight into its bin's segment of a
-//      shared-memory buffer (bins in descending order); then each warp sorts
-//      whole bins in registers, one at a time, and writes every key to its
-//      output slot (its bin's start + its rank in the bin).
+//      shared-memory buffer (bins in descending order); bins of more than
+//      kWarpBin keys are first split on the next 8 key bits by the whole CTA
+//      (more than kMaxLarge such bins: one bitonic sort of the buffer); then
+//      each warp sorts whole bins in registers, one at a time, and writes
+//      every key to its output slot (its bin's start + its rank in the bin).
 //      Otherwise: one pass collects the keys at or above the boundary and a
 //      bitonic sort orders them.
 // Rows of at most kSmallRow keys skip the digits: every candidate key goes
@@ -27,7 +29,9 @@
 // Each pass reads the row from shared memory: one bulk copy stages the whole
 // row when it holds at most kStageMax scores (else the row goes through in
 // chunks of that size, one copy each), and the first copy is issued before
-// the first digit is decided.
+// the first digit is decided. For a few very long rows, select_collect_kernel
+// (below) gathers step 3's keys beforehand over many CTAs, and the pass over
+// the row becomes a pass over that list.
 #include <algorithm>
 
 #include "common.cuh"
