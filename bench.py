@@ -514,21 +514,39 @@ def main():
     value, t_total = whole_job(pairs_step, K, sum(step_ms) / 1e3, dist, dev)
 
     # ---- end to end through the public Python API with host buffers ----
-    pin = lambda x: torch.from_numpy(x).pin_memory()
-    hq, hw, hbt, hvl = pin(W.q), pin(W.w), pin(W.block_table), pin(W.valid_lens)
-    ho_i = torch.empty((W.T, k), dtype=torch.int32).pin_memory()
-    ho_s = torch.empty((W.T, k), dtype=torch.float32).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hw, hbt, hvl))
-    d2h = ho_i.numel() * 4 + ho_s.numel() * 4
+    # The step's inputs travel as one pinned host block into one device block
+    # (q, w, block table, lengths at 256-byte-aligned offsets) and both
+    # outputs come back as one block: one copy each way.
+    import numpy as np
+
+    def packed(parts):
+        offs, total = [], 0
+        for x in parts:
+            offs.append(total)
+            total += (x.nbytes + 255) // 256 * 256
+        return offs, total
+
+    tdt = {np.dtype(np.float32): torch.float32, np.dtype(np.int32): torch.int32}
+    in_parts = [W.q, W.w, W.block_table, W.valid_lens]
+    in_offs, in_bytes = packed(in_parts)
+    h_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
+    for x, o in zip(in_parts, in_offs):
+        h_in[o:o + x.nbytes].copy_(torch.from_numpy(np.ascontiguousarray(x).view(np.uint8).reshape(-1)))
+    d_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+    eq, ew, ebt, evl = (d_in[o:o + x.nbytes].view(tdt[x.dtype]).view(x.shape) for x, o in zip(in_parts, in_offs))
+    out_bytes = (W.T * k * 4 + 255) // 256 * 256
+    d_out = torch.empty(2 * out_bytes, dtype=torch.uint8, device=dev)
+    e_i = d_out[:W.T * k * 4].view(torch.int32).view(W.T, k)
+    e_s = d_out[out_bytes:out_bytes + W.T * k * 4].view(torch.float32).view(W.T, k)
+    h_out = torch.empty(2 * out_bytes, dtype=torch.uint8).pin_memory()
+    h2d, d2h = in_bytes, 2 * out_bytes
     E = max(10, K // 10)
 
     def e2e_step():
-        q.copy_(hq, non_blocking=True); w.copy_(hw, non_blocking=True)
-        bt.copy_(hbt, non_blocking=True); vl.copy_(hvl, non_blocking=True)
-        idx.score_topk(q, w, bt, vl, k, entries_per_block=W.epb, bt_stride=W.bt_stride, keys_fp4=fp4,
-                       key_scale=sc, key_gscale=gs,
-                       out=(out_i, out_s), workspace=ws)
-        ho_i.copy_(out_i, non_blocking=True); ho_s.copy_(out_s, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
+        idx.score_topk(eq, ew, ebt, evl, k, entries_per_block=W.epb, bt_stride=W.bt_stride, keys_fp4=fp4,
+                       key_scale=sc, key_gscale=gs, out=(e_i, e_s), workspace=ws)
+        h_out.copy_(d_out, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -543,6 +561,9 @@ def main():
         e2e_ms.append((s0, s1))
     torch.cuda.synchronize()
     e2e_value, _ = whole_job(pairs_step, E, sum(s.elapsed_time(e) for s, e in e2e_ms) / 1e3, dist, dev)
+    # the host copy holds what the device-timed steps produced
+    if not torch.equal(h_out[:W.T * k * 4].view(torch.int32).view(W.T, k), out_i.cpu()):
+        raise RuntimeError("end-to-end top-k differs from the device-timed steps")
 
     kern_s = statistics.mean(kern_ms) / 1e3
     roof = roofline(W, kern_s)
