@@ -279,16 +279,23 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-QSA_STEP = "block_pool (8192 raw bf16 keys -> 512 pooled blocks) + score_topk (32 heads, F32 keys, k=64) + expand_blocks + gather_kv (1024 tokens, 4 kv heads x 128, K and V)"
+QSA_STEP = ("qsa_qprep (32 heads of one decode query at position 8192) + block_pool (8192 raw bf16 keys -> "
+            "512 pooled blocks) + score_topk (32 heads, F32 keys, k=64) + expand_blocks + gather_kv (1024 tokens, "
+            "4 kv heads x 128, K and V)")
 
 
 def _qsa_oracle(Q):
     """The float64 oracle over the whole QSA chain; returns seconds."""
     import numpy as np
     import oracle
+    hd = Q.raw_keys.shape[1]
+    nh = Q.q_raw_bits.shape[1] // hd
+    q_vals = (Q.q_raw_bits.astype(np.uint32) << 16).view(np.float32)
     t0 = time.perf_counter()
+    q = oracle.qsa_qprep_rows(q_vals, Q.q_norm_w, 1, Q.raw_keys.shape[0], nh * hd, nh, hd, Q.rot, Q.theta,
+                              Q.eps)[0]
     keys = oracle.block_pool(Q.raw_keys, Q.k_norm_w, 0, Q.n_blocks, Q.ratio, Q.rot, Q.theta, Q.eps)
-    sc = oracle.qsa_score(Q.q, keys)
+    sc = oracle.qsa_score(q, keys)
     order = np.lexsort((np.arange(sc.size), -sc))[:Q.top_k]
     pos = oracle.expand_blocks(order[None].astype(np.int32), Q.ratio)
     oracle.gather_kv(pos, Q.page_table, Q.page_table.shape[1], Q.page_table.shape[1], Q.block_size,
@@ -317,8 +324,11 @@ def run_qsa(args, rank, world):
     hd, nb = Q.raw_keys.shape[1], Q.n_blocks
     raw = torch.from_numpy(Q.raw_keys_bits.view(np.int16)).to(dev)
     nw = torch.from_numpy(Q.k_norm_w).to(dev)
-    q = torch.from_numpy(Q.q[None]).to(dev)
-    w = torch.full((1, Q.q.shape[0]), 1.0 / math.sqrt(hd), device=dev)
+    n_heads = Q.q.shape[0]
+    q_raw = torch.from_numpy(Q.q_raw_bits.view(np.int16)).to(dev)
+    q_nw = torch.from_numpy(Q.q_norm_w).to(dev)
+    q = torch.empty((1, n_heads, hd), device=dev)
+    w = torch.full((1, n_heads), 1.0 / math.sqrt(hd), device=dev)
     table = torch.arange(nb // 64, dtype=torch.int32, device=dev).reshape(1, -1)
     lens = torch.tensor([nb], dtype=torch.int32, device=dev)
     kc = torch.from_numpy(Q.k_cache_bits.view(np.int16)).to(dev)
@@ -334,6 +344,7 @@ def run_qsa(args, rank, world):
     stream = torch.cuda.current_stream()
 
     def step():
+        idx.qsa_qprep(q_raw, q_nw, n_heads, Q.rot, Q.theta, Q.eps, first_pos=Q.raw_keys.shape[0], out=q)
         idx.block_pool(raw, nw, bk, 0, nb, Q.ratio, Q.rot, Q.theta, Q.eps)
         idx.score_topk(q, w, table, lens, Q.top_k, entries_per_block=64, keys_f32=bk.reshape(nb // 64, 64, hd),
                        out=(gi, gs))
@@ -344,7 +355,7 @@ def run_qsa(args, rank, world):
         flush.zero_()
         step()
     torch.cuda.synchronize()
-    # The five launches of a step are captured once in a CUDA graph: issued
+    # The six launches of a step are captured once in a CUDA graph: issued
     # from Python one by one they take longer on the host than on the device.
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
@@ -361,8 +372,9 @@ def run_qsa(args, rank, world):
         torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in ev]
     value, t_total = whole_job(nb, K, sum(ms) / 1e3)
-    # end to end: q in from pinned host memory, the selected blocks and their scores out
-    hq = torch.from_numpy(Q.q[None].copy()).pin_memory()
+    # end to end: the query's projection row in from pinned host memory, the
+    # selected blocks and their scores out
+    hq = torch.from_numpy(Q.q_raw_bits.view(np.int16).copy()).pin_memory()
     ho_i = torch.empty((1, Q.top_k), dtype=torch.int32).pin_memory()
     ho_s = torch.empty((1, Q.top_k), dtype=torch.float32).pin_memory()
     E = max(10, K // 10)
@@ -371,7 +383,7 @@ def run_qsa(args, rank, world):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        q.copy_(hq, non_blocking=True)
+        q_raw.copy_(hq, non_blocking=True)
         graph.replay()
         ho_i.copy_(gi, non_blocking=True)
         ho_s.copy_(gs, non_blocking=True)
@@ -379,9 +391,10 @@ def run_qsa(args, rank, world):
         e2e.append((a, b))
     torch.cuda.synchronize()
     e2e_value, _ = whole_job(nb, E, sum(a.elapsed_time(b) for a, b in e2e) / 1e3)
-    # algorithmic bytes: raw keys in, pooled keys out and back in, the gathered rows in and out
+    # algorithmic bytes: the query row in and prepared q out and back in, raw keys in,
+    # pooled keys out and back in, the gathered rows in and out
     row = int(np.prod(kc.shape[2:])) * kc.element_size()
-    algo = raw.numel() * 2 + 2 * bk.numel() * 4 + 2 * 2 * n_tok * row
+    algo = q_raw.numel() * 2 + 2 * q.numel() * 4 + raw.numel() * 2 + 2 * bk.numel() * 4 + 2 * 2 * n_tok * row
     hbm, _, kind = peaks()
     achieved = algo / (t_total / K) / 1e9
     if rank == 0:
@@ -391,9 +404,9 @@ def run_qsa(args, rank, world):
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": "qsa: " + QSA_STEP, "pairs_per_step": nb, "seed": 1004, "cuda_graph": True,
                        "l2": "flushed before every timed step (256 MB write, outside the timed events)"},
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": hq.numel() * 4,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": hq.numel() * 2,
                     "d2h_bytes_per_step": ho_i.numel() * 4 + ho_s.numel() * 4},
-            "gpu_launches": 5 * K,
+            "gpu_launches": 6 * K,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                          "traffic": None, "kernel": "whole QSA chain (latency-bound)", "peak_kind": kind,
                          "algorithmic_bytes_per_launch": algo},

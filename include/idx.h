@@ -224,6 +224,26 @@ idx_status_t idx_block_pool(const uint16_t *raw_keys, const float *k_norm_w, flo
                             uint32_t rot, float theta, float eps, idx_stream_t stream);
 
 /*
+ * idx_qsa_qprep — query preparation for QSA block scoring.
+ *
+ * "metrale_model_layers/layers/ops/qsa.rs", qsa_qprep (one decode query) and
+ * qsa_qprep_rows (prefill rows): for row r < rows and head h < n_heads, the
+ * head's q x = qk[r*qkw + h*hd .. + hd), then y = x / sqrt(mean(x^2) + eps) *
+ * (1 + w), then rope on the first `rot` dimensions at position first_pos + r,
+ * pairing d with d + rot/2 exactly as idx_block_pool does.
+ *   qk        device [rows, qkw] bf16 (raw bit patterns): rows of the indexer
+ *             projection; head h's q at columns h*hd .. h*hd+hd-1
+ *   q_norm_w  device [hd] float32
+ *   q_out     device [rows, n_heads, hd] float32
+ *   hd a multiple of 32 in [32, 1024]; rot even, rot <= hd; qkw >= n_heads*hd
+ * A decode query is rows = 1, first_pos = its position, qkw = n_heads*hd.
+ * rows == 0 or n_heads == 0 returns IDX_OK without launching.
+ */
+idx_status_t idx_qsa_qprep(const uint16_t *qk, const float *q_norm_w, float *q_out, uint32_t rows,
+                           uint32_t first_pos, uint32_t qkw, uint32_t n_heads, uint32_t hd, uint32_t rot,
+                           float theta, float eps, idx_stream_t stream);
+
+/*
  * idx_expand_blocks — token positions of selected blocks, for idx_gather_kv.
  *
  * qsa.rs, qsa_gather fills slot i with position sel[i]; the page does not

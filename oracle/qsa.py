@@ -1,9 +1,11 @@
-"""QSA key pooling, QSA block score, and the selected-row K/V gather, in float64.
+"""QSA key pooling, QSA query preparation, QSA block score, and the selected-row
+K/V gather, in float64.
 
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 Source: "metrale_model_layers/layers/ops/qsa.rs" (doc comments of
-``qsa_block_pool``, ``qsa_score`` and ``qsa_gather``) and the gather described
+``qsa_block_pool``, ``qsa_qprep``, ``qsa_qprep_rows``, ``qsa_score`` and
+``qsa_gather``) and the gather described
 in commit c2f705a of "Commit graph, dsv4/kernels/indexer" (dense tile from the
 paged pool through the block table).
 """
@@ -52,6 +54,37 @@ def block_pool(raw_keys, k_norm_w, first_block: int, n_new: int, ratio: int,
             z[a_i] = x1 * c - x2 * s
             z[b_i] = x2 * c + x1 * s
         out[i] = z
+    return out
+
+
+def qsa_qprep_rows(qk, q_norm_w, rows: int, first_pos: int, qkw: int, n_heads: int, hd: int, rot: int,
+                   theta: float, eps: float, *, interleaved: bool = False) -> np.ndarray:
+    """Query preparation for QSA scoring, ``[rows, n_heads, hd]``.
+
+    qsa.rs, ``qsa_qprep`` (one decode query: per head, RMSNorm scaled by
+    ``1 + w``, then partial rope at ``pos``) and ``qsa_qprep_rows`` (the same
+    for ``rows`` prefill rows at positions ``first_pos + row``, reading q from
+    rows of the indexer projection ``qk``). Readings where the page is silent:
+    row ``r`` of ``qk`` has ``qkw`` values and head ``h``'s q is its columns
+    ``h*hd .. h*hd+hd-1``; RMSNorm and rope as in :func:`block_pool`.
+    """
+    qk = np.asarray(qk, dtype=np.float64).reshape(rows, qkw)
+    w = np.asarray(q_norm_w, dtype=np.float64)
+    out = np.zeros((rows, n_heads, hd), dtype=np.float64)
+    half = rot // 2
+    for r in range(rows):
+        pos = first_pos + r
+        for h in range(n_heads):
+            x = qk[r, h * hd:(h + 1) * hd]
+            y = x / math.sqrt(float(np.mean(x * x)) + eps) * (1.0 + w)
+            z = y.copy()
+            for j in range(half):
+                ang = pos * theta ** (-2.0 * j / rot)
+                c, s = math.cos(ang), math.sin(ang)
+                a_i, b_i = (2 * j, 2 * j + 1) if interleaved else (j, j + half)
+                z[a_i] = y[a_i] * c - y[b_i] * s
+                z[b_i] = y[b_i] * c + y[a_i] * s
+            out[r, h] = z
     return out
 
 

@@ -7,6 +7,7 @@ the inputs' device, and work is queued on the current CUDA stream.
 * :func:`score_topk`   -> ``idx_score_topk``   (scores, top-k indices and scores)
 * :func:`gather_kv`    -> ``idx_gather_kv``    (selected K/V rows -> dense tile)
 * :func:`block_pool`   -> ``idx_block_pool``   (QSA mean -> RMSNorm(1+w) -> RoPE)
+* :func:`qsa_qprep`    -> ``idx_qsa_qprep``    (QSA query: RMSNorm(1+w) -> RoPE)
 * :func:`expand_blocks` -> ``idx_expand_blocks`` (selected blocks -> positions)
 * :func:`valid_lens_from_blocks` -> ``idx_valid_lens_from_blocks``
 """
@@ -204,6 +205,27 @@ def block_pool(raw_keys, k_norm_w, block_keys, first_block, n_new, ratio, rot, t
             _ptr(raw_keys), _ptr(k_norm_w), _ptr(block_keys), first_block, n_new, ratio, hd, rot,
             ctypes.c_float(theta), ctypes.c_float(eps), _stream(raw_keys.device)))
     return block_keys
+
+
+def qsa_qprep(qk, q_norm_w, n_heads, rot, theta, eps, *, first_pos=0, out=None):
+    """QSA query preparation: rows of the indexer projection ``qk`` (bf16
+    ``[rows, qkw]``, head h's q at columns ``h*hd``) -> float32
+    ``[rows, n_heads, hd]``, RMSNorm scaled by ``1 + q_norm_w`` then rope at
+    positions ``first_pos + row``. A decode query is one row."""
+    torch = _torch()
+    _check(qk, "qk", dims=2)
+    if qk.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError("qk must hold bf16 bit patterns (bfloat16 or 16-bit int)")
+    _check(q_norm_w, "q_norm_w", torch.float32, 1)
+    rows, qkw = qk.shape
+    hd = q_norm_w.shape[0]
+    q_out = out if out is not None else torch.empty((rows, n_heads, hd), dtype=torch.float32, device=qk.device)
+    _check(q_out, "out", torch.float32, 3)
+    lib = load_library()
+    with torch.cuda.device(qk.device):
+        _raise("idx_qsa_qprep", lib.idx_qsa_qprep(_ptr(qk), _ptr(q_norm_w), _ptr(q_out), rows, first_pos, qkw,
+                                                  n_heads, hd, rot, theta, eps, _stream(qk.device)))
+    return q_out
 
 
 def expand_blocks(blocks, ratio):

@@ -211,6 +211,21 @@ idx_status_t idx_block_pool(const uint16_t *raw_keys, const float *k_norm_w, flo
              : IDX_ERR_CUDA;
 }
 
+idx_status_t idx_qsa_qprep(const uint16_t *qk, const float *q_norm_w, float *q_out, uint32_t rows,
+                           uint32_t first_pos, uint32_t qkw, uint32_t n_heads, uint32_t hd, uint32_t rot,
+                           float theta, float eps, idx_stream_t stream) {
+  if (hd < 32 || hd > 1024 || hd % 32 != 0 || rot % 2 != 0 || rot > hd) return IDX_ERR_INVALID_ARG;
+  if (rows == 0 || n_heads == 0) return IDX_OK;
+  if (static_cast<unsigned long long>(qkw) < static_cast<unsigned long long>(n_heads) * hd) return IDX_ERR_INVALID_ARG;
+  if (rows > 0x7FFFFFFFu || n_heads > 65535u) return IDX_ERR_UNSUPPORTED;
+  if (!qk || !q_norm_w || !q_out) return IDX_ERR_INVALID_ARG;
+  if (!aligned(qk, 2) || !aligned(q_norm_w, 4) || !aligned(q_out, 4)) return IDX_ERR_INVALID_ARG;
+  return launch_qsa_qprep(qk, q_norm_w, q_out, rows, first_pos, qkw, n_heads, hd, rot, theta, eps,
+                          reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? IDX_OK
+             : IDX_ERR_CUDA;
+}
+
 idx_status_t idx_expand_blocks(const int32_t *blocks, int32_t T, int32_t n_blocks, int32_t ratio,
                                int32_t *positions, idx_stream_t stream) {
   if (T < 0 || n_blocks < 0 || n_blocks > kMaxTopK || ratio < 1) return IDX_ERR_INVALID_ARG;

@@ -67,20 +67,22 @@ struct RopeFreqs {
   double f[kMaxRopeFreqs];
 };
 
-__global__ void block_pool_kernel(const uint16_t *__restrict__ raw, const float *__restrict__ w,
-                                  float *__restrict__ out, uint32_t first_block, uint32_t ratio,
-                                  uint32_t hd, uint32_t rot, float eps, const __grid_constant__ RopeFreqs rf) {
-  extern __shared__ float sm[];  // [hd] pooled-normalised values, then [32] partial sums
+// One row of hd values (the mean of `nrow` bf16 rows `stride` elements apart)
+// -> RMSNorm scaled by (1 + w) -> rope at `pos` -> dst. One thread per
+// dimension; `sm` holds hd + 32 floats. Shared by the block pooling and the
+// query preparation, which differ only in where their rows come from.
+__device__ __forceinline__ void norm_rope_row(const uint16_t *__restrict__ src, long long stride, uint32_t nrow,
+                                              const float *__restrict__ w, float *__restrict__ dst, uint32_t hd,
+                                              uint32_t rot, double pos, float eps, const RopeFreqs &rf, float *sm) {
   float *y_s = sm;
   float *red = sm + hd;
   const uint32_t d = threadIdx.x;
-  const uint32_t b = first_block + blockIdx.x;
   float m = 0.0f;
-  for (uint32_t r = 0; r < ratio; ++r) {
-    const uint32_t bits = raw[(static_cast<long long>(b) * ratio + r) * hd + d];
+  for (uint32_t r = 0; r < nrow; ++r) {
+    const uint32_t bits = src[static_cast<long long>(r) * stride + d];
     m += __uint_as_float(bits << 16);
   }
-  m = m / static_cast<float>(ratio);
+  m = m / static_cast<float>(nrow);
   float sq = m * m;
   for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
   if (lane_id() == 0) red[d >> 5] = sq;
@@ -99,19 +101,41 @@ __global__ void block_pool_kernel(const uint16_t *__restrict__ raw, const float 
   const uint32_t half = rot / 2;
   if (d < rot) {
     const uint32_t i = d < half ? d : d - half;
-    const double pos = static_cast<double>(b) * ratio;
     const double ang = pos * rf.f[i];
     constexpr double kTwoPi = 6.283185307179586476925286766559;
     const double turns = rint(ang * (1.0 / kTwoPi));
-    const float red = static_cast<float>(fma(-turns, kTwoPi, ang));
+    const float rd = static_cast<float>(fma(-turns, kTwoPi, ang));
     float s, c;
-    sincosf(red, &s, &c);
+    sincosf(rd, &s, &c);
     if (d < half)
       o = y * c - y_s[d + half] * s;
     else
       o = y * c + y_s[d - half] * s;
   }
-  out[static_cast<long long>(b) * hd + d] = o;
+  dst[d] = o;
+}
+
+__global__ void block_pool_kernel(const uint16_t *__restrict__ raw, const float *__restrict__ w,
+                                  float *__restrict__ out, uint32_t first_block, uint32_t ratio,
+                                  uint32_t hd, uint32_t rot, float eps, const __grid_constant__ RopeFreqs rf) {
+  extern __shared__ float sm[];  // [hd] pooled-normalised values, then [32] partial sums
+  const uint32_t b = first_block + blockIdx.x;
+  norm_rope_row(raw + static_cast<long long>(b) * ratio * hd, hd, ratio, w, out + static_cast<long long>(b) * hd,
+                hd, rot, static_cast<double>(b) * ratio, eps, rf, sm);
+}
+
+// qsa.rs, qsa_qprep / qsa_qprep_rows: row r, head h of the indexer
+// projection (q of head h at columns h*hd of a row of width qkw) -> RMSNorm
+// scaled by (1 + w) -> rope at position first_pos + r. Grid (rows, n_heads),
+// one thread per dimension, as on the page.
+__global__ void qsa_qprep_kernel(const uint16_t *__restrict__ qk, const float *__restrict__ w,
+                                 float *__restrict__ q_out, uint32_t first_pos, uint32_t qkw, uint32_t n_heads,
+                                 uint32_t hd, uint32_t rot, float eps, const __grid_constant__ RopeFreqs rf) {
+  extern __shared__ float sm[];
+  const uint32_t r = blockIdx.x, h = blockIdx.y;
+  norm_rope_row(qk + static_cast<long long>(r) * qkw + static_cast<long long>(h) * hd, 0, 1, w,
+                q_out + (static_cast<long long>(r) * n_heads + h) * hd, hd, rot,
+                static_cast<double>(first_pos) + r, eps, rf, sm);
 }
 
 // --------------------------------------------------------- expand blocks ----
@@ -179,6 +203,19 @@ cudaError_t launch_block_pool(const uint16_t *raw, const float *w, float *out, u
   for (uint32_t i = 0; i < rot / 2; ++i)
     rf.f[i] = std::pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(rot));
   block_pool_kernel<<<n_new, hd, smem, stream>>>(raw, w, out, first_block, ratio, hd, rot, eps, rf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qsa_qprep(const uint16_t *qk, const float *w, float *q_out, uint32_t rows, uint32_t first_pos,
+                             uint32_t qkw, uint32_t n_heads, uint32_t hd, uint32_t rot, float theta, float eps,
+                             cudaStream_t stream) {
+  const size_t smem = (static_cast<size_t>(hd) + 32) * sizeof(float);
+  if (rot / 2 > static_cast<uint32_t>(kMaxRopeFreqs)) return cudaErrorInvalidValue;
+  RopeFreqs rf;
+  for (uint32_t i = 0; i < rot / 2; ++i)
+    rf.f[i] = std::pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(rot));
+  qsa_qprep_kernel<<<dim3(rows, n_heads), hd, smem, stream>>>(qk, w, q_out, first_pos, qkw, n_heads, hd, rot, eps,
+                                                              rf);
   return cudaGetLastError();
 }
 

@@ -72,6 +72,9 @@ cudaError_t launch_gather_kv(const idx_gather_kv_args &a, cudaStream_t stream);
 cudaError_t launch_block_pool(const uint16_t *raw, const float *w, float *out, uint32_t first_block,
                               uint32_t n_new, uint32_t ratio, uint32_t hd, uint32_t rot, float theta,
                               float eps, cudaStream_t stream);
+cudaError_t launch_qsa_qprep(const uint16_t *qk, const float *w, float *q_out, uint32_t rows, uint32_t first_pos,
+                             uint32_t qkw, uint32_t n_heads, uint32_t hd, uint32_t rot, float theta, float eps,
+                             cudaStream_t stream);
 cudaError_t launch_expand_blocks(const int32_t *blocks, int T, int n_blocks, int ratio,
                                  int32_t *positions, cudaStream_t stream);
 cudaError_t launch_valid_lens(const int32_t *block_lens, int T, int epb, int32_t *valid_lens,

@@ -194,6 +194,8 @@ class QsaWorkload:
     k_cache_bits: np.ndarray    # [pages, block_size, nkv, hd] uint16 (bf16)
     v_cache_bits: np.ndarray
     page_table: np.ndarray      # [1, pages] int32
+    q_raw_bits: np.ndarray = None   # [1, n_heads*hd] uint16 (bf16): the decode query's projection row
+    q_norm_w: np.ndarray = None     # [hd] float32
     ratio: int = 16
     rot: int = 64
     theta: float = 1.0e6
@@ -218,7 +220,11 @@ def qsa(seed: int = 1004, *, n_tok: int = 8192, hd: int = 128, n_heads: int = 32
     kc = _to_bf16_bits(rng.standard_normal((pages, block_size, nkv, hd)).astype(np.float32))
     vc = _to_bf16_bits(rng.standard_normal((pages, block_size, nkv, hd)).astype(np.float32))
     table = rng.permutation(pages).astype(np.int32).reshape(1, pages)
-    return QsaWorkload(bits, vals, k_norm_w, q, kc, vc, table, ratio=ratio, top_k=top_k,
+    # drawn last, so the fields above keep their values: the raw projection
+    # row the decode query is prepared from, and its norm weight
+    q_raw_bits = _to_bf16_bits(rng.standard_normal((1, n_heads * hd)).astype(np.float32))
+    q_norm_w = (rng.standard_normal(hd) * 0.1).astype(np.float32)
+    return QsaWorkload(bits, vals, k_norm_w, q, kc, vc, table, q_raw_bits, q_norm_w, ratio=ratio, top_k=top_k,
                        block_size=block_size)
 
 

@@ -33,7 +33,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("idx_score_topk", "idx_score_topk_workspace_size", "idx_gather_kv", "idx_block_pool",
-              "idx_expand_blocks", "idx_valid_lens_from_blocks", "idx_status_string", "idx_version"):
+              "idx_qsa_qprep", "idx_expand_blocks", "idx_valid_lens_from_blocks", "idx_status_string",
+              "idx_version"):
         assert n in names
 
 
@@ -151,6 +152,9 @@ def test_empty_calls_launch_nothing(lib):
     assert lib.idx_block_pool(None, None, None, 0, 0, 16, 128, 64, ctypes.c_float(1e6), ctypes.c_float(1e-6), None) == 0
     assert lib.idx_expand_blocks(None, 0, 4, 16, None, None) == 0
     assert lib.idx_valid_lens_from_blocks(None, 0, 64, None, None) == 0
+    f = ctypes.c_float
+    assert lib.idx_qsa_qprep(None, None, None, 0, 5, 4096, 32, 128, 64, f(1e6), f(1e-6), None) == 0
+    assert lib.idx_qsa_qprep(None, None, None, 3, 5, 4096, 0, 128, 64, f(1e6), f(1e-6), None) == 0
     g = _lib.GatherKvArgs()
     g.T, g.n_sel, g.max_logical_blocks, g.P, g.block_size, g.row_bytes = 0, 5, 1, 1, 16, 1024
     assert lib.idx_gather_kv(ctypes.byref(g), None) == 0
@@ -160,6 +164,11 @@ def test_other_entry_points_validate(lib):
     assert lib.idx_block_pool(None, None, None, 0, 1, 16, 100, 64, ctypes.c_float(1e6), ctypes.c_float(1e-6), None) == 1
     assert lib.idx_block_pool(None, None, None, 0, 1, 16, 128, 63, ctypes.c_float(1e6), ctypes.c_float(1e-6), None) == 1
     assert lib.idx_expand_blocks(None, 1, 4097, 16, None, None) == 1
+    f = ctypes.c_float
+    assert lib.idx_qsa_qprep(None, None, None, 1, 0, 4096, 32, 100, 64, f(1e6), f(1e-6), None) == 1   # hd % 32
+    assert lib.idx_qsa_qprep(None, None, None, 1, 0, 4096, 32, 128, 63, f(1e6), f(1e-6), None) == 1   # odd rot
+    assert lib.idx_qsa_qprep(None, None, None, 1, 0, 4000, 32, 128, 64, f(1e6), f(1e-6), None) == 1   # qkw too small
+    assert lib.idx_qsa_qprep(None, None, None, 1, 0, 4096, 32, 128, 64, f(1e6), f(1e-6), None) == 1   # null pointers
     assert lib.idx_valid_lens_from_blocks(None, 1, 0, None, None) == 1
     g = _lib.GatherKvArgs()
     g.T, g.n_sel, g.max_logical_blocks, g.P, g.block_size, g.row_bytes = 1, 5, 1, 1, 16, 1000

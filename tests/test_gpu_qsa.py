@@ -1,5 +1,5 @@
 """GPU parity of the QSA pieces and the K/V gather against the float64 oracle:
-idx_block_pool, idx_gather_kv (bit-exact), idx_expand_blocks (exact),
+idx_block_pool, idx_qsa_qprep, idx_gather_kv (bit-exact), idx_expand_blocks (exact),
 idx_valid_lens_from_blocks (exact), and the QSA workload end to end
 (pool -> score -> top-k -> expand -> gather)."""
 
@@ -47,6 +47,24 @@ def test_block_pool_all_blocks():
     ref = oracle.block_pool(Q.raw_keys, Q.k_norm_w, 0, Q.n_blocks, Q.ratio, Q.rot, Q.theta, Q.eps)
     tol = POOL_REL_TOL * np.max(np.abs(ref))
     assert np.max(np.abs(got - ref)) <= tol
+
+
+@pytest.mark.parametrize("rows,first_pos,extra", [(1, 131071, 0), (7, 1000, 256)])
+def test_qsa_qprep_rows(rows, first_pos, extra):
+    """Query preparation: one decode query at a far position, and prefill
+    rows read from a wider projection (extra columns after the q heads)."""
+    rng = np.random.default_rng(20 + rows)
+    nh, hd, rot, theta, eps = 32, 128, 64, 1e6, 1e-6
+    qkw = nh * hd + extra
+    x = rng.standard_normal((rows, qkw)).astype(np.float32)
+    bits = wl._to_bf16_bits(x)
+    vals = wl._to_bf16_values(x)
+    w = (rng.standard_normal(hd) * 0.1).astype(np.float32)
+    got = _idx().qsa_qprep(torch.from_numpy(bits.view(np.int16)).cuda(), torch.from_numpy(w).cuda(), nh, rot,
+                           theta, eps, first_pos=first_pos).cpu().numpy()
+    ref = oracle.qsa_qprep_rows(vals, w, rows, first_pos, qkw, nh, hd, rot, theta, eps)
+    assert got.shape == (rows, nh, hd)
+    assert np.max(np.abs(got - ref)) <= POOL_REL_TOL * np.max(np.abs(ref))
 
 
 def test_block_pool_incremental_rows_only():

@@ -331,6 +331,34 @@ def pin_pool_special_cases():
     return bool(ok)
 
 
+def pin_qprep_rows():
+    """qsa.rs qsa_qprep / qsa_qprep_rows: the block pooling's normalisation
+    and rope applied to single rows of the projection at first_pos + row."""
+    rng = np.random.default_rng(8)
+    hd, nh, rows = 16, 3, 5
+    x = rng.standard_normal((rows, nh * hd))
+    w = rng.standard_normal(hd) * 0.1
+    ok = True
+    # a one-row "block" at position p is the query row at position p (ratio 1)
+    for h in range(nh):
+        want = oracle.block_pool(x[:, h * hd:(h + 1) * hd], w, 0, rows, 1, 8, 1e4, 1e-6)
+        got = oracle.qsa_qprep_rows(x, w, rows, 0, nh * hd, nh, hd, 8, 1e4, 1e-6)[:, h]
+        ok &= np.allclose(got, want, rtol=1e-15, atol=0)
+    # head h reads columns h*hd .. h*hd+hd-1 of a wider row; the rest is ignored
+    wide = np.concatenate([x, rng.standard_normal((rows, 7)) * 1e3], axis=1)
+    a = oracle.qsa_qprep_rows(wide, w, rows, 0, nh * hd + 7, nh, hd, 8, 1e4, 1e-6)
+    b = oracle.qsa_qprep_rows(x, w, rows, 0, nh * hd, nh, hd, 8, 1e4, 1e-6)
+    ok &= np.array_equal(a, b)
+    # row r sits at first_pos + r
+    c = oracle.qsa_qprep_rows(x[2:], w, rows - 2, 2, nh * hd, nh, hd, 8, 1e4, 1e-6)
+    ok &= np.allclose(c, b[2:], rtol=1e-15, atol=0)
+    # closed form: hd 4, rot 2, q = [2,2,2,2] (RMS 2) at position 3, w = 0:
+    # [1,1,1,1] with the pair (0,1) turned by 3 rad
+    out = oracle.qsa_qprep_rows(np.full((1, 4), 2.0), np.zeros(4), 1, 3, 4, 1, 4, 2, 1e6, 0.0)
+    ok &= np.allclose(out[0, 0], [math.cos(3) - math.sin(3), math.cos(3) + math.sin(3), 1, 1], atol=1e-15)
+    return bool(ok)
+
+
 def pin_qsa_score_handcase():
     """qsa.rs qsa_score on a hand-summed case: heads [1,0,..] and [0,-1,..],
     keys [2,3,..] and [-1,1,..], hd=4 -> score0 = (2 + 0)/2 = 1,
@@ -350,7 +378,7 @@ PINS = [pin_e2m1_printed_table, pin_e2m1_bitlevel, pin_e4m3_library, pin_e4m3_an
         lambda: pin_golden("tiny_score_shared.json"), pin_onehot_layout, pin_closed_form,
         pin_block_permutation, pin_pow2_scaling, pin_positive_scaling_topk, pin_topk_vs_lexsort,
         pin_topk_bruteforce, pin_mask, pin_bad_inputs, pin_valid_lens_from_blocks,
-        pin_gather_library, pin_pool_special_cases, pin_qsa_score_handcase, pin_expand_blocks]
+        pin_gather_library, pin_pool_special_cases, pin_qprep_rows, pin_qsa_score_handcase, pin_expand_blocks]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: getattr(f, "__name__", "golden"))
@@ -413,8 +441,23 @@ def _mut_weight_inside_relu(q_t, w_t, K):
     return np.maximum(dots * np.asarray(w_t, np.float64), 0.0).sum(axis=1)
 
 
+def _mut_qprep_ignores_first_pos(qk, q_norm_w, rows, first_pos, qkw, n_heads, hd, rot, theta, eps, **kw):
+    return _real_qprep(qk, q_norm_w, rows, 0, qkw, n_heads, hd, rot, theta, eps, **kw)
+
+
+def _mut_qprep_head_stride_qkw(qk, q_norm_w, rows, first_pos, qkw, n_heads, hd, rot, theta, eps, **kw):
+    qk = np.asarray(qk, np.float64).reshape(rows, qkw)
+    cols = np.concatenate([qk[:, h * qkw // n_heads:h * qkw // n_heads + hd] for h in range(n_heads)], axis=1)
+    return _real_qprep(cols, q_norm_w, rows, first_pos, n_heads * hd, n_heads, hd, rot, theta, eps, **kw)
+
+
+_real_qprep = oracle.qsa_qprep_rows
+
+
 @pytest.mark.parametrize("name,target,fn", [
     *[(k, v[0], v[1]) for k, v in MUTATIONS.items()],
+    ("qprep_ignores_first_pos", "qsa_qprep_rows", _mut_qprep_ignores_first_pos),
+    ("qprep_head_stride_qkw", "qsa_qprep_rows", _mut_qprep_head_stride_qkw),
     ("relu_dropped", "index_scores", _mut_index_scores_no_relu),
     ("weight_inside_relu", "index_scores", _mut_weight_inside_relu),
     ("group_of_8", "dequant_rows", _mut_group_by_8),
@@ -422,6 +465,6 @@ def _mut_weight_inside_relu(q_t, w_t, K):
     ("ties_high_index_first", "topk_sorted", _mut_ties_high_index_first),
 ])
 def test_planted_mistake_is_caught(monkeypatch, name, target, fn):
-    monkeypatch.setattr(oi, target, fn)
+    monkeypatch.setattr(oi, target, fn, raising=hasattr(oi, target) or not hasattr(oracle, target))
     monkeypatch.setattr(oracle, target, fn, raising=False)
     assert not _all_pins_pass(), f"planted mistake {name!r} in {target} went unnoticed"
