@@ -17,12 +17,14 @@ Every function states the passage of the source pages it follows:
   79ef87f (E2M1 decode fix) and c2f705a (score+top-k, gather KV,
   compute_valid_lens).
 * "metrale_model_layers/layers/ops/qsa.rs": the doc comments of
-  ``qsa_block_pool``, ``qsa_score``, ``qsa_gather`` and ``qsa_score_rows``.
+  ``qsa_block_pool``, ``qsa_qprep``, ``qsa_qprep_rows``, ``qsa_score``,
+  ``qsa_gather`` and ``qsa_score_rows``.
 
 Parity status. Every function is pinned by ``tests/test_oracle_pins.py``
-except the RoPE pairing convention inside ``block_pool`` (the pages do not say
-which dimensions are paired): parity unpinned for that convention; its
-special cases (identity at position 0, norm preservation, rot=0) are pinned.
+except the RoPE pairing convention inside ``block_pool`` and
+``qsa_qprep_rows`` (the pages do not say which dimensions are paired): parity
+unpinned for that convention; its special cases (identity at position 0, norm
+preservation, rot=0) are pinned.
 """
 
 from .indexer import (  # noqa: F401
