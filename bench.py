@@ -413,6 +413,114 @@ def run_qsa(args, rank, world):
             "cpu_baseline": cpu, "clocks": clk.summary()}), flush=True)
 
 
+def qsa_attn_case(seed: int, rows: int = 512, first_pos: int = 8192, nq: int = 32, nkv: int = 4, hd: int = 128,
+                  ratio: int = 16, bs: int = 16, topk: int = 64):
+    """Prefill rows at positions first_pos.. over 64 distinct complete blocks
+    each (ascending) plus their tails, from bf16 caches behind a shuffled page
+    table."""
+    import numpy as np
+    from sparse_attention_top_paged_gb300 import workloads
+    rng = np.random.default_rng(seed)
+    pages = (first_pos + rows + bs - 1) // bs
+    P = pages + 8
+    kbits = workloads._to_bf16_bits(rng.standard_normal((P, bs, nkv, hd)).astype(np.float32))
+    vbits = workloads._to_bf16_bits(rng.standard_normal((P, bs, nkv, hd)).astype(np.float32))
+    table = rng.permutation(P)[:pages].astype(np.int32)
+    ncomp = [(first_pos + r + 1) // ratio for r in range(rows)]
+    lists = np.stack([np.sort(rng.choice(ncomp[r], size=topk, replace=False)) for r in range(rows)]).astype(np.int32)
+    q = rng.standard_normal((rows, nq, hd)).astype(np.float32)
+    tokens = sum(topk * ratio + (first_pos + r + 1) - ncomp[r] * ratio for r in range(rows))
+    return dict(q=q, kbits=kbits, vbits=vbits, table=table, lists=lists, first_pos=first_pos, ratio=ratio,
+                tokens=tokens, rows=rows, nq=nq, nkv=nkv, hd=hd)
+
+
+def run_qsa_attn(args, rank, world):
+    """QSA prefill attention (idx_qsa_prefill_attn) over 512 rows: (row,
+    token) pairs attended per second; HBM roofline on the K and V bytes each
+    row's kv heads gather."""
+    import math
+    import numpy as np
+    import torch
+    import sparse_attention_top_paged_gb300 as idx
+    c = qsa_attn_case(1005 + rank)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        n = 4
+        vals = lambda b: (b.astype(np.uint32) << 16).view(np.float32)
+        t0 = time.perf_counter()
+        oracle.qsa_prefill_attn(c["q"][:n], vals(c["kbits"]), vals(c["vbits"]), c["table"], c["lists"][:n],
+                                c["first_pos"], c["ratio"], 1.0 / math.sqrt(c["hd"]))
+        dt = time.perf_counter() - t0
+        pairs_n = c["tokens"] * n / c["rows"]
+        cpu = {"value": pairs_n * c["nq"] / dt, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"first {n} of {c['rows']} rows, all {c['nq']} heads, numpy float64, {dt:.2f} s",
+               "seconds": dt}
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = torch.device("cuda")
+    q = torch.from_numpy(c["q"]).to(dev)
+    kc = torch.from_numpy(c["kbits"].view(np.int16)).to(dev)
+    vc = torch.from_numpy(c["vbits"].view(np.int16)).to(dev)
+    table = torch.from_numpy(c["table"]).to(dev)
+    lists = torch.from_numpy(c["lists"]).to(dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        idx.qsa_prefill_attn(q, kc, vc, table, lists, c["first_pos"], c["ratio"], out=out)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    pairs = c["tokens"] * c["nq"]            # (row, head, token) scores per step
+    value, t_total = whole_job(pairs, K, sum(a.elapsed_time(b) for a, b in ev) / 1e3)
+    hq = torch.from_numpy(c["q"]).pin_memory()
+    ho = torch.empty_like(hq).pin_memory()
+    E = max(10, K // 10)
+    e2e = []
+    for _ in range(E):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        q.copy_(hq, non_blocking=True)
+        step()
+        ho.copy_(out, non_blocking=True)
+        b.record(stream)
+        e2e.append((a, b))
+    torch.cuda.synchronize()
+    e2e_value, _ = whole_job(pairs, E, sum(a.elapsed_time(b) for a, b in e2e) / 1e3)
+    algo = c["tokens"] * c["nkv"] * c["hd"] * 2 * 2 + 2 * q.numel() * 4
+    hbm, _, kind = peaks()
+    achieved = algo / (t_total / K) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t_total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"qsa_attn: {c['rows']} prefill rows from position {c['first_pos']}, 64 selected "
+                                   f"blocks of 16 tokens + tail each, nq={c['nq']} nkv={c['nkv']} hd={c['hd']}, "
+                                   "bf16 paged K/V", "pairs_per_step": pairs, "seed": 1005,
+                       "l2": "flushed before every timed step (256 MB write, outside the timed events)"},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": hq.numel() * 4,
+                    "d2h_bytes_per_step": ho.numel() * 4},
+            "gpu_launches": K,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": None, "kernel": "qsa_prefill_attn_kernel", "peak_kind": kind,
+                         "algorithmic_bytes_per_launch": algo},
+            "cpu_baseline": cpu, "clocks": clk.summary()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -420,7 +528,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "tensor", "simt"])
-    ap.add_argument("--workload", default="batched_decode", choices=sorted(WORKLOADS) + ["qsa"])
+    ap.add_argument("--workload", default="batched_decode", choices=sorted(WORKLOADS) + ["qsa", "qsa_attn"])
     ap.add_argument("--cpu-queries", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -434,6 +542,8 @@ def main():
         return run_reference(args, rank, world)
     if args.workload == "qsa":
         return run_qsa(args, rank, world)
+    if args.workload == "qsa_attn":
+        return run_qsa_attn(args, rank, world)
 
     import torch
     import sparse_attention_top_paged_gb300 as idx

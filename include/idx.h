@@ -244,6 +244,37 @@ idx_status_t idx_qsa_qprep(const uint16_t *qk, const float *q_norm_w, float *q_o
                            float theta, float eps, idx_stream_t stream);
 
 /*
+ * idx_qsa_prefill_attn — prefill attention over the selected blocks plus the
+ * incomplete tail.
+ *
+ * "metrale_model_layers/layers/ops/qsa.rs", qsa_prefill_attn: row r sits at
+ * position p = first_pos + r; blocks of `ratio` tokens b < (p+1)/ratio are
+ * complete. For each row and query head h, one softmax over
+ * (q[r,h] . K[t]) * inv_sqrt_d for every token t of each selected block
+ * b = lists[r*topk + i] with 0 <= b < (p+1)/ratio (other entries are
+ * skipped; duplicates count twice) and every tail token
+ * ((p+1)/ratio)*ratio <= t <= p, with K and V of kv head h / (nq/nkv);
+ * attn_out[r,h] = sum softmax * V. A row with no token gets zeros.
+ *   q            device [rows, nq, hd] float32
+ *   k_cache,
+ *   v_cache      device [P, block_size, nkv, hd] bf16 (raw bit patterns);
+ *                token t lives in page block_table[t / block_size], slot
+ *                t % block_size
+ *   block_table  device [n_pages] int32 (one sequence)
+ *   lists        device [rows, topk] int32 block ids (NULL when topk == 0)
+ *   attn_out     device [rows, nq, hd] float32
+ *   hd in {64, 128, 256}; nq a multiple of nkv; ratio, block_size >= 1
+ * Device-side errors: a token whose page index is past n_pages or whose page
+ * is outside [0,P) is left out (IDX_STATUS_BAD_BLOCK in *dev_status).
+ * rows == 0 or nq == 0 returns IDX_OK without launching.
+ */
+idx_status_t idx_qsa_prefill_attn(const float *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                  const int32_t *block_table, int32_t n_pages, int32_t P, const int32_t *lists,
+                                  float *attn_out, uint32_t rows, uint32_t first_pos, uint32_t topk,
+                                  uint32_t ratio, uint32_t block_size, uint32_t nq, uint32_t nkv, uint32_t hd,
+                                  float inv_sqrt_d, int32_t *dev_status, idx_stream_t stream);
+
+/*
  * idx_expand_blocks — token positions of selected blocks, for idx_gather_kv.
  *
  * qsa.rs, qsa_gather fills slot i with position sel[i]; the page does not

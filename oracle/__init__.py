@@ -18,7 +18,7 @@ Every function states the passage of the source pages it follows:
   compute_valid_lens).
 * "metrale_model_layers/layers/ops/qsa.rs": the doc comments of
   ``qsa_block_pool``, ``qsa_qprep``, ``qsa_qprep_rows``, ``qsa_score``,
-  ``qsa_gather`` and ``qsa_score_rows``.
+  ``qsa_gather``, ``qsa_score_rows`` and ``qsa_prefill_attn``.
 
 Parity status. Every function is pinned by ``tests/test_oracle_pins.py``
 except the RoPE pairing convention inside ``block_pool`` and
@@ -43,4 +43,4 @@ from .indexer import (  # noqa: F401
     STATUS_BAD_LEN,
     STATUS_BAD_SEL,
 )
-from .qsa import block_pool, qsa_qprep_rows, qsa_score, gather_kv, expand_blocks  # noqa: F401
+from .qsa import block_pool, qsa_qprep_rows, qsa_prefill_attn, qsa_score, gather_kv, expand_blocks  # noqa: F401

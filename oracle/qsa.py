@@ -1,11 +1,11 @@
-"""QSA key pooling, QSA query preparation, QSA block score, and the selected-row
-K/V gather, in float64.
+"""QSA key pooling, QSA query preparation, QSA block score, the selected-row
+K/V gather and the prefill attention over the selected blocks, in float64.
 
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 Source: "metrale_model_layers/layers/ops/qsa.rs" (doc comments of
-``qsa_block_pool``, ``qsa_qprep``, ``qsa_qprep_rows``, ``qsa_score`` and
-``qsa_gather``) and the gather described
+``qsa_block_pool``, ``qsa_qprep``, ``qsa_qprep_rows``, ``qsa_score``,
+``qsa_gather`` and ``qsa_prefill_attn``) and the gather described
 in commit c2f705a of "Commit graph, dsv4/kernels/indexer" (dense tile from the
 paged pool through the block table).
 """
@@ -86,6 +86,64 @@ def qsa_qprep_rows(qk, q_norm_w, rows: int, first_pos: int, qkw: int, n_heads: i
                 z[b_i] = y[b_i] * c + y[a_i] * s
             out[r, h] = z
     return out
+
+
+def qsa_prefill_attn(q, k_cache, v_cache, block_table, lists, first_pos: int, ratio: int,
+                     inv_sqrt_d: float):
+    """Prefill attention over the selected blocks plus the incomplete tail.
+
+    qsa.rs, ``qsa_prefill_attn``: per (row, q head), attention over exactly the
+    selected blocks in ``lists`` plus the incomplete tail, read from the paged
+    cache. Readings where the page is silent: row ``r`` is at position
+    ``p = first_pos + r``; blocks ``b < (p+1) // ratio`` are complete and only
+    those entries of the row's list count (others are skipped, duplicates are
+    not merged); the tail is tokens ``((p+1)//ratio)*ratio .. p``; query head
+    ``h`` reads kv head ``h // (nq // nkv)``; token ``t`` is at page
+    ``block_table[t // block_size]``, slot ``t % block_size``; one softmax of
+    ``(q . k) * inv_sqrt_d`` weights V. A token whose page is missing or out
+    of range is left out and reported; a row with no token gives zeros.
+
+    q ``[rows, nq, hd]``; caches ``[P, block_size, nkv, hd]`` (values);
+    block_table ``[n_pages]``; lists ``[rows, topk]``. Returns
+    ``(out [rows, nq, hd], status)``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    kc = np.asarray(k_cache, dtype=np.float64)
+    vc = np.asarray(v_cache, dtype=np.float64)
+    table = np.asarray(block_table).reshape(-1)
+    lists = np.asarray(lists).reshape(q.shape[0], -1)
+    rows, nq, hd = q.shape
+    P, block_size, nkv, _ = kc.shape
+    out = np.zeros((rows, nq, hd), dtype=np.float64)
+    status = 0
+    for r in range(rows):
+        p = first_pos + r
+        ncomp = (p + 1) // ratio
+        tokens = []
+        for b in lists[r]:
+            if 0 <= b < ncomp:
+                tokens.extend(range(int(b) * ratio, int(b) * ratio + ratio))
+        tokens.extend(range(ncomp * ratio, p + 1))
+        keep = []
+        for t in tokens:
+            pg = t // block_size
+            page = int(table[pg]) if pg < len(table) else -1
+            if 0 <= page < P:
+                keep.append((page, t % block_size))
+            else:
+                status |= STATUS_BAD_BLOCK
+        if not keep:
+            continue
+        pages = np.array([k[0] for k in keep])
+        slots = np.array([k[1] for k in keep])
+        for h in range(nq):
+            kv = h // (nq // nkv)
+            K = kc[pages, slots, kv]              # [n_tokens, hd]
+            V = vc[pages, slots, kv]
+            s = (K @ q[r, h]) * inv_sqrt_d
+            e = np.exp(s - s.max())
+            out[r, h] = (e / e.sum()) @ V
+    return out, status
 
 
 def qsa_score(q, block_keys) -> np.ndarray:

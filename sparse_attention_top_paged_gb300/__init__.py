@@ -8,6 +8,7 @@ the inputs' device, and work is queued on the current CUDA stream.
 * :func:`gather_kv`    -> ``idx_gather_kv``    (selected K/V rows -> dense tile)
 * :func:`block_pool`   -> ``idx_block_pool``   (QSA mean -> RMSNorm(1+w) -> RoPE)
 * :func:`qsa_qprep`    -> ``idx_qsa_qprep``    (QSA query: RMSNorm(1+w) -> RoPE)
+* :func:`qsa_prefill_attn` -> ``idx_qsa_prefill_attn`` (attention over selected blocks + tail)
 * :func:`expand_blocks` -> ``idx_expand_blocks`` (selected blocks -> positions)
 * :func:`valid_lens_from_blocks` -> ``idx_valid_lens_from_blocks``
 """
@@ -226,6 +227,37 @@ def qsa_qprep(qk, q_norm_w, n_heads, rot, theta, eps, *, first_pos=0, out=None):
         _raise("idx_qsa_qprep", lib.idx_qsa_qprep(_ptr(qk), _ptr(q_norm_w), _ptr(q_out), rows, first_pos, qkw,
                                                   n_heads, hd, rot, theta, eps, _stream(qk.device)))
     return q_out
+
+
+def qsa_prefill_attn(q, k_cache, v_cache, block_table, lists, first_pos, ratio, *, inv_sqrt_d=None,
+                     dev_status=None, out=None):
+    """Attention of prefill rows (``q`` float32 ``[rows, nq, hd]``, row r at
+    position ``first_pos + r``) over the selected blocks ``lists`` (int32
+    ``[rows, topk]``) plus the incomplete tail, from paged bf16 caches
+    ``[P, block_size, nkv, hd]`` through ``block_table`` (int32 ``[n_pages]``).
+    Returns float32 ``[rows, nq, hd]``."""
+    import math
+    torch = _torch()
+    _check(q, "q", torch.float32, 3)
+    for name, c in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _check(c, name, dims=4)
+        if c.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+            raise TypeError(f"{name} must hold bf16 bit patterns (bfloat16 or 16-bit int)")
+    _check(block_table, "block_table", torch.int32, 1)
+    _check(lists, "lists", torch.int32, 2)
+    rows, nq, hd = q.shape
+    P, block_size, nkv, _ = k_cache.shape
+    topk = lists.shape[1]
+    scale = 1.0 / math.sqrt(hd) if inv_sqrt_d is None else inv_sqrt_d
+    attn = out if out is not None else torch.empty((rows, nq, hd), dtype=torch.float32, device=q.device)
+    _check(attn, "out", torch.float32, 3)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        _raise("idx_qsa_prefill_attn", lib.idx_qsa_prefill_attn(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[0], P,
+            _ptr(lists) if topk > 0 else None, _ptr(attn), rows, first_pos, topk, ratio, block_size, nq, nkv, hd,
+            scale, _ptr(dev_status), _stream(q.device)))
+    return attn
 
 
 def expand_blocks(blocks, ratio):

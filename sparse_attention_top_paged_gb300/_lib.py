@@ -94,6 +94,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.idx_qsa_qprep.argtypes = [c_vp, c_vp, c_vp, c_u32, c_u32, c_u32, c_u32, c_u32, c_u32, c_f32, c_f32,
                                       c_vp]
         lib.idx_qsa_qprep.restype = c_i32
+        lib.idx_qsa_prefill_attn.argtypes = [c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_u32, c_u32, c_u32,
+                                             c_u32, c_u32, c_u32, c_u32, c_u32, c_f32, c_vp, c_vp]
+        lib.idx_qsa_prefill_attn.restype = c_i32
         lib.idx_expand_blocks.argtypes = [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp]
         lib.idx_expand_blocks.restype = c_i32
         lib.idx_valid_lens_from_blocks.argtypes = [c_vp, c_i32, c_i32, c_vp, c_vp]

@@ -33,7 +33,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("idx_score_topk", "idx_score_topk_workspace_size", "idx_gather_kv", "idx_block_pool",
-              "idx_qsa_qprep", "idx_expand_blocks", "idx_valid_lens_from_blocks", "idx_status_string",
+              "idx_qsa_qprep", "idx_qsa_prefill_attn", "idx_expand_blocks", "idx_valid_lens_from_blocks", "idx_status_string",
               "idx_version"):
         assert n in names
 
@@ -155,6 +155,8 @@ def test_empty_calls_launch_nothing(lib):
     f = ctypes.c_float
     assert lib.idx_qsa_qprep(None, None, None, 0, 5, 4096, 32, 128, 64, f(1e6), f(1e-6), None) == 0
     assert lib.idx_qsa_qprep(None, None, None, 3, 5, 4096, 0, 128, 64, f(1e6), f(1e-6), None) == 0
+    assert lib.idx_qsa_prefill_attn(None, None, None, None, 4, 4, None, None, 0, 0, 64, 16, 16, 32, 4, 128,
+                                    f(0.088), None, None) == 0
     g = _lib.GatherKvArgs()
     g.T, g.n_sel, g.max_logical_blocks, g.P, g.block_size, g.row_bytes = 0, 5, 1, 1, 16, 1024
     assert lib.idx_gather_kv(ctypes.byref(g), None) == 0
@@ -169,6 +171,9 @@ def test_other_entry_points_validate(lib):
     assert lib.idx_qsa_qprep(None, None, None, 1, 0, 4096, 32, 128, 63, f(1e6), f(1e-6), None) == 1   # odd rot
     assert lib.idx_qsa_qprep(None, None, None, 1, 0, 4000, 32, 128, 64, f(1e6), f(1e-6), None) == 1   # qkw too small
     assert lib.idx_qsa_qprep(None, None, None, 1, 0, 4096, 32, 128, 64, f(1e6), f(1e-6), None) == 1   # null pointers
+    pa = lambda hd, nq, nkv: lib.idx_qsa_prefill_attn(None, None, None, None, 4, 4, None, None, 1, 0, 64, 16, 16,
+                                                      nq, nkv, hd, f(0.088), None, None)
+    assert pa(96, 32, 4) == 1 and pa(128, 30, 4) == 1 and pa(128, 32, 0) == 1 and pa(128, 32, 4) == 1
     assert lib.idx_valid_lens_from_blocks(None, 1, 0, None, None) == 1
     g = _lib.GatherKvArgs()
     g.T, g.n_sel, g.max_logical_blocks, g.P, g.block_size, g.row_bytes = 1, 5, 1, 1, 16, 1000

@@ -1,5 +1,5 @@
 """GPU parity of the QSA pieces and the K/V gather against the float64 oracle:
-idx_block_pool, idx_qsa_qprep, idx_gather_kv (bit-exact), idx_expand_blocks (exact),
+idx_block_pool, idx_qsa_qprep, idx_qsa_prefill_attn, idx_gather_kv (bit-exact), idx_expand_blocks (exact),
 idx_valid_lens_from_blocks (exact), and the QSA workload end to end
 (pool -> score -> top-k -> expand -> gather)."""
 
@@ -167,3 +167,60 @@ def test_qsa_end_to_end():
     assert st == 0
     assert np.array_equal(k_out.cpu().numpy().view(np.uint16), rk)
     assert np.array_equal(v_out.cpu().numpy().view(np.uint16), rv)
+
+
+def _attn_case(seed, hd, nq, nkv, rows=6, first_pos=3000, ratio=16, bs=16, topk=64, bad_page=None):
+    rng = np.random.default_rng(seed)
+    n_tok = first_pos + rows + 50
+    pages = (n_tok + bs - 1) // bs
+    P = pages + 3
+    kbits = wl._to_bf16_bits(rng.standard_normal((P, bs, nkv, hd)).astype(np.float32))
+    vbits = wl._to_bf16_bits(rng.standard_normal((P, bs, nkv, hd)).astype(np.float32))
+    table = rng.permutation(P)[:pages].astype(np.int32)
+    if bad_page is not None:
+        table[bad_page] = -1
+    lists = np.stack([rng.integers(-1, (first_pos + r + 1) // ratio + 3, size=topk) for r in range(rows)])
+    lists = lists.astype(np.int32)
+    q = rng.standard_normal((rows, nq, hd)).astype(np.float32)
+    return q, kbits, vbits, table, lists, first_pos, ratio
+
+
+def _attn_gpu(q, kbits, vbits, table, lists, first_pos, ratio):
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _idx().qsa_prefill_attn(torch.from_numpy(q).cuda(), torch.from_numpy(kbits.view(np.int16)).cuda(),
+                                  torch.from_numpy(vbits.view(np.int16)).cuda(), torch.from_numpy(table).cuda(),
+                                  torch.from_numpy(lists).cuda(), first_pos, ratio, dev_status=st)
+    return got.cpu().numpy(), int(st.item())
+
+
+def _bf16_vals(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+@pytest.mark.parametrize("hd,nq,nkv", [(128, 32, 4), (64, 8, 8), (256, 4, 1)])
+def test_qsa_prefill_attn(hd, nq, nkv):
+    """Prefill rows over 64 listed blocks (some invalid or incomplete, i.e.
+    skipped) plus their tails, grouped query heads, three head sizes."""
+    q, kb, vb, table, lists, fp, ratio = _attn_case(30 + hd, hd, nq, nkv)
+    got, st = _attn_gpu(q, kb, vb, table, lists, fp, ratio)
+    ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
+                                       1.0 / math.sqrt(hd))
+    assert st == ost == 0
+    assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
+
+
+def test_qsa_prefill_attn_missing_page_and_first_rows():
+    """A page missing from the table drops its tokens (reported); rows at
+    positions 0.. attend to their tails alone."""
+    q, kb, vb, table, lists, fp, ratio = _attn_case(41, 128, 8, 2, rows=20, first_pos=0, bad_page=0)
+    got, st = _attn_gpu(q, kb, vb, table, lists, fp, ratio)
+    ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
+                                       1.0 / math.sqrt(128))
+    assert st == ost == oracle.STATUS_BAD_BLOCK
+    assert np.max(np.abs(got - ref)) <= 1e-4 * max(np.max(np.abs(ref)), 1.0)
+    q, kb, vb, table, lists, fp, ratio = _attn_case(42, 128, 8, 2, rows=40, first_pos=0, bad_page=1)
+    got, st = _attn_gpu(q, kb, vb, table, lists, fp, ratio)
+    ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
+                                       1.0 / math.sqrt(128))
+    assert st == ost == oracle.STATUS_BAD_BLOCK
+    assert np.max(np.abs(got - ref)) <= 1e-4 * max(np.max(np.abs(ref)), 1.0)

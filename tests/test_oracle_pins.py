@@ -359,6 +359,50 @@ def pin_qprep_rows():
     return bool(ok)
 
 
+def pin_prefill_attn():
+    """qsa.rs qsa_prefill_attn: softmax attention over the selected complete
+    blocks plus the tail, through the page table, one kv head per group."""
+    rng = np.random.default_rng(9)
+    P, bs, nkv, hd = 6, 4, 2, 8
+    kc = rng.standard_normal((P, bs, nkv, hd))
+    vc = rng.standard_normal((P, bs, nkv, hd))
+    table = np.array([3, 0, 5, 1, 4, 2])
+    ok = True
+    # position 0, no complete block: one token (the tail is position 0 alone) -> its V
+    q = rng.standard_normal((1, 4, hd))
+    out, st = oracle.qsa_prefill_attn(q, kc, vc, table, np.full((1, 2), -1), 0, 8, 0.5)
+    ok &= st == 0 and np.allclose(out[0, 0], vc[3, 0, 0], rtol=0, atol=1e-15)
+    # equal scores (K = 0) -> the mean of V over the attended tokens:
+    # position 9, ratio 4: blocks 0, 1 complete; list [1, 7 (incomplete), 1 (again)]; tail 8, 9
+    z = np.zeros_like(kc)
+    out, st = oracle.qsa_prefill_attn(q, z, vc, table, np.array([[1, 7, 1]]), 9, 4, 0.5)
+    toks = [4, 5, 6, 7, 4, 5, 6, 7, 8, 9]
+    want = np.mean([vc[table[t // bs], t % bs, 0] for t in toks], axis=0)
+    ok &= st == 0 and np.allclose(out[0, 0], want, rtol=1e-13)
+    # two tokens, closed form: q.k = 2 for token 0 and 0 for token 1 (scale 0.5)
+    # -> weights e^1 / (e^1 + 1) and 1 / (e^1 + 1)
+    k2 = np.zeros_like(kc); k2[3, 0, 0, 0] = 2.0
+    q2 = np.zeros((1, 2, hd)); q2[0, 0, 0] = 1.0
+    out, _ = oracle.qsa_prefill_attn(q2, k2, vc, table, np.zeros((1, 0), int), 1, 8, 0.5)
+    a = math.e / (math.e + 1)
+    ok &= np.allclose(out[0, 0], a * vc[3, 0, 0] + (1 - a) * vc[3, 1, 0], rtol=1e-13)
+    # query heads 0,1 read kv head 0 and heads 2,3 kv head 1 (V zero / one per kv head)
+    v01 = np.zeros_like(vc); v01[:, :, 1] = 1.0
+    out, _ = oracle.qsa_prefill_attn(q, kc, v01, table, np.array([[0, 1]]), 9, 4, 0.5)
+    ok &= np.allclose(out[0, :2], 0.0) and np.allclose(out[0, 2:], 1.0)
+    # the order of the list does not matter; a missing page is left out and reported
+    lst = np.array([[0, 1], [1, 0]])
+    q3 = np.repeat(q[:, None], 2, axis=0).reshape(2, 4, hd)
+    o1, _ = oracle.qsa_prefill_attn(q3[:1], kc, vc, table, lst[:1], 9, 4, 0.5)
+    o2, _ = oracle.qsa_prefill_attn(q3[1:], kc, vc, table, lst[1:], 9, 4, 0.5)
+    ok &= np.allclose(o1, o2, rtol=1e-13)
+    bad = table.copy(); bad[2] = -1       # tokens 8..11 have no page
+    o3, st = oracle.qsa_prefill_attn(q3[:1], kc, vc, bad, lst[:1], 9, 4, 0.5)
+    o4, _ = oracle.qsa_prefill_attn(q3[:1], kc, vc, table, lst[:1], 7, 4, 0.5)   # same blocks, no tail
+    ok &= st == oracle.STATUS_BAD_BLOCK and np.allclose(o3, o4, rtol=1e-13)
+    return bool(ok)
+
+
 def pin_qsa_score_handcase():
     """qsa.rs qsa_score on a hand-summed case: heads [1,0,..] and [0,-1,..],
     keys [2,3,..] and [-1,1,..], hd=4 -> score0 = (2 + 0)/2 = 1,
@@ -378,7 +422,8 @@ PINS = [pin_e2m1_printed_table, pin_e2m1_bitlevel, pin_e4m3_library, pin_e4m3_an
         lambda: pin_golden("tiny_score_shared.json"), pin_onehot_layout, pin_closed_form,
         pin_block_permutation, pin_pow2_scaling, pin_positive_scaling_topk, pin_topk_vs_lexsort,
         pin_topk_bruteforce, pin_mask, pin_bad_inputs, pin_valid_lens_from_blocks,
-        pin_gather_library, pin_pool_special_cases, pin_qprep_rows, pin_qsa_score_handcase, pin_expand_blocks]
+        pin_gather_library, pin_pool_special_cases, pin_qprep_rows, pin_prefill_attn, pin_qsa_score_handcase,
+        pin_expand_blocks]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: getattr(f, "__name__", "golden"))
@@ -452,12 +497,41 @@ def _mut_qprep_head_stride_qkw(qk, q_norm_w, rows, first_pos, qkw, n_heads, hd, 
 
 
 _real_qprep = oracle.qsa_qprep_rows
+_real_attn = oracle.qsa_prefill_attn
+
+
+def _mut_attn_tail_excludes_own_position(q, k_cache, v_cache, block_table, lists, first_pos, ratio, inv_sqrt_d):
+    # attends like the real one but one position earlier (the row's own token dropped)
+    q = np.asarray(q, np.float64)
+    outs, st = [], 0
+    for r in range(q.shape[0]):
+        if first_pos + r == 0:
+            outs.append(np.zeros(q.shape[1:]))
+            continue
+        o, s_ = _real_attn(q[r:r + 1], k_cache, v_cache, block_table, np.asarray(lists)[r:r + 1],
+                           first_pos + r - 1, ratio, inv_sqrt_d)
+        outs.append(o[0]); st |= s_
+    return np.array(outs), st
+
+
+def _mut_attn_kv_head_modulo(q, k_cache, v_cache, block_table, lists, first_pos, ratio, inv_sqrt_d):
+    q = np.asarray(q, np.float64)
+    nq, nkv = q.shape[1], np.asarray(k_cache).shape[2]
+    outs = []
+    for h in range(nq):   # head h reads kv head h % nkv
+        kv = h % nkv
+        kc = np.asarray(k_cache)[:, :, kv:kv + 1]; vc = np.asarray(v_cache)[:, :, kv:kv + 1]
+        o, st = _real_attn(q[:, h:h + 1], kc, vc, block_table, lists, first_pos, ratio, inv_sqrt_d)
+        outs.append(o[:, 0])
+    return np.stack(outs, axis=1), st
 
 
 @pytest.mark.parametrize("name,target,fn", [
     *[(k, v[0], v[1]) for k, v in MUTATIONS.items()],
     ("qprep_ignores_first_pos", "qsa_qprep_rows", _mut_qprep_ignores_first_pos),
     ("qprep_head_stride_qkw", "qsa_qprep_rows", _mut_qprep_head_stride_qkw),
+    ("attn_tail_excludes_own_position", "qsa_prefill_attn", _mut_attn_tail_excludes_own_position),
+    ("attn_kv_head_modulo", "qsa_prefill_attn", _mut_attn_kv_head_modulo),
     ("relu_dropped", "index_scores", _mut_index_scores_no_relu),
     ("weight_inside_relu", "index_scores", _mut_weight_inside_relu),
     ("group_of_8", "dequant_rows", _mut_group_by_8),
