@@ -197,7 +197,7 @@ def _bf16_vals(bits):
     return (bits.astype(np.uint32) << 16).view(np.float32)
 
 
-@pytest.mark.parametrize("hd,nq,nkv", [(128, 32, 4), (64, 8, 8), (256, 4, 1)])
+@pytest.mark.parametrize("hd,nq,nkv", [(128, 32, 4), (64, 8, 8), (256, 4, 1), (64, 4, 2), (128, 16, 4)])
 def test_qsa_prefill_attn(hd, nq, nkv):
     """Prefill rows over 64 listed blocks (some invalid or incomplete, i.e.
     skipped) plus their tails, grouped query heads, three head sizes."""
