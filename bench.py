@@ -521,6 +521,94 @@ def run_qsa_attn(args, rank, world):
             "cpu_baseline": cpu, "clocks": clk.summary()}), flush=True)
 
 
+def run_gather_split(args, rank, world):
+    """The FP8 + BF16 split gather (idx_gather_split): 64 queries x 2048
+    selected positions from a 262144-token paged cache, 512 E4M3 + per-token
+    scale + 64 bf16 per token, into a dense bf16 tile. HBM bound: gathered
+    bytes in, the tile out."""
+    import numpy as np
+    import torch
+    import sparse_attention_top_paged_gb300 as idx
+    from sparse_attention_top_paged_gb300 import workloads
+    rng = np.random.default_rng(1006 + rank)
+    T, n, bs, nd, rd, n_tok = 64, 2048, 64, 512, 64, 262144
+    P = n_tok // bs
+    codes = rng.integers(0, 256, size=(P, bs, nd), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38
+    scale = rng.uniform(0.01, 4.0, size=(P, bs)).astype(np.float32)
+    rope = workloads._to_bf16_bits(rng.standard_normal((P, bs, rd)).astype(np.float32))
+    table = np.stack([rng.permutation(P) for _ in range(T)]).astype(np.int32)
+    sel = np.stack([np.sort(rng.choice(n_tok, size=n, replace=False)) for _ in range(T)]).astype(np.int32)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        t0 = time.perf_counter()
+        oracle.gather_split(sel[:2], table[:2], P, P, bs, codes, scale, rope)
+        dt = time.perf_counter() - t0
+        cpu = {"value": 2 * n / dt, "unit": "rows/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"2 of {T} queries ({2 * n} rows), numpy, {dt:.2f} s", "seconds": dt}
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = torch.device("cuda")
+    d = lambda x: torch.from_numpy(x).to(dev)
+    dsel, dtab, dcodes, dscale, drope = d(sel), d(table), d(codes), d(scale), d(rope.view(np.int16))
+    out = torch.empty((T, n, nd + rd), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        idx.gather_split(dsel, dtab, bs, dcodes, drope, dscale, out=out)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    rows = T * n
+    value, t_total = whole_job(rows, K, sum(a.elapsed_time(b) for a, b in ev) / 1e3)
+    hsel = torch.from_numpy(sel).pin_memory()
+    hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    E = max(10, K // 10)
+    e2e = []
+    for _ in range(E):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dsel.copy_(hsel, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        b.record(stream)
+        e2e.append((a, b))
+    torch.cuda.synchronize()
+    e2e_value, _ = whole_job(rows, E, sum(a.elapsed_time(b) for a, b in e2e) / 1e3)
+    algo = rows * (nd + 4 + 2 * rd + 2 * (nd + rd) + 4)   # nope, scale, rope in; the tile out; sel
+    hbm, _, kind = peaks()
+    achieved = algo / (t_total / K) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "gathered rows per sec (FP8+BF16 split -> BF16 tile)", "value": value, "unit": "rows/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8->bf16",
+            "data": "synthetic",
+            "config": {"workload": f"gather_split: T={T} x {n} positions of {n_tok}, 512 e4m3 + scale + 64 bf16 "
+                                   "per token, block 64", "rows_per_step": rows, "seed": 1006,
+                       "l2": "flushed before every timed step (256 MB write, outside the timed events)"},
+            "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": hsel.numel() * 4,
+                    "d2h_bytes_per_step": hout.numel() * 2},
+            "gpu_launches": K,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": None, "kernel": "gather_split_kernel", "peak_kind": kind,
+                         "algorithmic_bytes_per_launch": algo},
+            "cpu_baseline": cpu, "clocks": clk.summary()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -528,7 +616,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "tensor", "simt"])
-    ap.add_argument("--workload", default="batched_decode", choices=sorted(WORKLOADS) + ["qsa", "qsa_attn"])
+    ap.add_argument("--workload", default="batched_decode",
+                    choices=sorted(WORKLOADS) + ["qsa", "qsa_attn", "gather_split"])
     ap.add_argument("--cpu-queries", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -544,6 +633,8 @@ def main():
         return run_qsa(args, rank, world)
     if args.workload == "qsa_attn":
         return run_qsa_attn(args, rank, world)
+    if args.workload == "gather_split":
+        return run_gather_split(args, rank, world)
 
     import torch
     import sparse_attention_top_paged_gb300 as idx

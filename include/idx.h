@@ -203,6 +203,44 @@ typedef struct {
 idx_status_t idx_gather_kv(const idx_gather_kv_args *args, idx_stream_t stream);
 
 /*
+ * idx_gather_split — the dense BF16 tile of selected positions from a paged
+ * cache whose rows are split into an FP8 part and a BF16 part.
+ *
+ * "Commit graph, dsv4/kernels/indexer", commit c2f705a (gather_kv.cu): one
+ * output row per (query, top-k entry), rows resolved through the block
+ * table, FP8 dequantised to BF16, the BF16 part copied. The commit gives no
+ * layout; this one: for p = sel[t,i] resolved to (phys, row) exactly as in
+ * idx_gather_kv, with s = nope_scale ? nope_scale[phys, row] : 1,
+ *   out[t,i, d]            = bf16_rn(float(e4m3(nope[phys,row,d])) * s), d < nope_dim
+ *   out[t,i, nope_dim + d] = rope[phys,row,d],                           d < rope_dim
+ * (float multiply, then round to nearest even). p < 0 gives a zero row;
+ * a logical block past max_logical_blocks a zero row and IDX_STATUS_BAD_SEL;
+ * phys outside [0,P) a zero row and IDX_STATUS_BAD_BLOCK.
+ *   sel          device [T, n_sel] int32
+ *   nope         device [P, block_size, nope_dim] FP8 E4M3 (OCP e4m3fn)
+ *   nope_scale   device [P, block_size] float32, or NULL
+ *   rope         device [P, block_size, rope_dim] bf16 (raw bit patterns)
+ *   out          device [T, n_sel, nope_dim + rope_dim] bf16
+ *   nope_dim a multiple of 4, rope_dim even; pointers 4-byte aligned
+ */
+typedef struct {
+  int32_t T, n_sel;
+  const int32_t *sel;
+  const int32_t *block_table;
+  int32_t max_logical_blocks;
+  int64_t bt_stride;
+  int32_t P, block_size;
+  const uint8_t *nope;
+  const float *nope_scale;
+  const uint16_t *rope;
+  int32_t nope_dim, rope_dim;
+  uint16_t *out;
+  int32_t *dev_status;
+} idx_gather_split_args;
+
+idx_status_t idx_gather_split(const idx_gather_split_args *args, idx_stream_t stream);
+
+/*
  * idx_block_pool — pool newly complete blocks of raw keys into block keys.
  *
  * "metrale_model_layers/layers/ops/qsa.rs", qsa_block_pool: for block

@@ -43,4 +43,5 @@ from .indexer import (  # noqa: F401
     STATUS_BAD_LEN,
     STATUS_BAD_SEL,
 )
-from .qsa import block_pool, qsa_qprep_rows, qsa_prefill_attn, qsa_score, gather_kv, expand_blocks  # noqa: F401
+from .qsa import (block_pool, qsa_qprep_rows, qsa_prefill_attn, qsa_score, gather_kv, gather_split,  # noqa: F401
+                  bf16_round, expand_blocks)

@@ -16,7 +16,7 @@ import math
 
 import numpy as np
 
-from .indexer import STATUS_BAD_BLOCK, STATUS_BAD_SEL
+from .indexer import STATUS_BAD_BLOCK, STATUS_BAD_SEL, e4m3_decode
 
 
 def block_pool(raw_keys, k_norm_w, first_block: int, n_new: int, ratio: int,
@@ -208,3 +208,32 @@ def gather_kv(sel, block_table, bt_stride: int, max_lb: int, block_size: int,
             k_out[t, i] = kc[phys, p % block_size]
             v_out[t, i] = vc[phys, p % block_size]
     return k_out, v_out, status
+
+
+def bf16_round(x) -> np.ndarray:
+    """float32 values -> bf16 bit patterns, rounded to nearest, ties to even
+    (finite inputs)."""
+    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def gather_split(sel, block_table, bt_stride: int, max_lb: int, block_size: int, nope, nope_scale, rope):
+    """The dense-tile gather of commit c2f705a (gather_kv.cu): rows of a paged
+    cache split into an FP8 part and a BF16 part, FP8 dequantised to BF16.
+
+    Layout reading (the commit gives none): per token ``nope_dim`` E4M3
+    bytes, an optional float32 scale, ``rope_dim`` bf16 values; output row =
+    ``bf16_rn(float32(e4m3) * scale)`` followed by the rope part unchanged.
+    Positions resolve as in :func:`gather_kv`. Returns ``(out bf16 bits
+    [T, n_sel, nope_dim + rope_dim], status)``.
+    """
+    nope = np.asarray(nope, dtype=np.uint8)
+    rope = np.asarray(rope, dtype=np.uint16)
+    P, bs, nope_dim = nope.shape
+    rope_dim = rope.shape[2]
+    scale = np.ones((P, bs), np.float32) if nope_scale is None else np.asarray(nope_scale, np.float32)
+    # every (phys, row) dequantised once: float32 product, then bf16 rounding
+    deq = bf16_round(e4m3_decode(nope).astype(np.float32) * scale[:, :, None])
+    rows = np.concatenate([deq, rope], axis=2)          # [P, bs, nope_dim + rope_dim] bf16 bits
+    out, _, status = gather_kv(sel, block_table, bt_stride, max_lb, block_size, rows, rows)
+    return out, status

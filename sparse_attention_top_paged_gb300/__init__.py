@@ -6,6 +6,7 @@ the inputs' device, and work is queued on the current CUDA stream.
 
 * :func:`score_topk`   -> ``idx_score_topk``   (scores, top-k indices and scores)
 * :func:`gather_kv`    -> ``idx_gather_kv``    (selected K/V rows -> dense tile)
+* :func:`gather_split` -> ``idx_gather_split`` (FP8 + BF16 split rows -> dense BF16 tile)
 * :func:`block_pool`   -> ``idx_block_pool``   (QSA mean -> RMSNorm(1+w) -> RoPE)
 * :func:`qsa_qprep`    -> ``idx_qsa_qprep``    (QSA query: RMSNorm(1+w) -> RoPE)
 * :func:`qsa_prefill_attn` -> ``idx_qsa_prefill_attn`` (attention over selected blocks + tail)
@@ -186,6 +187,45 @@ def gather_kv(sel, block_table, block_size, k_cache, v_cache=None, *, bt_stride=
     with torch.cuda.device(k_cache.device):
         _raise("idx_gather_kv", lib.idx_gather_kv(ctypes.byref(a), _stream(k_cache.device)))
     return k_out, v_out
+
+
+def gather_split(sel, block_table, block_size, nope, rope, nope_scale=None, *, bt_stride=None, dev_status=None,
+                 out=None):
+    """Dense bf16 ``[T, n_sel, nope_dim + rope_dim]`` rows at positions ``sel``
+    (-1: zero row) from a paged cache split into FP8 E4M3 ``nope``
+    (uint8 ``[P, block_size, nope_dim]``, optional float32 per-token
+    ``nope_scale`` ``[P, block_size]``) and bf16 ``rope``
+    (``[P, block_size, rope_dim]``)."""
+    torch = _torch()
+    _check(sel, "sel", torch.int32, 2)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(nope, "nope", torch.uint8, 3)
+    _check(rope, "rope", dims=3)
+    if rope.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError("rope must hold bf16 bit patterns (bfloat16 or 16-bit int)")
+    if nope_scale is not None:
+        _check(nope_scale, "nope_scale", torch.float32, 2)
+    T, n = sel.shape
+    P, bs, nope_dim = nope.shape
+    rope_dim = rope.shape[2]
+    o = out if out is not None else torch.empty((T, n, nope_dim + rope_dim), dtype=torch.bfloat16, device=sel.device)
+    _check(o, "out", dims=3)
+    a = _lib.GatherSplitArgs()
+    a.T, a.n_sel = T, n
+    a.sel, a.block_table = sel.data_ptr(), block_table.data_ptr()
+    a.max_logical_blocks = block_table.shape[1]
+    a.bt_stride = block_table.shape[1] if bt_stride is None else bt_stride
+    a.P, a.block_size = P, block_size
+    a.nope, a.rope = nope.data_ptr(), rope.data_ptr()
+    a.nope_scale = nope_scale.data_ptr() if nope_scale is not None else None
+    a.nope_dim, a.rope_dim = nope_dim, rope_dim
+    a.out = o.data_ptr()
+    if dev_status is not None:
+        a.dev_status = dev_status.data_ptr()
+    lib = load_library()
+    with torch.cuda.device(sel.device):
+        _raise("idx_gather_split", lib.idx_gather_split(ctypes.byref(a), _stream(sel.device)))
+    return o
 
 
 def block_pool(raw_keys, k_norm_w, block_keys, first_block, n_new, ratio, rot, theta, eps):

@@ -59,6 +59,19 @@ class GatherKvArgs(ctypes.Structure):
     ]
 
 
+class GatherSplitArgs(ctypes.Structure):
+    """Mirror of ``idx_gather_split_args``."""
+    _fields_ = [
+        ("T", c_i32), ("n_sel", c_i32),
+        ("sel", c_vp), ("block_table", c_vp),
+        ("max_logical_blocks", c_i32), ("bt_stride", c_i64),
+        ("P", c_i32), ("block_size", c_i32),
+        ("nope", c_vp), ("nope_scale", c_vp), ("rope", c_vp),
+        ("nope_dim", c_i32), ("rope_dim", c_i32),
+        ("out", c_vp), ("dev_status", c_vp),
+    ]
+
+
 class IndexerError(RuntimeError):
     def __init__(self, where: str, code: int):
         super().__init__(f"{where} failed: {STATUS_NAMES.get(code, code)}")
@@ -89,6 +102,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.idx_score_topk_static.restype = c_i32
         lib.idx_gather_kv.argtypes = [P(GatherKvArgs), c_vp]
         lib.idx_gather_kv.restype = c_i32
+        lib.idx_gather_split.argtypes = [P(GatherSplitArgs), c_vp]
+        lib.idx_gather_split.restype = c_i32
         lib.idx_block_pool.argtypes = [c_vp, c_vp, c_vp, c_u32, c_u32, c_u32, c_u32, c_u32, c_f32, c_f32, c_vp]
         lib.idx_block_pool.restype = c_i32
         lib.idx_qsa_qprep.argtypes = [c_vp, c_vp, c_vp, c_u32, c_u32, c_u32, c_u32, c_u32, c_u32, c_f32, c_f32,

@@ -33,7 +33,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("idx_score_topk", "idx_score_topk_workspace_size", "idx_gather_kv", "idx_block_pool",
-              "idx_qsa_qprep", "idx_qsa_prefill_attn", "idx_expand_blocks", "idx_valid_lens_from_blocks", "idx_status_string",
+              "idx_qsa_qprep", "idx_qsa_prefill_attn", "idx_gather_split", "idx_expand_blocks", "idx_valid_lens_from_blocks", "idx_status_string",
               "idx_version"):
         assert n in names
 
@@ -160,6 +160,9 @@ def test_empty_calls_launch_nothing(lib):
     g = _lib.GatherKvArgs()
     g.T, g.n_sel, g.max_logical_blocks, g.P, g.block_size, g.row_bytes = 0, 5, 1, 1, 16, 1024
     assert lib.idx_gather_kv(ctypes.byref(g), None) == 0
+    sp = _lib.GatherSplitArgs()
+    sp.T, sp.n_sel, sp.max_logical_blocks, sp.P, sp.block_size, sp.nope_dim, sp.rope_dim = 0, 5, 1, 1, 16, 512, 64
+    assert lib.idx_gather_split(ctypes.byref(sp), None) == 0
 
 
 def test_other_entry_points_validate(lib):
@@ -178,3 +181,11 @@ def test_other_entry_points_validate(lib):
     g = _lib.GatherKvArgs()
     g.T, g.n_sel, g.max_logical_blocks, g.P, g.block_size, g.row_bytes = 1, 5, 1, 1, 16, 1000
     assert lib.idx_gather_kv(ctypes.byref(g), None) == 1
+    sp = _lib.GatherSplitArgs()
+    sp.T, sp.n_sel, sp.max_logical_blocks, sp.P, sp.block_size, sp.nope_dim, sp.rope_dim = 1, 5, 1, 1, 16, 510, 64
+    assert lib.idx_gather_split(ctypes.byref(sp), None) == 1      # nope_dim not a multiple of 4
+    sp.nope_dim, sp.rope_dim = 512, 63
+    assert lib.idx_gather_split(ctypes.byref(sp), None) == 1      # odd rope_dim
+    sp.rope_dim = 64
+    assert lib.idx_gather_split(ctypes.byref(sp), None) == 1      # null pointers
+    assert lib.idx_gather_split(None, None) == 1

@@ -1,5 +1,6 @@
 """GPU parity of the QSA pieces and the K/V gather against the float64 oracle:
-idx_block_pool, idx_qsa_qprep, idx_qsa_prefill_attn, idx_gather_kv (bit-exact), idx_expand_blocks (exact),
+idx_block_pool, idx_qsa_qprep, idx_qsa_prefill_attn, idx_gather_kv and idx_gather_split
+(bit-exact), idx_expand_blocks (exact),
 idx_valid_lens_from_blocks (exact), and the QSA workload end to end
 (pool -> score -> top-k -> expand -> gather)."""
 
@@ -224,3 +225,26 @@ def test_qsa_prefill_attn_missing_page_and_first_rows():
                                        1.0 / math.sqrt(128))
     assert st == ost == oracle.STATUS_BAD_BLOCK
     assert np.max(np.abs(got - ref)) <= 1e-4 * max(np.max(np.abs(ref)), 1.0)
+
+
+@pytest.mark.parametrize("with_scale", [True, False])
+def test_gather_split_bit_exact(with_scale):
+    """The FP8 + BF16 split gather: dequantised rows bit-exact against the
+    oracle, -1 and out-of-table positions zero, a bad table entry reported."""
+    rng = np.random.default_rng(50 + with_scale)
+    P, bs, nd, rd, T, n, mlb = 40, 16, 512, 64, 3, 200, 32
+    codes = rng.integers(0, 256, size=(P, bs, nd)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38                       # no NaN codes
+    scale = rng.uniform(0.01, 4.0, size=(P, bs)).astype(np.float32) if with_scale else None
+    rope = wl._to_bf16_bits(rng.standard_normal((P, bs, rd)).astype(np.float32))
+    table = np.stack([rng.permutation(P)[:mlb] for _ in range(T)]).astype(np.int32)
+    table[2, 5] = P + 7
+    sel = rng.integers(-1, mlb * bs + 20, size=(T, n)).astype(np.int32)
+    sel[2, 0] = 5 * bs + 3                                     # lands in the bad entry
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d = lambda x: torch.from_numpy(x).cuda()
+    got = _idx().gather_split(d(sel), d(table), bs, d(codes), d(rope.view(np.int16)),
+                              d(scale) if with_scale else None, dev_status=st)
+    ref, ost = oracle.gather_split(sel, table, mlb, mlb, bs, codes, scale, rope)
+    assert int(st.item()) == ost == (oracle.STATUS_BAD_BLOCK | oracle.STATUS_BAD_SEL)
+    assert np.array_equal(got.cpu().view(torch.int16).numpy().view(np.uint16), ref)

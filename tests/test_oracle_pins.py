@@ -403,6 +403,35 @@ def pin_prefill_attn():
     return bool(ok)
 
 
+def pin_gather_split_library():
+    """commit c2f705a's split gather: the FP8 part through torch's float8 decode,
+    a float32 multiply and torch's bfloat16 cast; the bf16 part unchanged; rows
+    resolved by fancy indexing; -1 gives zeros, a bad table entry zeros + status."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(10)
+    P, bs, nd, rd, T, n = 6, 4, 8, 4, 3, 5
+    codes = rng.integers(0, 256, size=(P, bs, nd)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C                       # no NaN codes
+    scale = rng.uniform(0.01, 3.0, size=(P, bs)).astype(np.float32)
+    rope = rng.integers(0, 65536, size=(P, bs, rd)).astype(np.uint16)
+    table = rng.permutation(P)[:4].astype(np.int32).reshape(1, 4).repeat(T, 0)
+    sel = rng.integers(-1, 16, size=(T, n)).astype(np.int32)
+    out, st = oracle.gather_split(sel, table, 4, 4, bs, codes, scale, rope)
+    deq = (torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32)
+           * torch.from_numpy(scale)[:, :, None]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    rows = np.concatenate([deq, rope], axis=2)
+    pos = np.clip(sel, 0, None)
+    want = np.where((sel >= 0)[..., None], rows[table[np.arange(T)[:, None], pos // bs], pos % bs], 0)
+    ok = st == 0 and np.array_equal(out, want)
+    # ties round to even: 1 + 2^-8 -> 1.0, 1 + 3*2^-8 -> 1 + 2^-6
+    ok &= np.array_equal(oracle.bf16_round(np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8], np.float32)), [0x3F80, 0x3F82])
+    bad = table.copy(); bad[1, 0] = P + 2
+    sel2 = np.zeros((T, n), np.int32); sel2[1, 0] = 1
+    out2, st2 = oracle.gather_split(sel2, bad, 4, 4, bs, codes, None, rope)
+    ok &= st2 == oracle.STATUS_BAD_BLOCK and not out2[1, 0].any()
+    return bool(ok)
+
+
 def pin_qsa_score_handcase():
     """qsa.rs qsa_score on a hand-summed case: heads [1,0,..] and [0,-1,..],
     keys [2,3,..] and [-1,1,..], hd=4 -> score0 = (2 + 0)/2 = 1,
@@ -422,7 +451,8 @@ PINS = [pin_e2m1_printed_table, pin_e2m1_bitlevel, pin_e4m3_library, pin_e4m3_an
         lambda: pin_golden("tiny_score_shared.json"), pin_onehot_layout, pin_closed_form,
         pin_block_permutation, pin_pow2_scaling, pin_positive_scaling_topk, pin_topk_vs_lexsort,
         pin_topk_bruteforce, pin_mask, pin_bad_inputs, pin_valid_lens_from_blocks,
-        pin_gather_library, pin_pool_special_cases, pin_qprep_rows, pin_prefill_attn, pin_qsa_score_handcase,
+        pin_gather_library, pin_gather_split_library, pin_pool_special_cases, pin_qprep_rows, pin_prefill_attn,
+        pin_qsa_score_handcase,
         pin_expand_blocks]
 
 
@@ -500,6 +530,10 @@ _real_qprep = oracle.qsa_qprep_rows
 _real_attn = oracle.qsa_prefill_attn
 
 
+def _mut_bf16_truncate(x):
+    return (np.asarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
 def _mut_attn_tail_excludes_own_position(q, k_cache, v_cache, block_table, lists, first_pos, ratio, inv_sqrt_d):
     # attends like the real one but one position earlier (the row's own token dropped)
     q = np.asarray(q, np.float64)
@@ -532,6 +566,7 @@ def _mut_attn_kv_head_modulo(q, k_cache, v_cache, block_table, lists, first_pos,
     ("qprep_head_stride_qkw", "qsa_qprep_rows", _mut_qprep_head_stride_qkw),
     ("attn_tail_excludes_own_position", "qsa_prefill_attn", _mut_attn_tail_excludes_own_position),
     ("attn_kv_head_modulo", "qsa_prefill_attn", _mut_attn_kv_head_modulo),
+    ("bf16_truncates", "bf16_round", _mut_bf16_truncate),
     ("relu_dropped", "index_scores", _mut_index_scores_no_relu),
     ("weight_inside_relu", "index_scores", _mut_weight_inside_relu),
     ("group_of_8", "dequant_rows", _mut_group_by_8),
