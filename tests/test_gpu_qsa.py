@@ -228,11 +228,14 @@ def test_qsa_prefill_attn_missing_page_and_first_rows():
 
 
 @pytest.mark.parametrize("with_scale", [True, False])
-def test_gather_split_bit_exact(with_scale):
+@pytest.mark.parametrize("nd,rd,n", [(512, 64, 200), (512, 64, 201), (36, 6, 101)])
+def test_gather_split_bit_exact(with_scale, nd, rd, n):
     """The FP8 + BF16 split gather: dequantised rows bit-exact against the
-    oracle, -1 and out-of-table positions zero, a bad table entry reported."""
-    rng = np.random.default_rng(50 + with_scale)
-    P, bs, nd, rd, T, n, mlb = 40, 16, 512, 64, 3, 200, 32
+    oracle, -1 and out-of-table positions zero, a bad table entry reported.
+    Full-size rows, an odd row count and a short row whose parts are not
+    multiples of 8."""
+    rng = np.random.default_rng(50 + with_scale + nd + n)
+    P, bs, T, mlb = 40, 16, 3, 32
     codes = rng.integers(0, 256, size=(P, bs, nd)).astype(np.uint8)
     codes[(codes & 0x7F) == 0x7F] = 0x38                       # no NaN codes
     scale = rng.uniform(0.01, 4.0, size=(P, bs)).astype(np.float32) if with_scale else None
