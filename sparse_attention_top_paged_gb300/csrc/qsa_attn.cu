@@ -10,7 +10,7 @@
 // With 2, 4 or 8 query heads per kv head and hd <= 128, one CTA per
 // (row, kv head) serves the whole group (qsa_prefill_attn_group_kernel);
 // otherwise one CTA of 8 warps per (row, head), the page's launch shape: each warp
-// keeps an online-softmax partial (running max, running sum, hd accumulators,
+// keeps an online-softmax partial (reference max, running sum, hd accumulators,
 // hd / 32 per lane) over its share of the tokens, one token per step (a
 // vector of K and V per lane, a warp sum for the score); the partials are
 // merged at the end. (Four tokens per step raised the registers to 76 at
@@ -22,6 +22,12 @@ namespace idx {
 namespace {
 
 constexpr int kAttnWarps = 8;
+// Online softmax with a lazy reference maximum: the exponentials are taken
+// against a running reference m that moves only when a score exceeds it by
+// more than kLazyMax, so the accumulators are rescaled on few tokens and each
+// weight exp(s - m) stays below e^kLazyMax (no f32 overflow). Any reference
+// gives the same softmax; the partials are merged against their own m.
+constexpr float kLazyMax = 8.0f;
 
 template <int HPL>  // head dims per lane (hd = 32 * HPL)
 __global__ void __launch_bounds__(kAttnWarps * 32)
@@ -77,13 +83,17 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     for (int j = 0; j < HPL; ++j) s = fmaf(qv[j], kx[j], s);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-    const float m_new = fmaxf(m, s);
-    const float corr = expf(m - m_new);   // 0 for the first token (m = -inf)
-    const float e = expf(s - m_new);
-    l = fmaf(l, corr, e);
+    if (s > m + kLazyMax) {               // warp-uniform: rescale to the new reference maximum
+      const float corr = expf(m - s);     // 0 for the first token (m = -inf)
+      l *= corr;
 #pragma unroll
-    for (int j = 0; j < HPL; ++j) acc[j] = fmaf(acc[j], corr, e * vx[j]);
-    m = m_new;
+      for (int j = 0; j < HPL; ++j) acc[j] *= corr;
+      m = s;
+    }
+    const float e = expf(s - m);          // at most e^kLazyMax
+    l += e;
+#pragma unroll
+    for (int j = 0; j < HPL; ++j) acc[j] = fmaf(e, vx[j], acc[j]);
   };
 
   const long long ncomp = (p + 1) / ratio;
@@ -139,7 +149,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
   const int r = blockIdx.x, kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long p = static_cast<long long>(first_pos) + r;
-  float qv[G][HPL], acc[G][HPL], m[G], l[G];
+  float qv[G][HPL], acc[G][HPL];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     const int h = kvh * G + g;
@@ -148,37 +158,50 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
       qv[g][j] = q[(static_cast<long long>(r) * nq + h) * hd + lane * HPL + j] * inv_sqrt_d;
       acc[g][j] = 0.0f;
     }
-    m[g] = -INFINITY;
-    l[g] = 0.0f;
   }
+  // The softmax state of head lane >> (5 - kLogG), kept by the lanes that
+  // hold that head's scores: the reference maximum and the running sum.
+  float m = -INFINITY, l = 0.0f;
   bool bad = false;
 
   auto bf16 = [](uint32_t bits16) { return __uint_as_float(bits16 << 16); };
-  auto load = [&](const uint16_t *base, long long off, float (&x)[HPL]) {
-    if constexpr (HPL == 2) {
-      const uint32_t v = *reinterpret_cast<const uint32_t *>(base + off);
-      x[0] = bf16(v & 0xFFFFu); x[1] = bf16(v >> 16);
-    } else {
+  // A token's K and V words for this lane (HPL bf16 values each), fetched one
+  // token ahead of their use so the next token's loads overlap this one's math.
+  struct Raw {
+    uint32_t k[HPL / 2], v[HPL / 2];
+    bool ok;
+  };
+  auto fetch = [&](long long pos, Raw &x) {
+    const long long pg = pos / block_size;
+    const int page = pg < n_pages ? table[pg] : -1;
+    x.ok = page >= 0 && page < P;   // warp-uniform
+    if (!x.ok) return;
+    const long long off = ((static_cast<long long>(page) * block_size + pos % block_size) * nkv + kvh) * hd +
+                          lane * HPL;
 #pragma unroll
-      for (int j = 0; j < HPL; j += 4) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(base + off + j);
-        x[j] = bf16(v.x & 0xFFFFu); x[j + 1] = bf16(v.x >> 16);
-        x[j + 2] = bf16(v.y & 0xFFFFu); x[j + 3] = bf16(v.y >> 16);
+    for (int j = 0; j < HPL / 2; j += 2) {
+      if constexpr (HPL == 2) {
+        x.k[j] = *reinterpret_cast<const uint32_t *>(kc + off);
+        x.v[j] = *reinterpret_cast<const uint32_t *>(vc + off);
+      } else {
+        const uint2 kk = *reinterpret_cast<const uint2 *>(kc + off + 2 * j);
+        const uint2 vv = *reinterpret_cast<const uint2 *>(vc + off + 2 * j);
+        x.k[j] = kk.x; x.k[j + 1] = kk.y;
+        x.v[j] = vv.x; x.v[j + 1] = vv.y;
       }
     }
   };
-  auto token = [&](long long pos) {
-    const long long pg = pos / block_size;
-    const int page = pg < n_pages ? table[pg] : -1;
-    if (page < 0 || page >= P) {   // warp-uniform
+  auto token = [&](const Raw &x) {
+    if (!x.ok) {
       bad = true;
       return;
     }
-    const long long off = ((static_cast<long long>(page) * block_size + pos % block_size) * nkv + kvh) * hd +
-                          lane * HPL;
     float kx[HPL], vx[HPL];
-    load(kc, off, kx);
-    load(vc, off, vx);
+#pragma unroll
+    for (int j = 0; j < HPL / 2; ++j) {
+      kx[2 * j] = bf16(x.k[j] & 0xFFFFu); kx[2 * j + 1] = bf16(x.k[j] >> 16);
+      vx[2 * j] = bf16(x.v[j] & 0xFFFFu); vx[2 * j + 1] = bf16(x.v[j] >> 16);
+    }
     float v[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -203,35 +226,58 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
 #pragma unroll
     for (int o = 16 >> kLogG; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], o);
     // lane l now holds the score of head l >> (5 - kLogG)
+    const float s = v[0];
+    const bool grow = s > m + kLazyMax;
+    if (__any_sync(0xFFFFFFFFu, grow)) {   // some head's reference maximum moves up: rescale
+      const float m_new = grow ? s : m;
+      const float corr = expf(m - m_new);  // 0 on a head's first token, 1 where nothing moved
+      l *= corr;
+      m = m_new;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float cg = __shfl_sync(0xFFFFFFFFu, corr, g << (5 - kLogG));
+#pragma unroll
+        for (int j = 0; j < HPL; ++j) acc[g][j] *= cg;
+      }
+    }
+    const float e = expf(s - m);           // at most e^kLazyMax
+    l += e;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const float sg = __shfl_sync(0xFFFFFFFFu, v[0], g << (5 - kLogG));
-      const float m_new = fmaxf(m[g], sg);
-      const float corr = expf(m[g] - m_new);
-      const float e = expf(sg - m_new);
-      l[g] = fmaf(l[g], corr, e);
+      const float eg = __shfl_sync(0xFFFFFFFFu, e, g << (5 - kLogG));
 #pragma unroll
-      for (int j = 0; j < HPL; ++j) acc[g][j] = fmaf(acc[g][j], corr, e * vx[j]);
-      m[g] = m_new;
+      for (int j = 0; j < HPL; ++j) acc[g][j] = fmaf(eg, vx[j], acc[g][j]);
     }
   };
 
   const long long ncomp = (p + 1) / ratio;
+  Raw cur{}, nxt{};
   for (uint32_t i = warp; i < topk; i += kAttnWarps) {
     const long long b = lists[static_cast<long long>(r) * topk + i];
     if (b < 0 || b >= ncomp) continue;
-    for (uint32_t t = 0; t < ratio; ++t) token(b * ratio + t);
+    fetch(b * ratio, cur);
+    for (uint32_t t = 0; t < ratio; ++t) {
+      if (t + 1 < ratio) fetch(b * ratio + t + 1, nxt);
+      token(cur);
+      cur = nxt;
+    }
   }
-  for (long long pos = ncomp * ratio + warp; pos <= p; pos += kAttnWarps) token(pos);
+  const long long tail0 = ncomp * ratio + warp;
+  if (tail0 <= p) fetch(tail0, cur);
+  for (long long pos = tail0; pos <= p; pos += kAttnWarps) {
+    if (pos + kAttnWarps <= p) fetch(pos + kAttnWarps, nxt);
+    token(cur);
+    cur = nxt;
+  }
 
 #pragma unroll
   for (int g = 0; g < G; ++g) {
 #pragma unroll
     for (int j = 0; j < HPL; ++j) part[warp][g][lane * HPL + j] = acc[g][j];
-    if (lane == 0) {
-      pm[warp][g] = m[g];
-      pl[warp][g] = l[g];
-    }
+  }
+  if ((lane & ((32 >> kLogG) - 1)) == 0) {   // the first lane of each head
+    pm[warp][lane >> (5 - kLogG)] = m;
+    pl[warp][lane >> (5 - kLogG)] = l;
   }
   if (lane == 0 && bad && dev_status) atomicOr(dev_status, IDX_STATUS_BAD_BLOCK);
   __syncthreads();
