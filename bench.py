@@ -522,7 +522,7 @@ def run_qsa_attn(args, rank, world):
             "gpu_launches": K,
             "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_FMA_TFLOPS, "unit": "TFLOP/s",
                          "frac": achieved / FP32_FMA_TFLOPS, "traffic": None,
-                         "kernel": "qsa_prefill_attn_group_kernel<4, 8>",
+                         "kernel": "qsa_prefill_attn_tile_kernel<128, 8>",
                          "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz",
                          "algorithmic_flops_per_launch": flops},
             "cpu_baseline": cpu, "clocks": clk.summary()}), flush=True)

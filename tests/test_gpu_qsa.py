@@ -198,16 +198,36 @@ def _bf16_vals(bits):
     return (bits.astype(np.uint32) << 16).view(np.float32)
 
 
-@pytest.mark.parametrize("hd,nq,nkv", [(128, 32, 4), (64, 8, 8), (256, 4, 1), (64, 4, 2), (128, 16, 4)])
+@pytest.mark.parametrize("hd,nq,nkv", [(128, 32, 4), (64, 8, 8), (256, 4, 1), (64, 4, 2), (128, 16, 4),
+                                       (64, 16, 2), (128, 4, 2), (128, 4, 4), (64, 8, 2), (128, 6, 2)])
 def test_qsa_prefill_attn(hd, nq, nkv):
     """Prefill rows over 64 listed blocks (some invalid or incomplete, i.e.
-    skipped) plus their tails, grouped query heads, three head sizes."""
+    skipped) plus their tails: 1, 2, 3, 4 and 8 query heads per kv head,
+    three head sizes."""
     q, kb, vb, table, lists, fp, ratio = _attn_case(30 + hd, hd, nq, nkv)
     got, st = _attn_gpu(q, kb, vb, table, lists, fp, ratio)
     ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
                                        1.0 / math.sqrt(hd))
     assert st == ost == 0
     assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
+
+
+def test_qsa_prefill_attn_k_cache_8_byte_aligned():
+    """A K cache that starts 8 bytes past a 16-byte boundary (the per-head
+    kernel's 8-byte loads) gives the same attention."""
+    q, kb, vb, table, lists, fp, ratio = _attn_case(77, 128, 16, 2)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kflat = torch.zeros(kb.size + 4, dtype=torch.int16, device="cuda")
+    kflat[4:] = torch.from_numpy(kb.view(np.int16).reshape(-1)).cuda()
+    kc = kflat[4:].view(kb.shape)
+    assert kc.data_ptr() % 16 == 8
+    got = _idx().qsa_prefill_attn(torch.from_numpy(q).cuda(), kc, torch.from_numpy(vb.view(np.int16)).cuda(),
+                                  torch.from_numpy(table).cuda(), torch.from_numpy(lists).cuda(), fp, ratio,
+                                  dev_status=st)
+    ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
+                                       1.0 / math.sqrt(128))
+    assert int(st.item()) == ost == 0
+    assert np.max(np.abs(got.cpu().numpy() - ref)) <= 1e-4 * np.max(np.abs(ref))
 
 
 def test_qsa_prefill_attn_missing_page_and_first_rows():
