@@ -116,11 +116,6 @@ def launches_per_step(W) -> int:
     return 3
 
 
-# FP32 FMA rate of the CUDA cores: 152 SMs x 128 lanes x 2 flops x 2.07 GHz
-# (the maximum SM clock), in TFLOP/s.
-FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
-
-
 def peaks():
     """(HBM GB/s, dense bf16/f16 tensor TFLOP/s burst, "measured"|"fallback")."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -441,9 +436,13 @@ def qsa_attn_case(seed: int, rows: int = 512, first_pos: int = 8192, nq: int = 3
 
 def run_qsa_attn(args, rank, world):
     """QSA prefill attention (idx_qsa_prefill_attn) over 512 rows: (row,
-    head, token) scores per second. Its K and V (17.8 MB) stay in L2, so the
-    bound is the CUDA cores: 4*hd flops per (row, head, token) (the q.k dot
-    product and the weighted V sum) against the FP32 FMA rate."""
+    head, token) scores per second. Both contractions run on the tensor
+    cores: 4*hd flops per (row, head, token) (the q.k dot product and the
+    weighted V sum) against the bf16 tensor peak. With 8 heads per kv head a
+    gathered K or V element feeds 16 flops, so the kernel is bound by the
+    gather of K and V rows from L2 (17.8 MB of pages, each row gathered by
+    every query row that selects it), far below the tensor peak; the line
+    carries those gathered bytes and their rate as context."""
     import math
     import numpy as np
     import torch
@@ -508,6 +507,8 @@ def run_qsa_attn(args, rank, world):
     e2e_value, _ = whole_job(pairs, E, sum(a.elapsed_time(b) for a, b in e2e) / 1e3)
     flops = 4.0 * c["hd"] * pairs
     achieved = flops / (t_total / K) / 1e12
+    gathered = c["tokens"] * c["nkv"] * c["hd"] * 2 * 2   # K and V rows, bf16, per (row, kv head, token)
+    _, tensor, kind = peaks()
     if rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -520,11 +521,12 @@ def run_qsa_attn(args, rank, world):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": hq.numel() * 4,
                     "d2h_bytes_per_step": ho.numel() * 4},
             "gpu_launches": K,
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_FMA_TFLOPS, "unit": "TFLOP/s",
-                         "frac": achieved / FP32_FMA_TFLOPS, "traffic": None,
-                         "kernel": "qsa_prefill_attn_tile_kernel<128, 8>",
-                         "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz",
-                         "algorithmic_flops_per_launch": flops},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tensor, "unit": "TFLOP/s",
+                         "frac": achieved / tensor, "traffic": None,
+                         "kernel": "qsa_prefill_attn_tile_kernel<128, 8>", "peak_kind": kind,
+                         "algorithmic_flops_per_launch": flops,
+                         "gathered_bytes_per_launch": gathered,
+                         "gathered_gbs": gathered / (t_total / K) / 1e9},
             "cpu_baseline": cpu, "clocks": clk.summary()}), flush=True)
 
 

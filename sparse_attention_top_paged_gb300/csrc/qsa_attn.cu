@@ -9,12 +9,14 @@
 // through the page table; attn_out[r][h] is the softmax-weighted sum of V.
 // With 1, 2, 4 or 8 query heads per kv head, hd <= 128 and a 16-byte aligned
 // K cache, one CTA per (row, kv head) serves the whole group over 32-token
-// tiles (qsa_prefill_attn_tile_kernel: lane per token for the scores, lane
-// per dimension for the V sum). Otherwise one CTA of 8 warps per (row, head),
+// tiles (qsa_prefill_attn_tile_kernel: both contractions of a tile on the
+// tensor cores). Otherwise one CTA of 8 warps per (row, head),
 // the page's launch shape: each warp keeps an online-softmax partial
 // (reference max, running sum, hd accumulators, hd / 32 per lane) over its
 // share of the tokens, one token per step (a vector of K and V per lane, a
 // warp sum for the score); the partials are merged at the end.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -135,31 +137,67 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
 }
 
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr) : "memory");
+}
+
+// c += a . b on one m16n8k16 tile: a 16x16 bf16 (row-major), b 16x8 bf16
+// (column-major), c 16x8 f32.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Shared-memory bytes of qsa_prefill_attn_tile_kernel<HD, G>.
 template <int HD, int G>
 constexpr size_t tile_smem_bytes() {
-  return static_cast<size_t>(kAttnWarps) * 32 * (HD * 2 + 16)   // staged K rows (padded)
-         + G * HD * 4                                          // scaled q of the group
-         + kAttnWarps * 32 * G * 4                             // the tile's weights
+  return static_cast<size_t>(kAttnWarps) * 32 * (HD * 2 + 16)   // staged K, then V, rows (padded)
+         + 2 * 8 * (HD + 8) * 2                                // scaled q, bf16 hi and lo rows (8 heads)
+         + kAttnWarps * 2 * 8 * 40 * 2                         // the tile's weights, bf16 hi and lo [head][token]
          + 2 * kAttnWarps * 32 * 8                             // row offsets of this tile and the next
          + 2 * kAttnWarps * G * 4;                             // per-warp maxima and sums
 }
 
 // The same attention over 32-token tiles, one CTA of 8 warps per (row, kv
-// head) serving its G query heads (G = 1, 2, 4 or 8; hd = 64 or 128). For the
-// scores lane t owns token t of the warp's tile: the tile's K rows are staged
-// into shared memory with coalesced asynchronous copies (rows padded by 16
-// bytes so that lanes reading the same chunk of different rows hit distinct
-// banks), and each lane forms its token's G dot products against q broadcast
-// from shared memory: no per-token shuffle reduction. The weighted V sum then
-// gives each lane hd / 32 dimensions and walks the tile's tokens. Once the scores are formed, the same staging rows receive
-// the tile's V rows (one asynchronous copy per tile, not a load per token),
-// while the next tile's offsets are looked up and the softmax runs. Tokens
-// are numbered list-major (token t of selected block i is i * ratio + t,
-// blocks that are not complete masked out), then the tail.
+// head) serving its G query heads (G = 1, 2, 4 or 8; hd = 64 or 128), both
+// contractions on the tensor cores (mma.sync m16n8k16, bf16 in, f32
+// accumulate):
+//   scores  S[32 tokens x 8 heads] = K_tile . q^T. The tile's K rows are
+//           staged into shared memory by coalesced asynchronous copies (rows
+//           padded by 16 bytes, so ldmatrix reads them without bank
+//           conflicts). K is bf16 already; q * inv_sqrt_d is split into a
+//           bf16 high part and a bf16 low part (the rounding residual), two
+//           MMAs, so q keeps about 17 significant bits.
+//   V sum   O^T[hd x 8 heads] += V_tile^T . P^T, V^T read from the staged V
+//           rows with ldmatrix.trans, the weights P split into bf16 high and
+//           low parts the same way (two MMAs).
+// Heads past G are zero rows of q and P. Once the scores are formed, the
+// staging rows receive the tile's V rows (one asynchronous copy per tile)
+// while the next tile's offsets are looked up and the softmax runs on the
+// score fragments. Rows of tokens without K/V are zero-filled so the V sum
+// sees finite values. Tokens are numbered list-major (token t of selected
+// block i is i * ratio + t, blocks that are not complete masked out), then
+// the tail.
 template <int HD, int G>
 __global__ void __launch_bounds__(kAttnWarps * 32, 2)
     qsa_prefill_attn_tile_kernel(const float *__restrict__ q, const uint16_t *__restrict__ kc,
@@ -167,24 +205,35 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
                                  int P, const int32_t *__restrict__ lists, float *__restrict__ out,
                                  uint32_t first_pos, uint32_t topk, uint32_t ratio, uint32_t block_size, uint32_t nq,
                                  uint32_t nkv, float inv_sqrt_d, int32_t *dev_status) {
-  constexpr int HPL = HD / 32;        // dimensions per lane in the V sum
-  constexpr int NC = HD / 8;          // 16-byte chunks of a K row
+  constexpr int NC = HD / 8;          // 16-byte chunks of a K or V row
   constexpr int ROWB = HD * 2 + 16;   // staged row stride in bytes
+  constexpr int QROW = HD + 8;        // q row stride in bf16 elements (16 bytes of padding)
+  constexpr int PROW = 40;            // weight row stride in bf16 elements: 32 tokens + 16 bytes
+  constexpr int MT = HD / 16;         // 16-dimension tiles of the V sum
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char *kbuf = smem;
-  float *qs = reinterpret_cast<float *>(smem + static_cast<size_t>(kAttnWarps) * 32 * ROWB);
-  float *ps = qs + G * HD;
-  long long *roff = reinterpret_cast<long long *>(ps + kAttnWarps * 32 * G);
+  __nv_bfloat16 *qb = reinterpret_cast<__nv_bfloat16 *>(smem + static_cast<size_t>(kAttnWarps) * 32 * ROWB);
+  __nv_bfloat16 *pb = qb + 2 * 8 * QROW;   // [warp][hi, lo][8 heads][PROW]
+  long long *roff = reinterpret_cast<long long *>(pb + kAttnWarps * 2 * 8 * PROW);
   float *pm = reinterpret_cast<float *>(roff + 2 * kAttnWarps * 32);
   float *pl = pm + kAttnWarps * G;
-  float *part = reinterpret_cast<float *>(smem);   // [warp][G][HD] after the tiles: aliases the staged rows
-  static_assert(kAttnWarps * G * HD * 4 <= kAttnWarps * 32 * ROWB, "merge buffer fits the staging area");
+  constexpr int PSTR = HD + 4;        // merge row stride in floats: the fragment stores hit distinct banks
+  float *part = reinterpret_cast<float *>(smem);   // [warp][G][PSTR] after the tiles: aliases the staged rows
+  static_assert(kAttnWarps * G * PSTR * 4 <= kAttnWarps * 32 * ROWB, "merge buffer fits the staging area");
 
   const int r = blockIdx.x, kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long p = static_cast<long long>(first_pos) + r;
-  for (int x = threadIdx.x; x < G * HD; x += kAttnWarps * 32)
-    qs[x] = q[(static_cast<long long>(r) * nq + static_cast<long long>(kvh) * G + x / HD) * HD + x % HD] * inv_sqrt_d;
+  for (int x = threadIdx.x; x < 8 * HD; x += kAttnWarps * 32) {
+    const int g = x / HD, d = x % HD;
+    const float v =
+        g < G ? q[(static_cast<long long>(r) * nq + static_cast<long long>(kvh) * G + g) * HD + d] * inv_sqrt_d : 0.0f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    qb[g * QROW + d] = hi;
+    qb[(8 + g) * QROW + d] = __float2bfloat16_rn(v - __bfloat162float(hi));   // v - hi is exact in f32
+  }
+  for (int x = threadIdx.x; x < kAttnWarps * 2 * 8 * PROW; x += kAttnWarps * 32)
+    pb[x] = __float2bfloat16_rn(0.0f);   // rows of heads past G stay zero
   __syncthreads();
 
   const long long ncomp = (p + 1) / ratio;
@@ -192,16 +241,21 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
   const long long tail0 = ncomp * ratio;
   const long long n_virt = n_list + (p + 1 - tail0);
   unsigned char *kw = kbuf + static_cast<size_t>(warp) * 32 * ROWB;
-  float *pw = ps + warp * 32 * G;
+  __nv_bfloat16 *pw = pb + warp * 2 * 8 * PROW;
   long long *ow2 = roff + warp * 64;   // [2][32]: this tile's and the next tile's row offsets
-  float acc[G][HPL], m[G], l[G];   // m: the head's reference maximum (warp-uniform); l: this lane's share of the sum
+  const uint32_t kaddr = static_cast<uint32_t>(__cvta_generic_to_shared(kw));
+  const uint32_t qaddr = static_cast<uint32_t>(__cvta_generic_to_shared(qb));
+  const uint32_t paddr = static_cast<uint32_t>(__cvta_generic_to_shared(pw));
+  // MMA fragment coordinates: lane holds rows (lane >> 2) and (lane >> 2) + 8
+  // of a 16-row tile and columns (heads) h0 = 2 * (lane & 3), h0 + 1.
+  const int h0 = 2 * (lane & 3);
+  // mo: the reference maxima of heads h0, h0 + 1; lo: this lane's share of
+  // their sums; o: O^T fragments (dimension 16mt + row, head h0 + (i & 1)).
+  float mo[2] = {-INFINITY, -INFINITY}, lo[2] = {0.0f, 0.0f}, o[MT][4];
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.0f;
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int j = 0; j < HPL; ++j) acc[g][j] = 0.0f;
-  }
+    for (int i = 0; i < 4; ++i) o[mt][i] = 0.0f;
   bool bad = false;
 
   // The K/V element offset of this lane's token of the tile starting at
@@ -225,12 +279,16 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
     return ((static_cast<long long>(page) * block_size + pos % block_size) * nkv + kvh) * HD;
   };
   // Copies the K or V rows listed in o[0..31] into the staging rows
-  // (consecutive lanes: consecutive chunks of one row) as one asynchronous group.
-  auto stage = [&](const uint16_t *cache, const long long *o) {
+  // (consecutive lanes: consecutive chunks of one row) as one asynchronous
+  // group; rows without a token are zero-filled.
+  auto stage = [&](const uint16_t *cache, const long long *offs) {
     for (int x = lane; x < 32 * NC; x += 32) {
       const int t = x / NC, c = x % NC;
-      const long long src = o[t];
-      if (src >= 0) cp_async16(kw + t * ROWB + c * 16, cache + src + c * 8);
+      const long long src = offs[t];
+      if (src >= 0)
+        cp_async16(kw + t * ROWB + c * 16, cache + src + c * 8);
+      else
+        *reinterpret_cast<uint4 *>(kw + t * ROWB + c * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
     cp_async_commit();
   };
@@ -245,105 +303,126 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
     stage(kc, ow);
     cp_async_wait_all();
     __syncwarp();
-    constexpr int NCH = G >= 4 ? 1 : 2;   // dependent chains per head (G >= 4 heads already interleave)
-    float sa[NCH][G];
+
+    // ---- scores: S[32 tokens x 8 heads] ----
+    // tokens 16mt + (lane >> 2) (+ 8 in [2..3]), heads h0 and h0 + 1; the
+    // q high and low parts accumulate apart (four independent MMA chains)
+    float c[2][4], cl[2][4];
 #pragma unroll
-    for (int u = 0; u < NCH; ++u)
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int g = 0; g < G; ++g) sa[u][g] = 0.0f;
-    if (off >= 0) {
-      const unsigned char *kr = kw + lane * ROWB;
-#pragma unroll 2
-      for (int c = 0; c < NC; ++c) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(kr + c * 16);
-        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-        float kx[8];
+      for (int i = 0; i < 4; ++i) c[mt][i] = cl[mt][i] = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          kx[2 * e] = __uint_as_float(wv[e] << 16);
-          kx[2 * e + 1] = __uint_as_float(wv[e] & 0xFFFF0000u);
-        }
+    for (int ks = 0; ks < HD / 16; ++ks) {
+      uint32_t bh[2], bl[2];   // q rows (heads) 0-7, dimensions 16ks .. 16ks + 15
+      const uint32_t qa = qaddr + ((lane & 7) * QROW + ks * 16 + ((lane >> 3) & 1) * 8) * 2;
+      ldsm_x2(bh, qa);
+      ldsm_x2(bl, qa + 8 * QROW * 2);
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float4 qa = *reinterpret_cast<const float4 *>(qs + g * HD + 8 * c);
-          const float4 qb = *reinterpret_cast<const float4 *>(qs + g * HD + 8 * c + 4);
-          float &a = sa[c % NCH][g];
-          a = fmaf(qa.x, kx[0], a); a = fmaf(qa.y, kx[1], a); a = fmaf(qa.z, kx[2], a); a = fmaf(qa.w, kx[3], a);
-          a = fmaf(qb.x, kx[4], a); a = fmaf(qb.y, kx[5], a); a = fmaf(qb.z, kx[6], a); a = fmaf(qb.w, kx[7], a);
-        }
+      for (int mt = 0; mt < 2; ++mt) {
+        uint32_t a[4];   // K rows 16mt .. 16mt + 15, dimensions 16ks .. 16ks + 15
+        ldsm_x4(a, kaddr + (16 * mt + (lane & 15)) * ROWB + (ks * 2 + (lane >> 4)) * 16);
+        mma_bf16(c[mt], a, bh);
+        mma_bf16(cl[mt], a, bl);
       }
     }
-    __syncwarp();   // every lane has read its K row: the V rows may land
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[mt][i] += cl[mt][i];
+    __syncwarp();   // every lane has read its K fragments: the V rows may land
     stage(vc, ow);
     const long long nbase = base + kAttnWarps * 32;
     const long long noff = nbase < n_virt ? token_offset(nbase) : -1;
     const uint32_t nlive = __ballot_sync(0xFFFFFFFFu, noff >= 0);
     ow2[32 * (buf ^ 1) + lane] = noff;
-    float ev[G];
+
+    // ---- softmax on the score fragments: a token without K/V scores -inf ----
+    float sv[2][4];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float sc = off >= 0 ? (NCH == 2 ? sa[0][g] + sa[NCH - 1][g] : sa[0][g]) : -INFINITY;
-      float mt = sc;
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, o));
-      if (mt > m[g] + kLazyMax) {   // warp-uniform: rescale to the new reference maximum
-        const float corr = expf(m[g] - mt);
-        l[g] *= corr;
-#pragma unroll
-        for (int j = 0; j < HPL; ++j) acc[g][j] *= corr;
-        m[g] = mt;
+      for (int i = 0; i < 4; ++i) {
+        const int t = 16 * mt + (lane >> 2) + 8 * (i >> 1);
+        sv[mt][i] = ((live >> t) & 1u) ? c[mt][i] : -INFINITY;
       }
-      ev[g] = off >= 0 ? expf(sc - m[g]) : 0.0f;
-      l[g] += ev[g];
-    }
-    if constexpr (G % 4 == 0) {
+    float mx[2];
 #pragma unroll
-      for (int g = 0; g < G; g += 4)
-        *reinterpret_cast<float4 *>(pw + lane * G + g) = make_float4(ev[g], ev[g + 1], ev[g + 2], ev[g + 3]);
-    } else {
+    for (int hh = 0; hh < 2; ++hh) {
+      mx[hh] = fmaxf(fmaxf(sv[0][hh], sv[0][hh + 2]), fmaxf(sv[1][hh], sv[1][hh + 2]));
 #pragma unroll
-      for (int g = 0; g < G; ++g) pw[lane * G + g] = ev[g];
+      for (int sh = 4; sh < 32; sh <<= 1) mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xFFFFFFFFu, mx[hh], sh));
     }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      if (h0 + hh < G && mx[hh] > mo[hh] + kLazyMax) {   // the head's reference maximum moves up: rescale
+        const float corr = expf(mo[hh] - mx[hh]);
+        mo[hh] = mx[hh];
+        lo[hh] *= corr;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          o[mt][hh] *= corr;
+          o[mt][hh + 2] *= corr;
+        }
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int hh = i & 1;
+        if (h0 + hh >= G) continue;
+        const int t = 16 * mt + (lane >> 2) + 8 * (i >> 1);
+        const float x = sv[mt][i];
+        const float e = x != -INFINITY ? expf(x - mo[hh]) : 0.0f;   // at most e^kLazyMax
+        lo[hh] += e;
+        const __nv_bfloat16 ehi = __float2bfloat16_rn(e);
+        pw[(h0 + hh) * PROW + t] = ehi;
+        pw[(8 + h0 + hh) * PROW + t] = __float2bfloat16_rn(e - __bfloat162float(ehi));
+      }
     cp_async_wait_all();
-    __syncwarp();
-#pragma unroll 4
-    for (int t = 0; t < 32; ++t) {
-      if (!((live >> t) & 1u)) continue;
-      const unsigned char *vr = kw + t * ROWB + lane * HPL * 2;
-      float vx[HPL];
-      if constexpr (HPL == 2) {
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(vr);
-        vx[0] = __uint_as_float(w << 16); vx[1] = __uint_as_float(w & 0xFFFF0000u);
-      } else {
-        const uint2 w = *reinterpret_cast<const uint2 *>(vr);
-        vx[0] = __uint_as_float(w.x << 16); vx[1] = __uint_as_float(w.x & 0xFFFF0000u);
-        vx[2] = __uint_as_float(w.y << 16); vx[3] = __uint_as_float(w.y & 0xFFFF0000u);
-      }
+    __syncwarp();   // the V rows and every lane's weights are in place
+
+    // ---- V sum: O^T[hd x 8 heads] += V^T . P^T ----
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float pt = pw[t * G + g];
+    for (int kk = 0; kk < 2; ++kk) {
+      uint32_t bh[2], bl[2];   // P rows (heads) 0-7, tokens 16kk .. 16kk + 15
+      const uint32_t pa = paddr + ((lane & 7) * PROW + kk * 16 + ((lane >> 3) & 1) * 8) * 2;
+      ldsm_x2(bh, pa);
+      ldsm_x2(bl, pa + 8 * PROW * 2);
+      const int tok = 16 * kk + (lane & 7) + ((lane >> 4) & 1) * 8;
 #pragma unroll
-        for (int j = 0; j < HPL; ++j) acc[g][j] = fmaf(pt, vx[j], acc[g][j]);
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t a[4];   // V^T: dimensions 16mt .. 16mt + 15, tokens 16kk .. 16kk + 15
+        ldsm_x4_trans(a, kaddr + tok * ROWB + (16 * mt + ((lane >> 3) & 1) * 8) * 2);
+        mma_bf16(o[mt], a, bh);
+        mma_bf16(o[mt], a, bl);
       }
     }
-    off = noff;   // the next tile rewrites pw and kw after the __syncwarp at its top
+    off = noff;   // the next tile rewrites the staging rows and weights after the __syncwarp at its top
     live = nlive;
   }
 
 #pragma unroll
-  for (int g = 0; g < G; ++g)
+  for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l[g] += __shfl_xor_sync(0xFFFFFFFFu, l[g], o);
+    for (int sh = 4; sh < 32; sh <<= 1) lo[hh] += __shfl_xor_sync(0xFFFFFFFFu, lo[hh], sh);
   if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && dev_status) atomicOr(dev_status, IDX_STATUS_BAD_BLOCK);
   __syncthreads();   // every warp is done with its staged rows: part reuses them
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int j = 0; j < HPL; ++j) part[(warp * G + g) * HD + lane * HPL + j] = acc[g][j];
-    if (lane == 0) {
-      pm[warp * G + g] = m[g];
-      pl[warp * G + g] = l[g];
+    for (int i = 0; i < 4; ++i) {
+      const int g = h0 + (i & 1);
+      if (g < G) part[(warp * G + g) * PSTR + 16 * mt + (lane >> 2) + 8 * (i >> 1)] = o[mt][i];
     }
+  if (lane < 4) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+      if (h0 + hh < G) {
+        pm[warp * G + h0 + hh] = mo[hh];
+        pl[warp * G + h0 + hh] = lo[hh];
+      }
   }
   __syncthreads();
   for (int x = threadIdx.x; x < G * HD; x += kAttnWarps * 32) {
@@ -351,17 +430,17 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, pm[w * G + g]);
-    float L = 0.0f, o = 0.0f;
+    float L = 0.0f, acc = 0.0f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kAttnWarps; ++w) {
         if (pm[w * G + g] == -INFINITY) continue;   // a warp that saw no token
-        const float c = expf(pm[w * G + g] - M);
-        L = fmaf(pl[w * G + g], c, L);
-        o = fmaf(part[(w * G + g) * HD + d], c, o);
+        const float cw = expf(pm[w * G + g] - M);
+        L = fmaf(pl[w * G + g], cw, L);
+        acc = fmaf(part[(w * G + g) * PSTR + d], cw, acc);
       }
     }
-    out[(static_cast<long long>(r) * nq + static_cast<long long>(kvh) * G + g) * HD + d] = L > 0.0f ? o / L : 0.0f;
+    out[(static_cast<long long>(r) * nq + static_cast<long long>(kvh) * G + g) * HD + d] = L > 0.0f ? acc / L : 0.0f;
   }
 }
 
