@@ -41,14 +41,12 @@
 namespace idx {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kMaxThreads = 1024;                // selection CTA: 1024 threads when every row has an SM, else 512
 constexpr int kBins = kScoreBins;                 // 12-bit digits
-constexpr int kPer = kBins / kThreads;            // bins each thread owns in a scan
 constexpr int kBndCap = 2048;                     // largest boundary bin collected (else refine)
 constexpr int kRankBinMax = kBndCap;              // largest bin above the boundary ordered in place
 constexpr int kWarpBin = 128;                     // bins up to this size are sorted by one warp
 constexpr int kMaxLarge = 8;                      // more larger bins than this: sort the whole buffer
-constexpr int kLargeKeys = kBndCap / kThreads;    // a large bin's keys per thread
 constexpr int kUnroll = 4;                        // 16-byte score loads in flight per thread
 constexpr int kSmallRow = 2048;                   // rows up to this long are sorted whole
 constexpr int kCollectThreads = 256;              // split collection: threads per CTA,
@@ -56,7 +54,6 @@ constexpr int kCollectMin = 2048;                 // at least this many keys per
 constexpr int kMaxChunks = 32;                    // at most this many CTAs per row
 constexpr int kCollectBuf = 2048;                 // keys a collecting CTA holds before flushing
 constexpr long long kSplitMinLen = 65536;         // split only rows at least this long
-static_assert(kBndCap % kThreads == 0, "a large bin's keys spread evenly over the threads");
 
 __host__ __device__ inline int pow2_at_least(int k) {
   int kp = 1;
@@ -67,8 +64,8 @@ __host__ __device__ inline int pow2_at_least(int k) {
 struct SelShared {
   uint32_t table[kBins];      // counts of the current digit; once the first digit decides,
                               // per bin: end of its buffer segment | count << 16
-  uint32_t warp_sum[kThreads / 32];
-  uint32_t warp_max[kThreads / 32];   // largest bin above the boundary (first digit)
+  uint32_t warp_sum[kMaxThreads / 32];
+  uint32_t warp_max[kMaxThreads / 32];   // largest bin above the boundary (first digit)
   int b_bin, b_above, b_cnt;  // boundary bin, its keys above, its keys
   int n_buf;                  // append cursor (later-digit decisions)
   int abort_flag;             // a staging copy never completed
@@ -102,6 +99,7 @@ __host__ __device__ inline SelSmem sel_smem(int k, long long max_len) {
 // Sorts out[0 .. m) descending (m a power of two, 64 <= m): bitonic network,
 // strides >= 64 through shared memory, strides <= 32 in registers (a warp
 // holds 64 consecutive keys) so they need no block barrier.
+template <int kThreads>
 __device__ void sort_desc(uint64_t *out, int m) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kWarps = kThreads / 32;
@@ -167,8 +165,9 @@ __device__ __forceinline__ bool bad_len(const ScoreParams &p, int L) {
 // first digit is decided); another row is read with 16-byte global loads,
 // four per thread in flight. pass(thr, f) calls f(key) for every key whose
 // score is not -inf and whose order (the key's top 32 bits) is >= thr.
-constexpr int kBlock = kThreads * 4 * kUnroll;
+template <int kThreads>
 struct RowSource {
+  static constexpr int kBlock = kThreads * 4 * kUnroll;
   const float *row;
   int L;
   bool staged;
@@ -426,10 +425,14 @@ __global__ void __launch_bounds__(kCollectThreads) select_collect_kernel(ScorePa
   if (s_n > 0u) flush();
 }
 
-__global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p, const float *__restrict__ scores,
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(ScoreParams p, const float *__restrict__ scores,
                                                               long long ld, const uint32_t *__restrict__ hist,
                                                               const uint64_t *__restrict__ cand,
                                                               uint32_t *__restrict__ cand_cnt, int cand_cap) {
+  constexpr int kPer = kBins / kThreads;           // bins each thread owns in a scan
+  constexpr int kLargeKeys = kBndCap / kThreads;   // a large bin's keys per thread
+  static_assert(kBndCap % kThreads == 0 && kThreads <= kMaxThreads, "a large bin's keys spread evenly");
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SelShared *sh = reinterpret_cast<SelShared *>(smem_raw);
   const SelSmem lay = sel_smem(p.top_k, static_cast<long long>(p.max_lb) * p.epb);
@@ -468,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p,
     const int m = max(64, pow2_at_least(count));
     for (int i = count + tid; i < m; i += kThreads) buf[i] = 0ull;
     __syncthreads();
-    sort_desc(buf, m);
+    sort_desc<kThreads>(buf, m);
     const int got = min(count, k);
     for (int i = tid; i < k; i += kThreads) {
       oi[i] = i < got ? key_index(buf[i]) : -1;
@@ -478,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p,
   }
 
   const uint32_t sbar = ptx::smem_addr(smem_raw + lay.bar);
-  RowSource rs{row, L, lay.stage_floats > 0 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0,
+  RowSource<kThreads> rs{row, L, lay.stage_floats > 0 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0,
                reinterpret_cast<float *>(smem_raw + lay.stage), static_cast<int>(lay.stage_floats), sbar, 0u, -1, -1,
                &sh->abort_flag};
   if (tid == 0) {
@@ -639,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p,
       const int m = max(64, pow2_at_least(total));   // total <= k - 1 + kBndCap, m <= cap
       for (int i = total + tid; i < m; i += kThreads) buf[i] = 0ull;
       __syncthreads();
-      sort_desc(buf, m);
+      sort_desc<kThreads>(buf, m);
       for (int i = tid; i < min(total, k); i += kThreads) emit(buf[i], i);
     } else {
       for (int x = 0; x < n_large; ++x) {
@@ -735,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(ScoreParams p,
     const int m = max(64, pow2_at_least(count));
     for (int i = count + tid; i < m; i += kThreads) buf[i] = 0ull;
     __syncthreads();
-    sort_desc(buf, m);
+    sort_desc<kThreads>(buf, m);
     produced = min(count, k);
     for (int i = tid; i < produced; i += kThreads) emit(buf[i], i);
   }
@@ -787,8 +790,13 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
                           const SelectPlan &pl, void *workspace, cudaStream_t stream) {
   if (p.T == 0) return cudaSuccess;
   const size_t smem = sel_smem(p.top_k, static_cast<long long>(p.max_lb) * p.epb).total;
-  cudaError_t e =
-      cudaFuncSetAttribute(topk_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  // One CTA per row: when every row gets an SM of its own, 1024 threads;
+  // with more rows than SMs, 512 (two CTAs share an SM when shared memory allows).
+  const int sms = device_sm_count();
+  const bool wide = sms > 0 && p.T <= sms;
+  void (*kern)(ScoreParams, const float *, long long, const uint32_t *, const uint64_t *, uint32_t *, int) =
+      wide ? topk_stream_kernel<1024> : topk_stream_kernel<512>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   uint64_t *cand = nullptr;
   uint32_t *cand_cnt = nullptr;
@@ -809,7 +817,7 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(p.T), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(wide ? 1024 : 512, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -817,7 +825,7 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, topk_stream_kernel, p, scores, ld, hist, static_cast<const uint64_t *>(cand),
+  return cudaLaunchKernelEx(&cfg, kern, p, scores, ld, hist, static_cast<const uint64_t *>(cand),
                             cand_cnt, pl.cand_cap);
 }
 
