@@ -45,7 +45,6 @@ constexpr int kMaxThreads = 1024;                // selection CTA: 1024 threads 
 constexpr int kBins = kScoreBins;                 // 12-bit digits
 constexpr int kBndCap = 2048;                     // largest boundary bin collected (else refine)
 constexpr int kRankBinMax = kBndCap;              // largest bin above the boundary ordered in place
-constexpr int kWarpBin = 128;                     // bins up to this size are sorted by one warp
 constexpr int kMaxLarge = 8;                      // more larger bins than this: sort the whole buffer
 constexpr int kUnroll = 4;                        // 16-byte score loads in flight per thread
 constexpr int kSmallRow = 2048;                   // rows up to this long are sorted whole
@@ -431,6 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
                                                               const uint64_t *__restrict__ cand,
                                                               uint32_t *__restrict__ cand_cnt, int cand_cap) {
   constexpr int kPer = kBins / kThreads;           // bins each thread owns in a scan
+  // Bins up to kWarpBin keys are sorted by one warp in registers: 128 with
+  // 1024 threads per row; 256 with 512 (more rows than SMs, as in prefill,
+  // where broad selections fill many bins past 128 and a warp-sorted bin
+  // saves the CTA-wide split).
+  constexpr int kWarpBin = kThreads == 1024 ? 128 : 256;
   constexpr int kLargeKeys = kBndCap / kThreads;   // a large bin's keys per thread
   static_assert(kBndCap % kThreads == 0 && kThreads <= kMaxThreads, "a large bin's keys spread evenly");
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -719,7 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
           const int cnt = min(n, total - start);
           if (cnt <= 32) warp_sort_segment<1>(buf, start, cnt, emit_if);
           else if (cnt <= 64) warp_sort_segment<2>(buf, start, cnt, emit_if);
-          else warp_sort_segment<4>(buf, start, cnt, emit_if);
+          else if (kWarpBin <= 128 || cnt <= 128) warp_sort_segment<4>(buf, start, cnt, emit_if);
+          else if constexpr (kWarpBin > 128) warp_sort_segment<8>(buf, start, cnt, emit_if);
         }
       }
     }
