@@ -530,16 +530,14 @@ def run_qsa_attn(args, rank, world):
             "cpu_baseline": cpu, "clocks": clk.summary()}), flush=True)
 
 
-def run_gather_split(args, rank, world):
-    """The FP8 + BF16 split gather (idx_gather_split): 64 queries x 2048
-    selected positions from a 262144-token paged cache, 512 E4M3 + per-token
-    scale + 64 bf16 per token, into a dense bf16 tile. HBM bound: gathered
-    bytes in, the tile out."""
+def gather_split_case(seed: int):
+    """The split-gather workload: 64 queries x 2048 sorted positions of a
+    262144-token cache (block 64), 512 E4M3 codes (no NaN code) + an f32
+    scale in [0.01, 4) + 64 bf16 rope values per token, one page-table
+    permutation per query."""
     import numpy as np
-    import torch
-    import sparse_attention_top_paged_gb300 as idx
     from sparse_attention_top_paged_gb300 import workloads
-    rng = np.random.default_rng(1006 + rank)
+    rng = np.random.default_rng(seed)
     T, n, bs, nd, rd, n_tok = 64, 2048, 64, 512, 64, 262144
     P = n_tok // bs
     codes = rng.integers(0, 256, size=(P, bs, nd), dtype=np.uint8)
@@ -548,6 +546,21 @@ def run_gather_split(args, rank, world):
     rope = workloads._to_bf16_bits(rng.standard_normal((P, bs, rd)).astype(np.float32))
     table = np.stack([rng.permutation(P) for _ in range(T)]).astype(np.int32)
     sel = np.stack([np.sort(rng.choice(n_tok, size=n, replace=False)) for _ in range(T)]).astype(np.int32)
+    return {"T": T, "n": n, "bs": bs, "nd": nd, "rd": rd, "n_tok": n_tok, "P": P, "codes": codes, "scale": scale,
+            "rope": rope, "table": table, "sel": sel}
+
+
+def run_gather_split(args, rank, world):
+    """The FP8 + BF16 split gather (idx_gather_split): 64 queries x 2048
+    selected positions from a 262144-token paged cache, 512 E4M3 + per-token
+    scale + 64 bf16 per token, into a dense bf16 tile. HBM bound: gathered
+    bytes in, the tile out."""
+    import numpy as np
+    import torch
+    import sparse_attention_top_paged_gb300 as idx
+    c = gather_split_case(1006 + rank)
+    T, n, bs, nd, rd, n_tok, P = c["T"], c["n"], c["bs"], c["nd"], c["rd"], c["n_tok"], c["P"]
+    codes, scale, rope, table, sel = c["codes"], c["scale"], c["rope"], c["table"], c["sel"]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle

@@ -795,10 +795,12 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
                           const SelectPlan &pl, void *workspace, cudaStream_t stream) {
   if (p.T == 0) return cudaSuccess;
   const size_t smem = sel_smem(p.top_k, static_cast<long long>(p.max_lb) * p.epb).total;
-  // One CTA per row: when every row gets an SM of its own, 1024 threads;
-  // with more rows than SMs, 512 (two CTAs share an SM when shared memory allows).
+  // One CTA per row: when every row gets an SM of its own and rows are longer
+  // than a whole-row sort, 1024 threads; with more rows than SMs, 512 (two
+  // CTAs share an SM when shared memory allows), and 512 for short rows, whose
+  // single sort of at most kSmallRow keys gains nothing from more warps.
   const int sms = device_sm_count();
-  const bool wide = sms > 0 && p.T <= sms;
+  const bool wide = sms > 0 && p.T <= sms && static_cast<long long>(p.max_lb) * p.epb > kSmallRow;
   void (*kern)(ScoreParams, const float *, long long, const uint32_t *, const uint64_t *, uint32_t *, int) =
       wide ? topk_stream_kernel<1024> : topk_stream_kernel<512>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

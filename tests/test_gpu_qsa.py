@@ -271,3 +271,47 @@ def test_gather_split_bit_exact(with_scale, nd, rd, n):
     ref, ost = oracle.gather_split(sel, table, mlb, mlb, bs, codes, scale, rope)
     assert int(st.item()) == ost == (oracle.STATUS_BAD_BLOCK | oracle.STATUS_BAD_SEL)
     assert np.array_equal(got.cpu().view(torch.int16).numpy().view(np.uint16), ref)
+
+
+def _bench():
+    import importlib
+    import os
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    return importlib.import_module("bench")
+
+
+def test_qsa_prefill_attn_bench_size_sampled_rows():
+    """The benchmark's attention workload (512 rows from position 8192, 64
+    selected blocks of 16 tokens plus the tail, 32 q heads over 4 kv heads,
+    hd 128) in the launch the benchmark times; sampled rows against the
+    oracle, each computed at its own position."""
+    c = _bench().qsa_attn_case(1005)
+    got, st = _attn_gpu(c["q"], c["kbits"], c["vbits"], c["table"], c["lists"], c["first_pos"], c["ratio"])
+    assert st == 0
+    kv, vv = _bf16_vals(c["kbits"]), _bf16_vals(c["vbits"])
+    for r in (0, 1, 137, 300, 511):
+        ref, ost = oracle.qsa_prefill_attn(c["q"][r:r + 1], kv, vv, c["table"], c["lists"][r:r + 1],
+                                           c["first_pos"] + r, c["ratio"], 1.0 / math.sqrt(c["hd"]))
+        assert ost == 0
+        assert np.max(np.abs(got[r:r + 1] - ref)) <= 1e-4 * np.max(np.abs(ref)), r
+
+
+def test_gather_split_bench_size_sampled_queries():
+    """The benchmark's split-gather workload (64 queries x 2048 positions of a
+    262144-token cache) in one launch; sampled queries bit-exact against the
+    oracle."""
+    c = _bench().gather_split_case(1006)
+    d = lambda x: torch.from_numpy(x).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _idx().gather_split(d(c["sel"]), d(c["table"]), c["bs"], d(c["codes"]), d(c["rope"].view(np.int16)),
+                              d(c["scale"]), dev_status=st)
+    assert int(st.item()) == 0
+    got = got.cpu().view(torch.int16).numpy().view(np.uint16)
+    for t in (0, 17, 63):
+        ref, ost = oracle.gather_split(c["sel"][t:t + 1], c["table"][t:t + 1], c["P"], c["P"], c["bs"], c["codes"],
+                                       c["scale"], c["rope"])
+        assert ost == 0
+        assert np.array_equal(got[t:t + 1], ref), t
