@@ -304,7 +304,7 @@ idx_status_t idx_qsa_qprep(const uint16_t *qk, const float *q_norm_w, float *q_o
  *   hd in {64, 128, 256}; nq a multiple of nkv; ratio, block_size >= 1
  * Alignment: q, block_table, lists, attn_out 4 bytes; k_cache and v_cache
  * 8 bytes (IDX_ERR_INVALID_ARG otherwise). With 1, 2, 4 or 8 query heads per
- * kv head, hd <= 128 and k_cache 16-byte aligned the tiled kernel runs;
+ * kv head, hd <= 128 and both caches 16-byte aligned the tiled kernel runs;
  * otherwise the per-head kernel (same result up to rounding order).
  * Device-side errors: a token whose page index is past n_pages or whose page
  * is outside [0,P) is left out (IDX_STATUS_BAD_BLOCK in *dev_status).

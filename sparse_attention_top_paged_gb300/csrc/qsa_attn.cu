@@ -7,8 +7,8 @@
 // complete (others are skipped) and over the tail tokens
 // ((p + 1) / ratio) * ratio .. p, with K and V of kv head h / (nq / nkv) read
 // through the page table; attn_out[r][h] is the softmax-weighted sum of V.
-// With 1, 2, 4 or 8 query heads per kv head, hd <= 128 and a 16-byte aligned
-// K cache, one CTA per (row, kv head) serves the whole group over 32-token
+// With 1, 2, 4 or 8 query heads per kv head, hd <= 128 and 16-byte aligned
+// K and V caches, one CTA per (row, kv head) serves the whole group over 32-token
 // tiles (qsa_prefill_attn_tile_kernel: both contractions of a tile on the
 // tensor cores). Otherwise one CTA of 8 warps per (row, head),
 // the page's launch shape: each warp keeps an online-softmax partial
@@ -482,7 +482,8 @@ extern "C" idx_status_t idx_qsa_prefill_attn(const float *q, const uint16_t *k_c
     return IDX_ERR_INVALID_ARG;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint32_t G = nq / nkv;
-  if ((G == 1 || G == 2 || G == 4 || G == 8) && (hd == 64 || hd == 128) && aligned_to(k_cache, 16)) {
+  if ((G == 1 || G == 2 || G == 4 || G == 8) && (hd == 64 || hd == 128) && aligned_to(k_cache, 16) &&
+      aligned_to(v_cache, 16)) {   // both caches are staged by 16-byte asynchronous copies
     const dim3 tgrid(rows, nkv);
 #define IDX_ATTN_TILE(HD_, G_)                                                                                  \
   launch_tile<HD_, G_>(tgrid, s, q, k_cache, v_cache, block_table, n_pages, P, lists, attn_out, first_pos, topk, \

@@ -212,18 +212,26 @@ def test_qsa_prefill_attn(hd, nq, nkv):
     assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
 
 
-def test_qsa_prefill_attn_k_cache_8_byte_aligned():
-    """A K cache that starts 8 bytes past a 16-byte boundary (the per-head
-    kernel's 8-byte loads) gives the same attention."""
+def _at_8_past_16(bits):
+    """The cache as a device tensor starting 8 bytes past a 16-byte boundary."""
+    flat = torch.zeros(bits.size + 4, dtype=torch.int16, device="cuda")
+    flat[4:] = torch.from_numpy(bits.view(np.int16).reshape(-1)).cuda()
+    t = flat[4:].view(bits.shape)
+    assert t.data_ptr() % 16 == 8
+    return t
+
+
+@pytest.mark.parametrize("which", ["k", "v"])
+def test_qsa_prefill_attn_cache_8_byte_aligned(which):
+    """A K or V cache that starts 8 bytes past a 16-byte boundary (the
+    per-head kernel's 8-byte loads instead of the tiled kernel's 16-byte
+    copies) gives the same attention."""
     q, kb, vb, table, lists, fp, ratio = _attn_case(77, 128, 16, 2)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    kflat = torch.zeros(kb.size + 4, dtype=torch.int16, device="cuda")
-    kflat[4:] = torch.from_numpy(kb.view(np.int16).reshape(-1)).cuda()
-    kc = kflat[4:].view(kb.shape)
-    assert kc.data_ptr() % 16 == 8
-    got = _idx().qsa_prefill_attn(torch.from_numpy(q).cuda(), kc, torch.from_numpy(vb.view(np.int16)).cuda(),
-                                  torch.from_numpy(table).cuda(), torch.from_numpy(lists).cuda(), fp, ratio,
-                                  dev_status=st)
+    kc = _at_8_past_16(kb) if which == "k" else torch.from_numpy(kb.view(np.int16)).cuda()
+    vc = _at_8_past_16(vb) if which == "v" else torch.from_numpy(vb.view(np.int16)).cuda()
+    got = _idx().qsa_prefill_attn(torch.from_numpy(q).cuda(), kc, vc, torch.from_numpy(table).cuda(),
+                                  torch.from_numpy(lists).cuda(), fp, ratio, dev_status=st)
     ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
                                        1.0 / math.sqrt(128))
     assert int(st.item()) == ost == 0
