@@ -450,9 +450,9 @@ cudaError_t launch_tile(dim3 grid, cudaStream_t s, const float *q, const uint16_
                         uint32_t first_pos, uint32_t topk, uint32_t ratio, uint32_t block_size, uint32_t nq,
                         uint32_t nkv, float inv_sqrt_d, int32_t *dev_status) {
   constexpr size_t bytes = tile_smem_bytes<HD, G>();
-  static const cudaError_t attr = cudaFuncSetAttribute(qsa_prefill_attn_tile_kernel<HD, G>,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       static_cast<int>(bytes));
+  // set on every call: the attribute belongs to the current device's context
+  const cudaError_t attr = cudaFuncSetAttribute(qsa_prefill_attn_tile_kernel<HD, G>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (attr != cudaSuccess) return attr;
   qsa_prefill_attn_tile_kernel<HD, G><<<grid, kAttnWarps * 32, bytes, s>>>(
       q, kc, vc, table, n_pages, P, lists, out, first_pos, topk, ratio, block_size, nq, nkv, inv_sqrt_d, dev_status);
