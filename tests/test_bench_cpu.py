@@ -66,3 +66,27 @@ def test_warmup_below_three_is_refused():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
                           "--warmup", "2"], capture_output=True, text=True, timeout=120, cwd=ROOT)
     assert out.returncode != 0 and "warmup" in out.stderr
+
+
+def test_gather_split_case_matches_its_recipe():
+    c = bench.gather_split_case(1006)
+    assert c["codes"].shape == (c["P"], c["bs"], c["nd"]) and c["P"] * c["bs"] == c["n_tok"]
+    assert not (((c["codes"] & 0x7F) == 0x7F).any())          # no E4M3 NaN code
+    assert c["sel"].shape == (c["T"], c["n"])
+    for row in c["sel"]:
+        assert (row[1:] > row[:-1]).all() and row[0] >= 0 and row[-1] < c["n_tok"]   # sorted, distinct
+    for perm in c["table"]:
+        assert sorted(perm.tolist()) == list(range(c["P"]))
+    assert (c["scale"] >= 0.01).all() and (c["scale"] < 4.0).all()
+
+
+def test_qsa_attn_case_token_count_is_its_definition():
+    c = bench.qsa_attn_case(7, rows=9, first_pos=100, nq=4, nkv=2, hd=64, ratio=16, bs=16, topk=4)
+    want = 0
+    for r in range(c["rows"]):
+        p = c["first_pos"] + r
+        ncomp = (p + 1) // c["ratio"]
+        blocks = c["lists"][r]
+        assert len(set(blocks.tolist())) == len(blocks) and (blocks >= 0).all() and (blocks < ncomp).all()
+        want += len(blocks) * c["ratio"] + (p + 1 - ncomp * c["ratio"])
+    assert c["tokens"] == want
