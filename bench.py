@@ -223,23 +223,50 @@ def _set_threads(threads: int):
 
 
 def _oracle_sample(args):
-    """Runs in a spawned process: the float64 oracle on the first n queries."""
-    name, seed, n_queries, threads = args
-    _set_threads(threads)
+    """Runs in a spawned process: the float64 oracle, one thread, on the first
+    n queries."""
+    name, seed, n_queries = args
+    _set_threads(1)
     W = make_workload(name, seed)
     n = min(n_queries, W.T)
     return _oracle_run(W, range(n)) + (n,)
 
 
+def _oracle_worker(name, seed, rows, barrier, out):
+    """Runs in a spawned process: the float64 oracle, one thread, on ``rows``
+    of the workload, started together with the other workers."""
+    _set_threads(1)
+    W = make_workload(name, seed)
+    barrier.wait()
+    t0 = time.perf_counter()
+    pairs, _ = _oracle_run(W, rows)
+    out.put((pairs, t0, time.perf_counter()))
+
+
 def cpu_baseline(name: str, seed: int, n_queries: int):
+    """The float64 oracle on the first n_queries queries of the workload:
+    once on one thread, and once with one single-threaded process per host
+    core, the queries dealt out between them (the reported value)."""
     import multiprocessing as mp
     cores = len(os.sched_getaffinity(0))
     ctx = mp.get_context("spawn")
     with ctx.Pool(1) as pool:
-        pairs, dt, n = pool.apply(_oracle_sample, ((name, seed, n_queries, cores),))
-    return {"value": pairs / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"first {n} of the {name} queries ({pairs} pairs), numpy float64, "
-                      f"{dt:.2f} s", "seconds": dt}
+        pairs1, dt1, n = pool.apply(_oracle_sample, ((name, seed, n_queries),))
+    procs = max(1, min(cores, n))
+    barrier, out = ctx.Barrier(procs), ctx.Queue()
+    workers = [ctx.Process(target=_oracle_worker, args=(name, seed, list(range(n))[i::procs], barrier, out))
+               for i in range(procs)]
+    for wkr in workers:
+        wkr.start()
+    res = [out.get() for _ in workers]
+    for wkr in workers:
+        wkr.join()
+    pairs = sum(r[0] for r in res)
+    dt = max(r[2] for r in res) - min(r[1] for r in res)
+    return {"value": pairs / dt, "unit": UNIT, "cores": procs, "kind": "oracle",
+            "sample": f"first {n} of the {name} queries ({pairs} pairs), numpy float64, one single-threaded "
+                      f"process per core ({procs}), {dt:.2f} s",
+            "seconds": dt, "single_thread_value": pairs1 / dt1, "single_thread_seconds": dt1}
 
 
 REFERENCE_BUDGET_S = 120.0
@@ -642,6 +669,8 @@ def main():
                     choices=sorted(WORKLOADS) + ["qsa", "qsa_attn", "gather_split"])
     ap.add_argument("--cpu-queries", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="batched_decode only: skip the long-decode and prefill sub-records")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -661,7 +690,7 @@ def main():
     import torch
     import sparse_attention_top_paged_gb300 as idx
 
-    # the CPU baseline runs in a spawned process before any GPU work
+    # the CPU baseline runs in spawned processes before any GPU work
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload, rank_seed(args.workload, 0), args.cpu_queries)
@@ -671,9 +700,56 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     W = make_workload(args.workload, rank_seed(args.workload, rank))
-    dev = torch.device("cuda", local)
+    rec = measure_score(W, args, args.steps, dev, flush, dist, e2e=True)
+    extra = {}
+    if args.workload == "batched_decode" and not args.no_extra_workloads:
+        # the other two full-size configurations, device-timed, same warm-up,
+        # at most EXTRA_STEPS timed steps each
+        del W
+        for name in ("long_decode", "prefill"):
+            W2 = make_workload(name, rank_seed(name, rank))
+            r2 = measure_score(W2, args, min(args.steps, EXTRA_STEPS), dev, flush, dist, e2e=False)
+            extra[name] = {"metric": METRIC, "value": r2["value"], "unit": UNIT, "steps": r2["steps"],
+                           "ms_per_step": r2["ms_per_step"], "config": workload_config(W2),
+                           "roofline": r2["roofline"], "clocks": r2["clocks"]}
+            del W2
+            torch.cuda.empty_cache()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": rec["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": rec["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": dict(rec["config"], parallelism=f"replicas x{world} (independent batches)",
+                           mma="tcgen05 kind::f16, f16 x f16 -> f32 (exact for NVFP4 x bf16-valued q)"),
+            "e2e": rec["e2e"],
+            "gpu_launches": rec["gpu_launches"],
+            "roofline": rec["roofline"],
+            "cpu_baseline": cpu,
+            "clocks": rec["clocks"],
+            "wall_s": rec["wall_s"],
+        }
+        if extra:
+            line["workloads"] = extra
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+EXTRA_STEPS = 2000
+
+
+def measure_score(W, args, K, dev, flush, dist, e2e):
+    """Device-timed idx_score_topk steps over W (L2 flushed before each), and
+    optionally the end-to-end leg through the public Python call."""
+    import ctypes
+    import numpy as np
+    import torch
+    import sparse_attention_top_paged_gb300 as idx
     q = torch.from_numpy(W.q).to(dev)
     w = torch.from_numpy(W.w).to(dev)
     bt = torch.from_numpy(W.block_table).to(dev)
@@ -685,7 +761,6 @@ def main():
     out_i = torch.empty((W.T, k), dtype=torch.int32, device=dev)
     out_s = torch.empty((W.T, k), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     lib = idx.load_library()
     stream = torch.cuda.current_stream(dev)
 
@@ -694,9 +769,8 @@ def main():
                             key_gscale=gs, topk_idx=out_i, topk_score=out_s, dev_status=status,
                             path=args.path)
     ws_bytes = idx.score_topk_workspace_bytes(a)
-    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
-    import ctypes
     sptr = ctypes.c_void_p(stream.cuda_stream)
 
     def step(events=None):
@@ -717,7 +791,6 @@ def main():
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
 
-    K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     # The scoring kernel is bracketed by events on every KSAMPLE-th timed step:
     # an event recorded between the scorer and the selection kernel stops the
@@ -733,7 +806,7 @@ def main():
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(dev.index) as clk:
         wall0 = time.perf_counter()
         for i in range(K):
             flush.zero_()
@@ -744,17 +817,27 @@ def main():
         wall = time.perf_counter() - wall0
     if dist:
         dist.barrier()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
     step_ms = [s.elapsed_time(e) for s, e in ev]
     kern_ms = [s.elapsed_time(e) for s, e in kev]
     pairs_step = W.pairs
     value, t_total = whole_job(pairs_step, K, sum(step_ms) / 1e3, dist, dev)
+    kern_s = statistics.mean(kern_ms) / 1e3
+    rec = {"value": value, "steps": K, "ms_per_step": 1e3 * t_total / K, "config": workload_config(W),
+           "roofline": dict(roofline(W, kern_s), kernel_ms=1e3 * kern_s, kernel_timed_steps=len(kern_ms)),
+           "clocks": clk.summary(), "wall_s": wall, "gpu_launches": launches_per_step(W) * K}
+    if not e2e:
+        return rec
 
     # ---- end to end through the public Python API with host buffers ----
     # The step's inputs travel as one pinned host block into one device block
     # (q, w, block table, lengths at 256-byte-aligned offsets) and both
-    # outputs come back as one block: one copy each way.
-    import numpy as np
-
+    # outputs come back as one block: one copy each way. Each step is timed
+    # on the host, from the first host-side call to the return of a
+    # synchronize after the copy out (what a caller waits for), once the L2
+    # flush before it has finished; the CUDA-event span of the same steps is
+    # reported beside it.
     def packed(parts):
         offs, total = [], 0
         for x in parts:
@@ -787,41 +870,27 @@ def main():
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_ms = []
+    host_s, dev_ms = [], []
     for _ in range(E):
         flush.zero_()
+        torch.cuda.synchronize()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
         s0.record(stream)
         e2e_step()
         s1.record(stream)
-        e2e_ms.append((s0, s1))
-    torch.cuda.synchronize()
-    e2e_value, _ = whole_job(pairs_step, E, sum(s.elapsed_time(e) for s, e in e2e_ms) / 1e3, dist, dev)
+        torch.cuda.synchronize()
+        host_s.append(time.perf_counter() - t0)
+        dev_ms.append(s0.elapsed_time(s1))
+    e2e_value, e2e_t = whole_job(pairs_step, E, sum(host_s), dist, dev)
+    e2e_dev, _ = whole_job(pairs_step, E, sum(dev_ms) / 1e3, dist, dev)
     # the host copy holds what the device-timed steps produced
     if not torch.equal(h_out[:W.T * k * 4].view(torch.int32).view(W.T, k), out_i.cpu()):
         raise RuntimeError("end-to-end top-k differs from the device-timed steps")
-
-    kern_s = statistics.mean(kern_ms) / 1e3
-    roof = roofline(W, kern_s)
-
-    if rank == 0:
-        clocks = clk.summary()
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": args.warmup, "ms_per_step": 1e3 * t_total / K, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-            "config": dict(workload_config(W), parallelism=f"replicas x{world} (independent batches)",
-                           mma="tcgen05 kind::f16, f16 x f16 -> f32 (exact for NVFP4 x bf16-valued q)"),
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step(W) * K,
-            "roofline": dict(roof, kernel_ms=1e3 * kern_s, kernel_timed_steps=len(kern_ms)),
-            "cpu_baseline": cpu,
-            "clocks": clocks,
-            "wall_s": wall,
-        }
-        print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
+    rec["e2e"] = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                  "ms_per_step": 1e3 * e2e_t / E, "timing": "host perf_counter around issue + copies + synchronize",
+                  "device_value": e2e_dev, "device_ms_per_step": statistics.mean(dev_ms), "steps": E}
+    return rec
 
 
 if __name__ == "__main__":

@@ -94,9 +94,11 @@ typedef enum { IDX_PATH_AUTO = 0, IDX_PATH_TENSOR = 1, IDX_PATH_SIMT = 2 } idx_p
  *              an out-of-range block; ld_scores >= max_logical_blocks * epb
  *   dev_status optional device int32 (IDX_STATUS_* bits ORed in)
  *   workspace  device scratch of at least idx_score_topk_workspace_size()
- *              bytes, 256-byte aligned. It must be zero-filled before its
- *              first use; every call leaves it ready for the next one.
- *              Calls that share a workspace must not overlap in time.
+ *              bytes, 256-byte aligned. It needs no initialisation: every
+ *              call writes each scratch word before it reads it (the q
+ *              preparation kernel zeroes the key histograms and the
+ *              selection's candidate counters). Calls that share a
+ *              workspace must not overlap in time.
  *   path       idx_path_t
  *   num_ctas   CTAs of the persistent score kernel; 0 = one per SM
  *   timing_events optional pair of cudaEvent_t (as void*): when both are

@@ -59,13 +59,13 @@ def _raise(where, code):
 
 
 def _workspace(device, nbytes):
-    """A zero-filled workspace of at least ``nbytes`` on ``device``, reused
-    across calls (the library leaves it ready for the next call)."""
+    """A workspace of at least ``nbytes`` on ``device``, reused across calls
+    (the library needs no initialised contents)."""
     torch = _torch()
     key = (str(device),)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
 

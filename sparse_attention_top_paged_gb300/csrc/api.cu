@@ -168,6 +168,9 @@ idx_status_t idx_score_topk(const idx_score_topk_args *args, idx_stream_t stream
   else
     e = launch_score_tc(r.p, r.num_ctas, static_cast<unsigned char *>(args->workspace) + r.qrec_off,
                         reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(args->workspace) + r.hist_off),
+                        r.sel.chunks > 0
+                            ? reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(args->workspace) + r.sel.cnt_off)
+                            : nullptr,
                         scores, r.sel.ld, s);
   if (e == cudaSuccess && timed) e = cudaEventRecord(ev1, s);
   const uint32_t *hist = r.plan == Plan::kTensor

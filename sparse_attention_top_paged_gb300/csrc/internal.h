@@ -63,10 +63,11 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
 bool score_tc_supported(const ScoreParams &p);
 size_t score_tc_workspace(const ScoreParams &p);  // per-query q records (bytes)
 // Also fills hist[t][d] (kScoreBins per query) with the number of valid keys
-// of query t whose selection key has top 12 bits d.
+// of query t whose selection key has top 12 bits d, and zeroes cand_cnt[t]
+// (the split collection's candidate counters) when cand_cnt is given.
 constexpr int kScoreBins = 4096;
-cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint32_t *hist, float *scores,
-                            long long ld, cudaStream_t stream);
+cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint32_t *hist, uint32_t *cand_cnt,
+                            float *scores, long long ld, cudaStream_t stream);
 // gather_pool.cu
 cudaError_t launch_gather_kv(const idx_gather_kv_args &a, cudaStream_t stream);
 cudaError_t launch_block_pool(const uint16_t *raw, const float *w, float *out, uint32_t first_block,

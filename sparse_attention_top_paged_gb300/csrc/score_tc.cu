@@ -11,7 +11,9 @@
 // qprep_kernel turns each q[t] into the MMA's B operand once, as a record in
 // global memory: per head a power-of-two scale 2^sigma, f16 hi and lo parts
 // (the lo part only feeds the MMA when some q value is not exact in f16, e.g.
-// bf16-valued q never needs it), w' = w 2^-sigma and the lo flags.
+// bf16-valued q never needs it), w' = w 2^-sigma and the lo flags. It also
+// zeroes the per-query key histograms (and the selection's candidate
+// counters), so the workspace needs no initialisation.
 //
 // score_tc_kernel is a persistent, warp-specialised pipeline:
 //   work     The tiles of 128 consecutive keys of every query, laid end to end,
@@ -176,12 +178,13 @@ __device__ long long block_incl_scan(long long v, long long *scratch, long long 
 // split into f16 hi + lo (lo = 0 whenever q is exact in f16 after scaling,
 // e.g. for bf16-valued q) and w' = w 2^-sigma undoes the scale after the ReLU.
 __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay, uint8_t *__restrict__ rec,
-                                                    uint32_t *__restrict__ hist) {
+                                                    uint32_t *__restrict__ hist, uint32_t *__restrict__ cand_cnt) {
   ptx::launch_dependents();  // the scorer may start its prologue meanwhile
   const int t = blockIdx.x;
-  {  // the blocks of query t zero its key histogram between them
+  {  // the blocks of query t zero its key histogram between them (and its candidate counter, when given)
     uint32_t *hz = hist + static_cast<size_t>(t) * kScoreBins;
     for (int i = blockIdx.y * blockDim.x + threadIdx.x; i < kScoreBins; i += gridDim.y * blockDim.x) hz[i] = 0u;
+    if (cand_cnt != nullptr && blockIdx.y == 0 && threadIdx.x == 0) cand_cnt[t] = 0u;
   }
   const int h = blockIdx.y * 8 + static_cast<int>(threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -781,8 +784,8 @@ size_t score_tc_workspace(const ScoreParams &p) {
   return static_cast<size_t>(p.T) * lay.rec_bytes;
 }
 
-cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint32_t *hist, float *scores,
-                            long long ld, cudaStream_t stream) {
+cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint32_t *hist, uint32_t *cand_cnt,
+                            float *scores, long long ld, cudaStream_t stream) {
   TcLayout lay;
   if (!make_layout(p, &lay)) return cudaErrorNotSupported;
   auto encode = get_encode();
@@ -800,7 +803,8 @@ cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint
                                        static_cast<int>(lay.smem_bytes));
   if (e != cudaSuccess) return e;
   uint8_t *rec = static_cast<uint8_t *>(qrec);
-  qprep_kernel<<<dim3(static_cast<unsigned>(p.T), static_cast<unsigned>(lay.Npad / 8)), 256, 0, stream>>>(p, lay, rec, hist);
+  qprep_kernel<<<dim3(static_cast<unsigned>(p.T), static_cast<unsigned>(lay.Npad / 8)), 256, 0, stream>>>(p, lay, rec, hist,
+                                                                                                          cand_cnt);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // The scorer may launch while qprep_kernel runs: its producer waits for the
   // records (griddepcontrol.wait) only before the first record copy.

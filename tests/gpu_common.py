@@ -53,6 +53,30 @@ def oracle_rows(W, rows=None):
                                   W.epb, rows=rows, **W.oracle_kwargs())
 
 
+def _oracle_rows_job(args):
+    """Runs in a spawned process: the oracle's score rows of one named
+    workload (rebuilt from its seed) for the given query rows."""
+    name, seed, rows = args
+    from sparse_attention_top_paged_gb300 import workloads as wl
+    W = getattr(wl, name)(seed)
+    return oracle_rows(W, rows)[0]
+
+
+def oracle_rows_parallel(name, seed, rows, procs=None):
+    """``oracle_rows`` of the named workload for many rows, split over spawned
+    processes (each rebuilds the workload from its seed)."""
+    import multiprocessing as mp
+    import os
+    rows = list(rows)
+    procs = procs or max(1, min(8, len(rows), len(os.sched_getaffinity(0))))
+    chunks = [rows[i::procs] for i in range(procs) if rows[i::procs]]
+    out = {}
+    with mp.get_context("spawn").Pool(len(chunks)) as pool:
+        for part in pool.map(_oracle_rows_job, [(name, seed, c) for c in chunks]):
+            out.update(part)
+    return out
+
+
 def check_against_oracle(W, gi, gs, ref_rows, so=None, label=""):
     for t, I in ref_rows.items():
         check_query(I, gi[t], gs[t], W.top_k, where=f"{label} query {t}")

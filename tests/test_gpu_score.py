@@ -13,7 +13,8 @@ import pytest
 
 import oracle
 from sparse_attention_top_paged_gb300 import workloads as wl
-from tests.gpu_common import check_against_oracle, ensure_built, oracle_rows, run_gpu, to_device
+from tests.gpu_common import (check_against_oracle, ensure_built, oracle_rows, oracle_rows_parallel, run_gpu,
+                              to_device)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -221,29 +222,75 @@ def test_f32_keys_qsa_scores():
 
 @pytest.mark.parametrize("path", ["tensor", "simt"])
 def test_batched_decode_full(path):
+    """Every one of the 64 queries of the benchmark's batch."""
     W = wl.batched_decode()
     gi, gs, st, _ = run_gpu(W, path)
     assert st == 0
-    sample = list(range(0, 64, 4))
-    rows, _ = oracle_rows(W, rows=sample)
+    rows, _ = oracle_rows(W)
     check_against_oracle(W, gi, gs, rows, None, f"batched/{path}")
 
 
 def test_long_decode_full():
+    """Every one of the 16 queries of 262,144 keys (the oracle runs in
+    parallel processes)."""
     W = wl.long_decode()
     gi, gs, st, _ = run_gpu(W, "auto")
     assert st == 0
-    rows, _ = oracle_rows(W, rows=[0, 15])
+    rows = oracle_rows_parallel("long_decode", W.meta["seed"], range(W.T))
     check_against_oracle(W, gi, gs, rows, None, "long")
+
+
+def prefill_sample_rows(T=4096, seed=3):
+    """The first and last 64 rows of the prefill batch and 128 seeded rows
+    between them."""
+    rng = np.random.default_rng(seed)
+    middle = rng.choice(np.arange(64, T - 64), size=128, replace=False)
+    return sorted(set(range(64)) | set(range(T - 64, T)) | set(int(x) for x in middle))
 
 
 def test_prefill_full():
     W = wl.prefill()
     gi, gs, st, _ = run_gpu(W, "auto")
     assert st == 0
-    sample = [0, 1, 2, 1000, 2047, 3000, 4094, 4095]
+    sample = prefill_sample_rows(W.T)
+    assert len(sample) == 256
     rows, _ = oracle_rows(W, rows=sample)
     check_against_oracle(W, gi, gs, rows, None, "prefill")
+
+
+def _garbage(ws, seed):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    ws.copy_(torch.randint(0, 256, (ws.numel(),), dtype=torch.uint8, generator=g))
+
+
+@pytest.mark.parametrize("case", ["batched", "split"])
+def test_workspace_needs_no_initialisation(case):
+    """The workspace may hold anything before a call: every call writes each
+    scratch word before reading it (score rows, q records, histograms and
+    the split collection's candidate counters). Two calls in a row, each on a
+    freshly garbage-filled workspace."""
+    import sparse_attention_top_paged_gb300 as idx
+    if case == "batched":
+        W = _small(51, T=8, lo=3000, hi=9000, k=256, max_lb=150, P=1300)
+    else:   # few rows of 64K+ keys: the selection's split collection runs
+        W = _long_rows(52, T=3, lo=65536, hi=80000, k=512, P=3800)
+    d = to_device(W)
+    out = (torch.empty((W.T, W.top_k), dtype=torch.int32, device="cuda"),
+           torch.empty((W.T, W.top_k), dtype=torch.float32, device="cuda"))
+    a = idx.make_score_args(d["q"], d["w"], d["bt"], d["vl"], W.top_k, entries_per_block=W.epb,
+                            keys_fp4=d["keys_fp4"], key_scale=d["key_scale"], key_gscale=d["key_gscale"],
+                            bt_stride=W.bt_stride, topk_idx=out[0], topk_score=out[1], path="tensor")
+    ws = torch.empty(idx.score_topk_workspace_bytes(a), dtype=torch.uint8, device="cuda")
+    rows, _ = oracle_rows(W)
+    for rep in range(2):
+        _garbage(ws, 100 + rep)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        gi, gs = idx.score_topk(d["q"], d["w"], d["bt"], d["vl"], W.top_k, entries_per_block=W.epb,
+                                bt_stride=W.bt_stride, keys_fp4=d["keys_fp4"], key_scale=d["key_scale"],
+                                key_gscale=d["key_gscale"], dev_status=st, path="tensor", workspace=ws, out=out)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        check_against_oracle(W, gi.cpu().numpy(), gs.cpu().numpy(), rows, None, f"garbage-ws/{case}/{rep}")
 
 
 def test_tensor_more_ctas_than_tiles():

@@ -5,9 +5,10 @@ runtime that owns all device memory and gives it no allocator, or a serving
 loop that must not allocate once running). idx_score_topk_static serves them
 with a scratch array built into the library instead of a caller workspace.
 Here it must return what idx_score_topk returns with a caller-provided
-workspace on the same inputs, on two calls in a row (the second call finds the
-first call's leftovers in the shared array), and must refuse, without
-launching, arguments that need more scratch than the array holds.
+workspace on the same inputs, and what the float64 oracle computes, on two
+calls in a row (the second call finds the first call's leftovers in the shared
+array), and must refuse, without launching, arguments that need more scratch
+than the array holds.
 """
 
 import ctypes
@@ -16,7 +17,7 @@ import numpy as np
 import pytest
 
 from sparse_attention_top_paged_gb300 import workloads as wl
-from tests.gpu_common import ensure_built, run_gpu, to_device
+from tests.gpu_common import check_against_oracle, ensure_built, oracle_rows, run_gpu, to_device
 from tests.parity import REL_TOL
 
 torch = pytest.importorskip("torch")
@@ -73,16 +74,20 @@ def test_static_scratch_matches_workspace_entry_point(lib):
     d = to_device(W)
     ref_i, ref_s, ref_st, _ = run_gpu(W, "auto", dev=d)   # idx_score_topk with a workspace
     assert ref_st == 0
-    for _ in range(2):
+    rows, _ = oracle_rows(W)
+    for call in range(2):
         gi, gs, st = _call_static(lib, W, d)
         assert st == 0
         _assert_same(ref_i, ref_s, gi, gs)
+        check_against_oracle(W, gi, gs, rows, None, f"static/{call}")
     # a different problem next: nothing of the previous call may leak into it
     W2 = _workload(22)
     d2 = to_device(W2)
     ref2 = run_gpu(W2, "auto", dev=d2)
     gi, gs, st = _call_static(lib, W2, d2)
     _assert_same(ref2[0], ref2[1], gi, gs)
+    rows2, _ = oracle_rows(W2)
+    check_against_oracle(W2, gi, gs, rows2, None, "static/next")
 
 
 def test_static_scratch_rejects_oversized_arguments(lib):
