@@ -8,17 +8,20 @@
 // a locked shared heap; here two kernels run back to back (the second may
 // start before the first ends):
 //
-// qprep_kernel turns each q[t] into the MMA's B operand once, as a record in
-// global memory: per head a power-of-two scale 2^sigma, f16 hi and lo parts
-// (the lo part only feeds the MMA when some q value is not exact in f16, e.g.
+// qprep_kernel turns q into the MMA's B operand once, as records in global
+// memory. A record serves a "row group" of R query rows: R = 2 when every row
+// reads the same block table (one sequence, many rows), so one decoded key
+// tile feeds both rows' dot products in a single MMA of N = 2 Npad; else R = 1.
+// Per head row: a power-of-two scale 2^sigma, f16 hi and lo parts (the lo
+// part only feeds the MMA when some q value is not exact in f16, e.g.
 // bf16-valued q never needs it), w' = w 2^-sigma and the lo flags. It also
 // zeroes the per-query key histograms (and the selection's candidate
 // counters), so the workspace needs no initialisation.
 //
 // score_tc_kernel is a persistent, warp-specialised pipeline:
-//   work     The tiles of 128 consecutive keys of every query, laid end to end,
-//            are split evenly over the CTAs (one per SM). A "segment" is a
-//            CTA's run of tiles of one query (it shares one B operand).
+//   work     The tiles of 128 consecutive keys of every row group, laid end to
+//            end, are split evenly over the CTAs (one per SM). A "segment" is
+//            a CTA's run of tiles of one row group (it shares one B operand).
 //   warp 18  resolver: looks up block-table entries and per-block global
 //            scales 32 blocks at a time (one per lane) into a ring of per-tile
 //            records, so no dependent global load sits on the copy path.
@@ -30,11 +33,12 @@
 //   warps 2-5 decoders: one thread per key row decodes 128 elements
 //            e2m1 * e4m3 exactly into f16 (hardware converts) and stores them
 //            to tensor memory as the MMA's A operand.
-//   warp 1   MMA issuer: D[128 keys x Npad heads] = A * B^T in f32, K = 128, as
+//   warp 1   MMA issuer: D[128 keys x R Npad heads] = A * B^T in f32, K = 128, as
 //            8 (or 16 with the lo part) tcgen05.mma kind::f16 steps.
 //   warps 6-17 epilogue, three groups of four taking tiles in turn: one
 //            thread per key reads its accumulator row (32 columns at a
-//            time) from tensor memory and forms I = g * sum_h (w_h 2^-sigma_h) relu(acc_h)
+//            time) from tensor memory and forms, per row of the group,
+//            I = g * sum_h (w_h 2^-sigma_h) relu(acc_h)
 //            (the per-block global scale g is factored out, so relu(g a) = g
 //            relu(a) for g > 0 and g min(a,0) for g < 0), then stores I to the
 //            score matrix (coalesced: a warp writes 32 consecutive keys). The
@@ -79,18 +83,20 @@ struct MetaEntry {
   int lb0;        // first logical block of the tile
   int s0;         // first key of the tile
   int nblk;       // blocks the tile touches (up to its last valid key)
-  int t;          // the tile's query
+  int t;          // the tile's row group
   int seg;        // first tile of the CTA's segment number seg - 1; 0: not a segment start
-  int pad_[10];
+  int len[2];     // keys of each row of the group (0: no such row, or a bad length)
+  int pad_[8];
 };
 static_assert(sizeof(MetaEntry) == 128, "meta entry");
 
-// Per-query B-operand record, written by qprep_kernel to global memory and
+// Per-row-group B-operand record, written by qprep_kernel to global memory and
 // copied verbatim into a shared-memory segment slot: f16 hi rows, f16 lo rows
-// (each Npad heads x 128 dims, K-major, 128-byte swizzled), w' (Npad floats),
-// lo flags (Npad ints).
+// (each NR = R Npad head rows x 128 dims, K-major, 128-byte swizzled), w' (NR
+// floats), lo flags (NR ints). Head row n holds head n % Npad of row
+// R * group + n / Npad.
 struct TcLayout {
-  int Npad, nseg, na, nd, ns, box_rows, bpt, epb_shift;
+  int Npad, R, NR, nq, nseg, na, nd, ne, ns, box_rows, bpt, epb_shift;
   uint32_t b_bytes, rec_w, rec_flags, rec_bytes, rec_smem;
   uint32_t off_b, off_raw, off_meta, off_bar, off_misc;
   uint32_t smem_bytes;
@@ -109,26 +115,36 @@ constexpr uint32_t kMiscBytes = 8 * 4 + (kThreads / 32) * 8;
 
 __host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-__device__ __forceinline__ int ntiles_of(const ScoreParams &p, int t) {
+// Keys of row t, or 0 for a length outside [0, max_lb * epb] (such a row is
+// padded by the selection and reported there).
+__device__ __forceinline__ int row_len(const ScoreParams &p, int t) {
   const int L = p.valid_lens[t];
-  if (L <= 0 || static_cast<long long>(L) > static_cast<long long>(p.max_lb) * p.epb) return 0;
+  return (L <= 0 || static_cast<long long>(L) > static_cast<long long>(p.max_lb) * p.epb) ? 0 : L;
+}
+
+// Tiles of row group tq (kRows rows): its longest valid row, in 128-key tiles.
+template <int kRows>
+__device__ __forceinline__ int ntiles_of(const ScoreParams &p, int tq) {
+  int L = row_len(p, tq * kRows);
+  if (kRows > 1 && tq * kRows + 1 < p.T) L = max(L, row_len(p, tq * kRows + 1));
   return (L + kTileKeys - 1) / kTileKeys;
 }
 
 // Deterministic walk over a CTA's tiles; every role runs its own copy.
+template <int kRows>
 struct Walker {
-  int t, j, nt;
-  __device__ void init(const ScoreParams &p, int t0, int j0) {
+  int t, j, nt;   // row group, tile within it, its tile count
+  __device__ void init(const ScoreParams &p, const TcLayout &lay, int t0, int j0) {
     t = t0;
     j = j0;
-    nt = (t0 < p.T) ? ntiles_of(p, t0) : 0;
+    nt = (t0 < lay.nq) ? ntiles_of<kRows>(p, t0) : 0;
   }
-  __device__ void next(const ScoreParams &p) {
+  __device__ void next(const ScoreParams &p, const TcLayout &lay) {
     if (++j == nt) {
       j = 0;
       do {
         ++t;
-      } while (t < p.T && (nt = ntiles_of(p, t)) == 0);
+      } while (t < lay.nq && (nt = ntiles_of<kRows>(p, t)) == 0);
     }
   }
 };
@@ -171,28 +187,35 @@ __device__ long long block_incl_scan(long long v, long long *scratch, long long 
   return before + x;
 }
 
-// q[t] -> the B-operand record of query t: one warp per head, 4 dims per lane.
-// Per head a power-of-two scale 2^sigma puts the largest |q| in [2^14, 2^15)
-// (sigma from the exponent field; subnormal or zero heads keep sigma 0;
-// clamped so 2^sigma and 2^-sigma are normal floats); the scaled values are
-// split into f16 hi + lo (lo = 0 whenever q is exact in f16 after scaling,
-// e.g. for bf16-valued q) and w' = w 2^-sigma undoes the scale after the ReLU.
+// q -> the B-operand record of row group tq: block (tq, y) prepares head rows
+// 8y .. 8y+7, one warp per head row, 4 dims per lane (head rows of absent
+// rows or heads are zero). Per head a power-of-two scale 2^sigma puts the
+// largest |q| in [2^14, 2^15) (sigma from the exponent field; subnormal or
+// zero heads keep sigma 0; clamped so 2^sigma and 2^-sigma are normal
+// floats); the scaled values are split into f16 hi + lo (lo = 0 whenever q is
+// exact in f16 after scaling, e.g. for bf16-valued q) and w' = w 2^-sigma
+// undoes the scale after the ReLU.
 __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay, uint8_t *__restrict__ rec,
                                                     uint32_t *__restrict__ hist, uint32_t *__restrict__ cand_cnt) {
   ptx::launch_dependents();  // the scorer may start its prologue meanwhile
-  const int t = blockIdx.x;
-  {  // the blocks of query t zero its key histogram between them (and its candidate counter, when given)
+  const int tq = blockIdx.x;
+  for (int rr = 0; rr < lay.R; ++rr) {
+    // the blocks of the group zero its rows' key histograms between them
+    // (and their candidate counters, when given)
+    const int t = tq * lay.R + rr;
+    if (t >= p.T) break;
     uint32_t *hz = hist + static_cast<size_t>(t) * kScoreBins;
     for (int i = blockIdx.y * blockDim.x + threadIdx.x; i < kScoreBins; i += gridDim.y * blockDim.x) hz[i] = 0u;
     if (cand_cnt != nullptr && blockIdx.y == 0 && threadIdx.x == 0) cand_cnt[t] = 0u;
   }
-  const int h = blockIdx.y * 8 + static_cast<int>(threadIdx.x >> 5);
+  const int n = blockIdx.y * 8 + static_cast<int>(threadIdx.x >> 5);   // head row of the record
   const int lane = threadIdx.x & 31;
-  if (h >= lay.Npad) return;
-  uint8_t *r = rec + static_cast<size_t>(t) * lay.rec_bytes;
+  if (n >= lay.NR) return;
+  const int h = n % lay.Npad, t = tq * lay.R + n / lay.Npad;
+  uint8_t *r = rec + static_cast<size_t>(tq) * lay.rec_bytes;
   float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
   float wv = 0.0f;
-  if (h < p.H) {
+  if (h < p.H && t < p.T) {
     x = reinterpret_cast<const float4 *>(p.q + (static_cast<long long>(t) * p.H + h) * 128)[lane];
     wv = p.w[static_cast<long long>(t) * p.H + h];
   }
@@ -213,9 +236,9 @@ __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay,
     any_lo |= (__half2float(lo[e]) != 0.0f);
   }
   // dims 4*lane .. 4*lane+3: K block kb = lane / 16 (64 dims each), 16-byte
-  // chunk jj = (lane / 2) % 8 of the head's 128-byte row, swizzled by h % 8
+  // chunk jj = (lane / 2) % 8 of the head row's 128 bytes, swizzled by n % 8
   const int ch = lane >> 1, kb = ch >> 3, jj = ch & 7;
-  const uint32_t off = kb * (lay.Npad * 128) + h * 128 + ((jj ^ (h & 7)) * 16) + (lane & 1) * 8;
+  const uint32_t off = kb * (lay.NR * 128) + n * 128 + ((jj ^ (n & 7)) * 16) + (lane & 1) * 8;
   uint2 vh, vl;
   vh.x = static_cast<uint32_t>(__half_as_ushort(hi[0])) | (static_cast<uint32_t>(__half_as_ushort(hi[1])) << 16);
   vh.y = static_cast<uint32_t>(__half_as_ushort(hi[2])) | (static_cast<uint32_t>(__half_as_ushort(hi[3])) << 16);
@@ -225,11 +248,12 @@ __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay,
   *reinterpret_cast<uint2 *>(r + lay.b_bytes + off) = vl;
   const bool warp_lo = __any_sync(0xFFFFFFFFu, any_lo);
   if (lane == 0) {
-    reinterpret_cast<float *>(r + lay.rec_w)[h] = wv * down;
-    reinterpret_cast<int *>(r + lay.rec_flags)[h] = warp_lo ? 1 : 0;
+    reinterpret_cast<float *>(r + lay.rec_w)[n] = wv * down;
+    reinterpret_cast<int *>(r + lay.rec_flags)[n] = warp_lo ? 1 : 0;
   }
 }
 
+template <int kRows>
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmap_nib, ScoreParams p, TcLayout lay,
                     const uint8_t *__restrict__ qrec, uint32_t *__restrict__ hist, float *__restrict__ scores,
@@ -272,9 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   long long *scan = reinterpret_cast<long long *>(misc + M_SCAN);
   const long long G = gridDim.x, c = blockIdx.x;
   long long g0 = 0, g1 = 0;
-  if (p.T <= kThreads) {
-    // one query per thread: a single scan gives the total and each query's range
-    const long long v = (static_cast<int>(threadIdx.x) < p.T) ? ntiles_of(p, threadIdx.x) : 0;
+  if (lay.nq <= kThreads) {
+    // one row group per thread: a single scan gives the total and each group's range
+    const long long v = (static_cast<int>(threadIdx.x) < lay.nq) ? ntiles_of<kRows>(p, threadIdx.x) : 0;
     long long total;
     const long long incl = block_incl_scan(v, scan, &total);
     const long long qg = total / G, rg = total % G;
@@ -286,14 +310,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       misc[M_J0] = static_cast<int>(g0 - excl);
     }
     if (threadIdx.x == 0 && g0 >= total) {
-      misc[M_T0] = p.T;
+      misc[M_T0] = lay.nq;
       misc[M_J0] = 0;
     }
   } else {
     long long total = 0;
     {
       long long local = 0;
-      for (int t = threadIdx.x; t < p.T; t += kThreads) local += ntiles_of(p, t);
+      for (int t = threadIdx.x; t < lay.nq; t += kThreads) local += ntiles_of<kRows>(p, t);
       long long tot;
       block_incl_scan(local, scan, &tot);
       total = tot;
@@ -302,14 +326,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     g0 = c * qg + (c * rg) / G;
     g1 = (c + 1) * qg + ((c + 1) * rg) / G;
     if (threadIdx.x == 0) {
-      misc[M_T0] = p.T;
+      misc[M_T0] = lay.nq;
       misc[M_J0] = 0;
     }
     __syncthreads();
     long long base = 0;
-    for (int chunk = 0; chunk < p.T; chunk += kThreads) {
+    for (int chunk = 0; chunk < lay.nq; chunk += kThreads) {
       const int t = chunk + threadIdx.x;
-      const long long v = (t < p.T) ? ntiles_of(p, t) : 0;
+      const long long v = (t < lay.nq) ? ntiles_of<kRows>(p, t) : 0;
       long long tot;
       const long long incl = block_incl_scan(v, scan, &tot);
       const long long excl = incl - v;
@@ -326,13 +350,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = static_cast<uint32_t>(misc[M_TMEM]);
   const int t0 = misc[M_T0], j0 = misc[M_J0];
   const int n_tiles = (g0 < g1) ? static_cast<int>(g1 - g0) : 0;
-  const int Npad = lay.Npad, nseg = lay.nseg, na = lay.na, nd = lay.nd;
+  const int Npad = lay.Npad, NR = lay.NR, nseg = lay.nseg, na = lay.na, nd = lay.nd;
   const uint32_t b_bytes = lay.b_bytes;
   uint8_t *sB = sm + lay.off_b;
   uint8_t *sRaw = sm + lay.off_raw;
   MetaEntry *sMeta = reinterpret_cast<MetaEntry *>(sm + lay.off_meta);
   const uint32_t tmem_a = tmem;                                  // A slots: 64 columns each
-  const uint32_t tmem_d = tmem + 64u * static_cast<uint32_t>(na);  // D slots: Npad columns each
+  const uint32_t tmem_d = tmem + 64u * static_cast<uint32_t>(na);  // D slots: NR columns each
 
   if (warp == 0) {
     // ================================================================ producer
@@ -445,15 +469,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp walks the tiles in lockstep; one elected lane issues.
     // Descriptors are built once per segment so the issue loop is nothing
     // but tcgen05.mma instructions.
-    Walker w;
-    w.init(p, t0, j0);
-    const uint32_t idesc = ptx::idesc_f16_f32(128, Npad);
+    Walker<kRows> w;
+    w.init(p, lay, t0, j0);
+    const uint32_t idesc = ptx::idesc_f16_f32(128, NR);
     bool need_lo = false;
     uint64_t bdh[8], bdl[8];
     Ring ra, rd, rs;
     rs.idx = -1;  // advanced at each segment start
     int ss = 0;
-    for (int i = 0; i < n_tiles; ++i, w.next(p), ra.next(na), rd.next(nd)) {
+    for (int i = 0; i < n_tiles; ++i, w.next(p, lay), ra.next(na), rd.next(nd)) {
       const bool seg_start = (i == 0) || (w.j == 0);
       const bool seg_end = (i == n_tiles - 1) || (w.j == w.nt - 1);
       bool ok = true;
@@ -464,13 +488,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t *slot = sB + ss * lay.rec_smem;
         const int *flags = reinterpret_cast<const int *>(slot + lay.rec_flags);
         int f = 0;
-        for (int h = lane; h < Npad; h += 32) f |= flags[h];
+        for (int h = lane; h < NR; h += 32) f |= flags[h];
         need_lo = __any_sync(0xFFFFFFFFu, f != 0);
         const uint32_t bh = ptx::smem_addr(slot);
         const uint32_t bl = ptx::smem_addr(slot + b_bytes);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint32_t boff = (k >> 2) * (Npad * 128) + (k & 3) * 32;
+          const uint32_t boff = (k >> 2) * (NR * 128) + (k & 3) * 32;
           bdh[k] = ptx::sdesc_sw128(bh + boff);
           bdl[k] = ptx::sdesc_sw128(bl + boff);
         }
@@ -480,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = ok && ptx::mbar_wait(bar(B_EMPTY_D + d), rd.phase ^ 1u, abort_flag, kTimeoutNs);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       ptx::tc_fence_after();
-      const uint32_t dt = tmem_d + d * Npad, at = tmem_a + a * 64;
+      const uint32_t dt = tmem_d + d * NR, at = tmem_a + a * 64;
       if (ptx::elect_one()) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) ptx::mma_ts_f16(dt, at + 8 * k, bdh[k], idesc, k > 0 ? 1u : 0u);
@@ -547,19 +571,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bpt = lay.bpt;                 // blocks per full tile (epb a power of two)
     const int tpb = 32 / bpt;                // tiles per batch
     const int d = lane / bpt, b = lane % bpt;
-    Walker w;
-    w.init(p, t0, j0);
+    Walker<kRows> w;
+    w.init(p, lay, t0, j0);
     int seg_base = 0;  // segments started before this batch
     for (int base = 0; base < n_tiles; base += tpb) {
       const int i = base + d;
       const bool tile_ok = i < n_tiles;
-      Walker wl = w;
-      for (int x = 0; x < d && tile_ok; ++x) wl.next(p);
-      int L = 0, s0 = 0, lb0 = 0, nblk = 0, phys = -1;
+      Walker<kRows> wl = w;
+      for (int x = 0; x < d && tile_ok; ++x) wl.next(p, lay);
+      int L = 0, s0 = 0, lb0 = 0, nblk = 0, phys = -1, l0 = 0, l1 = 0;
       float g = 0.0f;
       bool blk_ok = false, pv = false;
       if (tile_ok) {
-        L = p.valid_lens[wl.t];
+        l0 = row_len(p, wl.t * kRows);
+        l1 = (kRows > 1 && wl.t * kRows + 1 < p.T) ? row_len(p, wl.t * kRows + 1) : 0;
+        L = max(l0, l1);
         s0 = wl.j * kTileKeys;
         const int s_end = min(s0 + kTileKeys, L);
         lb0 = s0 >> lay.epb_shift;
@@ -595,32 +621,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         m.nblk = nblk;
         m.t = wl.t;
         m.seg = starts ? ord + 1 : 0;
+        m.len[0] = l0;
+        m.len[1] = l1;
       }
       __syncwarp();
       if (tile_ok && b == 0) ptx::mbar_arrive(bar(B_META_FULL + r));
-      for (int x = 0; x < tpb; ++x) w.next(p);
+      for (int x = 0; x < tpb; ++x) w.next(p, lay);
     }
   } else {
     // ============================================================== epilogue
-    // kEpiGroups groups of four warps take tiles in turn (one group's tile
-    // takes longer than the MMA of one tile). Every warp still walks every
+    // lay.ne (at most kEpiGroups, at most one per D slot) groups of four
+    // warps take tiles in turn (one group's tile takes longer than the MMA of
+    // one tile); the warps of any other group only keep count. Every warp still walks every
     // tile: it waits for each segment's q record and signals when it is done
     // with each segment's w', so a slot is reused only after every group is
     // done with it.
     const int row = 32 * (warp & 3) + lane;    // the TMEM lane (key row) this thread reads
     const int grp = (warp - kEpiWarp0) >> 2;
-    Walker w;
-    w.init(p, t0, j0);
-    int ss = 0, L = 0;
+    Walker<kRows> w;
+    w.init(p, lay, t0, j0);
+    int ss = 0;
     Ring rd, rm, rs, rg;   // rg.idx: the group whose tile this is
-    for (int i = 0; i < n_tiles; ++i, w.next(p), rd.next(nd), rm.next(kR), rg.next(kEpiGroups)) {
+    for (int i = 0; i < n_tiles; ++i, w.next(p, lay), rd.next(nd), rm.next(kR), rg.next(lay.ne)) {
       const bool seg_start = (i == 0) || (w.j == 0);
       const bool seg_end = (i == n_tiles - 1) || (w.j == w.nt - 1);
       bool ok = true;
       if (seg_start) {
         if (i > 0) rs.next(nseg);
         ss = rs.idx;
-        L = p.valid_lens[w.t];
         ok = ptx::mbar_wait(bar(B_SEG_FULL + ss), rs.phase, abort_flag, kTimeoutNs);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
       }
@@ -638,55 +666,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const int s_key = w.j * kTileKeys + row;
       const int b = (s_key >> lay.epb_shift) - sMeta[r].lb0;
-      const bool in_len = s_key < L;
-      const bool valid = in_len && b < kMaxBlocksPerTile && ((sMeta[r].mask >> b) & 1u);
+      const bool blk_ok = b < kMaxBlocksPerTile && ((sMeta[r].mask >> b) & 1u);
       const float g = (b < kMaxBlocksPerTile) ? sMeta[r].g[b] : 0.0f;
-      const float *wq = reinterpret_cast<const float *>(sB + ss * lay.rec_smem + lay.rec_w);  // w'_h
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // eight independent chains
-      const uint32_t taddr = tmem_d + d * Npad + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-      for (int c0 = 0; c0 < Npad; c0 += 32) {   // Npad is a multiple of 32
-        uint32_t v[32];
-        __syncwarp();  // the per-row sign branch below must not leave the warp split at these loads
-        ptx::tmem_ld32(taddr + c0, v);
-        ptx::tmem_wait_ld();
-        if (c0 + 32 >= Npad) {   // every accumulator column is in registers: hand back the slots
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::mbar_arrive(bar(B_EMPTY_D + d));
-            ptx::mbar_arrive(bar(B_META_EMPTY + r));
+      const int len0 = sMeta[r].len[0], len1 = sMeta[r].len[1];
+      const float *wq = reinterpret_cast<const float *>(sB + ss * lay.rec_smem + lay.rec_w);  // w'_n
+      const uint32_t taddr = tmem_d + d * NR + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+#pragma unroll
+      for (int rr = 0; rr < kRows; ++rr) {    // rows of the group: head rows rr Npad .. rr Npad + Npad - 1
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // eight independent chains
+        for (int c0 = rr * Npad; c0 < (rr + 1) * Npad; c0 += 32) {   // Npad is a multiple of 32
+          uint32_t v[32];
+          __syncwarp();  // the per-row sign branch below must not leave the warp split at these loads
+          ptx::tmem_ld32(taddr + c0, v);
+          ptx::tmem_wait_ld();
+          if (c0 + 32 >= NR) {   // every accumulator column is in registers: hand back the slots
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::mbar_arrive(bar(B_EMPTY_D + d));
+              ptx::mbar_arrive(bar(B_META_EMPTY + r));
+            }
+          }
+          const float4 *w4 = reinterpret_cast<const float4 *>(wq + c0);
+          if (g >= 0.0f) {          // relu(g a) = g max(a, 0)
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 ww = w4[e >> 2];
+              float *ac = acc + ((e >> 2) & 1) * 4;
+              ac[0] = fmaf(ww.x, fmaxf(__uint_as_float(v[e + 0]), 0.0f), ac[0]);
+              ac[1] = fmaf(ww.y, fmaxf(__uint_as_float(v[e + 1]), 0.0f), ac[1]);
+              ac[2] = fmaf(ww.z, fmaxf(__uint_as_float(v[e + 2]), 0.0f), ac[2]);
+              ac[3] = fmaf(ww.w, fmaxf(__uint_as_float(v[e + 3]), 0.0f), ac[3]);
+            }
+          } else {                  // relu(g a) = g min(a, 0)
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 ww = w4[e >> 2];
+              float *ac = acc + ((e >> 2) & 1) * 4;
+              ac[0] = fmaf(ww.x, fminf(__uint_as_float(v[e + 0]), 0.0f), ac[0]);
+              ac[1] = fmaf(ww.y, fminf(__uint_as_float(v[e + 1]), 0.0f), ac[1]);
+              ac[2] = fmaf(ww.z, fminf(__uint_as_float(v[e + 2]), 0.0f), ac[2]);
+              ac[3] = fmaf(ww.w, fminf(__uint_as_float(v[e + 3]), 0.0f), ac[3]);
+            }
           }
         }
-        const float4 *w4 = reinterpret_cast<const float4 *>(wq + c0);
-        if (g >= 0.0f) {          // relu(g a) = g max(a, 0)
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 ww = w4[e >> 2];
-            float *ac = acc + ((e >> 2) & 1) * 4;
-            ac[0] = fmaf(ww.x, fmaxf(__uint_as_float(v[e + 0]), 0.0f), ac[0]);
-            ac[1] = fmaf(ww.y, fmaxf(__uint_as_float(v[e + 1]), 0.0f), ac[1]);
-            ac[2] = fmaf(ww.z, fmaxf(__uint_as_float(v[e + 2]), 0.0f), ac[2]);
-            ac[3] = fmaf(ww.w, fmaxf(__uint_as_float(v[e + 3]), 0.0f), ac[3]);
-          }
-        } else {                  // relu(g a) = g min(a, 0)
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 ww = w4[e >> 2];
-            float *ac = acc + ((e >> 2) & 1) * 4;
-            ac[0] = fmaf(ww.x, fminf(__uint_as_float(v[e + 0]), 0.0f), ac[0]);
-            ac[1] = fmaf(ww.y, fminf(__uint_as_float(v[e + 1]), 0.0f), ac[1]);
-            ac[2] = fmaf(ww.z, fminf(__uint_as_float(v[e + 2]), 0.0f), ac[2]);
-            ac[3] = fmaf(ww.w, fminf(__uint_as_float(v[e + 3]), 0.0f), ac[3]);
-          }
+        const float sum = ((acc[0] + acc[4]) + (acc[1] + acc[5])) + ((acc[2] + acc[6]) + (acc[3] + acc[7]));
+        const int t = w.t * kRows + rr;
+        if (s_key < (rr == 0 ? len0 : len1)) {   // an absent row or a bad length has length 0
+          const float sc = __fadd_rn(g * sum, 0.0f);
+          scores[static_cast<long long>(t) * ld + s_key] = blk_ok ? sc : -INFINITY;
+          // the selection's first digit: top 12 bits of the order-preserving key
+          if (blk_ok && sc != -INFINITY)   // exactly the keys the selection will see
+            atomicAdd(hist + static_cast<size_t>(t) * kScoreBins + (float_order(sc) >> 20), 1u);
         }
-      }
-      const float sum = ((acc[0] + acc[4]) + (acc[1] + acc[5])) + ((acc[2] + acc[6]) + (acc[3] + acc[7]));
-      if (in_len) {
-        const float sc = __fadd_rn(g * sum, 0.0f);
-        scores[static_cast<long long>(w.t) * ld + s_key] = valid ? sc : -INFINITY;
-        // the selection's first digit: top 12 bits of the order-preserving key
-        if (valid && sc != -INFINITY)   // exactly the keys the selection will see
-          atomicAdd(hist + static_cast<size_t>(w.t) * kScoreBins + (float_order(sc) >> 20), 1u);
       }
       if (seg_end) {             // this warp is done with the segment's w'
         __syncwarp();
@@ -726,14 +758,24 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   TcLayout l{};
   l.Npad = round_up(p.H, 32);
   if (l.Npad > 256) return false;
-  l.nseg = (l.Npad <= 128) ? 2 : 1;
+  // Row pairs share one decoded key tile (one MMA of N = 2 Npad) when every
+  // row reads the same block table.
+  l.R = (p.bt_stride == 0 && p.T >= 2 && l.Npad <= 64) ? 2 : 1;
+  l.NR = l.R * l.Npad;
+  l.nq = (p.T + l.R - 1) / l.R;
+  l.nseg = (l.NR <= 128) ? 2 : 1;
   // Tensor memory (512 columns): na A slots of 64 columns (128 keys x 128 f16)
   // and nd D slots of Npad columns (128 keys x Npad f32 accumulators); more
   // slots let the decoders, the MMA and the epilogue run further apart.
-  l.na = (l.Npad <= 128) ? 4 : 2;
-  l.nd = (512 - 64 * l.na) / l.Npad;
+  l.na = (l.NR <= 64) ? 4 : 2;
+  l.nd = (512 - 64 * l.na) / l.NR;
   if (l.nd > kMaxSlots) l.nd = kMaxSlots;
   if (l.nd < 1) return false;
+  // Epilogue groups in use: at most one per D slot. A group waits for the D
+  // slot of its tile i with the slot's phase parity; the tile nd before it
+  // must already be complete for that parity to be unambiguous, which the
+  // group's own previous tile (i - ne) guarantees when ne <= nd.
+  l.ne = (l.nd < kEpiGroups) ? l.nd : kEpiGroups;
   if (p.epb < 16 || (p.epb & (p.epb - 1)) != 0) return false;  // power-of-two blocks of >= 16 keys
   l.box_rows = p.epb < 128 ? p.epb : 128;
   l.bpt = p.epb < 128 ? 128 / p.epb : 1;
@@ -741,10 +783,10 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   while ((1 << l.epb_shift) < p.epb) ++l.epb_shift;
   // B-operand records first (1 KB-aligned slots), then the raw stages (1 KB
   // multiples, as many as fit), then the small tables.
-  l.b_bytes = static_cast<uint32_t>(l.Npad) * 256u;
+  l.b_bytes = static_cast<uint32_t>(l.NR) * 256u;
   l.rec_w = 2u * l.b_bytes;
-  l.rec_flags = l.rec_w + static_cast<uint32_t>(l.Npad) * 4u;
-  l.rec_bytes = (l.rec_flags + static_cast<uint32_t>(l.Npad) * 4u + 127u) & ~127u;
+  l.rec_flags = l.rec_w + static_cast<uint32_t>(l.NR) * 4u;
+  l.rec_bytes = (l.rec_flags + static_cast<uint32_t>(l.NR) * 4u + 127u) & ~127u;
   l.rec_smem = (l.rec_bytes + 1023u) & ~1023u;
   l.off_b = 0;
   const uint32_t b_total = static_cast<uint32_t>(l.nseg) * l.rec_smem;
@@ -781,7 +823,7 @@ bool score_tc_supported(const ScoreParams &p) {
 size_t score_tc_workspace(const ScoreParams &p) {
   TcLayout lay;
   if (!make_layout(p, &lay)) return 0;
-  return static_cast<size_t>(p.T) * lay.rec_bytes;
+  return static_cast<size_t>(lay.nq) * lay.rec_bytes;
 }
 
 cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint32_t *hist, uint32_t *cand_cnt,
@@ -799,11 +841,13 @@ cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint
                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  void (*kern)(const CUtensorMap, ScoreParams, TcLayout, const uint8_t *, uint32_t *, float *, long long) =
+      (lay.R == 2) ? score_tc_kernel<2> : score_tc_kernel<1>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(lay.smem_bytes));
   if (e != cudaSuccess) return e;
   uint8_t *rec = static_cast<uint8_t *>(qrec);
-  qprep_kernel<<<dim3(static_cast<unsigned>(p.T), static_cast<unsigned>(lay.Npad / 8)), 256, 0, stream>>>(p, lay, rec, hist,
+  qprep_kernel<<<dim3(static_cast<unsigned>(lay.nq), static_cast<unsigned>(lay.NR / 8)), 256, 0, stream>>>(p, lay, rec, hist,
                                                                                                           cand_cnt);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // The scorer may launch while qprep_kernel runs: its producer waits for the
@@ -818,7 +862,7 @@ cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, score_tc_kernel, tmap, p, lay, static_cast<const uint8_t *>(rec), hist, scores, ld);
+  return cudaLaunchKernelEx(&cfg, kern, tmap, p, lay, static_cast<const uint8_t *>(rec), hist, scores, ld);
 }
 
 }  // namespace idx
