@@ -45,6 +45,8 @@ typedef enum {
 #define IDX_STATUS_BAD_LEN 2   /* a valid length outside [0, max_logical_blocks * epb]      */
 #define IDX_STATUS_BAD_SEL 4   /* a gather position whose logical block is past the table   */
 #define IDX_STATUS_TIMEOUT 8   /* an internal pipeline wait gave up (2 s); outputs invalid   */
+#define IDX_STATUS_DEBUG_BOUNDS 16 /* debug-bounds builds only (-DIDX_DEBUG_BOUNDS): an index
+                                      check failed and the access it guards was skipped    */
 
 typedef enum { IDX_KEYS_NVFP4 = 0, IDX_KEYS_F32 = 1 } idx_key_format_t;
 

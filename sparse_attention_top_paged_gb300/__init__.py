@@ -20,7 +20,7 @@ import ctypes
 
 from . import _lib
 from ._lib import (IndexerError, KEYS_F32, KEYS_NVFP4, PATHS, STATUS_BAD_BLOCK,  # noqa: F401
-                   STATUS_BAD_LEN, STATUS_BAD_SEL, load_library)
+                   STATUS_BAD_LEN, STATUS_BAD_SEL, STATUS_DEBUG_BOUNDS, STATUS_TIMEOUT, load_library)
 
 _workspaces: dict = {}
 

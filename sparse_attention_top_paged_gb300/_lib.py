@@ -19,7 +19,7 @@ STATUS_NAMES = {0: "IDX_OK", 1: "IDX_ERR_INVALID_ARG", 2: "IDX_ERR_UNSUPPORTED",
                 3: "IDX_ERR_WORKSPACE_TOO_SMALL", 4: "IDX_ERR_CUDA"}
 KEYS_NVFP4, KEYS_F32 = 0, 1
 PATHS = {"auto": 0, "tensor": 1, "simt": 2}
-STATUS_BAD_BLOCK, STATUS_BAD_LEN, STATUS_BAD_SEL, STATUS_TIMEOUT = 1, 2, 4, 8
+STATUS_BAD_BLOCK, STATUS_BAD_LEN, STATUS_BAD_SEL, STATUS_TIMEOUT, STATUS_DEBUG_BOUNDS = 1, 2, 4, 8, 16
 STATIC_SCRATCH_BYTES = 8 << 20
 
 c_i32, c_i64, c_u32, c_size, c_f32, c_vp = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32,

@@ -70,6 +70,38 @@ def build(verbose: bool = False, extra_flags=()) -> str:
     return LIB
 
 
+def build_variant(name: str, defines=(), sources=None) -> str:
+    """Build ``libidx_<name>.so`` beside libidx.so with extra preprocessor
+    ``defines`` (e.g. the failure-path test's short wait limit): the listed
+    ``sources`` (default: every ``csrc/*.cu``) are recompiled with them into
+    ``_build/<name>/`` and linked with the in-tree objects of the others.
+    Used by tests only; the product library is ``build()``'s."""
+    build()
+    nvcc = _nvcc()
+    vdir = os.path.join(BUILD, name)
+    os.makedirs(vdir, exist_ok=True)
+    flags = [f"-D{d}" for d in defines]
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    chosen = set(sources) if sources is not None else {os.path.basename(x) for x in srcs}
+    objs, jobs = [], []
+    for src in srcs:
+        base = os.path.basename(src)[:-3] + ".o"
+        if os.path.basename(src) in chosen:
+            obj = os.path.join(vdir, base)
+            jobs.append((src, obj))
+        else:
+            obj = os.path.join(BUILD, base)
+        objs.append(obj)
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
+        list(ex.map(lambda j: _compile(nvcc, j[0], j[1], flags), jobs))
+    lib = os.path.join(PKG, f"libidx_{name}.so")
+    cmd = [nvcc, *ARCH, "-shared", "-o", lib, *objs, "-lcudart_static", "-lrt", "-lpthread", "-ldl"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link of {os.path.basename(lib)} failed:\n{r.stdout}\n{r.stderr}")
+    return lib
+
+
 if __name__ == "__main__":
     import sys
     print(build(verbose="-v" in sys.argv))

@@ -15,7 +15,22 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/idx.h"
+
 namespace idx {
+
+// Index checks of debug-bounds builds (-DIDX_DEBUG_BOUNDS): a failed check ORs
+// IDX_STATUS_DEBUG_BOUNDS into the status word and the access it guards is
+// skipped. In other builds a check is the constant true and compiles away.
+#ifdef IDX_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_bounds(bool ok, int32_t *status) {
+  if (!ok && status != nullptr) atomicOr(status, IDX_STATUS_DEBUG_BOUNDS);
+  return ok;
+}
+#define IDX_IN_BOUNDS(cond, status) ::idx::in_bounds((cond), (status))
+#else
+#define IDX_IN_BOUNDS(cond, status) true
+#endif
 
 __device__ __forceinline__ uint32_t float_order(float f) {
   uint32_t b = __float_as_uint(__fadd_rn(f, 0.0f));  // -0 + 0 = +0

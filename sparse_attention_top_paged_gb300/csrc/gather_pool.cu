@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_kv_kernel(idx_gather
     }
   }
   if (err && lane_id() == 0 && a.dev_status) atomicOr(a.dev_status, err);
+  if (src_row >= 0 && !IDX_IN_BOUNDS(src_row < static_cast<long long>(a.P) * a.block_size, a.dev_status)) src_row = -1;
   const long long nvec = a.row_bytes / 16;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   {

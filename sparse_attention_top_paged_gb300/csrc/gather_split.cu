@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32) gather_split_kernel(idx_gath
     }
   }
   if (err && lane == 0 && a.dev_status) atomicOr(a.dev_status, err);
+  if (src >= 0 && !IDX_IN_BOUNDS(src < static_cast<long long>(a.P) * a.block_size, a.dev_status)) src = -1;
   const int width = a.nope_dim + a.rope_dim;   // even
   uint32_t *dst = reinterpret_cast<uint32_t *>(a.out + r * width);
   if (src < 0) {

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kSimtThreads) score_simt_kernel(ScoreParams p,
   // with a bad block, is the same for all of them)
 #pragma unroll
   for (int o = 1; o < G; o <<= 1) I += __shfl_xor_sync(0xFFFFFFFFu, I, o);
-  if (s < L && hg == 0) scores[static_cast<long long>(t) * ld + s] = I;
+  if (s < L && hg == 0 && IDX_IN_BOUNDS(t < p.T && s < ld, p.dev_status)) scores[static_cast<long long>(t) * ld + s] = I;
   if (__any_sync(0xFFFFFFFFu, bad) && lane_id() == 0 && p.dev_status)
     atomicOr(p.dev_status, IDX_STATUS_BAD_BLOCK);
 }

@@ -71,7 +71,16 @@ constexpr int kR = 64;                   // metadata ring (tiles)
 constexpr uint32_t kStageBytes = 9216;   // 128 x 64 B nibbles + 128 x 8 B scales
 constexpr uint32_t kScaleOff = 8192;
 constexpr int kMaxBlocksPerTile = 8;     // epb >= 16
+// A pipeline wait gives up after kTimeoutNs, raising the CTA's abort flag
+// (IDX_STATUS_TIMEOUT); the waits that drain asynchronous work before exit
+// always allow kDrainNs. Builds for the failure-path test shorten the first
+// (IDX_WAIT_LIMIT_NS).
+#ifdef IDX_WAIT_LIMIT_NS
+constexpr uint64_t kTimeoutNs = IDX_WAIT_LIMIT_NS;
+#else
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+#endif
+constexpr uint64_t kDrainNs = 2000000000ull;
 constexpr int kSmemLimit = 227 * 1024;
 
 // One tile's resolved blocks, written by the resolver warp, read by the
@@ -107,7 +116,8 @@ constexpr int kMaxSlots = 4;  // tensor-memory A and D slots (each)
 constexpr int B_FULL_RAW = 0, B_EMPTY_RAW = kMaxNS, B_FULL_A = 2 * kMaxNS, B_EMPTY_A = B_FULL_A + kMaxSlots,
               B_FULL_D = B_EMPTY_A + kMaxSlots, B_EMPTY_D = B_FULL_D + kMaxSlots,
               B_META_FULL = B_EMPTY_D + kMaxSlots, B_META_EMPTY = B_META_FULL + kR, B_SEG_FULL = B_META_EMPTY + kR,
-              B_SEG_BFREE = B_SEG_FULL + 2, B_SEG_WFREE = B_SEG_FULL + 4, B_COUNT = B_SEG_FULL + 6;
+              B_SEG_BFREE = B_SEG_FULL + 2, B_SEG_WFREE = B_SEG_FULL + 4, B_DRAIN = B_SEG_FULL + 6,
+              B_NEVER = B_DRAIN + 1, B_COUNT = B_NEVER + 1;
 
 // misc ints
 constexpr int M_TMEM = 0, M_ABORT = 1, M_T0 = 2, M_J0 = 3, M_SCAN = 8;  // then one long per warp (scan)
@@ -287,6 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(B_META_FULL + r), 1);   // resolver
       ptx::mbar_init(bar(B_META_EMPTY + r), 4);  // epilogue warps
     }
+    ptx::mbar_init(bar(B_DRAIN), 1);   // MMA commit before exit
+    ptx::mbar_init(bar(B_NEVER), 1);   // nothing arrives (failure-path test builds only)
     misc[M_ABORT] = 0;
     ptx::fence_mbar_init();
   }
@@ -368,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // and no two tiles of a batch share a stage
     const int nb = min(8, ns / 2);
     const uint64_t pol_stream = ptx::policy_evict_first();   // keys are read once
-    int issued = 0, last_seg = -1;
+    int issued = 0, last_seg0 = -1, last_seg1 = -1;   // latest record copied into each slot
     bool qrec_ready = false;
     for (int base = 0; base < n_tiles; base += nb) {
       const int i = base + lane;
@@ -387,11 +399,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tq = m.t;
         const uint32_t mask = m.mask;
         const int s0 = m.s0, lb0 = m.lb0, nblk = m.nblk;
-        uint32_t bytes = 0;
+        // a block's copies: its keys within the tile (rows lo .. hi of the
+        // tile's key range); a debug-bounds build checks them against the pool
+        auto copy_ok = [&](int b) {
+          const int blk0 = (lb0 + b) << lay.epb_shift;
+          const int lo = max(s0, blk0), hi = min(s0 + kTileKeys, blk0 + p.epb);
+          const long long row0 = (static_cast<long long>(m.phys[b]) << lay.epb_shift) + (lo - blk0);
+          return IDX_IN_BOUNDS(row0 >= 0 && row0 + (hi - lo) <= static_cast<long long>(p.P) * p.epb &&
+                                   hi - s0 <= kTileKeys,
+                               p.dev_status);
+        };
+        uint32_t bytes = 0, copied = 0;   // copied: bit b, block b's copies are issued
         for (int b = 0; b < nblk; ++b) {
-          if (!((mask >> b) & 1u)) continue;
+          if (!((mask >> b) & 1u) || !copy_ok(b)) continue;
           const int blk0 = (lb0 + b) << lay.epb_shift;
           bytes += static_cast<uint32_t>(min(s0 + kTileKeys, blk0 + p.epb) - max(s0, blk0)) * 72u;
+          copied |= 1u << b;
         }
         const uint32_t full = bar(B_FULL_RAW + s);
         uint8_t *stage = sRaw + static_cast<size_t>(s) * kStageBytes;
@@ -400,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           ptx::mbar_arrive_expect_tx(full, bytes);
           for (int b = 0; b < nblk; ++b) {
-            if (!((mask >> b) & 1u)) continue;
+            if (!((copied >> b) & 1u)) continue;
             const int blk0 = (lb0 + b) << lay.epb_shift;
             const int lo = max(s0, blk0), hi = min(s0 + kTileKeys, blk0 + p.epb);
             const long long row0 = (static_cast<long long>(m.phys[b]) << lay.epb_shift) + (lo - blk0);
@@ -444,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(sfull, lay.rec_bytes);
             ptx::bulk_g2s(ptx::smem_addr(sB + ss * lay.rec_smem), qrec + static_cast<size_t>(t_seg) * lay.rec_bytes,
                           lay.rec_bytes, sfull);
-            last_seg = ord;
+            if (ss == 0) last_seg0 = ord; else last_seg1 = ord;
           }
         }
         if (!__all_sync(0xFFFFFFFFu, __shfl_sync(0xFFFFFFFFu, seg_ok, 0))) break;
@@ -452,18 +475,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__shfl_sync(0xFFFFFFFFu, seg_ok, 0)) break;
     }
     // Never leave with copies in flight: the last ns tile stages (one per
-    // lane) and the last segment record (an earlier one was waited for before
-    // its slot's reuse).
+    // lane) and the latest record of each slot (an earlier one was waited for
+    // before its slot's reuse).
     volatile int no_abort = 0;
     if (lane < ns) {
       const int i = issued - ns + lane;
       if (i >= 0)
-        ptx::mbar_wait(bar(B_FULL_RAW + i % ns), static_cast<uint32_t>(i / ns) & 1u, &no_abort, kTimeoutNs);
+        ptx::mbar_wait(bar(B_FULL_RAW + i % ns), static_cast<uint32_t>(i / ns) & 1u, &no_abort, kDrainNs);
     }
-    last_seg = __shfl_sync(0xFFFFFFFFu, last_seg, 0);
-    if (lane == 0 && last_seg >= 0)
-      ptx::mbar_wait(bar(B_SEG_FULL + last_seg % nseg), static_cast<uint32_t>(last_seg / nseg) & 1u, &no_abort,
-                     kTimeoutNs);
+    const int ls0 = __shfl_sync(0xFFFFFFFFu, last_seg0, 0), ls1 = __shfl_sync(0xFFFFFFFFu, last_seg1, 0);
+    const int last_rec = (lane == 0) ? ls0 : ls1;
+    if ((lane == 0 || lane == 1) && last_rec >= 0)
+      ptx::mbar_wait(bar(B_SEG_FULL + last_rec % nseg), static_cast<uint32_t>(last_rec / nseg) & 1u, &no_abort,
+                     kDrainNs);
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     // The whole warp walks the tiles in lockstep; one elected lane issues.
@@ -477,6 +501,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ring ra, rd, rs;
     rs.idx = -1;  // advanced at each segment start
     int ss = 0;
+    bool any_mma = false;
+#ifdef IDX_TEST_STALL
+    // Failure-path test builds only: CTA 0 first waits for a barrier nothing
+    // ever arrives on, so its wait gives up, raises the abort flag and the
+    // whole CTA takes the abort-and-drain path.
+    if (blockIdx.x == 0) ptx::mbar_wait(bar(B_NEVER), 0u, abort_flag, kTimeoutNs);
+#endif
     for (int i = 0; i < n_tiles; ++i, w.next(p, lay), ra.next(na), rd.next(nd)) {
       const bool seg_start = (i == 0) || (w.j == 0);
       const bool seg_end = (i == n_tiles - 1) || (w.j == w.nt - 1);
@@ -517,6 +548,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (seg_end) ptx::mma_commit(bar(B_SEG_BFREE + ss));
       }
       __syncwarp();
+      any_mma = true;
+    }
+    // Never leave with MMAs in flight (the epilogue waits for each of them,
+    // but not after an abort): tensor memory is freed after this.
+    if (any_mma) {
+      volatile int no_abort = 0;
+      if (ptx::elect_one()) ptx::mma_commit(bar(B_DRAIN));
+      __syncwarp();
+      ptx::mbar_wait(bar(B_DRAIN), 0u, &no_abort, kDrainNs);
     }
   } else if (warp < kEpiWarp0) {
     // ============================================================== decoders
@@ -712,7 +752,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float sum = ((acc[0] + acc[4]) + (acc[1] + acc[5])) + ((acc[2] + acc[6]) + (acc[3] + acc[7]));
         const int t = w.t * kRows + rr;
-        if (s_key < (rr == 0 ? len0 : len1)) {   // an absent row or a bad length has length 0
+        if (s_key < (rr == 0 ? len0 : len1) && IDX_IN_BOUNDS(t < p.T && s_key < ld, p.dev_status)) {
+          // (an absent row or a bad length has length 0)
           const float sc = __fadd_rn(g * sum, 0.0f);
           scores[static_cast<long long>(t) * ld + s_key] = blk_ok ? sc : -INFINITY;
           // the selection's first digit: top 12 bits of the order-preserving key
