@@ -301,6 +301,79 @@ __device__ __forceinline__ void warp_sort_segment(const uint64_t *buf, int start
     if (lane * E + e < n) emit(v[e], start + lane * E + e);
 }
 
+// One warp orders buf[start .. start+n) (64 < n <= 256 keys of one first-digit
+// bin) by splitting it on the next 8 key bits: a count of the keys per sub-bin
+// (cnt: this warp's 256 counters in shared memory), a descending exclusive
+// scan of the counts gives each sub-bin's start, the keys are scattered to
+// their sub-bins, and each key's final rank is its sub-bin's start plus the
+// number of keys of its sub-bin that are larger. Returns false, having
+// written nothing, when some sub-bin holds more than 32 keys (many equal
+// leading bits, e.g. tied scores): the caller then sorts the bin by
+// comparisons.
+template <class Emit>
+__device__ __forceinline__ bool warp_radix_segment(uint64_t *buf, int start, int n, uint32_t *cnt, Emit &emit) {
+  const int lane = threadIdx.x & 31;
+  constexpr int E = 8;                       // keys per lane: key j = lane + 32 e
+#pragma unroll
+  for (int i = lane; i < 256; i += 32) cnt[i] = 0u;
+  __syncwarp();
+  uint64_t kk[E];
+  uint32_t dg[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int j = lane + 32 * e;
+    kk[e] = (j < n) ? buf[start + j] : 0ull;
+    dg[e] = static_cast<uint32_t>(kk[e] >> 44) & 255u;
+    if (j < n) atomicAdd(&cnt[dg[e]], 1u);
+  }
+  __syncwarp();
+  // descending exclusive scan: lane owns digits 255 - 8 lane - u (u < 8)
+  uint32_t c8[8], tot = 0, mx = 0;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    c8[u] = cnt[255 - 8 * lane - u];
+    tot += c8[u];
+    mx = max(mx, c8[u]);
+  }
+  if (__reduce_max_sync(0xFFFFFFFFu, mx) > 32u) return false;
+  uint32_t incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  uint32_t r = incl - tot;
+  __syncwarp();
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    cnt[255 - 8 * lane - u] = r | (c8[u] << 16);   // sub-bin start | its count
+    r += c8[u];
+  }
+  __syncwarp();
+  // scatter into the sub-bins (any order within one), then rank within each
+  uint32_t cur[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (lane + 32 * e < n) cur[e] = atomicAdd(&cnt[dg[e]], 1u) & 0xFFFFu;   // start + arrival order
+  __syncwarp();
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (lane + 32 * e < n) buf[start + static_cast<int>(cur[e])] = kk[e];
+  __syncwarp();
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if (lane + 32 * e >= n) continue;
+    const uint32_t sc = cnt[dg[e]];               // (start + count) | count << 16 after the arrivals
+    const int c = static_cast<int>(sc >> 16);
+    const int s0 = static_cast<int>(sc & 0xFFFFu) - c;
+    int rank = 0;
+    for (int x = s0; x < s0 + c; ++x) rank += (buf[start + x] > kk[e]) ? 1 : 0;
+    emit(kk[e], start + s0 + rank);
+  }
+  __syncwarp();
+  return true;
+}
+
 // Split collection, ahead of topk_stream_kernel on rows that come with the
 // scorer's first-digit histogram: CTA c of row t takes the c-th slice of the
 // row and appends every key the selection would place (at or above the
@@ -435,6 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
   // where broad selections fill many bins past 128 and a warp-sorted bin
   // saves the CTA-wide split).
   constexpr int kWarpBin = kThreads == 1024 ? 128 : 256;
+  // Bins above kRadixMin keys are split on the next 8 bits rather than sorted
+  // by comparisons (512 threads, where bins of 65..256 keys are common).
+  constexpr int kRadixMin = kThreads == 1024 ? 128 : 64;
   constexpr int kLargeKeys = kBndCap / kThreads;   // a large bin's keys per thread
   static_assert(kBndCap % kThreads == 0 && kThreads <= kMaxThreads, "a large bin's keys spread evenly");
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -707,9 +783,15 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
         }
         __syncthreads();   // sub_cnt / sub_cur are reused by the next large bin
       }
-      // Warp w sorts the small bins w, w + 16, ... one at a time, in
-      // registers, and writes each key to its output slot.
+      // Warp w orders the small bins w, w + 16, ... one at a time and writes
+      // each key to its output slot: bins of up to kRadixMin keys by a sort in
+      // registers, larger ones by a split on the next 8 key bits (in 256
+      // counters per warp, in the row's staging area, which the place pass
+      // is done with), or by a sort when that split leaves a crowded sub-bin.
       auto emit_if = [&](uint64_t kv, int pos) { emit(kv, pos); };
+      uint32_t *radix_cnt = (lay.stage_floats >= static_cast<size_t>(kThreads / 32) * 256)
+                                ? reinterpret_cast<uint32_t *>(smem_raw + lay.stage) + warp * 256
+                                : nullptr;
       for (int b0 = warp; b0 < kBins; b0 += 32 * (kThreads / 32)) {
         const int b = b0 + (kThreads / 32) * lane;       // this lane's bin of the group
         const uint32_t pk = (b < kBins) ? sh->table[b] : 0u;
@@ -723,7 +805,8 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
           const int cnt = min(n, total - start);
           if (cnt <= 32) warp_sort_segment<1>(buf, start, cnt, emit_if);
           else if (cnt <= 64) warp_sort_segment<2>(buf, start, cnt, emit_if);
-          else if (kWarpBin <= 128 || cnt <= 128) warp_sort_segment<4>(buf, start, cnt, emit_if);
+          else if (cnt > kRadixMin && radix_cnt != nullptr && warp_radix_segment(buf, start, cnt, radix_cnt, emit_if)) {
+          } else if (kWarpBin <= 128 || cnt <= 128) warp_sort_segment<4>(buf, start, cnt, emit_if);
           else if constexpr (kWarpBin > 128) warp_sort_segment<8>(buf, start, cnt, emit_if);
         }
       }
