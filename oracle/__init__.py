@@ -20,6 +20,11 @@ Every function states the passage of the source pages it follows:
   ``qsa_block_pool``, ``qsa_qprep``, ``qsa_qprep_rows``, ``qsa_score``,
   ``qsa_gather``, ``qsa_score_rows`` and ``qsa_prefill_attn``.
 
+The NVFP4-q mode (queries quantised to NVFP4 for the FP4 tensor-core MMA the
+header comment of "indexer_score_topk.cu" plans) is ``quantize_q_nvfp4`` /
+``dequantize_q_nvfp4`` / ``nvfp4_q`` in ``indexer.py``; scores in that mode are
+``score_topk_rows`` applied to ``nvfp4_q(q)``.
+
 Parity status. Every function is pinned by ``tests/test_oracle_pins.py``
 except the RoPE pairing convention inside ``block_pool`` and
 ``qsa_qprep_rows`` (the pages do not say which dimensions are paired): parity
@@ -42,6 +47,12 @@ from .indexer import (  # noqa: F401
     STATUS_BAD_BLOCK,
     STATUS_BAD_LEN,
     STATUS_BAD_SEL,
+    NVFP4_Q_RANGE,
+    e4m3_encode,
+    e2m1_encode,
+    quantize_q_nvfp4,
+    dequantize_q_nvfp4,
+    nvfp4_q,
 )
 from .qsa import (block_pool, qsa_qprep_rows, qsa_prefill_attn, qsa_score, gather_kv, gather_split,  # noqa: F401
                   bf16_round, expand_blocks)

@@ -233,3 +233,88 @@ def score_topk(q, w, block_table, bt_stride, max_lb, valid_lens, epb, k, *,
         cand = np.nonzero(~np.isneginf(I))[0]   # excluded keys carry -inf
         idx[r], sc[r] = topk_sorted(I[cand], k, index=cand)
     return idx, sc, status, scores
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 queries: the opt-in mode in which the dot products take q in NVFP4.
+#
+# The header comment of indexer_score_topk.cu plans a second phase that swaps
+# the FP32 dot products for the FP4 tensor-core MMA, which takes both operands
+# in FP4; the "Main kernel" argument list already calls the query inputs
+# "dequantized from FP4", and commit c2f705a's CSAIndexer keeps a placeholder
+# projection "until Nvfp4Linear with FP4 output". The pages give no recipe for
+# quantising q; this mode applies the NVFP4 scheme of the keys (E2M1 elements,
+# one E4M3 scale per 16 consecutive elements, "FP4 dequantization (NVFP4
+# scheme)") plus one float32 scale per (query, head) that maps the head's
+# largest |q| onto the top of the E2M1 x E4M3 range, 6 * 448 = 2688. Every
+# rounding decision is taken in float32, in this order:
+#     amax = max_d |x_d|,                gq = fl32(amax / 2688)  (0 if amax == 0)
+#     per group g of 16 elements:        s_g = E4M3(fl32(ag / fl32(6 * gq)))
+#     per element (code 0 if s_g == 0):  c_d = E2M1(fl32(x_d / fl32(gq * s_g)))
+#     dequantised:                       q_hat_d = gq * s_g * e2m1(c_d)
+# where E4M3() and E2M1() round to the nearest representable value, ties to
+# the even code, saturating at the largest finite value (448, 6); a value that
+# rounds to zero gets code 0 (no negative zero).
+
+NVFP4_Q_RANGE = 2688.0   # 6 (largest E2M1) * 448 (largest finite E4M3)
+
+
+def _nearest_even_code(x, grid):
+    """Index of the grid value nearest to each x (float64 distances), the even
+    index on a tie; values beyond the grid's end take its last entry."""
+    x = np.asarray(x, dtype=np.float64)
+    d = np.abs(x[..., None] - np.asarray(grid, dtype=np.float64))
+    best = d == d.min(axis=-1, keepdims=True)
+    pref = best * np.where(np.arange(len(grid)) % 2 == 0, 2, 1)   # prefer the even code of a tie
+    return np.argmax(pref, axis=-1)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Non-negative values to E4M3 bytes: nearest finite value (codes 0..0x7E),
+    ties to the even code, saturating at 448."""
+    grid = e4m3_decode(np.arange(0x7F))
+    return _nearest_even_code(x, grid).astype(np.uint8)
+
+
+def e2m1_encode(y) -> np.ndarray:
+    """Values to E2M1 codes: nearest magnitude of the E2M1 table, ties to the
+    even code, saturating at 6; bit 3 set for a negative value that does not
+    round to zero."""
+    y = np.asarray(y, dtype=np.float64)
+    c = _nearest_even_code(np.abs(y), E2M1_MAGNITUDES)
+    return np.where((y < 0) & (c != 0), c | 8, c).astype(np.uint8)
+
+
+def quantize_q_nvfp4(q):
+    """``q [..., 128]`` (taken as float32) -> ``(codes [..., 128] uint8,
+    scales [..., 8] uint8 E4M3, gq [...] float32)`` by the steps above."""
+    x = np.asarray(q, dtype=np.float32)
+    lead = x.shape[:-1]
+    xg = x.reshape(lead + (8, 16))
+    f32 = np.float32
+    amax = np.abs(x).max(axis=-1)
+    gq = np.where(amax > 0, amax / f32(NVFP4_Q_RANGE), f32(0)).astype(np.float32)
+    ag = np.abs(xg).max(axis=-1)                                              # [..., 8]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        s_f = (ag / (f32(6) * gq)[..., None]).astype(np.float32)
+    s_f = np.where(ag > 0, s_f, f32(0))
+    scales = e4m3_encode(s_f)
+    s_val = e4m3_decode(scales).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = (xg / (gq[..., None] * s_val)[..., None]).astype(np.float32)
+    codes = np.where((s_val > 0)[..., None], e2m1_encode(y), 0).astype(np.uint8)
+    return codes.reshape(lead + (128,)), scales, gq
+
+
+def dequantize_q_nvfp4(codes, scales, gq) -> np.ndarray:
+    """``q_hat = gq * s_g * e2m1(code)`` in float64 (exact)."""
+    codes = np.asarray(codes)
+    lead = codes.shape[:-1]
+    v = e2m1_decode(codes).reshape(lead + (8, 16))
+    s = e4m3_decode(scales)[..., None]
+    return (v * s * np.asarray(gq, dtype=np.float64)[..., None, None]).reshape(lead + (128,))
+
+
+def nvfp4_q(q) -> np.ndarray:
+    """The queries the NVFP4-q mode scores with: ``dequantize(quantize(q))``."""
+    return dequantize_q_nvfp4(*quantize_q_nvfp4(q))

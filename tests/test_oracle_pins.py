@@ -446,6 +446,116 @@ def pin_expand_blocks():
     return list(got[0]) == [6, 7, 8, 15, 16, 17, -1, -1, -1]
 
 
+
+# ------------------------------------------------- NVFP4 queries (opt-in) ----
+
+def _golden_vec(d, n=128):
+    v = np.zeros(n)
+    for off, vals in d.items():
+        v[int(off):int(off) + len(vals)] = vals
+    return v
+
+
+def pin_nvfp4_q_golden():
+    """The hand-worked head of tests/golden/nvfp4_q_example.json: every code,
+    scale and dequantised value."""
+    c = json.load(open(os.path.join(GOLDEN, "nvfp4_q_example.json")))
+    x = _golden_vec(c["x_nonzero"]).astype(np.float32)
+    codes, scales, gq = oracle.quantize_q_nvfp4(x)
+    ok = float(gq) == c["gq"] and list(scales) == c["scales"]
+    ok &= np.array_equal(codes, _golden_vec(c["codes_nonzero"]).astype(np.uint8))
+    ok &= np.array_equal(oracle.dequantize_q_nvfp4(codes, scales, gq), _golden_vec(c["q_hat_nonzero"]))
+    return bool(ok)
+
+
+def pin_e4m3_encode_library():
+    """The E4M3 encoder against torch's float8_e4m3fn cast (round to nearest
+    even) on random values and on every midpoint between neighbouring codes;
+    every code round-trips; values above 448 saturate."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    grid = oracle.e4m3_decode(np.arange(0x7F))
+    mids = ((grid[:-1] + grid[1:]) / 2).astype(np.float32)
+    x = np.concatenate([rng.uniform(0, 448, 3000), 2.0 ** rng.uniform(-12, 8.7, 3000), mids]).astype(np.float32)
+    x = x[x <= 448]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ok = np.array_equal(oracle.e4m3_encode(x), want)
+    ok &= np.array_equal(oracle.e4m3_encode(grid), np.arange(0x7F))
+    ok &= np.array_equal(oracle.e4m3_encode(np.array([449.0, 480.0, 1e6])), [0x7E] * 3)
+    return bool(ok)
+
+
+def pin_e2m1_encode_ties():
+    """E2M1 rounding at every midpoint of the table (ties to the even code),
+    next to them, past 6 and below zero; against a threshold search over the
+    table's midpoints for a dense sweep."""
+    ties = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    want_tie = [0, 2, 2, 4, 4, 6, 6]
+    ok = list(oracle.e2m1_encode(np.array(ties))) == want_tie
+    ok &= list(oracle.e2m1_encode(np.array([-0.2, -0.3, -7.0, 6.5, 100.0]))) == [0, 9, 15, 7, 7]
+    y = np.linspace(-8, 8, 64001)
+    mag = np.abs(y)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    c = np.searchsorted(mids, mag, side="left")          # count of midpoints strictly below |y|
+    at_mid = np.isin(mag, mids)
+    c = np.where(at_mid & (c % 2 == 1), c + 1, c)         # a midpoint goes to the even neighbour
+    want = np.where((y < 0) & (c != 0), c | 8, c)
+    ok &= np.array_equal(oracle.e2m1_encode(y), want)
+    return bool(ok)
+
+
+def pin_nvfp4_q_invariants():
+    """On random heads: each non-zero group's largest |x| lands on +-6 * gq * s;
+    every element is within gq * s of its value (half the widest E2M1 gap);
+    scaling q by 2^k scales gq by 2^k and changes no code or scale; -q flips
+    exactly the signs; a zero head quantises to zeros."""
+    rng = np.random.default_rng(9)
+    q = (rng.standard_normal((64, 128)) * np.exp2(rng.integers(-6, 6, size=(64, 1)))).astype(np.float32)
+    q[3] = 0
+    q[5, 16:32] = 0
+    codes, scales, gq = oracle.quantize_q_nvfp4(q)
+    qh = oracle.dequantize_q_nvfp4(codes, scales, gq)
+    s = oracle.e4m3_decode(scales) * gq[:, None].astype(np.float64)            # [64, 8]
+    xg = q.reshape(64, 8, 16).astype(np.float64)
+    hg = qh.reshape(64, 8, 16)
+    ok = True
+    arg = np.abs(xg).argmax(axis=-1)
+    top = np.take_along_axis(hg, arg[..., None], -1)[..., 0]
+    nz = np.abs(xg).max(-1) > 0
+    ok &= np.allclose(np.abs(top[nz]), 6 * s[nz], rtol=0, atol=0)
+    ok &= bool(np.all(np.abs(xg - hg) <= s[..., None] * (1 + 1e-6)))
+    for k in (-3, 5):
+        c2, s2, g2 = oracle.quantize_q_nvfp4(q * np.float32(2.0 ** k))
+        ok &= np.array_equal(c2, codes) and np.array_equal(s2, scales) and np.array_equal(g2, gq * np.float32(2.0 ** k))
+    c3, s3, g3 = oracle.quantize_q_nvfp4(-q)
+    ok &= np.array_equal(s3, scales) and np.array_equal(g3, gq)
+    ok &= np.array_equal(c3, np.where(codes != 0, codes ^ 8, 0))
+    ok &= not codes[3].any() and not scales[3].any() and gq[3] == 0
+    ok &= not scales[5, 1] and not codes[5, 16:32].any()
+    return bool(ok)
+
+
+def pin_nvfp4_q_scores_bound():
+    """Scores from NVFP4 queries stay within sum_h |w_h| sum_d |q - q_hat| |K|
+    of the exact scores (ReLU is 1-Lipschitz), on a small decode batch."""
+    W = wl.tiny_decode(1000)
+    rows = list(range(W.T))
+    exact, _ = oracle.score_topk_rows(W.q, W.w, W.block_table, W.bt_stride, W.max_lb, W.valid_lens, W.epb,
+                                      rows=rows, **W.oracle_kwargs())
+    qh = oracle.nvfp4_q(W.q)
+    approx, _ = oracle.score_topk_rows(qh, W.w, W.block_table, W.bt_stride, W.max_lb, W.valid_lens, W.epb,
+                                       rows=rows, **W.oracle_kwargs())
+    ok = True
+    for t in rows:
+        phys, slot, okm = oracle.resolve_slots(oi._table_row(W.block_table, W.bt_stride, W.max_lb, t),
+                                               int(W.valid_lens[t]), W.epb, W.keys_fp4.shape[0])
+        K = oracle.dequant_rows(W.keys_fp4, W.key_scale, W.key_gscale, phys[okm], slot[okm])
+        dq = np.abs(np.asarray(W.q[t], np.float64) - qh[t])                      # [H, D]
+        bound = np.abs(K) @ dq.T @ np.abs(np.asarray(W.w[t], np.float64))        # [n]
+        diff = np.abs(exact[t][okm] - approx[t][okm])
+        ok &= bool(np.all(diff <= bound * (1 + 1e-9) + 1e-12)) and bool(np.any(diff > 0))
+    return bool(ok)
+
 PINS = [pin_e2m1_printed_table, pin_e2m1_bitlevel, pin_e4m3_library, pin_e4m3_anchors,
         lambda: pin_golden("tiny_score_a.json"), lambda: pin_golden("tiny_score_ties.json"),
         lambda: pin_golden("tiny_score_shared.json"), pin_onehot_layout, pin_closed_form,
@@ -453,7 +563,8 @@ PINS = [pin_e2m1_printed_table, pin_e2m1_bitlevel, pin_e4m3_library, pin_e4m3_an
         pin_topk_bruteforce, pin_mask, pin_bad_inputs, pin_valid_lens_from_blocks,
         pin_gather_library, pin_gather_split_library, pin_pool_special_cases, pin_qprep_rows, pin_prefill_attn,
         pin_qsa_score_handcase,
-        pin_expand_blocks]
+        pin_expand_blocks, pin_nvfp4_q_golden, pin_e4m3_encode_library, pin_e2m1_encode_ties,
+        pin_nvfp4_q_invariants, pin_nvfp4_q_scores_bound]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: getattr(f, "__name__", "golden"))
@@ -560,6 +671,39 @@ def _mut_attn_kv_head_modulo(q, k_cache, v_cache, block_table, lists, first_pos,
     return np.stack(outs, axis=1), st
 
 
+def _mut_e4m3_encode_truncates(x):
+    grid = oracle.e4m3_decode(np.arange(0x7F))
+    return (np.searchsorted(grid, np.asarray(x, np.float64), side="right") - 1).clip(0, 0x7E).astype(np.uint8)
+
+
+def _mut_e2m1_ties_away(y):
+    y = np.asarray(y, np.float64)
+    mags = np.asarray(oracle.E2M1_MAGNITUDES)
+    d = np.abs(np.abs(y)[..., None] - mags)
+    best = d == d.min(-1, keepdims=True)
+    c = (best * np.arange(8)).max(-1)                       # the larger magnitude of a tie
+    return np.where((y < 0) & (c != 0), c | 8, c).astype(np.uint8)
+
+
+def _mut_quantize_groups_of_32(q):
+    """The same steps with one E4M3 scale per 32 elements (returned twice)."""
+    f32 = np.float32
+    x = np.asarray(q, np.float32)
+    lead = x.shape[:-1]
+    xg = x.reshape(lead + (4, 32))
+    amax = np.abs(x).max(-1)
+    gq = np.where(amax > 0, amax / f32(2688), f32(0)).astype(np.float32)
+    ag = np.abs(xg).max(-1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        s_f = np.where(ag > 0, (ag / (f32(6) * gq)[..., None]).astype(np.float32), f32(0))
+    sc = oracle.e4m3_encode(s_f)
+    sv = oracle.e4m3_decode(sc).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = (xg / (gq[..., None] * sv)[..., None]).astype(np.float32)
+    codes = np.where((sv > 0)[..., None], oracle.e2m1_encode(y), 0).astype(np.uint8)
+    return codes.reshape(lead + (128,)), np.repeat(sc, 2, -1), gq
+
+
 @pytest.mark.parametrize("name,target,fn", [
     *[(k, v[0], v[1]) for k, v in MUTATIONS.items()],
     ("qprep_ignores_first_pos", "qsa_qprep_rows", _mut_qprep_ignores_first_pos),
@@ -572,6 +716,10 @@ def _mut_attn_kv_head_modulo(q, k_cache, v_cache, block_table, lists, first_pos,
     ("group_of_8", "dequant_rows", _mut_group_by_8),
     ("block_and_slot_swapped", "resolve_slots", _mut_slot_swapped),
     ("ties_high_index_first", "topk_sorted", _mut_ties_high_index_first),
+    ("nvfp4_q_range_448", "NVFP4_Q_RANGE", 448.0),
+    ("e4m3_encode_truncates", "e4m3_encode", _mut_e4m3_encode_truncates),
+    ("e2m1_ties_away_from_zero", "e2m1_encode", _mut_e2m1_ties_away),
+    ("nvfp4_q_scale_per_32", "quantize_q_nvfp4", _mut_quantize_groups_of_32),
 ])
 def test_planted_mistake_is_caught(monkeypatch, name, target, fn):
     monkeypatch.setattr(oi, target, fn, raising=hasattr(oi, target) or not hasattr(oracle, target))
