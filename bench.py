@@ -125,23 +125,31 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def roofline(W, kern_s):
+# Dense FP4 (block-scaled) tensor rate over the bf16 rate, nominal: 13.5 / 2.25.
+FP4_OVER_BF16 = 6.0
+
+
+def roofline(W, kern_s, q_format="exact"):
     """Roofline of the scoring kernel (q preparation + scorer). Decode
     workloads stream every key once: HBM bound, 72.125 B per pair plus q, w
     and the length per query. Prefill shares 128 blocks of keys between 4096
     rows: the 2*H*D flops per pair on the tensor cores bound it (f16 runs at
-    the bf16 rate)."""
+    the bf16 rate; the NVFP4-q mode's FP4 MMA against the measured bf16 peak
+    times the nominal FP4/bf16 ratio)."""
     hbm, tensor, kind = peaks()
     if W.name == "prefill":
         flops = 2.0 * W.H * W.D * W.pairs
         achieved = flops / kern_s / 1e12
-        return {"bound": "tensor", "achieved": achieved, "peak": tensor, "unit": "TFLOP/s",
-                "frac": achieved / tensor, "traffic": None, "kernel": "score_tc_kernel",
-                "peak_kind": kind, "algorithmic_flops_per_launch": flops}
+        peak = tensor if q_format == "exact" else tensor * FP4_OVER_BF16
+        pk = kind if q_format == "exact" else f"{kind} bf16 x {FP4_OVER_BF16:g} (nominal FP4/bf16)"
+        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None, "kernel": "score_tc_kernel",
+                "peak_kind": pk, "algorithmic_flops_per_launch": flops}
     algo_bytes = W.pairs * BYTES_PER_PAIR + W.T * (4 * W.H * W.D + 4 * W.H + 4)
     achieved = algo_bytes / kern_s / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-            "traffic": recorded_traffic(W.name), "kernel": "score_tc_kernel", "peak_kind": kind,
+            "traffic": recorded_traffic(W.name) if q_format == "exact" else None, "kernel": "score_tc_kernel",
+            "peak_kind": kind,
             "algorithmic_bytes_per_launch": algo_bytes}
 
 
@@ -670,7 +678,9 @@ def main():
     ap.add_argument("--cpu-queries", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra-workloads", action="store_true",
-                    help="batched_decode only: skip the long-decode and prefill sub-records")
+                    help="batched_decode only: skip the long-decode, prefill and NVFP4-q sub-records")
+    ap.add_argument("--q-format", default="exact", choices=["exact", "nvfp4"],
+                    help="nvfp4: the opt-in mode scoring NVFP4-quantised queries on the FP4 MMA")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -704,18 +714,21 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     W = make_workload(args.workload, rank_seed(args.workload, rank))
-    rec = measure_score(W, args, args.steps, dev, flush, dist, e2e=True)
+    rec = measure_score(W, args, args.steps, dev, flush, dist, e2e=True, q_format=args.q_format)
     extra = {}
-    if args.workload == "batched_decode" and not args.no_extra_workloads:
+    if args.workload == "batched_decode" and not args.no_extra_workloads and args.q_format == "exact":
         # the other two full-size configurations, device-timed, same warm-up,
-        # at most EXTRA_STEPS timed steps each
+        # at most EXTRA_STEPS timed steps each; then the opt-in NVFP4-q mode
+        # on batched decode and prefill
         del W
-        for name in ("long_decode", "prefill"):
+        for name, qf in (("long_decode", "exact"), ("prefill", "exact"), ("batched_decode", "nvfp4"),
+                         ("prefill", "nvfp4")):
             W2 = make_workload(name, rank_seed(name, rank))
-            r2 = measure_score(W2, args, min(args.steps, EXTRA_STEPS), dev, flush, dist, e2e=False)
-            extra[name] = {"metric": METRIC, "value": r2["value"], "unit": UNIT, "steps": r2["steps"],
-                           "ms_per_step": r2["ms_per_step"], "config": workload_config(W2),
-                           "roofline": r2["roofline"], "clocks": r2["clocks"]}
+            r2 = measure_score(W2, args, min(args.steps, EXTRA_STEPS), dev, flush, dist, e2e=False, q_format=qf)
+            key = name if qf == "exact" else f"{name}_nvfp4_q"
+            extra[key] = {"metric": METRIC, "value": r2["value"], "unit": UNIT, "steps": r2["steps"],
+                          "ms_per_step": r2["ms_per_step"], "config": dict(workload_config(W2), q_format=qf),
+                          "roofline": r2["roofline"], "clocks": r2["clocks"]}
             del W2
             torch.cuda.empty_cache()
 
@@ -723,9 +736,14 @@ def main():
         line = {
             "metric": METRIC, "value": rec["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": rec["ms_per_step"], "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16" if args.q_format == "exact" else "e2m1",
+            "data": "synthetic",
             "config": dict(rec["config"], parallelism=f"replicas x{world} (independent batches)",
-                           mma="tcgen05 kind::f16, f16 x f16 -> f32 (exact for NVFP4 x bf16-valued q)"),
+                           q_format=args.q_format,
+                           mma=("tcgen05 kind::f16, f16 x f16 -> f32 (exact for NVFP4 x bf16-valued q)"
+                                if args.q_format == "exact" else
+                                "tcgen05 kind::mxf4nvf4 block-scaled, e2m1 x e2m1 with e4m3 group scales -> f32 "
+                                "(q quantised to NVFP4)")),
             "e2e": rec["e2e"],
             "gpu_launches": rec["gpu_launches"],
             "roofline": rec["roofline"],
@@ -743,7 +761,7 @@ def main():
 EXTRA_STEPS = 2000
 
 
-def measure_score(W, args, K, dev, flush, dist, e2e):
+def measure_score(W, args, K, dev, flush, dist, e2e, q_format="exact"):
     """Device-timed idx_score_topk steps over W (L2 flushed before each), and
     optionally the end-to-end leg through the public Python call."""
     import ctypes
@@ -767,7 +785,7 @@ def measure_score(W, args, K, dev, flush, dist, e2e):
     a = idx.make_score_args(q, w, bt, vl, k, entries_per_block=W.epb, bt_stride=W.bt_stride,
                             keys_fp4=fp4, key_scale=sc,
                             key_gscale=gs, topk_idx=out_i, topk_score=out_s, dev_status=status,
-                            path=args.path)
+                            path=args.path, q_format=q_format)
     ws_bytes = idx.score_topk_workspace_bytes(a)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
@@ -825,7 +843,7 @@ def measure_score(W, args, K, dev, flush, dist, e2e):
     value, t_total = whole_job(pairs_step, K, sum(step_ms) / 1e3, dist, dev)
     kern_s = statistics.mean(kern_ms) / 1e3
     rec = {"value": value, "steps": K, "ms_per_step": 1e3 * t_total / K, "config": workload_config(W),
-           "roofline": dict(roofline(W, kern_s), kernel_ms=1e3 * kern_s, kernel_timed_steps=len(kern_ms)),
+           "roofline": dict(roofline(W, kern_s, q_format), kernel_ms=1e3 * kern_s, kernel_timed_steps=len(kern_ms)),
            "clocks": clk.summary(), "wall_s": wall, "gpu_launches": launches_per_step(W) * K}
     if not e2e:
         return rec
@@ -864,7 +882,7 @@ def measure_score(W, args, K, dev, flush, dist, e2e):
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
         idx.score_topk(eq, ew, ebt, evl, k, entries_per_block=W.epb, bt_stride=W.bt_stride, keys_fp4=fp4,
-                       key_scale=sc, key_gscale=gs, out=(e_i, e_s), workspace=ws)
+                       key_scale=sc, key_gscale=gs, out=(e_i, e_s), workspace=ws, q_format=q_format)
         h_out.copy_(d_out, non_blocking=True)
 
     for _ in range(3):

@@ -54,6 +54,16 @@ typedef enum { IDX_KEYS_NVFP4 = 0, IDX_KEYS_F32 = 1 } idx_key_format_t;
  * NVFP4 keys and the CUDA-core path for F32 keys. */
 typedef enum { IDX_PATH_AUTO = 0, IDX_PATH_TENSOR = 1, IDX_PATH_SIMT = 2 } idx_path_t;
 
+/* How the queries enter the dot products. EXACT: q as given (float32; the
+ * tensor path is exact for q whose values are bf16). NVFP4 (opt-in, the
+ * FP4-MMA phase that the header comment of "indexer_score_topk.cu" plans):
+ * each head row of q is first quantised to NVFP4 exactly as
+ * idx_quantize_q_nvfp4 states, and the scores are those of the quantised
+ * queries, I[t,s] = sum_h w[t,h] * max(q_hat[t,h,:] . K[s,:], 0); the
+ * tensor cores then take keys and queries in FP4 directly (block-scaled MMA),
+ * with no decode of the keys. Tensor path and NVFP4 keys only, H <= 128. */
+typedef enum { IDX_Q_EXACT = 0, IDX_Q_NVFP4 = 1 } idx_q_format_t;
+
 /*
  * idx_score_topk — lightning-indexer scores and their top-k.
  *
@@ -110,6 +120,10 @@ typedef enum { IDX_PATH_AUTO = 0, IDX_PATH_TENSOR = 1, IDX_PATH_SIMT = 2 } idx_p
  *              alone. The second record keeps the selection kernel from
  *              launching early under the scorer's tail, which lengthens
  *              that call by a few microseconds.
+ *   q_format   idx_q_format_t (0, the zero-initialised default, is EXACT).
+ *              NVFP4 with F32 keys, the CUDA-core path or H > 128 gives
+ *              IDX_ERR_UNSUPPORTED; in that mode the key scale bytes are
+ *              read as unsigned E4M3 (their sign bit must be clear).
  * Device-side errors: a table entry outside [0,P) drops that block's keys
  * (IDX_STATUS_BAD_BLOCK); a valid length outside [0, max_logical_blocks*epb]
  * pads that query's whole output (IDX_STATUS_BAD_LEN).
@@ -139,6 +153,7 @@ typedef struct {
   int32_t path;     /* idx_path_t */
   int32_t num_ctas; /* 0 = one per SM of the current device */
   void *timing_events[2];
+  int32_t q_format; /* idx_q_format_t */
 } idx_score_topk_args;
 
 /* Bytes of workspace idx_score_topk needs for these arguments (host only; no
@@ -171,6 +186,31 @@ idx_status_t idx_score_topk(const idx_score_topk_args *args, idx_stream_t stream
  */
 #define IDX_STATIC_SCRATCH_BYTES (8u << 20)
 idx_status_t idx_score_topk_static(const idx_score_topk_args *args, idx_stream_t stream);
+
+/*
+ * idx_quantize_q_nvfp4 — the query quantisation of the NVFP4 q_format.
+ *
+ * The NVFP4 scheme of the keys ("FP4 dequantization (NVFP4 scheme)" section of
+ * "indexer_score_topk.cu": E2M1 elements, one FP8 E4M3 scale per 16 elements)
+ * plus one float32 scale per row that maps the row's largest |x| onto
+ * 6 * 448 = 2688. For each row x of 128 values, with every operation one
+ * float32 operation rounded to nearest:
+ *     amax = max |x|;     gq = amax / 2688             (0 when amax == 0)
+ *     group g of 16:      s_g = E4M3(ag / (6 * gq))    (ag: the group's max |x|)
+ *     element d:          c_d = E2M1(x_d / (gq * s_g)), 0 when s_g == 0
+ * E4M3() and E2M1() round to the nearest representable value, ties to the
+ * even code, saturating at 448 and 6; a value rounding to zero gets code 0.
+ * The row dequantises to gq * s_g * e2m1(c_d). q finite; rows whose largest
+ * |x| is below 1e-30 are outside the contract (gq * s_g may underflow).
+ *   q       device [rows, 128] float32, 16-byte aligned
+ *   codes   device [rows, 64] uint8 (output): element 2j in the low nibble of
+ *           byte j, E2M1 magnitude bits 0-2, sign bit 3
+ *   scales  device [rows, 8] uint8 (output), E4M3
+ *   gscale  device [rows] float32 (output)
+ * Returns IDX_ERR_INVALID_ARG for rows < 0, a null or misaligned pointer.
+ */
+idx_status_t idx_quantize_q_nvfp4(const float *q, int64_t rows, uint8_t *codes, uint8_t *scales, float *gscale,
+                                  idx_stream_t stream);
 
 /*
  * idx_gather_kv — copy selected rows of a paged K/V cache into a dense tile.

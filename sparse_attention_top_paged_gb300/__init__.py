@@ -73,8 +73,9 @@ def _workspace(device, nbytes):
 def make_score_args(q, w, block_table, valid_lens, top_k, *, entries_per_block, keys_fp4=None,
                     key_scale=None, key_gscale=None, keys_f32=None, bt_stride=None,
                     topk_idx=None, topk_score=None, scores_out=None, dev_status=None,
-                    path="auto", num_ctas=0):
-    """Build an ``idx_score_topk_args`` from torch tensors (no device work)."""
+                    path="auto", num_ctas=0, q_format="exact"):
+    """Build an ``idx_score_topk_args`` from torch tensors (no device work).
+    ``q_format="nvfp4"`` selects the opt-in NVFP4 query mode."""
     torch = _torch()
     _check(q, "q", torch.float32, 3)
     _check(w, "w", torch.float32, 2)
@@ -115,15 +116,18 @@ def make_score_args(q, w, block_table, valid_lens, top_k, *, entries_per_block, 
         a.dev_status = dev_status.data_ptr()
     a.path = PATHS[path]
     a.num_ctas = num_ctas
+    a.q_format = _lib.Q_FORMATS[q_format]
     return a
 
 
 def score_topk(q, w, block_table, valid_lens, top_k, *, entries_per_block, keys_fp4=None,
                key_scale=None, key_gscale=None, keys_f32=None, bt_stride=None, scores_out=None,
-               dev_status=None, path="auto", num_ctas=0, out=None, workspace=None):
+               dev_status=None, path="auto", num_ctas=0, out=None, workspace=None, q_format="exact"):
     """Top-k lightning-indexer keys per query: ``(topk_idx [T,k] int32,
     topk_score [T,k] float32)``. ``bt_stride=0`` shares table row 0 across
-    queries. ``scores_out`` (``[T, ld]`` float32) also receives every score."""
+    queries. ``scores_out`` (``[T, ld]`` float32) also receives every score.
+    ``q_format="nvfp4"``: score with q quantised to NVFP4 (opt-in; see
+    :func:`quantize_q_nvfp4`)."""
     torch = _torch()
     T = q.shape[0]
     if out is None:
@@ -135,7 +139,7 @@ def score_topk(q, w, block_table, valid_lens, top_k, *, entries_per_block, keys_
                         keys_fp4=keys_fp4, key_scale=key_scale, key_gscale=key_gscale,
                         keys_f32=keys_f32, bt_stride=bt_stride, topk_idx=topk_idx,
                         topk_score=topk_score, scores_out=scores_out, dev_status=dev_status,
-                        path=path, num_ctas=num_ctas)
+                        path=path, num_ctas=num_ctas, q_format=q_format)
     lib = load_library()
     with torch.cuda.device(q.device):
         need = ctypes.c_size_t(0)
@@ -145,6 +149,26 @@ def score_topk(q, w, block_table, valid_lens, top_k, *, entries_per_block, keys_
         a.workspace_bytes = ws.numel() * ws.element_size()
         _raise("idx_score_topk", lib.idx_score_topk(ctypes.byref(a), _stream(q.device)))
     return topk_idx, topk_score
+
+
+def quantize_q_nvfp4(q):
+    """The NVFP4 query quantisation of ``q_format="nvfp4"`` on its own:
+    ``q [..., 128]`` float32 -> ``(codes [..., 64] uint8, scales [..., 8]
+    uint8 E4M3, gscale [...] float32)``; codes pack element 2j in the low
+    nibble of byte j."""
+    torch = _torch()
+    if q.dtype != torch.float32 or q.shape[-1] != 128 or not q.is_cuda:
+        raise ValueError("q must be a CUDA float32 tensor with a last dimension of 128")
+    q = q.contiguous()
+    lead = tuple(q.shape[:-1])
+    rows = q.numel() // 128
+    codes = torch.empty(lead + (64,), dtype=torch.uint8, device=q.device)
+    scales = torch.empty(lead + (8,), dtype=torch.uint8, device=q.device)
+    gscale = torch.empty(lead, dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        _raise("idx_quantize_q_nvfp4", load_library().idx_quantize_q_nvfp4(
+            q.data_ptr(), rows, codes.data_ptr(), scales.data_ptr(), gscale.data_ptr(), _stream(q.device)))
+    return codes, scales, gscale
 
 
 def score_topk_workspace_bytes(args) -> int:

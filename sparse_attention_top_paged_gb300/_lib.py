@@ -19,6 +19,7 @@ STATUS_NAMES = {0: "IDX_OK", 1: "IDX_ERR_INVALID_ARG", 2: "IDX_ERR_UNSUPPORTED",
                 3: "IDX_ERR_WORKSPACE_TOO_SMALL", 4: "IDX_ERR_CUDA"}
 KEYS_NVFP4, KEYS_F32 = 0, 1
 PATHS = {"auto": 0, "tensor": 1, "simt": 2}
+Q_FORMATS = {"exact": 0, "nvfp4": 1}
 STATUS_BAD_BLOCK, STATUS_BAD_LEN, STATUS_BAD_SEL, STATUS_TIMEOUT, STATUS_DEBUG_BOUNDS = 1, 2, 4, 8, 16
 STATIC_SCRATCH_BYTES = 8 << 20
 
@@ -43,6 +44,7 @@ class ScoreTopkArgs(ctypes.Structure):
         ("workspace", c_vp), ("workspace_bytes", c_size),
         ("path", c_i32), ("num_ctas", c_i32),
         ("timing_events", c_vp * 2),
+        ("q_format", c_i32),
     ]
 
 
@@ -100,6 +102,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.idx_score_topk.restype = c_i32
         lib.idx_score_topk_static.argtypes = [P(ScoreTopkArgs), c_vp]
         lib.idx_score_topk_static.restype = c_i32
+        lib.idx_quantize_q_nvfp4.argtypes = [c_vp, c_i64, c_vp, c_vp, c_vp, c_vp]
+        lib.idx_quantize_q_nvfp4.restype = c_i32
         lib.idx_gather_kv.argtypes = [P(GatherKvArgs), c_vp]
         lib.idx_gather_kv.restype = c_i32
         lib.idx_gather_split.argtypes = [P(GatherSplitArgs), c_vp]

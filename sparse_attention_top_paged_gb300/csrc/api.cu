@@ -57,6 +57,7 @@ idx_status_t resolve(const idx_score_topk_args *a, Resolved *r) {
   if (a->path != IDX_PATH_AUTO && a->path != IDX_PATH_TENSOR && a->path != IDX_PATH_SIMT)
     return IDX_ERR_INVALID_ARG;
   if (a->num_ctas < 0) return IDX_ERR_INVALID_ARG;
+  if (a->q_format != IDX_Q_EXACT && a->q_format != IDX_Q_NVFP4) return IDX_ERR_INVALID_ARG;
   const long long max_len = static_cast<long long>(a->max_logical_blocks) * a->entries_per_block;
   if (max_len > 0x7FFFFFFFLL) return IDX_ERR_INVALID_ARG;
   const bool f32 = a->key_format == IDX_KEYS_F32;
@@ -93,6 +94,8 @@ idx_status_t resolve(const idx_score_topk_args *a, Resolved *r) {
   else
     plan = f32 ? Plan::kSimt : Plan::kTensor;
   if (plan == Plan::kTensor && f32) return IDX_ERR_UNSUPPORTED;
+  const bool nvfp4_q = a->q_format == IDX_Q_NVFP4;
+  if (nvfp4_q && (plan != Plan::kTensor || a->H > 128)) return IDX_ERR_UNSUPPORTED;
 
   ScoreParams &p = r->p;
   p.T = a->T; p.H = a->H; p.D = a->D;
@@ -105,9 +108,11 @@ idx_status_t resolve(const idx_score_topk_args *a, Resolved *r) {
   p.topk_idx = a->topk_idx; p.topk_score = a->topk_score;
   p.scores_out = a->scores_out; p.ld_scores = a->ld_scores;
   p.dev_status = a->dev_status;
+  p.q_format = a->q_format;
 
   if (plan == Plan::kTensor && !score_tc_supported(p)) {
-    if (a->path == IDX_PATH_TENSOR) return IDX_ERR_UNSUPPORTED;
+    // (the NVFP4 q mode has no CUDA-core counterpart: never a silent fallback)
+    if (a->path == IDX_PATH_TENSOR || nvfp4_q) return IDX_ERR_UNSUPPORTED;
     plan = Plan::kSimt;
   }
   r->plan = plan;
@@ -179,6 +184,18 @@ idx_status_t idx_score_topk(const idx_score_topk_args *args, idx_stream_t stream
                              : nullptr;
   if (e == cudaSuccess) e = launch_select(r.p, scores, r.sel.ld, hist, r.sel, args->workspace, s);
   return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
+idx_status_t idx_quantize_q_nvfp4(const float *q, int64_t rows, uint8_t *codes, uint8_t *scales, float *gscale,
+                                  idx_stream_t stream) {
+  if (rows < 0) return IDX_ERR_INVALID_ARG;
+  if (rows == 0) return IDX_OK;
+  if (!q || !codes || !scales || !gscale || !aligned(q, 16) || !aligned(codes, 2) || !aligned(gscale, 4))
+    return IDX_ERR_INVALID_ARG;
+  return launch_quantize_q_nvfp4(q, rows, codes, scales, gscale, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? IDX_OK
+             : IDX_ERR_CUDA;
 }
 
 idx_status_t idx_gather_kv(const idx_gather_kv_args *a, idx_stream_t stream) {

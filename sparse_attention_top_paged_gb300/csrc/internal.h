@@ -28,6 +28,7 @@ struct ScoreParams {
   float *scores_out;
   long long ld_scores;
   int32_t *dev_status;
+  int q_format;   // idx_q_format_t
 };
 
 // How TopK(I[t,:], k) is taken from the [T, ld] score matrix: one streaming
@@ -68,6 +69,9 @@ size_t score_tc_workspace(const ScoreParams &p);  // per-query q records (bytes)
 constexpr int kScoreBins = 4096;
 cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint32_t *hist, uint32_t *cand_cnt,
                             float *scores, long long ld, cudaStream_t stream);
+// The NVFP4 query quantisation of the NVFP4-q mode, for `rows` head rows of 128.
+cudaError_t launch_quantize_q_nvfp4(const float *q, long long rows, uint8_t *codes, uint8_t *scales, float *gscale,
+                                    cudaStream_t stream);
 // gather_pool.cu
 cudaError_t launch_gather_kv(const idx_gather_kv_args &a, cudaStream_t stream);
 cudaError_t launch_block_pool(const uint16_t *raw, const float *w, float *out, uint32_t first_block,

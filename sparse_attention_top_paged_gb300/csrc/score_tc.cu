@@ -47,6 +47,16 @@
 // Products e2m1 * e4m3 are exact in f16, and bf16-valued q is exact in the
 // scaled f16 hi part, so a single MMA pass computes the dot products with f32
 // accumulation only; full-precision f32 q takes the second (lo) pass.
+//
+// NVFP4-q mode (opt-in, the FP4-MMA phase that page's header comment plans):
+// qprep quantises each head of q to NVFP4 (nvfp4q.cuh) and the MMA is
+// tcgen05.mma kind::mxf4nvf4, which reads the keys' packed E2M1 nibbles
+// straight from the TMA stage and the q codes from the record, with the E4M3
+// group scales of both from tensor memory: nothing is decoded. The decoder
+// warps only copy each tile's key scales and the segment's q scales into the
+// tile's tensor-memory scale slot; the per-head float32 scale gq is folded
+// into w' (relu(gq a) = gq relu(a), gq >= 0). The stage is handed back when
+// the tile's MMAs complete.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -55,6 +65,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "nvfp4q.cuh"
 #include "tc_ptx.cuh"
 
 namespace idx {
@@ -104,9 +115,15 @@ static_assert(sizeof(MetaEntry) == 128, "meta entry");
 // (each NR = R Npad head rows x 128 dims, K-major, 128-byte swizzled), w' (NR
 // floats), lo flags (NR ints). Head row n holds head n % Npad of row
 // R * group + n / Npad.
+// NVFP4-q records instead hold the E2M1 codes (NR rows x 64 bytes, K-major,
+// 64-byte swizzled), then the E4M3 group scales as 1 KB of 32-bit words laid
+// out for the tensor-memory scale slot (word (c * 4 + j) * 32 + l: the four
+// scales of K step c of head row l + 32 j; zero past NR), then w' = w gq.
 struct TcLayout {
   int Npad, R, NR, nq, nseg, na, nd, ne, ns, box_rows, bpt, epb_shift;
-  uint32_t b_bytes, rec_w, rec_flags, rec_bytes, rec_smem;
+  int fp4;          // NVFP4-q mode
+  uint32_t a_cols;  // tensor-memory columns per A slot (decoded keys; or the scale slot)
+  uint32_t b_bytes, sfb_off, rec_w, rec_flags, rec_bytes, rec_smem;
   uint32_t off_b, off_raw, off_meta, off_bar, off_misc;
   uint32_t smem_bytes;
 };
@@ -220,14 +237,36 @@ __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay,
   }
   const int n = blockIdx.y * 8 + static_cast<int>(threadIdx.x >> 5);   // head row of the record
   const int lane = threadIdx.x & 31;
+  uint8_t *r = rec + static_cast<size_t>(tq) * lay.rec_bytes;
+  if (lay.fp4 && blockIdx.y == 0) {   // scale words of head rows NR .. 127 stay zero
+    uint32_t *sw = reinterpret_cast<uint32_t *>(r + lay.sfb_off);
+    for (int i = threadIdx.x; i < 256; i += blockDim.x)
+      if (((i >> 5) & 3) * 32 >= lay.NR) sw[i] = 0u;
+  }
   if (n >= lay.NR) return;
   const int h = n % lay.Npad, t = tq * lay.R + n / lay.Npad;
-  uint8_t *r = rec + static_cast<size_t>(tq) * lay.rec_bytes;
   float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
   float wv = 0.0f;
   if (h < p.H && t < p.T) {
     x = reinterpret_cast<const float4 *>(p.q + (static_cast<long long>(t) * p.H + h) * 128)[lane];
     wv = p.w[static_cast<long long>(t) * p.H + h];
+  }
+  if (lay.fp4) {
+    uint32_t codes16, scale;
+    float gq;
+    nvfp4_quantize_lane(x, codes16, scale, gq);
+    // codes: bytes 2 lane, 2 lane + 1 of head row n (64 bytes, 64-byte swizzle in 8-row groups)
+    const uint32_t off = (n >> 3) * 512 + (n & 7) * 64 + ((((lane >> 3) ^ ((n >> 1) & 3)) & 3) * 16) + ((2 * lane) & 15);
+    *reinterpret_cast<uint16_t *>(r + off) = static_cast<uint16_t>(codes16);
+    if ((lane & 3) == 0) {   // scale of group g = lane / 4: K step g / 4, byte g % 4 of its word
+      const int g = lane >> 2;
+      r[lay.sfb_off + (((g >> 2) * 4 + (n >> 5)) * 32 + (n & 31)) * 4 + (g & 3)] = static_cast<uint8_t>(scale);
+    }
+    if (lane == 0) {
+      reinterpret_cast<float *>(r + lay.rec_w)[n] = __fmul_rn(wv, gq);
+      reinterpret_cast<int *>(r + lay.rec_flags)[n] = 0;
+    }
+    return;
   }
   float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
 #pragma unroll
@@ -263,7 +302,7 @@ __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay,
   }
 }
 
-template <int kRows>
+template <int kRows, bool kFp4>
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmap_nib, ScoreParams p, TcLayout lay,
                     const uint8_t *__restrict__ qrec, uint32_t *__restrict__ hist, float *__restrict__ scores,
@@ -280,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::launch_dependents();  // the selection kernel may be scheduled as CTAs of this one finish
     for (int s = 0; s < lay.ns; ++s) {
       ptx::mbar_init(bar(B_FULL_RAW + s), 1);
-      ptx::mbar_init(bar(B_EMPTY_RAW + s), kDecWarps);
+      ptx::mbar_init(bar(B_EMPTY_RAW + s), kFp4 ? 1 : kDecWarps);   // decoders, or the MMA commit
     }
     for (int a = 0; a < kMaxSlots; ++a) {
       ptx::mbar_init(bar(B_FULL_A + a), kDecWarps);
@@ -367,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sB = sm + lay.off_b;
   uint8_t *sRaw = sm + lay.off_raw;
   MetaEntry *sMeta = reinterpret_cast<MetaEntry *>(sm + lay.off_meta);
-  const uint32_t tmem_a = tmem;                                  // A slots: 64 columns each
-  const uint32_t tmem_d = tmem + 64u * static_cast<uint32_t>(na);  // D slots: NR columns each
+  const uint32_t tmem_a = tmem;                                        // A slots: a_cols columns each
+  const uint32_t tmem_d = tmem + lay.a_cols * static_cast<uint32_t>(na);  // D slots: NR columns each
 
   if (warp == 0) {
     // ================================================================ producer
@@ -495,10 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // but tcgen05.mma instructions.
     Walker<kRows> w;
     w.init(p, lay, t0, j0);
-    const uint32_t idesc = ptx::idesc_f16_f32(128, NR);
+    const uint32_t idesc = kFp4 ? ptx::idesc_mxf4nvf4(128, NR) : ptx::idesc_f16_f32(128, NR);
     bool need_lo = false;
     uint64_t bdh[8], bdl[8];
-    Ring ra, rd, rs;
+    Ring ra, rd, rs, rraw;
     rs.idx = -1;  // advanced at each segment start
     int ss = 0;
     bool any_mma = false;
@@ -508,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // whole CTA takes the abort-and-drain path.
     if (blockIdx.x == 0) ptx::mbar_wait(bar(B_NEVER), 0u, abort_flag, kTimeoutNs);
 #endif
-    for (int i = 0; i < n_tiles; ++i, w.next(p, lay), ra.next(na), rd.next(nd)) {
+    for (int i = 0; i < n_tiles; ++i, w.next(p, lay), ra.next(na), rd.next(nd), rraw.next(lay.ns)) {
       const bool seg_start = (i == 0) || (w.j == 0);
       const bool seg_end = (i == n_tiles - 1) || (w.j == w.nt - 1);
       bool ok = true;
@@ -517,34 +556,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         ss = rs.idx;
         ok = ptx::mbar_wait(bar(B_SEG_FULL + ss), rs.phase, abort_flag, kTimeoutNs);
         const uint8_t *slot = sB + ss * lay.rec_smem;
-        const int *flags = reinterpret_cast<const int *>(slot + lay.rec_flags);
-        int f = 0;
-        for (int h = lane; h < NR; h += 32) f |= flags[h];
-        need_lo = __any_sync(0xFFFFFFFFu, f != 0);
-        const uint32_t bh = ptx::smem_addr(slot);
-        const uint32_t bl = ptx::smem_addr(slot + b_bytes);
+        if constexpr (kFp4) {   // q codes: K steps of 64 elements = 32 bytes into each 64-byte row
+          bdh[0] = ptx::sdesc_sw64(ptx::smem_addr(slot));
+          bdh[1] = ptx::sdesc_sw64(ptx::smem_addr(slot) + 32);
+        } else {
+          const int *flags = reinterpret_cast<const int *>(slot + lay.rec_flags);
+          int f = 0;
+          for (int h = lane; h < NR; h += 32) f |= flags[h];
+          need_lo = __any_sync(0xFFFFFFFFu, f != 0);
+          const uint32_t bh = ptx::smem_addr(slot);
+          const uint32_t bl = ptx::smem_addr(slot + b_bytes);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t boff = (k >> 2) * (NR * 128) + (k & 3) * 32;
-          bdh[k] = ptx::sdesc_sw128(bh + boff);
-          bdl[k] = ptx::sdesc_sw128(bl + boff);
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t boff = (k >> 2) * (NR * 128) + (k & 3) * 32;
+            bdh[k] = ptx::sdesc_sw128(bh + boff);
+            bdl[k] = ptx::sdesc_sw128(bl + boff);
+          }
         }
       }
-      const int a = ra.idx, d = rd.idx;
+      const int a = ra.idx, d = rd.idx, s = rraw.idx;
       ok = ok && ptx::mbar_wait(bar(B_FULL_A + a), ra.phase, abort_flag, kTimeoutNs);
       ok = ok && ptx::mbar_wait(bar(B_EMPTY_D + d), rd.phase ^ 1u, abort_flag, kTimeoutNs);
+      // NVFP4-q: the MMA reads the stage itself (the decoders waited for it too)
+      if (kFp4) ok = ok && ptx::mbar_wait(bar(B_FULL_RAW + s), rraw.phase, abort_flag, kTimeoutNs);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       ptx::tc_fence_after();
-      const uint32_t dt = tmem_d + d * NR, at = tmem_a + a * 64;
+      const uint32_t dt = tmem_d + d * NR, at = tmem_a + a * lay.a_cols;
       if (ptx::elect_one()) {
+        if constexpr (kFp4) {
+          // A: the stage's 128 key rows of 64 bytes; scale slot: key scales
+          // (columns 0-7), q scales (8-15), four columns per K step
+          const uint32_t sa = ptx::smem_addr(sRaw + static_cast<size_t>(s) * kStageBytes);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ptx::mma_ts_f16(dt, at + 8 * k, bdh[k], idesc, k > 0 ? 1u : 0u);
-        if (need_lo) {
+          for (int c = 0; c < 2; ++c)
+            ptx::mma_ss_nvf4(dt, ptx::sdesc_sw64(sa + 32 * c), bdh[c], idesc, at + 4 * c, at + 8 + 4 * c,
+                             c > 0 ? 1u : 0u);
+        } else {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) ptx::mma_ts_f16(dt, at + 8 * k, bdl[k], idesc, 1u);
+          for (int k = 0; k < 8; ++k) ptx::mma_ts_f16(dt, at + 8 * k, bdh[k], idesc, k > 0 ? 1u : 0u);
+          if (need_lo) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) ptx::mma_ts_f16(dt, at + 8 * k, bdl[k], idesc, 1u);
+          }
         }
         ptx::mma_commit(bar(B_EMPTY_A + a));
         ptx::mma_commit(bar(B_FULL_D + d));
+        if (kFp4) ptx::mma_commit(bar(B_EMPTY_RAW + s));
         if (seg_end) ptx::mma_commit(bar(B_SEG_BFREE + ss));
       }
       __syncwarp();
@@ -560,47 +617,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kEpiWarp0) {
     // ============================================================== decoders
-    const int row = 32 * (warp & 3) + lane;    // the TMEM lane this thread writes
-    const int rsw = (row >> 1) & 3;            // 64-byte swizzle of this row's chunks
-    constexpr int kHalves = 8 / kDecWarps;     // 64-element halves of the row per warp
-    const int half0 = (kDecWarps == 8) ? ((warp - 2) >> 2) : 0;
-    Ring rraw, ra;
-    for (int i = 0; i < n_tiles; ++i, rraw.next(lay.ns), ra.next(na)) {
-      const int s = rraw.idx, a = ra.idx;
-      bool ok = ptx::mbar_wait(bar(B_FULL_RAW + s), rraw.phase, abort_flag, kTimeoutNs);
-      ok = ok && ptx::mbar_wait(bar(B_EMPTY_A + a), ra.phase ^ 1u, abort_flag, kTimeoutNs);
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      ptx::tc_fence_after();
-      const uint8_t *stage = sRaw + static_cast<size_t>(s) * kStageBytes;
-      const uint2 scw = *reinterpret_cast<const uint2 *>(stage + kScaleOff + row * 8);
-      const uint32_t taddr = tmem_a + a * 64 + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-#pragma unroll
-      for (int hh = 0; hh < kHalves; ++hh) {
-        const int half = half0 + hh;
-        uint32_t v[32];
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = half * 2 + cc;  // 16-byte chunk: elements 32c .. 32c+31, groups 2c, 2c+1
-          const uint4 raw = *reinterpret_cast<const uint4 *>(stage + row * 64 + ((c ^ rsw) * 16));
-          const uint32_t sc2 = ptx::e4m3x2_to_f16x2(((c < 2 ? scw.x : scw.y) >> (16 * (c & 1))) & 0xFFFFu);
-          const uint32_t s_lo = __byte_perm(sc2, 0, 0x1010), s_hi = __byte_perm(sc2, 0, 0x3232);
-          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t e[4];
-            ptx::e2m1x8_to_f16x2x4(wv[q4], e);
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb) v[cc * 16 + q4 * 4 + bb] = ptx::hmul2(e[bb], q4 < 2 ? s_lo : s_hi);
-          }
+    if constexpr (kFp4) {
+      // NVFP4-q: nothing to decode. Each tile's key scales (from the stage) and
+      // its segment's q scales (from the record) go into the tile's
+      // tensor-memory scale slot: word j of K step c holds the four scales of
+      // row lane + 32 j, columns 4c + j (keys) and 8 + 4c + j (q). Every warp
+      // writes the same words into its own 32-lane quarter.
+      const uint32_t lane_q = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+      Walker<kRows> w;
+      w.init(p, lay, t0, j0);
+      Ring rraw, ra, rs;
+      int ss = 0;
+      for (int i = 0; i < n_tiles; ++i, w.next(p, lay), rraw.next(lay.ns), ra.next(na)) {
+        const int s = rraw.idx, a = ra.idx;
+        bool ok = true;
+        if (i == 0 || w.j == 0) {
+          if (i > 0) rs.next(nseg);
+          ss = rs.idx;
+          ok = ptx::mbar_wait(bar(B_SEG_FULL + ss), rs.phase, abort_flag, kTimeoutNs);
         }
-        ptx::tmem_st32(taddr + half * 32, v);
+        ok = ok && ptx::mbar_wait(bar(B_FULL_RAW + s), rraw.phase, abort_flag, kTimeoutNs);
+        ok = ok && ptx::mbar_wait(bar(B_EMPTY_A + a), ra.phase ^ 1u, abort_flag, kTimeoutNs);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+        ptx::tc_fence_after();
+        const uint8_t *stage = sRaw + static_cast<size_t>(s) * kStageBytes;
+        const uint32_t *qs = reinterpret_cast<const uint32_t *>(sB + ss * lay.rec_smem + lay.sfb_off);
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint2 sc = *reinterpret_cast<const uint2 *>(stage + kScaleOff + (lane + 32 * j) * 8);
+          v[j] = sc.x;       // K step 0: groups 0-3 of key row lane + 32 j
+          v[4 + j] = sc.y;   // K step 1: groups 4-7
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[8 + k] = qs[k * 32 + lane];
+        ptx::tmem_st16(tmem_a + a * lay.a_cols + lane_q, v);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(B_FULL_A + a));
       }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(bar(B_FULL_A + a));
-        ptx::mbar_arrive(bar(B_EMPTY_RAW + s));
+    } else {
+      const int row = 32 * (warp & 3) + lane;    // the TMEM lane this thread writes
+      const int rsw = (row >> 1) & 3;            // 64-byte swizzle of this row's chunks
+      constexpr int kHalves = 8 / kDecWarps;     // 64-element halves of the row per warp
+      const int half0 = (kDecWarps == 8) ? ((warp - 2) >> 2) : 0;
+      Ring rraw, ra;
+      for (int i = 0; i < n_tiles; ++i, rraw.next(lay.ns), ra.next(na)) {
+        const int s = rraw.idx, a = ra.idx;
+        bool ok = ptx::mbar_wait(bar(B_FULL_RAW + s), rraw.phase, abort_flag, kTimeoutNs);
+        ok = ok && ptx::mbar_wait(bar(B_EMPTY_A + a), ra.phase ^ 1u, abort_flag, kTimeoutNs);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+        ptx::tc_fence_after();
+        const uint8_t *stage = sRaw + static_cast<size_t>(s) * kStageBytes;
+        const uint2 scw = *reinterpret_cast<const uint2 *>(stage + kScaleOff + row * 8);
+        const uint32_t taddr = tmem_a + a * 64 + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+#pragma unroll
+        for (int hh = 0; hh < kHalves; ++hh) {
+          const int half = half0 + hh;
+          uint32_t v[32];
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = half * 2 + cc;  // 16-byte chunk: elements 32c .. 32c+31, groups 2c, 2c+1
+            const uint4 raw = *reinterpret_cast<const uint4 *>(stage + row * 64 + ((c ^ rsw) * 16));
+            const uint32_t sc2 = ptx::e4m3x2_to_f16x2(((c < 2 ? scw.x : scw.y) >> (16 * (c & 1))) & 0xFFFFu);
+            const uint32_t s_lo = __byte_perm(sc2, 0, 0x1010), s_hi = __byte_perm(sc2, 0, 0x3232);
+            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t e[4];
+              ptx::e2m1x8_to_f16x2x4(wv[q4], e);
+#pragma unroll
+              for (int bb = 0; bb < 4; ++bb) v[cc * 16 + q4 * 4 + bb] = ptx::hmul2(e[bb], q4 < 2 ? s_lo : s_hi);
+            }
+          }
+          ptx::tmem_st32(taddr + half * 32, v);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(bar(B_FULL_A + a));
+          ptx::mbar_arrive(bar(B_EMPTY_RAW + s));
+        }
       }
     }
   } else if (warp == kResolverWarp) {
@@ -799,6 +898,13 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   TcLayout l{};
   l.Npad = round_up(p.H, 32);
   if (l.Npad > 256) return false;
+  l.fp4 = (p.q_format == IDX_Q_NVFP4) ? 1 : 0;
+  if (l.fp4) {
+    // head rows in multiples of 64 (MMA N of 64 or 128); the q scale slot
+    // covers 128 head rows
+    l.Npad = round_up(p.H, 64);
+    if (l.Npad > 128) return false;
+  }
   // Row pairs share one decoded key tile (one MMA of N = 2 Npad) when every
   // row reads the same block table.
   l.R = (p.bt_stride == 0 && p.T >= 2 && l.Npad <= 64) ? 2 : 1;
@@ -808,8 +914,10 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   // Tensor memory (512 columns): na A slots of 64 columns (128 keys x 128 f16)
   // and nd D slots of Npad columns (128 keys x Npad f32 accumulators); more
   // slots let the decoders, the MMA and the epilogue run further apart.
-  l.na = (l.NR <= 64) ? 4 : 2;
-  l.nd = (512 - 64 * l.na) / l.NR;
+  // NVFP4-q: an A slot holds only the tile's scale factors (16 columns).
+  l.a_cols = l.fp4 ? 16u : 64u;
+  l.na = (l.fp4 || l.NR <= 64) ? 4 : 2;
+  l.nd = (512 - static_cast<int>(l.a_cols) * l.na) / l.NR;
   if (l.nd > kMaxSlots) l.nd = kMaxSlots;
   if (l.nd < 1) return false;
   // Epilogue groups in use: at most one per D slot. A group waits for the D
@@ -824,8 +932,15 @@ bool make_layout(const ScoreParams &p, TcLayout *out) {
   while ((1 << l.epb_shift) < p.epb) ++l.epb_shift;
   // B-operand records first (1 KB-aligned slots), then the raw stages (1 KB
   // multiples, as many as fit), then the small tables.
-  l.b_bytes = static_cast<uint32_t>(l.NR) * 256u;
-  l.rec_w = 2u * l.b_bytes;
+  if (l.fp4) {
+    l.b_bytes = static_cast<uint32_t>(l.NR) * 64u;   // E2M1 codes
+    l.sfb_off = l.b_bytes;                         // then 1 KB of scale words
+    l.rec_w = l.sfb_off + 1024u;
+  } else {
+    l.b_bytes = static_cast<uint32_t>(l.NR) * 256u;
+    l.sfb_off = 0;
+    l.rec_w = 2u * l.b_bytes;
+  }
   l.rec_flags = l.rec_w + static_cast<uint32_t>(l.NR) * 4u;
   l.rec_bytes = (l.rec_flags + static_cast<uint32_t>(l.NR) * 4u + 127u) & ~127u;
   l.rec_smem = (l.rec_bytes + 1023u) & ~1023u;
@@ -883,7 +998,8 @@ cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
   void (*kern)(const CUtensorMap, ScoreParams, TcLayout, const uint8_t *, uint32_t *, float *, long long) =
-      (lay.R == 2) ? score_tc_kernel<2> : score_tc_kernel<1>;
+      lay.fp4 ? ((lay.R == 2) ? score_tc_kernel<2, true> : score_tc_kernel<1, true>)
+              : ((lay.R == 2) ? score_tc_kernel<2, false> : score_tc_kernel<1, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(lay.smem_bytes));
   if (e != cudaSuccess) return e;
@@ -904,6 +1020,37 @@ cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, tmap, p, lay, static_cast<const uint8_t *>(rec), hist, scores, ld);
+}
+
+namespace {
+
+// The NVFP4-q mode's quantisation on its own, one warp per head row of 128:
+// codes [rows, 64] bytes (low nibble = even element), scales [rows, 8] E4M3,
+// gscale [rows] float32.
+__global__ void __launch_bounds__(256) quantize_q_kernel(const float *__restrict__ q, long long rows,
+                                                         uint8_t *__restrict__ codes, uint8_t *__restrict__ scales,
+                                                         float *__restrict__ gscale) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;   // whole warps
+  const float4 x = reinterpret_cast<const float4 *>(q + row * 128)[lane];
+  uint32_t c16, sc;
+  float gq;
+  nvfp4_quantize_lane(x, c16, sc, gq);
+  reinterpret_cast<uint16_t *>(codes + row * 64)[lane] = static_cast<uint16_t>(c16);
+  if ((lane & 3) == 0) scales[row * 8 + (lane >> 2)] = static_cast<uint8_t>(sc);
+  if (lane == 0) gscale[row] = gq;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_q_nvfp4(const float *q, long long rows, uint8_t *codes, uint8_t *scales, float *gscale,
+                                    cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  const long long blocks = (rows + 7) / 8;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  quantize_q_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q, rows, codes, scales, gscale);
+  return cudaGetLastError();
 }
 
 }  // namespace idx

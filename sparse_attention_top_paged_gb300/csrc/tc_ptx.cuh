@@ -177,6 +177,42 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Shared-memory matrix descriptor: K-major operand in the 64-byte swizzle
+// layout (rows of 64 bytes, 8-row groups 512 bytes apart; the layout the
+// 64-byte-swizzled TMA copies write).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(16u >> 4) << 16;    // leading byte offset (unused by this layout)
+  d |= static_cast<uint64_t>(512u >> 4) << 32;   // stride byte offset: next 8-row group
+  d |= static_cast<uint64_t>(1) << 46;           // descriptor version
+  d |= static_cast<uint64_t>(4) << 61;           // 64-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::mxf4nvf4 (block-scaled): E2M1 A and B, f32
+// accumulator, unsigned E4M3 scale factors, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (0u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= (A x scale_A) * (B x scale_B)^T, kind::mxf4nvf4, one CTA: A and
+// B packed E2M1 in shared memory (K = 64 per instruction), one E4M3 scale per
+// 16 elements of each row from tensor memory. Scale-factor columns: for M = 128
+// (and N <= 128) the K step's four scales of row r sit in column (r / 32) of a
+// 4-column block, lane r % 32 of every 32-lane quarter; the block's first
+// column must be a multiple of 4.
+__device__ __forceinline__ void mma_ss_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 #define IDX_R8(b) "r"(v[b + 0]), "r"(v[b + 1]), "r"(v[b + 2]), "r"(v[b + 3]), "r"(v[b + 4]), "r"(v[b + 5]), \
                   "r"(v[b + 6]), "r"(v[b + 7])
 #define IDX_W8(b) "=r"(v[b + 0]), "=r"(v[b + 1]), "=r"(v[b + 2]), "=r"(v[b + 3]), "=r"(v[b + 4]), \
@@ -188,6 +224,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
       IDX_R8(0), IDX_R8(8), IDX_R8(16), IDX_R8(24)
+      : "memory");
+}
+
+// 32 lanes x 16 columns of 32 bits.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      IDX_R8(0), IDX_R8(8)
       : "memory");
 }
 

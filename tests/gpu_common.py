@@ -30,7 +30,7 @@ def to_device(W):
     return d
 
 
-def run_gpu(W, path="auto", *, scores=False, num_ctas=0, dev=None):
+def run_gpu(W, path="auto", *, scores=False, num_ctas=0, dev=None, q_format="exact"):
     """One idx_score_topk call through the C ABI; returns numpy results."""
     import torch
     import sparse_attention_top_paged_gb300 as idx
@@ -42,7 +42,7 @@ def run_gpu(W, path="auto", *, scores=False, num_ctas=0, dev=None):
     keys = {k: d[k] for k in ("keys_fp4", "key_scale", "key_gscale", "keys_f32") if k in d}
     gi, gs = idx.score_topk(d["q"], d["w"], d["bt"], d["vl"], W.top_k, entries_per_block=W.epb,
                             bt_stride=W.bt_stride, scores_out=so, dev_status=st, path=path,
-                            num_ctas=num_ctas, **keys)
+                            num_ctas=num_ctas, q_format=q_format, **keys)
     torch.cuda.synchronize()
     return (gi.cpu().numpy(), gs.cpu().numpy(), int(st.item()),
             None if so is None else so.cpu().numpy())
@@ -53,18 +53,26 @@ def oracle_rows(W, rows=None):
                                   W.epb, rows=rows, **W.oracle_kwargs())
 
 
+def oracle_rows_nvfp4(W, rows=None):
+    """Oracle score rows of the NVFP4-q mode: the exact definition applied to
+    the NVFP4-quantised queries."""
+    return oracle.score_topk_rows(oracle.nvfp4_q(W.q), W.w, W.block_table, W.bt_stride, W.max_lb, W.valid_lens,
+                                  W.epb, rows=rows, **W.oracle_kwargs())
+
+
 def _oracle_rows_job(args):
     """Runs in a spawned process: the oracle's score rows of one named
     workload (rebuilt from its seed) for the given query rows."""
-    name, seed, rows = args
+    name, seed, rows, nvfp4 = args
     from sparse_attention_top_paged_gb300 import workloads as wl
     W = getattr(wl, name)(seed)
-    return oracle_rows(W, rows)[0]
+    return (oracle_rows_nvfp4 if nvfp4 else oracle_rows)(W, rows)[0]
 
 
-def oracle_rows_parallel(name, seed, rows, procs=None):
-    """``oracle_rows`` of the named workload for many rows, split over spawned
-    processes (each rebuilds the workload from its seed)."""
+def oracle_rows_parallel(name, seed, rows, procs=None, nvfp4=False):
+    """``oracle_rows`` (``oracle_rows_nvfp4`` with ``nvfp4``) of the named
+    workload for many rows, split over spawned processes (each rebuilds the
+    workload from its seed)."""
     import multiprocessing as mp
     import os
     rows = list(rows)
@@ -72,7 +80,7 @@ def oracle_rows_parallel(name, seed, rows, procs=None):
     chunks = [rows[i::procs] for i in range(procs) if rows[i::procs]]
     out = {}
     with mp.get_context("spawn").Pool(len(chunks)) as pool:
-        for part in pool.map(_oracle_rows_job, [(name, seed, c) for c in chunks]):
+        for part in pool.map(_oracle_rows_job, [(name, seed, c, nvfp4) for c in chunks]):
             out.update(part)
     return out
 

@@ -117,6 +117,7 @@ def test_workspace_size_host_only(lib):
     ("P", 0, 1), ("entries_per_block", 0, 1), ("max_logical_blocks", 0, 1), ("bt_stride", -1, 1),
     ("D", 64, 2), ("entries_per_block", 24, 2), ("key_format", 7, 1), ("path", 9, 1),
     ("q", 0, 1), ("q", 0x10004, 1), ("keys_fp4", 0x30008, 1), ("topk_idx", 0, 1), ("num_ctas", -2, 1),
+    ("q_format", 7, 1), ("q_format", 1, 2),   # NVFP4 q has no CUDA-core path
 ])
 def test_validation_rejects(lib, field, value, code):
     a = _good_args()
@@ -189,3 +190,11 @@ def test_other_entry_points_validate(lib):
     sp.rope_dim = 64
     assert lib.idx_gather_split(ctypes.byref(sp), None) == 1      # null pointers
     assert lib.idx_gather_split(None, None) == 1
+
+
+def test_quantize_q_nvfp4_validation_host_only(lib):
+    q = ctypes.c_void_p
+    assert lib.idx_quantize_q_nvfp4(q(0x10000), 0, q(0x20000), q(0x30000), q(0x40000), None) == 0   # nothing to do
+    assert lib.idx_quantize_q_nvfp4(q(0x10000), -1, q(0x20000), q(0x30000), q(0x40000), None) == 1
+    assert lib.idx_quantize_q_nvfp4(None, 4, q(0x20000), q(0x30000), q(0x40000), None) == 1
+    assert lib.idx_quantize_q_nvfp4(q(0x10008), 4, q(0x20000), q(0x30000), q(0x40000), None) == 1   # q 16-byte aligned
