@@ -176,15 +176,22 @@ struct RowSource {
   int resident, pending;
   volatile int *abort;
 
+  // The score at or above which a key's order is >= thr: float_order is
+  // monotonic, so one float compare replaces the order of every score (for
+  // any finite score, order >= thr <=> score >= the returned value; no
+  // finite score passes a NaN; -inf, the mark of an excluded key, never
+  // passes).
+  __device__ __forceinline__ static float threshold(uint32_t thr) {
+    return (thr <= float_order(-3.402823466e38f)) ? -3.402823466e38f : order_float(thr);
+  }
   template <class F>
-  __device__ __forceinline__ static void key4(float4 v, long long i0, uint32_t thr, F &f) {
+  __device__ __forceinline__ static void key4(float4 v, long long i0, float tf, F &f) {
     const float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      if (e[q] == -INFINITY) continue;
-      const uint32_t o = float_order(e[q]);
-      if (o >= thr)
-        f((static_cast<uint64_t>(o) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(i0 + q)));
+      if (e[q] >= tf)
+        f((static_cast<uint64_t>(float_order(e[q])) << 32) |
+          static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(i0 + q)));
     }
   }
   // Thread 0 starts copying chunk c (its 16-byte part; the tail of at most
@@ -215,6 +222,7 @@ struct RowSource {
   }
   template <class F>
   __device__ void pass(uint32_t thr, F &&f) {
+    const float tf = threshold(thr);
     if (!staged) {
       for (long long base = 0; base < L; base += kBlock) {
         float4 v[kUnroll];
@@ -227,7 +235,7 @@ struct RowSource {
           v[u].w = (i0 + 3 < L) ? row[i0 + 3] : -INFINITY;
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) key4(v[u], base + 4LL * (u * kThreads + threadIdx.x), thr, f);
+        for (int u = 0; u < kUnroll; ++u) key4(v[u], base + 4LL * (u * kThreads + threadIdx.x), tf, f);
       }
       return;
     }
@@ -247,12 +255,11 @@ struct RowSource {
       const long long c0 = static_cast<long long>(c) * chunk;
       const int n = static_cast<int>(min(static_cast<long long>(chunk), L - c0)), n4 = n & ~3;
       const float4 *s4 = reinterpret_cast<const float4 *>(stage);
-      for (int i = threadIdx.x; i < (n4 >> 2); i += kThreads) key4(s4[i], c0 + 4LL * i, thr, f);
+      for (int i = threadIdx.x; i < (n4 >> 2); i += kThreads) key4(s4[i], c0 + 4LL * i, tf, f);
       for (int i = n4 + threadIdx.x; i < n; i += kThreads) {
         const float e = row[c0 + i];
-        if (e == -INFINITY) continue;
-        const uint32_t o = float_order(e);
-        if (o >= thr) f((static_cast<uint64_t>(o) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(c0 + i)));
+        if (e >= tf)
+          f((static_cast<uint64_t>(float_order(e)) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(c0 + i)));
       }
     }
   }
@@ -527,6 +534,13 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
   // wait for that kernel's completion and memory first.
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
+  // the first digit's counts, loaded beside the row length (both wait on memory)
+  uint32_t hpre[kPer];
+  if (hist != nullptr) {
+    const uint32_t *h = hist + static_cast<size_t>(t) * kBins;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) hpre[j] = h[kBins - 1 - kPer * tid - j];
+  }
   const int L = p.valid_lens[t];
   if (bad_len(p, L)) {
     if (tid == 0 && p.dev_status) atomicOr(p.dev_status, IDX_STATUS_BAD_LEN);
@@ -587,9 +601,8 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
     const uint32_t dmask = (1u << width) - 1u;
     uint32_t c[kPer];
     if (rounds == 0 && hist != nullptr) {
-      const uint32_t *h = hist + static_cast<size_t>(t) * kBins;
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) c[j] = h[kBins - 1 - kPer * tid - j];
+      for (int j = 0; j < kPer; ++j) c[j] = hpre[j];
     } else {
       for (int b = tid; b < kBins; b += kThreads) sh->table[b] = 0u;
       __syncthreads();
