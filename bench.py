@@ -129,7 +129,7 @@ def peaks():
 FP4_OVER_BF16 = 6.0
 
 
-def roofline(W, kern_s, q_format="exact"):
+def roofline(W, kern_s, q_format="exact", q_elem_bytes=4):
     """Roofline of the scoring kernel (q preparation + scorer). Decode
     workloads stream every key once: HBM bound, 72.125 B per pair plus q, w
     and the length per query. Prefill shares 128 blocks of keys between 4096
@@ -145,7 +145,7 @@ def roofline(W, kern_s, q_format="exact"):
         return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": None, "kernel": "score_tc_kernel",
                 "peak_kind": pk, "algorithmic_flops_per_launch": flops}
-    algo_bytes = W.pairs * BYTES_PER_PAIR + W.T * (4 * W.H * W.D + 4 * W.H + 4)
+    algo_bytes = W.pairs * BYTES_PER_PAIR + W.T * (q_elem_bytes * W.H * W.D + 4 * W.H + 4)
     achieved = algo_bytes / kern_s / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "traffic": recorded_traffic(W.name) if q_format == "exact" else None, "kernel": "score_tc_kernel",
@@ -727,7 +727,7 @@ def main():
             r2 = measure_score(W2, args, min(args.steps, EXTRA_STEPS), dev, flush, dist, e2e=False, q_format=qf)
             key = name if qf == "exact" else f"{name}_nvfp4_q"
             extra[key] = {"metric": METRIC, "value": r2["value"], "unit": UNIT, "steps": r2["steps"],
-                          "ms_per_step": r2["ms_per_step"], "config": dict(workload_config(W2), q_format=qf),
+                          "ms_per_step": r2["ms_per_step"], "config": dict(r2["config"], q_format=qf),
                           "roofline": r2["roofline"], "clocks": r2["clocks"]}
             del W2
             torch.cuda.empty_cache()
@@ -769,6 +769,11 @@ def measure_score(W, args, K, dev, flush, dist, e2e, q_format="exact"):
     import torch
     import sparse_attention_top_paged_gb300 as idx
     q = torch.from_numpy(W.q).to(dev)
+    # The workloads' queries are bf16 values (the page's launcher upcasts its
+    # bf16 q_I): they go in as bf16 (q_dtype BF16), which the library reads as
+    # exactly those float32 values; a float32-only q stays float32.
+    if torch.equal(q.to(torch.bfloat16).float(), q):
+        q = q.to(torch.bfloat16)
     w = torch.from_numpy(W.w).to(dev)
     bt = torch.from_numpy(W.block_table).to(dev)
     vl = torch.from_numpy(W.valid_lens).to(dev)
@@ -842,8 +847,10 @@ def measure_score(W, args, K, dev, flush, dist, e2e, q_format="exact"):
     pairs_step = W.pairs
     value, t_total = whole_job(pairs_step, K, sum(step_ms) / 1e3, dist, dev)
     kern_s = statistics.mean(kern_ms) / 1e3
-    rec = {"value": value, "steps": K, "ms_per_step": 1e3 * t_total / K, "config": workload_config(W),
-           "roofline": dict(roofline(W, kern_s, q_format), kernel_ms=1e3 * kern_s, kernel_timed_steps=len(kern_ms)),
+    rec = {"value": value, "steps": K, "ms_per_step": 1e3 * t_total / K,
+           "config": dict(workload_config(W), q_dtype=str(q.dtype).replace("torch.", "")),
+           "roofline": dict(roofline(W, kern_s, q_format, q.element_size()), kernel_ms=1e3 * kern_s,
+                            kernel_timed_steps=len(kern_ms)),
            "clocks": clk.summary(), "wall_s": wall, "gpu_launches": launches_per_step(W) * K}
     if not e2e:
         return rec
@@ -863,8 +870,9 @@ def measure_score(W, args, K, dev, flush, dist, e2e, q_format="exact"):
             total += (x.nbytes + 255) // 256 * 256
         return offs, total
 
-    tdt = {np.dtype(np.float32): torch.float32, np.dtype(np.int32): torch.int32}
-    in_parts = [W.q, W.w, W.block_table, W.valid_lens]
+    tdt = {np.dtype(np.float32): torch.float32, np.dtype(np.int32): torch.int32, np.dtype(np.uint16): torch.bfloat16}
+    q_host = (q.view(torch.int16).cpu().numpy().view(np.uint16) if q.dtype == torch.bfloat16 else W.q)
+    in_parts = [q_host, W.w, W.block_table, W.valid_lens]
     in_offs, in_bytes = packed(in_parts)
     h_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
     for x, o in zip(in_parts, in_offs):
@@ -879,10 +887,15 @@ def measure_score(W, args, K, dev, flush, dist, e2e, q_format="exact"):
     h2d, d2h = in_bytes, 2 * out_bytes
     E = max(10, K // 10)
 
+    # The call is the public API's prepared form, as a serving loop holds it:
+    # a ScoreTopkPlan bound to the input and output blocks (arguments checked
+    # and marshalled once), run once per step over the freshly copied inputs.
+    plan = idx.ScoreTopkPlan(eq, ew, ebt, evl, k, entries_per_block=W.epb, bt_stride=W.bt_stride, keys_fp4=fp4,
+                             key_scale=sc, key_gscale=gs, out=(e_i, e_s), workspace=ws, q_format=q_format)
+
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
-        idx.score_topk(eq, ew, ebt, evl, k, entries_per_block=W.epb, bt_stride=W.bt_stride, keys_fp4=fp4,
-                       key_scale=sc, key_gscale=gs, out=(e_i, e_s), workspace=ws, q_format=q_format)
+        plan.run()
         h_out.copy_(d_out, non_blocking=True)
 
     for _ in range(3):
@@ -906,7 +919,8 @@ def measure_score(W, args, K, dev, flush, dist, e2e, q_format="exact"):
     if not torch.equal(h_out[:W.T * k * 4].view(torch.int32).view(W.T, k), out_i.cpu()):
         raise RuntimeError("end-to-end top-k differs from the device-timed steps")
     rec["e2e"] = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                  "ms_per_step": 1e3 * e2e_t / E, "timing": "host perf_counter around issue + copies + synchronize",
+                  "ms_per_step": 1e3 * e2e_t / E,
+                  "timing": "host perf_counter around copy in + ScoreTopkPlan.run + copy out + synchronize",
                   "device_value": e2e_dev, "device_ms_per_step": statistics.mean(dev_ms), "steps": E}
     return rec
 

@@ -64,6 +64,11 @@ typedef enum { IDX_PATH_AUTO = 0, IDX_PATH_TENSOR = 1, IDX_PATH_SIMT = 2 } idx_p
  * with no decode of the keys. Tensor path and NVFP4 keys only, H <= 128. */
 typedef enum { IDX_Q_EXACT = 0, IDX_Q_NVFP4 = 1 } idx_q_format_t;
 
+/* Element type of q: float32, or bf16 bit patterns (the indexer projection's
+ * output type; read as the exactly equal float32 values, so the results are
+ * those of the upcast q). BF16 needs the tensor path. */
+typedef enum { IDX_Q_F32 = 0, IDX_Q_BF16 = 1 } idx_q_dtype_t;
+
 /*
  * idx_score_topk — lightning-indexer scores and their top-k.
  *
@@ -91,8 +96,9 @@ typedef enum { IDX_Q_EXACT = 0, IDX_Q_NVFP4 = 1 } idx_q_format_t;
  *
  * Arguments (all sizes in elements):
  *   T >= 0, H in [1, 256], D: 128 (NVFP4) or 64/128 (F32)
- *   q          device [T, H, D] float32 (callers upcast bf16, as the
- *              score_topk launcher of commit c2f705a does)
+ *   q          device [T, H, D], float32 or bf16 (q_dtype); the score_topk
+ *              launcher of commit c2f705a upcasts bf16 to float32 first, a
+ *              bf16 q here is read as those same float32 values
  *   w          device [T, H] float32
  *   P >= 1, entries_per_block (epb) >= 1; NVFP4 needs epb % 16 == 0
  *   block_table device int32, row t at block_table + t * bt_stride, with
@@ -121,6 +127,8 @@ typedef enum { IDX_Q_EXACT = 0, IDX_Q_NVFP4 = 1 } idx_q_format_t;
  *              launching early under the scorer's tail, which lengthens
  *              that call by a few microseconds.
  *   q_format   idx_q_format_t (0, the zero-initialised default, is EXACT).
+ *   q_dtype    idx_q_dtype_t (0, the default, is F32); BF16 with the
+ *              CUDA-core path gives IDX_ERR_UNSUPPORTED.
  *              NVFP4 with F32 keys, the CUDA-core path or H > 128 gives
  *              IDX_ERR_UNSUPPORTED; in that mode the key scale bytes are
  *              read as unsigned E4M3 (their sign bit must be clear).
@@ -130,7 +138,7 @@ typedef enum { IDX_Q_EXACT = 0, IDX_Q_NVFP4 = 1 } idx_q_format_t;
  */
 typedef struct {
   int32_t T, H, D;
-  const float *q;
+  const void *q;    /* float32 or bf16, per q_dtype */
   const float *w;
   int32_t key_format; /* idx_key_format_t */
   const uint8_t *keys_fp4;
@@ -154,6 +162,7 @@ typedef struct {
   int32_t num_ctas; /* 0 = one per SM of the current device */
   void *timing_events[2];
   int32_t q_format; /* idx_q_format_t */
+  int32_t q_dtype;  /* idx_q_dtype_t */
 } idx_score_topk_args;
 
 /* Bytes of workspace idx_score_topk needs for these arguments (host only; no

@@ -77,7 +77,9 @@ def make_score_args(q, w, block_table, valid_lens, top_k, *, entries_per_block, 
     """Build an ``idx_score_topk_args`` from torch tensors (no device work).
     ``q_format="nvfp4"`` selects the opt-in NVFP4 query mode."""
     torch = _torch()
-    _check(q, "q", torch.float32, 3)
+    _check(q, "q", None, 3)
+    if q.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("q must be float32 or bfloat16")
     _check(w, "w", torch.float32, 2)
     _check(block_table, "block_table", torch.int32, 2)
     _check(valid_lens, "valid_lens", torch.int32, 1)
@@ -117,6 +119,7 @@ def make_score_args(q, w, block_table, valid_lens, top_k, *, entries_per_block, 
     a.path = PATHS[path]
     a.num_ctas = num_ctas
     a.q_format = _lib.Q_FORMATS[q_format]
+    a.q_dtype = _lib.Q_BF16 if q.dtype == torch.bfloat16 else _lib.Q_F32
     return a
 
 
@@ -149,6 +152,53 @@ def score_topk(q, w, block_table, valid_lens, top_k, *, entries_per_block, keys_
         a.workspace_bytes = ws.numel() * ws.element_size()
         _raise("idx_score_topk", lib.idx_score_topk(ctypes.byref(a), _stream(q.device)))
     return topk_idx, topk_score
+
+
+class ScoreTopkPlan:
+    """A prepared ``idx_score_topk`` call for a serving loop: the arguments
+    are checked and marshalled once, the outputs and the workspace allocated
+    once, and every :meth:`run` is one library call on the current stream
+    over whatever the bound tensors then hold (refill them in place between
+    runs). ``run`` can be captured in a CUDA graph with the step's copies.
+    Arguments as for :func:`score_topk`."""
+
+    def __init__(self, q, w, block_table, valid_lens, top_k, *, entries_per_block, keys_fp4=None,
+                 key_scale=None, key_gscale=None, keys_f32=None, bt_stride=None, scores_out=None,
+                 dev_status=None, path="auto", num_ctas=0, out=None, workspace=None, q_format="exact"):
+        torch = _torch()
+        T = q.shape[0]
+        if out is None:
+            out = (torch.empty((T, top_k), dtype=torch.int32, device=q.device),
+                   torch.empty((T, top_k), dtype=torch.float32, device=q.device))
+        self.topk_idx, self.topk_score = out
+        self._keep = (q, w, block_table, valid_lens, keys_fp4, key_scale, key_gscale, keys_f32, scores_out,
+                      dev_status)
+        self.args = make_score_args(q, w, block_table, valid_lens, top_k, entries_per_block=entries_per_block,
+                                    keys_fp4=keys_fp4, key_scale=key_scale, key_gscale=key_gscale,
+                                    keys_f32=keys_f32, bt_stride=bt_stride, topk_idx=self.topk_idx,
+                                    topk_score=self.topk_score, scores_out=scores_out, dev_status=dev_status,
+                                    path=path, num_ctas=num_ctas, q_format=q_format)
+        self.device = q.device
+        self._lib = load_library()
+        with torch.cuda.device(q.device):
+            need = ctypes.c_size_t(0)
+            _raise("idx_score_topk_workspace_size",
+                   self._lib.idx_score_topk_workspace_size(ctypes.byref(self.args), ctypes.byref(need)))
+            self.workspace = workspace if workspace is not None else torch.empty(
+                max(need.value, 256), dtype=torch.uint8, device=q.device)
+        if self.workspace.numel() * self.workspace.element_size() < need.value:
+            raise ValueError("workspace smaller than idx_score_topk_workspace_size")
+        self.args.workspace = self.workspace.data_ptr()
+        self.args.workspace_bytes = self.workspace.numel() * self.workspace.element_size()
+        self._args_ref = ctypes.byref(self.args)
+
+    def run(self, stream=None):
+        """One call on ``stream`` (a torch.cuda.Stream; default: the current
+        stream of the plan's device). Returns (topk_idx, topk_score)."""
+        torch = _torch()
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        _raise("idx_score_topk", self._lib.idx_score_topk(self._args_ref, ctypes.c_void_p(s.cuda_stream)))
+        return self.topk_idx, self.topk_score
 
 
 def quantize_q_nvfp4(q):

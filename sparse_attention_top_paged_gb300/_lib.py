@@ -20,6 +20,7 @@ STATUS_NAMES = {0: "IDX_OK", 1: "IDX_ERR_INVALID_ARG", 2: "IDX_ERR_UNSUPPORTED",
 KEYS_NVFP4, KEYS_F32 = 0, 1
 PATHS = {"auto": 0, "tensor": 1, "simt": 2}
 Q_FORMATS = {"exact": 0, "nvfp4": 1}
+Q_F32, Q_BF16 = 0, 1
 STATUS_BAD_BLOCK, STATUS_BAD_LEN, STATUS_BAD_SEL, STATUS_TIMEOUT, STATUS_DEBUG_BOUNDS = 1, 2, 4, 8, 16
 STATIC_SCRATCH_BYTES = 8 << 20
 
@@ -45,6 +46,7 @@ class ScoreTopkArgs(ctypes.Structure):
         ("path", c_i32), ("num_ctas", c_i32),
         ("timing_events", c_vp * 2),
         ("q_format", c_i32),
+        ("q_dtype", c_i32),
     ]
 
 

@@ -58,6 +58,7 @@ idx_status_t resolve(const idx_score_topk_args *a, Resolved *r) {
     return IDX_ERR_INVALID_ARG;
   if (a->num_ctas < 0) return IDX_ERR_INVALID_ARG;
   if (a->q_format != IDX_Q_EXACT && a->q_format != IDX_Q_NVFP4) return IDX_ERR_INVALID_ARG;
+  if (a->q_dtype != IDX_Q_F32 && a->q_dtype != IDX_Q_BF16) return IDX_ERR_INVALID_ARG;
   const long long max_len = static_cast<long long>(a->max_logical_blocks) * a->entries_per_block;
   if (max_len > 0x7FFFFFFFLL) return IDX_ERR_INVALID_ARG;
   const bool f32 = a->key_format == IDX_KEYS_F32;
@@ -96,10 +97,14 @@ idx_status_t resolve(const idx_score_topk_args *a, Resolved *r) {
   if (plan == Plan::kTensor && f32) return IDX_ERR_UNSUPPORTED;
   const bool nvfp4_q = a->q_format == IDX_Q_NVFP4;
   if (nvfp4_q && (plan != Plan::kTensor || a->H > 128)) return IDX_ERR_UNSUPPORTED;
+  const bool bf16_q = a->q_dtype == IDX_Q_BF16;
+  if (bf16_q && plan != Plan::kTensor) return IDX_ERR_UNSUPPORTED;
 
   ScoreParams &p = r->p;
   p.T = a->T; p.H = a->H; p.D = a->D;
-  p.q = a->q; p.w = a->w;
+  p.q = bf16_q ? nullptr : static_cast<const float *>(a->q);
+  p.q16 = bf16_q ? static_cast<const uint16_t *>(a->q) : nullptr;
+  p.w = a->w;
   p.keys_fp4 = a->keys_fp4; p.key_scale = a->key_scale;
   p.key_gscale = a->key_gscale; p.keys_f32 = a->keys_f32;
   p.P = a->P; p.epb = a->entries_per_block;
@@ -112,7 +117,7 @@ idx_status_t resolve(const idx_score_topk_args *a, Resolved *r) {
 
   if (plan == Plan::kTensor && !score_tc_supported(p)) {
     // (the NVFP4 q mode has no CUDA-core counterpart: never a silent fallback)
-    if (a->path == IDX_PATH_TENSOR || nvfp4_q) return IDX_ERR_UNSUPPORTED;
+    if (a->path == IDX_PATH_TENSOR || nvfp4_q || bf16_q) return IDX_ERR_UNSUPPORTED;
     plan = Plan::kSimt;
   }
   r->plan = plan;

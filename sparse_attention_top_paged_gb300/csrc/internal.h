@@ -14,7 +14,8 @@ constexpr int kMaxTopK = 4096;
 // Plain-data copy of the score arguments handed to kernels by value.
 struct ScoreParams {
   int T, H, D;
-  const float *q, *w;
+  const float *q, *w;          // q: float32 queries (null when q16 is given)
+  const uint16_t *q16;         // bf16 queries (tensor path), or null
   const uint8_t *keys_fp4, *key_scale;
   const float *key_gscale, *keys_f32;
   int P, epb;

@@ -248,7 +248,14 @@ __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay,
   float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
   float wv = 0.0f;
   if (h < p.H && t < p.T) {
-    x = reinterpret_cast<const float4 *>(p.q + (static_cast<long long>(t) * p.H + h) * 128)[lane];
+    const long long e0 = (static_cast<long long>(t) * p.H + h) * 128;
+    if (p.q16 != nullptr) {   // bf16: the float32 with the same leading 16 bits
+      const uint2 u = reinterpret_cast<const uint2 *>(p.q16 + e0)[lane];
+      x = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                      __uint_as_float(u.y & 0xFFFF0000u));
+    } else {
+      x = reinterpret_cast<const float4 *>(p.q + e0)[lane];
+    }
     wv = p.w[static_cast<long long>(t) * p.H + h];
   }
   if (lay.fp4) {

@@ -118,6 +118,7 @@ def test_workspace_size_host_only(lib):
     ("D", 64, 2), ("entries_per_block", 24, 2), ("key_format", 7, 1), ("path", 9, 1),
     ("q", 0, 1), ("q", 0x10004, 1), ("keys_fp4", 0x30008, 1), ("topk_idx", 0, 1), ("num_ctas", -2, 1),
     ("q_format", 7, 1), ("q_format", 1, 2),   # NVFP4 q has no CUDA-core path
+    ("q_dtype", 7, 1), ("q_dtype", 1, 2),     # bf16 q has no CUDA-core path
 ])
 def test_validation_rejects(lib, field, value, code):
     a = _good_args()

@@ -309,3 +309,50 @@ def test_tensor_many_short_queries(num_ctas):
     gi, gs, st, so = run_gpu(W, "tensor", scores=True, num_ctas=num_ctas)
     rows, _ = oracle_rows(W)
     check_against_oracle(W, gi, gs, rows, so, f"short/{num_ctas}")
+
+
+def test_prepared_plan_matches_the_call():
+    """ScoreTopkPlan: arguments marshalled once, run over refilled inputs."""
+    import sparse_attention_top_paged_gb300 as idx
+    W1 = _small(101, T=6, lo=2000, hi=7000, k=128, max_lb=120, P=800)
+    W2 = _small(102, T=6, lo=2000, hi=7000, k=128, max_lb=120, P=800)
+    d = to_device(W1)
+    plan = idx.ScoreTopkPlan(d["q"], d["w"], d["bt"], d["vl"], W1.top_k, entries_per_block=W1.epb,
+                             bt_stride=W1.bt_stride, keys_fp4=d["keys_fp4"], key_scale=d["key_scale"],
+                             key_gscale=d["key_gscale"])
+    for W in (W1, W2):
+        dW = to_device(W)
+        for name in ("q", "w", "bt", "vl", "keys_fp4", "key_scale", "key_gscale"):
+            d[name].copy_(dW[name])          # refill the bound tensors in place
+        gi, gs = plan.run()
+        torch.cuda.synchronize()
+        ref = run_gpu(W, "tensor")
+        assert np.array_equal(gi.cpu().numpy(), ref[0]) and np.array_equal(gs.cpu().numpy(), ref[1])
+        rows, _ = oracle_rows(W)
+        check_against_oracle(W, gi.cpu().numpy(), gs.cpu().numpy(), rows, None, f"plan/{W.meta['seed']}")
+
+
+@pytest.mark.parametrize("q_format", ["exact", "nvfp4"])
+@pytest.mark.parametrize("case", ["batched", "pairs"])
+def test_bf16_queries_equal_their_float32_upcast(q_format, case):
+    """q given as bf16 (q_dtype BF16) gives exactly what its float32 upcast
+    gives, on the tensor path; the CUDA-core path refuses it."""
+    import sparse_attention_top_paged_gb300 as idx
+    if case == "batched":
+        W = _small(111, T=6, lo=2000, hi=7000, k=128, max_lb=120, P=800)
+    else:
+        W = wl.prefill(8, rows=40, base=3000, ratio=4, n_blocks=20, top_k=128)
+    d = to_device(W)
+    q16 = d["q"].to(torch.bfloat16)
+    assert torch.equal(q16.float(), d["q"])      # the workloads' q values are bf16
+    kw = dict(entries_per_block=W.epb, bt_stride=W.bt_stride, keys_fp4=d["keys_fp4"], key_scale=d["key_scale"],
+              key_gscale=d["key_gscale"], q_format=q_format, path="tensor")
+    s32 = torch.full((W.T, W.max_lb * W.epb), float("nan"), dtype=torch.float32, device="cuda")
+    s16 = s32.clone()
+    i32, v32 = idx.score_topk(d["q"], d["w"], d["bt"], d["vl"], W.top_k, scores_out=s32, **kw)
+    i16, v16 = idx.score_topk(q16, d["w"], d["bt"], d["vl"], W.top_k, scores_out=s16, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(i32, i16) and torch.equal(v32, v16)
+    assert torch.equal(torch.nan_to_num(s32, nan=7.0), torch.nan_to_num(s16, nan=7.0))
+    with pytest.raises(idx.IndexerError):
+        idx.score_topk(q16, d["w"], d["bt"], d["vl"], W.top_k, **dict(kw, path="simt", q_format="exact"))
