@@ -214,16 +214,152 @@ __device__ long long block_incl_scan(long long v, long long *scratch, long long 
   return before + x;
 }
 
-// q -> the B-operand record of row group tq: block (tq, y) prepares head rows
-// 8y .. 8y+7, one warp per head row, 4 dims per lane (head rows of absent
-// rows or heads are zero). Per head a power-of-two scale 2^sigma puts the
-// largest |q| in [2^14, 2^15) (sigma from the exponent field; subnormal or
-// zero heads keep sigma 0; clamped so 2^sigma and 2^-sigma are normal
-// floats); the scaled values are split into f16 hi + lo (lo = 0 whenever q is
-// exact in f16 after scaling, e.g. for bf16-valued q) and w' = w 2^-sigma
-// undoes the scale after the ReLU.
+// q -> the B-operand record of row group tq: one block per record, one warp
+// per head row at a time, 4 dims per lane (head rows of absent rows or heads
+// are zero). load_head_row reads this lane's part of head row n.
+// Exact q: per head a power-of-two scale 2^sigma puts the largest |q| in
+// [2^14, 2^15) (sigma from the exponent field; subnormal or zero heads keep
+// sigma 0; clamped so 2^sigma and 2^-sigma are normal floats); the scaled
+// values are split into f16 hi + lo and w' = w 2^-sigma undoes the scale
+// after the ReLU. The lo part is written only when some head of the record
+// has a non-zero lo (never for bf16-valued q short of a 2^-31 dynamic range
+// within a head): the MMA reads it only then (the OR of the heads' flags).
+// NVFP4 q: the quantisation of nvfp4q.cuh, w' = w gq.
+__device__ __forceinline__ void load_head_row(const ScoreParams &p, const TcLayout &lay, int tq, int n, int lane,
+                                              float4 &x, float &wv) {
+  const int h = n % lay.Npad, t = tq * lay.R + n / lay.Npad;
+  x = make_float4(0.f, 0.f, 0.f, 0.f);
+  wv = 0.0f;
+  if (h < p.H && t < p.T) {
+    const long long e0 = (static_cast<long long>(t) * p.H + h) * 128;
+    if (p.q16 != nullptr) {   // bf16: the float32 with the same leading 16 bits
+      const uint2 u = reinterpret_cast<const uint2 *>(p.q16 + e0)[lane];
+      x = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                      __uint_as_float(u.y & 0xFFFF0000u));
+    } else {
+      x = reinterpret_cast<const float4 *>(p.q + e0)[lane];
+    }
+    wv = p.w[static_cast<long long>(t) * p.H + h];
+  }
+}
+
+// The exact-q split of this lane's 4 values of head row n: its offset in the
+// hi (and lo) rows, the packed f16 hi and lo, and w'. Returns whether this
+// warp's head row has a non-zero lo part.
+__device__ __forceinline__ bool split_head_row(const TcLayout &lay, int n, int lane, float4 x, float wv, uint32_t &off,
+                                               uint2 &vh, uint2 &vl, float &wq) {
+  float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  const int sigma = (ex == 0) ? 0 : max(-126, min(126, 141 - ex));
+  const float up = __uint_as_float(static_cast<uint32_t>(127 + sigma) << 23);
+  const float down = __uint_as_float(static_cast<uint32_t>(127 - sigma) << 23);
+  const float xs[4] = {x.x * up, x.y * up, x.z * up, x.w * up};
+  __half hi[4], lo[4];
+  bool any_lo = false;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    hi[e] = __float2half_rn(xs[e]);
+    lo[e] = __float2half_rn(xs[e] - __half2float(hi[e]));
+    any_lo |= (__half2float(lo[e]) != 0.0f);
+  }
+  // dims 4*lane .. 4*lane+3: K block kb = lane / 16 (64 dims each), 16-byte
+  // chunk jj = (lane / 2) % 8 of the head row's 128 bytes, swizzled by n % 8
+  const int ch = lane >> 1, kb = ch >> 3, jj = ch & 7;
+  off = kb * (lay.NR * 128) + n * 128 + ((jj ^ (n & 7)) * 16) + (lane & 1) * 8;
+  vh.x = static_cast<uint32_t>(__half_as_ushort(hi[0])) | (static_cast<uint32_t>(__half_as_ushort(hi[1])) << 16);
+  vh.y = static_cast<uint32_t>(__half_as_ushort(hi[2])) | (static_cast<uint32_t>(__half_as_ushort(hi[3])) << 16);
+  vl.x = static_cast<uint32_t>(__half_as_ushort(lo[0])) | (static_cast<uint32_t>(__half_as_ushort(lo[1])) << 16);
+  vl.y = static_cast<uint32_t>(__half_as_ushort(lo[2])) | (static_cast<uint32_t>(__half_as_ushort(lo[3])) << 16);
+  wq = wv * down;
+  return __any_sync(0xFFFFFFFFu, any_lo);
+}
+
+// One block per record (many records: as many blocks as records fill the
+// GPU); the lo rows only when needed.
 __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay, uint8_t *__restrict__ rec,
                                                     uint32_t *__restrict__ hist, uint32_t *__restrict__ cand_cnt) {
+  ptx::launch_dependents();  // the scorer may start its prologue meanwhile
+  constexpr int kWarps = 8, kAhead = 4;
+  const int tq = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the group's rows: zero their key histograms (and candidate counters)
+  for (int rr = 0; rr < lay.R; ++rr) {
+    const int t = tq * lay.R + rr;
+    if (t >= p.T) break;
+    uint4 *hz = reinterpret_cast<uint4 *>(hist + static_cast<size_t>(t) * kScoreBins);
+    for (int i = threadIdx.x; i < kScoreBins / 4; i += blockDim.x) hz[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (cand_cnt != nullptr && threadIdx.x == 0) cand_cnt[t] = 0u;
+  }
+  uint8_t *r = rec + static_cast<size_t>(tq) * lay.rec_bytes;
+  if (lay.fp4) {   // scale words of head rows NR .. 127 stay zero
+    uint32_t *sw = reinterpret_cast<uint32_t *>(r + lay.sfb_off);
+    for (int i = threadIdx.x; i < 256; i += blockDim.x)
+      if (((i >> 5) & 3) * 32 >= lay.NR) sw[i] = 0u;
+  }
+  bool any_lo = false;
+  for (int nb = warp; nb < lay.NR; nb += kAhead * kWarps) {
+    float4 x[kAhead];
+    float wv[kAhead];
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      const int n = nb + u * kWarps;
+      if (n < lay.NR) load_head_row(p, lay, tq, n, lane, x[u], wv[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      const int n = nb + u * kWarps;
+      if (n >= lay.NR) continue;
+      if (lay.fp4) {
+        uint32_t codes16, scale;
+        float gq;
+        nvfp4_quantize_lane(x[u], codes16, scale, gq);
+        // codes: bytes 2 lane, 2 lane + 1 of head row n (64 bytes, 64-byte swizzle in 8-row groups)
+        const uint32_t off =
+            (n >> 3) * 512 + (n & 7) * 64 + ((((lane >> 3) ^ ((n >> 1) & 3)) & 3) * 16) + ((2 * lane) & 15);
+        *reinterpret_cast<uint16_t *>(r + off) = static_cast<uint16_t>(codes16);
+        if ((lane & 3) == 0) {   // scale of group g = lane / 4: K step g / 4, byte g % 4 of its word
+          const int g = lane >> 2;
+          r[lay.sfb_off + (((g >> 2) * 4 + (n >> 5)) * 32 + (n & 31)) * 4 + (g & 3)] = static_cast<uint8_t>(scale);
+        }
+        if (lane == 0) {
+          reinterpret_cast<float *>(r + lay.rec_w)[n] = __fmul_rn(wv[u], gq);
+          reinterpret_cast<int *>(r + lay.rec_flags)[n] = 0;
+        }
+      } else {
+        uint32_t off;
+        uint2 vh, vl;
+        float wq;
+        const bool row_lo = split_head_row(lay, n, lane, x[u], wv[u], off, vh, vl, wq);
+        *reinterpret_cast<uint2 *>(r + off) = vh;
+        any_lo |= row_lo;
+        if (lane == 0) {
+          reinterpret_cast<float *>(r + lay.rec_w)[n] = wq;
+          reinterpret_cast<int *>(r + lay.rec_flags)[n] = row_lo ? 1 : 0;
+        }
+      }
+    }
+  }
+  // The lo rows, only when the MMA will read them: some head of the record
+  // has a non-zero lo (then every head's lo, zeros included, is written).
+  if (lay.fp4 || !__syncthreads_or(any_lo)) return;
+  for (int n = warp; n < lay.NR; n += kWarps) {
+    float4 x;
+    float wv;
+    load_head_row(p, lay, tq, n, lane, x, wv);
+    uint32_t off;
+    uint2 vh, vl;
+    float wq;
+    split_head_row(lay, n, lane, x, wv, off, vh, vl, wq);
+    *reinterpret_cast<uint2 *>(r + lay.b_bytes + off) = vl;
+  }
+}
+
+// Few records: block (tq, y) prepares head rows 8y .. 8y+7 of record tq, one
+// warp each, so the work spreads over more blocks; every head's lo row is
+// written (the blocks of a record cannot agree on skipping it).
+__global__ void __launch_bounds__(256) qprep_rows_kernel(ScoreParams p, TcLayout lay, uint8_t *__restrict__ rec,
+                                                         uint32_t *__restrict__ hist, uint32_t *__restrict__ cand_cnt) {
   ptx::launch_dependents();  // the scorer may start its prologue meanwhile
   const int tq = blockIdx.x;
   for (int rr = 0; rr < lay.R; ++rr) {
@@ -244,28 +380,16 @@ __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay,
       if (((i >> 5) & 3) * 32 >= lay.NR) sw[i] = 0u;
   }
   if (n >= lay.NR) return;
-  const int h = n % lay.Npad, t = tq * lay.R + n / lay.Npad;
-  float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wv = 0.0f;
-  if (h < p.H && t < p.T) {
-    const long long e0 = (static_cast<long long>(t) * p.H + h) * 128;
-    if (p.q16 != nullptr) {   // bf16: the float32 with the same leading 16 bits
-      const uint2 u = reinterpret_cast<const uint2 *>(p.q16 + e0)[lane];
-      x = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
-                      __uint_as_float(u.y & 0xFFFF0000u));
-    } else {
-      x = reinterpret_cast<const float4 *>(p.q + e0)[lane];
-    }
-    wv = p.w[static_cast<long long>(t) * p.H + h];
-  }
+  float4 x;
+  float wv;
+  load_head_row(p, lay, tq, n, lane, x, wv);
   if (lay.fp4) {
     uint32_t codes16, scale;
     float gq;
     nvfp4_quantize_lane(x, codes16, scale, gq);
-    // codes: bytes 2 lane, 2 lane + 1 of head row n (64 bytes, 64-byte swizzle in 8-row groups)
     const uint32_t off = (n >> 3) * 512 + (n & 7) * 64 + ((((lane >> 3) ^ ((n >> 1) & 3)) & 3) * 16) + ((2 * lane) & 15);
     *reinterpret_cast<uint16_t *>(r + off) = static_cast<uint16_t>(codes16);
-    if ((lane & 3) == 0) {   // scale of group g = lane / 4: K step g / 4, byte g % 4 of its word
+    if ((lane & 3) == 0) {
       const int g = lane >> 2;
       r[lay.sfb_off + (((g >> 2) * 4 + (n >> 5)) * 32 + (n & 31)) * 4 + (g & 3)] = static_cast<uint8_t>(scale);
     }
@@ -275,37 +399,15 @@ __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay,
     }
     return;
   }
-  float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-  const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-  const int sigma = (ex == 0) ? 0 : max(-126, min(126, 141 - ex));
-  const float up = __uint_as_float(static_cast<uint32_t>(127 + sigma) << 23);
-  const float down = __uint_as_float(static_cast<uint32_t>(127 - sigma) << 23);
-  const float xs[4] = {x.x * up, x.y * up, x.z * up, x.w * up};
-  __half hi[4], lo[4];
-  bool any_lo = false;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    hi[e] = __float2half_rn(xs[e]);
-    lo[e] = __float2half_rn(xs[e] - __half2float(hi[e]));
-    any_lo |= (__half2float(lo[e]) != 0.0f);
-  }
-  // dims 4*lane .. 4*lane+3: K block kb = lane / 16 (64 dims each), 16-byte
-  // chunk jj = (lane / 2) % 8 of the head row's 128 bytes, swizzled by n % 8
-  const int ch = lane >> 1, kb = ch >> 3, jj = ch & 7;
-  const uint32_t off = kb * (lay.NR * 128) + n * 128 + ((jj ^ (n & 7)) * 16) + (lane & 1) * 8;
+  uint32_t off;
   uint2 vh, vl;
-  vh.x = static_cast<uint32_t>(__half_as_ushort(hi[0])) | (static_cast<uint32_t>(__half_as_ushort(hi[1])) << 16);
-  vh.y = static_cast<uint32_t>(__half_as_ushort(hi[2])) | (static_cast<uint32_t>(__half_as_ushort(hi[3])) << 16);
-  vl.x = static_cast<uint32_t>(__half_as_ushort(lo[0])) | (static_cast<uint32_t>(__half_as_ushort(lo[1])) << 16);
-  vl.y = static_cast<uint32_t>(__half_as_ushort(lo[2])) | (static_cast<uint32_t>(__half_as_ushort(lo[3])) << 16);
+  float wq;
+  const bool row_lo = split_head_row(lay, n, lane, x, wv, off, vh, vl, wq);
   *reinterpret_cast<uint2 *>(r + off) = vh;
   *reinterpret_cast<uint2 *>(r + lay.b_bytes + off) = vl;
-  const bool warp_lo = __any_sync(0xFFFFFFFFu, any_lo);
   if (lane == 0) {
-    reinterpret_cast<float *>(r + lay.rec_w)[n] = wv * down;
-    reinterpret_cast<int *>(r + lay.rec_flags)[n] = warp_lo ? 1 : 0;
+    reinterpret_cast<float *>(r + lay.rec_w)[n] = wq;
+    reinterpret_cast<int *>(r + lay.rec_flags)[n] = row_lo ? 1 : 0;
   }
 }
 
@@ -1011,8 +1113,11 @@ cudaError_t launch_score_tc(const ScoreParams &p, int num_ctas, void *qrec, uint
                                        static_cast<int>(lay.smem_bytes));
   if (e != cudaSuccess) return e;
   uint8_t *rec = static_cast<uint8_t *>(qrec);
-  qprep_kernel<<<dim3(static_cast<unsigned>(lay.nq), static_cast<unsigned>(lay.NR / 8)), 256, 0, stream>>>(p, lay, rec, hist,
-                                                                                                          cand_cnt);
+  if (lay.nq >= 2 * num_ctas)   // enough records to fill the GPU block by block
+    qprep_kernel<<<static_cast<unsigned>(lay.nq), 256, 0, stream>>>(p, lay, rec, hist, cand_cnt);
+  else
+    qprep_rows_kernel<<<dim3(static_cast<unsigned>(lay.nq), static_cast<unsigned>(lay.NR / 8)), 256, 0, stream>>>(
+        p, lay, rec, hist, cand_cnt);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // The scorer may launch while qprep_kernel runs: its producer waits for the
   // records (griddepcontrol.wait) only before the first record copy.
