@@ -768,7 +768,12 @@ def measure_score(W, args, K, dev, flush, dist, e2e, q_format="exact"):
     import numpy as np
     import torch
     import sparse_attention_top_paged_gb300 as idx
-    q = torch.from_numpy(W.q).to(dev)   # float32, resident in HBM for the device-timed leg
+    q = torch.from_numpy(W.q).to(dev)
+    # The workloads' queries are bf16 values (the page's launcher upcasts its
+    # bf16 q_I): they go in as bf16 (q_dtype BF16), which the library reads as
+    # exactly those float32 values; a float32-only q stays float32.
+    if torch.equal(q.to(torch.bfloat16).float(), q):
+        q = q.to(torch.bfloat16)
     w = torch.from_numpy(W.w).to(dev)
     bt = torch.from_numpy(W.block_table).to(dev)
     vl = torch.from_numpy(W.valid_lens).to(dev)
@@ -865,14 +870,9 @@ def measure_score(W, args, K, dev, flush, dist, e2e, q_format="exact"):
             total += (x.nbytes + 255) // 256 * 256
         return offs, total
 
-    # The workloads' queries are bf16 values (the page's launcher upcasts its
-    # bf16 q_I): from the host they travel as bf16 (q_dtype BF16, half the
-    # bytes), which the library reads as exactly those float32 values; a
-    # float32-only q travels as float32.
+    # q travels in the dtype the device-timed leg used
     tdt = {np.dtype(np.float32): torch.float32, np.dtype(np.int32): torch.int32, np.dtype(np.uint16): torch.bfloat16}
-    qt = torch.from_numpy(W.q)
-    q_host = (qt.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-              if torch.equal(qt.to(torch.bfloat16).float(), qt) else W.q)
+    q_host = (q.view(torch.int16).cpu().numpy().view(np.uint16) if q.dtype == torch.bfloat16 else W.q)
     in_parts = [q_host, W.w, W.block_table, W.valid_lens]
     in_offs, in_bytes = packed(in_parts)
     h_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
@@ -919,7 +919,6 @@ def measure_score(W, args, K, dev, flush, dist, e2e, q_format="exact"):
     # the host copy holds what the device-timed steps produced
     if not torch.equal(h_out[:W.T * k * 4].view(torch.int32).view(W.T, k), out_i.cpu()):
         raise RuntimeError("end-to-end top-k differs from the device-timed steps")
-    rec["config"]["e2e_q_dtype"] = "bfloat16" if q_host.dtype == np.uint16 else "float32"
     rec["e2e"] = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                   "ms_per_step": 1e3 * e2e_t / E,
                   "timing": "host perf_counter around copy in + ScoreTopkPlan.run + copy out + synchronize",

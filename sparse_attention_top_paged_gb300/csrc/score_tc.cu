@@ -225,22 +225,33 @@ __device__ long long block_incl_scan(long long v, long long *scratch, long long 
 // has a non-zero lo (never for bf16-valued q short of a 2^-31 dynamic range
 // within a head): the MMA reads it only then (the OR of the heads' flags).
 // NVFP4 q: the quantisation of nvfp4q.cuh, w' = w gq.
+// The raw loads (a float4, or four bf16 in .x/.y) are kept apart from their
+// conversion (head_row_values) so several rows' loads can be in flight.
 __device__ __forceinline__ void load_head_row(const ScoreParams &p, const TcLayout &lay, int tq, int n, int lane,
-                                              float4 &x, float &wv) {
+                                              uint4 &raw, float &wv) {
   const int h = n % lay.Npad, t = tq * lay.R + n / lay.Npad;
-  x = make_float4(0.f, 0.f, 0.f, 0.f);
+  raw = make_uint4(0u, 0u, 0u, 0u);
   wv = 0.0f;
   if (h < p.H && t < p.T) {
     const long long e0 = (static_cast<long long>(t) * p.H + h) * 128;
-    if (p.q16 != nullptr) {   // bf16: the float32 with the same leading 16 bits
+    if (p.q16 != nullptr) {
       const uint2 u = reinterpret_cast<const uint2 *>(p.q16 + e0)[lane];
-      x = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
-                      __uint_as_float(u.y & 0xFFFF0000u));
+      raw.x = u.x;
+      raw.y = u.y;
     } else {
-      x = reinterpret_cast<const float4 *>(p.q + e0)[lane];
+      raw = reinterpret_cast<const uint4 *>(p.q + e0)[lane];
     }
     wv = p.w[static_cast<long long>(t) * p.H + h];
   }
+}
+
+// This lane's 4 values of a head row from its raw load (bf16: the float32
+// with the same leading 16 bits).
+__device__ __forceinline__ float4 head_row_values(const ScoreParams &p, uint4 raw) {
+  if (p.q16 != nullptr)
+    return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                       __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+  return make_float4(__uint_as_float(raw.x), __uint_as_float(raw.y), __uint_as_float(raw.z), __uint_as_float(raw.w));
 }
 
 // The exact-q split of this lane's 4 values of head row n: its offset in the
@@ -299,21 +310,22 @@ __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay,
   }
   bool any_lo = false;
   for (int nb = warp; nb < lay.NR; nb += kAhead * kWarps) {
-    float4 x[kAhead];
+    uint4 raw[kAhead];
     float wv[kAhead];
 #pragma unroll
     for (int u = 0; u < kAhead; ++u) {
       const int n = nb + u * kWarps;
-      if (n < lay.NR) load_head_row(p, lay, tq, n, lane, x[u], wv[u]);
+      if (n < lay.NR) load_head_row(p, lay, tq, n, lane, raw[u], wv[u]);
     }
 #pragma unroll
     for (int u = 0; u < kAhead; ++u) {
       const int n = nb + u * kWarps;
       if (n >= lay.NR) continue;
+      const float4 xu = head_row_values(p, raw[u]);
       if (lay.fp4) {
         uint32_t codes16, scale;
         float gq;
-        nvfp4_quantize_lane(x[u], codes16, scale, gq);
+        nvfp4_quantize_lane(xu, codes16, scale, gq);
         // codes: bytes 2 lane, 2 lane + 1 of head row n (64 bytes, 64-byte swizzle in 8-row groups)
         const uint32_t off =
             (n >> 3) * 512 + (n & 7) * 64 + ((((lane >> 3) ^ ((n >> 1) & 3)) & 3) * 16) + ((2 * lane) & 15);
@@ -330,7 +342,7 @@ __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay,
         uint32_t off;
         uint2 vh, vl;
         float wq;
-        const bool row_lo = split_head_row(lay, n, lane, x[u], wv[u], off, vh, vl, wq);
+        const bool row_lo = split_head_row(lay, n, lane, xu, wv[u], off, vh, vl, wq);
         *reinterpret_cast<uint2 *>(r + off) = vh;
         any_lo |= row_lo;
         if (lane == 0) {
@@ -344,13 +356,13 @@ __global__ void __launch_bounds__(256) qprep_kernel(ScoreParams p, TcLayout lay,
   // has a non-zero lo (then every head's lo, zeros included, is written).
   if (lay.fp4 || !__syncthreads_or(any_lo)) return;
   for (int n = warp; n < lay.NR; n += kWarps) {
-    float4 x;
+    uint4 raw;
     float wv;
-    load_head_row(p, lay, tq, n, lane, x, wv);
+    load_head_row(p, lay, tq, n, lane, raw, wv);
     uint32_t off;
     uint2 vh, vl;
     float wq;
-    split_head_row(lay, n, lane, x, wv, off, vh, vl, wq);
+    split_head_row(lay, n, lane, head_row_values(p, raw), wv, off, vh, vl, wq);
     *reinterpret_cast<uint2 *>(r + lay.b_bytes + off) = vl;
   }
 }
@@ -380,9 +392,10 @@ __global__ void __launch_bounds__(256) qprep_rows_kernel(ScoreParams p, TcLayout
       if (((i >> 5) & 3) * 32 >= lay.NR) sw[i] = 0u;
   }
   if (n >= lay.NR) return;
-  float4 x;
+  uint4 raw;
   float wv;
-  load_head_row(p, lay, tq, n, lane, x, wv);
+  load_head_row(p, lay, tq, n, lane, raw, wv);
+  const float4 x = head_row_values(p, raw);
   if (lay.fp4) {
     uint32_t codes16, scale;
     float gq;
