@@ -558,7 +558,7 @@ def run_qsa_attn(args, rank, world):
             "gpu_launches": K,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": tensor, "unit": "TFLOP/s",
                          "frac": achieved / tensor, "traffic": None,
-                         "kernel": "qsa_prefill_attn_tile_kernel<128, 8>", "peak_kind": kind,
+                         "kernel": "qsa_prefill_attn_tc_kernel", "peak_kind": kind,
                          "algorithmic_flops_per_launch": flops,
                          "gathered_bytes_per_launch": gathered,
                          "gathered_gbs": gathered / (t_total / K) / 1e9},

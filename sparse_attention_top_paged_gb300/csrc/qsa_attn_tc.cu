@@ -1,0 +1,533 @@
+// qsa_attn_tc.cu — QSA prefill attention on the tcgen05 tensor cores, for 8
+// query heads per kv head and hd = 128 ("metrale_model_layers/layers/ops/qsa.rs",
+// qsa_prefill_attn: per (row, query head) one softmax over every token of the
+// row's selected complete blocks and over the incomplete tail, with K and V of
+// the head's kv head read through the page table).
+//
+// Work item = (row, kv head); its tokens are numbered list-major (token t of
+// selected block i is i * ratio + t; blocks that are not complete are
+// skipped), then the tail, and cut into steps of 128 tokens. The kernel is
+// persistent, one CTA per SM taking items blockIdx.x, blockIdx.x + gridDim.x,
+// ... Its steps, laid end to end, flow through a ring of kStages shared-memory
+// stages:
+//   warps 9-16  two producer groups of four warps taking the steps in turn.
+//               For each step a group looks up its 128 tokens (list entry,
+//               then page), copies their K and V rows (256 bytes each) into
+//               the stage with 16-byte asynchronous copies in the 128-byte
+//               swizzled layout the MMAs read (two 16 KB halves of 64
+//               dimensions, token t's half-row at t * 128 bytes; zero rows for
+//               tokens that are missing), writes the step's Qs operand (q *
+//               inv_sqrt_d of the 8 heads split into bf16 high parts, rows 0-7,
+//               and low parts, rows 8-15: q keeps about 17 significant bits)
+//               and the token mask. The copies arrive on the stage's barrier
+//               when they land, so a group never waits on its own copies.
+//   warp 8      MMA issuer (tcgen05, kind::f16, bf16 operands, f32 in tensor
+//               memory). Step j: S^T[128 tokens x 16] = K . Qs^T into one of
+//               two S slots (S = column h + column 8 + h), issued as soon as
+//               the stage is full, one step ahead of the value MMA of the step
+//               before, so it runs while the softmax of that step does; then,
+//               once the weights are written, O^T[128 dims x 16] += V^T . P^T
+//               with V read in place as an MN-major operand (the step's token
+//               rows are its K rows). Its commit frees the stage.
+//   warps 0-7   softmax: warp w owns tensor-memory lanes 32 (w % 4) .. + 31
+//               (tokens of S, dimensions of O) for heads 4 (w / 4) .. + 3. Per
+//               step: the heads' maxima over the step, a lazy reference maximum
+//               that moves only when a score exceeds it by more than kLazy
+//               (the running sums and the head's two output columns are then
+//               rescaled), weights p = exp(S - ref) split into bf16 high and
+//               low parts as the value MMA's B operand (two P slots). At the
+//               item's end: dimension d of head h = (column h + column 8 + h)
+//               / sum.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace idx {
+namespace {
+
+constexpr int kComputeWarps = 8;
+constexpr int kMmaWarp = kComputeWarps;
+constexpr int kProdWarp0 = kMmaWarp + 1;
+constexpr int kProdGroups = 2;
+constexpr int kThreads = 32 * (kProdWarp0 + 4 * kProdGroups);
+constexpr int kStages = 3;
+constexpr int kTok = 128, kHd = 128, kGroup = 8;
+constexpr float kLazy = 8.0f;
+// a stage: K rows, V rows (32 KB each), the Qs operand (16 rows x 128 dims), the token mask
+constexpr uint32_t kOffK = 0, kOffV = 32768, kOffQ = 65536, kOffMask = 69632;
+constexpr uint32_t kStageBytes = 70656;                  // 1 KB aligned
+constexpr uint32_t kOffP = kStages * kStageBytes;        // two P slots: 16 rows x 128 tokens each
+constexpr uint32_t kOffRed = kOffP + 2 * 4096;           // [4 lane quarters][8 heads] maxima, then 2 x sums
+constexpr uint32_t kOffBar = kOffRed + 3 * 4 * kGroup * 4;
+// per stage: full, empty; per slot (step parity): S^T written, weights written
+constexpr int B_FULL = 0, B_EMPTY = kStages, B_S = 2 * kStages, B_P = 2 * kStages + 2, B_COUNT = 2 * kStages + 4;
+constexpr uint32_t kOffMisc = kOffBar + 8 * B_COUNT;     // tensor-memory address, abort flag, bad-block flag
+constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;    // + slack to align the base to 1 KB
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+constexpr uint32_t kTmemCols = 64;                       // S slots: columns 0-15, 16-31; O: 32-47
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+// Shared-memory descriptor, 128-byte swizzle: K-major (lbo unused: 16) or
+// MN-major (lbo = the stride between 64-element atoms along M or N); sbo =
+// the stride between groups of 8 rows.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// kind::f16 instruction descriptor: f32 accumulator, bf16 A and B, M = 128,
+// N = 16; A MN-major (transposed) when mn_a.
+__host__ __device__ constexpr uint32_t idesc_bf16(bool mn_a) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (mn_a ? (1u << 15) : 0u) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&v)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(taddr)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&v)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// The barrier receives one arrival once every earlier asynchronous copy of
+// this thread has landed (its initial count includes these arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Barrier 1 over the softmax warps; returns whether `ok` holds in every one of
+// their threads.
+__device__ __forceinline__ bool compute_sync_and(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred a, b;\n setp.ne.u32 a, %1, 0;\n"
+      " barrier.cta.red.and.pred b, 1, %2, a;\n selp.u32 %0, 1, 0, b;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(ok)), "n"(32 * kComputeWarps)
+      : "memory");
+  return r != 0;
+}
+
+// The byte offset of element (row, col) of a 128-byte-swizzled operand whose
+// rows hold 64 bf16 elements and whose second 64 columns sit `half` bytes on.
+__device__ __forceinline__ uint32_t sw128(int row, int col, uint32_t half) {
+  return (col >> 6) * half + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) + (col & 7) * 2;
+}
+
+struct Problem {
+  const float *q;
+  const uint16_t *kc, *vc;
+  const int32_t *table, *lists;
+  float *out;
+  int n_pages, P;
+  uint32_t first_pos, topk, ratio, block_size, nq, nkv;
+  float inv_sqrt_d;
+};
+
+// One item's token numbering: list tokens [0, n_list), then the tail.
+struct Item {
+  long long r, kvh, ncomp, n_list, tail0, n_virt;
+  __device__ void set(const Problem &pr, long long w) {
+    r = w / pr.nkv;
+    kvh = w % pr.nkv;
+    const long long p = static_cast<long long>(pr.first_pos) + r;
+    ncomp = (p + 1) / pr.ratio;
+    n_list = static_cast<long long>(pr.topk) * pr.ratio;
+    tail0 = ncomp * pr.ratio;
+    n_virt = n_list + (p + 1 - tail0);
+  }
+  // K/V element offset of virtual token v, or -1 (no token); a missing page
+  // sets `bad`.
+  __device__ long long offset(const Problem &pr, long long v, bool &bad) const {
+    long long pos = -1;
+    if (v < n_list) {
+      const long long b = pr.lists[r * pr.topk + v / pr.ratio];
+      if (b >= 0 && b < ncomp) pos = b * pr.ratio + v % pr.ratio;
+    } else if (v < n_virt) {
+      pos = tail0 + (v - n_list);
+    }
+    if (pos < 0) return -1;
+    const long long pg = pos / pr.block_size;
+    const int page = pg < pr.n_pages ? pr.table[pg] : -1;
+    if (page < 0 || page >= pr.P) {
+      bad = true;
+      return -1;
+    }
+    return ((static_cast<long long>(page) * pr.block_size + pos % pr.block_size) * pr.nkv + kvh) * kHd;
+  }
+};
+
+// The steps of a CTA in order: items blockIdx.x + i * gridDim.x with at least
+// one token, 128 tokens at a time.
+struct StepWalk {
+  long long w, items, base;
+  Item it;
+  bool valid;
+  __device__ void seek(const Problem &pr) {   // from item w: the first one with tokens
+    for (; w < items; w += gridDim.x) {
+      it.set(pr, w);
+      if (it.n_virt > 0) {
+        base = 0;
+        valid = true;
+        return;
+      }
+    }
+    valid = false;
+  }
+  __device__ void next(const Problem &pr) {
+    base += kTok;
+    if (base >= it.n_virt) {
+      w += gridDim.x;
+      seek(pr);
+    }
+  }
+};
+
+// A producer group: steps g, g + kProdGroups, ... of the CTA's walk.
+__device__ void producer(const Problem &pr, long long items, unsigned char *sm, uint32_t s_base, int g, int pw,
+                         int lane, volatile int *abort, int *bad_flag) {
+  const int ptid = 32 * pw + lane;
+  const uint32_t bar0 = s_base + kOffBar;
+  StepWalk sw;
+  sw.w = blockIdx.x;
+  sw.items = items;
+  sw.seek(pr);
+  for (int i = 0; i < g && sw.valid; ++i) sw.next(pr);
+  bool bad = false;
+  for (long long j = g; sw.valid; j += kProdGroups) {
+    const int s = static_cast<int>(j % kStages);
+    const uint32_t par = static_cast<uint32_t>((j / kStages) & 1);
+    // the step's q values (8 a thread) and token lookups, before the stage is free
+    float qv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int x = ptid + 128 * i, h = x >> 7, d = x & 127;
+      qv[i] = pr.q[((sw.it.r * pr.nq) + sw.it.kvh * kGroup + h) * kHd + d];
+    }
+    const long long off = sw.it.offset(pr, sw.base + ptid, bad);
+    const uint32_t live = __ballot_sync(0xFFFFFFFFu, off >= 0);
+    if (!ptx::mbar_wait(bar0 + 8 * (B_EMPTY + s), par ^ 1u, abort, kWaitNs)) break;
+    unsigned char *st = sm + s * kStageBytes;
+    const uint32_t st_a = s_base + s * kStageBytes;
+    if (lane == 0) reinterpret_cast<uint32_t *>(st + kOffMask)[pw] = live;
+    // a half-warp copies one token's 256-byte K row and V row (16 lanes x 16 bytes)
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const int t = 2 * i + (lane >> 4), c = lane & 15;
+      const long long src = __shfl_sync(0xFFFFFFFFu, off, t);
+      const uint32_t o = sw128(32 * pw + t, 8 * c, 16384);
+      if (src >= 0) {
+        cp_async16(st_a + kOffK + o, pr.kc + src + 8 * c);
+        cp_async16(st_a + kOffV + o, pr.vc + src + 8 * c);
+      } else {   // no token: zero rows, so the value sum sees finite values
+        *reinterpret_cast<uint4 *>(st + kOffK + o) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(st + kOffV + o) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int x = ptid + 128 * i, h = x >> 7, d = x & 127;
+      const float v = qv[i] * pr.inv_sqrt_d;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      *reinterpret_cast<__nv_bfloat16 *>(st + kOffQ + sw128(h, d, 2048)) = hi;
+      *reinterpret_cast<__nv_bfloat16 *>(st + kOffQ + sw128(8 + h, d, 2048)) =
+          __float2bfloat16_rn(v - __bfloat162float(hi));   // v - hi is exact in f32
+    }
+    cp_async_arrive(bar0 + 8 * (B_FULL + s));   // when this thread's copies have landed
+    ptx::mbar_arrive(bar0 + 8 * (B_FULL + s));  // its plain stores (release)
+    for (int i = 0; i < kProdGroups && sw.valid; ++i) sw.next(pr);
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  if (bad) *bad_flag = 1;
+}
+
+// The MMA warp's S^T for step j (its stage is full): stage j % kStages, S slot j & 1.
+__device__ __forceinline__ void issue_scores(uint32_t s_base, uint32_t tmem, long long j) {
+  ptx::fence_proxy_async_smem();   // the producers' plain and copied stores, to the tensor cores
+  ptx::tc_fence_after();
+  const uint32_t st_a = s_base + static_cast<uint32_t>(j % kStages) * kStageBytes;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    mma_ss(tmem + 16 * static_cast<uint32_t>(j & 1), sdesc(st_a + kOffK + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+           sdesc(st_a + kOffQ + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024), idesc_bf16(false), k > 0 ? 1u : 0u);
+  ptx::mma_commit(s_base + kOffBar + 8 * (B_S + static_cast<int>(j & 1)));
+}
+
+// The MMA warp's O^T += V^T . P^T for step j (its weights are written); its
+// commit frees the stage.
+__device__ __forceinline__ void issue_values(uint32_t s_base, uint32_t tmem, long long j, bool first) {
+  ptx::tc_fence_after();
+  const uint32_t st_a = s_base + static_cast<uint32_t>(j % kStages) * kStageBytes;
+  const uint32_t p_a = s_base + kOffP + 4096u * static_cast<uint32_t>(j & 1);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    mma_ss(tmem + 32, sdesc(st_a + kOffV + k * 2048, 16384, 1024), sdesc(p_a + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024),
+           idesc_bf16(true), (!first || k > 0) ? 1u : 0u);
+  ptx::mma_commit(s_base + kOffBar + 8 * (B_EMPTY + static_cast<int>(j % kStages)));
+}
+
+__device__ __forceinline__ uint32_t full_bar(uint32_t bar0, long long j) {
+  return bar0 + 8 * (B_FULL + static_cast<int>(j % kStages));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) qsa_prefill_attn_tc_kernel(Problem pr, long long items,
+                                                                          int32_t *dev_status) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // aligned by pointer arithmetic on the shared array, so accesses through sm stay shared-space ones
+  unsigned char *sm = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
+  float *red = reinterpret_cast<float *>(sm + kOffRed);   // maxima [4][8], sums [2][4][8]
+  uint32_t *tmem_p = reinterpret_cast<uint32_t *>(sm + kOffMisc);
+  volatile int *abort = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
+  int *bad_flag = reinterpret_cast<int *>(sm + kOffMisc + 8);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t s_base = ptx::smem_addr(sm), bar0 = s_base + kOffBar;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(bar0 + 8 * (B_FULL + s), 2 * 128);   // 128 producer threads x (copies landed + stores)
+      ptx::mbar_init(bar0 + 8 * (B_EMPTY + s), 1);        // the commit after the step's value MMA
+    }
+    ptx::mbar_init(bar0 + 8 * B_S, 1);
+    ptx::mbar_init(bar0 + 8 * (B_S + 1), 1);
+    ptx::mbar_init(bar0 + 8 * B_P, 1);                     // one softmax thread, once the weights are written
+    ptx::mbar_init(bar0 + 8 * (B_P + 1), 1);
+    *abort = 0;
+    *bad_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) ptx::tmem_alloc(ptx::smem_addr(tmem_p), kTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_p;
+
+  if (warp >= kProdWarp0) {
+    const int pwarp = warp - kProdWarp0;
+    producer(pr, items, sm, s_base, pwarp / 4, pwarp % 4, lane, abort, bad_flag);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      StepWalk sw;
+      sw.w = blockIdx.x;
+      sw.items = items;
+      sw.seek(pr);
+      bool ok = !sw.valid || ptx::mbar_wait(full_bar(bar0, 0), 0u, abort, kWaitNs);
+      if (sw.valid && ok) issue_scores(s_base, tmem, 0);
+      // Step j: S^T of step j + 1 once its stage is full (its S slot was last read
+      // before the weights of step j - 1) and O of step j once its weights are
+      // written, whichever can go first.
+      for (long long j = 0; sw.valid && ok; ++j) {
+        const bool first = sw.base == 0;   // the step starts an item: O restarts
+        StepWalk nx = sw;
+        nx.next(pr);
+        bool s_done = !nx.valid, o_done = false;
+        const uint32_t fb = full_bar(bar0, j + 1), pb = bar0 + 8 * (B_P + static_cast<int>(j & 1));
+        const uint32_t fpar = static_cast<uint32_t>(((j + 1) / kStages) & 1), ppar = static_cast<uint32_t>((j >> 1) & 1);
+        const uint64_t t0 = ptx::globaltimer();
+        // (suspending waits of a few tens of ns, so the poll takes no issue slots from the softmax warps)
+        for (uint32_t it = 1; !(s_done && o_done); ++it) {
+          if (!s_done && ptx::mbar_try_wait(fb, fpar, o_done ? 1000u : 32u)) {
+            issue_scores(s_base, tmem, j + 1);
+            s_done = true;
+          } else if (!o_done && ptx::mbar_try_wait(pb, ppar, s_done ? 1000u : 32u)) {
+            issue_values(s_base, tmem, j, first);
+            o_done = true;
+          } else if ((it & 63u) == 0u && (*abort || ptx::globaltimer() - t0 > kWaitNs)) {
+            *abort = 1;
+            ok = false;
+            break;
+          }
+        }
+        sw = nx;
+      }
+    }
+    __syncwarp();
+  } else {
+    const int qd = warp & 3, hh = warp >> 2;   // lane quarter; heads 4 hh .. 4 hh + 3
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+    bool ok = true;
+    long long j = 0;                           // the CTA's step counter
+    int item_parity = 0;
+    for (long long w = blockIdx.x; w < items && ok; w += gridDim.x, item_parity ^= 1) {
+      Item it;
+      it.set(pr, w);
+      float mref[4], lsum[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        mref[i] = -INFINITY;
+        lsum[i] = 0.0f;
+      }
+      for (long long base = 0; base < it.n_virt; base += kTok, ++j) {
+        const int s = static_cast<int>(j % kStages), b = static_cast<int>(j & 1);
+        // the stage's mask (producers' stores) and the step's S^T
+        bool w_ok = ptx::mbar_wait(bar0 + 8 * (B_FULL + s), static_cast<uint32_t>((j / kStages) & 1), abort, kWaitNs);
+        w_ok = w_ok && ptx::mbar_wait(bar0 + 8 * (B_S + b), static_cast<uint32_t>((j >> 1) & 1), abort, kWaitNs);
+        ptx::tc_fence_after();
+        const bool valid = (reinterpret_cast<const uint32_t *>(sm + s * kStageBytes + kOffMask)[qd] >> lane) & 1u;
+        uint32_t shi[4], slo[4];
+        tmem_ld4(t_lane + 16 * b + 4 * hh, shi);
+        tmem_ld4(t_lane + 16 * b + 8 + 4 * hh, slo);
+        ptx::tmem_wait_ld();
+        float sc[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          sc[i] = valid ? __uint_as_float(shi[i]) + __uint_as_float(slo[i]) : -INFINITY;
+          float m = sc[i];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+          if (lane == 0) red[qd * kGroup + 4 * hh + i] = m;
+        }
+        ok = compute_sync_and(w_ok);
+        if (!ok) break;
+        uint32_t rescale = 0;   // bit i: head 4 hh + i's reference moved after an earlier step contributed
+        float corr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int h = 4 * hh + i;
+          const float tm = fmaxf(fmaxf(red[h], red[kGroup + h]), fmaxf(red[2 * kGroup + h], red[3 * kGroup + h]));
+          corr[i] = 1.0f;
+          if (tm > mref[i] + kLazy) {   // (also the head's first finite score: mref = -inf)
+            corr[i] = (mref[i] == -INFINITY) ? 0.0f : __expf(mref[i] - tm);
+            if (base > 0) rescale |= 1u << i;
+            mref[i] = tm;
+            lsum[i] *= corr[i];
+          }
+        }
+        if (rescale) {   // the value MMA of step j - 1 is done once its stage is free again
+          const long long jp = j - 1;
+          w_ok = ptx::mbar_wait(bar0 + 8 * (B_EMPTY + static_cast<int>(jp % kStages)),
+                                static_cast<uint32_t>((jp / kStages) & 1), abort, kWaitNs);
+          ptx::tc_fence_after();
+          uint32_t ohi[4], olo[4];
+          tmem_ld4(t_lane + 32 + 4 * hh, ohi);
+          tmem_ld4(t_lane + 40 + 4 * hh, olo);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if ((rescale >> i) & 1u) {
+              ohi[i] = __float_as_uint(__uint_as_float(ohi[i]) * corr[i]);
+              olo[i] = __float_as_uint(__uint_as_float(olo[i]) * corr[i]);
+            }
+          tmem_st4(t_lane + 32 + 4 * hh, ohi);
+          tmem_st4(t_lane + 40 + 4 * hh, olo);
+          ptx::tmem_wait_st();
+        }
+        // P slot b was last read by the value MMA of step j - 2, done before the S^T of step j
+        unsigned char *pb = sm + kOffP + 4096 * b;
+        const int tok = 32 * qd + lane;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int h = 4 * hh + i;
+          // ex2-based exp: the argument is at most kLazy; relative error a few 1e-7
+          const float e = (sc[i] != -INFINITY) ? __expf(sc[i] - mref[i]) : 0.0f;
+          lsum[i] += e;
+          const __nv_bfloat16 ehi = __float2bfloat16_rn(e);
+          *reinterpret_cast<__nv_bfloat16 *>(pb + sw128(h, tok, 2048)) = ehi;
+          *reinterpret_cast<__nv_bfloat16 *>(pb + sw128(8 + h, tok, 2048)) =
+              __float2bfloat16_rn(e - __bfloat162float(ehi));
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ok = compute_sync_and(w_ok);
+        if (!ok) break;
+        if (tid == 0) ptx::mbar_arrive(bar0 + 8 * (B_P + b));
+      }
+      if (!ok) break;
+      // ---- the item's sums and output ----
+      bool w_ok = true;
+      if (it.n_virt > 0) {   // O is complete once the last step's stage is free again
+        const long long jp = j - 1;
+        w_ok = ptx::mbar_wait(bar0 + 8 * (B_EMPTY + static_cast<int>(jp % kStages)),
+                              static_cast<uint32_t>((jp / kStages) & 1), abort, kWaitNs);
+        ptx::tc_fence_after();
+      }
+      float *rs = red + 4 * kGroup * (1 + item_parity);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float l = lsum[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
+        if (lane == 0) rs[qd * kGroup + 4 * hh + i] = l;
+      }
+      ok = compute_sync_and(w_ok);
+      if (!ok) break;
+      uint32_t ohi[4] = {0u, 0u, 0u, 0u}, olo[4] = {0u, 0u, 0u, 0u};
+      if (it.n_virt > 0) {
+        tmem_ld4(t_lane + 32 + 4 * hh, ohi);
+        tmem_ld4(t_lane + 40 + 4 * hh, olo);
+        ptx::tmem_wait_ld();
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int h = 4 * hh + i;
+        const float L = rs[h] + rs[kGroup + h] + rs[2 * kGroup + h] + rs[3 * kGroup + h];
+        const float o = __uint_as_float(ohi[i]) + __uint_as_float(olo[i]);
+        pr.out[((it.r * pr.nq) + it.kvh * kGroup + h) * kHd + 32 * qd + lane] = L > 0.0f ? o / L : 0.0f;
+      }
+      ptx::tc_fence_before();   // the reads of O come before the next item's first value MMA
+    }
+    if (!ok) *abort = 1;
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && dev_status) {
+    if (*bad_flag) atomicOr(dev_status, IDX_STATUS_BAD_BLOCK);
+    if (*abort) atomicOr(dev_status, IDX_STATUS_TIMEOUT);
+  }
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool qsa_attn_tc_supported(uint32_t nq, uint32_t nkv, uint32_t hd, const void *kc, const void *vc) {
+  return hd == kHd && nkv > 0 && nq == nkv * kGroup && (reinterpret_cast<uintptr_t>(kc) & 15u) == 0 &&
+         (reinterpret_cast<uintptr_t>(vc) & 15u) == 0;
+}
+
+cudaError_t launch_qsa_attn_tc(const float *q, const uint16_t *kc, const uint16_t *vc, const int32_t *table,
+                               int n_pages, int P, const int32_t *lists, float *out, uint32_t rows, uint32_t first_pos,
+                               uint32_t topk, uint32_t ratio, uint32_t block_size, uint32_t nq, uint32_t nkv,
+                               float inv_sqrt_d, int32_t *dev_status, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // set on every call: the attribute belongs to the current device's context
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(qsa_prefill_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  const long long items = static_cast<long long>(rows) * nkv;
+  const int grid = static_cast<int>(items < sms ? items : sms);
+  const Problem pr{q, kc, vc, table, lists, out, n_pages, P, first_pos, topk, ratio, block_size, nq, nkv, inv_sqrt_d};
+  qsa_prefill_attn_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(pr, items, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace idx

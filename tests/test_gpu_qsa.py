@@ -238,16 +238,35 @@ def test_qsa_prefill_attn_cache_8_byte_aligned(which):
     assert np.max(np.abs(got.cpu().numpy() - ref)) <= 1e-4 * np.max(np.abs(ref))
 
 
-def test_qsa_prefill_attn_missing_page_and_first_rows():
+@pytest.mark.parametrize("scale,topk,ratio,first_pos", [(6.0, 64, 16, 3000), (6.0, 300, 4, 2000), (1.0, 5, 16, 700),
+                                                        (12.0, 129, 8, 1200), (0.0, 64, 16, 3000)])
+def test_qsa_prefill_attn_tensor_core_tiles(scale, topk, ratio, first_pos):
+    """8 query heads per kv head at hd 128 (the tcgen05 kernel's 128-token
+    tiles): peaked scores that move the lazy reference maximum between tiles,
+    up to 10 tiles a row with a ragged last tile, a single partial tile, and
+    constant scores (q = 0: plain means of V)."""
+    q, kb, vb, table, lists, fp, ratio = _attn_case(90 + topk, 128, 32, 4, rows=7, first_pos=first_pos,
+                                                    ratio=ratio, topk=topk)
+    q = (q * scale).astype(np.float32)
+    got, st = _attn_gpu(q, kb, vb, table, lists, fp, ratio)
+    ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
+                                       1.0 / math.sqrt(128))
+    assert st == ost == 0
+    assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
+
+
+@pytest.mark.parametrize("nq", [8, 16])
+def test_qsa_prefill_attn_missing_page_and_first_rows(nq):
     """A page missing from the table drops its tokens (reported); rows at
-    positions 0.. attend to their tails alone."""
-    q, kb, vb, table, lists, fp, ratio = _attn_case(41, 128, 8, 2, rows=20, first_pos=0, bad_page=0)
+    positions 0.. attend to their tails alone (4 and 8 query heads per kv
+    head)."""
+    q, kb, vb, table, lists, fp, ratio = _attn_case(41, 128, nq, 2, rows=20, first_pos=0, bad_page=0)
     got, st = _attn_gpu(q, kb, vb, table, lists, fp, ratio)
     ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
                                        1.0 / math.sqrt(128))
     assert st == ost == oracle.STATUS_BAD_BLOCK
     assert np.max(np.abs(got - ref)) <= 1e-4 * max(np.max(np.abs(ref)), 1.0)
-    q, kb, vb, table, lists, fp, ratio = _attn_case(42, 128, 8, 2, rows=40, first_pos=0, bad_page=1)
+    q, kb, vb, table, lists, fp, ratio = _attn_case(42, 128, nq, 2, rows=40, first_pos=0, bad_page=1)
     got, st = _attn_gpu(q, kb, vb, table, lists, fp, ratio)
     ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
                                        1.0 / math.sqrt(128))
