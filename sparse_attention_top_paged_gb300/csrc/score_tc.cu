@@ -430,7 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint8_t *__restrict__ qrec, uint32_t *__restrict__ hist, float *__restrict__ scores,
                     long long ld) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // aligned by pointer arithmetic on the shared array, so accesses through sm stay shared-space ones
+  uint8_t *sm = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + lay.off_bar);
   int *misc = reinterpret_cast<int *>(sm + lay.off_misc);
