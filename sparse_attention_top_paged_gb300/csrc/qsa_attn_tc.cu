@@ -18,9 +18,10 @@
 //               dimensions, token t's half-row at t * 128 bytes; zero rows for
 //               tokens that are missing), writes the step's Qs operand (q *
 //               inv_sqrt_d of the 8 heads split into bf16 high parts, rows 0-7,
-//               and low parts, rows 8-15: q keeps about 17 significant bits)
-//               and the token mask. The copies arrive on the stage's barrier
-//               when they land, so a group never waits on its own copies.
+//               and low parts, rows 8-15, once per item: q keeps about 17
+//               significant bits) and the token mask. The copies arrive on the
+//               stage's barrier when they land, so a group never waits on its
+//               own copies.
 //   warp 8      MMA issuer (tcgen05, kind::f16, bf16 operands, f32 in tensor
 //               memory). Step j: S^T[128 tokens x 16] = K . Qs^T into one of
 //               two S slots (S = column h + column 8 + h), issued as soon as
@@ -132,6 +133,24 @@ __device__ __forceinline__ bool compute_sync_and(bool ok) {
   return r != 0;
 }
 
+// Barrier 1 over the softmax warps; returns how many of their threads have
+// `pred` set.
+__device__ __forceinline__ uint32_t compute_sync_count(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred a;\n setp.ne.u32 a, %1, 0;\n barrier.cta.red.popc.u32 %0, 1, %2, a;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "n"(32 * kComputeWarps)
+      : "memory");
+  return r;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 // The byte offset of element (row, col) of a 128-byte-swizzled operand whose
 // rows hold 64 bf16 elements and whose second 64 columns sit `half` bytes on.
 __device__ __forceinline__ uint32_t sw128(int row, int col, uint32_t half) {
@@ -159,25 +178,6 @@ struct Item {
     n_list = static_cast<long long>(pr.topk) * pr.ratio;
     tail0 = ncomp * pr.ratio;
     n_virt = n_list + (p + 1 - tail0);
-  }
-  // K/V element offset of virtual token v, or -1 (no token); a missing page
-  // sets `bad`.
-  __device__ long long offset(const Problem &pr, long long v, bool &bad) const {
-    long long pos = -1;
-    if (v < n_list) {
-      const long long b = pr.lists[r * pr.topk + v / pr.ratio];
-      if (b >= 0 && b < ncomp) pos = b * pr.ratio + v % pr.ratio;
-    } else if (v < n_virt) {
-      pos = tail0 + (v - n_list);
-    }
-    if (pos < 0) return -1;
-    const long long pg = pos / pr.block_size;
-    const int page = pg < pr.n_pages ? pr.table[pg] : -1;
-    if (page < 0 || page >= pr.P) {
-      bad = true;
-      return -1;
-    }
-    return ((static_cast<long long>(page) * pr.block_size + pos % pr.block_size) * pr.nkv + kvh) * kHd;
   }
 };
 
@@ -207,7 +207,8 @@ struct StepWalk {
   }
 };
 
-// A producer group: steps g, g + kProdGroups, ... of the CTA's walk.
+// A producer group (four warps, a token a thread): steps g, g + kProdGroups,
+// ... of the CTA's walk; the groups' copies of consecutive steps overlap.
 __device__ void producer(const Problem &pr, long long items, unsigned char *sm, uint32_t s_base, int g, int pw,
                          int lane, volatile int *abort, int *bad_flag) {
   const int ptid = 32 * pw + lane;
@@ -218,17 +219,50 @@ __device__ void producer(const Problem &pr, long long items, unsigned char *sm, 
   sw.seek(pr);
   for (int i = 0; i < g && sw.valid; ++i) sw.next(pr);
   bool bad = false;
+  long long q_item = -1;   // the item whose Qs share this thread holds
+  // this thread's share of the item's Qs operand: dimension pairs x = ptid + 128 i
+  // (head x / 64, dimensions 2 (x % 64) and + 1), bf16 high and low parts
+  uint32_t qhi[4] = {0u, 0u, 0u, 0u}, qlo[4] = {0u, 0u, 0u, 0u};
   for (long long j = g; sw.valid; j += kProdGroups) {
     const int s = static_cast<int>(j % kStages);
     const uint32_t par = static_cast<uint32_t>((j / kStages) & 1);
-    // the step's q values (8 a thread) and token lookups, before the stage is free
-    float qv[8];
+    if (sw.w != q_item) {   // the group's first step of an item: its q rows, scaled and split once
+      q_item = sw.w;
+      float2 v[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int x = ptid + 128 * i, h = x >> 7, d = x & 127;
-      qv[i] = pr.q[((sw.it.r * pr.nq) + sw.it.kvh * kGroup + h) * kHd + d];
+      for (int i = 0; i < 4; ++i) {
+        const int x = ptid + 128 * i, h = x >> 6, d = 2 * (x & 63);
+        v[i] = *reinterpret_cast<const float2 *>(pr.q + ((sw.it.r * pr.nq) + sw.it.kvh * kGroup + h) * kHd + d);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a0 = v[i].x * pr.inv_sqrt_d, a1 = v[i].y * pr.inv_sqrt_d;
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(a0, a1);
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(a0 - __low2float(hi), a1 - __high2float(hi));   // exact differences
+        qhi[i] = *reinterpret_cast<const uint32_t *>(&hi);
+        qlo[i] = *reinterpret_cast<const uint32_t *>(&lo);
+      }
     }
-    const long long off = sw.it.offset(pr, sw.base + ptid, bad);
+    // this thread's token (list entry, then page), before the stage is free
+    long long off = -1;
+    {
+      const long long v = sw.base + ptid;
+      long long pos = -1;
+      if (v < sw.it.n_list) {
+        const long long b = pr.lists[sw.it.r * pr.topk + v / pr.ratio];
+        if (b >= 0 && b < sw.it.ncomp) pos = b * pr.ratio + v % pr.ratio;
+      } else if (v < sw.it.n_virt) {
+        pos = sw.it.tail0 + (v - sw.it.n_list);
+      }
+      if (pos >= 0) {
+        const long long pg = pos / pr.block_size;
+        const int page = pg < pr.n_pages ? pr.table[pg] : -1;
+        if (page < 0 || page >= pr.P)
+          bad = true;
+        else
+          off = ((static_cast<long long>(page) * pr.block_size + pos % pr.block_size) * pr.nkv + sw.it.kvh) * kHd;
+      }
+    }
     const uint32_t live = __ballot_sync(0xFFFFFFFFu, off >= 0);
     if (!ptx::mbar_wait(bar0 + 8 * (B_EMPTY + s), par ^ 1u, abort, kWaitNs)) break;
     unsigned char *st = sm + s * kStageBytes;
@@ -249,13 +283,10 @@ __device__ void producer(const Problem &pr, long long items, unsigned char *sm, 
       }
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int x = ptid + 128 * i, h = x >> 7, d = x & 127;
-      const float v = qv[i] * pr.inv_sqrt_d;
-      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-      *reinterpret_cast<__nv_bfloat16 *>(st + kOffQ + sw128(h, d, 2048)) = hi;
-      *reinterpret_cast<__nv_bfloat16 *>(st + kOffQ + sw128(8 + h, d, 2048)) =
-          __float2bfloat16_rn(v - __bfloat162float(hi));   // v - hi is exact in f32
+    for (int i = 0; i < 4; ++i) {
+      const int x = ptid + 128 * i, h = x >> 6, d = 2 * (x & 63);
+      *reinterpret_cast<uint32_t *>(st + kOffQ + sw128(h, d, 2048)) = qhi[i];
+      *reinterpret_cast<uint32_t *>(st + kOffQ + sw128(8 + h, d, 2048)) = qlo[i];
     }
     cp_async_arrive(bar0 + 8 * (B_FULL + s));   // when this thread's copies have landed
     ptx::mbar_arrive(bar0 + 8 * (B_FULL + s));  // its plain stores (release)
@@ -265,36 +296,45 @@ __device__ void producer(const Problem &pr, long long items, unsigned char *sm, 
   if (bad) *bad_flag = 1;
 }
 
-// The MMA warp's S^T for step j (its stage is full): stage j % kStages, S slot j & 1.
+// The MMA warp's S^T for step j (its stage is full): stage j % kStages, S slot
+// j & 1. The whole warp calls it (operands stay warp-uniform); one lane issues.
 __device__ __forceinline__ void issue_scores(uint32_t s_base, uint32_t tmem, long long j) {
-  ptx::fence_proxy_async_smem();   // the producers' plain and copied stores, to the tensor cores
-  ptx::tc_fence_after();
   const uint32_t st_a = s_base + static_cast<uint32_t>(j % kStages) * kStageBytes;
+  const uint32_t d = tmem + 16 * static_cast<uint32_t>(j & 1);
+  if (ptx::elect_one()) {
+    ptx::fence_proxy_async_smem();   // the producers' plain and copied stores, to the tensor cores
+    ptx::tc_fence_after();
 #pragma unroll
-  for (int k = 0; k < 8; ++k)
-    mma_ss(tmem + 16 * static_cast<uint32_t>(j & 1), sdesc(st_a + kOffK + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-           sdesc(st_a + kOffQ + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024), idesc_bf16(false), k > 0 ? 1u : 0u);
-  ptx::mma_commit(s_base + kOffBar + 8 * (B_S + static_cast<int>(j & 1)));
+    for (int k = 0; k < 8; ++k)
+      mma_ss(d, sdesc(st_a + kOffK + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+             sdesc(st_a + kOffQ + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024), idesc_bf16(false), k > 0 ? 1u : 0u);
+    ptx::mma_commit(s_base + kOffBar + 8 * (B_S + static_cast<int>(j & 1)));
+  }
+  __syncwarp();
 }
 
 // The MMA warp's O^T += V^T . P^T for step j (its weights are written); its
 // commit frees the stage.
 __device__ __forceinline__ void issue_values(uint32_t s_base, uint32_t tmem, long long j, bool first) {
-  ptx::tc_fence_after();
   const uint32_t st_a = s_base + static_cast<uint32_t>(j % kStages) * kStageBytes;
   const uint32_t p_a = s_base + kOffP + 4096u * static_cast<uint32_t>(j & 1);
+  if (ptx::elect_one()) {
+    ptx::tc_fence_after();
 #pragma unroll
-  for (int k = 0; k < 8; ++k)
-    mma_ss(tmem + 32, sdesc(st_a + kOffV + k * 2048, 16384, 1024), sdesc(p_a + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024),
-           idesc_bf16(true), (!first || k > 0) ? 1u : 0u);
-  ptx::mma_commit(s_base + kOffBar + 8 * (B_EMPTY + static_cast<int>(j % kStages)));
+    for (int k = 0; k < 8; ++k)
+      mma_ss(tmem + 32, sdesc(st_a + kOffV + k * 2048, 16384, 1024),
+             sdesc(p_a + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024), idesc_bf16(true), (!first || k > 0) ? 1u : 0u);
+    ptx::mma_commit(s_base + kOffBar + 8 * (B_EMPTY + static_cast<int>(j % kStages)));
+  }
+  __syncwarp();
 }
 
 __device__ __forceinline__ uint32_t full_bar(uint32_t bar0, long long j) {
   return bar0 + 8 * (B_FULL + static_cast<int>(j % kStages));
 }
 
-__global__ void __launch_bounds__(kThreads, 1) qsa_prefill_attn_tc_kernel(Problem pr, long long items,
+// 17 warps (20 for register allocation, in groups of 4): at most 96 registers a thread
+__global__ void __maxnreg__(96) qsa_prefill_attn_tc_kernel(Problem pr, long long items,
                                                                           int32_t *dev_status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // aligned by pointer arithmetic on the shared array, so accesses through sm stay shared-space ones
@@ -308,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prefill_attn_tc_kernel(Proble
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(bar0 + 8 * (B_FULL + s), 2 * 128);   // 128 producer threads x (copies landed + stores)
+      ptx::mbar_init(bar0 + 8 * (B_FULL + s), 2 * 128);   // a group's 128 threads x (copies landed + stores)
       ptx::mbar_init(bar0 + 8 * (B_EMPTY + s), 1);        // the commit after the step's value MMA
     }
     ptx::mbar_init(bar0 + 8 * B_S, 1);
@@ -329,40 +369,42 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prefill_attn_tc_kernel(Proble
     const int pwarp = warp - kProdWarp0;
     producer(pr, items, sm, s_base, pwarp / 4, pwarp % 4, lane, abort, bad_flag);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      StepWalk sw;
-      sw.w = blockIdx.x;
-      sw.items = items;
-      sw.seek(pr);
-      bool ok = !sw.valid || ptx::mbar_wait(full_bar(bar0, 0), 0u, abort, kWaitNs);
-      if (sw.valid && ok) issue_scores(s_base, tmem, 0);
-      // Step j: S^T of step j + 1 once its stage is full (its S slot was last read
-      // before the weights of step j - 1) and O of step j once its weights are
-      // written, whichever can go first.
-      for (long long j = 0; sw.valid && ok; ++j) {
-        const bool first = sw.base == 0;   // the step starts an item: O restarts
-        StepWalk nx = sw;
-        nx.next(pr);
-        bool s_done = !nx.valid, o_done = false;
-        const uint32_t fb = full_bar(bar0, j + 1), pb = bar0 + 8 * (B_P + static_cast<int>(j & 1));
-        const uint32_t fpar = static_cast<uint32_t>(((j + 1) / kStages) & 1), ppar = static_cast<uint32_t>((j >> 1) & 1);
-        const uint64_t t0 = ptx::globaltimer();
-        // (suspending waits of a few tens of ns, so the poll takes no issue slots from the softmax warps)
-        for (uint32_t it = 1; !(s_done && o_done); ++it) {
-          if (!s_done && ptx::mbar_try_wait(fb, fpar, o_done ? 1000u : 32u)) {
-            issue_scores(s_base, tmem, j + 1);
-            s_done = true;
-          } else if (!o_done && ptx::mbar_try_wait(pb, ppar, s_done ? 1000u : 32u)) {
-            issue_values(s_base, tmem, j, first);
-            o_done = true;
-          } else if ((it & 63u) == 0u && (*abort || ptx::globaltimer() - t0 > kWaitNs)) {
-            *abort = 1;
-            ok = false;
-            break;
-          }
+    // The whole warp walks the steps in lockstep; one elected lane issues.
+    StepWalk sw;
+    sw.w = blockIdx.x;
+    sw.items = items;
+    sw.seek(pr);
+    bool ok = !sw.valid || ptx::mbar_wait(full_bar(bar0, 0), 0u, abort, kWaitNs);
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    if (sw.valid && ok) issue_scores(s_base, tmem, 0);
+    // Step j: S^T of step j + 1 once its stage is full (its S slot was last read
+    // before the weights of step j - 1) and O of step j once its weights are
+    // written, whichever can go first.
+    for (long long j = 0; sw.valid && ok; ++j) {
+      const bool first = sw.base == 0;   // the step starts an item: O restarts
+      StepWalk nx = sw;
+      nx.next(pr);
+      bool s_done = !nx.valid, o_done = false;
+      const uint32_t fb = full_bar(bar0, j + 1), pb = bar0 + 8 * (B_P + static_cast<int>(j & 1));
+      const uint32_t fpar = static_cast<uint32_t>(((j + 1) / kStages) & 1), ppar = static_cast<uint32_t>((j >> 1) & 1);
+      const uint64_t t0 = ptx::globaltimer();
+      // (suspending waits of a few tens of ns, so the poll takes no issue slots from the softmax warps;
+      // lane 0's view decides for the warp)
+      for (uint32_t it = 1; !(s_done && o_done); ++it) {
+        if (!s_done && __shfl_sync(0xFFFFFFFFu, ptx::mbar_try_wait(fb, fpar, o_done ? 1000u : 32u), 0)) {
+          issue_scores(s_base, tmem, j + 1);
+          s_done = true;
+        } else if (!o_done && __shfl_sync(0xFFFFFFFFu, ptx::mbar_try_wait(pb, ppar, s_done ? 1000u : 32u), 0)) {
+          issue_values(s_base, tmem, j, first);
+          o_done = true;
+        } else if ((it & 63u) == 0u &&
+                   __shfl_sync(0xFFFFFFFFu, *abort != 0 || ptx::globaltimer() - t0 > kWaitNs, 0)) {
+          *abort = 1;
+          ok = false;
+          break;
         }
-        sw = nx;
       }
+      sw = nx;
     }
     __syncwarp();
   } else {
@@ -371,6 +413,22 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prefill_attn_tc_kernel(Proble
     bool ok = true;
     long long j = 0;                           // the CTA's step counter
     int item_parity = 0;
+    unsigned char *pslot = sm + kOffP;
+    const int tok = 32 * qd + lane;
+    // this thread's weights p = exp(S - ref) of heads 4 hh .. + 3 (token tok) into a P
+    // slot, split into bf16 high (rows h) and low (rows 8 + h) parts; their sum in lp
+    auto write_weights = [&](unsigned char *pb, const float (&sc)[4], const float (&mref)[4], float (&lp)[4]) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int h = 4 * hh + i;
+        // ex2-based exp: the argument is at most kLazy; relative error a few 1e-7
+        const float e = (sc[i] != -INFINITY) ? __expf(sc[i] - mref[i]) : 0.0f;
+        lp[i] = e;
+        const __nv_bfloat16 ehi = __float2bfloat16_rn(e);
+        *reinterpret_cast<__nv_bfloat16 *>(pb + sw128(h, tok, 2048)) = ehi;
+        *reinterpret_cast<__nv_bfloat16 *>(pb + sw128(8 + h, tok, 2048)) = __float2bfloat16_rn(e - __bfloat162float(ehi));
+      }
+    };
     for (long long w = blockIdx.x; w < items && ok; w += gridDim.x, item_parity ^= 1) {
       Item it;
       it.set(pr, w);
@@ -392,67 +450,71 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prefill_attn_tc_kernel(Proble
         tmem_ld4(t_lane + 16 * b + 8 + 4 * hh, slo);
         ptx::tmem_wait_ld();
         float sc[4];
+        bool exceed = false;   // a score above its head's reference by more than kLazy
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           sc[i] = valid ? __uint_as_float(shi[i]) + __uint_as_float(slo[i]) : -INFINITY;
-          float m = sc[i];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-          if (lane == 0) red[qd * kGroup + 4 * hh + i] = m;
+          exceed |= sc[i] > mref[i] + kLazy;   // (any finite score while mref = -inf)
         }
-        ok = compute_sync_and(w_ok);
-        if (!ok) break;
-        uint32_t rescale = 0;   // bit i: head 4 hh + i's reference moved after an earlier step contributed
-        float corr[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int h = 4 * hh + i;
-          const float tm = fmaxf(fmaxf(red[h], red[kGroup + h]), fmaxf(red[2 * kGroup + h], red[3 * kGroup + h]));
-          corr[i] = 1.0f;
-          if (tm > mref[i] + kLazy) {   // (also the head's first finite score: mref = -inf)
-            corr[i] = (mref[i] == -INFINITY) ? 0.0f : __expf(mref[i] - tm);
-            if (base > 0) rescale |= 1u << i;
-            mref[i] = tm;
-            lsum[i] *= corr[i];
-          }
-        }
-        if (rescale) {   // the value MMA of step j - 1 is done once its stage is free again
-          const long long jp = j - 1;
-          w_ok = ptx::mbar_wait(bar0 + 8 * (B_EMPTY + static_cast<int>(jp % kStages)),
-                                static_cast<uint32_t>((jp / kStages) & 1), abort, kWaitNs);
-          ptx::tc_fence_after();
-          uint32_t ohi[4], olo[4];
-          tmem_ld4(t_lane + 32 + 4 * hh, ohi);
-          tmem_ld4(t_lane + 40 + 4 * hh, olo);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if ((rescale >> i) & 1u) {
-              ohi[i] = __float_as_uint(__uint_as_float(ohi[i]) * corr[i]);
-              olo[i] = __float_as_uint(__uint_as_float(olo[i]) * corr[i]);
-            }
-          tmem_st4(t_lane + 32 + 4 * hh, ohi);
-          tmem_st4(t_lane + 40 + 4 * hh, olo);
-          ptx::tmem_wait_st();
-        }
-        // P slot b was last read by the value MMA of step j - 2, done before the S^T of step j
-        unsigned char *pb = sm + kOffP + 4096 * b;
-        const int tok = 32 * qd + lane;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int h = 4 * hh + i;
-          // ex2-based exp: the argument is at most kLazy; relative error a few 1e-7
-          const float e = (sc[i] != -INFINITY) ? __expf(sc[i] - mref[i]) : 0.0f;
-          lsum[i] += e;
-          const __nv_bfloat16 ehi = __float2bfloat16_rn(e);
-          *reinterpret_cast<__nv_bfloat16 *>(pb + sw128(h, tok, 2048)) = ehi;
-          *reinterpret_cast<__nv_bfloat16 *>(pb + sw128(8 + h, tok, 2048)) =
-              __float2bfloat16_rn(e - __bfloat162float(ehi));
-        }
+        // Weights against the current references, written as if none moves: the
+        // common case needs one barrier a step. P slot b was last read by the value
+        // MMA of step j - 2, done before the S^T of step j.
+        float lpart[4];
+        write_weights(pslot + 4096 * b, sc, mref, lpart);
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
-        ok = compute_sync_and(w_ok);
-        if (!ok) break;
+        if (compute_sync_count(exceed || !w_ok) != 0) {
+          // Some reference moves (an item's first step, or a jump): the heads' maxima
+          // over the step, then the weights again.
+          ok = compute_sync_and(w_ok);
+          if (!ok) break;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float m = warp_max(sc[i]);
+            if (lane == 0) red[qd * kGroup + 4 * hh + i] = m;
+          }
+          compute_sync_and(true);
+          uint32_t rescale = 0;   // bit i: head 4 hh + i's reference moved after an earlier step contributed
+          float corr[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int h = 4 * hh + i;
+            const float tm = fmaxf(fmaxf(red[h], red[kGroup + h]), fmaxf(red[2 * kGroup + h], red[3 * kGroup + h]));
+            corr[i] = 1.0f;
+            if (tm > mref[i] + kLazy) {
+              corr[i] = (mref[i] == -INFINITY) ? 0.0f : __expf(mref[i] - tm);
+              if (base > 0) rescale |= 1u << i;
+              mref[i] = tm;
+              lsum[i] *= corr[i];
+            }
+          }
+          if (rescale) {   // the value MMA of step j - 1 is done once its stage is free again
+            const long long jp = j - 1;
+            w_ok = ptx::mbar_wait(bar0 + 8 * (B_EMPTY + static_cast<int>(jp % kStages)),
+                                  static_cast<uint32_t>((jp / kStages) & 1), abort, kWaitNs);
+            ptx::tc_fence_after();
+            uint32_t ohi[4], olo[4];
+            tmem_ld4(t_lane + 32 + 4 * hh, ohi);
+            tmem_ld4(t_lane + 40 + 4 * hh, olo);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if ((rescale >> i) & 1u) {
+                ohi[i] = __float_as_uint(__uint_as_float(ohi[i]) * corr[i]);
+                olo[i] = __float_as_uint(__uint_as_float(olo[i]) * corr[i]);
+              }
+            tmem_st4(t_lane + 32 + 4 * hh, ohi);
+            tmem_st4(t_lane + 40 + 4 * hh, olo);
+            ptx::tmem_wait_st();
+          }
+          write_weights(pslot + 4096 * b, sc, mref, lpart);
+          ptx::fence_proxy_async_smem();
+          ptx::tc_fence_before();
+          ok = compute_sync_and(w_ok);
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lsum[i] += lpart[i];
         if (tid == 0) ptx::mbar_arrive(bar0 + 8 * (B_P + b));
       }
       if (!ok) break;
@@ -506,9 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prefill_attn_tc_kernel(Proble
 
 }  // namespace
 
-bool qsa_attn_tc_supported(uint32_t nq, uint32_t nkv, uint32_t hd, const void *kc, const void *vc) {
-  return hd == kHd && nkv > 0 && nq == nkv * kGroup && (reinterpret_cast<uintptr_t>(kc) & 15u) == 0 &&
-         (reinterpret_cast<uintptr_t>(vc) & 15u) == 0;
+bool qsa_attn_tc_supported(const float *q, uint32_t nq, uint32_t nkv, uint32_t hd, const void *kc, const void *vc) {
+  // q is read as float2 pairs, K and V rows by 16-byte copies
+  return hd == kHd && nkv > 0 && nq == nkv * kGroup && (reinterpret_cast<uintptr_t>(q) & 7u) == 0 &&
+         (reinterpret_cast<uintptr_t>(kc) & 15u) == 0 && (reinterpret_cast<uintptr_t>(vc) & 15u) == 0;
 }
 
 cudaError_t launch_qsa_attn_tc(const float *q, const uint16_t *kc, const uint16_t *vc, const int32_t *table,

@@ -255,6 +255,23 @@ def test_qsa_prefill_attn_tensor_core_tiles(scale, topk, ratio, first_pos):
     assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
 
 
+def test_qsa_prefill_attn_q_4_byte_aligned():
+    """q starting 4 bytes past an 8-byte boundary (the tensor-core kernel reads
+    q in float pairs, so the 32-token tile kernel serves it) gives the same
+    attention."""
+    q, kb, vb, table, lists, fp, ratio = _attn_case(78, 128, 16, 2)
+    flat = torch.zeros(q.size + 1, dtype=torch.float32, device="cuda")
+    flat[1:] = torch.from_numpy(q.reshape(-1)).cuda()
+    qd = flat[1:].view(q.shape)
+    assert qd.data_ptr() % 8 == 4
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _idx().qsa_prefill_attn(qd, torch.from_numpy(kb.view(np.int16)).cuda(), torch.from_numpy(vb.view(np.int16)).cuda(),
+                                  torch.from_numpy(table).cuda(), torch.from_numpy(lists).cuda(), fp, ratio, dev_status=st)
+    ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio, 1.0 / math.sqrt(128))
+    assert int(st.item()) == ost == 0
+    assert np.max(np.abs(got.cpu().numpy() - ref)) <= 1e-4 * np.max(np.abs(ref))
+
+
 @pytest.mark.parametrize("nq", [8, 16])
 def test_qsa_prefill_attn_missing_page_and_first_rows(nq):
     """A page missing from the table drops its tokens (reported); rows at
