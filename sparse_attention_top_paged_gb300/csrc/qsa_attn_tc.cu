@@ -10,7 +10,7 @@
 // persistent, one CTA per SM taking items blockIdx.x, blockIdx.x + gridDim.x,
 // ... Its steps, laid end to end, flow through a ring of kStages shared-memory
 // stages:
-//   warps 9-16  two producer groups of four warps taking the steps in turn.
+//   warps 9-20  three producer groups of four warps taking the steps in turn.
 //               For each step a group looks up its 128 tokens (list entry,
 //               then page), copies their K and V rows (256 bytes each) into
 //               the stage with 16-byte asynchronous copies in the 128-byte
@@ -51,7 +51,7 @@ namespace {
 constexpr int kComputeWarps = 8;
 constexpr int kMmaWarp = kComputeWarps;
 constexpr int kProdWarp0 = kMmaWarp + 1;
-constexpr int kProdGroups = 2;
+constexpr int kProdGroups = 3;
 constexpr int kThreads = 32 * (kProdWarp0 + 4 * kProdGroups);
 constexpr int kStages = 3;
 constexpr int kTok = 128, kHd = 128, kGroup = 8;
@@ -333,8 +333,8 @@ __device__ __forceinline__ uint32_t full_bar(uint32_t bar0, long long j) {
   return bar0 + 8 * (B_FULL + static_cast<int>(j % kStages));
 }
 
-// 17 warps (20 for register allocation, in groups of 4): at most 96 registers a thread
-__global__ void __maxnreg__(96) qsa_prefill_attn_tc_kernel(Problem pr, long long items,
+// 21 warps (24 for register allocation, in groups of 4): at most 80 registers a thread
+__global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long items,
                                                                           int32_t *dev_status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // aligned by pointer arithmetic on the shared array, so accesses through sm stay shared-space ones
@@ -388,17 +388,18 @@ __global__ void __maxnreg__(96) qsa_prefill_attn_tc_kernel(Problem pr, long long
       const uint32_t fb = full_bar(bar0, j + 1), pb = bar0 + 8 * (B_P + static_cast<int>(j & 1));
       const uint32_t fpar = static_cast<uint32_t>(((j + 1) / kStages) & 1), ppar = static_cast<uint32_t>((j >> 1) & 1);
       const uint64_t t0 = ptx::globaltimer();
-      // (suspending waits of a few tens of ns, so the poll takes no issue slots from the softmax warps;
-      // lane 0's view decides for the warp)
+      // (non-blocking probes of both, a short sleep between rounds so the poll takes few issue
+      // slots from the softmax warps; lane 0's view decides for the warp)
       for (uint32_t it = 1; !(s_done && o_done); ++it) {
-        if (!s_done && __shfl_sync(0xFFFFFFFFu, ptx::mbar_try_wait(fb, fpar, o_done ? 1000u : 32u), 0)) {
+        if (!s_done && __shfl_sync(0xFFFFFFFFu, ptx::mbar_test_wait(fb, fpar), 0)) {
           issue_scores(s_base, tmem, j + 1);
           s_done = true;
-        } else if (!o_done && __shfl_sync(0xFFFFFFFFu, ptx::mbar_try_wait(pb, ppar, s_done ? 1000u : 32u), 0)) {
+        } else if (!o_done && __shfl_sync(0xFFFFFFFFu, ptx::mbar_test_wait(pb, ppar), 0)) {
           issue_values(s_base, tmem, j, first);
           o_done = true;
-        } else if ((it & 63u) == 0u &&
-                   __shfl_sync(0xFFFFFFFFu, *abort != 0 || ptx::globaltimer() - t0 > kWaitNs, 0)) {
+        } else if ((it & 15u) != 0u) {
+          __nanosleep(20);
+        } else if (__shfl_sync(0xFFFFFFFFu, *abort != 0 || ptx::globaltimer() - t0 > kWaitNs, 0)) {
           *abort = 1;
           ok = false;
           break;
