@@ -159,7 +159,7 @@ class ScoreTopkPlan:
     are checked and marshalled once, the outputs and the workspace allocated
     once, and every :meth:`run` is one library call on the current stream
     over whatever the bound tensors then hold (refill them in place between
-    runs). ``run`` can be captured in a CUDA graph with the step's copies.
+    runs). :meth:`capture` records a step with its copies as one CUDA graph.
     Arguments as for :func:`score_topk`."""
 
     def __init__(self, q, w, block_table, valid_lens, top_k, *, entries_per_block, keys_fp4=None,
@@ -199,6 +199,29 @@ class ScoreTopkPlan:
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         _raise("idx_score_topk", self._lib.idx_score_topk(self._args_ref, ctypes.c_void_p(s.cuda_stream)))
         return self.topk_idx, self.topk_score
+
+    def capture(self, before=None, after=None):
+        """Record one serving step as a CUDA graph: ``before()`` (e.g. the
+        step's host-to-device copies into the bound inputs, from pinned
+        buffers), this plan's call, then ``after()`` (e.g. the copies of the
+        outputs back to pinned host buffers). Returns the torch CUDAGraph;
+        each ``replay()`` runs the step on the current stream over whatever
+        the pinned and bound buffers then hold, with one host launch."""
+        torch = _torch()
+        with torch.cuda.device(self.device):
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):   # one call outside the capture sets the kernels' attributes
+                self.run()
+            torch.cuda.current_stream().wait_stream(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                if before is not None:
+                    before()
+                self.run()
+                if after is not None:
+                    after()
+        return graph
 
 
 def quantize_q_nvfp4(q):

@@ -332,6 +332,42 @@ def test_prepared_plan_matches_the_call():
         check_against_oracle(W, gi.cpu().numpy(), gs.cpu().numpy(), rows, None, f"plan/{W.meta['seed']}")
 
 
+def test_captured_plan_step_with_copies():
+    """ScoreTopkPlan.capture: the step's host-to-device copies, the call and the
+    copies back as one CUDA graph, replayed over pinned host buffers refilled
+    in place; every replay equals a direct call on the same inputs."""
+    import sparse_attention_top_paged_gb300 as idx
+    Ws = [_small(121 + i, T=6, lo=2000, hi=7000, k=128, max_lb=120, P=800) for i in range(3)]
+    d = to_device(Ws[0])
+    names = ("q", "w", "bt", "vl")
+    host = {n: d[n].cpu().pin_memory() for n in names}
+    plan = idx.ScoreTopkPlan(d["q"], d["w"], d["bt"], d["vl"], Ws[0].top_k, entries_per_block=Ws[0].epb,
+                             bt_stride=Ws[0].bt_stride, keys_fp4=d["keys_fp4"], key_scale=d["key_scale"],
+                             key_gscale=d["key_gscale"])
+    hi = torch.empty(plan.topk_idx.shape, dtype=torch.int32).pin_memory()
+    hs = torch.empty(plan.topk_score.shape, dtype=torch.float32).pin_memory()
+
+    def before():
+        for n in names:
+            d[n].copy_(host[n], non_blocking=True)
+
+    def after():
+        hi.copy_(plan.topk_idx, non_blocking=True)
+        hs.copy_(plan.topk_score, non_blocking=True)
+
+    graph = plan.capture(before, after)
+    for W in Ws[1:] + Ws[:1]:
+        dW = to_device(W)
+        for name in ("keys_fp4", "key_scale", "key_gscale"):
+            d[name].copy_(dW[name])
+        for n in names:
+            host[n].copy_(dW[n].cpu())
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = run_gpu(W, "tensor")
+        assert np.array_equal(hi.numpy(), ref[0]) and np.array_equal(hs.numpy(), ref[1])
+
+
 @pytest.mark.parametrize("q_format", ["exact", "nvfp4"])
 @pytest.mark.parametrize("case", ["batched", "pairs"])
 def test_bf16_queries_equal_their_float32_upcast(q_format, case):
