@@ -255,6 +255,29 @@ def test_qsa_prefill_attn_tensor_core_tiles(scale, topk, ratio, first_pos):
     assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
 
 
+@pytest.mark.parametrize("nq", [8, 4])
+def test_qsa_prefill_attn_tail_only_and_empty_rows(nq):
+    """No selected blocks (topk = 0): every row attends to its tail alone, and
+    a row whose tail is empty (its position completes a block) gives zeros
+    (8 q heads per kv head: the tcgen05 kernel's items without a step; 4: the
+    tile kernel)."""
+    rng = np.random.default_rng(55)
+    rows, fp, ratio, bs, nkv, hd = 13, 7, 4, 16, 2, 128
+    pages = (fp + rows + bs - 1) // bs
+    kb = wl._to_bf16_bits(rng.standard_normal((pages + 1, bs, nkv, hd)).astype(np.float32))
+    vb = wl._to_bf16_bits(rng.standard_normal((pages + 1, bs, nkv, hd)).astype(np.float32))
+    table = rng.permutation(pages + 1)[:pages].astype(np.int32)
+    lists = np.zeros((rows, 0), dtype=np.int32)
+    q = rng.standard_normal((rows, nq * nkv, hd)).astype(np.float32)
+    got, st = _attn_gpu(q, kb, vb, table, lists, fp, ratio)
+    ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
+                                       1.0 / math.sqrt(hd))
+    assert st == ost == 0
+    empty = [r for r in range(rows) if (fp + r + 1) % ratio == 0]
+    assert empty and np.all(got[empty] == 0.0)
+    assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
+
+
 def test_qsa_prefill_attn_q_4_byte_aligned():
     """q starting 4 bytes past an 8-byte boundary (the tensor-core kernel reads
     q in float pairs, so the 32-token tile kernel serves it) gives the same
