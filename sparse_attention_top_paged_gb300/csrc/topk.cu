@@ -530,18 +530,21 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
   const int k = p.top_k;
   int32_t *oi = p.topk_idx + static_cast<long long>(t) * k;
   float *os = p.topk_score + static_cast<long long>(t) * k;
+  // The row length is an input of the call, complete before the call's first
+  // kernel (launched in plain stream order) started: read it at once, so the
+  // row's copy can go out as soon as the scores are there.
+  const int L = p.valid_lens[t];
   // This kernel may be launched before the one writing its input has ended:
   // wait for that kernel's completion and memory first.
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // the first digit's counts, loaded beside the row length (both wait on memory)
+  // the first digit's counts
   uint32_t hpre[kPer];
   if (hist != nullptr) {
     const uint32_t *h = hist + static_cast<size_t>(t) * kBins;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) hpre[j] = h[kBins - 1 - kPer * tid - j];
   }
-  const int L = p.valid_lens[t];
   if (bad_len(p, L)) {
     if (tid == 0 && p.dev_status) atomicOr(p.dev_status, IDX_STATUS_BAD_LEN);
     for (int i = tid; i < k; i += kThreads) {
