@@ -350,25 +350,26 @@ def _bench():
     return importlib.import_module("bench")
 
 
-def test_qsa_prefill_attn_bench_size_sampled_rows():
+def test_qsa_prefill_attn_bench_size_every_row():
     """The benchmark's attention workload (512 rows from position 8192, 64
     selected blocks of 16 tokens plus the tail, 32 q heads over 4 kv heads,
-    hd 128) in the launch the benchmark times; sampled rows against the
-    oracle, each computed at its own position."""
+    hd 128) in the launch the benchmark times; every row against the oracle,
+    within 1e-4 of the row's largest output."""
     c = _bench().qsa_attn_case(1005)
     got, st = _attn_gpu(c["q"], c["kbits"], c["vbits"], c["table"], c["lists"], c["first_pos"], c["ratio"])
     assert st == 0
-    kv, vv = _bf16_vals(c["kbits"]), _bf16_vals(c["vbits"])
-    for r in (0, 1, 137, 300, 511):
-        ref, ost = oracle.qsa_prefill_attn(c["q"][r:r + 1], kv, vv, c["table"], c["lists"][r:r + 1],
-                                           c["first_pos"] + r, c["ratio"], 1.0 / math.sqrt(c["hd"]))
-        assert ost == 0
-        assert np.max(np.abs(got[r:r + 1] - ref)) <= 1e-4 * np.max(np.abs(ref)), r
+    ref, ost = oracle.qsa_prefill_attn(c["q"], _bf16_vals(c["kbits"]), _bf16_vals(c["vbits"]), c["table"],
+                                       c["lists"], c["first_pos"], c["ratio"], 1.0 / math.sqrt(c["hd"]))
+    assert ost == 0
+    err = np.max(np.abs(got - ref), axis=(1, 2))
+    scale = np.max(np.abs(ref), axis=(1, 2))
+    bad = np.nonzero(err > 1e-4 * scale)[0]
+    assert bad.size == 0, (bad[:8], err[bad[:8]], scale[bad[:8]])
 
 
-def test_gather_split_bench_size_sampled_queries():
+def test_gather_split_bench_size_every_query():
     """The benchmark's split-gather workload (64 queries x 2048 positions of a
-    262144-token cache) in one launch; sampled queries bit-exact against the
+    262144-token cache) in one launch; every query bit-exact against the
     oracle."""
     c = _bench().gather_split_case(1006)
     d = lambda x: torch.from_numpy(x).cuda()
@@ -377,8 +378,7 @@ def test_gather_split_bench_size_sampled_queries():
                               d(c["scale"]), dev_status=st)
     assert int(st.item()) == 0
     got = got.cpu().view(torch.int16).numpy().view(np.uint16)
-    for t in (0, 17, 63):
-        ref, ost = oracle.gather_split(c["sel"][t:t + 1], c["table"][t:t + 1], c["P"], c["P"], c["bs"], c["codes"],
-                                       c["scale"], c["rope"])
-        assert ost == 0
-        assert np.array_equal(got[t:t + 1], ref), t
+    ref, ost = oracle.gather_split(c["sel"], c["table"], c["P"], c["P"], c["bs"], c["codes"], c["scale"], c["rope"])
+    assert ost == 0
+    bad = [t for t in range(c["T"]) if not np.array_equal(got[t], ref[t])]
+    assert not bad, bad[:8]
