@@ -63,12 +63,20 @@ constexpr uint32_t kOffP = kStages * kStageBytes;        // two P slots: 16 rows
 constexpr uint32_t kOffRed = kOffP + 2 * 4096;           // [4 lane quarters][8 heads] maxima, then 2 x sums
 constexpr uint32_t kOffBar = kOffRed + 3 * 4 * kGroup * 4;
 // per stage: full, empty; per slot (step parity): S^T written, weights written
-constexpr int B_FULL = 0, B_EMPTY = kStages, B_S = 2 * kStages, B_P = 2 * kStages + 2, B_COUNT = 2 * kStages + 4;
+constexpr int B_FULL = 0, B_EMPTY = kStages, B_S = 2 * kStages, B_P = 2 * kStages + 2, B_NEVER = 2 * kStages + 4,
+              B_COUNT = 2 * kStages + 5;
 constexpr uint32_t kOffMisc = kOffBar + 8 * B_COUNT;     // tensor-memory address, abort flag, bad-block flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;    // + slack to align the base to 1 KB
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 constexpr uint32_t kTmemCols = 64;                       // S slots: columns 0-15, 16-31; O: 32-47
+// Every wait gives up after kWaitNs (2 s; failure-path test builds shorten it
+// with IDX_WAIT_LIMIT_NS), raising the CTA's abort flag: the CTA then leaves
+// with no copy or MMA in flight and the call reports IDX_STATUS_TIMEOUT.
+#ifdef IDX_WAIT_LIMIT_NS
+constexpr uint64_t kWaitNs = IDX_WAIT_LIMIT_NS;
+#else
 constexpr uint64_t kWaitNs = 2000000000ull;
+#endif
 
 // Shared-memory descriptor, 128-byte swizzle: K-major (lbo unused: 16) or
 // MN-major (lbo = the stride between 64-element atoms along M or N); sbo =
@@ -355,6 +363,7 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
     ptx::mbar_init(bar0 + 8 * (B_S + 1), 1);
     ptx::mbar_init(bar0 + 8 * B_P, 1);                     // one softmax thread, once the weights are written
     ptx::mbar_init(bar0 + 8 * (B_P + 1), 1);
+    ptx::mbar_init(bar0 + 8 * B_NEVER, 1);                 // nothing arrives (failure-path test builds only)
     *abort = 0;
     *bad_flag = 0;
     ptx::fence_mbar_init();
@@ -374,7 +383,13 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
     sw.w = blockIdx.x;
     sw.items = items;
     sw.seek(pr);
-    bool ok = !sw.valid || ptx::mbar_wait(full_bar(bar0, 0), 0u, abort, kWaitNs);
+#ifdef IDX_TEST_STALL
+    // Failure-path test builds only: CTA 0's MMA warp first waits for a barrier
+    // nothing ever arrives on, so the wait gives up, raises the abort flag and
+    // the CTA leaves without issuing an MMA.
+    if (blockIdx.x == 0) ptx::mbar_wait(bar0 + 8 * B_NEVER, 0u, abort, kWaitNs);
+#endif
+    bool ok = *abort == 0 && (!sw.valid || ptx::mbar_wait(full_bar(bar0, 0), 0u, abort, kWaitNs));
     ok = __all_sync(0xFFFFFFFFu, ok);
     if (sw.valid && ok) issue_scores(s_base, tmem, 0);
     // Step j: S^T of step j + 1 once its stage is full (its S slot was last read

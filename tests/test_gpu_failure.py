@@ -63,6 +63,54 @@ def test_stalled_wait_reports_timeout_and_leaves_context_usable(stall_lib):
     check_against_oracle(W, ri, rs_, rows, None, "after-timeout")
 
 
+@pytest.fixture(scope="module")
+def stall_attn_lib():
+    """The prefill attention's tcgen05 kernel built with a 20 ms wait limit and
+    CTA 0's MMA warp waiting once for a barrier nothing arrives on."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+    from sparse_attention_top_paged_gb300 import _lib, build
+    path = build.build_variant("stall_attn", defines=("IDX_TEST_STALL=1", "IDX_WAIT_LIMIT_NS=20000000ull"),
+                               sources=("qsa_attn_tc.cu",))
+    return _lib.load_library(path)
+
+
+def test_attention_stalled_wait_reports_timeout_and_leaves_context_usable(stall_attn_lib):
+    """The attention's abort path: CTA 0 gives up without issuing an MMA, its
+    producers leave with their copies drained, the call returns promptly with
+    IDX_STATUS_TIMEOUT, and the regular library then computes correctly."""
+    import math
+    import oracle
+    import sparse_attention_top_paged_gb300 as idx
+    rng = np.random.default_rng(62)
+    rows, nq, nkv, hd, bs, ratio, fp, topk = 6, 16, 2, 128, 16, 16, 2000, 64
+    pages = (fp + rows + bs - 1) // bs
+    kb = wl._to_bf16_bits(rng.standard_normal((pages, bs, nkv, hd)).astype(np.float32))
+    vb = wl._to_bf16_bits(rng.standard_normal((pages, bs, nkv, hd)).astype(np.float32))
+    table = rng.permutation(pages).astype(np.int32)
+    lists = rng.integers(0, (fp + 1) // ratio, size=(rows, topk)).astype(np.int32)
+    q = rng.standard_normal((rows, nq, hd)).astype(np.float32)
+    d = lambda x: torch.from_numpy(x).cuda()
+    dq, dk, dv, dt, dl = d(q), d(kb.view(np.int16)), d(vb.view(np.int16)), d(table), d(lists)
+    out = torch.zeros_like(dq)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    rc = stall_attn_lib.idx_qsa_prefill_attn(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dt.data_ptr(), pages, pages,
+                                             dl.data_ptr(), out.data_ptr(), rows, fp, topk, ratio, bs, nq, nkv, hd,
+                                             1.0 / math.sqrt(hd), st.data_ptr(),
+                                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert rc == 0
+    assert int(st.item()) & idx.STATUS_TIMEOUT
+    assert elapsed < 10.0, elapsed
+    vals = lambda b: (b.astype(np.uint32) << 16).view(np.float32)
+    got = idx.qsa_prefill_attn(dq, dk, dv, dt, dl, fp, ratio).cpu().numpy()
+    ref, ost = oracle.qsa_prefill_attn(q, vals(kb), vals(vb), table, lists, fp, ratio, 1.0 / math.sqrt(hd))
+    assert ost == 0 and np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
+
+
 # --------------------------------------------------- debug-bounds build ----
 
 @pytest.fixture(scope="module")
