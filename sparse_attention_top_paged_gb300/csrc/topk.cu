@@ -397,6 +397,7 @@ __global__ void __launch_bounds__(kCollectThreads) select_collect_kernel(ScorePa
                                                                         uint32_t *__restrict__ cand_cnt, int cap) {
   constexpr int kW = kCollectThreads / 32, kPerC = kBins / kCollectThreads;
   constexpr int kRound = 4 * kCollectThreads;   // keys per round (one 16-byte load per thread)
+  constexpr int kBatch = 8;                      // rounds whose loads are in flight together
   static_assert(kCollectBuf >= 2 * kRound, "a round never overfills the buffer");
   __shared__ uint32_t warp_sum[kW], warp_max[kW];
   __shared__ int s_bin, s_cnt;
@@ -409,6 +410,28 @@ __global__ void __launch_bounds__(kCollectThreads) select_collect_kernel(ScorePa
   const int L = p.valid_lens[t];
   if (bad_len(p, L) || L <= kSmallRow) return;
   const uint32_t k = static_cast<uint32_t>(p.top_k);
+  const long long per = ((static_cast<long long>(L) + C - 1) / C + 3) & ~3LL;
+  const long long s0 = static_cast<long long>(c) * per, s1 = min(static_cast<long long>(L), s0 + per);
+  const float *row = scores + static_cast<long long>(t) * ld;
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  // The slice's first kBatch rounds (one 16-byte load per thread and round)
+  // are loaded before the boundary is decided: the two latencies overlap.
+  auto load_batch = [&](long long base, float4 (&v)[kBatch]) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const long long i0 = base + static_cast<long long>(u) * kRound + 4LL * tid;
+      if (vec && i0 + 3 < s1) {
+        v[u] = __ldcs(reinterpret_cast<const float4 *>(row + i0));
+      } else {
+        v[u].x = (i0 + 0 < s1) ? row[i0 + 0] : -INFINITY;
+        v[u].y = (i0 + 1 < s1) ? row[i0 + 1] : -INFINITY;
+        v[u].z = (i0 + 2 < s1) ? row[i0 + 2] : -INFINITY;
+        v[u].w = (i0 + 3 < s1) ? row[i0 + 3] : -INFINITY;
+      }
+    }
+  };
+  float4 v[kBatch];
+  load_batch(s0, v);
   // descending scan of the first-digit histogram (thread tid: bins kBins-1-kPerC*tid-j)
   const uint32_t *h = hist + static_cast<size_t>(t) * kBins;
   uint32_t cnt[kPerC], tot = 0;
@@ -455,10 +478,6 @@ __global__ void __launch_bounds__(kCollectThreads) select_collect_kernel(ScorePa
   if (max_above > static_cast<uint32_t>(kRankBinMax) || (!take_all && s_cnt > kBndCap)) return;
   const uint32_t thr = take_all ? 0u : static_cast<uint32_t>(s_bin);   // first digit of the weakest key taken
 
-  const long long per = ((static_cast<long long>(L) + C - 1) / C + 3) & ~3LL;
-  const long long s0 = static_cast<long long>(c) * per, s1 = min(static_cast<long long>(L), s0 + per);
-  const float *row = scores + static_cast<long long>(t) * ld;
-  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
   uint64_t *out = cand + static_cast<size_t>(t) * cap;
   // Keys go to a shared-memory buffer first (one shared atomic per warp and
   // element position); the buffer goes out with one global reservation when
@@ -476,29 +495,28 @@ __global__ void __launch_bounds__(kCollectThreads) select_collect_kernel(ScorePa
     if (tid == 0) s_n = 0u;
     __syncthreads();
   };
-  for (long long base = s0; base < s1; base += kRound) {
-    const long long i0 = base + 4LL * tid;
-    float e[4];
-    if (vec && i0 + 3 < s1) {
-      const float4 v = __ldcs(reinterpret_cast<const float4 *>(row + i0));
-      e[0] = v.x; e[1] = v.y; e[2] = v.z; e[3] = v.w;
-    } else {
+  for (long long bb = s0; bb < s1; bb += static_cast<long long>(kBatch) * kRound) {
+    if (bb != s0) load_batch(bb, v);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) e[q] = (i0 + q < s1) ? row[i0 + q] : -INFINITY;
-    }
+    for (int u = 0; u < kBatch; ++u) {
+      const long long base = bb + static_cast<long long>(u) * kRound;
+      if (base >= s1) break;   // (uniform: every thread has the same base)
+      const long long i0 = base + 4LL * tid;
+      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const bool ok = e[q] != -INFINITY && (float_order(e[q]) >> 20) >= thr;
-      const uint32_t m = __ballot_sync(0xFFFFFFFFu, ok);
-      if (m == 0u) continue;
-      uint32_t slot0 = 0;
-      if (lane == 0) slot0 = atomicAdd(&s_n, static_cast<uint32_t>(__popc(m)));
-      slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
-      const uint32_t slot = slot0 + __popc(m & lanemask_lt());
-      if (ok && slot < static_cast<uint32_t>(kCollectBuf)) s_buf[slot] = pack_key(e[q], static_cast<int32_t>(i0 + q));
+      for (int q = 0; q < 4; ++q) {
+        const bool ok = e[q] != -INFINITY && (float_order(e[q]) >> 20) >= thr;
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, ok);
+        if (m == 0u) continue;
+        uint32_t slot0 = 0;
+        if (lane == 0) slot0 = atomicAdd(&s_n, static_cast<uint32_t>(__popc(m)));
+        slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
+        const uint32_t slot = slot0 + __popc(m & lanemask_lt());
+        if (ok && slot < static_cast<uint32_t>(kCollectBuf)) s_buf[slot] = pack_key(e[q], static_cast<int32_t>(i0 + q));
+      }
+      __syncthreads();
+      if (s_n > static_cast<uint32_t>(kCollectBuf - kRound)) flush();   // room for one more round
     }
-    __syncthreads();
-    if (s_n > static_cast<uint32_t>(kCollectBuf - kRound)) flush();   // room for one more round
   }
   __syncthreads();
   if (s_n > 0u) flush();
