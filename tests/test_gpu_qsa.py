@@ -295,6 +295,20 @@ def test_qsa_prefill_attn_q_4_byte_aligned():
     assert np.max(np.abs(got.cpu().numpy() - ref)) <= 1e-4 * np.max(np.abs(ref))
 
 
+@pytest.mark.parametrize("nq,nkv,bs,ratio", [(64, 8, 16, 16), (16, 2, 64, 16), (16, 2, 16, 64), (8, 1, 32, 8)])
+def test_qsa_prefill_attn_tensor_core_geometry(nq, nkv, bs, ratio):
+    """The tcgen05 kernel (8 q heads per kv head, hd 128) over 1, 2 and 8 kv
+    heads, pages of 16, 32 and 64 tokens and blocks shorter or longer than a
+    page."""
+    q, kb, vb, table, lists, fp, ratio = _attn_case(150 + nkv + bs + ratio, 128, nq, nkv, rows=5, first_pos=2500,
+                                                    ratio=ratio, bs=bs, topk=48)
+    got, st = _attn_gpu(q, kb, vb, table, lists, fp, ratio)
+    ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
+                                       1.0 / math.sqrt(128))
+    assert st == ost == 0
+    assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
+
+
 @pytest.mark.parametrize("nq", [8, 16])
 def test_qsa_prefill_attn_missing_page_and_first_rows(nq):
     """A page missing from the table drops its tokens (reported); rows at
