@@ -1,5 +1,5 @@
-// qsa_attn_tc.cu — QSA prefill attention on the tcgen05 tensor cores, for 8
-// query heads per kv head and hd = 128 ("metrale_model_layers/layers/ops/qsa.rs",
+// qsa_attn_tc.cu — QSA prefill attention on the tcgen05 tensor cores, for G = 4
+// or 8 query heads per kv head and hd = 128 ("metrale_model_layers/layers/ops/qsa.rs",
 // qsa_prefill_attn: per (row, query head) one softmax over every token of the
 // row's selected complete blocks and over the incomplete tail, with K and V of
 // the head's kv head read through the page table).
@@ -17,9 +17,10 @@
 //               swizzled layout the MMAs read (two 16 KB halves of 64
 //               dimensions, token t's half-row at t * 128 bytes; zero rows for
 //               tokens that are missing), writes the step's Qs operand (q *
-//               inv_sqrt_d of the 8 heads split into bf16 high parts, rows 0-7,
+//               inv_sqrt_d of the G heads split into bf16 high parts, rows 0-7,
 //               and low parts, rows 8-15, once per item: q keeps about 17
-//               significant bits) and the token mask. The copies arrive on the
+//               significant bits; rows of unused head slots are zero) and the
+//               token mask. The copies arrive on the
 //               stage's barrier when they land, so a group never waits on its
 //               own copies.
 //   warp 8      MMA issuer (tcgen05, kind::f16, bf16 operands, f32 in tensor
@@ -31,7 +32,7 @@
 //               with V read in place as an MN-major operand (the step's token
 //               rows are its K rows). Its commit frees the stage.
 //   warps 0-7   softmax: warp w owns tensor-memory lanes 32 (w % 4) .. + 31
-//               (tokens of S, dimensions of O) for heads 4 (w / 4) .. + 3. Per
+//               (tokens of S, dimensions of O) for G / 2 heads. Per
 //               step: the heads' maxima over the step, a lazy reference maximum
 //               that moves only when a score exceeds it by more than kLazy
 //               (the running sums and the head's two output columns are then
@@ -54,7 +55,8 @@ constexpr int kProdWarp0 = kMmaWarp + 1;
 constexpr int kProdGroups = 3;
 constexpr int kThreads = 32 * (kProdWarp0 + 4 * kProdGroups);
 constexpr int kStages = 3;
-constexpr int kTok = 128, kHd = 128, kGroup = 8;
+constexpr int kTok = 128, kHd = 128;
+constexpr int kGroup = 8;   // head slots of the MMAs (N = 16: high and low parts); G <= 8 of them are used
 constexpr float kLazy = 8.0f;
 // a stage: K rows, V rows (32 KB each), the Qs operand (16 rows x 128 dims), the token mask
 constexpr uint32_t kOffK = 0, kOffV = 32768, kOffQ = 65536, kOffMask = 69632;
@@ -105,6 +107,14 @@ __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint3
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t (&v)[2]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(taddr) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, const uint32_t (&v)[2]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};" ::"r"(taddr), "r"(v[0]), "r"(v[1]) : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&v)[4]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
@@ -116,6 +126,16 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&v)[4])
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
                "r"(v[2]), "r"(v[3])
                : "memory");
+}
+
+// n consecutive columns of this warp's lanes (n = 2 or 4)
+template <int N>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&v)[N]) {
+  if constexpr (N == 2) tmem_ld2(taddr, v); else tmem_ld4(taddr, v);
+}
+template <int N>
+__device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t (&v)[N]) {
+  if constexpr (N == 2) tmem_st2(taddr, v); else tmem_st4(taddr, v);
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
@@ -217,6 +237,7 @@ struct StepWalk {
 
 // A producer group (four warps, a token a thread): steps g, g + kProdGroups,
 // ... of the CTA's walk; the groups' copies of consecutive steps overlap.
+template <int G>
 __device__ void producer(const Problem &pr, long long items, unsigned char *sm, uint32_t s_base, int g, int pw,
                          int lane, volatile int *abort, int *bad_flag) {
   const int ptid = 32 * pw + lane;
@@ -240,7 +261,8 @@ __device__ void producer(const Problem &pr, long long items, unsigned char *sm, 
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int x = ptid + 128 * i, h = x >> 6, d = 2 * (x & 63);
-        v[i] = *reinterpret_cast<const float2 *>(pr.q + ((sw.it.r * pr.nq) + sw.it.kvh * kGroup + h) * kHd + d);
+        v[i] = h < G ? *reinterpret_cast<const float2 *>(pr.q + ((sw.it.r * pr.nq) + sw.it.kvh * G + h) * kHd + d)
+                     : make_float2(0.0f, 0.0f);   // unused head slots: zero rows
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -342,6 +364,7 @@ __device__ __forceinline__ uint32_t full_bar(uint32_t bar0, long long j) {
 }
 
 // 21 warps (24 for register allocation, in groups of 4): at most 80 registers a thread
+template <int G>
 __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long items,
                                                                           int32_t *dev_status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -368,6 +391,9 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
     *bad_flag = 0;
     ptx::fence_mbar_init();
   }
+  // both P slots start at zero: the rows of unused head slots (G < 8) stay so
+  for (int i = tid; i < 2 * 4096 / 16; i += kThreads) reinterpret_cast<uint4 *>(sm + kOffP)[i] = make_uint4(0u, 0u, 0u, 0u);
+  ptx::fence_proxy_async_smem();
   if (warp == 0) ptx::tmem_alloc(ptx::smem_addr(tmem_p), kTmemCols);
   ptx::tc_fence_before();
   __syncthreads();
@@ -376,7 +402,7 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
 
   if (warp >= kProdWarp0) {
     const int pwarp = warp - kProdWarp0;
-    producer(pr, items, sm, s_base, pwarp / 4, pwarp % 4, lane, abort, bad_flag);
+    producer<G>(pr, items, sm, s_base, pwarp / 4, pwarp % 4, lane, abort, bad_flag);
   } else if (warp == kMmaWarp) {
     // The whole warp walks the steps in lockstep; one elected lane issues.
     StepWalk sw;
@@ -424,19 +450,20 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
     }
     __syncwarp();
   } else {
-    const int qd = warp & 3, hh = warp >> 2;   // lane quarter; heads 4 hh .. 4 hh + 3
+    constexpr int HPW = G / 2;                 // heads a warp serves
+    const int qd = warp & 3, hh = warp >> 2;   // lane quarter; heads HPW hh .. HPW hh + HPW - 1
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * qd) << 16);
     bool ok = true;
     long long j = 0;                           // the CTA's step counter
     int item_parity = 0;
     unsigned char *pslot = sm + kOffP;
     const int tok = 32 * qd + lane;
-    // this thread's weights p = exp(S - ref) of heads 4 hh .. + 3 (token tok) into a P
-    // slot, split into bf16 high (rows h) and low (rows 8 + h) parts; their sum in lp
-    auto write_weights = [&](unsigned char *pb, const float (&sc)[4], const float (&mref)[4], float (&lp)[4]) {
+    // this thread's weights p = exp(S - ref) of its heads (token tok) into a P slot,
+    // split into bf16 high (rows h) and low (rows 8 + h) parts; their sum in lp
+    auto write_weights = [&](unsigned char *pb, const float (&sc)[HPW], const float (&mref)[HPW], float (&lp)[HPW]) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int h = 4 * hh + i;
+      for (int i = 0; i < HPW; ++i) {
+        const int h = HPW * hh + i;
         // ex2-based exp: the argument is at most kLazy; relative error a few 1e-7
         const float e = (sc[i] != -INFINITY) ? __expf(sc[i] - mref[i]) : 0.0f;
         lp[i] = e;
@@ -448,9 +475,9 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
     for (long long w = blockIdx.x; w < items && ok; w += gridDim.x, item_parity ^= 1) {
       Item it;
       it.set(pr, w);
-      float mref[4], lsum[4];
+      float mref[HPW], lsum[HPW];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < HPW; ++i) {
         mref[i] = -INFINITY;
         lsum[i] = 0.0f;
       }
@@ -461,21 +488,21 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
         w_ok = w_ok && ptx::mbar_wait(bar0 + 8 * (B_S + b), static_cast<uint32_t>((j >> 1) & 1), abort, kWaitNs);
         ptx::tc_fence_after();
         const bool valid = (reinterpret_cast<const uint32_t *>(sm + s * kStageBytes + kOffMask)[qd] >> lane) & 1u;
-        uint32_t shi[4], slo[4];
-        tmem_ld4(t_lane + 16 * b + 4 * hh, shi);
-        tmem_ld4(t_lane + 16 * b + 8 + 4 * hh, slo);
+        uint32_t shi[HPW], slo[HPW];
+        tmem_ldn<HPW>(t_lane + 16 * b + HPW * hh, shi);
+        tmem_ldn<HPW>(t_lane + 16 * b + 8 + HPW * hh, slo);
         ptx::tmem_wait_ld();
-        float sc[4];
+        float sc[HPW];
         bool exceed = false;   // a score above its head's reference by more than kLazy
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < HPW; ++i) {
           sc[i] = valid ? __uint_as_float(shi[i]) + __uint_as_float(slo[i]) : -INFINITY;
           exceed |= sc[i] > mref[i] + kLazy;   // (any finite score while mref = -inf)
         }
         // Weights against the current references, written as if none moves: the
         // common case needs one barrier a step. P slot b was last read by the value
         // MMA of step j - 2, done before the S^T of step j.
-        float lpart[4];
+        float lpart[HPW];
         write_weights(pslot + 4096 * b, sc, mref, lpart);
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
@@ -485,16 +512,16 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
           ok = compute_sync_and(w_ok);
           if (!ok) break;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < HPW; ++i) {
             const float m = warp_max(sc[i]);
-            if (lane == 0) red[qd * kGroup + 4 * hh + i] = m;
+            if (lane == 0) red[qd * kGroup + HPW * hh + i] = m;
           }
           compute_sync_and(true);
-          uint32_t rescale = 0;   // bit i: head 4 hh + i's reference moved after an earlier step contributed
-          float corr[4];
+          uint32_t rescale = 0;   // bit i: head HPW hh + i's reference moved after an earlier step contributed
+          float corr[HPW];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int h = 4 * hh + i;
+          for (int i = 0; i < HPW; ++i) {
+            const int h = HPW * hh + i;
             const float tm = fmaxf(fmaxf(red[h], red[kGroup + h]), fmaxf(red[2 * kGroup + h], red[3 * kGroup + h]));
             corr[i] = 1.0f;
             if (tm > mref[i] + kLazy) {
@@ -509,18 +536,18 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
             w_ok = ptx::mbar_wait(bar0 + 8 * (B_EMPTY + static_cast<int>(jp % kStages)),
                                   static_cast<uint32_t>((jp / kStages) & 1), abort, kWaitNs);
             ptx::tc_fence_after();
-            uint32_t ohi[4], olo[4];
-            tmem_ld4(t_lane + 32 + 4 * hh, ohi);
-            tmem_ld4(t_lane + 40 + 4 * hh, olo);
+            uint32_t ohi[HPW], olo[HPW];
+            tmem_ldn<HPW>(t_lane + 32 + HPW * hh, ohi);
+            tmem_ldn<HPW>(t_lane + 40 + HPW * hh, olo);
             ptx::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < HPW; ++i)
               if ((rescale >> i) & 1u) {
                 ohi[i] = __float_as_uint(__uint_as_float(ohi[i]) * corr[i]);
                 olo[i] = __float_as_uint(__uint_as_float(olo[i]) * corr[i]);
               }
-            tmem_st4(t_lane + 32 + 4 * hh, ohi);
-            tmem_st4(t_lane + 40 + 4 * hh, olo);
+            tmem_stn<HPW>(t_lane + 32 + HPW * hh, ohi);
+            tmem_stn<HPW>(t_lane + 40 + HPW * hh, olo);
             ptx::tmem_wait_st();
           }
           write_weights(pslot + 4096 * b, sc, mref, lpart);
@@ -530,7 +557,7 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
           if (!ok) break;
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) lsum[i] += lpart[i];
+        for (int i = 0; i < HPW; ++i) lsum[i] += lpart[i];
         if (tid == 0) ptx::mbar_arrive(bar0 + 8 * (B_P + b));
       }
       if (!ok) break;
@@ -544,26 +571,26 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
       }
       float *rs = red + 4 * kGroup * (1 + item_parity);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < HPW; ++i) {
         float l = lsum[i];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
-        if (lane == 0) rs[qd * kGroup + 4 * hh + i] = l;
+        if (lane == 0) rs[qd * kGroup + HPW * hh + i] = l;
       }
       ok = compute_sync_and(w_ok);
       if (!ok) break;
-      uint32_t ohi[4] = {0u, 0u, 0u, 0u}, olo[4] = {0u, 0u, 0u, 0u};
+      uint32_t ohi[HPW] = {}, olo[HPW] = {};
       if (it.n_virt > 0) {
-        tmem_ld4(t_lane + 32 + 4 * hh, ohi);
-        tmem_ld4(t_lane + 40 + 4 * hh, olo);
+        tmem_ldn<HPW>(t_lane + 32 + HPW * hh, ohi);
+        tmem_ldn<HPW>(t_lane + 40 + HPW * hh, olo);
         ptx::tmem_wait_ld();
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int h = 4 * hh + i;
+      for (int i = 0; i < HPW; ++i) {
+        const int h = HPW * hh + i;
         const float L = rs[h] + rs[kGroup + h] + rs[2 * kGroup + h] + rs[3 * kGroup + h];
         const float o = __uint_as_float(ohi[i]) + __uint_as_float(olo[i]);
-        pr.out[((it.r * pr.nq) + it.kvh * kGroup + h) * kHd + 32 * qd + lane] = L > 0.0f ? o / L : 0.0f;
+        pr.out[((it.r * pr.nq) + it.kvh * G + h) * kHd + 32 * qd + lane] = L > 0.0f ? o / L : 0.0f;
       }
       ptx::tc_fence_before();   // the reads of O come before the next item's first value MMA
     }
@@ -585,8 +612,8 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
 }  // namespace
 
 bool qsa_attn_tc_supported(const float *q, uint32_t nq, uint32_t nkv, uint32_t hd, const void *kc, const void *vc) {
-  // q is read as float2 pairs, K and V rows by 16-byte copies
-  return hd == kHd && nkv > 0 && nq == nkv * kGroup && (reinterpret_cast<uintptr_t>(q) & 7u) == 0 &&
+  // 4 or 8 query heads per kv head; q is read as float2 pairs, K and V rows by 16-byte copies
+  return hd == kHd && nkv > 0 && (nq == nkv * 8 || nq == nkv * 4) && (reinterpret_cast<uintptr_t>(q) & 7u) == 0 &&
          (reinterpret_cast<uintptr_t>(kc) & 15u) == 0 && (reinterpret_cast<uintptr_t>(vc) & 15u) == 0;
 }
 
@@ -594,18 +621,19 @@ cudaError_t launch_qsa_attn_tc(const float *q, const uint16_t *kc, const uint16_
                                int n_pages, int P, const int32_t *lists, float *out, uint32_t rows, uint32_t first_pos,
                                uint32_t topk, uint32_t ratio, uint32_t block_size, uint32_t nq, uint32_t nkv,
                                float inv_sqrt_d, int32_t *dev_status, cudaStream_t stream) {
+  void (*kern)(Problem, long long, int32_t *) =
+      nq == nkv * 8 ? qsa_prefill_attn_tc_kernel<8> : qsa_prefill_attn_tc_kernel<4>;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   // set on every call: the attribute belongs to the current device's context
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(qsa_prefill_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>(rows) * nkv;
   const int grid = static_cast<int>(items < sms ? items : sms);
   const Problem pr{q, kc, vc, table, lists, out, n_pages, P, first_pos, topk, ratio, block_size, nq, nkv, inv_sqrt_d};
-  qsa_prefill_attn_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(pr, items, dev_status);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(pr, items, dev_status);
   return cudaGetLastError();
 }
 

@@ -255,12 +255,12 @@ def test_qsa_prefill_attn_tensor_core_tiles(scale, topk, ratio, first_pos):
     assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
 
 
-@pytest.mark.parametrize("nq", [8, 4])
+@pytest.mark.parametrize("nq", [8, 4, 2])
 def test_qsa_prefill_attn_tail_only_and_empty_rows(nq):
     """No selected blocks (topk = 0): every row attends to its tail alone, and
     a row whose tail is empty (its position completes a block) gives zeros
-    (8 q heads per kv head: the tcgen05 kernel's items without a step; 4: the
-    tile kernel)."""
+    (8 and 4 q heads per kv head: the tcgen05 kernel's items without a step;
+    2: the tile kernel)."""
     rng = np.random.default_rng(55)
     rows, fp, ratio, bs, nkv, hd = 13, 7, 4, 16, 2, 128
     pages = (fp + rows + bs - 1) // bs
@@ -295,10 +295,11 @@ def test_qsa_prefill_attn_q_4_byte_aligned():
     assert np.max(np.abs(got.cpu().numpy() - ref)) <= 1e-4 * np.max(np.abs(ref))
 
 
-@pytest.mark.parametrize("nq,nkv,bs,ratio", [(64, 8, 16, 16), (16, 2, 64, 16), (16, 2, 16, 64), (8, 1, 32, 8)])
+@pytest.mark.parametrize("nq,nkv,bs,ratio", [(64, 8, 16, 16), (16, 2, 64, 16), (16, 2, 16, 64), (8, 1, 32, 8),
+                                             (32, 8, 16, 16), (8, 2, 64, 16), (4, 1, 32, 8)])
 def test_qsa_prefill_attn_tensor_core_geometry(nq, nkv, bs, ratio):
-    """The tcgen05 kernel (8 q heads per kv head, hd 128) over 1, 2 and 8 kv
-    heads, pages of 16, 32 and 64 tokens and blocks shorter or longer than a
+    """The tcgen05 kernel (8 or 4 q heads per kv head, hd 128) over 1, 2 and 8
+    kv heads, pages of 16, 32 and 64 tokens and blocks shorter or longer than a
     page."""
     q, kb, vb, table, lists, fp, ratio = _attn_case(150 + nkv + bs + ratio, 128, nq, nkv, rows=5, first_pos=2500,
                                                     ratio=ratio, bs=bs, topk=48)
