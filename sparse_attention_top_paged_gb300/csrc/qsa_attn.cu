@@ -7,12 +7,12 @@
 // complete (others are skipped) and over the tail tokens
 // ((p + 1) / ratio) * ratio .. p, with K and V of kv head h / (nq / nkv) read
 // through the page table; attn_out[r][h] is the softmax-weighted sum of V.
-// With 4 or 8 query heads per kv head, hd = 128, 16-byte aligned K and V caches
-// and 8-byte aligned q,
-// qsa_attn_tc.cu's kernel runs (one CTA per (row, kv head) over 128-token
-// tiles, both contractions on tcgen05). With 1, 2, 4 or 8 query heads per kv
-// head otherwise, hd <= 128 and 16-byte aligned caches, one CTA per (row, kv
-// head) serves the whole group over 32-token tiles
+// With 1, 2, 4 or 8 query heads per kv head, hd = 128, 16-byte aligned K and V
+// caches and 8-byte aligned q, qsa_attn_tc.cu's kernel runs (a persistent
+// pipeline over (row, kv head) items in 128-token steps, both contractions on
+// tcgen05). With 1, 2, 4 or 8 query heads per kv head otherwise, hd <= 128 and
+// 16-byte aligned caches, one CTA per (row, kv head) serves the whole group
+// over 32-token tiles
 // (qsa_prefill_attn_tile_kernel: both contractions of a tile as warp-level
 // mma.sync). Otherwise one CTA of 8 warps per (row, head),
 // the page's launch shape: each warp keeps an online-softmax partial

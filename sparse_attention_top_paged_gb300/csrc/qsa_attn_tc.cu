@@ -1,5 +1,5 @@
-// qsa_attn_tc.cu — QSA prefill attention on the tcgen05 tensor cores, for G = 4
-// or 8 query heads per kv head and hd = 128 ("metrale_model_layers/layers/ops/qsa.rs",
+// qsa_attn_tc.cu — QSA prefill attention on the tcgen05 tensor cores, for G = 1,
+// 2, 4 or 8 query heads per kv head and hd = 128 ("metrale_model_layers/layers/ops/qsa.rs",
 // qsa_prefill_attn: per (row, query head) one softmax over every token of the
 // row's selected complete blocks and over the incomplete tail, with K and V of
 // the head's kv head read through the page table).
@@ -32,7 +32,7 @@
 //               with V read in place as an MN-major operand (the step's token
 //               rows are its K rows). Its commit frees the stage.
 //   warps 0-7   softmax: warp w owns tensor-memory lanes 32 (w % 4) .. + 31
-//               (tokens of S, dimensions of O) for G / 2 heads. Per
+//               (tokens of S, dimensions of O) for (G + 1) / 2 head slots. Per
 //               step: the heads' maxima over the step, a lazy reference maximum
 //               that moves only when a score exceeds it by more than kLazy
 //               (the running sums and the head's two output columns are then
@@ -107,6 +107,14 @@ __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint3
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t (&v)[1]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v[0]) : "r"(taddr) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, const uint32_t (&v)[1]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v[0]) : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t (&v)[2]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(taddr) : "memory");
 }
@@ -128,14 +136,18 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&v)[4])
                : "memory");
 }
 
-// n consecutive columns of this warp's lanes (n = 2 or 4)
+// n consecutive columns of this warp's lanes (n = 1, 2 or 4)
 template <int N>
 __device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&v)[N]) {
-  if constexpr (N == 2) tmem_ld2(taddr, v); else tmem_ld4(taddr, v);
+  if constexpr (N == 1) tmem_ld1(taddr, v);
+  else if constexpr (N == 2) tmem_ld2(taddr, v);
+  else tmem_ld4(taddr, v);
 }
 template <int N>
 __device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t (&v)[N]) {
-  if constexpr (N == 2) tmem_st2(taddr, v); else tmem_st4(taddr, v);
+  if constexpr (N == 1) tmem_st1(taddr, v);
+  else if constexpr (N == 2) tmem_st2(taddr, v);
+  else tmem_st4(taddr, v);
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
@@ -450,7 +462,7 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
     }
     __syncwarp();
   } else {
-    constexpr int HPW = G / 2;                 // heads a warp serves
+    constexpr int HPW = (G + 1) / 2;           // head slots a warp serves (with G = 1 the upper warps' slot is unused)
     const int qd = warp & 3, hh = warp >> 2;   // lane quarter; heads HPW hh .. HPW hh + HPW - 1
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * qd) << 16);
     bool ok = true;
@@ -590,7 +602,7 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
         const int h = HPW * hh + i;
         const float L = rs[h] + rs[kGroup + h] + rs[2 * kGroup + h] + rs[3 * kGroup + h];
         const float o = __uint_as_float(ohi[i]) + __uint_as_float(olo[i]);
-        pr.out[((it.r * pr.nq) + it.kvh * G + h) * kHd + 32 * qd + lane] = L > 0.0f ? o / L : 0.0f;
+        if (h < G) pr.out[((it.r * pr.nq) + it.kvh * G + h) * kHd + 32 * qd + lane] = L > 0.0f ? o / L : 0.0f;
       }
       ptx::tc_fence_before();   // the reads of O come before the next item's first value MMA
     }
@@ -612,8 +624,9 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
 }  // namespace
 
 bool qsa_attn_tc_supported(const float *q, uint32_t nq, uint32_t nkv, uint32_t hd, const void *kc, const void *vc) {
-  // 4 or 8 query heads per kv head; q is read as float2 pairs, K and V rows by 16-byte copies
-  return hd == kHd && nkv > 0 && (nq == nkv * 8 || nq == nkv * 4) && (reinterpret_cast<uintptr_t>(q) & 7u) == 0 &&
+  // 1, 2, 4 or 8 query heads per kv head; q is read as float2 pairs, K and V rows by 16-byte copies
+  return hd == kHd && nkv > 0 && (nq == nkv * 8 || nq == nkv * 4 || nq == nkv * 2 || nq == nkv) &&
+         (reinterpret_cast<uintptr_t>(q) & 7u) == 0 &&
          (reinterpret_cast<uintptr_t>(kc) & 15u) == 0 && (reinterpret_cast<uintptr_t>(vc) & 15u) == 0;
 }
 
@@ -621,8 +634,10 @@ cudaError_t launch_qsa_attn_tc(const float *q, const uint16_t *kc, const uint16_
                                int n_pages, int P, const int32_t *lists, float *out, uint32_t rows, uint32_t first_pos,
                                uint32_t topk, uint32_t ratio, uint32_t block_size, uint32_t nq, uint32_t nkv,
                                float inv_sqrt_d, int32_t *dev_status, cudaStream_t stream) {
+  const uint32_t G = nq / nkv;
   void (*kern)(Problem, long long, int32_t *) =
-      nq == nkv * 8 ? qsa_prefill_attn_tc_kernel<8> : qsa_prefill_attn_tc_kernel<4>;
+      G == 8 ? qsa_prefill_attn_tc_kernel<8> : G == 4 ? qsa_prefill_attn_tc_kernel<4>
+             : G == 2 ? qsa_prefill_attn_tc_kernel<2> : qsa_prefill_attn_tc_kernel<1>;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

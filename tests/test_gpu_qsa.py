@@ -255,14 +255,14 @@ def test_qsa_prefill_attn_tensor_core_tiles(scale, topk, ratio, first_pos):
     assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
 
 
-@pytest.mark.parametrize("nq", [8, 4, 2])
-def test_qsa_prefill_attn_tail_only_and_empty_rows(nq):
+@pytest.mark.parametrize("nq,hd", [(8, 128), (4, 128), (2, 128), (1, 128), (4, 64)])
+def test_qsa_prefill_attn_tail_only_and_empty_rows(nq, hd):
     """No selected blocks (topk = 0): every row attends to its tail alone, and
     a row whose tail is empty (its position completes a block) gives zeros
-    (8 and 4 q heads per kv head: the tcgen05 kernel's items without a step;
-    2: the tile kernel)."""
+    (hd 128: the tcgen05 kernel's items without a step; hd 64: the tile
+    kernel)."""
     rng = np.random.default_rng(55)
-    rows, fp, ratio, bs, nkv, hd = 13, 7, 4, 16, 2, 128
+    rows, fp, ratio, bs, nkv = 13, 7, 4, 16, 2
     pages = (fp + rows + bs - 1) // bs
     kb = wl._to_bf16_bits(rng.standard_normal((pages + 1, bs, nkv, hd)).astype(np.float32))
     vb = wl._to_bf16_bits(rng.standard_normal((pages + 1, bs, nkv, hd)).astype(np.float32))
@@ -278,11 +278,12 @@ def test_qsa_prefill_attn_tail_only_and_empty_rows(nq):
     assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
 
 
-def test_qsa_prefill_attn_q_4_byte_aligned():
+@pytest.mark.parametrize("nq", [16, 8, 4, 2])
+def test_qsa_prefill_attn_q_4_byte_aligned(nq):
     """q starting 4 bytes past an 8-byte boundary (the tensor-core kernel reads
     q in float pairs, so the 32-token tile kernel serves it) gives the same
-    attention."""
-    q, kb, vb, table, lists, fp, ratio = _attn_case(78, 128, 16, 2)
+    attention, at 8, 4, 2 and 1 q heads per kv head."""
+    q, kb, vb, table, lists, fp, ratio = _attn_case(78, 128, nq, 2)
     flat = torch.zeros(q.size + 1, dtype=torch.float32, device="cuda")
     flat[1:] = torch.from_numpy(q.reshape(-1)).cuda()
     qd = flat[1:].view(q.shape)
@@ -296,11 +297,12 @@ def test_qsa_prefill_attn_q_4_byte_aligned():
 
 
 @pytest.mark.parametrize("nq,nkv,bs,ratio", [(64, 8, 16, 16), (16, 2, 64, 16), (16, 2, 16, 64), (8, 1, 32, 8),
-                                             (32, 8, 16, 16), (8, 2, 64, 16), (4, 1, 32, 8)])
+                                             (32, 8, 16, 16), (8, 2, 64, 16), (4, 1, 32, 8), (16, 8, 16, 16),
+                                             (2, 1, 64, 16), (8, 8, 16, 16), (3, 3, 32, 8)])
 def test_qsa_prefill_attn_tensor_core_geometry(nq, nkv, bs, ratio):
-    """The tcgen05 kernel (8 or 4 q heads per kv head, hd 128) over 1, 2 and 8
-    kv heads, pages of 16, 32 and 64 tokens and blocks shorter or longer than a
-    page."""
+    """The tcgen05 kernel (8, 4, 2 or 1 q heads per kv head, hd 128) over 1, 2,
+    3 and 8 kv heads, pages of 16, 32 and 64 tokens and blocks shorter or
+    longer than a page."""
     q, kb, vb, table, lists, fp, ratio = _attn_case(150 + nkv + bs + ratio, 128, nq, nkv, rows=5, first_pos=2500,
                                                     ratio=ratio, bs=bs, topk=48)
     got, st = _attn_gpu(q, kb, vb, table, lists, fp, ratio)
