@@ -20,9 +20,8 @@
 //               inv_sqrt_d of the G heads split into bf16 high parts, rows 0-7,
 //               and low parts, rows 8-15, once per item: q keeps about 17
 //               significant bits; rows of unused head slots are zero) and the
-//               token mask. The copies arrive on the
-//               stage's barrier when they land, so a group never waits on its
-//               own copies.
+//               token mask. The copies arrive on the stage's barrier when they
+//               land, so a group never waits on its own copies.
 //   warp 8      MMA issuer (tcgen05, kind::f16, bf16 operands, f32 in tensor
 //               memory). Step j: S^T[128 tokens x 16] = K . Qs^T into one of
 //               two S slots (S = column h + column 8 + h), issued as soon as
@@ -32,14 +31,17 @@
 //               with V read in place as an MN-major operand (the step's token
 //               rows are its K rows). Its commit frees the stage.
 //   warps 0-7   softmax: warp w owns tensor-memory lanes 32 (w % 4) .. + 31
-//               (tokens of S, dimensions of O) for (G + 1) / 2 head slots. Per
-//               step: the heads' maxima over the step, a lazy reference maximum
-//               that moves only when a score exceeds it by more than kLazy
-//               (the running sums and the head's two output columns are then
-//               rescaled), weights p = exp(S - ref) split into bf16 high and
-//               low parts as the value MMA's B operand (two P slots). At the
-//               item's end: dimension d of head h = (column h + column 8 + h)
-//               / sum.
+//               (tokens of S, dimensions of O) for (G + 1) / 2 head slots. Each
+//               head keeps a lazy reference maximum that moves only when a
+//               score exceeds it by more than kLazy. Per step the warps write
+//               the weights p = exp(S - ref), split into bf16 high and low
+//               parts, as the value MMA's B operand (two P slots) and take one
+//               vote; only when some score broke its reference (an item's
+//               first step, or a jump) do they exchange the heads' maxima over
+//               the step, move the references, rescale the running sums and
+//               the head's two output columns, and write the weights again. At
+//               the item's end: dimension d of head h = (column h + column
+//               8 + h) / sum.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
