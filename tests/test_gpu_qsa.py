@@ -279,11 +279,12 @@ def test_qsa_prefill_attn_tail_only_and_empty_rows(nq, hd):
 
 
 @pytest.mark.parametrize("nq", [16, 8, 4, 2])
-def test_qsa_prefill_attn_q_4_byte_aligned(nq):
+@pytest.mark.parametrize("hd", [128, 64])
+def test_qsa_prefill_attn_q_4_byte_aligned(nq, hd):
     """q starting 4 bytes past an 8-byte boundary (the tensor-core kernel reads
     q in float pairs, so the 32-token tile kernel serves it) gives the same
-    attention, at 8, 4, 2 and 1 q heads per kv head."""
-    q, kb, vb, table, lists, fp, ratio = _attn_case(78, 128, nq, 2)
+    attention, at 8, 4, 2 and 1 q heads per kv head and hd 128 and 64."""
+    q, kb, vb, table, lists, fp, ratio = _attn_case(78 + hd, hd, nq, 2)
     flat = torch.zeros(q.size + 1, dtype=torch.float32, device="cuda")
     flat[1:] = torch.from_numpy(q.reshape(-1)).cuda()
     qd = flat[1:].view(q.shape)
@@ -291,7 +292,7 @@ def test_qsa_prefill_attn_q_4_byte_aligned(nq):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     got = _idx().qsa_prefill_attn(qd, torch.from_numpy(kb.view(np.int16)).cuda(), torch.from_numpy(vb.view(np.int16)).cuda(),
                                   torch.from_numpy(table).cuda(), torch.from_numpy(lists).cuda(), fp, ratio, dev_status=st)
-    ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio, 1.0 / math.sqrt(128))
+    ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio, 1.0 / math.sqrt(hd))
     assert int(st.item()) == ost == 0
     assert np.max(np.abs(got.cpu().numpy() - ref)) <= 1e-4 * np.max(np.abs(ref))
 
@@ -299,15 +300,16 @@ def test_qsa_prefill_attn_q_4_byte_aligned(nq):
 @pytest.mark.parametrize("nq,nkv,bs,ratio", [(64, 8, 16, 16), (16, 2, 64, 16), (16, 2, 16, 64), (8, 1, 32, 8),
                                              (32, 8, 16, 16), (8, 2, 64, 16), (4, 1, 32, 8), (16, 8, 16, 16),
                                              (2, 1, 64, 16), (8, 8, 16, 16), (3, 3, 32, 8)])
-def test_qsa_prefill_attn_tensor_core_geometry(nq, nkv, bs, ratio):
-    """The tcgen05 kernel (8, 4, 2 or 1 q heads per kv head, hd 128) over 1, 2,
-    3 and 8 kv heads, pages of 16, 32 and 64 tokens and blocks shorter or
-    longer than a page."""
-    q, kb, vb, table, lists, fp, ratio = _attn_case(150 + nkv + bs + ratio, 128, nq, nkv, rows=5, first_pos=2500,
-                                                    ratio=ratio, bs=bs, topk=48)
+@pytest.mark.parametrize("hd", [128, 64])
+def test_qsa_prefill_attn_tensor_core_geometry(nq, nkv, bs, ratio, hd):
+    """The tcgen05 kernel (8, 4, 2 or 1 q heads per kv head, hd 128) and the
+    tile kernel (hd 64) over 1, 2, 3 and 8 kv heads, pages of 16, 32 and 64
+    tokens and blocks shorter or longer than a page."""
+    q, kb, vb, table, lists, fp, ratio = _attn_case(150 + nkv + bs + ratio + hd, hd, nq, nkv, rows=5,
+                                                    first_pos=2500, ratio=ratio, bs=bs, topk=48)
     got, st = _attn_gpu(q, kb, vb, table, lists, fp, ratio)
     ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
-                                       1.0 / math.sqrt(128))
+                                       1.0 / math.sqrt(hd))
     assert st == ost == 0
     assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
 
