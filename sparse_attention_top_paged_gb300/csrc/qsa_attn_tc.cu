@@ -72,7 +72,7 @@ constexpr int B_FULL = 0, B_EMPTY = kStages, B_S = 2 * kStages, B_P = 2 * kStage
 constexpr uint32_t kOffMisc = kOffBar + 8 * B_COUNT;     // tensor-memory address, abort flag, bad-block flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;    // + slack to align the base to 1 KB
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-constexpr uint32_t kTmemCols = 64;                       // S slots: columns 0-15, 16-31; O: 32-47
+constexpr uint32_t kTmemCols = 64;   // S slots: columns 0-15, 16-31; O slots (item parity): 32-47, 48-63
 // Every wait gives up after kWaitNs (2 s; failure-path test builds shorten it
 // with IDX_WAIT_LIMIT_NS), raising the CTA's abort flag: the CTA then leaves
 // with no copy or MMA in flight and the call reports IDX_STATUS_TIMEOUT.
@@ -209,15 +209,16 @@ struct Problem {
   float inv_sqrt_d;
 };
 
-// One item's token numbering: list tokens [0, n_list), then the tail.
+// One item's token numbering: list tokens [0, n_list), then the tail. Items,
+// positions and token numbers are 32-bit (the launch checks that they fit).
 struct Item {
-  long long r, kvh, ncomp, n_list, tail0, n_virt;
-  __device__ void set(const Problem &pr, long long w) {
+  uint32_t r, kvh, ncomp, n_list, tail0, n_virt;
+  __device__ void set(const Problem &pr, uint32_t w) {
     r = w / pr.nkv;
-    kvh = w % pr.nkv;
-    const long long p = static_cast<long long>(pr.first_pos) + r;
+    kvh = w - r * pr.nkv;
+    const uint32_t p = pr.first_pos + r;
     ncomp = (p + 1) / pr.ratio;
-    n_list = static_cast<long long>(pr.topk) * pr.ratio;
+    n_list = pr.topk * pr.ratio;
     tail0 = ncomp * pr.ratio;
     n_virt = n_list + (p + 1 - tail0);
   }
@@ -226,11 +227,12 @@ struct Item {
 // The steps of a CTA in order: items blockIdx.x + i * gridDim.x with at least
 // one token, 128 tokens at a time.
 struct StepWalk {
-  long long w, items, base;
+  uint32_t w, items, base;
   Item it;
   bool valid;
+  uint32_t par = 0;   // parity of the item's ordinal in the CTA's walk
   __device__ void seek(const Problem &pr) {   // from item w: the first one with tokens
-    for (; w < items; w += gridDim.x) {
+    for (; w < items; w += gridDim.x, par ^= 1u) {
       it.set(pr, w);
       if (it.n_virt > 0) {
         base = 0;
@@ -244,6 +246,7 @@ struct StepWalk {
     base += kTok;
     if (base >= it.n_virt) {
       w += gridDim.x;
+      par ^= 1u;
       seek(pr);
     }
   }
@@ -252,7 +255,7 @@ struct StepWalk {
 // A producer group (four warps, a token a thread): steps g, g + kProdGroups,
 // ... of the CTA's walk; the groups' copies of consecutive steps overlap.
 template <int G>
-__device__ void producer(const Problem &pr, long long items, unsigned char *sm, uint32_t s_base, int g, int pw,
+__device__ void producer(const Problem &pr, uint32_t items, unsigned char *sm, uint32_t s_base, int g, int pw,
                          int lane, volatile int *abort, int *bad_flag) {
   const int ptid = 32 * pw + lane;
   const uint32_t bar0 = s_base + kOffBar;
@@ -262,11 +265,11 @@ __device__ void producer(const Problem &pr, long long items, unsigned char *sm, 
   sw.seek(pr);
   for (int i = 0; i < g && sw.valid; ++i) sw.next(pr);
   bool bad = false;
-  long long q_item = -1;   // the item whose Qs share this thread holds
+  uint32_t q_item = 0xFFFFFFFFu;   // the item whose Qs share this thread holds
   // this thread's share of the item's Qs operand: dimension pairs x = ptid + 128 i
   // (head x / 64, dimensions 2 (x % 64) and + 1), bf16 high and low parts
   uint32_t qhi[4] = {0u, 0u, 0u, 0u}, qlo[4] = {0u, 0u, 0u, 0u};
-  for (long long j = g; sw.valid; j += kProdGroups) {
+  for (uint32_t j = g; sw.valid; j += kProdGroups) {
     const int s = static_cast<int>(j % kStages);
     const uint32_t par = static_cast<uint32_t>((j / kStages) & 1);
     if (sw.w != q_item) {   // the group's first step of an item: its q rows, scaled and split once
@@ -275,7 +278,7 @@ __device__ void producer(const Problem &pr, long long items, unsigned char *sm, 
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int x = ptid + 128 * i, h = x >> 6, d = 2 * (x & 63);
-        v[i] = h < G ? *reinterpret_cast<const float2 *>(pr.q + ((sw.it.r * pr.nq) + sw.it.kvh * G + h) * kHd + d)
+        v[i] = h < G ? *reinterpret_cast<const float2 *>(pr.q + (static_cast<long long>(sw.it.r) * pr.nq + sw.it.kvh * G + h) * kHd + d)
                      : make_float2(0.0f, 0.0f);   // unused head slots: zero rows
       }
 #pragma unroll
@@ -290,21 +293,25 @@ __device__ void producer(const Problem &pr, long long items, unsigned char *sm, 
     // this thread's token (list entry, then page), before the stage is free
     long long off = -1;
     {
-      const long long v = sw.base + ptid;
-      long long pos = -1;
+      const uint32_t v = sw.base + ptid;
+      uint32_t pos = 0;
+      bool has = false;
       if (v < sw.it.n_list) {
-        const long long b = pr.lists[sw.it.r * pr.topk + v / pr.ratio];
-        if (b >= 0 && b < sw.it.ncomp) pos = b * pr.ratio + v % pr.ratio;
+        const uint32_t bi = v / pr.ratio;
+        const int b = pr.lists[static_cast<long long>(sw.it.r) * pr.topk + bi];
+        has = b >= 0 && static_cast<uint32_t>(b) < sw.it.ncomp;
+        pos = static_cast<uint32_t>(b) * pr.ratio + (v - bi * pr.ratio);
       } else if (v < sw.it.n_virt) {
+        has = true;
         pos = sw.it.tail0 + (v - sw.it.n_list);
       }
-      if (pos >= 0) {
-        const long long pg = pos / pr.block_size;
-        const int page = pg < pr.n_pages ? pr.table[pg] : -1;
+      if (has) {
+        const uint32_t pg = pos / pr.block_size;
+        const int page = pg < static_cast<uint32_t>(pr.n_pages) ? pr.table[pg] : -1;
         if (page < 0 || page >= pr.P)
           bad = true;
         else
-          off = ((static_cast<long long>(page) * pr.block_size + pos % pr.block_size) * pr.nkv + sw.it.kvh) * kHd;
+          off = ((static_cast<long long>(page) * pr.block_size + (pos - pg * pr.block_size)) * pr.nkv + sw.it.kvh) * kHd;
       }
     }
     const uint32_t live = __ballot_sync(0xFFFFFFFFu, off >= 0);
@@ -342,7 +349,7 @@ __device__ void producer(const Problem &pr, long long items, unsigned char *sm, 
 
 // The MMA warp's S^T for step j (its stage is full): stage j % kStages, S slot
 // j & 1. The whole warp calls it (operands stay warp-uniform); one lane issues.
-__device__ __forceinline__ void issue_scores(uint32_t s_base, uint32_t tmem, long long j) {
+__device__ __forceinline__ void issue_scores(uint32_t s_base, uint32_t tmem, uint32_t j) {
   const uint32_t st_a = s_base + static_cast<uint32_t>(j % kStages) * kStageBytes;
   const uint32_t d = tmem + 16 * static_cast<uint32_t>(j & 1);
   if (ptx::elect_one()) {
@@ -357,29 +364,29 @@ __device__ __forceinline__ void issue_scores(uint32_t s_base, uint32_t tmem, lon
   __syncwarp();
 }
 
-// The MMA warp's O^T += V^T . P^T for step j (its weights are written); its
-// commit frees the stage.
-__device__ __forceinline__ void issue_values(uint32_t s_base, uint32_t tmem, long long j, bool first) {
+// The MMA warp's O^T += V^T . P^T for step j (its weights are written) into the
+// item's O slot; its commit frees the stage.
+__device__ __forceinline__ void issue_values(uint32_t s_base, uint32_t tmem, uint32_t j, bool first, uint32_t oslot) {
   const uint32_t st_a = s_base + static_cast<uint32_t>(j % kStages) * kStageBytes;
   const uint32_t p_a = s_base + kOffP + 4096u * static_cast<uint32_t>(j & 1);
   if (ptx::elect_one()) {
     ptx::tc_fence_after();
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-      mma_ss(tmem + 32, sdesc(st_a + kOffV + k * 2048, 16384, 1024),
+      mma_ss(tmem + 32 + oslot, sdesc(st_a + kOffV + k * 2048, 16384, 1024),
              sdesc(p_a + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024), idesc_bf16(true), (!first || k > 0) ? 1u : 0u);
     ptx::mma_commit(s_base + kOffBar + 8 * (B_EMPTY + static_cast<int>(j % kStages)));
   }
   __syncwarp();
 }
 
-__device__ __forceinline__ uint32_t full_bar(uint32_t bar0, long long j) {
+__device__ __forceinline__ uint32_t full_bar(uint32_t bar0, uint32_t j) {
   return bar0 + 8 * (B_FULL + static_cast<int>(j % kStages));
 }
 
 // 21 warps (24 for register allocation, in groups of 4): at most 80 registers a thread
 template <int G>
-__global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long items,
+__global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, uint32_t items,
                                                                           int32_t *dev_status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // aligned by pointer arithmetic on the shared array, so accesses through sm stay shared-space ones
@@ -435,8 +442,9 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
     // Step j: S^T of step j + 1 once its stage is full (its S slot was last read
     // before the weights of step j - 1) and O of step j once its weights are
     // written, whichever can go first.
-    for (long long j = 0; sw.valid && ok; ++j) {
+    for (uint32_t j = 0; sw.valid && ok; ++j) {
       const bool first = sw.base == 0;   // the step starts an item: O restarts
+      const uint32_t oslot = 16u * sw.par;   // the item's O slot
       StepWalk nx = sw;
       nx.next(pr);
       bool s_done = !nx.valid, o_done = false;
@@ -450,7 +458,7 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
           issue_scores(s_base, tmem, j + 1);
           s_done = true;
         } else if (!o_done && __shfl_sync(0xFFFFFFFFu, ptx::mbar_test_wait(pb, ppar), 0)) {
-          issue_values(s_base, tmem, j, first);
+          issue_values(s_base, tmem, j, first, oslot);
           o_done = true;
         } else if ((it & 15u) != 0u) {
           __nanosleep(20);
@@ -468,7 +476,7 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
     const int qd = warp & 3, hh = warp >> 2;   // lane quarter; heads HPW hh .. HPW hh + HPW - 1
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * qd) << 16);
     bool ok = true;
-    long long j = 0;                           // the CTA's step counter
+    uint32_t j = 0;                            // the CTA's step counter (the launch keeps it below 2^31)
     int item_parity = 0;
     unsigned char *pslot = sm + kOffP;
     const int tok = 32 * qd + lane;
@@ -486,7 +494,38 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
         *reinterpret_cast<__nv_bfloat16 *>(pb + sw128(8 + h, tok, 2048)) = __float2bfloat16_rn(e - __bfloat162float(ehi));
       }
     };
-    for (long long w = blockIdx.x; w < items && ok; w += gridDim.x, item_parity ^= 1) {
+    // An item's output waits for its last value MMA; it is written after the next
+    // item's first step (or at the next item's end, or the CTA's), so the tensor
+    // pipe does not drain at each item's end. O and the sums alternate by item parity.
+    bool pend = false, pend_steps = false, pend_fail = false;
+    long long pend_out = 0;             // the item's first output element
+    uint32_t pend_bar = 0, pend_ph = 0;  // its last step's empty barrier and phase parity
+    int pend_par = 0;
+    auto flush = [&]() -> bool {
+      bool f_ok = true;
+      uint32_t ohi[HPW] = {}, olo[HPW] = {};
+      if (pend_steps) {   // O is complete once the item's last stage is free again
+        f_ok = ptx::mbar_wait(pend_bar, pend_ph, abort, kWaitNs);
+        ptx::tc_fence_after();
+        if (f_ok) {
+          tmem_ldn<HPW>(t_lane + 32 + 16 * pend_par + HPW * hh, ohi);
+          tmem_ldn<HPW>(t_lane + 40 + 16 * pend_par + HPW * hh, olo);
+          ptx::tmem_wait_ld();
+        }
+      }
+      const float *rs = red + 4 * kGroup * (1 + pend_par);
+#pragma unroll
+      for (int i = 0; i < HPW; ++i) {
+        const int h = HPW * hh + i;
+        const float L = rs[h] + rs[kGroup + h] + rs[2 * kGroup + h] + rs[3 * kGroup + h];
+        const float o = __uint_as_float(ohi[i]) + __uint_as_float(olo[i]);
+        if (h < G) pr.out[pend_out + h * kHd + 32 * qd + lane] = L > 0.0f ? o / L : 0.0f;
+      }
+      ptx::tc_fence_before();   // the reads of O come before the first value MMA of the item after next
+      pend = false;
+      return f_ok;
+    };
+    for (uint32_t w = blockIdx.x; w < items && ok; w += gridDim.x, item_parity ^= 1) {
       Item it;
       it.set(pr, w);
       float mref[HPW], lsum[HPW];
@@ -495,7 +534,9 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
         mref[i] = -INFINITY;
         lsum[i] = 0.0f;
       }
-      for (long long base = 0; base < it.n_virt; base += kTok, ++j) {
+      // one 128-token step of the item (the first one is peeled: after it the previous
+      // item's output is written)
+      auto step = [&](uint32_t base) {
         const int s = static_cast<int>(j % kStages), b = static_cast<int>(j & 1);
         // the stage's mask (producers' stores) and the step's S^T
         bool w_ok = ptx::mbar_wait(bar0 + 8 * (B_FULL + s), static_cast<uint32_t>((j / kStages) & 1), abort, kWaitNs);
@@ -520,11 +561,11 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
         write_weights(pslot + 4096 * b, sc, mref, lpart);
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
-        if (compute_sync_count(exceed || !w_ok) != 0) {
+        if (compute_sync_count(exceed || !w_ok || pend_fail) != 0) {
           // Some reference moves (an item's first step, or a jump): the heads' maxima
           // over the step, then the weights again.
-          ok = compute_sync_and(w_ok);
-          if (!ok) break;
+          ok = compute_sync_and(w_ok && !pend_fail);
+          if (!ok) return;
 #pragma unroll
           for (int i = 0; i < HPW; ++i) {
             const float m = warp_max(sc[i]);
@@ -546,13 +587,14 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
             }
           }
           if (rescale) {   // the value MMA of step j - 1 is done once its stage is free again
-            const long long jp = j - 1;
+            const uint32_t jp = j - 1;
             w_ok = ptx::mbar_wait(bar0 + 8 * (B_EMPTY + static_cast<int>(jp % kStages)),
                                   static_cast<uint32_t>((jp / kStages) & 1), abort, kWaitNs);
             ptx::tc_fence_after();
             uint32_t ohi[HPW], olo[HPW];
-            tmem_ldn<HPW>(t_lane + 32 + HPW * hh, ohi);
-            tmem_ldn<HPW>(t_lane + 40 + HPW * hh, olo);
+            const uint32_t oc = t_lane + 32 + 16 * item_parity + HPW * hh;
+            tmem_ldn<HPW>(oc, ohi);
+            tmem_ldn<HPW>(oc + 8, olo);
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < HPW; ++i)
@@ -560,29 +602,38 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
                 ohi[i] = __float_as_uint(__uint_as_float(ohi[i]) * corr[i]);
                 olo[i] = __float_as_uint(__uint_as_float(olo[i]) * corr[i]);
               }
-            tmem_stn<HPW>(t_lane + 32 + HPW * hh, ohi);
-            tmem_stn<HPW>(t_lane + 40 + HPW * hh, olo);
+            tmem_stn<HPW>(oc, ohi);
+            tmem_stn<HPW>(oc + 8, olo);
             ptx::tmem_wait_st();
           }
           write_weights(pslot + 4096 * b, sc, mref, lpart);
           ptx::fence_proxy_async_smem();
           ptx::tc_fence_before();
           ok = compute_sync_and(w_ok);
-          if (!ok) break;
+          if (!ok) return;
         }
 #pragma unroll
         for (int i = 0; i < HPW; ++i) lsum[i] += lpart[i];
         if (tid == 0) ptx::mbar_arrive(bar0 + 8 * (B_P + b));
+      };
+      uint32_t base = 0;
+      if (base < it.n_virt) {
+        step(base);
+        base += kTok;
+        ++j;
+        // the previous item's output (its last value MMA went before this step's; the
+        // stage's next phase needs weights of a later step, so the wait cannot miss it)
+        if (ok && pend) pend_fail = !flush();
       }
+      for (; ok && base < it.n_virt; base += kTok, ++j) step(base);
       if (!ok) break;
-      // ---- the item's sums and output ----
-      bool w_ok = true;
-      if (it.n_virt > 0) {   // O is complete once the last step's stage is free again
-        const long long jp = j - 1;
-        w_ok = ptx::mbar_wait(bar0 + 8 * (B_EMPTY + static_cast<int>(jp % kStages)),
-                              static_cast<uint32_t>((jp / kStages) & 1), abort, kWaitNs);
-        ptx::tc_fence_after();
+      if (pend) {   // an item without steps: the previous item's sums need a barrier first
+        ok = compute_sync_and(!pend_fail);
+        if (!ok) break;
+        ok = compute_sync_and(flush());
+        if (!ok) break;
       }
+      // ---- the item's sums; its output once its last value MMA is done ----
       float *rs = red + 4 * kGroup * (1 + item_parity);
 #pragma unroll
       for (int i = 0; i < HPW; ++i) {
@@ -591,22 +642,16 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
         if (lane == 0) rs[qd * kGroup + HPW * hh + i] = l;
       }
-      ok = compute_sync_and(w_ok);
-      if (!ok) break;
-      uint32_t ohi[HPW] = {}, olo[HPW] = {};
-      if (it.n_virt > 0) {
-        tmem_ldn<HPW>(t_lane + 32 + HPW * hh, ohi);
-        tmem_ldn<HPW>(t_lane + 40 + HPW * hh, olo);
-        ptx::tmem_wait_ld();
-      }
-#pragma unroll
-      for (int i = 0; i < HPW; ++i) {
-        const int h = HPW * hh + i;
-        const float L = rs[h] + rs[kGroup + h] + rs[2 * kGroup + h] + rs[3 * kGroup + h];
-        const float o = __uint_as_float(ohi[i]) + __uint_as_float(olo[i]);
-        if (h < G) pr.out[((it.r * pr.nq) + it.kvh * G + h) * kHd + 32 * qd + lane] = L > 0.0f ? o / L : 0.0f;
-      }
-      ptx::tc_fence_before();   // the reads of O come before the next item's first value MMA
+      pend = true;
+      pend_steps = it.n_virt > 0;
+      pend_out = (static_cast<long long>(it.r) * pr.nq + it.kvh * G) * kHd;
+      pend_bar = bar0 + 8 * (B_EMPTY + static_cast<int>((j - 1) % kStages));
+      pend_ph = static_cast<uint32_t>(((j - 1) / kStages) & 1);
+      pend_par = item_parity;
+    }
+    if (ok && pend) {   // the CTA's last item
+      ok = compute_sync_and(!pend_fail);
+      if (ok) ok = compute_sync_and(flush());
     }
     if (!ok) *abort = 1;
   }
@@ -625,9 +670,16 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, long long
 
 }  // namespace
 
-bool qsa_attn_tc_supported(const float *q, uint32_t nq, uint32_t nkv, uint32_t hd, const void *kc, const void *vc) {
-  // 1, 2, 4 or 8 query heads per kv head; q is read as float2 pairs, K and V rows by 16-byte copies
+bool qsa_attn_tc_supported(const float *q, uint32_t nq, uint32_t nkv, uint32_t hd, const void *kc, const void *vc,
+                           uint32_t rows, uint32_t first_pos, uint32_t topk, uint32_t ratio) {
+  // 1, 2, 4 or 8 query heads per kv head; q is read as float2 pairs, K and V rows by 16-byte copies;
+  // the steps of all items (at most (topk + 1) ratio tokens an item), the items, positions
+  // and token numbers fit the kernel's 32-bit counters
+  const unsigned long long tokens = (static_cast<unsigned long long>(topk) + 1) * ratio;
+  const unsigned long long steps = static_cast<unsigned long long>(rows) * nkv * (tokens / kTok + 1);
   return hd == kHd && nkv > 0 && (nq == nkv * 8 || nq == nkv * 4 || nq == nkv * 2 || nq == nkv) &&
+         steps < (1ull << 31) && tokens < (1ull << 31) &&
+         static_cast<unsigned long long>(first_pos) + rows < (1ull << 31) &&
          (reinterpret_cast<uintptr_t>(q) & 7u) == 0 &&
          (reinterpret_cast<uintptr_t>(kc) & 15u) == 0 && (reinterpret_cast<uintptr_t>(vc) & 15u) == 0;
 }
@@ -637,7 +689,7 @@ cudaError_t launch_qsa_attn_tc(const float *q, const uint16_t *kc, const uint16_
                                uint32_t topk, uint32_t ratio, uint32_t block_size, uint32_t nq, uint32_t nkv,
                                float inv_sqrt_d, int32_t *dev_status, cudaStream_t stream) {
   const uint32_t G = nq / nkv;
-  void (*kern)(Problem, long long, int32_t *) =
+  void (*kern)(Problem, uint32_t, int32_t *) =
       G == 8 ? qsa_prefill_attn_tc_kernel<8> : G == 4 ? qsa_prefill_attn_tc_kernel<4>
              : G == 2 ? qsa_prefill_attn_tc_kernel<2> : qsa_prefill_attn_tc_kernel<1>;
   int dev = 0, sms = 0;
@@ -647,8 +699,8 @@ cudaError_t launch_qsa_attn_tc(const float *q, const uint16_t *kc, const uint16_
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  const long long items = static_cast<long long>(rows) * nkv;
-  const int grid = static_cast<int>(items < sms ? items : sms);
+  const uint32_t items = rows * nkv;   // below 2^31 (checked with the support)
+  const int grid = static_cast<int>(items < static_cast<uint32_t>(sms) ? items : static_cast<uint32_t>(sms));
   const Problem pr{q, kc, vc, table, lists, out, n_pages, P, first_pos, topk, ratio, block_size, nq, nkv, inv_sqrt_d};
   kern<<<grid, kThreads, kSmemBytes, stream>>>(pr, items, dev_status);
   return cudaGetLastError();
