@@ -52,8 +52,8 @@ namespace idx {
 namespace {
 
 constexpr int kComputeWarps = 8;
-constexpr int kMmaWarp = kComputeWarps;
-constexpr int kProdWarp0 = kMmaWarp + 1;
+constexpr int kMmaWarp = kComputeWarps;   // issues the score MMAs; the next warp the value MMAs
+constexpr int kProdWarp0 = kMmaWarp + 2;
 constexpr int kProdGroups = 3;
 constexpr int kThreads = 32 * (kProdWarp0 + 4 * kProdGroups);
 constexpr int kStages = 3;
@@ -370,6 +370,7 @@ __device__ __forceinline__ void issue_values(uint32_t s_base, uint32_t tmem, uin
   const uint32_t st_a = s_base + static_cast<uint32_t>(j % kStages) * kStageBytes;
   const uint32_t p_a = s_base + kOffP + 4096u * static_cast<uint32_t>(j & 1);
   if (ptx::elect_one()) {
+    ptx::fence_proxy_async_smem();   // the V rows (their landing was seen by the softmax warps)
     ptx::tc_fence_after();
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -384,7 +385,7 @@ __device__ __forceinline__ uint32_t full_bar(uint32_t bar0, uint32_t j) {
   return bar0 + 8 * (B_FULL + static_cast<int>(j % kStages));
 }
 
-// 21 warps (24 for register allocation, in groups of 4): at most 80 registers a thread
+// 22 warps (24 for register allocation, in groups of 4): at most 80 registers a thread
 template <int G>
 __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, uint32_t items,
                                                                           int32_t *dev_status) {
@@ -425,50 +426,38 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, uint32_t 
     const int pwarp = warp - kProdWarp0;
     producer<G>(pr, items, sm, s_base, pwarp / 4, pwarp % 4, lane, abort, bad_flag);
   } else if (warp == kMmaWarp) {
-    // The whole warp walks the steps in lockstep; one elected lane issues.
+    // Score MMAs. The whole warp walks the steps in lockstep; one elected lane issues.
     StepWalk sw;
     sw.w = blockIdx.x;
     sw.items = items;
     sw.seek(pr);
 #ifdef IDX_TEST_STALL
-    // Failure-path test builds only: CTA 0's MMA warp first waits for a barrier
+    // Failure-path test builds only: CTA 0's score warp first waits for a barrier
     // nothing ever arrives on, so the wait gives up, raises the abort flag and
     // the CTA leaves without issuing an MMA.
     if (blockIdx.x == 0) ptx::mbar_wait(bar0 + 8 * B_NEVER, 0u, abort, kWaitNs);
 #endif
-    bool ok = *abort == 0 && (!sw.valid || ptx::mbar_wait(full_bar(bar0, 0), 0u, abort, kWaitNs));
-    ok = __all_sync(0xFFFFFFFFu, ok);
-    if (sw.valid && ok) issue_scores(s_base, tmem, 0);
-    // Step j: S^T of step j + 1 once its stage is full (its S slot was last read
-    // before the weights of step j - 1) and O of step j once its weights are
-    // written, whichever can go first.
-    for (uint32_t j = 0; sw.valid && ok; ++j) {
-      const bool first = sw.base == 0;   // the step starts an item: O restarts
-      const uint32_t oslot = 16u * sw.par;   // the item's O slot
-      StepWalk nx = sw;
-      nx.next(pr);
-      bool s_done = !nx.valid, o_done = false;
-      const uint32_t fb = full_bar(bar0, j + 1), pb = bar0 + 8 * (B_P + static_cast<int>(j & 1));
-      const uint32_t fpar = static_cast<uint32_t>(((j + 1) / kStages) & 1), ppar = static_cast<uint32_t>((j >> 1) & 1);
-      const uint64_t t0 = ptx::globaltimer();
-      // (non-blocking probes of both, a short sleep between rounds so the poll takes few issue
-      // slots from the softmax warps; lane 0's view decides for the warp)
-      for (uint32_t it = 1; !(s_done && o_done); ++it) {
-        if (!s_done && __shfl_sync(0xFFFFFFFFu, ptx::mbar_test_wait(fb, fpar), 0)) {
-          issue_scores(s_base, tmem, j + 1);
-          s_done = true;
-        } else if (!o_done && __shfl_sync(0xFFFFFFFFu, ptx::mbar_test_wait(pb, ppar), 0)) {
-          issue_values(s_base, tmem, j, first, oslot);
-          o_done = true;
-        } else if ((it & 15u) != 0u) {
-          __nanosleep(20);
-        } else if (__shfl_sync(0xFFFFFFFFu, *abort != 0 || ptx::globaltimer() - t0 > kWaitNs, 0)) {
-          *abort = 1;
-          ok = false;
-          break;
-        }
-      }
-      sw = nx;
+    for (uint32_t j = 0; sw.valid; ++j, sw.next(pr)) {
+      // S^T of step j once its stage is full and its S slot's last reader, the
+      // softmax of step j - 2, has written its weights
+      bool ok = *abort == 0 && ptx::mbar_wait(full_bar(bar0, j), (j / kStages) & 1u, abort, kWaitNs);
+      if (ok && j >= 2) ok = ptx::mbar_wait(bar0 + 8 * (B_P + static_cast<int>(j & 1)), ((j - 2) >> 1) & 1u, abort, kWaitNs);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      issue_scores(s_base, tmem, j);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp + 1) {
+    // Value MMAs: O of step j once its weights are written (a second issuing warp, so
+    // a step's value MMAs need not wait behind the issue of the next step's scores).
+    StepWalk sw;
+    sw.w = blockIdx.x;
+    sw.items = items;
+    sw.seek(pr);
+    for (uint32_t j = 0; sw.valid; ++j, sw.next(pr)) {
+      const bool ok =
+          *abort == 0 && ptx::mbar_wait(bar0 + 8 * (B_P + static_cast<int>(j & 1)), (j >> 1) & 1u, abort, kWaitNs);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      issue_values(s_base, tmem, j, sw.base == 0, 16u * sw.par);   // an item's first step restarts its O slot
     }
     __syncwarp();
   } else {
@@ -556,7 +545,13 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, uint32_t 
         }
         // Weights against the current references, written as if none moves: the
         // common case needs one barrier a step. P slot b was last read by the value
-        // MMA of step j - 2, done before the S^T of step j.
+        // MMA of step j - 2 (another warp issues those: its commit, not this step's
+        // S^T, says it is done; the stage's next phase needs weights of step j + 1).
+        if (j >= 2) {
+          const uint32_t jp = j - 2;
+          w_ok = w_ok && ptx::mbar_wait(bar0 + 8 * (B_EMPTY + static_cast<int>(jp % kStages)),
+                                        (jp / kStages) & 1u, abort, kWaitNs);
+        }
         float lpart[HPW];
         write_weights(pslot + 4096 * b, sc, mref, lpart);
         ptx::fence_proxy_async_smem();
