@@ -10,7 +10,7 @@
 // persistent, one CTA per SM taking items blockIdx.x, blockIdx.x + gridDim.x,
 // ... Its steps, laid end to end, flow through a ring of kStages shared-memory
 // stages:
-//   warps 9-20  three producer groups of four warps taking the steps in turn.
+//   warps 10-21 three producer groups of four warps taking the steps in turn.
 //               For each step a group looks up its 128 tokens (list entry,
 //               then page), copies their K and V rows (256 bytes each) into
 //               the stage with 16-byte asynchronous copies in the 128-byte
@@ -22,26 +22,31 @@
 //               significant bits; rows of unused head slots are zero) and the
 //               token mask. The copies arrive on the stage's barrier when they
 //               land, so a group never waits on its own copies.
-//   warp 8      MMA issuer (tcgen05, kind::f16, bf16 operands, f32 in tensor
-//               memory). Step j: S^T[128 tokens x 16] = K . Qs^T into one of
-//               two S slots (S = column h + column 8 + h), issued as soon as
-//               the stage is full, one step ahead of the value MMA of the step
-//               before, so it runs while the softmax of that step does; then,
-//               once the weights are written, O^T[128 dims x 16] += V^T . P^T
-//               with V read in place as an MN-major operand (the step's token
-//               rows are its K rows). Its commit frees the stage.
+//   warp 8      score MMAs (tcgen05, kind::f16, bf16 operands, f32 in tensor
+//               memory): S^T[128 tokens x 16] = K . Qs^T of step j into S slot
+//               j % 2 (S = column h + column 8 + h), as soon as the stage is
+//               full and the softmax of step j - 2 has left the slot.
+//   warp 9      value MMAs: O^T[128 dims x 16] += V^T . P^T of step j once its
+//               weights are written, V read in place as an MN-major operand
+//               (the step's token rows are its K rows), into the item's O slot
+//               (two, by item parity). Its commit frees the stage. With two
+//               issuing warps a step's value MMAs never wait behind the issue
+//               of the next step's scores.
 //   warps 0-7   softmax: warp w owns tensor-memory lanes 32 (w % 4) .. + 31
 //               (tokens of S, dimensions of O) for (G + 1) / 2 head slots. Each
 //               head keeps a lazy reference maximum that moves only when a
 //               score exceeds it by more than kLazy. Per step the warps write
 //               the weights p = exp(S - ref), split into bf16 high and low
-//               parts, as the value MMA's B operand (two P slots) and take one
+//               parts, as the value MMA's B operand (two P slots, a slot
+//               reused once the value MMA two steps back is done) and take one
 //               vote; only when some score broke its reference (an item's
 //               first step, or a jump) do they exchange the heads' maxima over
 //               the step, move the references, rescale the running sums and
-//               the head's two output columns, and write the weights again. At
-//               the item's end: dimension d of head h = (column h + column
-//               8 + h) / sum.
+//               the head's two output columns, and write the weights again. An
+//               item's output, dimension d of head h = (column h + column 8 +
+//               h) / sum, is written after the next item's first step, once
+//               its last value MMA is done, so the tensor pipe does not drain
+//               at each item's end.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
