@@ -28,7 +28,8 @@ namespace idx {
 
 // qsa_attn_tc.cu: the tcgen05 kernel for 1, 2, 4 or 8 query heads per kv head, hd = 128.
 bool qsa_attn_tc_supported(const float *q, uint32_t nq, uint32_t nkv, uint32_t hd, const void *kc, const void *vc,
-                           uint32_t rows, uint32_t first_pos, uint32_t topk, uint32_t ratio);
+                           uint32_t rows, uint32_t first_pos, uint32_t topk, uint32_t ratio, int P,
+                           uint32_t block_size);
 cudaError_t launch_qsa_attn_tc(const float *q, const uint16_t *kc, const uint16_t *vc, const int32_t *table,
                                int n_pages, int P, const int32_t *lists, float *out, uint32_t rows, uint32_t first_pos,
                                uint32_t topk, uint32_t ratio, uint32_t block_size, uint32_t nq, uint32_t nkv,
@@ -495,7 +496,7 @@ extern "C" idx_status_t idx_qsa_prefill_attn(const float *q, const uint16_t *k_c
     return IDX_ERR_INVALID_ARG;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint32_t G = nq / nkv;
-  if (qsa_attn_tc_supported(q, nq, nkv, hd, k_cache, v_cache, rows, first_pos, topk, ratio)) {
+  if (qsa_attn_tc_supported(q, nq, nkv, hd, k_cache, v_cache, rows, first_pos, topk, ratio, P, block_size)) {
     const cudaError_t e = launch_qsa_attn_tc(q, k_cache, v_cache, block_table, n_pages, P, lists, attn_out, rows,
                                              first_pos, topk, ratio, block_size, nq, nkv, inv_sqrt_d, dev_status, s);
     return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;

@@ -295,8 +295,9 @@ __device__ void producer(const Problem &pr, uint32_t items, unsigned char *sm, u
         qlo[i] = *reinterpret_cast<const uint32_t *>(&lo);
       }
     }
-    // this thread's token (list entry, then page), before the stage is free
-    long long off = -1;
+    // this thread's token (list entry, then page), before the stage is free: its cache
+    // row (page, slot, kv head), 128 elements each, or -1
+    int crow = -1;
     {
       const uint32_t v = sw.base + ptid;
       uint32_t pos = 0;
@@ -316,23 +317,25 @@ __device__ void producer(const Problem &pr, uint32_t items, unsigned char *sm, u
         if (page < 0 || page >= pr.P)
           bad = true;
         else
-          off = ((static_cast<long long>(page) * pr.block_size + (pos - pg * pr.block_size)) * pr.nkv + sw.it.kvh) * kHd;
+          crow = static_cast<int>((static_cast<uint32_t>(page) * pr.block_size + (pos - pg * pr.block_size)) * pr.nkv +
+                                  sw.it.kvh);
       }
     }
-    const uint32_t live = __ballot_sync(0xFFFFFFFFu, off >= 0);
+    const uint32_t live = __ballot_sync(0xFFFFFFFFu, crow >= 0);
     if (!ptx::mbar_wait(bar0 + 8 * (B_EMPTY + s), par ^ 1u, abort, kWaitNs)) break;
     unsigned char *st = sm + s * kStageBytes;
     const uint32_t st_a = s_base + s * kStageBytes;
     if (lane == 0) reinterpret_cast<uint32_t *>(st + kOffMask)[pw] = live;
     // a half-warp copies one token's 256-byte K row and V row (16 lanes x 16 bytes)
-#pragma unroll 4
+    const uint16_t *kc_l = pr.kc + 8 * (lane & 15), *vc_l = pr.vc + 8 * (lane & 15);
+#pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int t = 2 * i + (lane >> 4), c = lane & 15;
-      const long long src = __shfl_sync(0xFFFFFFFFu, off, t);
+      const int src = __shfl_sync(0xFFFFFFFFu, crow, t);
       const uint32_t o = sw128(32 * pw + t, 8 * c, 16384);
       if (src >= 0) {
-        cp_async16(st_a + kOffK + o, pr.kc + src + 8 * c);
-        cp_async16(st_a + kOffV + o, pr.vc + src + 8 * c);
+        cp_async16(st_a + kOffK + o, kc_l + static_cast<long long>(src) * kHd);
+        cp_async16(st_a + kOffV + o, vc_l + static_cast<long long>(src) * kHd);
       } else {   // no token: zero rows, so the value sum sees finite values
         *reinterpret_cast<uint4 *>(st + kOffK + o) = make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4 *>(st + kOffV + o) = make_uint4(0u, 0u, 0u, 0u);
@@ -671,14 +674,17 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, uint32_t 
 }  // namespace
 
 bool qsa_attn_tc_supported(const float *q, uint32_t nq, uint32_t nkv, uint32_t hd, const void *kc, const void *vc,
-                           uint32_t rows, uint32_t first_pos, uint32_t topk, uint32_t ratio) {
-  // 1, 2, 4 or 8 query heads per kv head; q is read as float2 pairs, K and V rows by 16-byte copies;
+                           uint32_t rows, uint32_t first_pos, uint32_t topk, uint32_t ratio, int P,
+                           uint32_t block_size) {
+  // 1, 2, 4 or 8 query heads per kv head; q is read as float2 pairs, K and V rows by 16-byte copies
+  // (their cache rows, P x block_size x nkv of them, are numbered in 31 bits);
   // the steps of all items (at most (topk + 1) ratio tokens an item), the items, positions
   // and token numbers fit the kernel's 32-bit counters
   const unsigned long long tokens = (static_cast<unsigned long long>(topk) + 1) * ratio;
   const unsigned long long steps = static_cast<unsigned long long>(rows) * nkv * (tokens / kTok + 1);
   return hd == kHd && nkv > 0 && (nq == nkv * 8 || nq == nkv * 4 || nq == nkv * 2 || nq == nkv) &&
          steps < (1ull << 31) && tokens < (1ull << 31) &&
+         static_cast<unsigned long long>(P) * block_size * nkv < (1ull << 31) &&
          static_cast<unsigned long long>(first_pos) + rows < (1ull << 31) &&
          (reinterpret_cast<uintptr_t>(q) & 7u) == 0 &&
          (reinterpret_cast<uintptr_t>(kc) & 15u) == 0 && (reinterpret_cast<uintptr_t>(vc) & 15u) == 0;
