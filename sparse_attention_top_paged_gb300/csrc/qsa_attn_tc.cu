@@ -204,6 +204,21 @@ __device__ __forceinline__ uint32_t sw128(int row, int col, uint32_t half) {
   return (col >> 6) * half + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) + (col & 7) * 2;
 }
 
+// floor(n / d) for n < 2^31 as (n m) >> s, with s = 31 + ceil(log2 d) and m =
+// ceil(2^s / d) < 2^32: division by an invariant integer through multiplication
+// (Granlund and Montgomery); m d - 2^s < d keeps the error below one for such n.
+struct DivU {
+  uint32_t m, s;
+};
+inline DivU div_magic(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  return DivU{static_cast<uint32_t>(((1ull << (31 + l)) + d - 1) / d), 31 + l};
+}
+__device__ __forceinline__ uint32_t divu(uint32_t n, DivU d) {
+  return static_cast<uint32_t>((static_cast<unsigned long long>(n) * d.m) >> d.s);
+}
+
 struct Problem {
   const float *q;
   const uint16_t *kc, *vc;
@@ -212,6 +227,7 @@ struct Problem {
   int n_pages, P;
   uint32_t first_pos, topk, ratio, block_size, nq, nkv;
   float inv_sqrt_d;
+  DivU by_ratio, by_block;   // the token lookups' divisions (operands below 2^31)
 };
 
 // One item's token numbering: list tokens [0, n_list), then the tail. Items,
@@ -303,7 +319,7 @@ __device__ void producer(const Problem &pr, uint32_t items, unsigned char *sm, u
       uint32_t pos = 0;
       bool has = false;
       if (v < sw.it.n_list) {
-        const uint32_t bi = v / pr.ratio;
+        const uint32_t bi = divu(v, pr.by_ratio);
         const int b = pr.lists[static_cast<long long>(sw.it.r) * pr.topk + bi];
         has = b >= 0 && static_cast<uint32_t>(b) < sw.it.ncomp;
         pos = static_cast<uint32_t>(b) * pr.ratio + (v - bi * pr.ratio);
@@ -312,7 +328,7 @@ __device__ void producer(const Problem &pr, uint32_t items, unsigned char *sm, u
         pos = sw.it.tail0 + (v - sw.it.n_list);
       }
       if (has) {
-        const uint32_t pg = pos / pr.block_size;
+        const uint32_t pg = divu(pos, pr.by_block);
         const int page = pg < static_cast<uint32_t>(pr.n_pages) ? pr.table[pg] : -1;
         if (page < 0 || page >= pr.P)
           bad = true;
@@ -707,7 +723,8 @@ cudaError_t launch_qsa_attn_tc(const float *q, const uint16_t *kc, const uint16_
   if (e != cudaSuccess) return e;
   const uint32_t items = rows * nkv;   // below 2^31 (checked with the support)
   const int grid = static_cast<int>(items < static_cast<uint32_t>(sms) ? items : static_cast<uint32_t>(sms));
-  const Problem pr{q, kc, vc, table, lists, out, n_pages, P, first_pos, topk, ratio, block_size, nq, nkv, inv_sqrt_d};
+  const Problem pr{q, kc, vc, table, lists, out, n_pages, P, first_pos, topk, ratio, block_size, nq, nkv,
+                   inv_sqrt_d, div_magic(ratio), div_magic(block_size)};
   kern<<<grid, kThreads, kSmemBytes, stream>>>(pr, items, dev_status);
   return cudaGetLastError();
 }
