@@ -278,6 +278,42 @@ def test_qsa_prefill_attn_tail_only_and_empty_rows(nq, hd):
     assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
 
 
+@pytest.mark.parametrize("nq", [8, 2])
+def test_qsa_prefill_attn_tail_only_many_items(nq):
+    """Tail-only rows (topk = 0) over more items than SMs: a CTA's items
+    alternate between one short step and none (every fourth row's tail is
+    empty), so outputs written after a later item, or at the end of an item
+    without steps, and both tensor-memory O slots are exercised."""
+    rng = np.random.default_rng(56)
+    rows, fp, ratio, bs, nkv, hd = 613, 7, 4, 16, 2, 128
+    pages = (fp + rows + bs - 1) // bs
+    kb = wl._to_bf16_bits(rng.standard_normal((pages + 1, bs, nkv, hd)).astype(np.float32))
+    vb = wl._to_bf16_bits(rng.standard_normal((pages + 1, bs, nkv, hd)).astype(np.float32))
+    table = rng.permutation(pages + 1)[:pages].astype(np.int32)
+    lists = np.zeros((rows, 0), dtype=np.int32)
+    q = rng.standard_normal((rows, nq * nkv, hd)).astype(np.float32)
+    got, st = _attn_gpu(q, kb, vb, table, lists, fp, ratio)
+    ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
+                                       1.0 / math.sqrt(hd))
+    assert st == ost == 0
+    empty = [r for r in range(rows) if (fp + r + 1) % ratio == 0]
+    assert len(empty) > 100 and np.all(got[empty] == 0.0)
+    assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
+
+
+@pytest.mark.parametrize("nq", [8, 1])
+def test_qsa_prefill_attn_one_and_two_step_items(nq):
+    """700 rows over 8 listed blocks of 16 tokens: items of one step (rows whose
+    tail is empty) and of two, several per CTA, with 8 and 1 q heads per kv
+    head; every row against the oracle."""
+    q, kb, vb, table, lists, fp, ratio = _attn_case(57 + nq, 128, nq, 1, rows=700, first_pos=1000, topk=8)
+    got, st = _attn_gpu(q, kb, vb, table, lists, fp, ratio)
+    ref, ost = oracle.qsa_prefill_attn(q, _bf16_vals(kb), _bf16_vals(vb), table, lists, fp, ratio,
+                                       1.0 / math.sqrt(128))
+    assert st == ost == 0
+    assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref))
+
+
 @pytest.mark.parametrize("nq", [16, 8, 4, 2])
 @pytest.mark.parametrize("hd", [128, 64])
 def test_qsa_prefill_attn_q_4_byte_aligned(nq, hd):
