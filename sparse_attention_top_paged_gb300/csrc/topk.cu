@@ -24,6 +24,10 @@
 //      every key to its output slot (its bin's start + its rank in the bin).
 //      Otherwise: one pass collects the keys at or above the boundary and a
 //      bitonic sort orders them.
+//      When rows are at most half as many as SMs (and no list was collected
+//      beforehand), two CTAs take each row: both decide the boundary alike,
+//      then the first places, orders and writes the bins whose segment starts
+//      in the first half of the buffer and the second the rest.
 // Rows of at most kSmallRow keys skip the digits: every candidate key goes
 // into the buffer and one bitonic sort orders them.
 // Each pass reads the row from shared memory: one bulk copy stages the whole
@@ -71,6 +75,7 @@ struct SelShared {
   uint32_t sub_cnt[256], sub_cur[256];  // a large bin's split by the next 8 key bits
   int n_large;
   uint32_t large[8];          // packed entries of the large bins (kMaxLarge)
+  int split_bin;              // two CTAs a row: the highest bin of the second one's part
 };
 
 // Dynamic shared memory: SelShared, then the key buffer: up to k - 1 keys
@@ -526,7 +531,8 @@ template <int kThreads>
 __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(ScoreParams p, const float *__restrict__ scores,
                                                               long long ld, const uint32_t *__restrict__ hist,
                                                               const uint64_t *__restrict__ cand,
-                                                              uint32_t *__restrict__ cand_cnt, int cand_cap) {
+                                                              uint32_t *__restrict__ cand_cnt, int cand_cap,
+                                                              int halves_arg) {
   constexpr int kPer = kBins / kThreads;           // bins each thread owns in a scan
   // Bins up to kWarpBin keys are sorted by one warp in registers: 128 with
   // 1024 threads per row; 256 with 512 (more rows than SMs, as in prefill,
@@ -544,7 +550,14 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
   uint64_t *buf = reinterpret_cast<uint64_t *>(smem_raw + lay.buf);
   const int cap = static_cast<int>(lay.cap);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int t = blockIdx.x;
+  // With two CTAs a row (halves = 2; rows without a split collection), both
+  // decide the boundary alike, then each places, orders and writes only the
+  // bins of its part of the output: the first CTA the bins whose segment
+  // starts in the first half of the buffer, the second the rest. Whatever is
+  // not decided on the first digit, and the padding, is the first CTA's.
+  // (only the 1024-thread variant, used when rows leave SMs idle, is launched so)
+  const int halves = kThreads == 1024 ? halves_arg : 1;
+  const int t = blockIdx.x / halves, h = blockIdx.x - t * halves;
   const int k = p.top_k;
   int32_t *oi = p.topk_idx + static_cast<long long>(t) * k;
   float *os = p.topk_score + static_cast<long long>(t) * k;
@@ -564,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
     for (int j = 0; j < kPer; ++j) hpre[j] = h[kBins - 1 - kPer * tid - j];
   }
   if (bad_len(p, L)) {
+    if (h != 0) return;
     if (tid == 0 && p.dev_status) atomicOr(p.dev_status, IDX_STATUS_BAD_LEN);
     for (int i = tid; i < k; i += kThreads) {
       oi[i] = -1;
@@ -575,6 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
 
   // ---- a short row: every candidate key into the buffer, one sort ----
   if (L <= kSmallRow && pow2_at_least(max(L, 64)) <= cap) {
+    if (h != 0) return;
     if (tid == 0) sh->n_buf = 0;
     __syncthreads();
     for (int i = tid; i < L; i += kThreads) {
@@ -610,6 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
     sh->b_above = 0;
     sh->b_cnt = 0;
     sh->n_buf = 0;
+    sh->split_bin = -1;
   }
 
   // ---- locate the boundary bin, digit by digit ----
@@ -717,8 +733,28 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
   if (((take_all && rounds == 0) || (!take_all && rounds == 1)) && max_above <= kRankBinMax) {
     // ---- decided on the first digit: place, rank, write ----
     // (keys below the boundary bin are dropped on their top 32 bits alone)
+    const int total = min(take_all ? static_cast<int>(all_keys) : sh->b_above + sh->b_cnt, cap);
+    bool solo = halves == 1;
+    if (!solo) {   // the second CTA's part: the bins whose segment starts at total / 2 or later
+      if (tid == 0) sh->n_large = 0;
+      __syncthreads();
+      const uint32_t split = static_cast<uint32_t>(total + 1) / 2u;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const uint32_t e = sh->table[kBins - 1 - kPer * tid - j];
+        if (e != 0u && (e & 0xFFFFu) >= split) atomicMax(&sh->split_bin, kBins - 1 - kPer * tid - j);
+        if (static_cast<int>(e >> 16) > kWarpBin) atomicAdd(&sh->n_large, 1);
+      }
+      __syncthreads();
+      // so many large bins that the whole buffer is sorted at once: the first CTA alone
+      solo = sh->n_large > kMaxLarge;
+      if (solo && h != 0) return;
+    }
+    const int split_bin = sh->split_bin;
+    // bin b is this CTA's: the first CTA takes the bins above split_bin, the second the others
+    auto mine = [&](int b) { return solo || ((b > split_bin) == (h == 0)); };
     auto place = [&](uint64_t key) {
-      if ((key & mask) >= prefix) {
+      if ((key & mask) >= prefix && mine(static_cast<int>(key >> 52))) {
         const uint32_t old = atomicAdd(&sh->table[key >> 52], 1u);
         if (static_cast<int>(old & 0xFFFFu) < cap) buf[old & 0xFFFFu] = key;
       }
@@ -733,7 +769,6 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
       rs.pass(static_cast<uint32_t>(prefix >> 32), place);
     }
     __syncthreads();
-    const int total = min(take_all ? static_cast<int>(all_keys) : sh->b_above + sh->b_cnt, cap);
     // Every bin holding some of the k best keys is now a contiguous segment
     // of buf. Bins of more than kWarpBin keys ("large") are first ordered by
     // the next 8 key bits, one bin at a time by the whole CTA, so each of
@@ -745,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const uint32_t e = sh->table[kBins - 1 - kPer * tid - j];
-      if (static_cast<int>(e >> 16) > kWarpBin) {
+      if (static_cast<int>(e >> 16) > kWarpBin && mine(kBins - 1 - kPer * tid - j)) {
         const int slot = atomicAdd(&sh->n_large, 1);
         if (slot < kMaxLarge) sh->large[slot] = e;
       }
@@ -828,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
                                 : nullptr;
       for (int b0 = warp; b0 < kBins; b0 += 32 * (kThreads / 32)) {
         const int b = b0 + (kThreads / 32) * lane;       // this lane's bin of the group
-        const uint32_t pk = (b < kBins) ? sh->table[b] : 0u;
+        const uint32_t pk = (b < kBins && mine(b)) ? sh->table[b] : 0u;
         uint32_t todo = __ballot_sync(0xFFFFFFFFu, pk != 0u && static_cast<int>(pk >> 16) <= kWarpBin);
         while (todo) {
           const int l = __ffs(todo) - 1;
@@ -849,6 +884,7 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
   } else {
     // ---- decided on a later digit, or a bin above the boundary too large to
     // rank by comparison: collect, sort, write ----
+    if (h != 0) return;
     rs.pass(static_cast<uint32_t>(prefix >> 32), [&](uint64_t key) {
       if ((key & mask) >= prefix) {
         const int slot = atomicAdd(&sh->n_buf, 1);
@@ -864,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
     produced = min(count, k);
     for (int i = tid; i < produced; i += kThreads) emit(buf[i], i);
   }
-  for (int i = produced + tid; i < k; i += kThreads) {
+  for (int i = produced + tid; h == 0 && i < k; i += kThreads) {
     oi[i] = -1;
     os[i] = -INFINITY;
   }
@@ -918,7 +954,7 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
   // single sort of at most kSmallRow keys gains nothing from more warps.
   const int sms = device_sm_count();
   const bool wide = sms > 0 && p.T <= sms && static_cast<long long>(p.max_lb) * p.epb > kSmallRow;
-  void (*kern)(ScoreParams, const float *, long long, const uint32_t *, const uint64_t *, uint32_t *, int) =
+  void (*kern)(ScoreParams, const float *, long long, const uint32_t *, const uint64_t *, uint32_t *, int, int) =
       wide ? topk_stream_kernel<1024> : topk_stream_kernel<512>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -939,8 +975,11 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
     e = cudaLaunchKernelEx(&ca, select_collect_kernel, p, scores, ld, hist, cand, cand_cnt, pl.cand_cap);
     if (e != cudaSuccess) return e;
   }
+  // Rows that leave SMs idle (at most half as many as SMs, each streamed whole):
+  // two CTAs a row, each ordering and writing the bins of one part of the output.
+  const int halves = (wide && cand == nullptr && 2 * p.T <= sms) ? 2 : 1;   // (wide: the 1024-thread variant)
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.T), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(p.T * halves), 1, 1);
   cfg.blockDim = dim3(wide ? 1024 : 512, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -950,7 +989,7 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, p, scores, ld, hist, static_cast<const uint64_t *>(cand),
-                            cand_cnt, pl.cand_cap);
+                            cand_cnt, pl.cand_cap, halves);
 }
 
 }  // namespace idx
