@@ -438,30 +438,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = misc + M_ABORT;
   auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
 
-  if (threadIdx.x == 0) {
-    ptx::launch_dependents();  // the selection kernel may be scheduled as CTAs of this one finish
-    for (int s = 0; s < lay.ns; ++s) {
+  if (warp == 0) {   // the barriers, spread over the warp's lanes (the metadata ring alone has 2 kR)
+    if (lane == 0) ptx::launch_dependents();  // the selection kernel may be scheduled as CTAs of this one finish
+    for (int s = lane; s < lay.ns; s += 32) {
       ptx::mbar_init(bar(B_FULL_RAW + s), 1);
       ptx::mbar_init(bar(B_EMPTY_RAW + s), kFp4 ? 1 : kDecWarps);   // decoders, or the MMA commit
     }
-    for (int a = 0; a < kMaxSlots; ++a) {
-      ptx::mbar_init(bar(B_FULL_A + a), kDecWarps);
-      ptx::mbar_init(bar(B_EMPTY_A + a), 1);
-      ptx::mbar_init(bar(B_FULL_D + a), 1);
-      ptx::mbar_init(bar(B_EMPTY_D + a), 4);
+    if (lane < kMaxSlots) {
+      ptx::mbar_init(bar(B_FULL_A + lane), kDecWarps);
+      ptx::mbar_init(bar(B_EMPTY_A + lane), 1);
+      ptx::mbar_init(bar(B_FULL_D + lane), 1);
+      ptx::mbar_init(bar(B_EMPTY_D + lane), 4);
     }
-    for (int a = 0; a < 2; ++a) {
-      ptx::mbar_init(bar(B_SEG_FULL + a), 1);   // producer (record copy)
-      ptx::mbar_init(bar(B_SEG_BFREE + a), 1);
-      ptx::mbar_init(bar(B_SEG_WFREE + a), 4 * kEpiGroups);  // one arrive per epilogue warp
+    if (lane < 2) {
+      ptx::mbar_init(bar(B_SEG_FULL + lane), 1);   // producer (record copy)
+      ptx::mbar_init(bar(B_SEG_BFREE + lane), 1);
+      ptx::mbar_init(bar(B_SEG_WFREE + lane), 4 * kEpiGroups);  // one arrive per epilogue warp
     }
-    for (int r = 0; r < kR; ++r) {
+    for (int r = lane; r < kR; r += 32) {
       ptx::mbar_init(bar(B_META_FULL + r), 1);   // resolver
       ptx::mbar_init(bar(B_META_EMPTY + r), 4);  // epilogue warps
     }
-    ptx::mbar_init(bar(B_DRAIN), 1);   // MMA commit before exit
-    ptx::mbar_init(bar(B_NEVER), 1);   // nothing arrives (failure-path test builds only)
-    misc[M_ABORT] = 0;
+    if (lane == 0) {
+      ptx::mbar_init(bar(B_DRAIN), 1);   // MMA commit before exit
+      ptx::mbar_init(bar(B_NEVER), 1);   // nothing arrives (failure-path test builds only)
+      misc[M_ABORT] = 0;
+    }
     ptx::fence_mbar_init();
   }
   if (warp == 1) ptx::tmem_alloc(ptx::smem_addr(misc + M_TMEM), 512);
