@@ -24,10 +24,10 @@
 //      every key to its output slot (its bin's start + its rank in the bin).
 //      Otherwise: one pass collects the keys at or above the boundary and a
 //      bitonic sort orders them.
-//      When rows are at most half as many as SMs (and no list was collected
-//      beforehand), two CTAs take each row: both decide the boundary alike,
-//      then the first places, orders and writes the bins whose segment starts
-//      in the first half of the buffer and the second the rest.
+//      When rows leave SMs idle, several CTAs take each row (2 when each has
+//      to stream the row, up to 4 when they read a list collected beforehand):
+//      all decide the boundary alike, then CTA h places, orders and writes the
+//      bins whose segment starts in part h of the buffer.
 // Rows of at most kSmallRow keys skip the digits: every candidate key goes
 // into the buffer and one bitonic sort orders them.
 // Each pass reads the row from shared memory: one bulk copy stages the whole
@@ -50,6 +50,7 @@ constexpr int kBins = kScoreBins;                 // 12-bit digits
 constexpr int kBndCap = 2048;                     // largest boundary bin collected (else refine)
 constexpr int kRankBinMax = kBndCap;              // largest bin above the boundary ordered in place
 constexpr int kMaxLarge = 8;                      // more larger bins than this: sort the whole buffer
+constexpr int kMaxParts = 4;                      // CTAs that share one row's ordering (8 measured slower on long decode)
 constexpr int kUnroll = 4;                        // 16-byte score loads in flight per thread
 constexpr int kSmallRow = 2048;                   // rows up to this long are sorted whole
 constexpr int kCollectThreads = 256;              // split collection: threads per CTA,
@@ -75,7 +76,7 @@ struct SelShared {
   uint32_t sub_cnt[256], sub_cur[256];  // a large bin's split by the next 8 key bits
   int n_large;
   uint32_t large[8];          // packed entries of the large bins (kMaxLarge)
-  int split_bin;              // two CTAs a row: the highest bin of the second one's part
+  int split_bin[kMaxParts];   // several CTAs a row: split_bin[q], the highest bin of part q (q >= 1)
 };
 
 // Dynamic shared memory: SelShared, then the key buffer: up to k - 1 keys
@@ -89,7 +90,7 @@ struct SelSmem {
 };
 __host__ __device__ inline SelSmem sel_smem(int k, long long max_len) {
   SelSmem m{};
-  m.buf = (sizeof(SelShared) + 15) & ~size_t(15);
+  m.buf = (sizeof(SelShared) + 127) & ~size_t(127);   // 128-byte aligned: a warp's 16-byte reads of the staged row then span whole lines
   const int want = k + kBndCap;
   m.cap = static_cast<size_t>(pow2_at_least(want < 64 ? 64 : want));
   m.stage = m.buf + m.cap * 8;
@@ -527,12 +528,11 @@ __global__ void __launch_bounds__(kCollectThreads) select_collect_kernel(ScorePa
   if (s_n > 0u) flush();
 }
 
-template <int kThreads>
+template <int kThreads, int kParts>
 __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(ScoreParams p, const float *__restrict__ scores,
                                                               long long ld, const uint32_t *__restrict__ hist,
                                                               const uint64_t *__restrict__ cand,
-                                                              uint32_t *__restrict__ cand_cnt, int cand_cap,
-                                                              int halves_arg) {
+                                                              uint32_t *__restrict__ cand_cnt, int cand_cap) {
   constexpr int kPer = kBins / kThreads;           // bins each thread owns in a scan
   // Bins up to kWarpBin keys are sorted by one warp in registers: 128 with
   // 1024 threads per row; 256 with 512 (more rows than SMs, as in prefill,
@@ -550,14 +550,15 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
   uint64_t *buf = reinterpret_cast<uint64_t *>(smem_raw + lay.buf);
   const int cap = static_cast<int>(lay.cap);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // With two CTAs a row (halves = 2; rows without a split collection), both
-  // decide the boundary alike, then each places, orders and writes only the
-  // bins of its part of the output: the first CTA the bins whose segment
-  // starts in the first half of the buffer, the second the rest. Whatever is
-  // not decided on the first digit, and the padding, is the first CTA's.
-  // (only the 1024-thread variant, used when rows leave SMs idle, is launched so)
-  const int halves = kThreads == 1024 ? halves_arg : 1;
-  const int t = blockIdx.x / halves, h = blockIdx.x - t * halves;
+  // With several CTAs a row (parts > 1: rows that leave SMs idle), all decide
+  // the boundary alike, then CTA h places, orders and writes only the bins of
+  // part h of the output: the bins whose buffer segment starts in
+  // [h total / parts, (h + 1) total / parts). Whatever is not decided on the
+  // first digit, and the padding, is the first CTA's.
+  // (only the 1024-thread variant is launched so; one instantiation per count)
+  constexpr int parts = kParts;
+  static_assert(parts >= 1 && parts <= kMaxParts && (kThreads == 1024 || parts == 1), "parts");
+  const int t = blockIdx.x / parts, h = blockIdx.x - t * parts;
   const int k = p.top_k;
   int32_t *oi = p.topk_idx + static_cast<long long>(t) * k;
   float *os = p.topk_score + static_cast<long long>(t) * k;
@@ -625,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
     sh->b_above = 0;
     sh->b_cnt = 0;
     sh->n_buf = 0;
-    sh->split_bin = -1;
+    for (int q = 0; q < kMaxParts; ++q) sh->split_bin[q] = -1;
   }
 
   // ---- locate the boundary bin, digit by digit ----
@@ -734,15 +735,17 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
     // ---- decided on the first digit: place, rank, write ----
     // (keys below the boundary bin are dropped on their top 32 bits alone)
     const int total = min(take_all ? static_cast<int>(all_keys) : sh->b_above + sh->b_cnt, cap);
-    bool solo = halves == 1;
-    if (!solo) {   // the second CTA's part: the bins whose segment starts at total / 2 or later
+    bool solo = parts == 1;
+    if (!solo) {   // part q >= 1 starts at the highest bin whose segment starts at ceil(q total / parts) or later
       if (tid == 0) sh->n_large = 0;
       __syncthreads();
-      const uint32_t split = static_cast<uint32_t>(total + 1) / 2u;
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
         const uint32_t e = sh->table[kBins - 1 - kPer * tid - j];
-        if (e != 0u && (e & 0xFFFFu) >= split) atomicMax(&sh->split_bin, kBins - 1 - kPer * tid - j);
+        if (e != 0u)
+          for (int q = 1; q < parts; ++q)
+            if ((e & 0xFFFFu) >= static_cast<uint32_t>((q * total + parts - 1) / parts))
+              atomicMax(&sh->split_bin[q], kBins - 1 - kPer * tid - j);
         if (static_cast<int>(e >> 16) > kWarpBin) atomicAdd(&sh->n_large, 1);
       }
       __syncthreads();
@@ -750,9 +753,9 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
       solo = sh->n_large > kMaxLarge;
       if (solo && h != 0) return;
     }
-    const int split_bin = sh->split_bin;
-    // bin b is this CTA's: the first CTA takes the bins above split_bin, the second the others
-    auto mine = [&](int b) { return solo || ((b > split_bin) == (h == 0)); };
+    // bin b is this CTA's: at most split_bin[h] (part 0: any), above split_bin[h + 1] (last part: any)
+    const int hi_bin = (h > 0) ? sh->split_bin[h] : kBins, lo_bin = (h + 1 < parts) ? sh->split_bin[h + 1] : -1;
+    auto mine = [&](int b) { return solo || (b <= hi_bin && b > lo_bin); };
     auto place = [&](uint64_t key) {
       if ((key & mask) >= prefix && mine(static_cast<int>(key >> 52))) {
         const uint32_t old = atomicAdd(&sh->table[key >> 52], 1u);
@@ -905,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_stream_kernel(
     os[i] = -INFINITY;
   }
   if (tid == 0 && sh->abort_flag && p.dev_status) atomicOr(p.dev_status, IDX_STATUS_TIMEOUT);
-  if (cand_cnt != nullptr) {
+  if (cand_cnt != nullptr && parts == 1) {   // (with several CTAs a row the q preparation of the next call zeroes it)
     __syncthreads();   // every thread has read the row's count
     if (tid == 0) cand_cnt[t] = 0u;   // left zero for the next call
   }
@@ -954,15 +957,24 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
   // single sort of at most kSmallRow keys gains nothing from more warps.
   const int sms = device_sm_count();
   const bool wide = sms > 0 && p.T <= sms && static_cast<long long>(p.max_lb) * p.epb > kSmallRow;
-  void (*kern)(ScoreParams, const float *, long long, const uint32_t *, const uint64_t *, uint32_t *, int, int) =
-      wide ? topk_stream_kernel<1024> : topk_stream_kernel<512>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
   uint64_t *cand = nullptr;
   uint32_t *cand_cnt = nullptr;
   if (pl.chunks > 0 && hist != nullptr) {
     cand = reinterpret_cast<uint64_t *>(static_cast<unsigned char *>(workspace) + pl.cand_off);
     cand_cnt = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(workspace) + pl.cnt_off);
+  }
+  // Rows that leave SMs idle: several CTAs a row (the 1024-thread variant), each
+  // ordering and writing the bins of one part of the output; 2 when each streams
+  // the whole row, up to kMaxParts when they read a collected candidate list.
+  int parts = 1;
+  if (wide)
+    while (2 * parts <= (cand == nullptr ? 2 : kMaxParts) && 2 * parts * p.T <= sms) parts *= 2;
+  void (*kern)(ScoreParams, const float *, long long, const uint32_t *, const uint64_t *, uint32_t *, int) =
+      !wide ? topk_stream_kernel<512, 1>
+            : parts == 4 ? topk_stream_kernel<1024, 4> : parts == 2 ? topk_stream_kernel<1024, 2> : topk_stream_kernel<1024, 1>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (cand != nullptr) {
     cudaLaunchConfig_t ca{};
     ca.gridDim = dim3(static_cast<unsigned>(pl.chunks), static_cast<unsigned>(p.T), 1);
     ca.blockDim = dim3(kCollectThreads, 1, 1);
@@ -975,11 +987,8 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
     e = cudaLaunchKernelEx(&ca, select_collect_kernel, p, scores, ld, hist, cand, cand_cnt, pl.cand_cap);
     if (e != cudaSuccess) return e;
   }
-  // Rows that leave SMs idle (at most half as many as SMs, each streamed whole):
-  // two CTAs a row, each ordering and writing the bins of one part of the output.
-  const int halves = (wide && cand == nullptr && 2 * p.T <= sms) ? 2 : 1;   // (wide: the 1024-thread variant)
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.T * halves), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(p.T * parts), 1, 1);
   cfg.blockDim = dim3(wide ? 1024 : 512, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -989,7 +998,7 @@ cudaError_t launch_select(const ScoreParams &p, const float *scores, long long l
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, p, scores, ld, hist, static_cast<const uint64_t *>(cand),
-                            cand_cnt, pl.cand_cap, halves);
+                            cand_cnt, pl.cand_cap);
 }
 
 }  // namespace idx
