@@ -143,6 +143,50 @@ def test_split_collection_falls_back_and_takes_all():
     assert np.all(gi[1, 640:] == -1) and np.all(np.isneginf(gs[1, 640:]))
 
 
+def _scaled_copies(W, n_var, high_per_100=100):
+    """Every key of the pool a copy of one key (one global scale for all
+    blocks) whose eight E4M3 group scales are set to one code: code 0x30 + 2 v
+    (v = slot % n_var) for high_per_100 of every 100 pool slots, else 0x08.
+    Scores are then that key's score times the scale (the ReLU'd sum is
+    positively homogeneous), so each variant's keys tie exactly and variants
+    about 20 % apart fall in distinct 12-bit bins."""
+    D2 = W.keys_fp4.shape[2]
+    flat_k = W.keys_fp4.reshape(-1, D2)
+    flat_s = W.key_scale.reshape(-1, W.key_scale.shape[2])
+    g = np.arange(flat_k.shape[0])
+    flat_k[:] = flat_k[0]
+    code = np.where(g % 100 < high_per_100, 0x30 + 2 * (g % n_var), 0x08).astype(np.uint8)
+    flat_s[:] = code[:, None]
+    W.key_gscale[:] = W.key_gscale[0]
+    return W
+
+
+@pytest.mark.parametrize("n_var", [12, 28])
+def test_many_tied_keys_in_few_bins(n_var):
+    """4 rows of 6000 keys, k = 2048, 12 or 28 distinct scores: the candidates
+    fill 5 or 10 bins of 200-500 keys, ordered by the rows' two CTAs, or, past
+    eight such bins, by the first CTA alone (one sort of the buffer)."""
+    W = _scaled_copies(_small(21, T=4, lo=6000, hi=6000, k=2048, max_lb=94, P=1024), n_var)
+    gi, gs, st, _ = run_gpu(W, "tensor")
+    assert st == 0
+    rows, _ = oracle_rows(W)
+    assert len(np.unique(rows[0])) == n_var
+    check_against_oracle(W, gi, gs, rows, None, f"tied{n_var}")
+
+
+@pytest.mark.parametrize("n_var,high", [(14, 4), (28, 100)])
+def test_many_tied_keys_long_rows(n_var, high):
+    """3 rows of 70000 keys, k = 2048: 14 high scores on 4 % of the keys (about
+    ten bins of ~200 tied keys among the candidates: the collected list ordered
+    by the first of a row's four CTAs alone), or 28 scores over all keys (a
+    boundary bin past 2048 keys, refined on later digits)."""
+    W = _scaled_copies(_long_rows(22, T=3, lo=70000, hi=70000, k=2048, P=3400), n_var, high)
+    gi, gs, st, _ = run_gpu(W, "tensor")
+    assert st == 0
+    rows, _ = oracle_rows(W)
+    check_against_oracle(W, gi, gs, rows, None, f"tied-long{n_var}")
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_bad_inputs_report_status(path):
     W = _small(8, T=4, lo=2000, hi=3000, k=64, max_lb=50, P=300)
