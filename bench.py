@@ -661,7 +661,7 @@ def run_gather_split(args, rank, world):
                     "d2h_bytes_per_step": hout.numel() * 2},
             "gpu_launches": K,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": None, "kernel": "gather_split_kernel", "peak_kind": kind,
+                         "traffic": None, "kernel": "gather_split_vec_kernel", "peak_kind": kind,
                          "algorithmic_bytes_per_launch": algo},
             "cpu_baseline": cpu, "clocks": clk.summary()}), flush=True)
 
