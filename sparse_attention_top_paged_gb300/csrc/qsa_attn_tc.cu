@@ -73,7 +73,7 @@ constexpr uint32_t kOffRed = kOffP + 2 * 4096;           // [4 lane quarters][8 
 constexpr uint32_t kOffBar = kOffRed + 3 * 4 * kGroup * 4;
 // per stage: full, empty; per slot (step parity): S^T written, weights written
 constexpr int B_FULL = 0, B_EMPTY = kStages, B_S = 2 * kStages, B_P = 2 * kStages + 2, B_NEVER = 2 * kStages + 4,
-              B_COUNT = 2 * kStages + 5;
+              B_DRAIN = 2 * kStages + 5, B_COUNT = 2 * kStages + 7;   // B_DRAIN: one per MMA-issuing warp
 constexpr uint32_t kOffMisc = kOffBar + 8 * B_COUNT;     // tensor-memory address, abort flag, bad-block flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;    // + slack to align the base to 1 KB
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -405,6 +405,16 @@ __device__ __forceinline__ void issue_values(uint32_t s_base, uint32_t tmem, uin
   __syncwarp();
 }
 
+// After a wait gave up: the MMA warp's own MMAs retire before the CTA frees
+// tensor memory (a commit tracks every earlier MMA of the issuing thread; the
+// wait on it is bounded too).
+__device__ __forceinline__ void drain_mmas(uint32_t bar) {
+  if (ptx::elect_one()) ptx::mma_commit(bar);
+  __syncwarp();
+  volatile int no_abort = 0;
+  ptx::mbar_wait(bar, 0u, &no_abort, kWaitNs);
+}
+
 __device__ __forceinline__ uint32_t full_bar(uint32_t bar0, uint32_t j) {
   return bar0 + 8 * (B_FULL + static_cast<int>(j % kStages));
 }
@@ -433,6 +443,8 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, uint32_t 
     ptx::mbar_init(bar0 + 8 * B_P, 1);                     // one softmax thread, once the weights are written
     ptx::mbar_init(bar0 + 8 * (B_P + 1), 1);
     ptx::mbar_init(bar0 + 8 * B_NEVER, 1);                 // nothing arrives (failure-path test builds only)
+    ptx::mbar_init(bar0 + 8 * B_DRAIN, 1);                 // the score warp's commit when it gives up
+    ptx::mbar_init(bar0 + 8 * (B_DRAIN + 1), 1);           // the value warp's
     *abort = 0;
     *bad_flag = 0;
     ptx::fence_mbar_init();
@@ -470,6 +482,7 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, uint32_t 
       issue_scores(s_base, tmem, j);
     }
     __syncwarp();
+    if (*abort) drain_mmas(bar0 + 8 * B_DRAIN);
   } else if (warp == kMmaWarp + 1) {
     // Value MMAs: O of step j once its weights are written (a second issuing warp, so
     // a step's value MMAs need not wait behind the issue of the next step's scores).
@@ -484,6 +497,7 @@ __global__ void __maxnreg__(80) qsa_prefill_attn_tc_kernel(Problem pr, uint32_t 
       issue_values(s_base, tmem, j, sw.base == 0, 16u * sw.par);   // an item's first step restarts its O slot
     }
     __syncwarp();
+    if (*abort) drain_mmas(bar0 + 8 * (B_DRAIN + 1));
   } else {
     constexpr int HPW = (G + 1) / 2;           // head slots a warp serves (with G = 1 the upper warps' slot is unused)
     const int qd = warp & 3, hh = warp >> 2;   // lane quarter; heads HPW hh .. HPW hh + HPW - 1
