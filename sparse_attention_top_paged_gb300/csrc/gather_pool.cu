@@ -41,15 +41,29 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_kv_kernel(idx_gather
   if (src_row >= 0 && !IDX_IN_BOUNDS(src_row < static_cast<long long>(a.P) * a.block_size, a.dev_status)) src_row = -1;
   const long long nvec = a.row_bytes / 16;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  {
-    const uint4 *src = static_cast<const uint4 *>(a.k_cache) + (src_row >= 0 ? src_row : 0) * nvec;
-    uint4 *dst = static_cast<uint4 *>(a.k_out) + r * nvec;
-    for (long long c = lane_id(); c < nvec; c += 32) __stcs(dst + c, src_row >= 0 ? __ldg(src + c) : zero);
-  }
-  if (a.v_cache) {
-    const uint4 *src = static_cast<const uint4 *>(a.v_cache) + (src_row >= 0 ? src_row : 0) * nvec;
-    uint4 *dst = static_cast<uint4 *>(a.v_out) + r * nvec;
-    for (long long c = lane_id(); c < nvec; c += 32) __stcs(dst + c, src_row >= 0 ? __ldg(src + c) : zero);
+  const uint4 *ks = static_cast<const uint4 *>(a.k_cache) + (src_row >= 0 ? src_row : 0) * nvec;
+  const uint4 *vs = a.v_cache ? static_cast<const uint4 *>(a.v_cache) + (src_row >= 0 ? src_row : 0) * nvec : nullptr;
+  uint4 *kd = static_cast<uint4 *>(a.k_out) + r * nvec;
+  uint4 *vd = a.v_cache ? static_cast<uint4 *>(a.v_out) + r * nvec : nullptr;
+  // two 16-byte pieces of the K row and of the V row a lane at a time, all four
+  // loads issued before any store (a store could alias a later load, so the
+  // compiler would not move the load ahead of it)
+  for (long long c0 = lane_id(); c0 < nvec; c0 += 64) {
+    const long long c1 = c0 + 32;
+    const bool has1 = c1 < nvec;
+    const uint4 k0 = src_row >= 0 ? __ldg(ks + c0) : zero;
+    const uint4 k1 = (src_row >= 0 && has1) ? __ldg(ks + c1) : zero;
+    uint4 v0 = zero, v1 = zero;
+    if (vs != nullptr && src_row >= 0) {
+      v0 = __ldg(vs + c0);
+      if (has1) v1 = __ldg(vs + c1);
+    }
+    __stcs(kd + c0, k0);
+    if (has1) __stcs(kd + c1, k1);
+    if (vd != nullptr) {
+      __stcs(vd + c0, v0);
+      if (has1) __stcs(vd + c1, v1);
+    }
   }
 }
 
