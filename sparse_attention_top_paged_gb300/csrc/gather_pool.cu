@@ -159,31 +159,54 @@ constexpr int kExpandThreads = 256;
 
 __global__ void __launch_bounds__(kExpandThreads) expand_blocks_kernel(const int32_t *blocks, int n_blocks,
                                                                        int ratio, int32_t *positions) {
-  extern __shared__ int32_t ids[];
+  extern __shared__ int32_t ids[];   // m sorted ids, then (rank path) the n_blocks ids as read
   const int t = blockIdx.x;
   int m = 1;
   while (m < n_blocks) m <<= 1;
-  for (int i = threadIdx.x; i < m; i += kExpandThreads) {
-    int32_t v = INT_MAX;
+  if (n_blocks <= kExpandThreads) {
+    // one thread per id: its place in ascending order is the number of smaller
+    // ids, plus the equal ones read before it (two barriers instead of a network)
+    int32_t *in = ids + m;
+    const int i = threadIdx.x;
+    int32_t v = INT_MAX;   // (invalid ids sort last)
     if (i < n_blocks) {
       const int32_t b = blocks[static_cast<long long>(t) * n_blocks + i];
       if (b >= 0) v = b;
+      in[i] = v;
     }
-    ids[i] = v;
-  }
-  __syncthreads();
-  for (int size = 2; size <= m; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < (m >> 1); i += kExpandThreads) {
-        const int lo = ((i & ~(stride - 1)) << 1) | (i & (stride - 1)), hi = lo + stride;
-        const bool asc = (lo & size) == 0;
-        const int32_t a = ids[lo], c = ids[hi];
-        if ((a > c) == asc) {
-          ids[lo] = c;
-          ids[hi] = a;
-        }
+    __syncthreads();
+    if (i < n_blocks) {
+      int rank = 0;
+      for (int j = 0; j < n_blocks; ++j) {
+        const int32_t u = in[j];
+        rank += (u < v || (u == v && j < i)) ? 1 : 0;
       }
-      __syncthreads();
+      ids[rank] = v;
+    }
+    __syncthreads();
+  } else {
+    for (int i = threadIdx.x; i < m; i += kExpandThreads) {
+      int32_t v = INT_MAX;
+      if (i < n_blocks) {
+        const int32_t b = blocks[static_cast<long long>(t) * n_blocks + i];
+        if (b >= 0) v = b;
+      }
+      ids[i] = v;
+    }
+    __syncthreads();
+    for (int size = 2; size <= m; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = threadIdx.x; i < (m >> 1); i += kExpandThreads) {
+          const int lo = ((i & ~(stride - 1)) << 1) | (i & (stride - 1)), hi = lo + stride;
+          const bool asc = (lo & size) == 0;
+          const int32_t a = ids[lo], c = ids[hi];
+          if ((a > c) == asc) {
+            ids[lo] = c;
+            ids[hi] = a;
+          }
+        }
+        __syncthreads();
+      }
     }
   }
   const long long n_out = static_cast<long long>(n_blocks) * ratio;
@@ -239,8 +262,8 @@ cudaError_t launch_expand_blocks(const int32_t *blocks, int T, int n_blocks, int
   if (T == 0 || n_blocks == 0) return cudaSuccess;
   int m = 1;
   while (m < n_blocks) m <<= 1;
-  expand_blocks_kernel<<<T, kExpandThreads, static_cast<size_t>(m) * 4, stream>>>(blocks, n_blocks, ratio,
-                                                                                  positions);
+  const size_t smem = static_cast<size_t>(n_blocks <= kExpandThreads ? 2 * m : m) * 4;   // (the rank path reads a copy)
+  expand_blocks_kernel<<<T, kExpandThreads, smem, stream>>>(blocks, n_blocks, ratio, positions);
   return cudaGetLastError();
 }
 

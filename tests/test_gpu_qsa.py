@@ -121,10 +121,14 @@ def test_gather_bad_rows_and_k_only():
     assert v2 is None and np.array_equal(k2, rk)
 
 
-def test_expand_blocks_exact():
-    rng = np.random.default_rng(5)
-    blocks = np.stack([rng.permutation(512)[:64] for _ in range(3)]).astype(np.int32)
-    blocks[1, 10:] = -1
+@pytest.mark.parametrize("nb", [1, 64, 256, 257, 1000])
+def test_expand_blocks_exact(nb):
+    """Up to 256 selected blocks (one thread ranks each id) and more (a sorting
+    network), with unselected (-1) entries and repeated ids."""
+    rng = np.random.default_rng(5 + nb)
+    blocks = np.stack([rng.permutation(4 * nb)[:nb] for _ in range(3)]).astype(np.int32)
+    blocks[1, nb // 6:] = -1
+    blocks[2, : nb // 2] = blocks[2, nb // 2: 2 * (nb // 2)]   # each id of the second half twice
     got = _idx().expand_blocks(torch.from_numpy(blocks).cuda(), 16).cpu().numpy()
     assert np.array_equal(got, oracle.expand_blocks(blocks, 16))
 
