@@ -293,7 +293,8 @@ __device__ void producer(const Problem &pr, uint32_t items, unsigned char *sm, u
   for (uint32_t j = g; sw.valid; j += kProdGroups) {
     const int s = static_cast<int>(j % kStages);
     const uint32_t par = static_cast<uint32_t>((j / kStages) & 1);
-    if (sw.w != q_item) {   // the group's first step of an item: its q rows, scaled and split once
+    const bool q_new = sw.w != q_item;
+    if (q_new) {   // the group's first step of an item: its q rows, scaled and split once
       q_item = sw.w;
       float2 v[4];
 #pragma unroll
@@ -357,11 +358,16 @@ __device__ void producer(const Problem &pr, uint32_t items, unsigned char *sm, u
         *reinterpret_cast<uint4 *>(st + kOffV + o) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
+    // (group g fills stage g only: the stage still holds this item's Qs from the
+    // group's previous step unless the item changed)
+    static_assert(kProdGroups == kStages, "a group owns its stage");
+    if (q_new) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int x = ptid + 128 * i, h = x >> 6, d = 2 * (x & 63);
-      *reinterpret_cast<uint32_t *>(st + kOffQ + sw128(h, d, 2048)) = qhi[i];
-      *reinterpret_cast<uint32_t *>(st + kOffQ + sw128(8 + h, d, 2048)) = qlo[i];
+      for (int i = 0; i < 4; ++i) {
+        const int x = ptid + 128 * i, h = x >> 6, d = 2 * (x & 63);
+        *reinterpret_cast<uint32_t *>(st + kOffQ + sw128(h, d, 2048)) = qhi[i];
+        *reinterpret_cast<uint32_t *>(st + kOffQ + sw128(8 + h, d, 2048)) = qlo[i];
+      }
     }
     cp_async_arrive(bar0 + 8 * (B_FULL + s));   // when this thread's copies have landed
     ptx::mbar_arrive(bar0 + 8 * (B_FULL + s));  // its plain stores (release)
